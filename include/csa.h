@@ -1,0 +1,260 @@
+/*
+ * libcsa — the hot path of one Compressed Sparse Attention (CSA) layer on
+ * NVIDIA GB300 (sm_103a): compressor, lightning indexer + top-k, and the
+ * shared-KV sparse MQA with an attention sink, for decode and chunked prefill.
+ *
+ * Page titles used in the citations below:
+ *   [hca_csa]   "CSA / HCA" (zdszero.github.io, hca_csa)
+ *   [KV 压缩]   "DeepSeek-V4 的 KV 压缩：从删 token 误解到预算检索"
+ *   [CSA2 详解] "DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2：从模型原理到推理基础设施"
+ *   [结构对比]  "DeepSeek 注意力结构对比：MHA、GQA、MLA、DSA、CSA、HCA、CSA2"
+ *   [CED]       "从 GPT 到 CED：DeepSeek-V4.1-Flash 如何改变上下文的计算方式"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Plain C ABI.  bf16 tensors are passed as `uint16_t*` (raw bfloat16 bits),
+ *   FP8 E4M3 (finite-only "fn" variant, no scale) as `uint8_t*`.
+ * - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *   never allocates device memory.  Scratch memory ("workspace") is passed by
+ *   the caller and must be at least csa_workspace_size() bytes.
+ * - `stream` is a cudaStream_t passed as `void*` (NULL = legacy default stream).
+ *   Every call is asynchronous on that stream.
+ * - Layouts are dense row-major unless a stride argument says otherwise.  All
+ *   base pointers must be 16-byte aligned.
+ * - Argument errors are detected on the host before any launch and returned
+ *   (CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED / CSA_ERR_WORKSPACE); outputs
+ *   are then left untouched.  A failed launch returns CSA_ERR_CUDA.
+ * - Data-dependent errors (a position or index outside the caches, a bounded
+ *   device-side wait that gave up) cannot be seen by the host at call time.
+ *   The kernels clamp the offending access, keep running, and record the
+ *   error in a device status word; csa_check_status() reports and clears it.
+ *   No kernel traps.
+ * - The model dimensions are fixed by the pages for V4-Flash/Pro CSA layers
+ *   ([CSA2 详解] §3.1; [hca_csa] "CSA：轻压缩 + 稀疏选择"): 64 query heads of
+ *   width 512 sharing one 512-wide K=V latent, partial RoPE on its last 64
+ *   channels, 64 indexer heads of width 128.  Calls with other values return
+ *   CSA_ERR_UNSUPPORTED.
+ */
+#ifndef LIBCSA_CSA_H
+#define LIBCSA_CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer     */
+  CSA_ERR_UNSUPPORTED = 2,  /* a dimension other than the ones listed above   */
+  CSA_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed         */
+  CSA_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up             */
+  CSA_ERR_INDEX_RANGE = 5,  /* a position / index pointed outside a cache     */
+  CSA_ERR_WORKSPACE = 6     /* workspace missing or smaller than required     */
+} csa_status;
+
+/* Hyper-parameters of one CSA layer. */
+typedef struct {
+  int32_t m;          /* compression ratio: one entry per m tokens (4)        */
+  int32_t n_heads;    /* query heads (64)                                    */
+  int32_t head_dim;   /* shared K=V latent width (512)                        */
+  int32_t rope_dim;   /* trailing channels that carry RoPE (64)               */
+  int32_t idx_heads;  /* lightning-indexer heads n_h^I (64)                   */
+  int32_t idx_dim;    /* lightning-indexer width c^I (128)                    */
+  int32_t topk;       /* entries selected per query, 1..2048 (512 or 1024)    */
+  int32_t swa_window; /* raw sliding-window rows per query, 1..1024 (128)     */
+  float rope_theta;   /* RoPE base (1e4)                                      */
+  float rms_eps;      /* RMSNorm epsilon (1e-6)                               */
+  float sm_scale;     /* logit scale applied to q·kv (1/sqrt(512))            */
+} csa_params;
+
+/* Fills *p with the V4-Flash CSA values listed above (topk = 512). */
+void csa_default_params(csa_params *p);
+
+/* Operation codes for csa_workspace_size(). */
+enum {
+  CSA_OP_COMPRESS = 0,
+  CSA_OP_INDEX_TOPK = 1,
+  CSA_OP_SPARSE_ATTN = 2,
+  CSA_OP_LAYER_DECODE = 3,
+  CSA_OP_LAYER_PREFILL = 4
+};
+
+/* Bytes of workspace the call `op` needs for B sequences of Q queries over a
+ * cache of n_cap entries.  Returns 0 for an invalid combination. */
+size_t csa_workspace_size(int32_t op, const csa_params *p, int32_t B, int32_t Q,
+                          int64_t n_cap);
+
+/*
+ * csa_compress — overlapped compressor, bulk form.
+ * [hca_csa] "CSA 的重叠窗口", the Softmax_row and C_i^Comp equations, and
+ * "压缩算子：逐通道 softmax 的软池化"; i = 0 boundary in the same section;
+ * RoPE position = first token of the entry's own block ([CSA2 详解] §7.4).
+ *
+ * For every sequence b and every entry i in [entry0, entry0 + n_new):
+ *   per channel d, softmax over the 2m logits
+ *     Za[b, m*i + r, d] + Ba[r, d]            (block i, slots r = 0..m-1)
+ *     Zb[b, m*(i-1) + r, d] + Bb[r, d]        (block i-1)
+ *   weights the matching rows of Ca / Cb and sums them; the 512-vector is then
+ *   RMS-normalised (eps = p->rms_eps) and scaled by rms_w, and the last
+ *   rope_dim channels are rotated in interleaved pairs (D-R+2j, D-R+2j+1) by
+ *   angle (m*i) * rope_theta^(-2j/R).  For i = 0 the block-(i-1) slots are
+ *   absent (logit -inf, value 0).
+ *
+ * Ca, Za, Cb, Zb : [B][m*n_new][D] bf16 — rows of the chunk's tokens; row j of
+ *                  sequence b is token m*entry0 + j.
+ * Cb_prev, Zb_prev: [B][m][D] bf16 — Cb/Zb rows of the m tokens before the
+ *                  chunk (block entry0-1).  Must be NULL iff entry0 == 0.
+ * Ba, Bb         : [m][D] bf16 block-slot biases ("ape").
+ * rms_w          : [D] bf16 RMSNorm weight.
+ * kv_out         : entry e of sequence b is written at
+ *                  kv_out + b*kv_stride_b + e*D (bf16); rows entry0.. only.
+ */
+csa_status csa_compress(const csa_params *p, int32_t B, int32_t n_new,
+                        int64_t entry0, const uint16_t *Ca, const uint16_t *Za,
+                        const uint16_t *Cb, const uint16_t *Zb,
+                        const uint16_t *Cb_prev, const uint16_t *Zb_prev,
+                        const uint16_t *Ba, const uint16_t *Bb,
+                        const uint16_t *rms_w, uint16_t *kv_out,
+                        int64_t kv_stride_b, void *stream);
+
+/*
+ * csa_index_topk — lightning indexer + top-k over the causally visible entries.
+ * Score: [hca_csa] "CSA：轻压缩 + 稀疏选择", equation I_{t,s}; also
+ * [结构对比] DSA section.  Visibility: [KV 压缩] §9.8 (entry s is visible to
+ * the query at position t iff (s+1)*m <= t+1, i.e. s < V(t) = floor((t+1)/m)).
+ * Selection over all visible entries, window included ([hca_csa] "top-k 的选择
+ * 范围不排除 SWA 窗口").
+ *
+ *   I[b,q,s] = sum_h wI[b,q,h] * max(0, sum_c qI[b,q,h,c] * kI[b,s,c])
+ *
+ * for s < V(q_pos[b,q]); the min(topk, V) entries with the largest I are
+ * returned in idx_out[b,q,:] in ascending entry order, followed by -1 for the
+ * remaining slots.  Equal scores are broken toward the smaller entry index.
+ * score_out (optional) receives the fp32 score of each returned entry (and
+ * -inf in the -1 slots).
+ *
+ * q_pos : [B][Q] int32, absolute token position of each query.  V(t) must not
+ *         exceed n_cap (else CSA_ERR_INDEX_RANGE is recorded and V is clamped).
+ * qI    : [B][Q][64][128] e4m3.      wI : [B][Q][64] bf16 (scale included).
+ * kI    : [B][n_cap][128] e4m3 indexer keys, entry numbering shared with the
+ *         main compressed KV ([hca_csa] "K^IComp 与主压缩 KV 一一对应").
+ * idx_out: [B][Q][topk] int32.  score_out: [B][Q][topk] fp32 or NULL.
+ * Accuracy: FP8 products are exact; they are accumulated in fp32 by the tensor
+ * cores and the head sum is fp32.
+ */
+csa_status csa_index_topk(const csa_params *p, int32_t B, int32_t Q,
+                          const int32_t *q_pos, const uint8_t *qI,
+                          const uint16_t *wI, const uint8_t *kI, int64_t n_cap,
+                          int32_t *idx_out, float *score_out, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
+ * csa_sparse_attn — shared-KV MQA over [SWA rows || selected entries || sink].
+ * [hca_csa] "设计：近处看原文，远处看摘要", the o_{t,i} equation and the bullet
+ * on attn_sink; gather semantics [KV 压缩] §9.6; window [KV 压缩] §9.5.
+ *
+ * For the query at position t (= q_pos[b,q]) and head h, the row set is
+ *   the raw window rows of positions max(0, t-W+1) .. t   (W = swa_window)
+ *   the compressed rows kv_comp[b, idx[b,q,j]] for every idx != -1,
+ * l_{h,j} = sm_scale * q[b,q,h,:] . row_j, and
+ *   out[b,q,h,:] = sum_j e^{l_hj} row_j / (sum_j e^{l_hj} + e^{sink[h]}).
+ * The sink enters the denominator only and is not scaled by sm_scale.
+ * lse[b,q,h] (optional) = log(sum_j e^{l_hj} + e^{sink[h]}).
+ *
+ * q      : [B][Q][64][512] bf16.        kv_comp : [B][n_cap][512] bf16.
+ * idx    : [B][Q][topk] int32, -1 marks an empty slot; any other value outside
+ *          [0, n_cap) records CSA_ERR_INDEX_RANGE and the slot is skipped.
+ * swa    : swa_mode 0 (decode ring): [B][W][512], position u in slot u mod W.
+ *          swa_mode 1 (linear):      [B][swa_len][512], row j holds position
+ *          swa_pos0[b] + j (swa_pos0 is a [B] int32 device array); a needed
+ *          position outside the buffer records CSA_ERR_INDEX_RANGE and is
+ *          skipped.
+ * sink   : [64] fp32.   out : [B][Q][64][512] bf16.   lse : [B][Q][64] or NULL.
+ */
+csa_status csa_sparse_attn(const csa_params *p, int32_t B, int32_t Q,
+                           const int32_t *q_pos, const uint16_t *q,
+                           const uint16_t *kv_comp, int64_t n_cap,
+                           const int32_t *idx, const uint16_t *swa,
+                           int32_t swa_mode, int64_t swa_len,
+                           const int32_t *swa_pos0, const float *sink,
+                           uint16_t *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * csa_layer_decode — one decode step of a CSA layer for B sequences (Q = 1).
+ * Order of the path: [KV 压缩] §9.9; emission at block boundaries [KV 压缩]
+ * §9.3 and [hca_csa] "KV cache：成品与原料" (an entry is produced only when
+ * (t+1) mod m == 0, reading the 2m staged rows).
+ *
+ *   1. if (q_pos[b]+1) % m == 0: entry i = (q_pos[b]+1)/m - 1 is compressed
+ *      from the staged rows (block i from ring_Ca/Za, block i-1 from
+ *      ring_Cb/Zb) and written to kv_comp[b, i];
+ *   2. csa_index_topk over the V(t) visible entries;
+ *   3. csa_sparse_attn with the ring window (swa_mode 0).
+ *
+ * ring_Ca/Za/Cb/Zb: [B][2m][512] bf16 compressor staging rows; the row of
+ *         token u sits in slot u mod 2m and the slots hold tokens t-2m+1..t.
+ * kI    : [B][n_cap][128] e4m3 — must already hold entries 0..V(t)-1 (the
+ *         indexer keys come from a separate compressor that is not part of
+ *         this call).
+ * swa_ring: [B][W][512] bf16 holding positions t-W+1..t (slot u mod W).
+ * idx_out: [B][topk] int32 (the selection), out [B][64][512], lse [B][64] or NULL.
+ */
+csa_status csa_layer_decode(
+    const csa_params *p, int32_t B, const int32_t *q_pos,
+    const uint16_t *ring_Ca, const uint16_t *ring_Za, const uint16_t *ring_Cb,
+    const uint16_t *ring_Zb, const uint16_t *Ba, const uint16_t *Bb,
+    const uint16_t *rms_w, uint16_t *kv_comp, int64_t n_cap,
+    const uint8_t *kI, const uint8_t *qI, const uint16_t *wI,
+    const uint16_t *q, const uint16_t *swa_ring, const float *sink,
+    int32_t *idx_out, uint16_t *out, float *lse, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
+ * csa_layer_prefill — one chunk of Q query tokens at positions pos0..pos0+Q-1
+ * (pos0 a multiple of m, given on the host), causal per query.
+ * [hca_csa] "在 SGLang 里的落点" (large-batch prefill has the decode
+ * semantics); future entries masked before top-k [KV 压缩] §9.8.
+ *
+ *   1. compress the chunk: entries pos0/m .. (pos0+Q)/m - 1 (a trailing
+ *      incomplete block produces no entry) → kv_comp, as csa_compress;
+ *   2. index + top-k for each query t over its own V(t);
+ *   3. sparse attention with the linear window.
+ *
+ * Ca/Za/Cb/Zb : [B][Q][512] bf16 rows of the chunk's tokens.
+ * Cb_prev/Zb_prev: [B][m][512] rows of the block before the chunk, NULL iff
+ *         pos0 == 0.
+ * kI    : must already hold entries 0..(pos0+Q)/m - 1.
+ * qI [B][Q][64][128], wI [B][Q][64], q [B][Q][64][512].
+ * swa   : [B][W-1+Q][512] bf16, row j = position pos0-(W-1)+j (rows before
+ *         position 0 are never read).
+ * idx_out [B][Q][topk], out [B][Q][64][512], lse [B][Q][64] or NULL.
+ */
+csa_status csa_layer_prefill(
+    const csa_params *p, int32_t B, int32_t Q, int64_t pos0,
+    const uint16_t *Ca, const uint16_t *Za, const uint16_t *Cb,
+    const uint16_t *Zb, const uint16_t *Cb_prev, const uint16_t *Zb_prev,
+    const uint16_t *Ba, const uint16_t *Bb, const uint16_t *rms_w,
+    uint16_t *kv_comp, int64_t n_cap, const uint8_t *kI, const uint8_t *qI,
+    const uint16_t *wI, const uint16_t *q, const uint16_t *swa,
+    const float *sink, int32_t *idx_out, uint16_t *out, float *lse,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device (CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_INDEX_RANGE), or
+ * CSA_ERR_CUDA if the stream reported an error.
+ */
+csa_status csa_check_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *csa_status_string(csa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBCSA_CSA_H */

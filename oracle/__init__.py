@@ -1,0 +1,266 @@
+"""CSA oracle — TEST INFRASTRUCTURE ONLY.
+
+Plain fp64 CPU statement of one CSA layer's hot path (compressor, visibility,
+lightning indexer, top-k, joint softmax with sink), used to check the CUDA
+library.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm may import this package.  It shares no code with the
+CUDA path: the arithmetic lives in ``csa_oracle.c`` (double precision,
+single-threaded); this module only marshals numpy arrays and composes the
+per-query steps in the order the pages give them ("DeepSeek-V4 的 KV 压缩：
+从删 token 误解到预算检索" §9.9: window indices, indexer top-k, compressed
+cache write at block boundaries, gather + attention).
+
+Every array argument holds raw storage bits: bf16 as ``np.uint16``, FP8 E4M3
+as ``np.uint8``; the attention sink is ``np.float32``.
+
+Parity pins for every function live in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_csa.so")
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile csa_oracle.c into liboracle_csa.so next to it (gcc, no FMA
+    contraction so that the rounding order is the one written)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(
+            ["gcc", "-O2", "-ffp-contract=off", "-std=c11", "-fPIC", "-shared",
+             _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.orc_bf16.restype = ctypes.c_double
+        lib.orc_bf16.argtypes = [ctypes.c_uint16]
+        lib.orc_e4m3.restype = ctypes.c_double
+        lib.orc_e4m3.argtypes = [ctypes.c_uint8]
+        lib.orc_compress_pool.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int] + [_u16p] * 6 + [_f64p]
+        lib.orc_rmsnorm.argtypes = [ctypes.c_int, _f64p, _u16p, ctypes.c_double, _f64p]
+        lib.orc_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p]
+        lib.orc_compress_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
+                                           + [_u16p] * 7 + [_f64p])
+        lib.orc_visible.restype = ctypes.c_int64
+        lib.orc_visible.argtypes = [ctypes.c_int64, ctypes.c_int]
+        lib.orc_index_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _f64p]
+        lib.orc_topk.restype = ctypes.c_int
+        lib.orc_topk.argtypes = [ctypes.c_int64, ctypes.c_int, _f64p, _i32p]
+        lib.orc_attend.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p, _u16p, _f32p,
+                                   ctypes.c_double, _f64p, _f64p]
+        lib.orc_decode_bf16.argtypes = [ctypes.c_int64, _u16p, _f64p]
+        lib.orc_decode_e4m3.argtypes = [ctypes.c_int64, _u8p, _f64p]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctype)
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctype)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- storage formats ------------------------------------------------------
+
+def bf16_to_f64(bits) -> np.ndarray:
+    bits = _c(bits, np.uint16)
+    out = np.empty(bits.shape, np.float64)
+    _load().orc_decode_bf16(bits.size, _ptr(bits, _u16p), _ptr(out, _f64p))
+    return out
+
+
+def e4m3_to_f64(bits) -> np.ndarray:
+    bits = _c(bits, np.uint8)
+    out = np.empty(bits.shape, np.float64)
+    _load().orc_decode_e4m3(bits.size, _ptr(bits, _u8p), _ptr(out, _f64p))
+    return out
+
+
+# ---- compressor -----------------------------------------------------------
+
+def compress_pool(Ca, Za, Cb, Zb, Ba, Bb) -> np.ndarray:
+    """Per-channel softmax pooling of one entry before Norm/RoPE.  Ca/Za are
+    the m rows of block i; Cb/Zb the m rows of block i-1 or None for i = 0."""
+    Ca, Za, Ba, Bb = (_c(a, np.uint16) for a in (Ca, Za, Ba, Bb))
+    m, D = Ca.shape
+    has_prev = Cb is not None
+    Cb = _c(Cb, np.uint16) if has_prev else None
+    Zb = _c(Zb, np.uint16) if has_prev else None
+    x = np.empty(D, np.float64)
+    _load().orc_compress_pool(m, D, int(has_prev), _ptr(Ca, _u16p), _ptr(Za, _u16p), _ptr(Cb, _u16p),
+                              _ptr(Zb, _u16p), _ptr(Ba, _u16p), _ptr(Bb, _u16p), _ptr(x, _f64p))
+    return x
+
+
+def rmsnorm(x, w, eps) -> np.ndarray:
+    x = _c(x, np.float64)
+    w = _c(w, np.uint16)
+    y = np.empty_like(x)
+    _load().orc_rmsnorm(x.size, _ptr(x, _f64p), _ptr(w, _u16p), eps, _ptr(y, _f64p))
+    return y
+
+
+def rope(y, rope_dim, theta, pos) -> np.ndarray:
+    y = np.array(y, dtype=np.float64, copy=True)
+    _load().orc_rope(y.size, rope_dim, theta, float(pos), _ptr(y, _f64p))
+    return y
+
+
+def compress_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, *, rope_dim=64, theta=1e4, eps=1e-6) -> np.ndarray:
+    """Entry i = RoPE(Norm(pool)); Cb/Zb are block i-1's rows (ignored for i = 0)."""
+    Ca, Za, Ba, Bb, w = (_c(a, np.uint16) for a in (Ca, Za, Ba, Bb, w))
+    m, D = Ca.shape
+    if i > 0:
+        Cb, Zb = _c(Cb, np.uint16), _c(Zb, np.uint16)
+    else:
+        Cb = Zb = None
+    out = np.empty(D, np.float64)
+    _load().orc_compress_entry(m, D, rope_dim, theta, eps, int(i), _ptr(Ca, _u16p), _ptr(Za, _u16p),
+                               _ptr(Cb, _u16p), _ptr(Zb, _u16p), _ptr(Ba, _u16p), _ptr(Bb, _u16p),
+                               _ptr(w, _u16p), _ptr(out, _f64p))
+    return out
+
+
+def compress(entry0, n_new, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, w, *, m=4, rope_dim=64,
+             theta=1e4, eps=1e-6) -> np.ndarray:
+    """Bulk form for one sequence: Ca/Za/Cb/Zb hold the chunk's m*n_new token
+    rows (row j = token m*entry0 + j); Cb_prev/Zb_prev the m rows before the
+    chunk (None iff entry0 == 0).  Returns [n_new, D]."""
+    D = Ca.shape[-1]
+    out = np.empty((n_new, D), np.float64)
+    for e in range(n_new):
+        i = entry0 + e
+        blk = slice(m * e, m * e + m)
+        if i == 0:
+            cb = zb = None
+        elif e == 0:
+            cb, zb = Cb_prev, Zb_prev
+        else:
+            prev = slice(m * (e - 1), m * e)
+            cb, zb = Cb[prev], Zb[prev]
+        out[e] = compress_entry(i, Ca[blk], Za[blk], cb, zb, Ba, Bb, w, rope_dim=rope_dim, theta=theta,
+                                eps=eps)
+    return out
+
+
+# ---- visibility, indexer, top-k -------------------------------------------
+
+def visible(t: int, m: int = 4) -> int:
+    return int(_load().orc_visible(int(t), int(m)))
+
+
+def index_scores(qI, wI, kI) -> np.ndarray:
+    """qI [H, Dk] e4m3, wI [H] bf16, kI [V, Dk] e4m3 -> scores [V] (fp64)."""
+    qI, kI = _c(qI, np.uint8), _c(kI, np.uint8)
+    wI = _c(wI, np.uint16)
+    H, Dk = qI.shape
+    V = kI.shape[0]
+    out = np.empty(V, np.float64)
+    _load().orc_index_scores(H, Dk, V, _ptr(qI, _u8p), _ptr(wI, _u16p), _ptr(kI, _u8p), _ptr(out, _f64p))
+    return out
+
+
+def topk(scores, k: int) -> np.ndarray:
+    scores = _c(scores, np.float64)
+    idx = np.empty(k, np.int32)
+    _load().orc_topk(scores.size, k, _ptr(scores, _f64p), _ptr(idx, _i32p))
+    return idx
+
+
+# ---- attention ------------------------------------------------------------
+
+def attend(q, rows, sink, sm_scale):
+    """q [H, D] bf16, rows [n, D] bf16, sink [H] fp32 -> (out [H, D], lse [H])."""
+    q, rows = _c(q, np.uint16), _c(rows, np.uint16)
+    sink = _c(sink, np.float32)
+    H, D = q.shape
+    out = np.empty((H, D), np.float64)
+    lse = np.empty(H, np.float64)
+    _load().orc_attend(H, D, rows.shape[0], _ptr(q, _u16p), _ptr(rows, _u16p), _ptr(sink, _f32p),
+                       float(sm_scale), _ptr(out, _f64p), _ptr(lse, _f64p))
+    return out, lse
+
+
+def window_positions(t: int, W: int) -> np.ndarray:
+    """Raw window of the query at t: positions max(0, t-W+1) .. t, the current
+    token included (reading recorded in the design doc)."""
+    return np.arange(max(0, t - W + 1), t + 1, dtype=np.int64)
+
+
+def gather_rows(t, idx, kv_comp, swa_row_of, W):
+    """Row set of the query at t: its window rows, then kv_comp[idx] for idx != -1."""
+    pos = window_positions(t, W)
+    swa_rows = np.stack([swa_row_of(int(u)) for u in pos]) if len(pos) else np.zeros((0, kv_comp.shape[1]), np.uint16)
+    sel = idx[idx >= 0]
+    return np.concatenate([swa_rows, kv_comp[sel]], axis=0)
+
+
+def attend_query(t, q, idx, kv_comp, swa_row_of, sink, *, W=128, sm_scale=1.0 / np.sqrt(512.0)):
+    rows = gather_rows(t, np.asarray(idx), kv_comp, swa_row_of, W)
+    return attend(q, rows, sink, sm_scale)
+
+
+# ---- layer compositions -----------------------------------------------------
+
+def layer_decode_one(t, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w, kv_comp, kI, qI, wI, q, swa_ring,
+                     sink, *, m=4, topk_k=512, W=128, rope_dim=64, theta=1e4, eps=1e-6,
+                     sm_scale=1.0 / np.sqrt(512.0)):
+    """One decode step of one sequence (the query at position t).
+
+    kv_comp [n_cap, D] is copied; if (t+1) % m == 0 entry (t+1)/m - 1 is
+    compressed from the staged ring rows (slot u mod 2m holds token u) and
+    stored in the copy.  Returns (kv_comp_after, idx [topk], out [H, D], lse [H]).
+    """
+    kv = np.array(kv_comp, copy=True)
+    if (t + 1) % m == 0:
+        i = (t + 1) // m - 1
+        slots_a = [(m * i + r) % (2 * m) for r in range(m)]
+        slots_b = [(m * (i - 1) + r) % (2 * m) for r in range(m)]
+        entry = compress_entry(i, ring_Ca[slots_a], ring_Za[slots_a], ring_Cb[slots_b], ring_Zb[slots_b],
+                               Ba, Bb, rms_w, rope_dim=rope_dim, theta=theta, eps=eps)
+        kv[i] = f64_to_bf16_bits(entry)
+    V = visible(t, m)
+    scores = index_scores(qI, wI, kI[:V])
+    idx = topk(scores, topk_k)
+    out, lse = attend_query(t, q, idx, kv, lambda u: swa_ring[u % W], sink, W=W, sm_scale=sm_scale)
+    return kv, idx, out, lse
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round-to-nearest-even of doubles to bf16 bits, used where the path
+    stores a bf16 result that a later step reads (the compressed cache).
+    Rounds to binary32 with round-to-odd first, which makes the second
+    rounding (binary32 -> bf16, nearest-even) the correctly rounded result."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)
+    u = f.view(np.uint32).astype(np.int64)
+    inexact = f.astype(np.float64) != x
+    overshoot = np.abs(f.astype(np.float64)) > np.abs(x)
+    u = np.where(inexact & overshoot, u - 1, u)      # truncate toward zero
+    u = np.where(inexact, u | 1, u)                  # sticky bit: round to odd
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)

@@ -1,0 +1,246 @@
+/*
+ * CSA oracle — TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded fp64 CPU statement of what one CSA layer's
+ * hot path computes.  It exists to check the CUDA library against; only the
+ * tests, the package's smoke check and the benchmark's CPU-baseline leg may
+ * load it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * Inputs are taken as their raw storage bits (bf16 as uint16, FP8 E4M3 as
+ * uint8, sink as fp32) and decoded here from the format definitions; all
+ * arithmetic is then in double, in the order the pages state it.
+ *
+ * Pages cited (by title):
+ *   [hca_csa]   "CSA / HCA" (zdszero.github.io, hca_csa)
+ *   [KV 压缩]   "DeepSeek-V4 的 KV 压缩：从删 token 误解到预算检索"
+ *   [CSA2 详解] "DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2：从模型原理到推理基础设施"
+ *   [结构对比]  "DeepSeek 注意力结构对比：MHA、GQA、MLA、DSA、CSA、HCA、CSA2"
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- storage formats ---------------------------------------------------- */
+
+/* bfloat16: the upper 16 bits of an IEEE-754 binary32. */
+double orc_bf16(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* FP8 E4M3 ("fn": no infinities, S.1111.111 is NaN): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 is subnormal. */
+double orc_e4m3(uint8_t bits) {
+  int sign = bits >> 7;
+  int e = (bits >> 3) & 0xF;
+  int f = bits & 0x7;
+  double mag;
+  if (e == 0xF && f == 0x7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)f / 8.0, 1 - 7);
+  else
+    mag = ldexp(1.0 + (double)f / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+/* ---- compressor ([hca_csa] "CSA 的重叠窗口") ------------------------------ */
+
+/*
+ * Soft pooling of entry i, before Norm and RoPE.  For each channel d the 2m
+ * logits are Za[r][d] + Ba[r][d] (block i) and Zb[r][d] + Bb[r][d] (block
+ * i-1); Softmax_row normalises over all 2m of them, and the weighted C rows
+ * are summed.  With has_prev == 0 (entry 0) the block-(i-1) logits are -inf
+ * and their C rows are 0, as the page states for i = 0.
+ *   Ca, Za : [m][D] rows of block i;  Cb, Zb : [m][D] rows of block i-1.
+ *   Ba, Bb : [m][D].                  x     : [D] output.
+ */
+void orc_compress_pool(int m, int D, int has_prev, const uint16_t *Ca,
+                       const uint16_t *Za, const uint16_t *Cb,
+                       const uint16_t *Zb, const uint16_t *Ba,
+                       const uint16_t *Bb, double *x) {
+  double logit[64], value[64];
+  for (int d = 0; d < D; ++d) {
+    int n = 0;
+    for (int r = 0; r < m; ++r) {
+      logit[n] = orc_bf16(Za[r * D + d]) + orc_bf16(Ba[r * D + d]);
+      value[n] = orc_bf16(Ca[r * D + d]);
+      ++n;
+    }
+    for (int r = 0; r < m; ++r) {
+      if (has_prev) {
+        logit[n] = orc_bf16(Zb[r * D + d]) + orc_bf16(Bb[r * D + d]);
+        value[n] = orc_bf16(Cb[r * D + d]);
+      } else {
+        logit[n] = -INFINITY;
+        value[n] = 0.0;
+      }
+      ++n;
+    }
+    double mx = -INFINITY;
+    for (int j = 0; j < n; ++j)
+      if (logit[j] > mx) mx = logit[j];
+    double num = 0.0, den = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double e = exp(logit[j] - mx);
+      num += e * value[j];
+      den += e;
+    }
+    x[d] = num / den;
+  }
+}
+
+/* RMSNorm ("Norm" in the C_i^Comp equation): y = x / sqrt(mean(x^2) + eps) * w. */
+void orc_rmsnorm(int D, const double *x, const uint16_t *w, double eps,
+                 double *y) {
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) ss += x[d] * x[d];
+  double inv = 1.0 / sqrt(ss / (double)D + eps);
+  for (int d = 0; d < D; ++d) y[d] = x[d] * inv * orc_bf16(w[d]);
+}
+
+/* Partial RoPE on the last R channels, interleaved pairs (D-R+2j, D-R+2j+1),
+ * rotated by angle pos * theta^(-2j/R) (in place). */
+void orc_rope(int D, int R, double theta, double pos, double *y) {
+  for (int j = 0; j < R / 2; ++j) {
+    double freq = pow(theta, -2.0 * (double)j / (double)R);
+    double phi = pos * freq;
+    double c = cos(phi), s = sin(phi);
+    int a = D - R + 2 * j;
+    double u = y[a], v = y[a + 1];
+    y[a] = u * c - v * s;
+    y[a + 1] = u * s + v * c;
+  }
+}
+
+/* One compressed entry i: RoPE(Norm(pool)), RoPE position m*i (the first
+ * token of the entry's own block, [CSA2 详解] §7.4). */
+void orc_compress_entry(int m, int D, int R, double theta, double eps,
+                        int64_t i, const uint16_t *Ca, const uint16_t *Za,
+                        const uint16_t *Cb, const uint16_t *Zb,
+                        const uint16_t *Ba, const uint16_t *Bb,
+                        const uint16_t *w, double *out) {
+  double *x = (double *)malloc(sizeof(double) * (size_t)D);
+  orc_compress_pool(m, D, i > 0, Ca, Za, Cb, Zb, Ba, Bb, x);
+  orc_rmsnorm(D, x, w, eps, out);
+  orc_rope(D, R, theta, (double)m * (double)i, out);
+  free(x);
+}
+
+/* ---- visibility ([KV 压缩] §9.8) ---------------------------------------- */
+
+/* Entry s covers tokens up to m*s + m - 1, so the query at position t sees
+ * entries s with (s+1)*m <= t+1: the count is floor((t+1)/m). */
+int64_t orc_visible(int64_t t, int m) { return (t + 1) / m; }
+
+/* ---- lightning indexer ([hca_csa] equation I_{t,s}) ---------------------- */
+
+/* scores[s] = sum_h w[h] * ReLU(q[h,:] . k[s,:]) for s < V.
+ *   q : [H][Dk] e4m3;  w : [H] bf16;  k : [V][Dk] e4m3. */
+void orc_index_scores(int H, int Dk, int64_t V, const uint8_t *q,
+                      const uint16_t *w, const uint8_t *k, double *scores) {
+  for (int64_t s = 0; s < V; ++s) {
+    double total = 0.0;
+    for (int h = 0; h < H; ++h) {
+      double dot = 0.0;
+      for (int c = 0; c < Dk; ++c)
+        dot += orc_e4m3(q[h * Dk + c]) * orc_e4m3(k[s * Dk + c]);
+      double relu = dot > 0.0 ? dot : 0.0;
+      total += orc_bf16(w[h]) * relu;
+    }
+    scores[s] = total;
+  }
+}
+
+/* ---- top-k ---------------------------------------------------------------- */
+
+typedef struct {
+  double score;
+  int64_t index;
+} orc_scored;
+
+/* Larger score first; equal scores: smaller entry index first. */
+static int orc_by_score(const void *pa, const void *pb) {
+  const orc_scored *a = (const orc_scored *)pa, *b = (const orc_scored *)pb;
+  if (a->score > b->score) return -1;
+  if (a->score < b->score) return 1;
+  return (a->index < b->index) ? -1 : (a->index > b->index);
+}
+
+static int orc_by_index(const void *pa, const void *pb) {
+  int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+  return (a > b) - (a < b);
+}
+
+/* The min(k, V) entries with the largest scores (ties toward the smaller
+ * index), written in ascending entry order, then -1 up to k slots.  Returns
+ * the number of selected entries.  Sorting "按位置" follows [结构对比] CSA2. */
+int orc_topk(int64_t V, int k, const double *scores, int32_t *idx) {
+  orc_scored *all = (orc_scored *)malloc(sizeof(orc_scored) * (size_t)(V > 0 ? V : 1));
+  for (int64_t s = 0; s < V; ++s) {
+    all[s].score = scores[s];
+    all[s].index = s;
+  }
+  qsort(all, (size_t)V, sizeof(orc_scored), orc_by_score);
+  int n = (int)(V < k ? V : k);
+  for (int j = 0; j < n; ++j) idx[j] = (int32_t)all[j].index;
+  qsort(idx, (size_t)n, sizeof(int32_t), orc_by_index);
+  for (int j = n; j < k; ++j) idx[j] = -1;
+  free(all);
+  return n;
+}
+
+/* ---- joint softmax with sink ([hca_csa] o_{t,i} equation) ---------------- */
+
+/*
+ * One query: H heads of width D attend to n_rows shared K=V rows.
+ *   l_{h,j} = sm_scale * q[h,:] . row_j
+ *   out[h,:] = sum_j e^{l_hj - M} row_j / (sum_j e^{l_hj - M} + e^{sink_h - M})
+ * with M = max(max_j l_hj, sink_h); lse[h] = M + log(denominator).  The sink
+ * is one more logit in the shared denominator with a zero value row.
+ *   q : [H][D] bf16;  rows : [n_rows][D] bf16 (already gathered);  sink : [H].
+ *   out : [H][D];  lse : [H] (may be NULL).
+ */
+void orc_attend(int H, int D, int n_rows, const uint16_t *q,
+                const uint16_t *rows, const float *sink, double sm_scale,
+                double *out, double *lse) {
+  size_t n = (size_t)(n_rows > 0 ? n_rows : 1);
+  double *logit = (double *)malloc(sizeof(double) * n);
+  double *weight = (double *)malloc(sizeof(double) * n);
+  for (int h = 0; h < H; ++h) {
+    double mx = (double)sink[h];
+    for (int j = 0; j < n_rows; ++j) {
+      double dot = 0.0;
+      for (int c = 0; c < D; ++c)
+        dot += orc_bf16(q[h * D + c]) * orc_bf16(rows[(size_t)j * D + c]);
+      logit[j] = sm_scale * dot;
+      if (logit[j] > mx) mx = logit[j];
+    }
+    double den = exp((double)sink[h] - mx);
+    for (int j = 0; j < n_rows; ++j) {
+      weight[j] = exp(logit[j] - mx);
+      den += weight[j];
+    }
+    for (int c = 0; c < D; ++c) {
+      double num = 0.0;
+      for (int j = 0; j < n_rows; ++j)
+        num += weight[j] * orc_bf16(rows[(size_t)j * D + c]);
+      out[h * D + c] = num / den;
+    }
+    if (lse) lse[h] = mx + log(den);
+  }
+  free(weight);
+  free(logit);
+}
+
+/* ---- array helpers for the Python wrapper -------------------------------- */
+
+void orc_decode_bf16(int64_t n, const uint16_t *in, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16(in[i]);
+}
+
+void orc_decode_e4m3(int64_t n, const uint8_t *in, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3(in[i]);
+}

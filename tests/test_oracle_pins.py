@@ -1,0 +1,381 @@
+"""Pins of the CPU oracle to facts the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: the storage
+formats as decoded by PyTorch, hand-derived closed forms stored under
+tests/golden/ (each with its citation), the pages' worked block-structure
+example, textbook special cases (mean pooling, plain softmax attention via
+scipy, unit RMS, rotation algebra), brute force on tiny inputs, and the top-k
+error bound of "DeepSeek-V4 的 KV 压缩：从删 token 误解到预算检索" §2.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+def bf16_bits(x):
+    t = torch.tensor(np.asarray(x, dtype=np.float64), dtype=torch.float64).to(torch.bfloat16)
+    back = t.to(torch.float64).numpy()
+    assert np.array_equal(back, np.asarray(x, dtype=np.float64)), "value not exact in bf16"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def e4m3_bits(x):
+    t = torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    back = t.to(torch.float64).numpy()
+    assert np.array_equal(back, np.asarray(x, dtype=np.float64)), "value not exact in e4m3"
+    return t.view(torch.uint8).numpy()
+
+
+def rand_bf16(shape, scale=1.0):
+    return bf16_bits(torch.tensor(RNG.standard_normal(shape) * scale).to(torch.bfloat16).double().numpy())
+
+
+def rand_e4m3(shape):
+    return torch.tensor(RNG.standard_normal(shape), dtype=torch.float32).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def closed_form(expr):
+    return float(eval(expr, {"__builtins__": {}},
+                      {"e": math.e, "exp": math.exp, "log": math.log, "sqrt": math.sqrt, "cos": math.cos,
+                       "sin": math.sin}))
+
+
+def load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---- storage formats ------------------------------------------------------
+
+def test_e4m3_decoder_matches_torch_on_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_bf16_decoder_matches_torch_on_all_codes():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(codes.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_to_f64(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def test_bf16_store_rounding_matches_torch():
+    x = RNG.standard_normal(50000) * np.exp(RNG.uniform(-30, 30, 50000))
+    ref = torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.f64_to_bf16_bits(x), ref)
+
+
+# ---- compressor -----------------------------------------------------------
+
+def test_golden_compressor_tiny(golden_dir):
+    g = load(golden_dir, "compressor_tiny_m2.json")
+    m, D = g["m"], g["D"]
+    tok = {k: bf16_bits(v) for k, v in g["tokens"].items()}
+    Ba, Bb, w = bf16_bits(g["Ba"]), bf16_bits(g["Bb"]), bf16_bits(g["rms_w"])
+    n = len(g["expected"])
+    got = oracle.compress(0, n, tok["Ca"], tok["Za"], tok["Cb"], tok["Zb"], None, None, Ba, Bb, w, m=m,
+                          rope_dim=g["rope_dim"], theta=g["theta"], eps=g["eps"])
+    for i in range(n):
+        want = [closed_form(e) for e in g["expected"]["entry%d" % i]]
+        np.testing.assert_allclose(got[i], want, rtol=1e-13, atol=1e-13)
+
+
+def test_golden_block_structure_of_worked_example(golden_dir):
+    """Perturbing one token row changes exactly the entries the page's
+    flowchart connects it to (pins the block / stream index arithmetic)."""
+    g = load(golden_dir, "block_structure_m4.json")
+    m, T, n = g["m"], g["n_tokens"], g["n_entries"]
+    D = 8
+    base = {k: rand_bf16((T, D)) for k in ("Ca", "Za", "Cb", "Zb")}
+    Ba, Bb, w = rand_bf16((m, D)), rand_bf16((m, D)), bf16_bits(np.ones(D))
+
+    def run(t):
+        return oracle.compress(0, n, t["Ca"], t["Za"], t["Cb"], t["Zb"], None, None, Ba, Bb, w, m=m, rope_dim=2)
+
+    ref = run(base)
+    for feed in g["feeds"]:
+        for tok in feed["tokens"]:
+            for which in ("C", "Z"):
+                t = {k: v.copy() for k, v in base.items()}
+                name = which + feed["stream"]
+                t[name][tok] = rand_bf16(D, scale=3.0)
+                changed = [i for i in range(n) if not np.array_equal(run(t)[i], ref[i])]
+                assert changed == feed["entries"], (name, tok, changed)
+
+
+def test_pool_with_flat_logits_is_mean_pooling():
+    """Constant Z and B make every per-channel softmax flat: the entry is the
+    mean of its 2m rows (m rows for entry 0, whose b slots are -inf)."""
+    m, D = 4, 32
+    Ca, Cb = rand_bf16((m, D)), rand_bf16((m, D))
+    Z = bf16_bits(np.full((m, D), 0.75))
+    B0 = bf16_bits(np.zeros((m, D)))
+    dec = oracle.bf16_to_f64
+    x = oracle.compress_pool(Ca, Z, Cb, Z, B0, B0)
+    np.testing.assert_allclose(x, np.concatenate([dec(Ca), dec(Cb)]).mean(0), rtol=1e-14, atol=1e-15)
+    x0 = oracle.compress_pool(Ca, Z, None, None, B0, B0)
+    np.testing.assert_allclose(x0, dec(Ca).mean(0), rtol=1e-14, atol=1e-15)
+
+
+def test_pool_dominant_bias_selects_its_slot():
+    """A block-slot bias 100 above every other logit puts all weight on that
+    slot's row (B^a / B^b are added to Z before the softmax)."""
+    m, D = 4, 16
+    Ca, Za, Cb, Zb = (rand_bf16((m, D)) for _ in range(4))
+    dec = oracle.bf16_to_f64
+    for stream, r in (("a", 2), ("b", 1)):
+        Ba, Bb = bf16_bits(np.zeros((m, D))), bf16_bits(np.zeros((m, D)))
+        (Ba if stream == "a" else Bb)[r] = bf16_bits(np.full(D, 100.0))
+        x = oracle.compress_pool(Ca, Za, Cb, Zb, Ba, Bb)
+        want = dec(Ca)[r] if stream == "a" else dec(Cb)[r]
+        np.testing.assert_allclose(x, want, rtol=1e-12, atol=1e-12)
+
+
+def test_pool_weights_are_per_channel():
+    """Channel d's weights depend only on channel d's logits: perturbing Z in
+    one channel leaves every other channel unchanged."""
+    m, D = 4, 16
+    Ca, Za, Cb, Zb, Ba, Bb = (rand_bf16((m, D)) for _ in range(6))
+    x = oracle.compress_pool(Ca, Za, Cb, Zb, Ba, Bb)
+    Za2 = Za.copy()
+    Za2[:, 5] = rand_bf16(m, scale=4.0)
+    y = oracle.compress_pool(Ca, Za2, Cb, Zb, Ba, Bb)
+    keep = np.arange(D) != 5
+    assert np.array_equal(x[keep], y[keep]) and x[5] != y[5]
+
+
+def test_rmsnorm_gives_unit_rms_and_applies_weight():
+    x = RNG.standard_normal(512) * 3.7
+    ones = bf16_bits(np.ones(512))
+    y = oracle.rmsnorm(x, ones, 0.0)
+    assert abs(np.sqrt(np.mean(y ** 2)) - 1.0) < 1e-14
+    np.testing.assert_allclose(oracle.rmsnorm(5.0 * x, ones, 0.0), y, rtol=1e-14)
+    w = rand_bf16(512)
+    np.testing.assert_allclose(oracle.rmsnorm(x, w, 0.0), y * oracle.bf16_to_f64(w), rtol=1e-14, atol=1e-15)
+    # eps enters under the square root with the mean square
+    y_eps = oracle.rmsnorm(np.full(4, 1.0), bf16_bits(np.ones(4)), 3.0)
+    np.testing.assert_allclose(y_eps, np.full(4, 0.5), rtol=1e-15)
+
+
+def test_rope_rotation_algebra():
+    D, R, theta = 512, 64, 1e4
+    y = RNG.standard_normal(D)
+    np.testing.assert_array_equal(oracle.rope(y, R, theta, 0.0), y)
+    p1, p2 = 37.0, 1000.0
+    a = oracle.rope(oracle.rope(y, R, theta, p1), R, theta, p2)
+    np.testing.assert_allclose(a, oracle.rope(y, R, theta, p1 + p2), rtol=1e-9, atol=1e-9)
+    z = oracle.rope(y, R, theta, 123.0)
+    np.testing.assert_array_equal(z[: D - R], y[: D - R])
+    pairs = lambda v: np.hypot(v[D - R::2], v[D - R + 1::2])
+    np.testing.assert_allclose(pairs(z), pairs(y), rtol=1e-13)
+    # (1, 0) in pair j at position 1 turns counter-clockwise by theta^(-2j/R)
+    for j in (0, 1, 7, 31):
+        e = np.zeros(D)
+        e[D - R + 2 * j] = 1.0
+        r = oracle.rope(e, R, theta, 1.0)
+        ang = math.atan2(r[D - R + 2 * j + 1], r[D - R + 2 * j])
+        assert abs(ang - theta ** (-2.0 * j / R)) < 1e-13
+
+
+def test_compress_entry_is_rope_of_norm_of_pool_at_block_start():
+    m, D, R = 4, 64, 16
+    Ca, Za, Cb, Zb, Ba, Bb = (rand_bf16((m, D)) for _ in range(6))
+    w = rand_bf16(D)
+    i = 11
+    x = oracle.compress_pool(Ca, Za, Cb, Zb, Ba, Bb)
+    want = oracle.rope(oracle.rmsnorm(x, w, 1e-6), R, 1e4, m * i)
+    got = oracle.compress_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, rope_dim=R, theta=1e4, eps=1e-6)
+    np.testing.assert_array_equal(got, want)
+
+
+# ---- visibility, indexer, top-k -------------------------------------------
+
+def test_visibility_matches_last_covered_token_reading():
+    """'DeepSeek-V4 的 KV 压缩' §9.8: with m = 4 entry j is readable at t >= 4j+3."""
+    for t in range(0, 300):
+        brute = sum(1 for j in range(200) if t >= 4 * j + 3)
+        assert oracle.visible(t, 4) == brute
+    for m in (1, 2, 8, 128):
+        for t in (0, m - 2, m - 1, m, 5 * m - 1, 5 * m):
+            if t >= 0:
+                assert oracle.visible(t, m) == sum(1 for j in range(10) if t >= m * j + m - 1)
+
+
+def test_golden_indexer_tiny(golden_dir):
+    g = load(golden_dir, "indexer_tiny.json")
+    q, w, k = e4m3_bits(g["qI"]), bf16_bits(g["wI"]), e4m3_bits(g["kI"])
+    s = oracle.index_scores(q, w, k)
+    np.testing.assert_array_equal(s, g["expected_scores"])
+    for kk, want in g["expected_topk"].items():
+        np.testing.assert_array_equal(oracle.topk(s, int(kk)), want)
+
+
+def test_indexer_single_head_unit_query_reads_one_key_channel():
+    V, Dk = 50, 128
+    k = rand_e4m3((V, Dk))
+    for c in (0, 17, 127):
+        q = np.zeros((1, Dk), np.uint8)
+        q[0, c] = 0x38  # 1.0
+        s = oracle.index_scores(q, bf16_bits([1.0]), k)
+        np.testing.assert_array_equal(s, np.maximum(0.0, oracle.e4m3_to_f64(k[:, c])))
+
+
+def test_indexer_relu_per_head_then_weighted_sum():
+    """Two heads with opposite queries: ReLU keeps exactly one of q.k and -q.k,
+    so with weights (1, 1) the score is |q.k| and with (1, -1) it is q.k."""
+    V, Dk = 40, 128
+    k = rand_e4m3((V, Dk))
+    q1 = rand_e4m3((1, Dk))
+    q = np.concatenate([q1, q1 ^ 0x80])  # sign flip of every e4m3 code
+    dots = oracle.e4m3_to_f64(k) @ oracle.e4m3_to_f64(q1[0])
+    np.testing.assert_allclose(oracle.index_scores(q, bf16_bits([1.0, 1.0]), k), np.abs(dots), rtol=1e-15)
+    np.testing.assert_allclose(oracle.index_scores(q, bf16_bits([1.0, -1.0]), k), dots, rtol=1e-15)
+
+
+def test_topk_matches_exhaustive_subset_search():
+    """Brute force: among all k-subsets whose every member scores >= every
+    non-member, the answer is the lexicographically smallest (ties toward the
+    smaller index), listed ascending."""
+    for trial in range(200):
+        V = int(RNG.integers(1, 9))
+        k = int(RNG.integers(1, 10))
+        scores = RNG.integers(-2, 3, V).astype(np.float64)  # many ties
+        kk = min(k, V)
+        best = None
+        for sub in itertools.combinations(range(V), kk):
+            inside = scores[list(sub)]
+            outside = np.delete(scores, list(sub))
+            if outside.size == 0 or inside.min() >= outside.max():
+                if best is None or sub < best:
+                    best = sub
+        want = list(best) + [-1] * (k - kk)
+        np.testing.assert_array_equal(oracle.topk(scores, k), want)
+
+
+# ---- attention ------------------------------------------------------------
+
+def test_golden_attention_tiny(golden_dir):
+    g = load(golden_dir, "attention_tiny.json")
+    sink = np.array([float(s) for s in g["sink"]], np.float32)
+    out, lse = oracle.attend(bf16_bits(g["q"]), bf16_bits(g["rows"]), sink, g["sm_scale"])
+    want = np.array([[closed_form(e) for e in row] for row in g["expected_out"]])
+    np.testing.assert_allclose(out, want, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse, [closed_form(e) for e in g["expected_lse"]], rtol=1e-14)
+
+
+def test_attention_without_sink_is_plain_softmax_attention():
+    H, D, n = 4, 64, 23
+    q, rows = rand_bf16((H, D)), rand_bf16((n, D))
+    scale = 1 / math.sqrt(D)
+    out, _ = oracle.attend(q, rows, np.full(H, -np.inf, np.float32), scale)
+    Q, K = oracle.bf16_to_f64(q), oracle.bf16_to_f64(rows)
+    want = scipy.special.softmax(scale * Q @ K.T, axis=1) @ K
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_sink_limits_and_single_row():
+    H, D = 3, 32
+    q, rows = rand_bf16((H, D)), rand_bf16((5, D))
+    out, _ = oracle.attend(q, rows, np.full(H, 1e4, np.float32), 0.1)
+    assert np.all(out == 0.0)  # all weight leaks to the sink
+    one = rows[2:3]
+    out1, lse1 = oracle.attend(q, one, np.full(H, -np.inf, np.float32), 0.1)
+    np.testing.assert_array_equal(out1, np.broadcast_to(oracle.bf16_to_f64(one[0]), (H, D)))
+    # a finite sink scales a single row by e^l / (e^l + e^s)
+    s = np.array([0.0, 1.0, -2.0], np.float32)
+    out2, _ = oracle.attend(q, one, s, 0.1)
+    l = 0.1 * oracle.bf16_to_f64(q) @ oracle.bf16_to_f64(one[0])
+    frac = 1.0 / (1.0 + np.exp(s.astype(np.float64) - l))
+    np.testing.assert_allclose(out2, frac[:, None] * oracle.bf16_to_f64(one[0])[None, :], rtol=1e-13)
+
+
+def test_attention_is_invariant_to_row_order():
+    H, D, n = 2, 32, 9
+    q, rows = rand_bf16((H, D)), rand_bf16((n, D))
+    sink = np.array([0.3, -1.0], np.float32)
+    a, la = oracle.attend(q, rows, sink, 0.2)
+    b, lb = oracle.attend(q, rows[RNG.permutation(n)], sink, 0.2)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(la, lb, rtol=1e-14)
+
+
+def test_attention_topk_error_bound():
+    """'DeepSeek-V4 的 KV 压缩' §2: ||o - o_S|| <= 2 V R_t(S), V the largest value
+    norm and R_t(S) the full-attention mass outside S (sink kept on both sides
+    as a member of S with a zero value row)."""
+    H, D, n = 4, 64, 60
+    for trial in range(20):
+        q, rows = rand_bf16((H, D), scale=2.0), rand_bf16((n, D))
+        sink = RNG.standard_normal(H).astype(np.float32)
+        scale = 1 / math.sqrt(D)
+        full, lse = oracle.attend(q, rows, sink, scale)
+        S = np.sort(RNG.choice(n, size=int(RNG.integers(1, n)), replace=False))
+        sparse, _ = oracle.attend(q, rows[S], sink, scale)
+        K = oracle.bf16_to_f64(rows)
+        logits = scale * oracle.bf16_to_f64(q) @ K.T
+        alpha = np.exp(logits - lse[:, None])
+        outside = np.setdiff1d(np.arange(n), S)
+        R = alpha[:, outside].sum(1)
+        Vmax = np.linalg.norm(K, axis=1).max()
+        err = np.linalg.norm(full - sparse, axis=1)
+        assert np.all(err <= 2 * Vmax * R + 1e-12)
+
+
+def test_dense_selection_equals_full_attention_over_visible_entries():
+    """When k covers every visible entry the sparse path is full attention over
+    the window rows plus all V(t) entries."""
+    W, D, H, n_cap, m = 8, 32, 2, 12, 4
+    t = 37                      # V(t) = 9
+    kv = rand_bf16((n_cap, D))
+    swa_ring = rand_bf16((W, D))
+    q, sink = rand_bf16((H, D)), np.array([0.1, -0.4], np.float32)
+    V = oracle.visible(t, m)
+    idx = oracle.topk(RNG.standard_normal(V), 16)
+    out, _ = oracle.attend_query(t, q, idx, kv, lambda u: swa_ring[u % W], sink, W=W, sm_scale=0.3)
+    rows = np.concatenate([swa_ring[[u % W for u in range(t - W + 1, t + 1)]], kv[:V]])
+    want, _ = oracle.attend(q, rows, sink, 0.3)
+    np.testing.assert_allclose(out, want, rtol=1e-13, atol=1e-15)
+    # the window of an early query starts at position 0
+    assert list(oracle.window_positions(3, 128)) == [0, 1, 2, 3]
+    assert list(oracle.window_positions(200, 128)) == list(range(73, 201))
+
+
+def test_decode_emission_reads_the_staged_rows_of_blocks_i_and_i_minus_1():
+    """The decode ring (slot u mod 2m) reproduces the bulk compressor's entry."""
+    m, D, T = 4, 64, 24
+    rows = {k: rand_bf16((T, D)) for k in ("Ca", "Za", "Cb", "Zb")}
+    Ba, Bb, w = rand_bf16((m, D)), rand_bf16((m, D)), rand_bf16(D)
+    bulk = oracle.compress(0, T // m, rows["Ca"], rows["Za"], rows["Cb"], rows["Zb"], None, None, Ba, Bb, w,
+                           m=m, rope_dim=16)
+    for t in (3, 7, 23):
+        ring = {k: np.zeros((2 * m, D), np.uint16) for k in rows}
+        for u in range(max(0, t - 2 * m + 1), t + 1):
+            for k in rows:
+                ring[k][u % (2 * m)] = rows[k][u]
+        n_cap, H = T // m, 2
+        kv = np.zeros((n_cap, D), np.uint16)
+        kI = rand_e4m3((n_cap, 128))
+        kv_after, _, _, _ = oracle.layer_decode_one(
+            t, ring["Ca"], ring["Za"], ring["Cb"], ring["Zb"], Ba, Bb, w, kv, kI, rand_e4m3((H, 128)),
+            rand_bf16(H), rand_bf16((H, D)), rand_bf16((8, D)), np.zeros(H, np.float32), m=m, topk_k=4, W=8,
+            rope_dim=16)
+        i = (t + 1) // m - 1
+        np.testing.assert_array_equal(kv_after[i], oracle.f64_to_bf16_bits(bulk[i]))
