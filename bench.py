@@ -1,0 +1,396 @@
+"""Benchmark of the CSA layer hot path (decode step of the 128K-context
+workload: 64 sequences, 32768 compressed entries each, top-k 512, window 128).
+
+One step = one csa_layer_decode call over the batch: block-boundary emission
+of the new compressed entry, lightning indexer over every visible entry,
+top-k, and the sparse attention.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one process per GPU) every rank decodes its own batch
+of 64 sequences (weak scaling; no data exchange); the time is the maximum
+over ranks.  `--impl reference` times the CPU oracle (the only reference this
+method has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA-layer decode queries/s & indexer HBM GB/s, attn TC util vs GB300 peak"
+UNIT = "queries/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        time.sleep(0.05)
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((ts, float(f[1]), float(f[2]), f))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        t0, t1 = (self.marks + [0, 0])[:2] if len(self.marks) >= 2 else (0, 0)
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.05] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3][5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import compressed_sparse_attention_02_gb300 as csa
+    import synthetic as syn
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = syn.WORKLOADS[args.workload]
+    if args.batch:
+        w = syn.Workload(w.name, w.config, w.kind, B=args.batch, t=w.t, topk=w.topk, n_cap=w.n_cap,
+                         hadamard_kI=w.hadamard_kI)
+    assert w.kind == "decode"
+    B = w.B
+    # each rank's batch is its own slice of sequences (seeded per sequence)
+    x = syn.decode_inputs(syn.Workload(w.name, w.config + 100 * rank, w.kind, B=B, t=w.t, topk=w.topk,
+                                       n_cap=w.n_cap, hadamard_kI=w.hadamard_kI), device=dev)
+    p = csa.csa_default_params(topk=w.topk)
+    kv = x["kv"]
+    idx = torch.empty(B, w.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, 64, dtype=torch.float32, device=dev)
+    ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, w.n_cap, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"],
+                             x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], x["qI"], x["wI"], x["q"], x["swa"],
+                             x["sink"], idx, out, lse, ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = csa.csa_check_status()
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + csa.csa_status_string(st))
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark()
+    launches0 = csa.csa_launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    launches = csa.csa_launch_count() - launches0
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if clocks:
+        clocks.stop()
+    result = {
+        "metric": METRIC, "value": world * B * args.steps / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
+        "data": "synthetic (seeded N(0,1) inputs in the pages' shapes; no trained weights)",
+        "config": {"workload": w.name, "batch_per_gpu": B, "context_tokens": w.t + 1,
+                   "compressed_entries": w.n_cap, "topk": w.topk, "swa_window": w.W, "m": w.m,
+                   "l2": "inputs larger than L2 (K^I %d MiB + KV cache %d MiB per GPU)"
+                         % (B * w.n_cap * 128 >> 20, B * w.n_cap * 1024 >> 20)},
+        "gpu_launches": launches,
+    }
+    if clocks:
+        result["clocks"] = clocks.summary()
+    if rank == 0 and not args.no_extras:
+        result.update(stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args))
+        result["e2e"] = end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args)
+        result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
+    return result
+
+
+def stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args):
+    """Live stage durations of the same decode step (events recorded between
+    the layer call's kernels on its stream), and the roofline of the
+    dominant kernel (the indexer score kernel)."""
+    n = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        csa.csa_set_trace_events(evs[i])
+        step()
+    csa.csa_set_trace_events(None)
+    torch.cuda.synchronize()
+    stage = [[evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(n)] for s in range(4)]
+    mean = [sum(v) / n for v in stage]
+    hbm, bf16, src = peaks()
+    V = (w.t + 1) // w.m
+    idx_bytes = B * (V * 128 + 64 * 128 + 64 * 2)
+    idx_ms = mean[1]
+    achieved = idx_bytes / (idx_ms * 1e-3) / 1e9
+    n_rows = min(w.W, w.t + 1) + min(w.topk, V)
+    attn_flops = B * 4.0 * 64 * 512 * n_rows
+    attn_bytes = B * (n_rows * 1024 + 2 * 64 * 1024)
+    attn_ms = mean[3]
+    traffic = _traffic_from_profile()
+    return {
+        "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_source": src,
+                     "algorithmic_bytes_per_launch": idx_bytes, "avg_launch_ms": idx_ms},
+        "stages_ms": {"compress_emit": mean[0], "index_scores": mean[1], "topk": mean[2], "sparse_attn": mean[3],
+                      "traced_steps": n},
+        "attn": {"tflops": attn_flops / (attn_ms * 1e-3) / 1e12, "tc_frac_of_bf16_peak":
+                 attn_flops / (attn_ms * 1e-3) / 1e12 / bf16, "gbs": attn_bytes / (attn_ms * 1e-3) / 1e9,
+                 "hbm_frac": attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm},
+        "index_topk_gbs": idx_bytes / ((mean[1] + mean[2]) * 1e-3) / 1e9,
+    }
+
+
+def _traffic_from_profile():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (scaled from the captured batch to the full launch), or None when
+    the kernel source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "index_score_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(os.path.join(ROOT, d["source_file"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != d["source_sha256"]:
+                return None
+        return d.get("dram_bytes_per_full_launch")
+    except Exception:
+        return None
+
+
+def end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args):
+    """Same metric through the same C-ABI call with the step's inputs in
+    pinned host memory: each step copies them to the device (queries, indexer
+    queries and weights, positions, the compressor staging rows, the new
+    token's window row and the new entry's indexer key) and reads back the
+    outputs (attention output and selection)."""
+    names = ["q", "qI", "wI", "q_pos", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb"]
+    host = {k: x[k].cpu().pin_memory() for k in names}
+    slot = w.t % w.W
+    entry = (w.t + 1) // w.m - 1
+    host["swa_row"] = x["swa"][:, slot].cpu().pin_memory()
+    host["kI_row"] = x["kI"][:, entry].cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    idx_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    dev = {k: torch.empty_like(x[k]) for k in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
+
+    def step():
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        x["swa"][:, slot].copy_(host["swa_row"], non_blocking=True)
+        x["kI"][:, entry].copy_(host["kI_row"], non_blocking=True)
+        csa.csa_layer_decode(p, B, dev["q_pos"], dev["ring_Ca"], dev["ring_Za"], dev["ring_Cb"], dev["ring_Zb"],
+                             x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], dev["qI"], dev["wI"], dev["q"],
+                             x["swa"], x["sink"], idx, out, lse, ws)
+        out_h.copy_(out, non_blocking=True)
+        idx_h.copy_(idx, non_blocking=True)
+
+    n = min(args.steps, 500)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": B * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_step_inputs(w, x, b):
+    b16 = lambda t: __import__("synthetic").bits(t)
+    return dict(t=w.t, ring_Ca=b16(x["ring_Ca"][b]), ring_Za=b16(x["ring_Za"][b]), ring_Cb=b16(x["ring_Cb"][b]),
+                ring_Zb=b16(x["ring_Zb"][b]), Ba=b16(x["Ba"]), Bb=b16(x["Bb"]), rms_w=b16(x["rms_w"]),
+                kv_comp=b16(x["kv"][b]), kI=b16(x["kI"][b]), qI=b16(x["qI"][b, 0]), wI=b16(x["wI"][b, 0]),
+                q=b16(x["q"][b, 0]), swa_ring=b16(x["swa"][b]), sink=b16(x["sink"]))
+
+
+def cpu_baseline(w, x, seconds):
+    """The oracle's full decode step, one sequence at a time (single thread),
+    for as many sequences as fit in about `seconds`."""
+    import oracle
+    done, t0 = 0, time.perf_counter()
+    while done < w.B and (done == 0 or time.perf_counter() - t0 < seconds):
+        a = _oracle_step_inputs(w, x, done)
+        oracle.layer_decode_one(a.pop("t"), **a, m=w.m, topk_k=w.topk, W=w.W)
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d of the %d sequences of one decode step (full step each: emission, indexer over %d "
+                      "entries, top-%d, attention over %d rows), fp64, single thread"
+                      % (done, w.B, (w.t + 1) // w.m, w.topk, min(w.W, w.t + 1) + w.topk)}
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on this workload's inputs.  Each step
+    decodes a bounded sample: one sequence's step restricted to h of the 64
+    query heads and h of the 64 indexer heads (work per head is identical,
+    so the rate scales by h/64); h is chosen so the whole run stays within a
+    few minutes."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synthetic as syn
+
+    w = syn.WORKLOADS[args.workload]
+    x = syn.decode_inputs(syn.Workload(w.name, w.config, w.kind, B=1, t=w.t, topk=w.topk, n_cap=w.n_cap,
+                                       hadamard_kI=w.hadamard_kI), device="cpu")
+    a = _oracle_step_inputs(w, x, 0)
+    t = a.pop("t")
+
+    def one(h):
+        oracle.layer_decode_one(t, **dict(a, qI=a["qI"][:h], wI=a["wI"][:h], q=a["q"][:h], sink=a["sink"][:h]),
+                                m=w.m, topk_k=w.topk, W=w.W)
+
+    t0 = time.perf_counter()
+    one(1)
+    per_head = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    h = int(max(1, min(64, budget / max(per_head, 1e-6))))
+    for _ in range(args.warmup):
+        one(h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one(h)
+    dt = time.perf_counter() - t0
+    value = args.steps * (h / 64.0) / dt
+    sample = ("per step: one sequence of the decode step on %d of 64 query heads and %d of 64 indexer heads "
+              "(value scaled by %d/64), fp64 oracle, single thread" % (h, h, h))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "batch_per_gpu": w.B},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+"""Python binding of libcsa, the GB300 (sm_103a) CSA layer hot path.
+
+Argument marshalling only: every function below forwards to the C entry point
+of the same name in ``libcsa.so`` (declared in ``include/csa.h``), passing
+device pointers (``tensor.data_ptr()``), sizes, and the current CUDA stream.
+All computation runs in the library's CUDA kernels; there is no fallback, and
+importing this package fails if the library has not been built
+(``python compressed_sparse_attention_02_gb300/build.py``).
+
+Tensor conventions: bf16 tensors are ``torch.bfloat16``, FP8 E4M3 tensors are
+``torch.float8_e4m3fn`` (or uint8 holding the same bits), positions and
+indices ``torch.int32``, the sink ``torch.float32``; every tensor is
+contiguous and on the current CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libcsa.so")
+
+if not os.path.exists(LIBRARY_PATH):
+    raise ImportError(
+        "libcsa.so is not built (expected at %s); run python compressed_sparse_attention_02_gb300/build.py"
+        % LIBRARY_PATH)
+
+_lib = ctypes.CDLL(LIBRARY_PATH)
+
+CSA_OK = 0
+STATUS_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA",
+                4: "CSA_ERR_TIMEOUT", 5: "CSA_ERR_INDEX_RANGE", 6: "CSA_ERR_WORKSPACE"}
+CSA_OP_COMPRESS, CSA_OP_INDEX_TOPK, CSA_OP_SPARSE_ATTN, CSA_OP_LAYER_DECODE, CSA_OP_LAYER_PREFILL = range(5)
+
+
+class CsaParams(ctypes.Structure):
+    """Mirror of ``csa_params``."""
+    _fields_ = [("m", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("swa_window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float)]
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s returned %s: %s" % (where, STATUS_NAMES.get(status, status),
+                                                  csa_status_string(status)))
+
+
+_vp = ctypes.c_void_p
+_i32, _i64, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_P = ctypes.POINTER(CsaParams)
+
+_lib.csa_default_params.argtypes = [_P]
+_lib.csa_default_params.restype = None
+_lib.csa_workspace_size.argtypes = [_i32, _P, _i32, _i32, _i64]
+_lib.csa_workspace_size.restype = _sz
+_lib.csa_compress.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64, _vp]
+_lib.csa_index_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
+_lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
+                                 _vp, _sz, _vp]
+_lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
+_lib.csa_layer_prefill.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
+for _f in ("csa_compress", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode", "csa_layer_prefill"):
+    getattr(_lib, _f).restype = ctypes.c_int
+_lib.csa_set_trace_events.argtypes = [ctypes.POINTER(_vp), _i32]
+_lib.csa_set_trace_events.restype = ctypes.c_int
+_lib.csa_launch_count.argtypes = []
+_lib.csa_launch_count.restype = ctypes.c_uint64
+_lib.csa_check_status.argtypes = [_vp]
+_lib.csa_check_status.restype = ctypes.c_int
+_lib.csa_status_string.argtypes = [ctypes.c_int]
+_lib.csa_status_string.restype = ctypes.c_char_p
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str):
+    if status != CSA_OK:
+        raise CsaError(status, where)
+
+
+def csa_default_params(**overrides) -> CsaParams:
+    """The V4-Flash CSA parameters (m=4, 64x512 heads, top-k 512, window 128,
+    theta 1e4, eps 1e-6, scale 1/sqrt(512)), with any field overridden."""
+    p = CsaParams()
+    _lib.csa_default_params(ctypes.byref(p))
+    for k, v in overrides.items():
+        setattr(p, k, v)
+    return p
+
+
+def csa_status_string(status: int) -> str:
+    return _lib.csa_status_string(int(status)).decode()
+
+
+def csa_workspace_size(op: int, params: CsaParams, B: int, Q: int, n_cap: int) -> int:
+    return int(_lib.csa_workspace_size(op, ctypes.byref(params), B, Q, n_cap))
+
+
+def workspace(op: int, params: CsaParams, B: int, Q: int, n_cap: int, device=None) -> torch.Tensor:
+    """Allocates (through torch) a workspace of csa_workspace_size() bytes."""
+    n = csa_workspace_size(op, params, B, Q, n_cap)
+    if n == 0:
+        raise CsaError(2, "csa_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def csa_compress(params, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_out, kv_stride_b,
+                 stream=None):
+    _check(_lib.csa_compress(ctypes.byref(params), B, n_new, entry0, _ptr(Ca), _ptr(Za), _ptr(Cb), _ptr(Zb),
+                             _ptr(Cb_prev), _ptr(Zb_prev), _ptr(Ba), _ptr(Bb), _ptr(rms_w), _ptr(kv_out),
+                             kv_stride_b, _stream(stream)), "csa_compress")
+
+
+def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, ws, stream=None):
+    _check(_lib.csa_index_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
+                               _ptr(idx_out), _ptr(score_out), _ptr(ws), 0 if ws is None else ws.numel(),
+                               _stream(stream)), "csa_index_topk")
+
+
+def csa_sparse_attn(params, B, Q, q_pos, q, kv_comp, n_cap, idx, swa, swa_mode, swa_len, swa_pos0, sink, out,
+                    lse=None, ws=None, stream=None):
+    _check(_lib.csa_sparse_attn(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(q), _ptr(kv_comp), n_cap, _ptr(idx),
+                                _ptr(swa), swa_mode, swa_len, _ptr(swa_pos0), _ptr(sink), _ptr(out), _ptr(lse),
+                                _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)), "csa_sparse_attn")
+
+
+def csa_layer_decode(params, B, q_pos, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI,
+                     wI, q, swa_ring, sink, idx_out, out, lse, ws, stream=None):
+    _check(_lib.csa_layer_decode(ctypes.byref(params), B, _ptr(q_pos), _ptr(ring_Ca), _ptr(ring_Za),
+                                 _ptr(ring_Cb), _ptr(ring_Zb), _ptr(Ba), _ptr(Bb), _ptr(rms_w), _ptr(kv_comp),
+                                 n_cap, _ptr(kI), _ptr(qI), _ptr(wI), _ptr(q), _ptr(swa_ring), _ptr(sink),
+                                 _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                                 _stream(stream)), "csa_layer_decode")
+
+
+def csa_layer_prefill(params, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI,
+                      wI, q, swa, sink, idx_out, out, lse, ws, stream=None):
+    _check(_lib.csa_layer_prefill(ctypes.byref(params), B, Q, pos0, _ptr(Ca), _ptr(Za), _ptr(Cb), _ptr(Zb),
+                                  _ptr(Cb_prev), _ptr(Zb_prev), _ptr(Ba), _ptr(Bb), _ptr(rms_w), _ptr(kv_comp),
+                                  n_cap, _ptr(kI), _ptr(qI), _ptr(wI), _ptr(q), _ptr(swa), _ptr(sink),
+                                  _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                                  _stream(stream)), "csa_layer_prefill")
+
+
+def csa_check_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status."""
+    return int(_lib.csa_check_status(_stream(stream)))
+
+
+def csa_set_trace_events(events) -> None:
+    """Record the five stage-boundary events (torch.cuda.Event, timing
+    enabled) in every following layer call; None turns tracing off."""
+    if events is None:
+        _check(_lib.csa_set_trace_events(None, 0), "csa_set_trace_events")
+        return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event at its first record
+            e.record()
+    arr = (_vp * len(events))(*[e.cuda_event for e in events])
+    _check(_lib.csa_set_trace_events(arr, len(events)), "csa_set_trace_events")
+
+
+def csa_launch_count() -> int:
+    """Kernels launched by libcsa in this process so far."""
+    return int(_lib.csa_launch_count())

@@ -1,0 +1,460 @@
+// C ABI of libcsa (declared in include/csa.h): host-side argument checks,
+// workspace sizing, and the launch sequences of the single-stage and layer
+// calls.  No call allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/csa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace csa {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace csa
+
+namespace {
+
+// Device status word: kernels OR error bits into it, csa_check_status reads
+// and clears it.  One per device (module globals are per context).
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// Stage tracing (csa_set_trace_events): events recorded between the stages
+// of the layer calls.
+cudaEvent_t g_trace[5] = {};
+bool g_trace_on = false;
+
+void trace(int stage, cudaStream_t st) {
+  if (g_trace_on) cudaEventRecord(g_trace[stage], st);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+
+// Dimensions the kernels are built for; anything else is unsupported.
+csa_status check_params(const csa_params* p) {
+  if (!p) return CSA_ERR_INVALID_ARG;
+  if (p->n_heads != csa::kHeads || p->head_dim != csa::kDim || p->rope_dim != csa::kRope ||
+      p->idx_heads != csa::kIdxHeads || p->idx_dim != csa::kIdxDim)
+    return CSA_ERR_UNSUPPORTED;
+  if (!(p->m == 1 || p->m == 2 || p->m == 4 || p->m == 8)) return CSA_ERR_UNSUPPORTED;
+  if (p->topk < 1 || p->topk > csa::kMaxTopk) return CSA_ERR_UNSUPPORTED;
+  if (p->swa_window < 1 || p->swa_window > csa::kMaxWindow) return CSA_ERR_UNSUPPORTED;
+  if (!(p->rope_theta > 0.f) || !(p->rms_eps >= 0.f) || !isfinite(p->sm_scale)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+struct IndexWs {
+  size_t scores_off, cand_key_off, cand_idx_off, total;
+  int64_t score_ld;
+  int chunk, n_chunks;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
+  w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 4));
+  csa::topk_chunking(rows, n_cap, k, &w->chunk, &w->n_chunks);
+  if (static_cast<int64_t>(w->n_chunks) * k > csa::kTopkMaxItems && w->n_chunks > 1) return false;
+  w->scores_off = 0;
+  size_t off = round_up(static_cast<size_t>(rows) * w->score_ld * 4, 256);
+  w->cand_key_off = off;
+  const size_t cand = w->n_chunks > 1 ? static_cast<size_t>(rows) * w->n_chunks * k * 4 : 0;
+  off = round_up(off + cand, 256);
+  w->cand_idx_off = off;
+  off = round_up(off + cand, 256);
+  w->total = off;
+  return true;
+}
+
+csa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+// Shared body of csa_index_topk and the layer calls.
+csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
+                          const uint8_t* qI, const uint16_t* wI, const uint8_t* kI, int64_t n_cap,
+                          int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes, cudaStream_t st,
+                          bool traced = false) {
+  IndexWs w;
+  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < w.total || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  unsigned* status = status_ptr();
+  if (!enc || !status) return CSA_ERR_CUDA;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
+
+  csa::IndexArgs ia;
+  ia.qI = qI;
+  ia.wI = wI;
+  ia.kI = kI;
+  ia.q_pos = q_pos;
+  ia.pos_base = pos_base;
+  ia.B = B;
+  ia.Q = Q;
+  ia.m = p->m;
+  ia.n_cap = n_cap;
+  ia.scores = scores;
+  ia.score_ld = w.score_ld;
+  ia.status = status;
+  csa_status s = cuda_status(csa::launch_index_scores(ia, enc, st));
+  if (s != CSA_OK) return s;
+  if (traced) trace(2, st);
+
+  csa::TopkArgs ta;
+  ta.scores = scores;
+  ta.score_ld = w.score_ld;
+  ta.q_pos = q_pos;
+  ta.pos_base = pos_base;
+  ta.B = B;
+  ta.Q = Q;
+  ta.m = p->m;
+  ta.k = p->topk;
+  ta.n_cap = n_cap;
+  ta.chunk = w.chunk;
+  ta.n_chunks = w.n_chunks;
+  ta.idx_out = idx_out;
+  ta.score_out = score_out;
+  ta.cand_key = reinterpret_cast<uint32_t*>(wsb + w.cand_key_off);
+  ta.cand_idx = reinterpret_cast<int32_t*>(wsb + w.cand_idx_off);
+  ta.status = status;
+  return cuda_status(csa::launch_topk(ta, st));
+}
+
+csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
+                    const uint16_t* q, const uint16_t* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
+                    int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
+                    const float* sink, uint16_t* out, float* lse, cudaStream_t st) {
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  csa::AttnArgs aa;
+  aa.q_pos = q_pos;
+  aa.pos_base = pos_base;
+  aa.q = q;
+  aa.kv = kv;
+  aa.n_cap = n_cap;
+  aa.idx = idx;
+  aa.k = p->topk;
+  aa.swa = swa;
+  aa.swa_mode = swa_mode;
+  aa.swa_len = swa_len;
+  aa.swa_pos0 = swa_pos0;
+  aa.swa_pos0_base = swa_pos0_base;
+  aa.W = p->swa_window;
+  aa.sink = sink;
+  aa.out = out;
+  aa.lse = lse;
+  aa.B = B;
+  aa.Q = Q;
+  aa.sm_scale = p->sm_scale;
+  aa.status = status;
+  return cuda_status(csa::launch_sparse_attn(aa, st));
+}
+
+csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,
+                        const uint16_t* Ca, const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
+                        const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
+                        const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
+                        int64_t n_cap, const int32_t* q_pos, cudaStream_t st) {
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  csa::CompressArgs ca;
+  ca.mode = mode;
+  ca.B = B;
+  ca.m = p->m;
+  ca.n_new = n_new;
+  ca.entry0 = entry0;
+  ca.Ca = Ca;
+  ca.Za = Za;
+  ca.Cb = Cb;
+  ca.Zb = Zb;
+  ca.Cb_prev = Cb_prev;
+  ca.Zb_prev = Zb_prev;
+  ca.Ba = Ba;
+  ca.Bb = Bb;
+  ca.rms_w = rms_w;
+  ca.kv_out = kv_out;
+  ca.kv_stride_b = kv_stride_b;
+  ca.n_cap = n_cap;
+  ca.q_pos = q_pos;
+  ca.rope_theta = static_cast<double>(p->rope_theta);
+  ca.rms_eps = p->rms_eps;
+  ca.status = status;
+  return cuda_status(csa::launch_compress(ca, st));
+}
+
+bool n_cap_ok(int64_t n_cap) { return n_cap >= 1 && n_cap <= (int64_t(1) << 30); }
+
+}  // namespace
+
+extern "C" {
+
+void csa_default_params(csa_params* p) {
+  if (!p) return;
+  p->m = 4;
+  p->n_heads = 64;
+  p->head_dim = 512;
+  p->rope_dim = 64;
+  p->idx_heads = 64;
+  p->idx_dim = 128;
+  p->topk = 512;
+  p->swa_window = 128;
+  p->rope_theta = 10000.f;
+  p->rms_eps = 1e-6f;
+  p->sm_scale = 0.044194173824159216f;  // 1/sqrt(512)
+}
+
+size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {
+  if (check_params(p) != CSA_OK || B < 0 || Q < 0 || !n_cap_ok(n_cap)) return 0;
+  IndexWs w;
+  switch (op) {
+    case CSA_OP_COMPRESS:
+    case CSA_OP_SPARSE_ATTN:
+      return 16;  // no scratch needed; a non-zero size keeps callers uniform
+    case CSA_OP_INDEX_TOPK:
+    case CSA_OP_LAYER_PREFILL:
+      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w) ? w.total : 0;
+    case CSA_OP_LAYER_DECODE:
+      return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w) ? w.total : 0;
+    default:
+      return 0;
+  }
+}
+
+csa_status csa_compress(const csa_params* p, int32_t B, int32_t n_new, int64_t entry0, const uint16_t* Ca,
+                        const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb, const uint16_t* Cb_prev,
+                        const uint16_t* Zb_prev, const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w,
+                        uint16_t* kv_out, int64_t kv_stride_b, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return CSA_OK;
+  if (!ok_ptr(Ca) || !ok_ptr(Za) || !ok_ptr(Cb) || !ok_ptr(Zb) || !ok_ptr(Ba) || !ok_ptr(Bb) ||
+      !ok_ptr(rms_w) || !ok_ptr(kv_out))
+    return CSA_ERR_INVALID_ARG;
+  if ((entry0 > 0) != (Cb_prev != nullptr) || (Cb_prev == nullptr) != (Zb_prev == nullptr) || !ok_opt(Cb_prev) ||
+      !ok_opt(Zb_prev))
+    return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b < (entry0 + n_new) * csa::kDim && B > 1) return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b % 8 != 0) return CSA_ERR_INVALID_ARG;
+  return run_compress(p, 0, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_out,
+                      kv_stride_b, entry0 + n_new, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
+                          const uint16_t* wI, const uint8_t* kI, int64_t n_cap, int32_t* idx_out, float* score_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Q == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(idx_out) || !ok_opt(score_out))
+    return CSA_ERR_INVALID_ARG;
+  return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint16_t* q,
+                           const uint16_t* kv_comp, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
+                           int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, const float* sink,
+                           uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 2147483647 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Q == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(q) || !ok_ptr(kv_comp) || !ok_ptr(idx) || !ok_ptr(swa) || !ok_ptr(sink) ||
+      !ok_ptr(out) || !ok_opt(lse))
+    return CSA_ERR_INVALID_ARG;
+  if (swa_mode == 0) {
+    swa_len = p->swa_window;
+  } else if (swa_mode == 1) {
+    if (swa_len < 1 || !ok_ptr(swa_pos0)) return CSA_ERR_INVALID_ARG;
+  } else {
+    return CSA_ERR_INVALID_ARG;
+  }
+  return run_attn(p, B, Q, q_pos, 0, q, kv_comp, n_cap, idx, swa, swa_mode, swa_len, swa_pos0, 0, sink, out, lse,
+                  static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
+                            const uint16_t* ring_Za, const uint16_t* ring_Cb, const uint16_t* ring_Zb,
+                            const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_comp,
+                            int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
+                            const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
+                            uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(ring_Ca) || !ok_ptr(ring_Za) || !ok_ptr(ring_Cb) || !ok_ptr(ring_Zb) ||
+      !ok_ptr(Ba) || !ok_ptr(Bb) || !ok_ptr(rms_w) || !ok_ptr(kv_comp) || !ok_ptr(kI) || !ok_ptr(qI) ||
+      !ok_ptr(wI) || !ok_ptr(q) || !ok_ptr(swa_ring) || !ok_ptr(sink) || !ok_ptr(idx_out) || !ok_ptr(out) ||
+      !ok_opt(lse))
+    return CSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  IndexWs w;
+  if (!index_workspace(B, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+  // 1. emission of the entry that completes at this step (if any)
+  trace(0, st);
+  s = run_compress(p, 1, B, 1, 0, ring_Ca, ring_Za, ring_Cb, ring_Zb, nullptr, nullptr, Ba, Bb, rms_w, kv_comp,
+                   n_cap * csa::kDim, n_cap, q_pos, st);
+  if (s != CSA_OK) return s;
+  trace(1, st);
+  // 2. indexer + top-k over the visible entries
+  s = run_index_topk(p, B, 1, q_pos, 0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st, true);
+  if (s != CSA_OK) return s;
+  trace(3, st);
+  // 3. sparse attention over the window ring and the selection
+  s = run_attn(p, B, 1, q_pos, 0, q, kv_comp, n_cap, idx_out, swa_ring, 0, p->swa_window, nullptr, 0, sink, out,
+               lse, st);
+  trace(4, st);
+  return s;
+}
+
+csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
+                             const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb, const uint16_t* Cb_prev,
+                             const uint16_t* Zb_prev, const uint16_t* Ba, const uint16_t* Bb,
+                             const uint16_t* rms_w, uint16_t* kv_comp, int64_t n_cap, const uint8_t* kI,
+                             const uint8_t* qI, const uint16_t* wI, const uint16_t* q, const uint16_t* swa,
+                             const float* sink, int32_t* idx_out, uint16_t* out, float* lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || pos0 < 0 || pos0 % p->m != 0 || !n_cap_ok(n_cap))
+    return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Q == 0) return CSA_OK;
+  const int64_t entry0 = pos0 / p->m;
+  const int64_t n_new = (pos0 + Q) / p->m - entry0;
+  if (entry0 + n_new > n_cap) return CSA_ERR_INVALID_ARG;
+  if (!ok_ptr(Ca) || !ok_ptr(Za) || !ok_ptr(Cb) || !ok_ptr(Zb) || !ok_ptr(Ba) || !ok_ptr(Bb) || !ok_ptr(rms_w) ||
+      !ok_ptr(kv_comp) || !ok_ptr(kI) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(q) || !ok_ptr(swa) ||
+      !ok_ptr(sink) || !ok_ptr(idx_out) || !ok_ptr(out) || !ok_opt(lse))
+    return CSA_ERR_INVALID_ARG;
+  if ((pos0 > 0) != (Cb_prev != nullptr) || (Cb_prev == nullptr) != (Zb_prev == nullptr) || !ok_opt(Cb_prev) ||
+      !ok_opt(Zb_prev))
+    return CSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  IndexWs w;
+  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+  trace(0, st);
+  // 1. compress the chunk's complete blocks.  Rows are [B][Q][D]; the
+  //    compressor reads m*n_new of them per sequence with a stride of Q rows.
+  if (n_new > 0) {
+    if (static_cast<int64_t>(Q) != n_new * p->m) {
+      // Ragged chunk: compress sequence by sequence so the row stride is Q.
+      for (int32_t b = 0; b < B; ++b) {
+        const int64_t off = static_cast<int64_t>(b) * Q * csa::kDim;
+        const int64_t poff = static_cast<int64_t>(b) * p->m * csa::kDim;
+        s = run_compress(p, 0, 1, n_new, entry0, Ca + off, Za + off, Cb + off, Zb + off,
+                         Cb_prev ? Cb_prev + poff : nullptr, Zb_prev ? Zb_prev + poff : nullptr, Ba, Bb, rms_w,
+                         kv_comp + static_cast<int64_t>(b) * n_cap * csa::kDim, n_cap * csa::kDim, n_cap, nullptr,
+                         st);
+        if (s != CSA_OK) return s;
+      }
+    } else {
+      s = run_compress(p, 0, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp,
+                       n_cap * csa::kDim, n_cap, nullptr, st);
+      if (s != CSA_OK) return s;
+    }
+  }
+  trace(1, st);
+  // 2. indexer + top-k, each query over its own V(t)
+  s = run_index_topk(p, B, Q, nullptr, pos0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st,
+                     true);
+  if (s != CSA_OK) return s;
+  trace(3, st);
+  // 3. sparse attention with the linear window (row j = position pos0-(W-1)+j)
+  s = run_attn(p, B, Q, nullptr, pos0, q, kv_comp, n_cap, idx_out, swa, 1, static_cast<int64_t>(p->swa_window) - 1 + Q,
+               nullptr, pos0 - (p->swa_window - 1), sink, out, lse, st);
+  trace(4, st);
+  return s;
+}
+
+uint64_t csa_launch_count(void) { return csa::g_launches.load(std::memory_order_relaxed); }
+
+csa_status csa_set_trace_events(void* const* events, int32_t n_events) {
+  if (!events) {
+    g_trace_on = false;
+    return CSA_OK;
+  }
+  if (n_events != 5) return CSA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i) {
+    if (!events[i]) return CSA_ERR_INVALID_ARG;
+    g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_trace_on = true;
+  return CSA_OK;
+}
+
+csa_status csa_check_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
+  unsigned* p = status_ptr();
+  if (!p) return CSA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, p, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  const unsigned zero = 0;
+  if (word && cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return CSA_ERR_CUDA;
+  if (word & csa::kErrTimeout) return CSA_ERR_TIMEOUT;
+  if (word & csa::kErrIndexRange) return CSA_ERR_INDEX_RANGE;
+  return CSA_OK;
+}
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID_ARG: return "CSA_ERR_INVALID_ARG: null, misaligned or out-of-range argument";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: dimensions other than the supported CSA shape";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA call or launch failed";
+    case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case CSA_ERR_INDEX_RANGE: return "CSA_ERR_INDEX_RANGE: a position or index pointed outside a cache";
+    case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "CSA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

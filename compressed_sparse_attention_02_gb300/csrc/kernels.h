@@ -1,0 +1,107 @@
+// Host-side launchers of the CSA kernels (internal to libcsa; the public C ABI
+// is include/csa.h).  Every launcher enqueues on `stream` and returns the
+// launch's cudaError_t; arguments are validated by the C-ABI layer first.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+// Counts successful kernel launches (reported by csa_launch_count).
+void note_launch();
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+// Fixed model dimensions the kernels are specialised for.
+constexpr int kHeads = 64;      // query heads
+constexpr int kDim = 512;       // shared K=V latent width
+constexpr int kRope = 64;       // RoPE channels (the last kRope of kDim)
+constexpr int kIdxHeads = 64;   // indexer heads
+constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
+constexpr int kMaxTopk = 2048;
+constexpr int kMaxWindow = 1024;
+constexpr int kTopkMaxItems = 16384;  // items one top-k block selects from
+
+// ---- compressor --------------------------------------------------------------
+struct CompressArgs {
+  int mode;                 // 0: bulk chunk, 1: decode ring (one entry at most)
+  int B, m;
+  int64_t n_new, entry0;    // bulk: entries entry0 .. entry0+n_new-1
+  const uint16_t *Ca, *Za, *Cb, *Zb;  // bulk [B][m*n_new][D]; ring [B][2m][D]
+  const uint16_t *Cb_prev, *Zb_prev;  // bulk [B][m][D] or null
+  const uint16_t *Ba, *Bb, *rms_w;
+  uint16_t* kv_out;
+  int64_t kv_stride_b;      // elements between sequences of kv_out
+  int64_t n_cap;            // ring mode: entries the cache holds
+  const int32_t* q_pos;     // ring mode: [B] positions
+  double rope_theta;
+  float rms_eps;
+  unsigned* status;
+};
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
+
+// ---- lightning indexer scores (tcgen05, FP8) -------------------------------------
+struct IndexArgs {
+  const uint8_t* qI;        // [B][Q][64][128]
+  const uint16_t* wI;       // [B][Q][64]
+  const uint8_t* kI;        // [B][n_cap][128]
+  const int32_t* q_pos;     // [B][Q] or null (then pos_base + q)
+  int64_t pos_base;
+  int B, Q, m;
+  int64_t n_cap;
+  float* scores;            // [B*Q][score_ld]
+  int64_t score_ld;
+  unsigned* status;
+};
+cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                                cudaStream_t stream);
+
+// ---- top-k -------------------------------------------------------------------------
+struct TopkArgs {
+  const float* scores;
+  int64_t score_ld;
+  const int32_t* q_pos;
+  int64_t pos_base;
+  int B, Q, m, k;
+  int64_t n_cap;
+  int chunk, n_chunks;      // from topk_chunking()
+  int32_t* idx_out;         // [B][Q][k]
+  float* score_out;         // [B][Q][k] or null
+  uint32_t* cand_key;       // [B*Q][n_chunks][k] (n_chunks > 1)
+  int32_t* cand_idx;
+  unsigned* status;
+};
+// Chooses the chunk length the first selection pass works on.
+void topk_chunking(int64_t rows, int64_t n_cap, int k, int* chunk, int* n_chunks);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
+// ---- sparse attention (tcgen05, bf16) ------------------------------------------------
+struct AttnArgs {
+  const int32_t* q_pos;     // [B][Q] or null (then pos_base + q)
+  int64_t pos_base;
+  const uint16_t* q;        // [B][Q][64][512]
+  const uint16_t* kv;       // [B][n_cap][512]
+  int64_t n_cap;
+  const int32_t* idx;       // [B][Q][k]
+  int k;
+  const uint16_t* swa;
+  int swa_mode;             // 0 ring [B][W][512]; 1 linear [B][swa_len][512]
+  int64_t swa_len;
+  const int32_t* swa_pos0;  // [B] (mode 1) or null (then swa_pos0_base)
+  int64_t swa_pos0_base;
+  int W;
+  const float* sink;        // [64]
+  uint16_t* out;            // [B][Q][64][512]
+  float* lse;               // [B][Q][64] or null
+  int B, Q;
+  float sm_scale;
+  unsigned* status;
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace csa

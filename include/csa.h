@@ -244,6 +244,19 @@ csa_status csa_layer_prefill(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Optional stage tracing, for profiling.  With events != NULL (n_events == 5
+ * cudaEvent_t handles passed as void*), every csa_layer_decode and
+ * csa_layer_prefill call records events[0] on its stream before its first
+ * kernel and events[s] after stage s: 1 compressor, 2 indexer scores, 3 top-k,
+ * 4 sparse attention.  events == NULL turns tracing off.  The setting is
+ * process-wide; set it only while no layer call runs on another thread.
+ */
+csa_status csa_set_trace_events(void *const *events, int32_t n_events);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t csa_launch_count(void);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device (CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_INDEX_RANGE), or
  * CSA_ERR_CUDA if the stream reported an error.

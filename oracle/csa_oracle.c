@@ -141,17 +141,22 @@ int64_t orc_visible(int64_t t, int m) { return (t + 1) / m; }
  *   q : [H][Dk] e4m3;  w : [H] bf16;  k : [V][Dk] e4m3. */
 void orc_index_scores(int H, int Dk, int64_t V, const uint8_t *q,
                       const uint16_t *w, const uint8_t *k, double *scores) {
+  double *qd = (double *)malloc(sizeof(double) * (size_t)H * (size_t)Dk);
+  double *kd = (double *)malloc(sizeof(double) * (size_t)Dk);
+  for (int i = 0; i < H * Dk; ++i) qd[i] = orc_e4m3(q[i]);
   for (int64_t s = 0; s < V; ++s) {
+    for (int c = 0; c < Dk; ++c) kd[c] = orc_e4m3(k[s * Dk + c]);
     double total = 0.0;
     for (int h = 0; h < H; ++h) {
       double dot = 0.0;
-      for (int c = 0; c < Dk; ++c)
-        dot += orc_e4m3(q[h * Dk + c]) * orc_e4m3(k[s * Dk + c]);
+      for (int c = 0; c < Dk; ++c) dot += qd[h * Dk + c] * kd[c];
       double relu = dot > 0.0 ? dot : 0.0;
       total += orc_bf16(w[h]) * relu;
     }
     scores[s] = total;
   }
+  free(kd);
+  free(qd);
 }
 
 /* ---- top-k ---------------------------------------------------------------- */

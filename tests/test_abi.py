@@ -1,0 +1,90 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point include/csa.h declares, and rejects bad arguments on the host before any
+launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__._load_builder().build()
+    import compressed_sparse_attention_02_gb300 as csa
+    return csa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_entry_point_is_exported(lib):
+    names = declared_functions()
+    assert {"csa_compress", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode", "csa_layer_prefill",
+            "csa_check_status", "csa_workspace_size"} <= set(names)
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_default_params_and_status_strings(lib):
+    p = lib.csa_default_params()
+    assert (p.m, p.n_heads, p.head_dim, p.rope_dim, p.idx_heads, p.idx_dim, p.topk, p.swa_window) == \
+        (4, 64, 512, 64, 64, 128, 512, 128)
+    assert abs(p.sm_scale - 512 ** -0.5) < 1e-7 and p.rope_theta == 1e4
+    for s in range(7):
+        assert lib.csa_status_string(s).startswith(lib.STATUS_NAMES[s])
+
+
+def test_workspace_sizes(lib):
+    p = lib.csa_default_params()
+    n = lib.csa_workspace_size(lib.CSA_OP_LAYER_DECODE, p, 64, 1, 32768)
+    assert n >= 64 * 32768 * 4
+    assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, p, 8, 1, 262144) >= 8 * 262144 * 4
+    bad = lib.csa_default_params(head_dim=256)
+    assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, bad, 1, 1, 1024) == 0
+
+
+def _call_raw(lib, fn, *args):
+    return getattr(ctypes.CDLL(lib.LIBRARY_PATH), fn)(*args)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    raw.csa_index_topk.restype = ctypes.c_int
+    raw.csa_compress.restype = ctypes.c_int
+    raw.csa_layer_decode.restype = ctypes.c_int
+    p = lib.csa_default_params()
+    P = ctypes.byref(p)
+    fake = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: rejected first
+    odd = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+    i64 = ctypes.c_int64
+    # null pointers
+    assert raw.csa_index_topk(P, 1, 1, None, None, None, None, i64(1024), None, None, None, ctypes.c_size_t(0),
+                              None) == 1
+    # misaligned pointer
+    assert raw.csa_compress(P, 1, 4, i64(0), odd, fake, fake, fake, None, None, fake, fake, fake, fake, i64(4096),
+                            None) == 1
+    # previous-block rows must be given iff entry0 > 0
+    assert raw.csa_compress(P, 1, 4, i64(3), fake, fake, fake, fake, None, None, fake, fake, fake, fake,
+                            i64(8 * 512), None) == 1
+    # unsupported dimensions
+    p2 = lib.csa_default_params(n_heads=128)
+    assert raw.csa_compress(ctypes.byref(p2), 1, 4, i64(0), fake, fake, fake, fake, None, None, fake, fake, fake,
+                            fake, i64(4096), None) == 2
+    p3 = lib.csa_default_params(topk=4096)
+    assert raw.csa_index_topk(ctypes.byref(p3), 1, 1, fake, fake, fake, fake, i64(1024), fake, None, fake,
+                              ctypes.c_size_t(1 << 30), None) == 2
+    # workspace too small
+    assert raw.csa_index_topk(P, 1, 1, fake, fake, fake, fake, i64(1024), fake, None, fake, ctypes.c_size_t(16),
+                              None) == 6
+    # empty batch is a no-op
+    assert raw.csa_compress(P, 0, 4, i64(0), None, None, None, None, None, None, None, None, None, None, i64(0),
+                            None) == 0

@@ -1,0 +1,154 @@
+"""Whole-layer parity (csa_layer_decode / csa_layer_prefill) against the
+oracle's composition of the same steps, on every workload of the pages'
+configurations (full size; sampled sequences / queries where the oracle
+would take too long)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from _util import assert_close, bits, check_topk
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def csa():
+    import compressed_sparse_attention_02_gb300 as m
+    return m
+
+
+def run_decode(csa, p, w, g, kv):
+    B = w.B
+    idx = torch.empty(B, p.topk, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, w.n_cap)
+    csa.csa_layer_decode(p, B, g["q_pos"], g["ring_Ca"], g["ring_Za"], g["ring_Cb"], g["ring_Zb"], g["Ba"], g["Bb"],
+                         g["rms_w"], kv, w.n_cap, g["kI"], g["qI"], g["wI"], g["q"], g["swa"], g["sink"], idx, out, lse,
+                         ws)
+    st = csa.csa_check_status()
+    assert st == 0, csa.csa_status_string(st)
+    return idx.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check_decode_seq(w, x, b, kv_in, kv_gpu, idx, out, lse):
+    """Oracle decode step of sequence b (its own emission, selection and
+    attention) against the GPU results."""
+    kv_o, idx_o, out_o, lse_o = oracle.layer_decode_one(
+        w.t, bits(x["ring_Ca"][b]), bits(x["ring_Za"][b]), bits(x["ring_Cb"][b]), bits(x["ring_Zb"][b]),
+        bits(x["Ba"]), bits(x["Bb"]), bits(x["rms_w"]), kv_in, bits(x["kI"][b]), bits(x["qI"][b, 0]),
+        bits(x["wI"][b, 0]), bits(x["q"][b, 0]), bits(x["swa"][b]), bits(x["sink"]), m=w.m, topk_k=w.topk, W=w.W)
+    if (w.t + 1) % w.m == 0:
+        i = (w.t + 1) // w.m - 1
+        assert_close(kv_gpu[i], oracle.bf16_to_f64(kv_o[i]), "emitted entry b=%d" % b)
+    V = oracle.visible(w.t, w.m)
+    scores = oracle.index_scores(bits(x["qI"][b, 0]), bits(x["wI"][b, 0]), bits(x["kI"][b])[:V])
+    check_topk(idx, scores, w.topk, "b=%d" % b)
+    assert_close(out, out_o, "out b=%d" % b)
+    np.testing.assert_allclose(lse, lse_o, rtol=1e-3, atol=1e-3)
+
+
+@pytest.mark.parametrize("cfg,samples", [(0, [0]), (2, [0, 41, 63]), (3, [3])])
+def test_layer_decode(csa, cfg, samples):
+    w = syn.WORKLOADS[cfg]
+    x = syn.decode_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=w.topk)
+    kv = x["kv"].clone()
+    idx, out, lse = run_decode(csa, p, w, x, kv)
+    for b in samples:
+        check_decode_seq(w, x, b, bits(x["kv"][b]), kv[b].float().cpu().numpy(), idx[b], out[b], lse[b])
+
+
+def test_layer_decode_v4flash_cache_from_the_compressor(csa):
+    """Batch 32 x 8192 tokens: the cache is built by the bulk compressor over
+    the whole context, then one decode step at t = 8191 re-emits the last
+    entry from the staging ring."""
+    w = syn.WORKLOADS[1]
+    T = w.t + 1
+    rows = syn.compressor_rows(1, w.B, T, device=DEV)
+    x = syn.decode_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=w.topk)
+    kv = torch.zeros(w.B, w.n_cap, 512, dtype=torch.bfloat16, device=DEV)
+    csa.csa_compress(p, w.B, w.n_cap, 0, rows["Ca"], rows["Za"], rows["Cb"], rows["Zb"], None, None, x["Ba"], x["Bb"],
+                     x["rms_w"], kv, w.n_cap * 512)
+    for k in ("Ca", "Za", "Cb", "Zb"):  # the ring holds the last 2m tokens' rows
+        u = torch.arange(T - 2 * w.m, T, device=DEV)
+        x["ring_" + k] = torch.empty_like(x["ring_" + k])
+        x["ring_" + k][:, u % (2 * w.m)] = rows[k][:, u]
+    idx, out, lse = run_decode(csa, p, w, x, kv)
+    for b in (0, 17):
+        kv_o = oracle.compress(0, w.n_cap, bits(rows["Ca"][b]), bits(rows["Za"][b]), bits(rows["Cb"][b]),
+                               bits(rows["Zb"][b]), None, None, bits(x["Ba"]), bits(x["Bb"]), bits(x["rms_w"]))
+        kv_g = kv[b].float().cpu().numpy()
+        assert_close(kv_g, kv_o, "bulk cache b=%d" % b)
+        check_decode_seq(w, x, b, oracle.f64_to_bf16_bits(kv_o), kv_g, idx[b], out[b], lse[b])
+
+
+def run_prefill(csa, p, w, x):
+    B, Q = w.B, w.Q
+    g = x
+    kv = x["kv"].clone()
+    idx = torch.empty(B, Q, p.topk, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, x["n_cap"])
+    prev = w.pos0 > 0
+    csa.csa_layer_prefill(p, B, Q, w.pos0, g["Ca"], g["Za"], g["Cb"], g["Zb"], g["Cb_prev"] if prev else None,
+                          g["Zb_prev"] if prev else None, g["Ba"], g["Bb"], g["rms_w"], kv, x["n_cap"], g["kI"],
+                          g["qI"], g["wI"], g["q"], g["swa"], g["sink"], idx, out, lse, ws)
+    st = csa.csa_check_status()
+    assert st == 0, csa.csa_status_string(st)
+    return kv, idx.cpu().numpy(), out, lse.cpu().numpy()
+
+
+def check_prefill(w, x, kv_gpu, idx, out, lse, b, queries):
+    m, W, Q, pos0 = w.m, w.W, w.Q, w.pos0
+    e0 = pos0 // m
+    n_new = (pos0 + Q) // m - e0
+    prev = pos0 > 0
+    new = oracle.compress(e0, n_new, bits(x["Ca"][b])[: m * n_new], bits(x["Za"][b])[: m * n_new],
+                          bits(x["Cb"][b])[: m * n_new], bits(x["Zb"][b])[: m * n_new],
+                          bits(x["Cb_prev"][b]) if prev else None, bits(x["Zb_prev"][b]) if prev else None,
+                          bits(x["Ba"]), bits(x["Bb"]), bits(x["rms_w"]), m=m)
+    kv_g = kv_gpu[b].float().cpu().numpy()
+    assert_close(kv_g[e0:e0 + n_new], new, "prefill entries b=%d" % b)
+    kv_o = bits(x["kv"][b]).copy()
+    kv_o[e0:e0 + n_new] = oracle.f64_to_bf16_bits(new)
+    lin = bits(x["swa"][b])
+    kI = bits(x["kI"][b])
+    for j in queries:
+        t = pos0 + j
+        V = oracle.visible(t, m)
+        scores = oracle.index_scores(bits(x["qI"][b, j]), bits(x["wI"][b, j]), kI[:V])
+        check_topk(idx[b, j], scores, w.topk, "q=%d" % j)
+        sel = oracle.topk(scores, w.topk)
+        o, l = oracle.attend_query(t, bits(x["q"][b, j]), sel, kv_o, lambda u: lin[u - (pos0 - (W - 1))],
+                                   bits(x["sink"]), W=W)
+        assert_close(out[b, j].float().cpu().numpy(), o, "prefill out q=%d" % j)
+        np.testing.assert_allclose(lse[b, j], l, rtol=1e-3, atol=1e-3)
+
+
+@pytest.mark.parametrize("B,Q,pos0,k", [(2, 64, 512, 64), (1, 70, 0, 16), (1, 45, 8, 32)])
+def test_layer_prefill_small(csa, B, Q, pos0, k):
+    """Every query checked; includes a chunk at position 0 (no previous block)
+    and ragged chunks whose trailing partial block yields no entry."""
+    w = syn.Workload("prefill-small", 50 + Q, "prefill", B=B, t=pos0 + Q - 1, topk=k, n_cap=0, Q=Q, pos0=pos0)
+    x = syn.prefill_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=k)
+    kv, idx, out, lse = run_prefill(csa, p, w, x)
+    for b in range(B):
+        check_prefill(w, x, kv, idx, out, lse, b, range(Q))
+
+
+def test_layer_prefill_chunk_of_4096_at_61440(csa):
+    """The chunked-prefill configuration at full size; queries sampled: the
+    first and last 8 and every 256th."""
+    w = syn.WORKLOADS[4]
+    x = syn.prefill_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=w.topk)
+    kv, idx, out, lse = run_prefill(csa, p, w, x)
+    qs = sorted(set(list(range(8)) + list(range(w.Q - 8, w.Q)) + list(range(0, w.Q, 256))))
+    check_prefill(w, x, kv, idx, out, lse, 0, qs)
