@@ -60,6 +60,8 @@ _lib.csa_workspace_size.argtypes = [_i32, _P, _i32, _i32, _i64]
 _lib.csa_workspace_size.restype = _sz
 _lib.csa_compress.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64, _vp]
 _lib.csa_index_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
+_lib.csa_index_topk_static.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]
+_lib.csa_index_topk_static.restype = ctypes.c_int
 _lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]
 _lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
@@ -128,6 +130,20 @@ def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, w
     _check(_lib.csa_index_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
                                _ptr(idx_out), _ptr(score_out), _ptr(ws), 0 if ws is None else ws.numel(),
                                _stream(stream)), "csa_index_topk")
+
+
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def csa_index_topk_static(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, stream=None):
+    """csa_index_topk with its scratch in libcsa's fixed 16 MiB device array
+    instead of a caller-provided workspace, for callers that cannot allocate
+    device memory at the call (their own pool holds the GPU's memory, or they
+    must not risk cudaMalloc blocking the host and synchronising the device).
+    The first call on a device should come before any stream capture; calls
+    that can overlap on the GPU race on the shared array."""
+    _check(_lib.csa_index_topk_static(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
+                                      _ptr(idx_out), _ptr(score_out), _stream(stream)), "csa_index_topk_static")
 
 
 def csa_sparse_attn(params, B, Q, q_pos, q, kv_comp, n_cap, idx, swa, swa_mode, swa_len, swa_pos0, sink, out,

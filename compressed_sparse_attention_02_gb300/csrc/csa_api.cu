@@ -225,6 +225,25 @@ csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new,
 
 bool n_cap_ok(int64_t n_cap) { return n_cap >= 1 && n_cap <= (int64_t(1) << 30); }
 
+// Scratch of csa_index_topk_static: a fixed device array, so that callers
+// who cannot allocate device memory can still run the indexer.  Host code
+// sees only a stand-in for this symbol; its device address is looked up once
+// per device (with that device current) and passed to the kernels.
+__device__ __align__(256) unsigned char g_static_scratch[CSA_STATIC_SCRATCH_BYTES];
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
+void* static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_static_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_static_scratch_ptr[dev] = p;
+  }
+  return g_static_scratch_ptr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -292,6 +311,24 @@ csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     return CSA_ERR_INVALID_ARG;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
                         static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_index_topk_static(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos,
+                                 const uint8_t* qI, const uint16_t* wI, const uint8_t* kI, int64_t n_cap,
+                                 int32_t* idx_out, float* score_out, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || Q == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(idx_out) || !ok_opt(score_out))
+    return CSA_ERR_INVALID_ARG;
+  IndexWs w;
+  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (w.total > CSA_STATIC_SCRATCH_BYTES) return CSA_ERR_WORKSPACE;  // beyond the fixed array
+  void* scratch = static_scratch();
+  if (!scratch) return CSA_ERR_CUDA;
+  return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, scratch,
+                        CSA_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
 }
 
 csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint16_t* q,

@@ -152,6 +152,34 @@ csa_status csa_index_topk(const csa_params *p, int32_t B, int32_t Q,
                           size_t workspace_bytes, void *stream);
 
 /*
+ * csa_index_topk_static — csa_index_topk without a caller-provided workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory where they call the indexer: for example a
+ * serving process whose own pool allocator has reserved the GPU's memory up
+ * front (a cudaMalloc would fail or take memory the pool counts on), or a
+ * latency-critical loop that must not call cudaMalloc because it can block
+ * the host and synchronise the device.
+ *
+ * Arguments, results and errors are those of csa_index_topk.  The scratch is
+ * one fixed device array inside libcsa of CSA_STATIC_SCRATCH_BYTES (16 MiB)
+ * that every GPU that loads the library holds until the process exits; a call
+ * whose scratch need, csa_workspace_size(CSA_OP_INDEX_TOPK, ...), exceeds it
+ * returns CSA_ERR_WORKSPACE without launching anything.  The call allocates
+ * nothing.  The first call on each device (with that device current) looks
+ * up the array's device address; make that first call before any stream
+ * capture.  Every call uses the same array, which keeps the previous call's
+ * contents (nothing in it needs to start at zero): calls that can run on the
+ * GPU at the same time (other streams, other host threads) race on it, so
+ * the caller must serialise them.
+ */
+#define CSA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+csa_status csa_index_topk_static(const csa_params *p, int32_t B, int32_t Q,
+                                 const int32_t *q_pos, const uint8_t *qI,
+                                 const uint16_t *wI, const uint8_t *kI,
+                                 int64_t n_cap, int32_t *idx_out,
+                                 float *score_out, void *stream);
+
+/*
  * csa_sparse_attn — shared-KV MQA over [SWA rows || selected entries || sink].
  * [hca_csa] "设计：近处看原文，远处看摘要", the o_{t,i} equation and the bullet
  * on attn_sink; gather semantics [KV 压缩] §9.6; window [KV 压缩] §9.5.
