@@ -27,6 +27,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "CSA-layer decode queries/s & indexer HBM GB/s, attn TC util vs GB300 peak"
+QSETS = 4
 UNIT = "queries/s"
 
 
@@ -130,6 +131,12 @@ def run_ours(args, rank, world, local_rank):
     # each rank's batch is its own slice of sequences (seeded per sequence)
     x = syn.decode_inputs(syn.Workload(w.name, w.config + 100 * rank, w.kind, B=B, t=w.t, topk=w.topk,
                                        n_cap=w.n_cap, hadamard_kI=w.hadamard_kI), device=dev)
+    # Consecutive steps use different queries (QSETS sets, rotated), so each
+    # step selects and gathers different cache rows: the selected rows of one
+    # step are not left in L2 for the next.
+    qsets = [syn.indexer_query(w.config + 100 * rank + 1000 * r, B, 1, device=dev) for r in range(QSETS)]
+    for r, qs in enumerate(qsets):
+        qs["q"] = syn.main_query(w.config + 100 * rank + 1000 * r, B, 1, device=dev)
     p = csa.csa_default_params(topk=w.topk)
     kv = x["kv"]
     idx = torch.empty(B, w.topk, dtype=torch.int32, device=dev)
@@ -137,10 +144,13 @@ def run_ours(args, rank, world, local_rank):
     lse = torch.empty(B, 64, dtype=torch.float32, device=dev)
     ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, w.n_cap, device=dev)
     stream = torch.cuda.current_stream()
+    counter = [0]
 
     def step():
+        qs = qsets[counter[0] % QSETS]
+        counter[0] += 1
         csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"],
-                             x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], x["qI"], x["wI"], x["q"], x["swa"],
+                             x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], qs["qI"], qs["wI"], qs["q"], x["swa"],
                              x["sink"], idx, out, lse, ws)
 
     def barrier():
@@ -187,15 +197,16 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) inputs in the pages' shapes; no trained weights)",
         "config": {"workload": w.name, "batch_per_gpu": B, "context_tokens": w.t + 1,
                    "compressed_entries": w.n_cap, "topk": w.topk, "swa_window": w.W, "m": w.m,
-                   "l2": "inputs larger than L2 (K^I %d MiB + KV cache %d MiB per GPU)"
-                         % (B * w.n_cap * 128 >> 20, B * w.n_cap * 1024 >> 20)},
+                   "l2": "inputs larger than L2 (K^I %d MiB + KV cache %d MiB per GPU); queries rotate over "
+                         "%d sets so consecutive steps gather different rows"
+                         % (B * w.n_cap * 128 >> 20, B * w.n_cap * 1024 >> 20, QSETS)},
         "gpu_launches": launches,
     }
     if clocks:
         result["clocks"] = clocks.summary()
     if rank == 0 and not args.no_extras:
         result.update(stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args))
-        result["e2e"] = end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args)
+        result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
 
@@ -254,7 +265,7 @@ def _traffic_from_profile():
         return None
 
 
-def end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args):
+def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args):
     """Same metric through the same C-ABI call with the step's inputs in
     pinned host memory: each step copies them to the device (queries, indexer
     queries and weights, positions, the compressor staging rows, the new
@@ -262,6 +273,7 @@ def end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args):
     outputs (attention output and selection)."""
     names = ["q", "qI", "wI", "q_pos", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb"]
     host = {k: x[k].cpu().pin_memory() for k in names}
+    hsets = [{k: qs[k].cpu().pin_memory() for k in ("q", "qI", "wI")} for qs in qsets]
     slot = w.t % w.W
     entry = (w.t + 1) // w.m - 1
     host["swa_row"] = x["swa"][:, slot].cpu().pin_memory()
@@ -272,9 +284,13 @@ def end_to_end(csa, torch, w, x, p, B, kv, out, idx, lse, ws, stream, args):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + idx_h.numel() * idx_h.element_size()
 
+    counter = [0]
+
     def step():
+        hs = hsets[counter[0] % len(hsets)]
+        counter[0] += 1
         for k in names:
-            dev[k].copy_(host[k], non_blocking=True)
+            dev[k].copy_(hs.get(k, host[k]), non_blocking=True)
         x["swa"][:, slot].copy_(host["swa_row"], non_blocking=True)
         x["kI"][:, entry].copy_(host["kI_row"], non_blocking=True)
         csa.csa_layer_decode(p, B, dev["q_pos"], dev["ring_Ca"], dev["ring_Za"], dev["ring_Cb"], dev["ring_Zb"],

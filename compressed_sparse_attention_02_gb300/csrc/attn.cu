@@ -18,6 +18,14 @@
 // The reference maximum only moves when a tile exceeds it by more than 2^8,
 // so O^T is rarely rescaled; the final division uses the same reference, so
 // the result does not depend on when it moved.
+//
+// Decode (few queries) runs NH = 32 heads per CTA, two CTAs per query, so
+// twice as many SMs share the per-query work; prefill runs all 64 heads per
+// CTA (its rows then cross L2 once per query).  At start every CTA asks L2 to
+// prefetch all of its query's rows (cp.async.bulk.prefetch.L2), so the HBM
+// reads of the whole batch are in flight at once and the tile gathers that
+// follow mostly hit L2.  With NH = 32 the P tile keeps its 64-head layout with
+// the upper 32 columns zero, so both MMAs use the same operand layouts.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -26,34 +34,41 @@
 namespace csa {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: two per TMEM lane quadrant
 constexpr int kTileRows = 128;
-constexpr uint32_t kQBytes = kHeads * kDim * 2;           // 64 KiB: [8 blocks][64 heads][128 B]
 constexpr uint32_t kKVBytes = kTileRows * kDim * 2;       // 128 KiB: [8 blocks][128 rows][128 B]
 constexpr uint32_t kPBytes = kTileRows * kHeads * 2;      // 16 KiB: [128 rows][64 heads]
-constexpr uint32_t kQBlock = kHeads * 128;                // 8 KiB per 64-channel block of Q
 constexpr uint32_t kKVBlock = kTileRows * 128;            // 16 KiB per 64-channel block of KV
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 64;                            // O^T columns start here
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleSlack = 8.0f;                     // log2 units
 
-constexpr size_t kSmem = 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 +
-                         4 * kHeads * 4 + 4 * kHeads * 4 + 64;
+template <int NH>
+constexpr size_t smem_bytes() {
+  return 1024 + NH * kDim * 2 + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
+         4 * kHeads * 4 + 64;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Reduce-scatter of 64 per-thread values across a warp: afterwards lane l
-// holds the reduction over all 32 lanes of values 2l and 2l+1.
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], float& out0, float& out1) {
+// Reduce-scatter of N (16 or 32) per-thread values across a warp: afterwards
+// lane l holds in v[0] the reduction over all 32 lanes of value l >> (5 -
+// log2 N) (lanes that share that index hold the same result).
+template <int N, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N]) {
   const int lane = threadIdx.x & 31;
+  constexpr int kSteps = N == 32 ? 5 : 4;  // log2 N
 #pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int half = 32 >> step;
+  for (int step = 0; step < kSteps; ++step) {
+    const int half = (N / 2) >> step;
     const int mask = 16 >> step;
     const bool upper = (lane & mask) != 0;
 #pragma unroll
@@ -64,29 +79,41 @@ __device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], float& out
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  out0 = v[0];
-  out1 = v[1];
+#pragma unroll
+  for (int mask = 16 >> kSteps; mask > 0; mask >>= 1) {
+    const float recv = __shfl_xor_sync(0xffffffffu, v[0], mask);
+    v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+  }
 }
 
+template <int NH>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+  constexpr int kSplit = kHeads / NH;            // CTAs per query
+  constexpr uint32_t kQBlock = NH * 128;         // bytes of one 64-channel block of Q
+  constexpr int HW = NH / 2;                     // heads per warp (two warps share a TMEM quadrant)
+  constexpr int kShift = HW == 32 ? 0 : 1;       // lane -> head after a reduce-scatter of HW values
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = base;
-  uint8_t* kv_s = q_s + kQBytes;
-  uint8_t* p_s = kv_s + kKVBytes;
+  uint8_t* q_s = base;                                          // [8 blocks][NH heads][128 B]
+  uint8_t* kv_s = q_s + NH * kDim * 2;                          // [8 blocks][128 rows][128 B]
+  uint8_t* p_s = kv_s + kKVBytes;                               // [128 rows][64 heads] bf16
   int32_t* sel_s = reinterpret_cast<int32_t*>(p_s + kPBytes);
   const uint16_t** row_src = reinterpret_cast<const uint16_t**>(sel_s + kMaxTopk);  // [128]
-  float* red_s = reinterpret_cast<float*>(row_src + kTileRows);  // [4 warps][64]
-  float* m_ref = red_s + 4 * kHeads;                           // running reference max (log2 units)
-  float* l_sum = m_ref + kHeads;                               // running denominator
-  float* alpha = l_sum + kHeads;                               // per-tile rescale factor
-  float* fin = alpha + kHeads;                                 // final per-head output scale
+  float* red_s = reinterpret_cast<float*>(row_src + kTileRows);  // [4 row quadrants][NH]
+  float* m_ref = red_s + 4 * kHeads;                             // running reference max (log2 units)
+  float* l_sum = m_ref + kHeads;                                 // running denominator
+  float* alpha = l_sum + kHeads;                                 // per-tile rescale factor
+  float* fin = alpha + kHeads;                                   // final per-head output scale
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(fin + kHeads);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);          // [0] n_sel, [1] rescale, [2] abort
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qi = blockIdx.x, b = blockIdx.y;
+  const int quad = warp & 3;                  // TMEM lane quadrant == 32 tile rows
+  const int hw0 = (warp >> 2) * HW;           // first head (within the CTA) of this warp
+  const int qi = blockIdx.x / kSplit;
+  const int h0 = (blockIdx.x % kSplit) * NH;  // first head of this CTA
+  const int b = blockIdx.y;
   const int64_t row_q = static_cast<int64_t>(b) * a.Q + qi;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + qi;
 
@@ -95,20 +122,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     mbar_init(mma_bar, 1);
     fence_mbar_init();
     flags[1] = 0;
-    flags[2] = 0;
   }
-  if (tid < kHeads) {
+  if (tid < NH) {
     m_ref[tid] = -INFINITY;
     l_sum[tid] = 0.f;
   }
 
-  // Q tile: [8 channel blocks][64 heads][128 B], 128-byte swizzle.
+  // Q tile of this CTA's heads: [8 channel blocks][NH heads][128 B], swizzled.
   {
-    const uint16_t* qg = a.q + row_q * kHeads * kDim;
-    for (int ch = tid; ch < kHeads * kDim / 8; ch += kThreads) {
+    const uint16_t* qg = a.q + (row_q * kHeads + h0) * kDim;
+    for (int ch = tid; ch < NH * kDim / 8; ch += kThreads) {
       const int h = ch >> 6, blk = (ch >> 3) & 7, c = ch & 7;
       cp_async_16(q_s + blk * kQBlock + swz(h, c), qg + h * kDim + blk * 64 + c * 8);
     }
+  }
+  if (NH < 64) {  // the P tile's unused head columns stay zero
+    for (int r = tid; r < kTileRows; r += kThreads)
+#pragma unroll
+      for (int c = NH / 8; c < 8; ++c) *reinterpret_cast<uint4*>(p_s + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
   }
 
   // Compact the selected entries (drop -1, flag out-of-range indices).
@@ -120,16 +151,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     for (int j = lo; j < hi; ++j) {
       const int32_t v = ig[j];
       if (v >= 0 && v < a.n_cap) ++cnt;
-      else if (v != -1) record_error(a.status, kErrIndexRange);
+      else if (v != -1 && h0 == 0) record_error(a.status, kErrIndexRange);
     }
-    // exclusive scan of cnt over the 128 threads
     int x = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, off);
       if (lane >= off) x += y;
     }
-    __shared__ int wtot[4];
+    __shared__ int wtot[kThreads / 32];
     if (lane == 31) wtot[warp] = x;
     __syncthreads();
     int before = x - cnt;
@@ -146,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tlane = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's TMEM quadrant
   const int n_sel = flags[0];
   const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
   const int n_rows = n_swa + n_sel;
@@ -154,29 +185,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   const uint16_t* kv_b = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
   const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
 
-  constexpr uint32_t idesc_s = instr_desc(kTileRows, kHeads, 1, 1, 0, 0);  // bf16, K-major A/B
+  // Address of row j of this query's row set (null: absent / skipped).
+  auto row_at = [&](int j) -> const uint16_t* {
+    if (j < n_swa) {
+      const int64_t u = t - n_swa + 1 + j;  // window position
+      if (a.swa_mode == 0) return a.swa + (static_cast<int64_t>(b) * a.W + u % a.W) * kDim;
+      const int64_t rr = u - swa_pos0;
+      if (rr >= 0 && rr < a.swa_len) return a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
+      return nullptr;
+    }
+    if (j < n_rows) return kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
+    return nullptr;
+  };
+  // Put every row of this query in flight towards L2 now.
+  for (int j = tid; j < n_rows; j += kThreads) {
+    const uint16_t* src = row_at(j);
+    if (src) prefetch_l2(src, kDim * 2);
+  }
+
+  constexpr uint32_t idesc_s = instr_desc(kTileRows, NH, 1, 1, 0, 0);      // bf16, K-major A/B
   constexpr uint32_t idesc_o = instr_desc(kTileRows, kHeads, 1, 1, 1, 1);  // bf16, MN-major A/B
   uint32_t phase = 0;
   bool ok = true;
 
   for (int tile = 0; tile < n_tiles && ok; ++tile) {
     const int r0 = tile * kTileRows;
-    // ---- resolve the tile's 128 row addresses (null: no row / skipped row)
-    {
+    // ---- resolve the tile's 128 row addresses
+    if (tid < kTileRows) {
       const int j = r0 + tid;
-      const uint16_t* src = nullptr;
-      if (j < n_swa) {
-        const int64_t u = t - n_swa + 1 + j;  // window position
-        if (a.swa_mode == 0) {
-          src = a.swa + (static_cast<int64_t>(b) * a.W + u % a.W) * kDim;
-        } else {
-          const int64_t rr = u - swa_pos0;
-          if (rr >= 0 && rr < a.swa_len) src = a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
-          else record_error(a.status, kErrIndexRange);
-        }
-      } else if (j < n_rows) {
-        src = kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
-      }
+      const uint16_t* src = row_at(j);
+      if (!src && j < n_swa && h0 == 0) record_error(a.status, kErrIndexRange);
       row_src[tid] = src;
     }
     __syncthreads();
@@ -212,35 +250,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     phase ^= 1u;
     tc_fence_after();
 
-    // ---- logits of this thread's row, per-head tile max
-    const int r = tid;  // TMEM lane == tile row
+    // ---- logits of this thread's row (its warp's HW heads), per-head tile max
+    const int r = quad * 32 + lane;  // TMEM lane == tile row
     const bool valid = row_src[r] != nullptr;
-    float l[64];
+    float l[HW];
     {
-      uint32_t v0[32], v1[32];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-      tmem_ld32(taddr, v0);
-      tmem_ld32(taddr + 32, v1);
-      tmem_wait_ld();
+      if constexpr (HW == 32) {
+        uint32_t v[32];
+        tmem_ld32(tlane + hw0, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        l[h] = valid ? __uint_as_float(v0[h]) * scale2 : -INFINITY;
-        l[32 + h] = valid ? __uint_as_float(v1[h]) * scale2 : -INFINITY;
+        for (int h = 0; h < 32; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
+      } else {
+        uint32_t v[16];
+        tmem_ld16(tlane + hw0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
       }
     }
     {
-      float tmp[64];
+      float tmp[HW];
 #pragma unroll
-      for (int h = 0; h < 64; ++h) tmp[h] = l[h];
-      float m0, m1;
-      warp_reduce_scatter64<true>(tmp, m0, m1);
-      red_s[warp * kHeads + 2 * lane] = m0;
-      red_s[warp * kHeads + 2 * lane + 1] = m1;
+      for (int h = 0; h < HW; ++h) tmp[h] = l[h];
+      warp_reduce_scatter<HW, true>(tmp);
+      if ((lane & kShift) == 0) red_s[quad * NH + hw0 + (lane >> kShift)] = tmp[0];
     }
     __syncthreads();
-    if (tid < kHeads) {
-      const float tmax = fmaxf(fmaxf(red_s[tid], red_s[kHeads + tid]),
-                               fmaxf(red_s[2 * kHeads + tid], red_s[3 * kHeads + tid]));
+    if (tid < NH) {
+      const float tmax = fmaxf(fmaxf(red_s[tid], red_s[NH + tid]), fmaxf(red_s[2 * NH + tid], red_s[3 * NH + tid]));
       const float mo = m_ref[tid];
       float al = 1.f;
       if (tmax > mo + kRescaleSlack) {  // also taken on the first tile (mo = -inf)
@@ -253,53 +291,58 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     }
     __syncthreads();
 
-    // ---- rescale O^T columns of heads whose reference moved
+    // ---- rescale the O^T columns of this warp's heads when a reference moved
     if (flags[1]) {
 #pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+      for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
+        if constexpr (HW == 32) {
           uint32_t v[32];
-          const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kOCol + blk * 64 + half * 32;
           tmem_ld32(taddr, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[half * 32 + h]);
+          for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
           tmem_st32(taddr, v);
+        } else {
+          uint32_t v[16];
+          tmem_ld16(taddr, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
+          tmem_st16(taddr, v);
         }
+      }
       tmem_wait_st();
     }
 
     // ---- P = 2^(l - m_ref) as bf16 into the swizzled P tile; row sums
     {
-      float pf[64];
-      uint8_t* prow = p_s;
+      float pf[HW];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < HW / 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int h = c * 8 + 2 * i;
-          const float ref0 = m_ref[h] == -INFINITY ? 0.f : m_ref[h];
-          const float ref1 = m_ref[h + 1] == -INFINITY ? 0.f : m_ref[h + 1];
+          const float m0 = m_ref[hw0 + h], m1 = m_ref[hw0 + h + 1];
+          const float ref0 = m0 == -INFINITY ? 0.f : m0;
+          const float ref1 = m1 == -INFINITY ? 0.f : m1;
           const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(l[h] - ref0), exp2f(l[h + 1] - ref1));
           pf[h] = __low2float(pb);
           pf[h + 1] = __high2float(pb);
           w[i] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        *reinterpret_cast<uint4*>(prow + swz(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(p_s + swz(r, hw0 / 8 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      float s0, s1;
-      warp_reduce_scatter64<false>(pf, s0, s1);
+      warp_reduce_scatter<HW, false>(pf);
       __syncthreads();  // everyone is done reading red_s (tile max) and flags
-      red_s[warp * kHeads + 2 * lane] = s0;
-      red_s[warp * kHeads + 2 * lane + 1] = s1;
+      if ((lane & kShift) == 0) red_s[quad * NH + hw0 + (lane >> kShift)] = pf[0];
     }
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
-    if (tid < kHeads) {
-      l_sum[tid] += (red_s[tid] + red_s[kHeads + tid]) + (red_s[2 * kHeads + tid] + red_s[3 * kHeads + tid]);
+    if (tid < NH) {
+      l_sum[tid] += (red_s[tid] + red_s[NH + tid]) + (red_s[2 * NH + tid] + red_s[3 * NH + tid]);
       if (tid == 0) flags[1] = 0;
     }
 
@@ -318,7 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       tc_commit(mma_bar);
     }
     __syncwarp();
-    // block-uniform: every thread waits, all leave together if one gave up
     if (!__syncthreads_and(mbar_wait(mma_bar, phase, a.status))) { ok = false; break; }
     phase ^= 1u;
     tc_fence_after();
@@ -327,40 +369,48 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
 
   // ---- epilogue: out = O^T / (l_sum + 2^(sink*log2e - m_ref))
   __syncthreads();
-  if (tid < kHeads) {
+  if (tid < NH) {
     const float mr = m_ref[tid];
-    const float sk = a.sink[tid] * kLog2e;
+    const float sk = a.sink[h0 + tid] * kLog2e;
     const float M = fmaxf(mr, sk);
     const float keep = mr == -INFINITY ? 0.f : exp2f(mr - M);
     const float den = l_sum[tid] * keep + exp2f(sk - M);
     fin[tid] = M == -INFINITY ? 0.f : keep / den;
-    if (a.lse) a.lse[row_q * kHeads + tid] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
+    if (a.lse) a.lse[row_q * kHeads + h0 + tid] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
   }
   __syncthreads();
-  uint16_t* out_s = reinterpret_cast<uint16_t*>(kv_s);  // [64 heads][512] bf16 staging
+  uint16_t* out_s = reinterpret_cast<uint16_t*>(kv_s);  // [NH heads][512] bf16 staging
   if (ok && n_tiles > 0) {
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk)
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
+    for (int blk = 0; blk < 4; ++blk) {
+      const int chn = blk * 128 + quad * 32 + lane;
+      const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
+      if constexpr (HW == 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + kOCol + blk * 64 + half * 32, v);
+        tmem_ld32(taddr, v);
         tmem_wait_ld();
-        const int chn = blk * 128 + warp * 32 + lane;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          const int head = half * 32 + h;
-          out_s[head * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * fin[head]));
-        }
+        for (int h = 0; h < 32; ++h)
+          out_s[(hw0 + h) * kDim + chn] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * fin[hw0 + h]));
+      } else {
+        uint32_t v[16];
+        tmem_ld16(taddr, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+          out_s[(hw0 + h) * kDim + chn] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * fin[hw0 + h]));
       }
+    }
   } else {
-    for (int e = tid; e < kHeads * kDim; e += kThreads) out_s[e] = 0;
+    for (int e = tid; e < NH * kDim; e += kThreads) out_s[e] = 0;
   }
   __syncthreads();
   {
-    uint4* og = reinterpret_cast<uint4*>(a.out + row_q * kHeads * kDim);
+    uint4* og = reinterpret_cast<uint4*>(a.out + (row_q * kHeads + h0) * kDim);
     const uint4* os = reinterpret_cast<const uint4*>(out_s);
-    for (int e = tid; e < kHeads * kDim / 8; e += kThreads) og[e] = os[e];
+    for (int e = tid; e < NH * kDim / 8; e += kThreads) og[e] = os[e];
   }
 
   // A timed-out wait leaves MMAs possibly in flight: give them a bounded
@@ -374,15 +424,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   }
 }
 
+template <int NH>
+cudaError_t launch_nh(const AttnArgs& a, cudaStream_t stream) {
+  constexpr size_t smem = smem_bytes<NH>();
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  sparse_attn_kernel<NH><<<dim3(a.Q * (kHeads / NH), a.B), kThreads, smem, stream>>>(a);
+  return counted(cudaGetLastError());
+}
+
 }  // namespace
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmem));
-  if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(a.Q, a.B), kThreads, kSmem, stream>>>(a);
-  return counted(cudaGetLastError());
+  // Few queries: split the heads over two CTAs per query to occupy more SMs.
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (static_cast<int64_t>(a.B) * a.Q < sms) return launch_nh<32>(a, stream);
+  return launch_nh<64>(a, stream);
 }
 
 }  // namespace csa

@@ -10,7 +10,9 @@
 // 16-byte load (a warp reads 512 contiguous bytes of a row).  Softmax,
 // normalisation and rotation are fp32; the RoPE angle is formed and reduced
 // modulo 2*pi in fp64 because positions reach 2^20 and an fp32 angle would
-// be off by ~0.1 rad there.
+// be off by ~0.1 rad there.  The 32 inverse frequencies are computed once on
+// the host (fp64) and passed with the arguments, so the device does one
+// multiply, one reduction and one fp32 sincos per channel pair.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -21,8 +23,7 @@ namespace {
 
 constexpr int kThreads = kDim / 8;  // 64
 
-__device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void unpack8(const uint4 u, float (&v)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -94,32 +95,37 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     }
   }
 
-  // Logits (Z + B) of the 2M slots, per channel.
-  float la[M][8], lb[M][8];
+  // Issue every load of the entry first (one memory round trip), then math.
+  uint4 zr[2 * M], cr[2 * M], br[2 * M];
+#pragma unroll
+  for (int r = 0; r < M; ++r) {
+    zr[r] = __ldg(reinterpret_cast<const uint4*>(za[r] + d0));
+    cr[r] = __ldg(reinterpret_cast<const uint4*>(ca[r] + d0));
+    br[r] = __ldg(reinterpret_cast<const uint4*>(a.Ba + r * D + d0));
+    if (has_prev) {
+      zr[M + r] = __ldg(reinterpret_cast<const uint4*>(zb[r] + d0));
+      cr[M + r] = __ldg(reinterpret_cast<const uint4*>(cb[r] + d0));
+      br[M + r] = __ldg(reinterpret_cast<const uint4*>(a.Bb + r * D + d0));
+    }
+  }
+  const uint4 wr = __ldg(reinterpret_cast<const uint4*>(a.rms_w + d0));
+  const int slots = has_prev ? 2 * M : M;  // block i-1 slots are absent for entry 0
+
+  // Logits (Z + B) of the slots, per channel, and their maximum.
+  float lg[2 * M][8];
   float mx[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
 #pragma unroll
-  for (int r = 0; r < M; ++r) {
-    float z[8], bias[8];
-    load8(za[r] + d0, z);
-    load8(a.Ba + r * D + d0, bias);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      la[r][j] = z[j] + bias[j];
-      mx[j] = fmaxf(mx[j], la[r][j]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < M; ++r) {
-    if (has_prev) {
+  for (int r = 0; r < 2 * M; ++r) {
+    if (r < slots) {
       float z[8], bias[8];
-      load8(zb[r] + d0, z);
-      load8(a.Bb + r * D + d0, bias);
+      unpack8(zr[r], z);
+      unpack8(br[r], bias);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        lb[r][j] = z[j] + bias[j];
-        mx[j] = fmaxf(mx[j], lb[r][j]);
+        lg[r][j] = z[j] + bias[j];
+        mx[j] = fmaxf(mx[j], lg[r][j]);
       }
     }
   }
@@ -130,24 +136,13 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
 #pragma unroll
   for (int j = 0; j < 8; ++j) num[j] = den[j] = 0.f;
 #pragma unroll
-  for (int r = 0; r < M; ++r) {
-    float c[8];
-    load8(ca[r] + d0, c);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float w = exp2f((la[r][j] - mx[j]) * kLog2e);
-      num[j] = fmaf(w, c[j], num[j]);
-      den[j] += w;
-    }
-  }
-  if (has_prev) {
-#pragma unroll
-    for (int r = 0; r < M; ++r) {
+  for (int r = 0; r < 2 * M; ++r) {
+    if (r < slots) {
       float c[8];
-      load8(cb[r] + d0, c);
+      unpack8(cr[r], c);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float w = exp2f((lb[r][j] - mx[j]) * kLog2e);
+        const float w = exp2f((lg[r][j] - mx[j]) * kLog2e);
         num[j] = fmaf(w, c[j], num[j]);
         den[j] += w;
       }
@@ -170,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
   const float total = warp_ss[0] + warp_ss[1];
   const float inv = rsqrtf(total / static_cast<float>(D) + a.rms_eps);
   float w[8];
-  load8(a.rms_w + d0, w);
+  unpack8(wr, w);
   float y[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) y[j] = x[j] * inv * w[j];
@@ -179,12 +174,12 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
   if (d0 >= D - kRope) {
     const double pos = static_cast<double>(M) * static_cast<double>(i);
     const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
 #pragma unroll
     for (int pr = 0; pr < 4; ++pr) {
       const int jp = (d0 + 2 * pr - (D - kRope)) / 2;
-      const double freq = pow(a.rope_theta, -2.0 * jp / static_cast<double>(kRope));
-      double phi = pos * freq;
-      phi -= two_pi * rint(phi / two_pi);
+      double phi = pos * a.inv_freq[jp];
+      phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
       float s, c;
       sincosf(static_cast<float>(phi), &s, &c);
       const float u = y[2 * pr], v = y[2 * pr + 1];
@@ -198,8 +193,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
 
 }  // namespace
 
-cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream) {
-  if (a.B <= 0) return cudaSuccess;
+cudaError_t launch_compress(const CompressArgs& args, cudaStream_t stream) {
+  if (args.B <= 0) return cudaSuccess;
+  CompressArgs a = args;
+  for (int j = 0; j < kRope / 2; ++j) a.inv_freq[j] = pow(a.rope_theta, -2.0 * j / static_cast<double>(kRope));
   dim3 grid(a.mode == 0 ? static_cast<unsigned>(a.n_new) : 1u, static_cast<unsigned>(a.B));
   if (grid.x == 0) return cudaSuccess;
   switch (a.m) {

@@ -86,7 +86,7 @@ csa_status check_params(const csa_params* p) {
 }
 
 struct IndexWs {
-  size_t scores_off, cand_key_off, cand_idx_off, total;
+  size_t scores_off, hist_off, cand_key_off, cand_idx_off, total;
   int64_t score_ld;
   int chunk, n_chunks;
 };
@@ -99,6 +99,8 @@ bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
   if (static_cast<int64_t>(w->n_chunks) * k > csa::kTopkMaxItems && w->n_chunks > 1) return false;
   w->scores_off = 0;
   size_t off = round_up(static_cast<size_t>(rows) * w->score_ld * 4, 256);
+  w->hist_off = off;  // per row: counts of the 2048 score-key top digits
+  off = round_up(off + static_cast<size_t>(rows) * 2048 * 4, 256);
   w->cand_key_off = off;
   const size_t cand = w->n_chunks > 1 ? static_cast<size_t>(rows) * w->n_chunks * k * 4 : 0;
   off = round_up(off + cand, 256);
@@ -123,6 +125,9 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   if (!enc || !status) return CSA_ERR_CUDA;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + w.hist_off);
+  const size_t hist_bytes = static_cast<size_t>(B) * Q * 2048 * 4;
+  if (cudaMemsetAsync(hist, 0, hist_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
 
   csa::IndexArgs ia;
   ia.qI = qI;
@@ -136,6 +141,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ia.n_cap = n_cap;
   ia.scores = scores;
   ia.score_ld = w.score_ld;
+  ia.hist = hist;
   ia.status = status;
   csa_status s = cuda_status(csa::launch_index_scores(ia, enc, st));
   if (s != CSA_OK) return s;
@@ -144,6 +150,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   csa::TopkArgs ta;
   ta.scores = scores;
   ta.score_ld = w.score_ld;
+  ta.hist = hist;
   ta.q_pos = q_pos;
   ta.pos_base = pos_base;
   ta.B = B;

@@ -9,17 +9,25 @@
 // epilogue thread then owns one key and reduces its 64 head scores with the
 // head weights and ReLU in registers: no cross-thread reduction.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: q^I once, then a STAGES-deep ring of 16 KiB
-//               K^I tiles (128-byte swizzle), L2 evict-first;
-//   warp 1      TMEM owner and MMA issuer (one thread), double-buffered
-//               accumulators so the epilogue of tile n overlaps MMA n+1;
-//   warps 2..5  epilogue: tcgen05.ld, weighted ReLU sum, coalesced fp32
-//               score stores (only for keys visible to the query).
+// Persistent grid: exactly the CTAs that fit on the GPU at once, each taking
+// an equal contiguous range of the flattened (query group, key tile) space.
+// Warp roles (576 threads):
+//   warp 0      TMA producer: q^I of each query group it meets (two buffers),
+//               and a STAGES-deep ring of 16 KiB K^I tiles (128-byte
+//               swizzle, L2 evict-first);
+//   warp 1      TMEM owner and MMA issuer (one thread) into NBUF TMEM
+//               accumulators, so epilogues of earlier tiles overlap MMAs;
+//   warps 2..17 epilogue, four groups of four warps (one query per tile:
+//               groups take tiles in turn; four queries: a group per query):
+//               tcgen05.ld, weighted ReLU sum (four independent chains),
+//               coalesced fp32 score stores for keys visible to the query,
+//               and the row's histogram of score-key top digits (used by
+//               the top-k to go straight to the digit holding the k-th).
 // Every wait is bounded; a timeout records the error, the roles drain their
 // own in-flight work and the CTA releases TMEM and exits.
 #include <cuda_bf16.h>
 
+#include "keys.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -30,64 +38,99 @@ constexpr int kTileKeys = 128;
 constexpr uint32_t kKeyTileBytes = kTileKeys * kIdxDim;   // 16 KiB
 constexpr uint32_t kQBytes = kIdxHeads * kIdxDim;         // 8 KiB per query
 
+constexpr int kEpiGroups = 4;                // 4 warps per group, one per TMEM lane quadrant
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kIndexThreads = 64 + 32 * kEpiWarps;
+
 template <int QPC>
 struct IndexCfg {
   static constexpr int N = kIdxHeads * QPC;
-  static constexpr int STAGES = QPC == 1 ? 6 : 6;
-  static constexpr uint32_t TMEM_COLS = 2 * N;
-  static constexpr size_t SMEM = 1024 + QPC * kQBytes + STAGES * kKeyTileBytes + QPC * kIdxHeads * 4 +
-                                 (2 * STAGES + 6) * 8 + 16 + QPC * 8 + 16;
+  static constexpr int STAGES = QPC == 1 ? 12 : 8;  // one CTA per SM: 192 / 128 KiB of keys in flight
+  static constexpr int NBUF = QPC == 1 ? 4 : 2;     // TMEM accumulators; tile n uses buffer n % NBUF
+  static constexpr uint32_t TMEM_COLS = NBUF * N;
+  static constexpr size_t SMEM = 1024 + 2 * QPC * kQBytes + STAGES * kKeyTileBytes + kEpiWarps * kIdxHeads * 4 +
+                                 (2 * STAGES + 2 * NBUF + 5) * 8 + 16;
+};
+
+// Work split: the flattened (query group, key tile) space is cut into
+// gridDim.x equal contiguous ranges, one per CTA, with gridDim.x a multiple of
+// the CTAs an SM holds; a range may cross into the next query group, whose
+// q^I is then loaded into the other of two q^I buffers.  Tiles past a group's
+// last visible key are skipped by every role alike.
+struct GroupInfo {
+  int64_t vis[4];   // visible entries of each query of the group
+  int64_t vmax;
+  int b, q0;
 };
 
 template <int QPC>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, int64_t g, int groups_per_seq) {
+  GroupInfo gi;
+  gi.b = static_cast<int>(g / groups_per_seq);
+  gi.q0 = static_cast<int>(g % groups_per_seq) * QPC;
+  gi.vmax = 0;
+#pragma unroll
+  for (int j = 0; j < QPC; ++j) {
+    const int q = gi.q0 + j;
+    int64_t V = 0;
+    if (q < a.Q) {
+      const int64_t t = a.q_pos ? static_cast<int64_t>(__ldg(a.q_pos + static_cast<int64_t>(gi.b) * a.Q + q))
+                                : a.pos_base + q;
+      V = t >= 0 ? (t + 1) / a.m : 0;
+      if (V > a.n_cap) V = a.n_cap;
+    }
+    gi.vis[j] = V;
+    gi.vmax = V > gi.vmax ? V : gi.vmax;
+  }
+  return gi;
+}
+
+// True if a query of the group sits past what the cache holds (V(t) > n_cap).
+template <int QPC>
+__device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const GroupInfo& gi) {
+  bool past = false;
+#pragma unroll
+  for (int j = 0; j < QPC; ++j) {
+    const int q = gi.q0 + j;
+    if (q < a.Q) {
+      const int64_t t = a.q_pos ? static_cast<int64_t>(__ldg(a.q_pos + static_cast<int64_t>(gi.b) * a.Q + q))
+                                : a.pos_base + q;
+      past |= t >= 0 && (t + 1) / a.m > a.n_cap;
+    }
+  }
+  return past;
+}
+
+template <int QPC>
+__global__ void __maxnreg__(112)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                       const IndexArgs a, const int tiles_per_cta) {
+                       const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
   using Cfg = IndexCfg<QPC>;
   constexpr int N = Cfg::N;
   constexpr int STAGES = Cfg::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = base;
-  uint8_t* k_s = q_s + QPC * kQBytes;
-  float* w_s = reinterpret_cast<float*>(k_s + STAGES * kKeyTileBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(w_s + QPC * kIdxHeads);
+  uint8_t* q_s = base;                                   // [2][QPC * 8 KiB]
+  uint8_t* k_s = q_s + 2 * QPC * kQBytes;                // [STAGES][16 KiB]
+  constexpr int NBUF = Cfg::NBUF;
+  float* w_s = reinterpret_cast<float*>(k_s + STAGES * kKeyTileBytes);  // [epilogue warps][64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(w_s + kEpiWarps * kIdxHeads);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* q_full = acc_empty + 2;
-  uint64_t* mma_done = q_full + 1;
+  uint64_t* acc_full = empty + STAGES;   // [NBUF]
+  uint64_t* acc_empty = acc_full + NBUF; // [NBUF]
+  uint64_t* q_full = acc_empty + NBUF;   // [2]
+  uint64_t* q_empty = q_full + 2;     // [2]
+  uint64_t* mma_done = q_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-  int64_t* vis = reinterpret_cast<int64_t*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.z;
-  const int q0 = blockIdx.y * QPC;
-
-  // Visible entries V(t) = floor((t+1)/m) of each query of the group.
-  if (threadIdx.x < QPC) {
-    const int q = q0 + threadIdx.x;
-    int64_t V = 0;
-    if (q < a.Q) {
-      const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[static_cast<int64_t>(b) * a.Q + q]) : a.pos_base + q;
-      V = t >= 0 ? (t + 1) / a.m : 0;
-      if (V > a.n_cap) {
-        if (blockIdx.x == 0) record_error(a.status, kErrIndexRange);
-        V = a.n_cap;
-      }
-    }
-    vis[threadIdx.x] = V;
-  }
-  __syncthreads();
-  int64_t vmax = 0;
-#pragma unroll
-  for (int j = 0; j < QPC; ++j) vmax = vis[j] > vmax ? vis[j] : vmax;
-  const int64_t tile0 = static_cast<int64_t>(blockIdx.x) * tiles_per_cta;
-  const int64_t tiles_needed = (vmax + kTileKeys - 1) / kTileKeys;
-  const int n_my = static_cast<int>(min(static_cast<int64_t>(tiles_per_cta), tiles_needed - tile0));
-  if (n_my <= 0) return;  // uniform: nothing of this group is visible here
+  const int64_t n_groups = static_cast<int64_t>(a.B) * groups_per_seq;
+  const int64_t units = n_groups * tiles_per_group;
+  const int64_t u0 = units * blockIdx.x / gridDim.x;
+  const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+  if (u0 >= u1) return;
 
   if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
   if (threadIdx.x == 0) {
@@ -95,21 +138,17 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < NBUF; ++x) {
       mbar_init(&acc_full[x], 1);
-      mbar_init(&acc_empty[x], 4);
+      // one query per tile: the owning group's 4 warps; else every epilogue warp
+      mbar_init(&acc_empty[x], QPC == 1 ? 4 : kEpiWarps);
     }
-    mbar_init(q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_empty[x], 1);
+    }
     mbar_init(mma_done, 1);
     fence_mbar_init();
-  }
-  if (threadIdx.x >= 64) {
-    for (int e = threadIdx.x - 64; e < QPC * kIdxHeads; e += 128) {
-      const int q = q0 + e / kIdxHeads;
-      const int h = e % kIdxHeads;
-      const uint16_t wb = q < a.Q ? a.wI[(static_cast<int64_t>(b) * a.Q + q) * kIdxHeads + h] : uint16_t(0);
-      w_s[e] = __uint_as_float(static_cast<uint32_t>(wb) << 16);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -122,78 +161,168 @@ __global__ void __launch_bounds__(192, 1)
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_q);
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(q_full, QPC * kQBytes);
-      for (int j = 0; j < QPC; ++j)
-        tma_load_2d(q_s + j * kQBytes, &tm_q, 0,
-                    static_cast<int32_t>((static_cast<int64_t>(b) * a.Q + q0 + j) * kIdxHeads), q_full);
       uint32_t issued = 0, parity = 0;
-      for (int it = 0; it < n_my; ++it) {
+      uint32_t q_uses[2] = {0, 0};
+      int64_t seen_g = -1;
+      bool active = false;
+      GroupInfo gi{};
+      int qb = 1, it = 0;
+      bool ok = true;
+      for (int64_t u = u0; u < u1 && ok; ++u) {
+        const int64_t g = u / tiles_per_group;
+        const int64_t tile = u % tiles_per_group;
+        if (g != seen_g) {
+          gi = group_info<QPC>(a, g, groups_per_seq);
+          seen_g = g;
+          active = gi.vmax > tile * kTileKeys;  // the group has work in this range
+          if (active) {
+            qb ^= 1;
+            if (q_uses[qb] > 0 && !(ok = mbar_wait(&q_empty[qb], (q_uses[qb] - 1) & 1u, a.status))) break;
+            mbar_arrive_expect_tx(&q_full[qb], QPC * kQBytes);
+            for (int j = 0; j < QPC; ++j)
+              tma_load_2d(q_s + (qb * QPC + j) * kQBytes, &tm_q, 0,
+                          static_cast<int32_t>((static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j) * kIdxHeads),
+                          &q_full[qb]);
+            ++q_uses[qb];
+          }
+        }
+        if (!active || tile * kTileKeys >= gi.vmax) continue;
         const int s = it % STAGES;
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, a.status)) break;
+        if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
         mbar_arrive_expect_tx(&full[s], kKeyTileBytes);
-        tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>((tile0 + it) * kTileKeys), b,
-                    &full[s], pol);
+        tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s], pol);
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | ((use & 1u) << s);
+        ++it;
       }
       // Our own copies must have landed before the CTA may exit.
       for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s)) mbar_wait(&full[s], (parity >> s) & 1u, a.status);
-      mbar_wait(q_full, 0, a.status);
+      for (int x = 0; x < 2; ++x)
+        if (q_uses[x]) mbar_wait(&q_full[x], (q_uses[x] - 1) & 1u, a.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = instr_desc(kTileKeys, N, 0, 0, 0, 0);
-      bool ok = mbar_wait(q_full, 0, a.status);
-      const uint32_t qb = smem_u32(q_s);
-      for (int it = 0; ok && it < n_my; ++it) {
+      uint32_t q_uses[2] = {0, 0};
+      int64_t seen_g = -1;
+      bool active = false;
+      GroupInfo gi{};
+      int qb = 1, it = 0;
+      bool ok = true;
+      for (int64_t u = u0; u < u1 && ok; ++u) {
+        const int64_t g = u / tiles_per_group;
+        const int64_t tile = u % tiles_per_group;
+        if (g != seen_g) {
+          gi = group_info<QPC>(a, g, groups_per_seq);
+          seen_g = g;
+          active = gi.vmax > tile * kTileKeys;
+          if (active) {
+            if (q_uses[qb] > 0) tc_commit(&q_empty[qb]);  // previous group's buffer is free once its MMAs end
+            qb ^= 1;
+            if (!(ok = mbar_wait(&q_full[qb], q_uses[qb] & 1u, a.status))) break;
+            ++q_uses[qb];
+          }
+        }
+        if (!active || tile * kTileKeys >= gi.vmax) continue;
         const int s = it % STAGES;
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
-        const int x = it & 1;
-        const uint32_t xuse = static_cast<uint32_t>(it >> 1);
+        const int x = it % NBUF;
+        const uint32_t xuse = static_cast<uint32_t>(it / NBUF);
         if (xuse > 0 && !(ok = mbar_wait(&acc_empty[x], (xuse - 1) & 1u, a.status))) break;
         if (!(ok = mbar_wait(&full[s], use & 1u, a.status))) break;
         tc_fence_after();
         const uint32_t kb = smem_u32(k_s + s * kKeyTileBytes);
+        const uint32_t qbase = smem_u32(q_s + qb * QPC * kQBytes);
 #pragma unroll
         for (int kk = 0; kk < kIdxDim / 32; ++kk) {
           const uint64_t ad = smem_desc(kb + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(qb + kk * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(qbase + kk * 32, 16, 1024, kSwizzle128B);
           mma_f8(tmem + x * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
         tc_commit(&empty[s]);
         tc_commit(&acc_full[x]);
+        ++it;
       }
       tc_commit(mma_done);
     }
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
-    const int sub = warp & 3;  // TMEM sub-partition this warp may access
+    // Four groups of 4 warps; in a group, warp w reads TMEM lane quadrant
+    // w % 4 (keys 32*(w%4) .. +31 of the tile).  With one query per tile the
+    // groups take tiles in turn; with four, every group takes every tile and
+    // scores its own query.
+    const int ew = warp - 2;
+    const int grp = ew >> 2;
+    const int sub = warp & 3;
     const int row = sub * 32 + lane;
-    for (int it = 0; it < n_my; ++it) {
-      const int x = it & 1;
-      const uint32_t xuse = static_cast<uint32_t>(it >> 1);
+    constexpr int kMyQ = QPC == 1 ? 1 : 1;  // queries scored per tile by one group
+    const int jq = QPC == 1 ? 0 : grp;       // the query this group scores
+    float4* w_mine = reinterpret_cast<float4*>(w_s + ew * kIdxHeads);  // this warp's copy of the head weights
+    int64_t seen_g = -1;
+    bool active = false;
+    GroupInfo gi{};
+    int it = 0;
+    for (int64_t u = u0; u < u1; ++u) {
+      const int64_t g = u / tiles_per_group;
+      const int64_t tile = u % tiles_per_group;
+      if (g != seen_g) {
+        gi = group_info<QPC>(a, g, groups_per_seq);
+        seen_g = g;
+        active = gi.vmax > tile * kTileKeys;
+        if (active) {
+          __syncwarp();  // the warp is done with the previous group's weights
+          const int q = gi.q0 + jq;
+          float* wf = reinterpret_cast<float*>(w_mine);
+          for (int e = lane; e < kIdxHeads; e += 32) {
+            const uint16_t wb = q < a.Q ? a.wI[(static_cast<int64_t>(gi.b) * a.Q + q) * kIdxHeads + e] : uint16_t(0);
+            wf[e] = __uint_as_float(static_cast<uint32_t>(wb) << 16);
+          }
+          __syncwarp();
+        }
+      }
+      if (!active || tile * kTileKeys >= gi.vmax) continue;
+      if (tile == 0 && warp == 2 && lane == 0 && group_past_cache<QPC>(a, gi)) record_error(a.status, kErrIndexRange);
+      const int my_it = it++;
+      if (QPC == 1 && (my_it & (kEpiGroups - 1)) != grp) continue;  // another group's tile
+      const int x = my_it % NBUF;
+      const uint32_t xuse = static_cast<uint32_t>(my_it / NBUF);
       // every lane waits; the warp leaves together if any lane gave up
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[x], xuse & 1u, a.status))) break;
       tc_fence_after();
-      const int64_t s_idx = (tile0 + it) * kTileKeys + row;
+      const int64_t s_idx = tile * kTileKeys + row;
 #pragma unroll
-      for (int j = 0; j < QPC; ++j) {
-        uint32_t r0[32], r1[32];
+      for (int jj = 0; jj < kMyQ; ++jj) {
+        const int j = jq;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(sub * 32) << 16) + x * N + j * kIdxHeads;
-        tmem_ld32(taddr, r0);
-        tmem_ld32(taddr + 32, r1);
+        uint32_t r[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16 * c, r[c]);
         tmem_wait_ld();
-        const float* w = w_s + j * kIdxHeads;
-        float acc = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-        for (int h = 0; h < 32; ++h) acc = fmaf(w[h], fmaxf(__uint_as_float(r0[h]), 0.f), acc);
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) acc = fmaf(w[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), acc);
-        if (s_idx < vis[j]) a.scores[(static_cast<int64_t>(b) * a.Q + q0 + j) * a.score_ld + s_idx] = acc;
+          for (int v = 0; v < 4; ++v) {
+            const float4 w4 = w_mine[c * 4 + v];
+            const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              acc[e] = fmaf(wv[e], fmaxf(__uint_as_float(r[c][4 * v + e]), 0.f), acc[e]);
+          }
+        }
+        const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        const bool valid = s_idx < gi.vis[j];
+        const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
+        if (valid) a.scores[row_off * a.score_ld + s_idx] = score;
+        if (a.hist) {  // first-digit histogram of the row, one atomic per distinct digit per warp
+          const int bin = valid ? static_cast<int>(score_key(score) >> kKeyBinShift) : -1;
+          const unsigned peers = __match_any_sync(0xffffffffu, bin);
+          if (valid && lane == __ffs(peers) - 1) atomicAdd(a.hist + row_off * kKeyBins + bin, __popc(peers));
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -240,27 +369,21 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   using Cfg = IndexCfg<QPC>;
   CUtensorMap tm_k, tm_q;
   if (!encode_maps(a, encode, QPC, &tm_k, &tm_q)) return cudaErrorInvalidValue;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::SMEM));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::SMEM));
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t tiles_per_seq = (a.n_cap + kTileKeys - 1) / kTileKeys;
-  const int64_t groups = (a.Q + QPC - 1) / QPC;
-  // Enough CTAs to cover every SM several times, with at least 4 tiles each
-  // so the pipeline has room to run.
-  const int64_t target_ctas = 4LL * sms;
-  int64_t per_cta = (tiles_per_seq * groups * a.B + target_ctas - 1) / target_ctas;
-  if (per_cta < 4) per_cta = 4;
-  if (per_cta > tiles_per_seq) per_cta = tiles_per_seq;
-  const int64_t chunks = (tiles_per_seq + per_cta - 1) / per_cta;
-  dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(groups), static_cast<unsigned>(a.B));
-  index_score_kernel<QPC><<<grid, 192, Cfg::SMEM, stream>>>(tm_k, tm_q, a, static_cast<int>(per_cta));
+  const int per_sm = 1;  // the ring fills most of shared memory
+  const int64_t tiles_per_group = (a.n_cap + kTileKeys - 1) / kTileKeys;
+  const int64_t groups_per_seq = (a.Q + QPC - 1) / QPC;
+  const int64_t units = tiles_per_group * groups_per_seq * a.B;
+  // One wave of CTAs that all stay resident; each takes an equal range.
+  int64_t ctas = static_cast<int64_t>(sms) * per_sm;
+  if (ctas > units) ctas = units;
+  index_score_kernel<QPC><<<static_cast<unsigned>(ctas), kIndexThreads, Cfg::SMEM, stream>>>(
+      tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
   return counted(cudaGetLastError());
 }
 

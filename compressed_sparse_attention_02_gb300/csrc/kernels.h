@@ -42,6 +42,7 @@ struct CompressArgs {
   double rope_theta;
   float rms_eps;
   unsigned* status;
+  double inv_freq[kRope / 2];  // theta^(-2j/R), filled by launch_compress
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
 
@@ -56,6 +57,7 @@ struct IndexArgs {
   int64_t n_cap;
   float* scores;            // [B*Q][score_ld]
   int64_t score_ld;
+  uint32_t* hist;           // [B*Q][2048] key top-digit counts (zeroed by the caller) or null
   unsigned* status;
 };
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
@@ -65,6 +67,7 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
 struct TopkArgs {
   const float* scores;
   int64_t score_ld;
+  const uint32_t* hist;     // [B*Q][2048] from the indexer, or null
   const int32_t* q_pos;
   int64_t pos_base;
   int B, Q, m, k;
