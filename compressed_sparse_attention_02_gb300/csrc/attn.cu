@@ -436,7 +436,8 @@ cudaError_t launch_nh(const AttnArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
+cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
+  (void)encode;  // rows are gathered with cp.async; no tensor map is needed
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
   // Few queries: split the heads over two CTAs per query to occupy more SMs.
   int dev = 0, sms = 148;

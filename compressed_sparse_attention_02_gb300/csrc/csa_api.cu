@@ -173,7 +173,8 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
                     int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
                     const float* sink, uint16_t* out, float* lse, cudaStream_t st) {
   unsigned* status = status_ptr();
-  if (!status) return CSA_ERR_CUDA;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!status || !enc) return CSA_ERR_CUDA;
   csa::AttnArgs aa;
   aa.q_pos = q_pos;
   aa.pos_base = pos_base;
@@ -195,7 +196,7 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.Q = Q;
   aa.sm_scale = p->sm_scale;
   aa.status = status;
-  return cuda_status(csa::launch_sparse_attn(aa, st));
+  return cuda_status(csa::launch_sparse_attn(aa, enc, st));
 }
 
 csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,

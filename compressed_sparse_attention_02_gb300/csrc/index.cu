@@ -102,7 +102,7 @@ __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const Group
 }
 
 template <int QPC>
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kIndexThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
   using Cfg = IndexCfg<QPC>;
@@ -168,9 +168,12 @@ __global__ void __maxnreg__(112)
       GroupInfo gi{};
       int qb = 1, it = 0;
       bool ok = true;
+      int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
       for (int64_t u = u0; u < u1 && ok; ++u) {
-        const int64_t g = u / tiles_per_group;
-        const int64_t tile = u % tiles_per_group;
+        if (++tile == tiles_per_group) {  // advance (group, tile) without dividing
+          tile = 0;
+          ++g;
+        }
         if (g != seen_g) {
           gi = group_info<QPC>(a, g, groups_per_seq);
           seen_g = g;
@@ -212,9 +215,12 @@ __global__ void __maxnreg__(112)
       GroupInfo gi{};
       int qb = 1, it = 0;
       bool ok = true;
+      int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
       for (int64_t u = u0; u < u1 && ok; ++u) {
-        const int64_t g = u / tiles_per_group;
-        const int64_t tile = u % tiles_per_group;
+        if (++tile == tiles_per_group) {  // advance (group, tile) without dividing
+          tile = 0;
+          ++g;
+        }
         if (g != seen_g) {
           gi = group_info<QPC>(a, g, groups_per_seq);
           seen_g = g;
@@ -266,9 +272,12 @@ __global__ void __maxnreg__(112)
     bool active = false;
     GroupInfo gi{};
     int it = 0;
+    int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
     for (int64_t u = u0; u < u1; ++u) {
-      const int64_t g = u / tiles_per_group;
-      const int64_t tile = u % tiles_per_group;
+      if (++tile == tiles_per_group) {
+        tile = 0;
+        ++g;
+      }
       if (g != seen_g) {
         gi = group_info<QPC>(a, g, groups_per_seq);
         seen_g = g;
@@ -298,20 +307,23 @@ __global__ void __maxnreg__(112)
       for (int jj = 0; jj < kMyQ; ++jj) {
         const int j = jq;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(sub * 32) << 16) + x * N + j * kIdxHeads;
-        uint32_t r[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16 * c, r[c]);
-        tmem_wait_ld();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int half = 0; half < 2; ++half) {  // 32 heads at a time keeps registers low
+          uint32_t r[2][16];
+          tmem_ld16(taddr + 32 * half, r[0]);
+          tmem_ld16(taddr + 32 * half + 16, r[1]);
+          tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float4 w4 = w_mine[c * 4 + v];
-            const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              acc[e] = fmaf(wv[e], fmaxf(__uint_as_float(r[c][4 * v + e]), 0.f), acc[e]);
+            for (int v = 0; v < 4; ++v) {
+              const float4 w4 = w_mine[half * 8 + c * 4 + v];
+              const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                acc[e] = fmaf(wv[e], fmaxf(__uint_as_float(r[c][4 * v + e]), 0.f), acc[e]);
+            }
           }
         }
         const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);

@@ -105,6 +105,6 @@ struct AttnArgs {
   float sm_scale;
   unsigned* status;
 };
-cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream);
 
 }  // namespace csa
