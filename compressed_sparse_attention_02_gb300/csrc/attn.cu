@@ -5,16 +5,18 @@
 // 预算检索" §9.5–9.6; flash-style running max / running sum with a fused sink
 // ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §19.3).
 //
-// One CTA (128 threads) per query.  The 64 heads share every K=V row, so both
-// products run with the gathered rows on the MMA's M side:
+// One CTA of 8 warps per query (or per half of the heads, below).  The 64
+// heads share every K=V row, so both products run with the gathered rows on
+// the MMA's M side:
 //   S^T[row, head]  = KV_tile[128 x 512] . Q^T[512 x 64]   (K-major A and B)
 //   O^T[ch, head]  += V^T[512 x 128] . P^T[128 x 64]       (MN-major A and B)
 // The same 128-byte-swizzled KV tile in shared memory serves as the K-major A
 // operand of the first product and the MN-major A operand of the second.  S^T
 // (64 TMEM columns) and O^T (4 x 64 columns, one per 128-channel block) live in
-// TMEM.  Thread r owns tile row r: it reads its 64 head logits with one
-// tcgen05.ld, and per-head maxima and sums over rows use a warp
-// reduce-scatter (62 shuffles) plus a 4-warp combine in shared memory.
+// TMEM.  Two warps share each TMEM lane quadrant (32 tile rows) and split the
+// CTA's heads between them: a thread owns one tile row and half the heads,
+// reads their logits with one tcgen05.ld, and per-head maxima and sums over
+// rows use a warp reduce-scatter plus a 4-quadrant combine in shared memory.
 // The reference maximum only moves when a tile exceeds it by more than 2^8,
 // so O^T is rarely rescaled; the final division uses the same reference, so
 // the result does not depend on when it moved.

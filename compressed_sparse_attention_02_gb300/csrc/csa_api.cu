@@ -86,26 +86,38 @@ csa_status check_params(const csa_params* p) {
 }
 
 struct IndexWs {
-  size_t scores_off, hist_off, cand_key_off, cand_idx_off, total;
-  int64_t score_ld;
-  int chunk, n_chunks;
+  size_t scores_off, hist_off, count_off, done_off, bits_off, ties_off, cand_key_off, cand_idx_off, total;
+  size_t zero_bytes;  // hist, candidate counts and row counters, cleared before each call
+  int64_t score_ld, bits_ld;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Scratch of the indexer and top-k: scores [rows][score_ld] fp32; per row the
+// counts of the 2048 score-key first digits, the crossing-digit candidate
+// count and the count of CTAs done with the row (contiguous, so one memset
+// clears them); the two position bitmaps; the candidate keys and positions.
 bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
+  (void)k;
+  if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
   w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 4));
-  csa::topk_chunking(rows, n_cap, k, &w->chunk, &w->n_chunks);
-  if (static_cast<int64_t>(w->n_chunks) * k > csa::kTopkMaxItems && w->n_chunks > 1) return false;
+  w->bits_ld = csa::topk_bits_ld(n_cap);
+  const size_t R = static_cast<size_t>(rows);
   w->scores_off = 0;
-  size_t off = round_up(static_cast<size_t>(rows) * w->score_ld * 4, 256);
-  w->hist_off = off;  // per row: counts of the 2048 score-key top digits
-  off = round_up(off + static_cast<size_t>(rows) * 2048 * 4, 256);
+  size_t off = round_up(R * w->score_ld * 4, 256);
+  w->hist_off = off;
+  w->count_off = off + R * 2048 * 4;
+  w->done_off = w->count_off + R * 4;
+  w->zero_bytes = R * 2048 * 4 + R * 8;
+  off = round_up(off + w->zero_bytes, 256);
+  w->bits_off = off;
+  off = round_up(off + R * w->bits_ld * 4, 256);
+  w->ties_off = off;
+  off = round_up(off + R * w->bits_ld * 4, 256);
   w->cand_key_off = off;
-  const size_t cand = w->n_chunks > 1 ? static_cast<size_t>(rows) * w->n_chunks * k * 4 : 0;
-  off = round_up(off + cand, 256);
+  off = round_up(off + R * csa::kTopkCandCap * 4, 256);
   w->cand_idx_off = off;
-  off = round_up(off + cand, 256);
+  off = round_up(off + R * csa::kTopkCandCap * 4, 256);
   w->total = off;
   return true;
 }
@@ -126,8 +138,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + w.hist_off);
-  const size_t hist_bytes = static_cast<size_t>(B) * Q * 2048 * 4;
-  if (cudaMemsetAsync(hist, 0, hist_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
 
   csa::IndexArgs ia;
   ia.qI = qI;
@@ -158,12 +169,16 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ta.m = p->m;
   ta.k = p->topk;
   ta.n_cap = n_cap;
-  ta.chunk = w.chunk;
-  ta.n_chunks = w.n_chunks;
   ta.idx_out = idx_out;
   ta.score_out = score_out;
+  ta.bits = reinterpret_cast<uint32_t*>(wsb + w.bits_off);
+  ta.ties = reinterpret_cast<uint32_t*>(wsb + w.ties_off);
+  ta.bits_ld = w.bits_ld;
+  ta.cand_count = reinterpret_cast<unsigned*>(wsb + w.count_off);
+  ta.row_done = reinterpret_cast<unsigned*>(wsb + w.done_off);
   ta.cand_key = reinterpret_cast<uint32_t*>(wsb + w.cand_key_off);
   ta.cand_idx = reinterpret_cast<int32_t*>(wsb + w.cand_idx_off);
+  ta.cand_cap = csa::kTopkCandCap;
   ta.status = status;
   return cuda_status(csa::launch_topk(ta, st));
 }

@@ -38,17 +38,30 @@ constexpr int kTileKeys = 128;
 constexpr uint32_t kKeyTileBytes = kTileKeys * kIdxDim;   // 16 KiB
 constexpr uint32_t kQBytes = kIdxHeads * kIdxDim;         // 8 KiB per query
 
-constexpr int kEpiGroups = 4;                // 4 warps per group, one per TMEM lane quadrant
-constexpr int kEpiWarps = 4 * kEpiGroups;
-constexpr int kIndexThreads = 64 + 32 * kEpiWarps;
+// Shape of the decode (one query per group) configuration.
+#ifndef CSA_INDEX_DECODE_STAGES
+#define CSA_INDEX_DECODE_STAGES 4
+#endif
+#ifndef CSA_INDEX_DECODE_GROUPS
+#define CSA_INDEX_DECODE_GROUPS 2
+#endif
+#ifndef CSA_INDEX_DECODE_CTAS_PER_SM
+#define CSA_INDEX_DECODE_CTAS_PER_SM 2
+#endif
 
 template <int QPC>
 struct IndexCfg {
   static constexpr int N = kIdxHeads * QPC;
-  static constexpr int STAGES = QPC == 1 ? 12 : 8;  // one CTA per SM: 192 / 128 KiB of keys in flight
-  static constexpr int NBUF = QPC == 1 ? 4 : 2;     // TMEM accumulators; tile n uses buffer n % NBUF
-  static constexpr uint32_t TMEM_COLS = NBUF * N;
-  static constexpr size_t SMEM = 1024 + 2 * QPC * kQBytes + STAGES * kKeyTileBytes + kEpiWarps * kIdxHeads * 4 +
+  // Epilogue groups of 4 warps (one per TMEM lane quadrant).  One query per
+  // group: the groups take tiles in turn; four queries: a group per query.
+  static constexpr int GROUPS = QPC == 1 ? CSA_INDEX_DECODE_GROUPS : 4;
+  static constexpr int EPI_WARPS = 4 * GROUPS;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int CTAS_PER_SM = QPC == 1 ? CSA_INDEX_DECODE_CTAS_PER_SM : 1;
+  static constexpr int STAGES = QPC == 1 ? CSA_INDEX_DECODE_STAGES : 8;
+  static constexpr int NBUF = QPC == 1 ? (GROUPS < 2 ? 2 : GROUPS) : 2;  // TMEM accumulators; tile n: n % NBUF
+  static constexpr uint32_t TMEM_COLS = NBUF * N <= 32 ? 32 : (NBUF * N <= 64 ? 64 : (NBUF * N <= 128 ? 128 : (NBUF * N <= 256 ? 256 : 512)));
+  static constexpr size_t SMEM = 1024 + 2 * QPC * kQBytes + STAGES * kKeyTileBytes + EPI_WARPS * kIdxHeads * 4 +
                                  (2 * STAGES + 2 * NBUF + 5) * 8 + 16;
 };
 
@@ -102,7 +115,7 @@ __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const Group
 }
 
 template <int QPC>
-__global__ void __launch_bounds__(kIndexThreads, 1)
+__global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PER_SM)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
   using Cfg = IndexCfg<QPC>;
@@ -114,6 +127,8 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
   uint8_t* q_s = base;                                   // [2][QPC * 8 KiB]
   uint8_t* k_s = q_s + 2 * QPC * kQBytes;                // [STAGES][16 KiB]
   constexpr int NBUF = Cfg::NBUF;
+  constexpr int kEpiWarps = Cfg::EPI_WARPS;
+  constexpr int kEpiGroups = Cfg::GROUPS;
   float* w_s = reinterpret_cast<float*>(k_s + STAGES * kKeyTileBytes);  // [epilogue warps][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(w_s + kEpiWarps * kIdxHeads);
   uint64_t* empty = full + STAGES;
@@ -296,7 +311,7 @@ __global__ void __launch_bounds__(kIndexThreads, 1)
       if (!active || tile * kTileKeys >= gi.vmax) continue;
       if (tile == 0 && warp == 2 && lane == 0 && group_past_cache<QPC>(a, gi)) record_error(a.status, kErrIndexRange);
       const int my_it = it++;
-      if (QPC == 1 && (my_it & (kEpiGroups - 1)) != grp) continue;  // another group's tile
+      if (QPC == 1 && (my_it % kEpiGroups) != grp) continue;  // another group's tile
       const int x = my_it % NBUF;
       const uint32_t xuse = static_cast<uint32_t>(my_it / NBUF);
       // every lane waits; the warp leaves together if any lane gave up
@@ -387,14 +402,14 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int per_sm = 1;  // the ring fills most of shared memory
+  const int per_sm = Cfg::CTAS_PER_SM;
   const int64_t tiles_per_group = (a.n_cap + kTileKeys - 1) / kTileKeys;
   const int64_t groups_per_seq = (a.Q + QPC - 1) / QPC;
   const int64_t units = tiles_per_group * groups_per_seq * a.B;
   // One wave of CTAs that all stay resident; each takes an equal range.
   int64_t ctas = static_cast<int64_t>(sms) * per_sm;
   if (ctas > units) ctas = units;
-  index_score_kernel<QPC><<<static_cast<unsigned>(ctas), kIndexThreads, Cfg::SMEM, stream>>>(
+  index_score_kernel<QPC><<<static_cast<unsigned>(ctas), Cfg::THREADS, Cfg::SMEM, stream>>>(
       tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
   return counted(cudaGetLastError());
 }

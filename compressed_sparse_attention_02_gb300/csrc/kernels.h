@@ -25,7 +25,7 @@ constexpr int kIdxHeads = 64;   // indexer heads
 constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
-constexpr int kTopkMaxItems = 16384;  // items one top-k block selects from
+constexpr int kTopkCandCap = 4096;    // crossing-digit candidates a top-k row keeps
 
 // ---- compressor --------------------------------------------------------------
 struct CompressArgs {
@@ -67,20 +67,25 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
 struct TopkArgs {
   const float* scores;
   int64_t score_ld;
-  const uint32_t* hist;     // [B*Q][2048] from the indexer, or null
+  const uint32_t* hist;     // [B*Q][2048] key first-digit counts from the indexer
   const int32_t* q_pos;
   int64_t pos_base;
   int B, Q, m, k;
   int64_t n_cap;
-  int chunk, n_chunks;      // from topk_chunking()
   int32_t* idx_out;         // [B][Q][k]
   float* score_out;         // [B][Q][k] or null
-  uint32_t* cand_key;       // [B*Q][n_chunks][k] (n_chunks > 1)
-  int32_t* cand_idx;
+  uint32_t* bits;           // [B*Q][bits_ld] selected-position bitmap (scratch)
+  uint32_t* ties;           // [B*Q][bits_ld] threshold-tie bitmap (scratch)
+  int64_t bits_ld;          // topk_bits_ld(n_cap)
+  unsigned* cand_count;     // [B*Q], zeroed by the caller
+  unsigned* row_done;       // [B*Q], zeroed by the caller
+  uint32_t* cand_key;       // [B*Q][cand_cap]
+  int32_t* cand_idx;        // [B*Q][cand_cap]
+  int cand_cap;             // <= kTopkCandCap
   unsigned* status;
 };
-// Chooses the chunk length the first selection pass works on.
-void topk_chunking(int64_t rows, int64_t n_cap, int k, int* chunk, int* n_chunks);
+// Words per row of the top-k position bitmaps (a multiple of 4).
+int64_t topk_bits_ld(int64_t n_cap);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 // ---- sparse attention (tcgen05, bf16) ------------------------------------------------

@@ -4,19 +4,28 @@
 // ("DeepSeek 注意力结构对比" CSA2 section: sorted by position); equal scores
 // are broken toward the smaller entry index.
 //
-// Scores become order-preserving 32-bit keys (sign-magnitude flip; -0 is
-// folded into +0 and NaN maps to the smallest key).  One 1024-thread CTA
-// holds up to 32768 keys of a row in shared memory and finds the k-th largest
-// by successive refinement: the current key interval [lo, hi] is cut into
-// 2048 equal bins (the keys spread over many bins, so the shared-memory
-// histogram sees few conflicting atomics), the bin holding the k-th key
-// becomes the next interval, and the search stops when that bin holds exactly
-// the keys still needed or a single key value (at most four passes for 32-bit
-// keys).  A compaction in position order (warp ballots, one scan over warps)
-// then emits every key above the threshold plus the first ties at it, so the
-// output is already sorted by entry.  Rows longer than 32768 are cut into
-// chunks whose local top-k (an exact superset of the global one) are merged
-// by a second selection.
+// Scores are compared as order-preserving 32-bit keys (keys.cuh).  While it
+// scores, the indexer counts each row's keys by their top 11 bits (the
+// "digit"), so the digit d* that holds the k-th largest key is known without
+// another pass over the row.  One kernel then selects, one CTA per 4096 keys
+// of a row:
+//   filter  a key whose digit is above d* is selected.  Each thread reads 16
+//           consecutive keys from shared memory and builds their half of a
+//           32-bit word of the row's position bitmap.  A key whose digit is
+//           d* is a candidate: the CTA gathers its candidates in shared
+//           memory and appends them, with their positions, to the row's list
+//           (one global atomic per CTA).
+//   finish  the last CTA of the row to finish its filter (release/acquire on
+//           a per-row counter; no CTA waits for another) resolves the
+//           candidates exactly: two more digits (11 and 10 bits) give the
+//           threshold key; candidates above it are selected, and of those
+//           equal to it the ones at the lowest positions (read in order from
+//           a tie bitmap).  These extra positions are merged into the
+//           bitmap as it is read out in position order, which gives the
+//           ascending output; the selected scores are gathered last.
+// When d* alone holds exactly the keys still needed, the filter selects all of
+// d* and the finish only reads the bitmap out.  A row whose candidate list
+// overflows is resolved from its scores in global memory (slower, exact).
 #include "keys.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -24,38 +33,63 @@
 namespace csa {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 2048;
-constexpr int kChunk = 32768;  // keys one CTA selects from
+constexpr int kItems = 4096;     // keys per CTA: 16 consecutive keys per thread
+constexpr int kLocalCap = 2048;  // candidates one CTA gathers before the row falls back
+constexpr int kEmitWords = 8;    // bitmap words a thread reads per round of the read-out
+constexpr int kRoundWords = kThreads * kEmitWords;
+static_assert(kItems == 16 * kThreads, "a thread covers half a bitmap word");
+static_assert(kTopkCandCap >= 2 * kLocalCap && kTopkCandCap >= kRoundWords && kRoundWords >= kMaxTopk,
+              "shared-memory reuse");
 
-constexpr int kCandCap = 4096;  // keys of the crossing digit resolved in shared memory
-
-struct SelectSmem {
-  int hist[kBins];
-  int wval[kWarps];
-  int wtotal;
-  uint32_t wmin[kWarps], wmax[kWarps];
-  int bin, above, in_bin;
-  int n_cand;
-  uint32_t cand[kCandCap];
+struct Crossing {
+  int bin, above, in_bin;  // the bin, the count in higher bins, the count in it
 };
 
-// Exclusive scan over the 32 warps of one value per warp (every lane of a
-// warp passes the same `v`); returns the warp's prefix, *total the sum.
-__device__ int warp_values_scan(int v, SelectSmem& sm, int* total) {
+struct __align__(16) Smem {
+  union {
+    struct {
+      float vals[kItems];        // the CTA's scores
+      uint32_t lkey[kLocalCap];  // its candidates
+      int32_t lpos[kLocalCap];
+    } f;
+    struct {
+      uint32_t ckey[kTopkCandCap];  // the row's candidates
+      int32_t cpos[kTopkCandCap];
+    } c;
+    struct {
+      uint32_t rbuf[kRoundWords];  // extra selected positions of one read-out round
+      int32_t sel[kMaxTopk];       // the selected positions, ascending
+    } e;
+  } u;
+  union {
+    int hist[2048];           // digit counts
+    int32_t xpos[kMaxTopk];   // extra selected positions (unordered)
+  } h;
+  int wsum[kWarps];
+  int wval[kWarps];
+  int wtotal;
+  Crossing out;
+  int n_local, cand_base, last, nx;
+  uint64_t bar;
+};
+
+// Exclusive scan over the warps of the block of one value per warp (every
+// lane of a warp passes the same v); returns the warp's prefix, *total the sum.
+__device__ int warps_scan(int v, Smem& sm, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) sm.wval[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    const int x = sm.wval[lane];
+    const int x = lane < kWarps ? sm.wval[lane] : 0;
     int incl = x;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += y;
     }
-    sm.wval[lane] = incl - x;
+    if (lane < kWarps) sm.wval[lane] = incl - x;
     if (lane == 31) sm.wtotal = incl;
   }
   __syncthreads();
@@ -65,165 +99,102 @@ __device__ int warp_values_scan(int v, SelectSmem& sm, int* total) {
   return r;
 }
 
-// Emits, in position order, every key > thr and the first `ties` keys == thr.
-// Warp w owns positions [w*span, (w+1)*span); its lanes visit them 32 at a
-// time; one scan over warps gives each warp its first output slot.
-template <class Emit>
-__device__ void compact_in_order(const uint32_t* keys, int n, uint32_t thr, int ties, SelectSmem& sm, Emit emit) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int span = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int p0 = min(n, warp * span), p1 = min(n, p0 + span);
-  int gt = 0, eq = 0;
-  for (int p = p0 + lane; p < p1; p += 32) {
-    const uint32_t k = keys[p];
-    gt += k > thr;
-    eq += k == thr;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, off);
-    eq += __shfl_xor_sync(0xffffffffu, eq, off);
-  }
-  int total;
-  const int eq_before = warp_values_scan(eq, sm, &total);
-  const int take = max(0, min(eq, ties - eq_before));
-  int slot = warp_values_scan(gt + take, sm, &total);
-  int seen = 0;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int base = p0; base < p1; base += 32) {
-    const int p = base + lane;
-    const uint32_t k = p < p1 ? keys[p] : 0u;
-    const bool is_gt = p < p1 && k > thr;
-    const bool is_eq = p < p1 && k == thr;
-    const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
-    const bool take_it = is_gt || (is_eq && seen + __popc(eqm & lt) < take);
-    const unsigned selm = __ballot_sync(0xffffffffu, take_it);
-    if (take_it) emit(p, slot + __popc(selm & lt));
-    slot += __popc(selm);
-    seen += __popc(eqm);
-  }
-}
-
-// Finds, among the counts hist[0..nb) scanned from the top bin down, the bin
-// where the running count first reaches `need`; sets sm.bin, sm.above (count
-// in higher bins) and sm.in_bin.  Every thread holds nb / kThreads bins.
-__device__ void find_crossing(const int* hist_s, const uint32_t* hist_g, int nb, int need, SelectSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int per = nb / kThreads;  // 1 or 2
-  const int b0 = nb - 1 - per * tid;
-  int c[2] = {0, 0};
-  for (int u = 0; u < per; ++u) c[u] = hist_g ? static_cast<int>(__ldg(hist_g + b0 - u)) : hist_s[b0 - u];
-  const int x = c[0] + c[1];
-  int incl = x;
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  int total;
-  const int wprefix = warp_values_scan(__shfl_sync(0xffffffffu, incl, 31), sm, &total);
-  int cum = wprefix + incl - x;
-  for (int u = 0; u < per; ++u) {
-    if (cum < need && cum + c[u] >= need) {
-      sm.bin = b0 - u;
-      sm.above = cum;
-      sm.in_bin = c[u];
-    }
-    cum += c[u];
-  }
-  __syncthreads();
+  return x;
 }
 
-// Selects the kk largest of keys[0..n) (kk <= n <= kChunk), ties toward the
-// smaller position, and calls emit(position, slot) for each, with slots
-// 0..kk-1 in ascending position order.  Warp w owns positions
-// [w*span, (w+1)*span); its lanes visit them 32 at a time.
-template <class Emit>
-__device__ void block_select(const uint32_t* keys, int n, int kk, SelectSmem& sm, Emit emit) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int span = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
-  const int p0 = min(n, warp * span), p1 = min(n, p0 + span);
+// The block-wide exclusive prefix of this thread's count; *total the sum.
+__device__ int block_prefix(int cnt, Smem& sm, int* total) {
+  const int incl = warp_incl_scan(cnt);
+  const int wbase = warps_scan(__shfl_sync(0xffffffffu, incl, 31), sm, total);
+  return wbase + incl - cnt;
+}
 
-  uint32_t thr = 0u;
-  int ties = n;  // kk == n: everything is taken
-  if (kk < n) {
-    // key interval of the row
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    for (int p = p0 + lane; p < p1; p += 32) {
-      const uint32_t k = keys[p];
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
-    }
+// Scanning the counts of nb (1024 or 2048) bins of sm.h.hist from the top bin
+// down, finds the bin in which the running count first reaches `need`.  Thread
+// t holds bins nb-1-per*t down to nb-per*(t+1); two barriers.  If the counts
+// never reach `need` the result is {0, 0, 0}.
+__device__ Crossing find_crossing(int nb, int need, Smem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = nb / kThreads;  // 4 or 8
+  const int lo = nb - per * (static_cast<int>(threadIdx.x) + 1);
+  int c[8];
+  const int4 v0 = *reinterpret_cast<const int4*>(sm.h.hist + lo + per - 4);
+  const int4 v1 = per == 8 ? *reinterpret_cast<const int4*>(sm.h.hist + lo) : make_int4(0, 0, 0, 0);
+  c[0] = v0.w, c[1] = v0.z, c[2] = v0.y, c[3] = v0.x;  // highest bin first
+  c[4] = v1.w, c[5] = v1.z, c[6] = v1.y, c[7] = v1.x;
+  int x = 0;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
-      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+  for (int u = 0; u < 8; ++u) x += c[u];
+  const int incl = warp_incl_scan(x);
+  if (lane == 31) sm.wsum[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int s = sm.wsum[w];
+    before += w < warp ? s : 0;
+    total += s;
+  }
+  int cum = before + incl - x;
+  if (cum < need && cum + x >= need) {
+    const int top = lo + per - 1;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < per && cum < need && cum + c[u] >= need) sm.out = Crossing{top - u, cum, c[u]};
+      cum += c[u];
     }
-    if (lane == 0) {
-      sm.wmin[warp] = kmin;
-      sm.wmax[warp] = kmax;
+  }
+  __syncthreads();
+  return total >= need ? sm.out : Crossing{0, 0, 0};
+}
+
+// Resolves the key digits below the first, 11 then 10 bits, among keys whose
+// first digit is d*; key_at(i) for i < n gives the keys to count.  Returns the
+// exact threshold key; *need becomes how many keys equal to it are taken and
+// *n_eq how many there are.
+template <class KeyAt>
+__device__ uint32_t resolve_threshold(uint32_t dstar, int64_t n, KeyAt key_at, Smem& sm, int* need, int* n_eq) {
+  uint32_t prefix = dstar << kKeyBinShift;
+  int in_bin = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    const int nb = pass == 0 ? 2048 : 1024;
+    const uint32_t mask = pass == 0 ? 0xFFE00000u : 0xFFFFFC00u;
+    for (int i = threadIdx.x; i < nb; i += kThreads) sm.h.hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t k = key_at(i);
+      if ((k & mask) == prefix) atomicAdd(&sm.h.hist[(k >> shift) & (nb - 1)], 1);
     }
     __syncthreads();
-    uint32_t lo = sm.wmin[0], hi = sm.wmax[0];
-    for (int w = 1; w < kWarps; ++w) {
-      lo = min(lo, sm.wmin[w]);
-      hi = max(hi, sm.wmax[w]);
-    }
-    int remaining = kk;
-    bool whole = false;
-    while (lo < hi) {
-      const uint64_t R = static_cast<uint64_t>(hi - lo) + 1u;
-      for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0;
-      __syncthreads();
-      for (int p = p0 + lane; p < p1; p += 32) {
-        const uint32_t k = keys[p];
-        if (k >= lo && k <= hi)
-          atomicAdd(&sm.hist[static_cast<int>(static_cast<uint64_t>(k - lo) * kBins / R)], 1);
-      }
-      __syncthreads();
-      // Thread t owns bins 2047-2t and 2046-2t: counts from the top bin down.
-      const int b0 = kBins - 1 - 2 * tid;
-      const int c0 = sm.hist[b0], c1 = sm.hist[b0 - 1];
-      const int x = c0 + c1;
-      int incl = x;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      int total;
-      const int wprefix = warp_values_scan(__shfl_sync(0xffffffffu, incl, 31), sm, &total);
-      const int excl = wprefix + incl - x;  // keys in the bins above this thread's two
-      if (excl < remaining && excl + c0 >= remaining) {
-        sm.bin = b0;
-        sm.above = excl;
-        sm.in_bin = c0;
-      } else if (excl + c0 < remaining && excl + x >= remaining) {
-        sm.bin = b0 - 1;
-        sm.above = excl + c0;
-        sm.in_bin = c1;
-      }
-      __syncthreads();
-      const int bin = sm.bin;
-      remaining -= sm.above;
-      const bool exact_bin = sm.in_bin == remaining;
-      __syncthreads();
-      // keys of bin b: lo + ceil(b*R/kBins) .. lo + ceil((b+1)*R/kBins) - 1
-      const uint32_t blo = lo + static_cast<uint32_t>((static_cast<uint64_t>(bin) * R + kBins - 1) / kBins);
-      const uint32_t bhi =
-          lo + static_cast<uint32_t>((static_cast<uint64_t>(bin + 1) * R + kBins - 1) / kBins) - 1u;
-      lo = blo;
-      hi = bhi;
-      if (exact_bin) {  // the whole bin is taken: select every key >= lo
-        whole = true;
-        break;
-      }
-    }
-    thr = lo;
-    ties = whole ? n : remaining;
+    const Crossing c = find_crossing(nb, *need, sm);
+    prefix |= static_cast<uint32_t>(c.bin) << shift;
+    *need -= c.above;
+    in_bin = c.in_bin;
   }
+  *n_eq = in_bin;
+  return prefix;
+}
 
-  compact_in_order(keys, n, thr, ties, sm, emit);
+__device__ __forceinline__ void push_extra(Smem& sm, int32_t pos) {
+  const int slot = atomicAdd(&sm.nx, 1);
+  if (slot < kMaxTopk) sm.h.xpos[slot] = pos;
+}
+
+// One bulk async copy global -> shared completing on `bar` (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ int64_t visible_entries(const TopkArgs& a, int b, int q) {
@@ -232,186 +203,245 @@ __device__ __forceinline__ int64_t visible_entries(const TopkArgs& a, int b, int
   return V > a.n_cap ? a.n_cap : V;
 }
 
-// Pass 1: top-k of one chunk of one (sequence, query) row.  With a single
-// chunk the result is final; otherwise it is a candidate list.
-__global__ void __launch_bounds__(kThreads, 1) topk_chunk_kernel(const TopkArgs a) {
-  extern __shared__ uint32_t keys[];
-  __shared__ SelectSmem sm;
-  const int b = blockIdx.z, q = blockIdx.y, c = blockIdx.x;
-  const int64_t row = static_cast<int64_t>(b) * a.Q + q;
-  const int64_t V = visible_entries(a, b, q);
-  const int64_t c0 = static_cast<int64_t>(c) * a.chunk;
-  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), V - c0)));
-  const int kk = min(a.k, n);
-  const bool final_pass = a.n_chunks == 1;
-  if (!final_pass && n <= 0) return;
-
-  const float* src = a.scores + row * a.score_ld + c0;
-  if (final_pass && a.hist && kk < n) {
-    // The indexer counted the row's first digits: go straight to the digit
-    // holding the k-th key and resolve only that digit's keys.
-    find_crossing(nullptr, a.hist + row * kKeyBins, kKeyBins, kk, sm);
-    const uint32_t dstar = static_cast<uint32_t>(sm.bin);
-    const int remaining = kk - sm.above;
-    const bool whole = sm.in_bin == remaining;
-    if (threadIdx.x == 0) sm.n_cand = 0;
-    // all loads first (independent, so they overlap), then the candidates
-    for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(src + i));
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    for (int base = 0; base < n; base += kThreads) {
-      const int i = base + threadIdx.x;
-      const uint32_t key = i < n ? keys[i] : 0u;
-      const bool c = !whole && i < n && (key >> kKeyBinShift) == dstar;
-      const unsigned m = __ballot_sync(0xffffffffu, c);
-      int pos0 = 0;
-      if (m && lane == 0) pos0 = atomicAdd(&sm.n_cand, __popc(m));
-      pos0 = __shfl_sync(0xffffffffu, pos0, 0);
-      const int pos = pos0 + __popc(m & ((1u << lane) - 1u));
-      if (c && pos < kCandCap) sm.cand[pos] = key;
+// The `need` lowest positions of the tie bitmap go to the extra list.
+__device__ void take_ties(const uint32_t* ties, int64_t nwords, int need, Smem& sm) {
+  __syncthreads();  // the tie bits of every thread are in the bitmap
+  int done = 0;
+  for (int64_t w0 = 0; w0 < nwords && done < need; w0 += kThreads) {
+    const int64_t w = w0 + threadIdx.x;
+    uint32_t word = w < nwords ? __ldcg(ties + w) : 0u;
+    int total;
+    int before = done + block_prefix(__popc(word), sm, &total);
+    while (word && before < need) {
+      const int bit = __ffs(word) - 1;
+      word &= word - 1;
+      push_extra(sm, static_cast<int32_t>(w * 32 + bit));
+      ++before;
     }
-    __syncthreads();
-    uint32_t thr;
-    int ties;
-    if (whole) {
-      thr = dstar << kKeyBinShift;  // every key of the digit is taken
-      ties = n;
-    } else if (sm.n_cand <= kCandCap) {
-      // two more digits (11 + 10 bits) over the candidates only
-      const int nc = sm.n_cand;
-      uint32_t prefix = dstar << kKeyBinShift;
-      int need = remaining;
-      for (int pass = 0; pass < 2; ++pass) {
-        const int shift = pass == 0 ? 10 : 0;
-        const int nb = pass == 0 ? 2048 : 1024;
-        const uint32_t mask = pass == 0 ? 0xFFE00000u : 0xFFFFFC00u;
-        for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
-        __syncthreads();
-        for (int i = threadIdx.x; i < nc; i += kThreads) {
-          const uint32_t k = sm.cand[i];
-          if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (nb - 1)], 1);
-        }
-        __syncthreads();
-        find_crossing(sm.hist, nullptr, nb, need, sm);
-        prefix |= static_cast<uint32_t>(sm.bin) << shift;
-        need -= sm.above;
-        __syncthreads();
-      }
-      thr = prefix;
-      ties = need;
-    } else {
-      // pathological digit (more than kCandCap equal-digit keys): refine
-      // over the whole row instead
-      block_select(keys, n, kk, sm, [&](int pos, int slot) {
-        a.idx_out[row * a.k + slot] = static_cast<int32_t>(c0 + pos);
-        if (a.score_out) a.score_out[row * a.k + slot] = key_score(keys[pos]);
-      });
-      for (int j = kk + threadIdx.x; j < a.k; j += kThreads) {
-        a.idx_out[row * a.k + j] = -1;
-        if (a.score_out) a.score_out[row * a.k + j] = -INFINITY;
-      }
-      return;
-    }
-    int32_t* idx = a.idx_out + row * a.k;
-    float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
-    compact_in_order(keys, n, thr, ties, sm, [&](int pos, int slot) {
-      idx[slot] = static_cast<int32_t>(c0 + pos);
-      if (sc) sc[slot] = key_score(keys[pos]);
-    });
-    for (int j = kk + threadIdx.x; j < a.k; j += kThreads) {
-      idx[j] = -1;
-      if (sc) sc[j] = -INFINITY;
-    }
-    return;
-  }
-  for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = score_key(__ldg(src + i));
-  __syncthreads();
-
-  if (final_pass) {
-    int32_t* idx = a.idx_out + row * a.k;
-    float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
-    block_select(keys, n, kk, sm, [&](int pos, int slot) {
-      idx[slot] = static_cast<int32_t>(c0 + pos);
-      if (sc) sc[slot] = key_score(keys[pos]);
-    });
-    for (int j = kk + threadIdx.x; j < a.k; j += kThreads) {
-      idx[j] = -1;
-      if (sc) sc[j] = -INFINITY;
-    }
-  } else {
-    uint32_t* ck = a.cand_key + (row * a.n_chunks + c) * a.k;
-    int32_t* ci = a.cand_idx + (row * a.n_chunks + c) * a.k;
-    block_select(keys, n, kk, sm, [&](int pos, int slot) {
-      ck[slot] = keys[pos];
-      ci[slot] = static_cast<int32_t>(c0 + pos);
-    });
+    done += total;
   }
 }
 
-// Pass 2: merge the per-chunk candidates of one row into the final top-k.
-// Every chunk but the last non-empty one holds exactly k candidates (chunks
-// are at least 2k long), so the candidates sit contiguously in chunk order,
-// i.e. in ascending entry order.
-__global__ void __launch_bounds__(kThreads, 1) topk_merge_kernel(const TopkArgs a) {
-  extern __shared__ uint32_t keys[];
-  __shared__ SelectSmem sm;
-  const int b = blockIdx.y, q = blockIdx.x;
-  const int64_t row = static_cast<int64_t>(b) * a.Q + q;
-  const int64_t V = visible_entries(a, b, q);
-  int32_t* pos_idx = reinterpret_cast<int32_t*>(keys + kTopkMaxItems);
-
-  const int64_t n_full = V / a.chunk;
-  const int64_t rest = V - n_full * a.chunk;
-  const int total = static_cast<int>(n_full * a.k + min(static_cast<int64_t>(a.k), rest));
-  const uint32_t* ck = a.cand_key + row * a.n_chunks * a.k;
-  const int32_t* ci = a.cand_idx + row * a.n_chunks * a.k;
-  for (int f = threadIdx.x; f < total; f += kThreads) {
-    keys[f] = __ldg(ck + f);
-    pos_idx[f] = __ldg(ci + f);
+// The finish of one row, run by the last of its CTAs.
+__device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Crossing& c, Smem& sm) {
+  const float* src = a.scores + row * a.score_ld;
+  const uint32_t* bits = a.bits + row * a.bits_ld;
+  uint32_t* ties = a.ties + row * a.bits_ld;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwords = (V + 31) >> 5;
+  const uint32_t dstar = static_cast<uint32_t>(c.bin);
+  int need = a.k - c.above;
+  if (threadIdx.x == 0) sm.nx = 0;
+  if (c.in_bin != need) {
+    const int nc = static_cast<int>(__ldcg(a.cand_count + row));
+    int n_eq = 0;
+    if (nc <= a.cand_cap) {
+      for (int i = threadIdx.x; i < nc; i += kThreads) {
+        sm.u.c.ckey[i] = __ldcg(a.cand_key + row * a.cand_cap + i);
+        sm.u.c.cpos[i] = __ldcg(a.cand_idx + row * a.cand_cap + i);
+      }
+      const uint32_t thr = resolve_threshold(dstar, nc, [&](int64_t i) { return sm.u.c.ckey[i]; }, sm, &need, &n_eq);
+      const bool all_eq = n_eq == need;  // every key equal to thr is taken
+      for (int i = threadIdx.x; i < nc; i += kThreads) {
+        const uint32_t k = sm.u.c.ckey[i];
+        const int p = sm.u.c.cpos[i];
+        if (k > thr || (k == thr && all_eq)) push_extra(sm, p);
+        if (k == thr && !all_eq) atomicOr(ties + (p >> 5), 1u << (p & 31));
+      }
+      if (!all_eq) take_ties(ties, nwords, need, sm);
+    } else {
+      // the candidate list overflowed: the same digits counted over the row's scores
+      const uint32_t thr =
+          resolve_threshold(dstar, V, [&](int64_t i) { return score_key(__ldg(src + i)); }, sm, &need, &n_eq);
+      const bool all_eq = n_eq == need;
+      for (int64_t base = 0; base < V; base += kThreads) {
+        const int64_t i = base + threadIdx.x;
+        const uint32_t k = i < V ? score_key(__ldg(src + i)) : 0u;
+        const bool in = i < V && (k >> kKeyBinShift) == dstar;
+        if (in && (k > thr || (k == thr && all_eq))) push_extra(sm, static_cast<int32_t>(i));
+        const unsigned em = __ballot_sync(0xffffffffu, in && k == thr && !all_eq);
+        if (lane == 0 && em) atomicOr(ties + ((i - lane) >> 5), em);
+      }
+      if (!all_eq) take_ties(ties, nwords, need, sm);
+    }
   }
   __syncthreads();
-  const int kk = min(a.k, total);
+  const int nx = min(sm.nx, kMaxTopk);
+  // Read the bitmap out in position order, rounds of 2048 words: eight
+  // consecutive words per thread, the round's extra positions OR-ed in from
+  // shared memory, one block scan per round.
+  int out = 0;
+  for (int64_t w0 = 0; w0 < nwords && out < a.k; w0 += kRoundWords) {
+    const int64_t wb = w0 + kEmitWords * threadIdx.x;
+    uint32_t wd[kEmitWords];
+    if (wb < nwords) {  // bits_ld is a multiple of kEmitWords: both vectors stay inside the row
+      const uint4 lo = __ldcg(reinterpret_cast<const uint4*>(bits + wb));
+      const uint4 hi = __ldcg(reinterpret_cast<const uint4*>(bits + wb + 4));
+      wd[0] = lo.x, wd[1] = lo.y, wd[2] = lo.z, wd[3] = lo.w, wd[4] = hi.x, wd[5] = hi.y, wd[6] = hi.z, wd[7] = hi.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < kEmitWords; ++e) wd[e] = 0u;
+    }
+    if (nx > 0) {
+      uint4* rb = reinterpret_cast<uint4*>(sm.u.e.rbuf + kEmitWords * threadIdx.x);
+      rb[0] = make_uint4(0, 0, 0, 0);
+      rb[1] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+      for (int j = threadIdx.x; j < nx; j += kThreads) {
+        const int32_t p = sm.h.xpos[j];
+        const int64_t w = (p >> 5) - w0;
+        if (w >= 0 && w < kRoundWords) atomicOr(sm.u.e.rbuf + w, 1u << (p & 31));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < kEmitWords; ++e) wd[e] |= sm.u.e.rbuf[kEmitWords * threadIdx.x + e];
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kEmitWords; ++e) {
+      if (wb + e >= nwords) wd[e] = 0u;
+      cnt += __popc(wd[e]);
+    }
+    int total;
+    int slot = out + block_prefix(cnt, sm, &total);
+#pragma unroll
+    for (int e = 0; e < kEmitWords; ++e) {
+      uint32_t word = wd[e];
+      while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1;
+        if (slot < a.k) sm.u.e.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
+        ++slot;
+      }
+    }
+    out += total;
+  }
+  __syncthreads();
   int32_t* idx = a.idx_out + row * a.k;
   float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
-  block_select(keys, total, kk, sm, [&](int pos, int slot) {
-    idx[slot] = pos_idx[pos];
-    if (sc) sc[slot] = key_score(keys[pos]);
-  });
-  for (int j = kk + threadIdx.x; j < a.k; j += kThreads) {
-    idx[j] = -1;
-    if (sc) sc[j] = -INFINITY;
+  for (int j = threadIdx.x; j < a.k; j += kThreads) {
+    const int32_t p = j < out ? sm.u.e.sel[j] : -1;
+    idx[j] = p;
+    if (sc) sc[j] = p >= 0 ? __ldg(src + p) + 0.0f : -INFINITY;
   }
+}
+
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a) {
+  __shared__ Smem sm;
+  const int b = blockIdx.z, q = blockIdx.y;
+  const int64_t row = static_cast<int64_t>(b) * a.Q + q;
+  const int64_t V = visible_entries(a, b, q);
+  const float* src = a.scores + row * a.score_ld;
+  if (V <= a.k) {  // every visible entry is selected; the row's first CTA writes it
+    if (blockIdx.x != 0) return;
+    for (int j = threadIdx.x; j < a.k; j += kThreads) {
+      a.idx_out[row * a.k + j] = j < V ? j : -1;
+      if (a.score_out) a.score_out[row * a.k + j] = j < V ? __ldg(src + j) + 0.0f : -INFINITY;
+    }
+    return;
+  }
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kItems;
+  if (i0 >= V) return;
+  const int n_in = static_cast<int>(min(V - i0, static_cast<int64_t>(kItems)));
+  // the chunk's scores and the row's digit counts, one bulk copy each
+  if (threadIdx.x == 0) {
+    const uint32_t vbytes = static_cast<uint32_t>((n_in * 4 + 15) & ~15);  // score rows are padded to 16 B
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&sm.bar, vbytes + kKeyBins * 4);
+    bulk_load(sm.u.f.vals, src + i0, vbytes, &sm.bar);
+    bulk_load(sm.h.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.bar);
+    sm.n_local = 0;
+  }
+  __syncthreads();
+  if (!__syncthreads_and(mbar_wait(&sm.bar, 0, a.status))) return;
+  const Crossing c = find_crossing(kKeyBins, a.k, sm);
+  const uint32_t dstar = static_cast<uint32_t>(c.bin);
+  const bool whole = c.in_bin == a.k - c.above;
+  const uint32_t dsel = whole ? dstar : dstar + 1;  // keys with digit >= dsel are selected outright
+
+  // 16 consecutive keys per thread, read as four float4 in a rotated order so
+  // that the eight threads of a shared-memory phase hit distinct banks
+  const int t = threadIdx.x, lane = t & 31;
+  uint32_t smask = 0, cmask = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int jj = (j + (t >> 1)) & 3;
+    const float4 x = reinterpret_cast<const float4*>(sm.u.f.vals)[4 * t + jj];
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int bit = 4 * jj + e;
+      const bool in = 16 * t + bit < n_in;
+      const uint32_t d = score_key(xs[e]) >> kKeyBinShift;
+      smask |= static_cast<uint32_t>(in && d >= dsel) << bit;
+      cmask |= static_cast<uint32_t>(in && !whole && d == dstar) << bit;
+    }
+  }
+  // thread pairs (2u, 2u+1) make bitmap word u of the chunk
+  const uint32_t upper = __shfl_down_sync(0xffffffffu, smask, 1);
+  if ((t & 1) == 0 && 16 * t < n_in) {
+    const int64_t w = (i0 >> 5) + (t >> 1);
+    a.bits[row * a.bits_ld + w] = smask | (upper << 16);
+    a.ties[row * a.bits_ld + w] = 0u;
+  }
+  if (__any_sync(0xffffffffu, cmask != 0)) {
+    const int cnt = __popc(cmask);
+    const int incl = warp_incl_scan(cnt);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sm.n_local, incl);
+    int slot = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+    while (cmask) {
+      const int bit = __ffs(cmask) - 1;
+      cmask &= cmask - 1;
+      if (slot < kLocalCap) {
+        sm.u.f.lkey[slot] = score_key(sm.u.f.vals[16 * t + bit]);
+        sm.u.f.lpos[slot] = static_cast<int32_t>(i0 + 16 * t + bit);
+      }
+      ++slot;
+    }
+  }
+  __syncthreads();
+  const int n_local = sm.n_local;
+  if (n_local > 0) {
+    // a CTA whose list overflowed pushes the row's count past the cap: the
+    // finish then counts from the scores
+    const unsigned add = n_local > kLocalCap ? static_cast<unsigned>(a.cand_cap) + 1u : static_cast<unsigned>(n_local);
+    if (threadIdx.x == 0) sm.cand_base = static_cast<int>(atomicAdd(a.cand_count + row, add));
+    __syncthreads();
+    const int base = sm.cand_base;
+    for (int j = threadIdx.x; j < n_local && j < kLocalCap; j += kThreads) {
+      if (base + j < a.cand_cap) {
+        a.cand_key[row * a.cand_cap + base + j] = sm.u.f.lkey[j];
+        a.cand_idx[row * a.cand_cap + base + j] = sm.u.f.lpos[j];
+      }
+    }
+  }
+  // The last CTA of the row to get here finishes it: the barrier orders this
+  // CTA's writes before thread 0's release, and its acquire (with the
+  // barrier after it) orders the other CTAs' writes before the finish reads.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned n_ctas = static_cast<unsigned>((V + kItems - 1) / kItems);
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.row_done + row) : "memory");
+    sm.last = prev == n_ctas - 1;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  finish_row(a, row, V, c, sm);
 }
 
 }  // namespace
 
-void topk_chunking(int64_t rows, int64_t n_cap, int k, int* chunk, int* n_chunks) {
-  (void)rows;
-  (void)k;
-  int64_t nc = (n_cap + kChunk - 1) / kChunk;
-  if (nc < 1) nc = 1;
-  *chunk = kChunk;
-  *n_chunks = static_cast<int>(nc);
-}
+int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + kEmitWords - 1) / kEmitWords * kEmitWords; }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  const int64_t items = a.n_chunks == 1 ? (a.n_cap < a.chunk ? a.n_cap : a.chunk) : a.chunk;
-  const size_t smem1 = static_cast<size_t>(items) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem1));
-  if (e != cudaSuccess) return e;
-  topk_chunk_kernel<<<dim3(a.n_chunks, a.Q, a.B), kThreads, smem1, stream>>>(a);
-  if ((e = counted(cudaGetLastError())) != cudaSuccess) return e;
-  if (a.n_chunks > 1) {
-    const size_t smem2 = static_cast<size_t>(kTopkMaxItems) * 8;
-    e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem2));
-    if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<dim3(a.Q, a.B), kThreads, smem2, stream>>>(a);
-    e = counted(cudaGetLastError());
-  }
-  return e;
+  if (a.cand_cap > kTopkCandCap) return cudaErrorInvalidValue;
+  const int64_t chunks = (a.n_cap + kItems - 1) / kItems;
+  topk_kernel<<<dim3(static_cast<unsigned>(chunks), a.Q, a.B), kThreads, 0, stream>>>(a);
+  return counted(cudaGetLastError());
 }
 
 }  // namespace csa

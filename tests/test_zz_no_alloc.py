@@ -25,7 +25,7 @@ def csa():
 
 
 def test_static_scratch_matches_workspace_entry_point_on_two_calls(csa):
-    B, n_cap, k = 8, 65536, 512          # two chunks per row: the chunk + merge top-k path
+    B, n_cap, k = 8, 65536, 512          # rows of 65536 visible entries, 2 MiB of scores
     t = 4 * n_cap - 1
     p = csa.csa_default_params(topk=k)
     assert csa.csa_workspace_size(csa.CSA_OP_INDEX_TOPK, p, B, 1, n_cap) <= csa.STATIC_SCRATCH_BYTES
