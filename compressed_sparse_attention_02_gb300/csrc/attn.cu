@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
 
+  pdl_launch_dependents();
+  pdl_wait();  // before any global access and before TMEM is taken
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3;                  // TMEM lane quadrant == 32 tile rows
   const int hw0 = (warp >> 2) * HW;           // first head (within the CTA) of this warp
@@ -432,8 +434,7 @@ cudaError_t launch_nh(const AttnArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<NH><<<dim3(a.Q * (kHeads / NH), a.B), kThreads, smem, stream>>>(a);
-  return counted(cudaGetLastError());
+  return launch_pdl(sparse_attn_kernel<NH>, dim3(a.Q * (kHeads / NH), a.B), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace

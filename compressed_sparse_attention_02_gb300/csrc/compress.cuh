@@ -1,0 +1,216 @@
+// Overlapped CSA compressor for one entry: per-channel softmax pooling over
+// 2m slots, RMSNorm, partial RoPE.  Page "CSA / HCA" (zdszero, hca_csa),
+// section "CSA 的重叠窗口" (Softmax_row and C_i^Comp equations, i = 0
+// boundary); RoPE position = first token of the entry's block ("DeepSeek-V4
+// CSA/HCA 与 DeepSeek-V4.1 CSA2" §7.4); decode emission only at a block
+// boundary ("DeepSeek-V4 的 KV 压缩：从删 token 误解到预算检索" §9.3).
+//
+// A group of kDim / CPT threads computes one entry; thread t owns channels
+// CPT*t .. CPT*t+CPT-1 and reads each of the 4*m source rows it needs with
+// one load of CPT bf16 values.  Softmax, normalisation and rotation are fp32;
+// the RoPE angle is formed and reduced modulo 2*pi in fp64 because positions
+// reach 2^20 and an fp32 angle would be off by ~0.1 rad there.  The 32
+// inverse frequencies come precomputed (fp64) with the arguments, so the
+// device does one multiply, one reduction and one fp32 sincos per pair.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace csa {
+
+template <int CPT>
+struct Bf16Vec;
+template <>
+struct Bf16Vec<8> {
+  using T = uint4;
+  static __device__ __forceinline__ void unpack(const T u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ T pack(const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Bf16Vec<2> {
+  using T = uint32_t;
+  static __device__ __forceinline__ void unpack(const T u, float (&v)[2]) {
+    v[0] = __uint_as_float(u << 16);
+    v[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ T pack(const float (&v)[2]) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+};
+
+// Computes entry (e-th of the chunk in bulk mode; the one completing at
+// q_pos[b] in ring mode) of sequence b.  `red` holds one float per warp of
+// the group; sync() is a barrier over exactly the group's threads.  Every
+// thread of the group must call this with the same (b, e).
+template <int M, int CPT, class Sync>
+__device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync) {
+  using V = Bf16Vec<CPT>;
+  using L = typename V::T;
+  constexpr int D = kDim;
+  constexpr int NT = D / CPT;
+  const int d0 = t * CPT;
+
+  // Locate entry i and the rows of block i (a stream) and block i-1 (b stream).
+  int64_t i;
+  const uint16_t *ca[M], *za[M], *cb[M], *zb[M];
+  bool has_prev;
+  if (a.mode == 0) {
+    i = a.entry0 + e;
+    has_prev = i > 0;
+    const int64_t T = static_cast<int64_t>(M) * a.n_new;
+    const int64_t seq = static_cast<int64_t>(b) * T * D;
+#pragma unroll
+    for (int r = 0; r < M; ++r) {
+      const int64_t row_a = seq + (M * e + r) * D;
+      ca[r] = a.Ca + row_a;
+      za[r] = a.Za + row_a;
+      if (e > 0) {
+        const int64_t row_b = seq + (M * (e - 1) + r) * D;
+        cb[r] = a.Cb + row_b;
+        zb[r] = a.Zb + row_b;
+      } else {
+        // block entry0-1 lives in the separate "previous block" rows
+        const int64_t row_b = (static_cast<int64_t>(b) * M + r) * D;
+        cb[r] = a.Cb_prev ? a.Cb_prev + row_b : nullptr;
+        zb[r] = a.Zb_prev ? a.Zb_prev + row_b : nullptr;
+      }
+    }
+  } else {
+    const int64_t tp = a.q_pos[b];
+    if (tp < 0 || (tp + 1) % M != 0) return;  // no block completes at this step
+    i = (tp + 1) / M - 1;
+    if (i >= a.n_cap) {
+      if (t == 0) record_error(a.status, kErrIndexRange);
+      return;
+    }
+    has_prev = i > 0;
+    const int64_t ring = static_cast<int64_t>(b) * 2 * M * D;
+#pragma unroll
+    for (int r = 0; r < M; ++r) {
+      const int64_t slot_a = (M * i + r) % (2 * M);
+      const int64_t slot_b = (M * (i - 1) + r + 2 * M) % (2 * M);
+      ca[r] = a.Ca + ring + slot_a * D;
+      za[r] = a.Za + ring + slot_a * D;
+      cb[r] = a.Cb + ring + slot_b * D;
+      zb[r] = a.Zb + ring + slot_b * D;
+    }
+  }
+
+  // Issue every load of the entry first (one memory round trip), then math.
+  L zr[2 * M], cr[2 * M], br[2 * M];
+#pragma unroll
+  for (int r = 0; r < M; ++r) {
+    zr[r] = __ldg(reinterpret_cast<const L*>(za[r] + d0));
+    cr[r] = __ldg(reinterpret_cast<const L*>(ca[r] + d0));
+    br[r] = __ldg(reinterpret_cast<const L*>(a.Ba + r * D + d0));
+    if (has_prev) {
+      zr[M + r] = __ldg(reinterpret_cast<const L*>(zb[r] + d0));
+      cr[M + r] = __ldg(reinterpret_cast<const L*>(cb[r] + d0));
+      br[M + r] = __ldg(reinterpret_cast<const L*>(a.Bb + r * D + d0));
+    }
+  }
+  const L wr = __ldg(reinterpret_cast<const L*>(a.rms_w + d0));
+  const int slots = has_prev ? 2 * M : M;  // block i-1 slots are absent for entry 0
+
+  // Maximum logit (Z + B) of the slots, per channel.
+  float mx[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) mx[j] = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < 2 * M; ++r) {
+    if (r < slots) {
+      float z[CPT], bias[CPT];
+      V::unpack(zr[r], z);
+      V::unpack(br[r], bias);
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) mx[j] = fmaxf(mx[j], z[j] + bias[j]);
+    }
+  }
+
+  // Softmax-weighted sum of the C rows.
+  constexpr float kLog2e = 1.4426950408889634f;
+  float num[CPT], den[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) num[j] = den[j] = 0.f;
+#pragma unroll
+  for (int r = 0; r < 2 * M; ++r) {
+    if (r < slots) {
+      float z[CPT], bias[CPT], c[CPT];
+      V::unpack(zr[r], z);
+      V::unpack(br[r], bias);
+      V::unpack(cr[r], c);
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const float w = exp2f((z[j] + bias[j] - mx[j]) * kLog2e);
+        num[j] = fmaf(w, c[j], num[j]);
+        den[j] += w;
+      }
+    }
+  }
+  float x[CPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    x[j] = num[j] / den[j];
+    ss = fmaf(x[j], x[j], ss);
+  }
+
+  // RMSNorm over the 512 channels: warp sums, then the group's warps combine.
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((t & 31) == 0) red[t >> 5] = ss;
+  sync();
+  float total = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) total += red[w];
+  const float inv = rsqrtf(total / static_cast<float>(D) + a.rms_eps);
+  float w[CPT];
+  V::unpack(wr, w);
+  float y[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) y[j] = x[j] * inv * w[j];
+
+  // Partial RoPE on channels D-R .. D-1, interleaved pairs, position M*i.
+  if (d0 >= D - kRope) {
+    const double pos = static_cast<double>(M) * static_cast<double>(i);
+    const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+#pragma unroll
+    for (int pr = 0; pr < CPT / 2; ++pr) {
+      const int jp = (d0 + 2 * pr - (D - kRope)) / 2;
+      double phi = pos * a.inv_freq[jp];
+      phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
+      float s, c;
+      sincosf(static_cast<float>(phi), &s, &c);
+      const float u = y[2 * pr], v = y[2 * pr + 1];
+      y[2 * pr] = u * c - v * s;
+      y[2 * pr + 1] = u * s + v * c;
+    }
+  }
+
+  *reinterpret_cast<L*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * D + d0) = V::pack(y);
+}
+
+// theta^(-2j/R) for the 32 rotated pairs, in fp64 on the host.
+void fill_inv_freq(CompressArgs* a);
+
+}  // namespace csa

@@ -128,7 +128,8 @@ csa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_E
 csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
                           const uint8_t* qI, const uint16_t* wI, const uint8_t* kI, int64_t n_cap,
                           int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes, cudaStream_t st,
-                          bool traced = false) {
+                          bool traced = false, bool zeroed = false,
+                          const csa::CompressArgs* ride_along = nullptr) {
   IndexWs w;
   if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < w.total || !aligned16(ws)) return CSA_ERR_WORKSPACE;
@@ -138,7 +139,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + w.hist_off);
-  if (cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (!zeroed && cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
 
   csa::IndexArgs ia;
   ia.qI = qI;
@@ -180,7 +181,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ta.cand_idx = reinterpret_cast<int32_t*>(wsb + w.cand_idx_off);
   ta.cand_cap = csa::kTopkCandCap;
   ta.status = status;
-  return cuda_status(csa::launch_topk(ta, st));
+  return cuda_status(csa::launch_topk(ta, ride_along, st));
 }
 
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
@@ -214,14 +215,12 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   return cuda_status(csa::launch_sparse_attn(aa, enc, st));
 }
 
-csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,
-                        const uint16_t* Ca, const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
-                        const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
-                        const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
-                        int64_t n_cap, const int32_t* q_pos, cudaStream_t st) {
-  unsigned* status = status_ptr();
-  if (!status) return CSA_ERR_CUDA;
-  csa::CompressArgs ca;
+csa::CompressArgs compress_args(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,
+                                const uint16_t* Ca, const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
+                                const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
+                                const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
+                                int64_t n_cap, const int32_t* q_pos, unsigned* status) {
+  csa::CompressArgs ca = {};
   ca.mode = mode;
   ca.B = B;
   ca.m = p->m;
@@ -243,6 +242,18 @@ csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new,
   ca.rope_theta = static_cast<double>(p->rope_theta);
   ca.rms_eps = p->rms_eps;
   ca.status = status;
+  return ca;
+}
+
+csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,
+                        const uint16_t* Ca, const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
+                        const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
+                        const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
+                        int64_t n_cap, const int32_t* q_pos, cudaStream_t st) {
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  const csa::CompressArgs ca = compress_args(p, mode, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb,
+                                             rms_w, kv_out, kv_stride_b, n_cap, q_pos, status);
   return cuda_status(csa::launch_compress(ca, st));
 }
 
@@ -397,14 +408,24 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   IndexWs w;
   if (!index_workspace(B, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
-  // 1. emission of the entry that completes at this step (if any)
+  // the top-k counters are cleared first, so that the four kernels follow
+  // one another directly (programmatic launches)
+  if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  // 1. emission of the entry that completes at this step (if any).  Only the
+  //    attention reads it, so it is computed by extra CTAs of the top-k launch
+  //    where that kernel can carry it, else by its own kernel first.
+  const csa::CompressArgs ca = compress_args(p, 1, B, 1, 0, ring_Ca, ring_Za, ring_Cb, ring_Zb, nullptr, nullptr, Ba,
+                                             Bb, rms_w, kv_comp, n_cap * csa::kDim, n_cap, q_pos, status);
+  const bool ride_along = csa::topk_can_carry_compress(p->m);
   trace(0, st);
-  s = run_compress(p, 1, B, 1, 0, ring_Ca, ring_Za, ring_Cb, ring_Zb, nullptr, nullptr, Ba, Bb, rms_w, kv_comp,
-                   n_cap * csa::kDim, n_cap, q_pos, st);
-  if (s != CSA_OK) return s;
+  if (!ride_along && (s = cuda_status(csa::launch_compress(ca, st))) != CSA_OK) return s;
   trace(1, st);
   // 2. indexer + top-k over the visible entries
-  s = run_index_topk(p, B, 1, q_pos, 0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st, true);
+  s = run_index_topk(p, B, 1, q_pos, 0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st, true,
+                     true, ride_along ? &ca : nullptr);
   if (s != CSA_OK) return s;
   trace(3, st);
   // 3. sparse attention over the window ring and the selection
@@ -440,6 +461,8 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   IndexWs w;
   if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+  if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
+    return CSA_ERR_CUDA;
   trace(0, st);
   // 1. compress the chunk's complete blocks.  Rows are [B][Q][D]; the
   //    compressor reads m*n_new of them per sequence with a stride of Q rows.
@@ -464,7 +487,7 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   trace(1, st);
   // 2. indexer + top-k, each query over its own V(t)
   s = run_index_topk(p, B, Q, nullptr, pos0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st,
-                     true);
+                     true, true);
   if (s != CSA_OK) return s;
   trace(3, st);
   // 3. sparse attention with the linear window (row j = position pos0-(W-1)+j)

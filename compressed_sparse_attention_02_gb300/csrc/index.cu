@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   using Cfg = IndexCfg<QPC>;
   constexpr int N = Cfg::N;
   constexpr int STAGES = Cfg::STAGES;
+  pdl_launch_dependents();
+  pdl_wait();  // before any global access and before TMEM is taken
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -409,9 +411,8 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   // One wave of CTAs that all stay resident; each takes an equal range.
   int64_t ctas = static_cast<int64_t>(sms) * per_sm;
   if (ctas > units) ctas = units;
-  index_score_kernel<QPC><<<static_cast<unsigned>(ctas), Cfg::THREADS, Cfg::SMEM, stream>>>(
-      tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
-  return counted(cudaGetLastError());
+  return launch_pdl(index_score_kernel<QPC>, dim3(static_cast<unsigned>(ctas)), dim3(Cfg::THREADS), Cfg::SMEM,
+                    stream, tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
 }
 
 }  // namespace

@@ -17,6 +17,27 @@ inline cudaError_t counted(cudaError_t e) {
   return e;
 }
 
+// Launches a kernel with programmatic stream serialization: it may start (and
+// wait in pdl_wait) while the kernel before it in the stream finishes, which
+// hides the launch gap between the stages.  Every kernel of this library
+// calls pdl_launch_dependents() and then pdl_wait() before its first global
+// memory access, so stream order holds for all data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...));
+}
+
 // Fixed model dimensions the kernels are specialised for.
 constexpr int kHeads = 64;      // query heads
 constexpr int kDim = 512;       // shared K=V latent width
@@ -86,7 +107,11 @@ struct TopkArgs {
 };
 // Words per row of the top-k position bitmaps (a multiple of 4).
 int64_t topk_bits_ld(int64_t n_cap);
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+// ride_along: optional decode-mode (mode 1) compressor arguments for the same
+// B sequences, computed by extra CTAs of the same launch (m for which
+// topk_can_carry_compress holds).
+bool topk_can_carry_compress(int m);
+cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream);
 
 // ---- sparse attention (tcgen05, bf16) ------------------------------------------------
 struct AttnArgs {

@@ -75,6 +75,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// A kernel launched with programmatic stream serialization may be scheduled
+// once every CTA of the kernel before it has signalled (or exited); it must
+// wait for that kernel's completion before touching global memory.  Both
+// are no-ops for a kernel launched without the attribute.
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- proxy fences -----------------------------------------------------------
 
 // Makes generic-proxy shared-memory writes visible to the async proxy (TMA,

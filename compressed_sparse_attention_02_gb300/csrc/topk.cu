@@ -26,6 +26,10 @@
 // When d* alone holds exactly the keys still needed, the filter selects all of
 // d* and the finish only reads the bitmap out.  A row whose candidate list
 // overflows is resolved from its scores in global memory (slower, exact).
+//
+// A decode step's compressor entry (compress.cuh) can ride along: one extra
+// CTA per sequence computes it, so its latency hides behind the selection.
+#include "compress.cuh"
 #include "keys.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -69,6 +73,7 @@ struct __align__(16) Smem {
   } h;
   int wsum[kWarps];
   int wval[kWarps];
+  float red[kWarps];
   int wtotal;
   Crossing out;
   int n_local, cand_base, last, nx;
@@ -326,8 +331,26 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a) {
+// The compressor entry of sequence b, 2 channels per thread (m <= 4: the
+// m = 8 routine would not fit this kernel's register budget).
+__device__ void compress_ride_along(const CompressArgs& c, int b, Smem& sm) {
+  const auto sync = [] { __syncthreads(); };
+  switch (c.m) {
+    case 1: compress_entry<1, 2>(c, b, 0, threadIdx.x, sm.red, sync); break;
+    case 2: compress_entry<2, 2>(c, b, 0, threadIdx.x, sm.red, sync); break;
+    case 4: compress_entry<4, 2>(c, b, 0, threadIdx.x, sm.red, sync); break;
+    default: break;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, const CompressArgs comp) {
   __shared__ Smem sm;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (comp.B > 0 && blockIdx.x == gridDim.x - 1) {  // the extra column: compressor entries
+    if (blockIdx.y == 0) compress_ride_along(comp, blockIdx.z, sm);
+    return;
+  }
   const int b = blockIdx.z, q = blockIdx.y;
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   const int64_t V = visible_entries(a, b, q);
@@ -434,14 +457,22 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a) {
 
 }  // namespace
 
+bool topk_can_carry_compress(int m) { return m == 1 || m == 2 || m == 4; }
+
 int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + kEmitWords - 1) / kEmitWords * kEmitWords; }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
   if (a.cand_cap > kTopkCandCap) return cudaErrorInvalidValue;
-  const int64_t chunks = (a.n_cap + kItems - 1) / kItems;
-  topk_kernel<<<dim3(static_cast<unsigned>(chunks), a.Q, a.B), kThreads, 0, stream>>>(a);
-  return counted(cudaGetLastError());
+  CompressArgs c = {};
+  if (ride_along) {
+    if (ride_along->mode != 1 || ride_along->B != a.B || !topk_can_carry_compress(ride_along->m))
+      return cudaErrorInvalidValue;
+    c = *ride_along;
+    fill_inv_freq(&c);
+  }
+  const int64_t chunks = (a.n_cap + kItems - 1) / kItems + (ride_along ? 1 : 0);
+  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(chunks), a.Q, a.B), dim3(kThreads), 0, stream, a, c);
 }
 
 }  // namespace csa

@@ -123,3 +123,47 @@ def test_full_size_decode_configs_sampled(csa, cfg, samples):
     idx, sc = run(csa, p, x["qI"], x["wI"], kI, pos, w.n_cap)
     for b in samples:
         check_row(idx[b, 0], sc[b, 0], x["qI"][b, 0], x["wI"][b, 0], kI[b], w.t, w.topk, what="c%d b=%d" % (cfg, b))
+
+
+def periodic_keys(seed, n_cap, period):
+    base = syn.indexer_keys(seed, 1, period)
+    return base.view(torch.uint8)[:, torch.arange(n_cap) % period].contiguous().view(torch.float8_e4m3fn)
+
+
+@pytest.mark.parametrize("period,k", [(1, 512), (5, 700), (37, 300)])
+def test_repeated_scores_over_a_long_row(csa, period, k):
+    """20000 visible entries (five 4096-entry chunks) whose keys repeat with a
+    short period, so each score occurs 20000/period times exactly: with period
+    1 every score is equal (the whole row competes in one digit, past every
+    candidate buffer, and the k lowest positions win); periods 5 and 37 put
+    thousands or hundreds of equal keys at the threshold across chunk
+    boundaries."""
+    n_cap = 20000
+    x = syn.indexer_query(6, 1, 1)
+    kI = periodic_keys(6, n_cap, period)
+    p = csa.csa_default_params(topk=k)
+    t = 4 * n_cap - 1
+    idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
+    check_row(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, what="period %d" % period)
+    if period == 1:
+        assert np.array_equal(idx[0, 0], np.arange(k)), "equal scores: the k lowest positions"
+
+
+def test_selection_is_exactly_the_keys_of_one_score(csa):
+    """Two distinct keys over 20000 entries: the higher-scoring one at every
+    16th position (1250 entries) and k = 1250, so the selection is exactly
+    those positions and nothing at the threshold is left over."""
+    n_cap, k = 20000, 1250
+    x = syn.indexer_query(7, 1, 1)
+    two = syn.indexer_keys(7, 1, 2)
+    s2 = oracle.index_scores(bits(x["qI"][0, 0]), bits(x["wI"][0, 0]), bits(two[0]))
+    assert s2[0] != s2[1]
+    hi, lo = (0, 1) if s2[0] > s2[1] else (1, 0)
+    pick = torch.full((n_cap,), lo, dtype=torch.long)
+    pick[::16] = hi
+    kI = two.view(torch.uint8)[:, pick].contiguous().view(torch.float8_e4m3fn)
+    p = csa.csa_default_params(topk=k)
+    t = 4 * n_cap - 1
+    idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
+    assert np.array_equal(idx[0, 0], np.arange(0, n_cap, 16))
+    check_row(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, what="one score")

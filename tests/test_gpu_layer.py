@@ -62,6 +62,21 @@ def test_layer_decode(csa, cfg, samples):
         check_decode_seq(w, x, b, bits(x["kv"][b]), kv[b].float().cpu().numpy(), idx[b], out[b], lse[b])
 
 
+@pytest.mark.parametrize("m,t", [(1, 299), (2, 599), (8, 2399), (8, 2395), (4, 3)])
+def test_layer_decode_other_compression_ratios(csa, m, t):
+    """Decode steps for m = 1, 2 and 8 (the emitted entry is computed inside
+    the top-k launch for m <= 4 and by its own kernel for m = 8), a step that
+    emits nothing (t+1 not a multiple of m) and one at the very first block
+    (no previous block, fewer visible entries than k)."""
+    w = syn.Workload("decode-m%d" % m, 0, "decode", B=3, t=t, topk=64, n_cap=400, m=m)
+    x = syn.decode_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=w.topk, m=m)
+    kv = x["kv"].clone()
+    idx, out, lse = run_decode(csa, p, w, x, kv)
+    for b in range(w.B):
+        check_decode_seq(w, x, b, bits(x["kv"][b]), kv[b].float().cpu().numpy(), idx[b], out[b], lse[b])
+
+
 def test_layer_decode_v4flash_cache_from_the_compressor(csa):
     """Batch 32 x 8192 tokens: the cache is built by the bulk compressor over
     the whole context, then one decode step at t = 8191 re-emits the last
