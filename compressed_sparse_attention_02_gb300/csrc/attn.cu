@@ -5,29 +5,34 @@
 // 预算检索" §9.5–9.6; flash-style running max / running sum with a fused sink
 // ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §19.3).
 //
-// One CTA of 8 warps per query (or per half of the heads, below).  The 64
-// heads share every K=V row, so both products run with the gathered rows on
-// the MMA's M side:
+// A query's rows are shared by `split` CTAs (1, 2, 4 or 8; a thread-block
+// cluster when above 1), each holding all 64 heads and a contiguous slice of
+// the query's row set.  The 64 heads share every K=V row, so both products
+// run with the gathered rows on the MMA's M side:
 //   S^T[row, head]  = KV_tile[128 x 512] . Q^T[512 x 64]   (K-major A and B)
 //   O^T[ch, head]  += V^T[512 x 128] . P^T[128 x 64]       (MN-major A and B)
 // The same 128-byte-swizzled KV tile in shared memory serves as the K-major A
 // operand of the first product and the MN-major A operand of the second.  S^T
 // (64 TMEM columns) and O^T (4 x 64 columns, one per 128-channel block) live in
 // TMEM.  Two warps share each TMEM lane quadrant (32 tile rows) and split the
-// CTA's heads between them: a thread owns one tile row and half the heads,
-// reads their logits with one tcgen05.ld, and per-head maxima and sums over
-// rows use a warp reduce-scatter plus a 4-quadrant combine in shared memory.
-// The reference maximum only moves when a tile exceeds it by more than 2^8,
-// so O^T is rarely rescaled; the final division uses the same reference, so
-// the result does not depend on when it moved.
+// heads between them: a thread owns one tile row and 32 heads, reads their
+// logits with one tcgen05.ld, and per-head maxima and sums over rows use a
+// warp reduce-scatter plus a 4-quadrant combine in shared memory.  The
+// reference maximum only moves when a tile exceeds it by more than 2^8, so
+// O^T is rarely rescaled; the final division uses the same reference, so the
+// result does not depend on when it moved.
 //
-// Decode (few queries) runs NH = 32 heads per CTA, two CTAs per query, so
-// twice as many SMs share the per-query work; prefill runs all 64 heads per
-// CTA (its rows then cross L2 once per query).  At start every CTA asks L2 to
-// prefetch all of its query's rows (cp.async.bulk.prefetch.L2), so the HBM
-// reads of the whole batch are in flight at once and the tile gathers that
-// follow mostly hit L2.  With NH = 32 the P tile keeps its 64-head layout with
-// the upper 32 columns zero, so both MMAs use the same operand layouts.
+// With split > 1 each CTA ends with its slice's (O^T, reference max, sum) per
+// head.  The cluster combines them through distributed shared memory: every
+// CTA reads all CTAs' maxima and sums, scales its own O^T by its share of the
+// joint softmax (sink included once), stages it as fp32 in its (now free) KV
+// buffer, and then sums one channel slice over the cluster's buffers and
+// writes it.  Decode (few queries) splits so that about one CTA per SM runs;
+// every row is then gathered once.  Prefill runs one CTA per query.
+//
+// Before its first tile every CTA asks L2 for all of its rows (plain line
+// prefetches), so the HBM reads of the whole batch are in flight at once and
+// the tile gathers that follow mostly hit L2.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -46,14 +51,21 @@ constexpr uint32_t kOCol = 64;                            // O^T columns start h
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleSlack = 8.0f;                     // log2 units
 
-template <int NH>
-constexpr size_t smem_bytes() {
-  return 1024 + NH * kDim * 2 + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
-         4 * kHeads * 4 + 64;
-}
+constexpr uint32_t kQBytes = kHeads * kDim * 2;           // 64 KiB: [8 blocks][64 heads][128 B]
+constexpr uint32_t kQBlock = kHeads * 128;                // 8 KiB per 64-channel block of Q
+constexpr int HW = kHeads / 2;                            // heads per warp (two warps share a TMEM quadrant)
+constexpr int kMaxSplit = 4;  // the exchange below needs 2*(split-1)/split of 192 KiB
+static_assert(kKVBytes == kHeads * kDim * 4, "the KV buffer stages the fp32 partial output");
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+constexpr size_t kSmemBytes = 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
+                              4 * kHeads * 4 + 2 * kMaxSplit * kHeads * 4 + 64;
+static_assert(kQBytes + kKVBytes == 192 * 1024, "the output exchange uses the Q and KV buffers");
+
+// Asks L2 to fetch one 1 KiB row: eight 128-byte lines, plain prefetches
+// (cheap to issue from every thread, unlike one bulk prefetch per row).
+__device__ __forceinline__ void prefetch_row_l2(const uint16_t* row) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c * 64) : "memory");
 }
 
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block.
@@ -61,16 +73,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Reduce-scatter of N (16 or 32) per-thread values across a warp: afterwards
-// lane l holds in v[0] the reduction over all 32 lanes of value l >> (5 -
-// log2 N) (lanes that share that index hold the same result).
-template <int N, bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N]) {
+// Reduce-scatter of 32 per-thread values across a warp: afterwards lane l
+// holds in v[0] the reduction over all 32 lanes of value l.
+template <bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
   const int lane = threadIdx.x & 31;
-  constexpr int kSteps = N == 32 ? 5 : 4;  // log2 N
 #pragma unroll
-  for (int step = 0; step < kSteps; ++step) {
-    const int half = (N / 2) >> step;
+  for (int step = 0; step < 5; ++step) {
+    const int half = 16 >> step;
     const int mask = 16 >> step;
     const bool upper = (lane & mask) != 0;
 #pragma unroll
@@ -81,42 +91,43 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N]) {
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-#pragma unroll
-  for (int mask = 16 >> kSteps; mask > 0; mask >>= 1) {
-    const float recv = __shfl_xor_sync(0xffffffffu, v[0], mask);
-    v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
-  }
 }
 
-template <int NH>
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
-  constexpr int kSplit = kHeads / NH;            // CTAs per query
-  constexpr uint32_t kQBlock = NH * 128;         // bytes of one 64-channel block of Q
-  constexpr int HW = NH / 2;                     // heads per warp (two warps share a TMEM quadrant)
-  constexpr int kShift = HW == 32 ? 0 : 1;       // lane -> head after a reduce-scatter of HW values
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a, const int split) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = base;                                          // [8 blocks][NH heads][128 B]
-  uint8_t* kv_s = q_s + NH * kDim * 2;                          // [8 blocks][128 rows][128 B]
+  uint8_t* q_s = base;                                          // [8 blocks][64 heads][128 B]
+  uint8_t* kv_s = q_s + kQBytes;                                // [8 blocks][128 rows][128 B]
   uint8_t* p_s = kv_s + kKVBytes;                               // [128 rows][64 heads] bf16
   int32_t* sel_s = reinterpret_cast<int32_t*>(p_s + kPBytes);
   const uint16_t** row_src = reinterpret_cast<const uint16_t**>(sel_s + kMaxTopk);  // [128]
-  float* red_s = reinterpret_cast<float*>(row_src + kTileRows);  // [4 row quadrants][NH]
+  float* red_s = reinterpret_cast<float*>(row_src + kTileRows);  // [4 row quadrants][64]
   float* m_ref = red_s + 4 * kHeads;                             // running reference max (log2 units)
   float* l_sum = m_ref + kHeads;                                 // running denominator
   float* alpha = l_sum + kHeads;                                 // per-tile rescale factor
   float* fin = alpha + kHeads;                                   // final per-head output scale
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(fin + kHeads);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  float* ml_s = fin + kHeads;  // [split][2][64]: every slice's reference max and sum (split > 1)
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(ml_s + 2 * kMaxSplit * kHeads);
+  uint64_t* recv_bar = mma_bar + 1;  // incoming output slices (split > 1)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
 
   pdl_launch_dependents();
-  pdl_wait();  // before any global access and before TMEM is taken
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3;                  // TMEM lane quadrant == 32 tile rows
-  const int hw0 = (warp >> 2) * HW;           // first head (within the CTA) of this warp
-  const int qi = blockIdx.x / kSplit;
-  const int h0 = (blockIdx.x % kSplit) * NH;  // first head of this CTA
+  if (split > 1) {
+    if (tid == 0) {  // expects the (split-1) output slices the peers will send
+      mbar_init(recv_bar, 1);
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((split - 1) * (kKVBytes / split)));
+      fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive();  // waited on before the first access to a peer
+  }
+  pdl_wait();  // before any global access and before TMEM is taken
+  const int quad = warp & 3;         // TMEM lane quadrant == 32 tile rows
+  const int hw0 = (warp >> 2) * HW;  // first head of this warp
+  const int qi = blockIdx.x / split;
+  const int rank = blockIdx.x % split;  // == the CTA's rank in its cluster
   const int b = blockIdx.y;
   const int64_t row_q = static_cast<int64_t>(b) * a.Q + qi;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + qi;
@@ -127,24 +138,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     fence_mbar_init();
     flags[1] = 0;
   }
-  if (tid < NH) {
+  if (tid < kHeads) {
     m_ref[tid] = -INFINITY;
     l_sum[tid] = 0.f;
+    fin[tid] = a.sink[tid] * kLog2e;  // the sink logit until the epilogue
   }
 
-  // Q tile of this CTA's heads: [8 channel blocks][NH heads][128 B], swizzled.
+  // Q tile: [8 channel blocks][64 heads][128 B], swizzled.
   {
-    const uint16_t* qg = a.q + (row_q * kHeads + h0) * kDim;
-    for (int ch = tid; ch < NH * kDim / 8; ch += kThreads) {
+    const uint16_t* qg = a.q + row_q * kHeads * kDim;
+    for (int ch = tid; ch < kHeads * kDim / 8; ch += kThreads) {
       const int h = ch >> 6, blk = (ch >> 3) & 7, c = ch & 7;
       cp_async_16(q_s + blk * kQBlock + swz(h, c), qg + h * kDim + blk * 64 + c * 8);
     }
   }
-  if (NH < 64) {  // the P tile's unused head columns stay zero
-    for (int r = tid; r < kTileRows; r += kThreads)
-#pragma unroll
-      for (int c = NH / 8; c < 8; ++c) *reinterpret_cast<uint4*>(p_s + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-  }
+
+  const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
+  const uint16_t* kv_b = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
+  const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
+  // Address of window row j (0 <= j < n_swa), null if the window buffer lacks it.
+  auto swa_row = [&](int j) -> const uint16_t* {
+    const int64_t u = t - n_swa + 1 + j;  // window position
+    if (a.swa_mode == 0) return a.swa + (static_cast<int64_t>(b) * a.W + u % a.W) * kDim;
+    const int64_t rr = u - swa_pos0;
+    if (rr >= 0 && rr < a.swa_len) return a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
+    return nullptr;
+  };
 
   // Compact the selected entries (drop -1, flag out-of-range indices).
   {
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     for (int j = lo; j < hi; ++j) {
       const int32_t v = ig[j];
       if (v >= 0 && v < a.n_cap) ++cnt;
-      else if (v != -1 && h0 == 0) record_error(a.status, kErrIndexRange);
+      else if (v != -1 && rank == 0) record_error(a.status, kErrIndexRange);
     }
     int x = cnt;
 #pragma unroll
@@ -174,51 +193,46 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     }
     if (tid == kThreads - 1) flags[0] = before;
   }
-  cp_async_commit_wait_all();
-  fence_proxy_async_smem();
+  __syncthreads();
+  const int n_sel = flags[0];
+  const int n_rows = n_swa + n_sel;
+  // this CTA's slice of the row set [window rows || selected rows]
+  const int per_cta = (n_rows + split - 1) / split;
+  const int r_lo = min(n_rows, rank * per_cta);
+  const int r_hi = min(n_rows, r_lo + per_cta);
+  const int n_tiles = (r_hi - r_lo + kTileRows - 1) / kTileRows;
+  const float scale2 = a.sm_scale * kLog2e;
+
+  // Address of row j of the query's row set (null: absent / skipped).
+  auto row_at = [&](int j) -> const uint16_t* {
+    if (j < n_swa) return swa_row(j);
+    if (j < n_rows) return kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
+    return nullptr;
+  };
+  // Put every row of the slice in flight towards L2.  The Q tile's copies
+  // stay in flight too: the first tile's gather waits for them.
+  for (int j = r_lo + tid; j < r_hi; j += kThreads) {
+    const uint16_t* src = row_at(j);
+    if (src) prefetch_row_l2(src);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tlane = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's TMEM quadrant
-  const int n_sel = flags[0];
-  const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
-  const int n_rows = n_swa + n_sel;
-  const int n_tiles = (n_rows + kTileRows - 1) / kTileRows;
-  const float scale2 = a.sm_scale * kLog2e;
-  const uint16_t* kv_b = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
-  const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
 
-  // Address of row j of this query's row set (null: absent / skipped).
-  auto row_at = [&](int j) -> const uint16_t* {
-    if (j < n_swa) {
-      const int64_t u = t - n_swa + 1 + j;  // window position
-      if (a.swa_mode == 0) return a.swa + (static_cast<int64_t>(b) * a.W + u % a.W) * kDim;
-      const int64_t rr = u - swa_pos0;
-      if (rr >= 0 && rr < a.swa_len) return a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
-      return nullptr;
-    }
-    if (j < n_rows) return kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
-    return nullptr;
-  };
-  // Put every row of this query in flight towards L2 now.
-  for (int j = tid; j < n_rows; j += kThreads) {
-    const uint16_t* src = row_at(j);
-    if (src) prefetch_l2(src, kDim * 2);
-  }
-
-  constexpr uint32_t idesc_s = instr_desc(kTileRows, NH, 1, 1, 0, 0);      // bf16, K-major A/B
+  constexpr uint32_t idesc_s = instr_desc(kTileRows, kHeads, 1, 1, 0, 0);  // bf16, K-major A/B
   constexpr uint32_t idesc_o = instr_desc(kTileRows, kHeads, 1, 1, 1, 1);  // bf16, MN-major A/B
   uint32_t phase = 0;
   bool ok = true;
 
   for (int tile = 0; tile < n_tiles && ok; ++tile) {
-    const int r0 = tile * kTileRows;
+    const int r0 = r_lo + tile * kTileRows;
     // ---- resolve the tile's 128 row addresses
     if (tid < kTileRows) {
       const int j = r0 + tid;
-      const uint16_t* src = row_at(j);
-      if (!src && j < n_swa && h0 == 0) record_error(a.status, kErrIndexRange);
+      const uint16_t* src = j < r_hi ? row_at(j) : nullptr;
+      if (!src && j < n_swa && j < r_hi) record_error(a.status, kErrIndexRange);
       row_src[tid] = src;
     }
     __syncthreads();
@@ -254,35 +268,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     phase ^= 1u;
     tc_fence_after();
 
-    // ---- logits of this thread's row (its warp's HW heads), per-head tile max
+    // ---- logits of this thread's row (its warp's 32 heads), per-head tile max
     const int r = quad * 32 + lane;  // TMEM lane == tile row
     const bool valid = row_src[r] != nullptr;
     float l[HW];
     {
-      if constexpr (HW == 32) {
-        uint32_t v[32];
-        tmem_ld32(tlane + hw0, v);
-        tmem_wait_ld();
+      uint32_t v[32];
+      tmem_ld32(tlane + hw0, v);
+      tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
-      } else {
-        uint32_t v[16];
-        tmem_ld16(tlane + hw0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 16; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
-      }
+      for (int h = 0; h < 32; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
     }
     {
       float tmp[HW];
 #pragma unroll
       for (int h = 0; h < HW; ++h) tmp[h] = l[h];
-      warp_reduce_scatter<HW, true>(tmp);
-      if ((lane & kShift) == 0) red_s[quad * NH + hw0 + (lane >> kShift)] = tmp[0];
+      warp_reduce_scatter<true>(tmp);
+      red_s[quad * kHeads + hw0 + lane] = tmp[0];
     }
     __syncthreads();
-    if (tid < NH) {
-      const float tmax = fmaxf(fmaxf(red_s[tid], red_s[NH + tid]), fmaxf(red_s[2 * NH + tid], red_s[3 * NH + tid]));
+    if (tid < kHeads) {
+      const float tmax = fmaxf(fmaxf(red_s[tid], red_s[kHeads + tid]),
+                               fmaxf(red_s[2 * kHeads + tid], red_s[3 * kHeads + tid]));
       const float mo = m_ref[tid];
       float al = 1.f;
       if (tmax > mo + kRescaleSlack) {  // also taken on the first tile (mo = -inf)
@@ -300,21 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
         const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
-        if constexpr (HW == 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr, v);
-          tmem_wait_ld();
+        uint32_t v[32];
+        tmem_ld32(taddr, v);
+        tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
-          tmem_st32(taddr, v);
-        } else {
-          uint32_t v[16];
-          tmem_ld16(taddr, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
-          tmem_st16(taddr, v);
-        }
+        for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
+        tmem_st32(taddr, v);
       }
       tmem_wait_st();
     }
@@ -338,15 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
         }
         *reinterpret_cast<uint4*>(p_s + swz(r, hw0 / 8 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      warp_reduce_scatter<HW, false>(pf);
+      warp_reduce_scatter<false>(pf);
       __syncthreads();  // everyone is done reading red_s (tile max) and flags
-      if ((lane & kShift) == 0) red_s[quad * NH + hw0 + (lane >> kShift)] = pf[0];
+      red_s[quad * kHeads + hw0 + lane] = pf[0];
     }
     tc_fence_before();
     fence_proxy_async_smem();
     __syncthreads();
-    if (tid < NH) {
-      l_sum[tid] += (red_s[tid] + red_s[NH + tid]) + (red_s[2 * NH + tid] + red_s[3 * NH + tid]);
+    if (tid < kHeads) {
+      l_sum[tid] += (red_s[tid] + red_s[kHeads + tid]) + (red_s[2 * kHeads + tid] + red_s[3 * kHeads + tid]);
       if (tid == 0) flags[1] = 0;
     }
 
@@ -370,51 +368,128 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     tc_fence_after();
     __syncthreads();  // kv_s / p_s may be overwritten by the next tile
   }
+  __syncthreads();
+  const bool live = ok && n_tiles > 0;  // TMEM holds this CTA's O^T
+  uint16_t* og = a.out + row_q * kHeads * kDim;
 
-  // ---- epilogue: out = O^T / (l_sum + 2^(sink*log2e - m_ref))
-  __syncthreads();
-  if (tid < NH) {
-    const float mr = m_ref[tid];
-    const float sk = a.sink[h0 + tid] * kLog2e;
-    const float M = fmaxf(mr, sk);
-    const float keep = mr == -INFINITY ? 0.f : exp2f(mr - M);
-    const float den = l_sum[tid] * keep + exp2f(sk - M);
-    fin[tid] = M == -INFINITY ? 0.f : keep / den;
-    if (a.lse) a.lse[row_q * kHeads + h0 + tid] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
-  }
-  __syncthreads();
-  uint16_t* out_s = reinterpret_cast<uint16_t*>(kv_s);  // [NH heads][512] bf16 staging
-  if (ok && n_tiles > 0) {
+  // ---- epilogue: out = sum over the slices s of O_s^T * 2^(m_s - M) / den,
+  //      M the joint maximum (sink included), den = sum_s l_s 2^(m_s - M) +
+  //      2^(sink*log2e - M).  `share(s, h)` is slice s's factor for head h.
+  auto factors = [&](int h, const float* mvals, const float* lvals, int stride, int n, float* out_f) {
+    const float sk = fin[h];
+    float M = sk;
+    for (int s = 0; s < n; ++s) M = fmaxf(M, mvals[s * stride + h]);
+    float den = M == -INFINITY ? 0.f : exp2f(sk - M);
+    for (int s = 0; s < n; ++s) {
+      const float ms = mvals[s * stride + h];
+      if (ms != -INFINITY) den += lvals[s * stride + h] * exp2f(ms - M);
+    }
+    for (int s = 0; s < n; ++s) {
+      const float ms = mvals[s * stride + h];
+      out_f[s * kHeads + h] = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M) / den;
+    }
+    if (a.lse && rank == 0) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
+  };
+  if (split == 1) {
+    if (tid < kHeads) factors(tid, m_ref, l_sum, 0, 1, alpha);
+    __syncthreads();
+    // O^T from TMEM straight to global: for a head, a warp's lanes hold 32
+    // consecutive channels (one 64-byte store).
 #pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
       const int chn = blk * 128 + quad * 32 + lane;
-      const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
-      if constexpr (HW == 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr, v);
+      uint32_t v[32];
+      if (live) {
+        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
         tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 32; ++h)
-          out_s[(hw0 + h) * kDim + chn] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * fin[hw0 + h]));
-      } else {
-        uint32_t v[16];
-        tmem_ld16(taddr, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 16; ++h)
-          out_s[(hw0 + h) * kDim + chn] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * fin[hw0 + h]));
       }
+#pragma unroll
+      for (int h = 0; h < 32; ++h)
+        og[(hw0 + h) * kDim + chn] =
+            live ? __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * alpha[hw0 + h])) : uint16_t(0);
     }
   } else {
-    for (int e = tid; e < NH * kDim; e += kThreads) out_s[e] = 0;
-  }
-  __syncthreads();
-  {
-    uint4* og = reinterpret_cast<uint4*>(a.out + (row_q * kHeads + h0) * kDim);
-    const uint4* os = reinterpret_cast<const uint4*>(out_s);
-    for (int e = tid; e < NH * kDim / 8; e += kThreads) og[e] = os[e];
+    // Channel slice c (cw channels, whole 128-channel blocks) of the output
+    // belongs to CTA c.  Each CTA stages its raw O^T for the other CTAs'
+    // slices, fp32 [64 heads][cw], in its Q/KV buffers, and one thread sends
+    // each to its owner with a bulk copy; every CTA also sends its (max, sum)
+    // to all.  The owner scales what it receives and its own share (read from
+    // TMEM) by the slices' factors and adds them.  Staging slot of destination
+    // o: o or o-1 (skipping this CTA); receiving slot of source s: split-1 +
+    // (s or s-1).
+    const int cw = kDim / split;
+    const uint32_t slab = kKVBytes / split;  // bytes of one slice
+    uint8_t* xbuf = q_s;                     // [2*(split-1)][slab], Q and KV buffers in turn
+    auto slot = [&](int x) { return x < rank ? x : x - 1; };
+    const int own_blk0 = rank * 4 / split, own_blks = 4 / split;
+    cluster_wait();  // every CTA of the cluster has started
+    if (tid < kHeads) {
+      for (int s = 0; s < split; ++s) {
+        dsmem_st_f32(dsmem_addr(&ml_s[(rank * 2) * kHeads + tid], s), m_ref[tid]);
+        dsmem_st_f32(dsmem_addr(&ml_s[(rank * 2 + 1) * kHeads + tid], s), l_sum[tid]);
+      }
+    }
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      if (blk >= own_blk0 && blk < own_blk0 + own_blks) continue;
+      const int chn = blk * 128 + quad * 32 + lane;
+      const int owner = chn / cw, c = chn - owner * cw;
+      uint32_t v[32];
+      if (live) {
+        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
+        tmem_wait_ld();
+      }
+      float* dst = reinterpret_cast<float*>(xbuf + slot(owner) * slab) + hw0 * cw + c;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) dst[h * cw] = live ? __uint_as_float(v[h]) : 0.f;
+    }
+    fence_proxy_async_smem();
+    cluster_sync();  // all slices done: (max, sum) delivered, staging complete, receiving slots free
+    if (tid == 0) {
+      for (int o = 0; o < split; ++o) {
+        if (o == rank) continue;
+        // in owner o, this CTA's slice lands in receiving slot split-1 + (rank < o ? rank : rank-1)
+        const int rslot = (split - 1) + (rank < o ? rank : rank - 1);
+        bulk_copy_to_cluster(dsmem_addr(xbuf + rslot * slab, o), xbuf + slot(o) * slab, slab,
+                             dsmem_addr(recv_bar, o));
+      }
+      bulk_commit_group();
+    }
+    // every slice's factor per head (alpha is free: [split][64] factors in ml's place)
+    float* fs = red_s;  // [split <= 4][64]
+    if (tid < kHeads) factors(tid, ml_s, ml_s + kHeads, 2 * kHeads, split, fs);
+    // own share from TMEM while the slices travel
+    float acc[2][32];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (k >= own_blks) break;
+      uint32_t v[32];
+      if (live) {
+        tmem_ld32(tlane + kOCol + (own_blk0 + k) * 64 + hw0, v);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) acc[k][h] = live ? __uint_as_float(v[h]) : 0.f;
+    }
+    const bool got = __syncthreads_and(mbar_wait(recv_bar, 0, a.status));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (k >= own_blks) break;
+      const int chn = (own_blk0 + k) * 128 + quad * 32 + lane;
+      const int c = chn - rank * cw;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) acc[k][h] *= fs[rank * kHeads + hw0 + h];
+      for (int s = 0; s < split && got; ++s) {
+        if (s == rank) continue;
+        const float* src = reinterpret_cast<const float*>(xbuf + (split - 1 + slot(s)) * slab) + hw0 * cw + c;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) acc[k][h] = fmaf(src[h * cw], fs[s * kHeads + hw0 + h], acc[k][h]);
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[k][h]));
+    }
+    if (tid == 0) bulk_wait_all();  // this CTA's sends have left its shared memory
+    cluster_sync();                 // and every CTA has received before any leaves
   }
 
   // A timed-out wait leaves MMAs possibly in flight: give them a bounded
@@ -428,13 +503,39 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   }
 }
 
-template <int NH>
-cudaError_t launch_nh(const AttnArgs& a, cudaStream_t stream) {
-  constexpr size_t smem = smem_bytes<NH>();
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return launch_pdl(sparse_attn_kernel<NH>, dim3(a.Q * (kHeads / NH), a.B), dim3(kThreads), smem, stream, a);
+// The largest cluster size (a power of two up to kMaxSplit) that the device
+// can schedule for this kernel at all, found once per device.
+int max_split(int dev) {
+  constexpr int kDevices = 64;
+  static int cached[kDevices] = {};
+  if (dev >= 0 && dev < kDevices && cached[dev] > 0) return cached[dev];
+  int split = kMaxSplit;
+  for (; split > 1; split /= 2) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_attn_kernel, &cfg) == cudaSuccess && n > 0) break;
+    cudaGetLastError();  // a refused size is not an error of the launch
+  }
+  if (dev >= 0 && dev < kDevices) cached[dev] = split;
+  return split;
+}
+
+// CTAs per query: enough that the launch covers about one CTA per SM, at
+// most what a cluster allows, a divisor of the 512 channels.
+int choose_split(int64_t queries, int sms, int limit) {
+  int split = 1;
+  while (split < limit && queries * split * 2 <= sms) split *= 2;
+  return split;
 }
 
 }  // namespace
@@ -442,12 +543,15 @@ cudaError_t launch_nh(const AttnArgs& a, cudaStream_t stream) {
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
   (void)encode;  // rows are gathered with cp.async; no tensor map is needed
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  // Few queries: split the heads over two CTAs per query to occupy more SMs.
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (static_cast<int64_t>(a.B) * a.Q < sms) return launch_nh<32>(a, stream);
-  return launch_nh<64>(a, stream);
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int split = choose_split(static_cast<int64_t>(a.B) * a.Q, sms, max_split(dev));
+  return launch_pdl_cluster(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
+                            kSmemBytes, stream, static_cast<unsigned>(split), a, split);
 }
 
 }  // namespace csa

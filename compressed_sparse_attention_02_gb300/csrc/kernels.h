@@ -17,25 +17,36 @@ inline cudaError_t counted(cudaError_t e) {
   return e;
 }
 
-// Launches a kernel with programmatic stream serialization: it may start (and
+// Launches a kernel with programmatic stream serialization (and, for
+// cluster_x > 1, in clusters of cluster_x CTAs along x): it may start (and
 // wait in pdl_wait) while the kernel before it in the stream finishes, which
 // hides the launch gap between the stages.  Every kernel of this library
 // calls pdl_launch_dependents() and then pdl_wait() before its first global
 // memory access, so stream order holds for all data.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                              Args&&... args) {
-  cudaLaunchAttribute attr[1];
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
   return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...));
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, stream, 1u, static_cast<Args&&>(args)...);
 }
 
 // Fixed model dimensions the kernels are specialised for.
