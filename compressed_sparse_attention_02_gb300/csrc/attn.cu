@@ -93,7 +93,8 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a, const int split) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a, const int split) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = base;                                          // [8 blocks][64 heads][128 B]
@@ -109,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   float* ml_s = fin + kHeads;  // [split][2][64]: every slice's reference max and sum (split > 1)
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(ml_s + 2 * kMaxSplit * kHeads);
   uint64_t* recv_bar = mma_bar + 1;  // incoming output slices (split > 1)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  uint64_t* q_full = recv_bar + 1;   // the Q tile (TMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
 
   pdl_launch_dependents();
@@ -135,22 +137,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
     mbar_init(mma_bar, 1);
+    mbar_init(q_full, 1);
     fence_mbar_init();
     flags[1] = 0;
+    // Q tile: 8 boxes of [64 heads][64 channels] into [8 blocks][64 heads][128 B], swizzled
+    prefetch_tensormap(&tm_q);
+    mbar_arrive_expect_tx(q_full, kHeads * kDim * 2);
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk)
+      tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
   }
   if (tid < kHeads) {
     m_ref[tid] = -INFINITY;
     l_sum[tid] = 0.f;
     fin[tid] = a.sink[tid] * kLog2e;  // the sink logit until the epilogue
-  }
-
-  // Q tile: [8 channel blocks][64 heads][128 B], swizzled.
-  {
-    const uint16_t* qg = a.q + row_q * kHeads * kDim;
-    for (int ch = tid; ch < kHeads * kDim / 8; ch += kThreads) {
-      const int h = ch >> 6, blk = (ch >> 3) & 7, c = ch & 7;
-      cp_async_16(q_s + blk * kQBlock + swz(h, c), qg + h * kDim + blk * 64 + c * 8);
-    }
   }
 
   const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
@@ -209,8 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     if (j < n_rows) return kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
     return nullptr;
   };
-  // Put every row of the slice in flight towards L2.  The Q tile's copies
-  // stay in flight too: the first tile's gather waits for them.
+  // Put every row of the slice in flight towards L2.
   for (int j = r_lo + tid; j < r_hi; j += kThreads) {
     const uint16_t* src = row_at(j);
     if (src) prefetch_row_l2(src);
@@ -236,16 +235,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       row_src[tid] = src;
     }
     __syncthreads();
-    // ---- gather 128 rows (16-byte cp.async, a warp covers 512 contiguous bytes)
-    for (int ch = tid; ch < kTileRows * 64; ch += kThreads) {
-      const int r = ch >> 6, blk = (ch >> 3) & 7, c = ch & 7;
-      const uint16_t* src = row_src[r];
-      uint8_t* dst = kv_s + blk * kKVBlock + swz(r, c);
-      if (src) cp_async_16(dst, src + blk * 64 + c * 8);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    // ---- gather 128 rows: thread tid copies 16-byte chunk (tid & 7) of
+    //      channel block (tid >> 3) & 7 of rows (tid >> 6) + 4i, so a warp
+    //      covers 512 contiguous bytes of a row
+    {
+      const int pblk = (tid >> 3) & 7, pc = tid & 7;
+      uint8_t* blk_s = kv_s + pblk * kKVBlock;
+#pragma unroll
+      for (int i = 0; i < kTileRows * 64 / kThreads; ++i) {
+        const int r = (tid >> 6) + i * (kThreads / 64);
+        const uint16_t* src = row_src[r];
+        uint8_t* dst = blk_s + swz(r, pc);
+        if (src) cp_async_16(dst, src + pblk * 64 + pc * 8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     cp_async_commit_wait_all();
     fence_proxy_async_smem();
+    if (tile == 0 && !__syncthreads_and(mbar_wait(q_full, 0, a.status))) {  // Q has landed
+      ok = false;
+      break;
+    }
     __syncthreads();
 
     // ---- S^T = KV . Q^T  (32 MMAs of K = 16)
@@ -369,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
     __syncthreads();  // kv_s / p_s may be overwritten by the next tile
   }
   __syncthreads();
+  // with no tile the Q tile's copy may still be in flight: its buffer is reused below
+  if (n_tiles == 0 && !__syncthreads_and(mbar_wait(q_full, 0, a.status))) ok = false;
   const bool live = ok && n_tiles > 0;  // TMEM holds this CTA's O^T
   uint16_t* og = a.out + row_q * kHeads * kDim;
 
@@ -541,8 +553,20 @@ int choose_split(int64_t queries, int sms, int limit) {
 }  // namespace
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
-  (void)encode;  // rows are gathered with cp.async; no tensor map is needed
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
+  // q: [B*Q*64 rows][512 bf16]; a box is one 64-channel block of one query's 64 heads
+  CUtensorMap tm_q;
+  {
+    cuuint64_t dim[2] = {static_cast<cuuint64_t>(kDim),
+                         static_cast<cuuint64_t>(a.B) * static_cast<cuuint64_t>(a.Q) * kHeads};
+    cuuint64_t stride[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kHeads)};
+    cuuint32_t ones[2] = {1, 1};
+    if (!encode || encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q), dim, stride, box,
+                          ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -551,7 +575,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
   if (e != cudaSuccess) return e;
   const int split = choose_split(static_cast<int64_t>(a.B) * a.Q, sms, max_split(dev));
   return launch_pdl_cluster(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
-                            kSmemBytes, stream, static_cast<unsigned>(split), a, split);
+                            kSmemBytes, stream, static_cast<unsigned>(split), tm_q, a, split);
 }
 
 }  // namespace csa
