@@ -206,6 +206,8 @@ def run_ours(args, rank, world, local_rank):
         result["clocks"] = clocks.summary()
     if rank == 0 and not args.no_extras:
         result.update(stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args))
+        result["attn"].update(attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream))
+        result["prefill"] = prefill_profile(csa, torch, dev)
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -238,16 +240,101 @@ def stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, a
     return {
         "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic, "peak_source": src,
+                     "frac_of_nominal_8000": achieved / 8000.0,
                      "algorithmic_bytes_per_launch": idx_bytes, "avg_launch_ms": idx_ms},
         # the decode step's compressor entry rides in the top-k launch (m <= 4),
         # so its own stage is empty and "topk" includes it
         "stages_ms": {"compress_emit": mean[0], "index_scores": mean[1], "topk": mean[2], "sparse_attn": mean[3],
                       "traced_steps": n, "note": "events between stages break the programmatic overlap"},
-        "attn": {"tflops": attn_flops / (attn_ms * 1e-3) / 1e12, "tc_frac_of_bf16_peak":
+        "attn": {"binding_roofline_frac": max(attn_bytes / (hbm * 1e9), attn_flops / (bf16 * 1e12)) / (attn_ms * 1e-3),
+                 "tflops": attn_flops / (attn_ms * 1e-3) / 1e12, "tc_frac_of_bf16_peak":
                  attn_flops / (attn_ms * 1e-3) / 1e12 / bf16, "gbs": attn_bytes / (attn_ms * 1e-3) / 1e9,
                  "hbm_frac": attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm},
         "index_topk_gbs": idx_bytes / ((mean[1] + mean[2]) * 1e-3) / 1e9,
     }
+
+
+def attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream):
+    """The sparse attention alone, repeated on the same selection, so its rows
+    (40 MiB) are L2-resident: the warm-L2 counterpart of the in-step number."""
+    hbm, bf16, _ = peaks()
+    wsa = csa.workspace(csa.CSA_OP_SPARSE_ATTN, p, B, 1, w.n_cap, device=kv.device)
+
+    def attn():
+        csa.csa_sparse_attn(p, B, 1, x["q_pos"], x["q"], kv, w.n_cap, idx, x["swa"], 0, w.W, None, x["sink"], out,
+                            lse, wsa)
+    for _ in range(5):
+        attn()
+    torch.cuda.synchronize()
+    n = 200
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        attn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    V = (w.t + 1) // w.m
+    n_rows = min(w.W, w.t + 1) + min(w.topk, V)
+    flops = B * 4.0 * 64 * 512 * n_rows
+    return {"warm_l2_ms": ms, "warm_l2_tflops": flops / (ms * 1e-3) / 1e12,
+            "warm_l2_tc_frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / bf16}
+
+
+def prefill_profile(csa, torch, dev):
+    """The chunked-prefill layer call of the 64K-context workload (4096 queries
+    at positions 61440..65535 over 16384 entries): stage durations, whole-call
+    time, and the attention's tensor-core rate (prefill attention is where the
+    bf16 tensor peak is the meaningful roofline)."""
+    import synthetic as syn
+    hbm, bf16, _ = peaks()
+    w = syn.WORKLOADS[4]
+    B, Q = w.B, w.Q
+    x = syn.prefill_inputs(w, device=dev)
+    p = csa.csa_default_params(topk=w.topk)
+    kv = x["kv"].clone()
+    idx = torch.empty(B, Q, p.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=dev)
+    ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, x["n_cap"], device=dev)
+
+    def step():
+        csa.csa_layer_prefill(p, B, Q, w.pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"], x["Zb_prev"],
+                              x["Ba"], x["Bb"], x["rms_w"], kv, x["n_cap"], x["kI"], x["qI"], x["wI"], x["q"],
+                              x["swa"], x["sink"], idx, out, lse, ws)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after prefill warm-up")
+    n = 10
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    for i in range(n):
+        csa.csa_set_trace_events(evs[i])
+        step()
+    csa.csa_set_trace_events(None)
+    torch.cuda.synchronize()
+    st = [sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(n)) / n for s in range(4)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    # every query attends its 128 window rows and min(k, V(t)) selected entries
+    rows = sum(min(w.W, t + 1) + min(w.topk, (t + 1) // w.m) for t in range(w.pos0, w.pos0 + Q))
+    attn_flops = B * 4.0 * 64 * 512 * rows
+    pairs = sum(min(x["n_cap"], (t + 1) // w.m) for t in range(w.pos0, w.pos0 + Q))
+    index_flops = B * 2.0 * 64 * 128 * pairs
+    res = {"workload": w.name, "tokens_per_s": B * Q / (ms * 1e-3), "ms_per_call": ms,
+           "stages_ms": {"compress": st[0], "index_scores": st[1], "topk": st[2], "sparse_attn": st[3]},
+           "attn_tflops": attn_flops / (st[3] * 1e-3) / 1e12,
+           "attn_tc_frac_of_bf16_peak": attn_flops / (st[3] * 1e-3) / 1e12 / bf16,
+           "index_fp8_tflops": index_flops / (st[1] * 1e-3) / 1e12}
+    del x, kv, idx, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def _traffic_from_profile():

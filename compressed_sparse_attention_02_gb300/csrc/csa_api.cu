@@ -408,8 +408,8 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   IndexWs w;
   if (!index_workspace(B, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
-  // the top-k counters are cleared first, so that the four kernels follow
-  // one another directly (programmatic launches)
+  // the top-k counters are cleared first, so that the kernels follow one
+  // another directly (programmatic launches)
   if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
   unsigned* status = status_ptr();

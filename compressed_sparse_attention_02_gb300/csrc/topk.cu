@@ -76,7 +76,8 @@ struct __align__(16) Smem {
   float red[kWarps];
   int wtotal;
   Crossing out;
-  int n_local, cand_base, last, nx;
+  int n_local, last, nx;
+  unsigned cand_base;
   uint64_t bar;
 };
 
@@ -238,12 +239,15 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
   int need = a.k - c.above;
   if (threadIdx.x == 0) sm.nx = 0;
   if (c.in_bin != need) {
-    const int nc = static_cast<int>(__ldcg(a.cand_count + row));
+    const unsigned ncu = __ldcg(a.cand_count + row);
     int n_eq = 0;
-    if (nc <= a.cand_cap) {
+    if (ncu <= static_cast<unsigned>(a.cand_cap)) {
+      const int nc = static_cast<int>(ncu);
       for (int i = threadIdx.x; i < nc; i += kThreads) {
-        sm.u.c.ckey[i] = __ldcg(a.cand_key + row * a.cand_cap + i);
-        sm.u.c.cpos[i] = __ldcg(a.cand_idx + row * a.cand_cap + i);
+        const int32_t p = __ldcg(a.cand_idx + row * a.cand_cap + i);
+        const bool ok = p >= 0 && p < V;  // positions come from this row's filter; checked all the same
+        sm.u.c.ckey[i] = ok ? __ldcg(a.cand_key + row * a.cand_cap + i) : 0u;
+        sm.u.c.cpos[i] = ok ? p : 0;
       }
       const uint32_t thr = resolve_threshold(dstar, nc, [&](int64_t i) { return sm.u.c.ckey[i]; }, sm, &need, &n_eq);
       const bool all_eq = n_eq == need;  // every key equal to thr is taken
@@ -430,11 +434,12 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, con
     // a CTA whose list overflowed pushes the row's count past the cap: the
     // finish then counts from the scores
     const unsigned add = n_local > kLocalCap ? static_cast<unsigned>(a.cand_cap) + 1u : static_cast<unsigned>(n_local);
-    if (threadIdx.x == 0) sm.cand_base = static_cast<int>(atomicAdd(a.cand_count + row, add));
+    if (threadIdx.x == 0) sm.cand_base = atomicAdd(a.cand_count + row, add);
     __syncthreads();
-    const int base = sm.cand_base;
+    // unsigned throughout: slots at or past the cap are dropped, whatever the count holds
+    const unsigned base = sm.cand_base, cap = static_cast<unsigned>(a.cand_cap);
     for (int j = threadIdx.x; j < n_local && j < kLocalCap; j += kThreads) {
-      if (base + j < a.cand_cap) {
+      if (base < cap && static_cast<unsigned>(j) < cap - base) {
         a.cand_key[row * a.cand_cap + base + j] = sm.u.f.lkey[j];
         a.cand_idx[row * a.cand_cap + base + j] = sm.u.f.lpos[j];
       }
