@@ -43,6 +43,27 @@ def parse():
     return ap.parse_args()
 
 
+def rank_config(config: int, rank: int) -> int:
+    """Seed base of a rank's inputs: every rank decodes its own sequences."""
+    return config + 100 * rank
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (all ranks call this)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, batch: int, steps: int, ms: float) -> float:
+    """Whole-job queries/s: every rank's batch, per step, over the slowest rank's time."""
+    return world * batch * steps / (ms / 1e3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -129,14 +150,14 @@ def run_ours(args, rank, world, local_rank):
     assert w.kind == "decode"
     B = w.B
     # each rank's batch is its own slice of sequences (seeded per sequence)
-    x = syn.decode_inputs(syn.Workload(w.name, w.config + 100 * rank, w.kind, B=B, t=w.t, topk=w.topk,
+    x = syn.decode_inputs(syn.Workload(w.name, rank_config(w.config, rank), w.kind, B=B, t=w.t, topk=w.topk,
                                        n_cap=w.n_cap, hadamard_kI=w.hadamard_kI), device=dev)
     # Consecutive steps use different queries (QSETS sets, rotated), so each
     # step selects and gathers different cache rows: the selected rows of one
     # step are not left in L2 for the next.
-    qsets = [syn.indexer_query(w.config + 100 * rank + 1000 * r, B, 1, device=dev) for r in range(QSETS)]
+    qsets = [syn.indexer_query(rank_config(w.config, rank) + 1000 * r, B, 1, device=dev) for r in range(QSETS)]
     for r, qs in enumerate(qsets):
-        qs["q"] = syn.main_query(w.config + 100 * rank + 1000 * r, B, 1, device=dev)
+        qs["q"] = syn.main_query(rank_config(w.config, rank) + 1000 * r, B, 1, device=dev)
     p = csa.csa_default_params(topk=w.topk)
     kv = x["kv"]
     idx = torch.empty(B, w.topk, dtype=torch.int32, device=dev)
@@ -183,15 +204,11 @@ def run_ours(args, rank, world, local_rank):
     if clocks:
         clocks.mark()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if clocks:
         clocks.stop()
     result = {
-        "metric": METRIC, "value": world * B * args.steps / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_value(world, B, args.steps, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
         "data": "synthetic (seeded N(0,1) inputs in the pages' shapes; no trained weights)",
