@@ -57,7 +57,7 @@ constexpr int kIdxHeads = 64;   // indexer heads
 constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
-constexpr int kTopkCandCap = 4096;    // crossing-digit candidates a top-k row keeps
+constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k row keeps
 
 // ---- compressor --------------------------------------------------------------
 struct CompressArgs {

@@ -16,13 +16,15 @@
 //           memory and appends them, with their positions, to the row's list
 //           (one global atomic per CTA).
 //   finish  the last CTA of the row to finish its filter (release/acquire on
-//           a per-row counter; no CTA waits for another) resolves the
-//           candidates exactly: two more digits (11 and 10 bits) give the
-//           threshold key; candidates above it are selected, and of those
-//           equal to it the ones at the lowest positions (read in order from
-//           a tie bitmap).  These extra positions are merged into the
-//           bitmap as it is read out in position order, which gives the
-//           ascending output; the selected scores are gathered last.
+//           a per-row counter; no CTA waits for another) loads the row's
+//           bitmap and candidates together and resolves the candidates
+//           exactly: the next 11 bits of their keys give the crossing bin;
+//           when that bin holds at most 32 keys one warp ranks them by (key,
+//           position), else a last 10-bit digit gives the threshold key and
+//           the keys equal to it are taken in position order from a tie
+//           bitmap.  The selected candidates are OR-ed into the bitmap, which
+//           is then read out in position order (the ascending output), and
+//           the selected scores are gathered last.
 // When d* alone holds exactly the keys still needed, the filter selects all of
 // d* and the finish only reads the bitmap out.  A row whose candidate list
 // overflows is resolved from its scores in global memory (slower, exact).
@@ -44,7 +46,7 @@ constexpr int kLocalCap = 2048;  // candidates one CTA gathers before the row fa
 constexpr int kEmitWords = 8;    // bitmap words a thread reads per round of the read-out
 constexpr int kRoundWords = kThreads * kEmitWords;
 static_assert(kItems == 16 * kThreads, "a thread covers half a bitmap word");
-static_assert(kTopkCandCap >= 2 * kLocalCap && kTopkCandCap >= kRoundWords && kRoundWords >= kMaxTopk,
+static_assert(kTopkCandCap == kRoundWords && kLocalCap == kTopkCandCap && kRoundWords >= kMaxTopk,
               "shared-memory reuse");
 
 struct Crossing {
@@ -61,11 +63,9 @@ struct __align__(16) Smem {
     struct {
       uint32_t ckey[kTopkCandCap];  // the row's candidates
       int32_t cpos[kTopkCandCap];
+      uint32_t bm[kRoundWords];     // one read-out round of the row's position bitmap
+      int32_t sel[kMaxTopk];        // the selected positions, ascending
     } c;
-    struct {
-      uint32_t rbuf[kRoundWords];  // extra selected positions of one read-out round
-      int32_t sel[kMaxTopk];       // the selected positions, ascending
-    } e;
   } u;
   union {
     int hist[2048];           // digit counts
@@ -76,9 +76,11 @@ struct __align__(16) Smem {
   float red[kWarps];
   int wtotal;
   Crossing out;
-  int n_local, last, nx;
+  int n_local, last, nx, nsmall;
   unsigned cand_base;
-  uint64_t bar;
+  uint32_t small_key[32];  // the keys of a small crossing bin
+  int32_t small_pos[32];
+  uint64_t hist_bar, vals_bar;
 };
 
 // Exclusive scan over the warps of the block of one value per warp (every
@@ -194,6 +196,13 @@ __device__ __forceinline__ void push_extra(Smem& sm, int32_t pos) {
   if (slot < kMaxTopk) sm.h.xpos[slot] = pos;
 }
 
+// Selects position pos: in the staged first round of the bitmap, or in the
+// list of positions past it (rows longer than kRoundWords words).
+__device__ __forceinline__ void mark(Smem& sm, int32_t pos) {
+  if ((pos >> 5) < kRoundWords) atomicOr(&sm.u.c.bm[pos >> 5], 1u << (pos & 31));
+  else push_extra(sm, pos);
+}
+
 // One bulk async copy global -> shared completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -221,7 +230,7 @@ __device__ void take_ties(const uint32_t* ties, int64_t nwords, int need, Smem& 
     while (word && before < need) {
       const int bit = __ffs(word) - 1;
       word &= word - 1;
-      push_extra(sm, static_cast<int32_t>(w * 32 + bit));
+      mark(sm, static_cast<int32_t>(w * 32 + bit));
       ++before;
     }
     done += total;
@@ -238,6 +247,28 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
   const uint32_t dstar = static_cast<uint32_t>(c.bin);
   int need = a.k - c.above;
   if (threadIdx.x == 0) sm.nx = 0;
+  // Words [w0, w0 + kRoundWords) of the bitmap into sm.u.c.bm, eight
+  // consecutive words per thread (bits_ld is a multiple of 8: the vectors
+  // stay inside the row); words past the row read as zero.
+  auto load_round = [&](int64_t w0) {
+    const int64_t wb = w0 + kEmitWords * threadIdx.x;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (wb < nwords) {
+      lo = __ldcg(reinterpret_cast<const uint4*>(bits + wb));
+      hi = __ldcg(reinterpret_cast<const uint4*>(bits + wb + 4));
+      const uint32_t left = static_cast<uint32_t>(nwords - wb);
+      if (left < 8) {  // the row's last words: the rest of the group is not the row's
+        uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        for (uint32_t e = left; e < 8; ++e) v[e] = 0u;
+        lo = make_uint4(v[0], v[1], v[2], v[3]);
+        hi = make_uint4(v[4], v[5], v[6], v[7]);
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x);
+    dst[0] = lo;
+    dst[1] = hi;
+  };
+  load_round(0);  // in flight with the candidate loads below
   if (c.in_bin != need) {
     const unsigned ncu = __ldcg(a.cand_count + row);
     int n_eq = 0;
@@ -249,15 +280,68 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
         sm.u.c.ckey[i] = ok ? __ldcg(a.cand_key + row * a.cand_cap + i) : 0u;
         sm.u.c.cpos[i] = ok ? p : 0;
       }
-      const uint32_t thr = resolve_threshold(dstar, nc, [&](int64_t i) { return sm.u.c.ckey[i]; }, sm, &need, &n_eq);
-      const bool all_eq = n_eq == need;  // every key equal to thr is taken
-      for (int i = threadIdx.x; i < nc; i += kThreads) {
-        const uint32_t k = sm.u.c.ckey[i];
-        const int p = sm.u.c.cpos[i];
-        if (k > thr || (k == thr && all_eq)) push_extra(sm, p);
-        if (k == thr && !all_eq) atomicOr(ties + (p >> 5), 1u << (p & 31));
+      // the next 11 bits of the candidates' keys
+      for (int i = threadIdx.x; i < 2048; i += kThreads) sm.h.hist[i] = 0;
+      if (threadIdx.x == 0) sm.nsmall = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < nc; i += kThreads)
+        atomicAdd(&sm.h.hist[(sm.u.c.ckey[i] >> 10) & 2047], 1);
+      __syncthreads();
+      const Crossing cc = find_crossing(2048, need, sm);
+      const uint32_t p22 = (dstar << 11) | static_cast<uint32_t>(cc.bin);  // the crossing bin's top 22 bits
+      const int need2 = need - cc.above;
+      if (cc.in_bin <= 32) {
+        // keys above the bin are taken; the bin's keys are ranked by one warp
+        for (int i = threadIdx.x; i < nc; i += kThreads) {
+          const uint32_t k22 = sm.u.c.ckey[i] >> 10;
+          if (k22 > p22) mark(sm, sm.u.c.cpos[i]);
+          if (k22 == p22) {
+            const int slot = atomicAdd(&sm.nsmall, 1);
+            if (slot < 32) {
+              sm.small_key[slot] = sm.u.c.ckey[i];
+              sm.small_pos[slot] = sm.u.c.cpos[i];
+            }
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+          const int nb = min(sm.nsmall, 32);
+          const bool has = lane < nb;
+          const uint32_t kl = has ? sm.small_key[lane] : 0u;
+          const int32_t pl = has ? sm.small_pos[lane] : 0;
+          int rank = 0;  // keys of the bin before this one: larger, or equal at a smaller position
+          for (int j = 0; j < nb; ++j) {
+            const uint32_t kj = __shfl_sync(0xffffffffu, kl, j);
+            const int32_t pj = __shfl_sync(0xffffffffu, pl, j);
+            rank += (kj > kl) || (kj == kl && pj < pl);
+          }
+          if (has && rank < need2) mark(sm, pl);
+        }
+      } else {
+        // a crowded bin: one more digit (10 bits) gives the threshold key
+        uint32_t thr;
+        {
+          for (int i = threadIdx.x; i < 1024; i += kThreads) sm.h.hist[i] = 0;
+          __syncthreads();
+          for (int i = threadIdx.x; i < nc; i += kThreads) {
+            const uint32_t k = sm.u.c.ckey[i];
+            if ((k >> 10) == p22) atomicAdd(&sm.h.hist[k & 1023], 1);
+          }
+          __syncthreads();
+          const Crossing c2 = find_crossing(1024, need2, sm);
+          thr = (p22 << 10) | static_cast<uint32_t>(c2.bin);
+          need = need2 - c2.above;
+          n_eq = c2.in_bin;
+        }
+        const bool all_eq = n_eq == need;  // every key equal to thr is taken
+        for (int i = threadIdx.x; i < nc; i += kThreads) {
+          const uint32_t k = sm.u.c.ckey[i];
+          const int p = sm.u.c.cpos[i];
+          if (k > thr || (k == thr && all_eq)) mark(sm, p);
+          if (k == thr && !all_eq) atomicOr(ties + (p >> 5), 1u << (p & 31));
+        }
+        if (!all_eq) take_ties(ties, nwords, need, sm);
       }
-      if (!all_eq) take_ties(ties, nwords, need, sm);
     } else {
       // the candidate list overflowed: the same digits counted over the row's scores
       const uint32_t thr =
@@ -267,7 +351,7 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
         const int64_t i = base + threadIdx.x;
         const uint32_t k = i < V ? score_key(__ldg(src + i)) : 0u;
         const bool in = i < V && (k >> kKeyBinShift) == dstar;
-        if (in && (k > thr || (k == thr && all_eq))) push_extra(sm, static_cast<int32_t>(i));
+        if (in && (k > thr || (k == thr && all_eq))) mark(sm, static_cast<int32_t>(i));
         const unsigned em = __ballot_sync(0xffffffffu, in && k == thr && !all_eq);
         if (lane == 0 && em) atomicOr(ties + ((i - lane) >> 5), em);
       }
@@ -275,42 +359,31 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
     }
   }
   __syncthreads();
-  const int nx = min(sm.nx, kMaxTopk);
-  // Read the bitmap out in position order, rounds of 2048 words: eight
-  // consecutive words per thread, the round's extra positions OR-ed in from
-  // shared memory, one block scan per round.
+  const int nx = min(sm.nx, kMaxTopk);  // selected positions past the first round
+  // Read the bitmap out in position order, rounds of kRoundWords words from
+  // shared memory: eight consecutive words per thread, one block scan per
+  // round.  Later rounds (rows longer than 65536 entries) are loaded here and
+  // get their selected candidates from the list.
   int out = 0;
   for (int64_t w0 = 0; w0 < nwords && out < a.k; w0 += kRoundWords) {
-    const int64_t wb = w0 + kEmitWords * threadIdx.x;
-    uint32_t wd[kEmitWords];
-    if (wb < nwords) {  // bits_ld is a multiple of kEmitWords: both vectors stay inside the row
-      const uint4 lo = __ldcg(reinterpret_cast<const uint4*>(bits + wb));
-      const uint4 hi = __ldcg(reinterpret_cast<const uint4*>(bits + wb + 4));
-      wd[0] = lo.x, wd[1] = lo.y, wd[2] = lo.z, wd[3] = lo.w, wd[4] = hi.x, wd[5] = hi.y, wd[6] = hi.z, wd[7] = hi.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < kEmitWords; ++e) wd[e] = 0u;
-    }
-    if (nx > 0) {
-      uint4* rb = reinterpret_cast<uint4*>(sm.u.e.rbuf + kEmitWords * threadIdx.x);
-      rb[0] = make_uint4(0, 0, 0, 0);
-      rb[1] = make_uint4(0, 0, 0, 0);
+    if (w0 > 0) {
+      __syncthreads();  // the previous round is read out
+      load_round(w0);
       __syncthreads();
       for (int j = threadIdx.x; j < nx; j += kThreads) {
         const int32_t p = sm.h.xpos[j];
         const int64_t w = (p >> 5) - w0;
-        if (w >= 0 && w < kRoundWords) atomicOr(sm.u.e.rbuf + w, 1u << (p & 31));
+        if (w >= 0 && w < kRoundWords) atomicOr(&sm.u.c.bm[w], 1u << (p & 31));
       }
       __syncthreads();
-#pragma unroll
-      for (int e = 0; e < kEmitWords; ++e) wd[e] |= sm.u.e.rbuf[kEmitWords * threadIdx.x + e];
     }
+    const int64_t wb = w0 + kEmitWords * threadIdx.x;
+    const uint4 lo = reinterpret_cast<const uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x)[0];
+    const uint4 hi = reinterpret_cast<const uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x)[1];
+    const uint32_t wd[kEmitWords] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     int cnt = 0;
 #pragma unroll
-    for (int e = 0; e < kEmitWords; ++e) {
-      if (wb + e >= nwords) wd[e] = 0u;
-      cnt += __popc(wd[e]);
-    }
+    for (int e = 0; e < kEmitWords; ++e) cnt += __popc(wd[e]);
     int total;
     int slot = out + block_prefix(cnt, sm, &total);
 #pragma unroll
@@ -319,7 +392,7 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
       while (word) {
         const int bit = __ffs(word) - 1;
         word &= word - 1;
-        if (slot < a.k) sm.u.e.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
+        if (slot < a.k) sm.u.c.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
         ++slot;
       }
     }
@@ -329,7 +402,7 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
   int32_t* idx = a.idx_out + row * a.k;
   float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
   for (int j = threadIdx.x; j < a.k; j += kThreads) {
-    const int32_t p = j < out ? sm.u.e.sel[j] : -1;
+    const int32_t p = j < out ? sm.u.c.sel[j] : -1;
     idx[j] = p;
     if (sc) sc[j] = p >= 0 ? __ldg(src + p) + 0.0f : -INFINITY;
   }
@@ -370,19 +443,26 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, con
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kItems;
   if (i0 >= V) return;
   const int n_in = static_cast<int>(min(V - i0, static_cast<int64_t>(kItems)));
-  // the chunk's scores and the row's digit counts, one bulk copy each
+  // the row's digit counts and the chunk's scores, one bulk copy each on
+  // barriers of their own: the crossing search starts once the counts land
   if (threadIdx.x == 0) {
     const uint32_t vbytes = static_cast<uint32_t>((n_in * 4 + 15) & ~15);  // score rows are padded to 16 B
-    mbar_init(&sm.bar, 1);
+    mbar_init(&sm.hist_bar, 1);
+    mbar_init(&sm.vals_bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&sm.bar, vbytes + kKeyBins * 4);
-    bulk_load(sm.u.f.vals, src + i0, vbytes, &sm.bar);
-    bulk_load(sm.h.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.bar);
+    mbar_arrive_expect_tx(&sm.hist_bar, kKeyBins * 4);
+    bulk_load(sm.h.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
+    mbar_arrive_expect_tx(&sm.vals_bar, vbytes);
+    bulk_load(sm.u.f.vals, src + i0, vbytes, &sm.vals_bar);
     sm.n_local = 0;
   }
   __syncthreads();
-  if (!__syncthreads_and(mbar_wait(&sm.bar, 0, a.status))) return;
+  if (!__syncthreads_and(mbar_wait(&sm.hist_bar, 0, a.status))) {
+    mbar_wait(&sm.vals_bar, 0, a.status);  // no copy of ours stays in flight
+    return;
+  }
   const Crossing c = find_crossing(kKeyBins, a.k, sm);
+  if (!__syncthreads_and(mbar_wait(&sm.vals_bar, 0, a.status))) return;
   const uint32_t dstar = static_cast<uint32_t>(c.bin);
   const bool whole = c.in_bin == a.k - c.above;
   const uint32_t dsel = whole ? dstar : dstar + 1;  // keys with digit >= dsel are selected outright
