@@ -40,7 +40,7 @@ class CsaParams(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("swa_window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
-                ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float), ("inverse_rope", ctypes.c_int32)]
 
 
 class CsaError(RuntimeError):

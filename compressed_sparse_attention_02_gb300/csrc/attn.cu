@@ -68,6 +68,26 @@ __device__ __forceinline__ void prefetch_row_l2(const uint16_t* row) {
   for (int c = 0; c < 8; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c * 64) : "memory");
 }
 
+// Inverse partial RoPE of the output: channel chn's pair (D-R+2j, D-R+2j+1)
+// is turned by -t * theta^(-2j/R).  rope_angle gives (sin, cos) of t *
+// theta^(-2j/R), formed and reduced modulo 2*pi in fp64 (positions reach
+// 2^20); inverse_rope turns one value, exchanging it with the pair's other
+// lane (adjacent lanes of a warp: every lane of the warp must call it).
+__device__ __forceinline__ void rope_angle(int chn, int64_t t, const AttnArgs& a, float* s, float* c) {
+  const int j = (chn - (kDim - kRope)) >> 1;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  double phi = static_cast<double>(t) * a.inv_freq[j];
+  phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
+  sincosf(static_cast<float>(phi), s, c);
+}
+
+__device__ __forceinline__ float inverse_rope(float x, int chn, float s, float c) {
+  const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+  // pair (u, v) -> (u cos + v sin, -u sin + v cos)
+  return (chn & 1) ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
+}
+
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
@@ -415,10 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
         tmem_wait_ld();
       }
+      const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
+      float rs = 0.f, rc = 1.f;
+      if (rot) rope_angle(chn, t, a, &rs, &rc);
 #pragma unroll
-      for (int h = 0; h < 32; ++h)
-        og[(hw0 + h) * kDim + chn] =
-            live ? __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * alpha[hw0 + h])) : uint16_t(0);
+      for (int h = 0; h < 32; ++h) {
+        float o = live ? __uint_as_float(v[h]) * alpha[hw0 + h] : 0.f;
+        if (rot) o = inverse_rope(o, chn, rs, rc);
+        og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      }
     }
   } else {
     // Channel slice c (cw channels, whole 128-channel blocks) of the output
@@ -497,8 +522,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 32; ++h) acc[k][h] = fmaf(src[h * cw], fs[s * kHeads + hw0 + h], acc[k][h]);
       }
+      const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
+      float rs = 0.f, rc = 1.f;
+      if (rot) rope_angle(chn, t, a, &rs, &rc);
 #pragma unroll
-      for (int h = 0; h < 32; ++h) og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[k][h]));
+      for (int h = 0; h < 32; ++h) {
+        const float o = rot ? inverse_rope(acc[k][h], chn, rs, rc) : acc[k][h];
+        og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      }
     }
     if (tid == 0) bulk_wait_all();  // this CTA's sends have left its shared memory
     cluster_sync();                 // and every CTA has received before any leaves

@@ -82,6 +82,7 @@ csa_status check_params(const csa_params* p) {
   if (p->topk < 1 || p->topk > csa::kMaxTopk) return CSA_ERR_UNSUPPORTED;
   if (p->swa_window < 1 || p->swa_window > csa::kMaxWindow) return CSA_ERR_UNSUPPORTED;
   if (!(p->rope_theta > 0.f) || !(p->rms_eps >= 0.f) || !isfinite(p->sm_scale)) return CSA_ERR_INVALID_ARG;
+  if (p->inverse_rope != 0 && p->inverse_rope != 1) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 
@@ -211,6 +212,9 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.B = B;
   aa.Q = Q;
   aa.sm_scale = p->sm_scale;
+  aa.inverse_rope = p->inverse_rope;
+  for (int j = 0; j < csa::kRope / 2; ++j)
+    aa.inv_freq[j] = pow(static_cast<double>(p->rope_theta), -2.0 * j / static_cast<double>(csa::kRope));
   aa.status = status;
   return cuda_status(csa::launch_sparse_attn(aa, enc, st));
 }
@@ -295,6 +299,7 @@ void csa_default_params(csa_params* p) {
   p->rope_theta = 10000.f;
   p->rms_eps = 1e-6f;
   p->sm_scale = 0.044194173824159216f;  // 1/sqrt(512)
+  p->inverse_rope = 0;
 }
 
 size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {

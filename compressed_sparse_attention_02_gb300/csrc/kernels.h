@@ -144,6 +144,8 @@ struct AttnArgs {
   float* lse;               // [B][Q][64] or null
   int B, Q;
   float sm_scale;
+  int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
+  double inv_freq[kRope / 2];  // theta^(-2j/R), host fp64
   unsigned* status;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream);

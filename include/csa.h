@@ -68,6 +68,8 @@ typedef struct {
   float rope_theta;   /* RoPE base (1e4)                                      */
   float rms_eps;      /* RMSNorm epsilon (1e-6)                               */
   float sm_scale;     /* logit scale applied to q·kv (1/sqrt(512))            */
+  int32_t inverse_rope; /* 1: rotate the output's last rope_dim channels back
+                           by the query position (see csa_sparse_attn); 0    */
 } csa_params;
 
 /* Fills *p with the V4-Flash CSA values listed above (topk = 512). */
@@ -201,6 +203,13 @@ csa_status csa_index_topk_static(const csa_params *p, int32_t B, int32_t Q,
  *          position outside the buffer records CSA_ERR_INDEX_RANGE and is
  *          skipped.
  * sink   : [64] fp32.   out : [B][Q][64][512] bf16.   lse : [B][Q][64] or NULL.
+ *
+ * With p->inverse_rope = 1 each head's output then gets the inverse of the
+ * RoPE the rows carry, at the query position ([CSA2 详解] §12.1 "Partial RoPE
+ * 与 inverse RoPE"; [KV 压缩] §9.6 kernel note): channels (448+2j, 449+2j)
+ * are rotated by the angle -t * rope_theta^(-2j/64), the same interleaved
+ * pairing and frequencies as the compressor's RoPE.  The layer calls pass
+ * the flag through.  Any value other than 0 or 1 is CSA_ERR_INVALID_ARG.
  */
 csa_status csa_sparse_attn(const csa_params *p, int32_t B, int32_t Q,
                            const int32_t *q_pos, const uint16_t *q,

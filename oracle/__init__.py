@@ -205,6 +205,19 @@ def attend(q, rows, sink, sm_scale):
     return out, lse
 
 
+def inverse_rope(o, t, *, rope_dim=64, theta=1e4) -> np.ndarray:
+    """Inverse partial RoPE of attention outputs ([CSA2 详解] §12.1 "Partial
+    RoPE 与 inverse RoPE"; [KV 压缩] §9.6, the note after the kernel path): the
+    rows carry RoPE on their last rope_dim channels, so a weighted sum of them
+    carries the rotations too; each head's output is turned back by the angle
+    of the query position t, i.e. RoPE at position -t with the same pairs and
+    frequencies.  o [H, D] -> [H, D] float64."""
+    o = np.array(o, dtype=np.float64, copy=True)
+    for h in range(o.shape[0]):
+        o[h] = rope(o[h], rope_dim, theta, -float(t))
+    return o
+
+
 def window_positions(t: int, W: int) -> np.ndarray:
     """Raw window of the query at t: positions max(0, t-W+1) .. t, the current
     token included (reading recorded in the design doc)."""
@@ -219,9 +232,13 @@ def gather_rows(t, idx, kv_comp, swa_row_of, W):
     return np.concatenate([swa_rows, kv_comp[sel]], axis=0)
 
 
-def attend_query(t, q, idx, kv_comp, swa_row_of, sink, *, W=128, sm_scale=1.0 / np.sqrt(512.0)):
+def attend_query(t, q, idx, kv_comp, swa_row_of, sink, *, W=128, sm_scale=1.0 / np.sqrt(512.0),
+                 inverse_rope_out=False, rope_dim=64, theta=1e4):
     rows = gather_rows(t, np.asarray(idx), kv_comp, swa_row_of, W)
-    return attend(q, rows, sink, sm_scale)
+    out, lse = attend(q, rows, sink, sm_scale)
+    if inverse_rope_out:
+        out = inverse_rope(out, t, rope_dim=rope_dim, theta=theta)
+    return out, lse
 
 
 # ---- layer compositions -----------------------------------------------------

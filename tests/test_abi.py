@@ -39,6 +39,7 @@ def test_default_params_and_status_strings(lib):
     assert (p.m, p.n_heads, p.head_dim, p.rope_dim, p.idx_heads, p.idx_dim, p.topk, p.swa_window) == \
         (4, 64, 512, 64, 64, 128, 512, 128)
     assert abs(p.sm_scale - 512 ** -0.5) < 1e-7 and p.rope_theta == 1e4
+    assert p.inverse_rope == 0 and ctypes.sizeof(p) == 12 * 4
     for s in range(7):
         assert lib.csa_status_string(s).startswith(lib.STATUS_NAMES[s])
 
@@ -49,6 +50,8 @@ def test_workspace_sizes(lib):
     assert n >= 64 * 32768 * 4
     assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, p, 8, 1, 262144) >= 8 * 262144 * 4
     bad = lib.csa_default_params(head_dim=256)
+    assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, bad, 1, 1, 1024) == 0
+    bad = lib.csa_default_params(inverse_rope=2)  # a flag: 0 or 1
     assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, bad, 1, 1, 1024) == 0
 
 

@@ -34,7 +34,7 @@ def oracle_ring(p, q, kv, idx, swa, sink, t):
     W = p.swa_window
     ring = bits(swa)
     return oracle.attend_query(t, bits(q), np.asarray(idx), bits(kv), lambda u: ring[u % W], bits(sink), W=W,
-                               sm_scale=p.sm_scale)
+                               sm_scale=p.sm_scale, inverse_rope_out=bool(p.inverse_rope), theta=p.rope_theta)
 
 
 def test_tiny_decode_config_with_oracle_selection(csa):
@@ -166,3 +166,38 @@ def test_linear_window_many_queries(csa):
                                        lambda u: lin[u - (pos0 - (W - 1))], bits(x["sink"]), W=W,
                                        sm_scale=p.sm_scale)
             assert_close(out[b, j].float().cpu().numpy(), o, "b=%d q=%d" % (b, j))
+
+
+@pytest.mark.parametrize("B", [2, 96])
+def test_inverse_rope_epilogue(csa, B):
+    """The output's last 64 channels turned back by the query position: B = 2
+    runs the rows of a query over a cluster (the rotation is applied by the
+    CTA owning those channels), B = 96 one CTA per query; positions up to
+    2^20 - 1 exercise the angle reduction."""
+    n_cap, k = 300, 64
+    w = syn.Workload("inv-rope", 11, "decode", B=B, t=1199, topk=k, n_cap=n_cap)
+    x = syn.decode_inputs(w)
+    p = csa.csa_default_params(topk=k)
+    p.inverse_rope = 1
+    pos = [1199 if b % 2 == 0 else (1 << 20) - 1 - 7 * b for b in range(B)]
+    rng = np.random.default_rng(3)
+    sel = np.stack([np.sort(rng.choice(n_cap, k, replace=False)).astype(np.int32) for _ in range(B)])
+    out, lse = run_ring(csa, p, x["q"], x["kv"], torch.from_numpy(sel).view(B, 1, k), x["swa"], x["sink"], pos)
+    assert csa.csa_check_status() == 0
+    for b in sorted({0, 1, B - 1}):
+        o, l = oracle_ring(p, x["q"][b, 0], x["kv"][b], sel[b], x["swa"][b], x["sink"], pos[b])
+        assert_close(out[b, 0].float().cpu().numpy(), o, "inverse rope b=%d" % b)
+        np.testing.assert_allclose(lse[b, 0].cpu().numpy(), l, rtol=1e-3, atol=1e-3)
+
+
+def test_inverse_rope_flag_is_validated(csa):
+    p = csa.csa_default_params()
+    p.inverse_rope = 2
+    out = torch.empty(1, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(csa.CsaError):
+        csa.csa_sparse_attn(p, 1, 1, torch.zeros(1, 1, dtype=torch.int32, device=DEV),
+                            torch.zeros(1, 1, 64, 512, dtype=torch.bfloat16, device=DEV),
+                            torch.zeros(1, 16, 512, dtype=torch.bfloat16, device=DEV), 16,
+                            torch.full((1, 1, p.topk), -1, dtype=torch.int32, device=DEV),
+                            torch.zeros(1, 128, 512, dtype=torch.bfloat16, device=DEV), 0, 128, None,
+                            torch.zeros(64, device=DEV), out)

@@ -379,3 +379,38 @@ def test_decode_emission_reads_the_staged_rows_of_blocks_i_and_i_minus_1():
             rope_dim=16)
         i = (t + 1) // m - 1
         np.testing.assert_array_equal(kv_after[i], oracle.f64_to_bf16_bits(bulk[i]))
+
+
+# ---- inverse partial RoPE ([CSA2 详解] §12.1) -----------------------------------
+
+@pytest.mark.parametrize("t", [0, 1, 777, 131071, 1 << 20])
+def test_inverse_rope_undoes_rope_at_the_same_position(t):
+    rng = np.random.default_rng(5 + t % 97)
+    x = rng.standard_normal((3, 512))
+    rotated = np.stack([oracle.rope(r, 64, 1e4, t) for r in x])
+    back = oracle.inverse_rope(rotated, t)
+    np.testing.assert_allclose(back, x, rtol=0, atol=1e-9)
+
+
+def test_inverse_rope_keeps_the_plain_channels_and_the_pair_norms():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((2, 512))
+    y = oracle.inverse_rope(x, 4321)
+    np.testing.assert_array_equal(y[:, :448], x[:, :448])
+    n0 = x[:, 448:].reshape(2, 32, 2)
+    n1 = y[:, 448:].reshape(2, 32, 2)
+    np.testing.assert_allclose(np.hypot(n1[..., 0], n1[..., 1]), np.hypot(n0[..., 0], n0[..., 1]), atol=1e-12)
+    assert not np.allclose(y[:, 448:], x[:, 448:])
+
+
+def test_inverse_rope_recovers_the_output_of_unrotated_rows():
+    """The page's reason for the step: rows all rotated to the query's
+    position t and summed with any weights give, after the inverse rotation,
+    the same weighted sum of the unrotated rows."""
+    rng = np.random.default_rng(7)
+    t = 90001
+    rows = rng.standard_normal((40, 512))
+    wts = rng.random((64, 40))
+    wts /= wts.sum(1, keepdims=True)
+    rotated = np.stack([oracle.rope(r, 64, 1e4, t) for r in rows])
+    np.testing.assert_allclose(oracle.inverse_rope(wts @ rotated, t), wts @ rows, rtol=0, atol=1e-9)
