@@ -60,6 +60,11 @@ def _load():
         lib.orc_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p]
         lib.orc_compress_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
                                            + [_u16p] * 7 + [_f64p])
+        lib.orc_hadamard.argtypes = [ctypes.c_int, _f64p, _f64p]
+        lib.orc_to_e4m3.restype = ctypes.c_uint8
+        lib.orc_to_e4m3.argtypes = [ctypes.c_double]
+        lib.orc_index_key_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
+                                            + [_u16p] * 7 + [_f64p, _u8p])
         lib.orc_visible.restype = ctypes.c_int64
         lib.orc_visible.argtypes = [ctypes.c_int64, ctypes.c_int]
         lib.orc_index_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _f64p]
@@ -203,6 +208,58 @@ def attend(q, rows, sink, sm_scale):
     _load().orc_attend(H, D, rows.shape[0], _ptr(q, _u16p), _ptr(rows, _u16p), _ptr(sink, _f32p),
                        float(sm_scale), _ptr(out, _f64p), _ptr(lse, _f64p))
     return out, lse
+
+
+def hadamard(x) -> np.ndarray:
+    """H_n x / sqrt(n), Sylvester H_n (n = len(x), a power of two)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().orc_hadamard(x.size, _ptr(x, _f64p), _ptr(y, _f64p))
+    return y
+
+
+def to_e4m3(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, saturating at +-448) of doubles."""
+    x = np.asarray(x, dtype=np.float64)
+    lib = _load()
+    return np.array([lib.orc_to_e4m3(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def index_key_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, *, rope_dim=64, theta=1e4, eps=1e-6):
+    """Indexer key entry i ([hca_csa] "CSA：轻压缩 + 稀疏选择"): the compressor's
+    steps at width 128, then H_128/sqrt(128), then E4M3.  Returns (values
+    before rounding [128] f64, codes [128] u8)."""
+    Ca, Za, Ba, Bb, w = (_c(a, np.uint16) for a in (Ca, Za, Ba, Bb, w))
+    m, D = Ca.shape
+    if i > 0:
+        Cb, Zb = _c(Cb, np.uint16), _c(Zb, np.uint16)
+    else:
+        Cb = Zb = None
+    pre = np.empty(D, np.float64)
+    codes = np.empty(D, np.uint8)
+    _load().orc_index_key_entry(m, D, rope_dim, theta, eps, int(i), _ptr(Ca, _u16p), _ptr(Za, _u16p),
+                                _ptr(Cb, _u16p), _ptr(Zb, _u16p), _ptr(Ba, _u16p), _ptr(Bb, _u16p), _ptr(w, _u16p),
+                                _ptr(pre, _f64p), _ptr(codes, _u8p))
+    return pre, codes
+
+
+def index_keys(entry0, n_new, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, w, *, m=4, rope_dim=64, theta=1e4,
+               eps=1e-6):
+    """Indexer keys of entries entry0 .. entry0+n_new-1 from a chunk's rows
+    (layout as compress()): (values before rounding [n_new,128], codes)."""
+    pre = np.empty((n_new, Ca.shape[-1]), np.float64)
+    codes = np.empty((n_new, Ca.shape[-1]), np.uint8)
+    for e in range(n_new):
+        i = entry0 + e
+        a_rows = slice(m * e, m * e + m)
+        if e > 0:
+            b_rows = slice(m * (e - 1), m * e)
+            cb, zb = Cb[b_rows], Zb[b_rows]
+        else:
+            cb, zb = Cb_prev, Zb_prev
+        pre[e], codes[e] = index_key_entry(i, Ca[a_rows], Za[a_rows], cb, zb, Ba, Bb, w, rope_dim=rope_dim,
+                                           theta=theta, eps=eps)
+    return pre, codes
 
 
 def inverse_rope(o, t, *, rope_dim=64, theta=1e4) -> np.ndarray:

@@ -129,6 +129,68 @@ void orc_compress_entry(int m, int D, int R, double theta, double eps,
   free(x);
 }
 
+/* ---- indexer keys ([hca_csa] "CSA：轻压缩 + 稀疏选择": the indexer has a
+ * compressor of its own at head_dim 128, followed by a Hadamard rotation so
+ * that the keys quantise well to FP8) ------------------------------------- */
+
+/* y = H_n x / sqrt(n): H_n is the Sylvester Hadamard matrix (n a power of
+ * two), H_1 = [1], H_2k = [[H_k, H_k], [H_k, -H_k]], whose entry (r, c) is
+ * (-1)^(number of bits set in r AND c).  Dense product, as the definition. */
+void orc_hadamard(int n, const double *x, double *y) {
+  for (int r = 0; r < n; ++r) {
+    double acc = 0.0;
+    for (int c = 0; c < n; ++c) {
+      unsigned v = (unsigned)(r & c);
+      int parity = 0;
+      while (v) {
+        parity ^= (int)(v & 1u);
+        v >>= 1;
+      }
+      acc += parity ? -x[c] : x[c];
+    }
+    y[r] = acc / sqrt((double)n);
+  }
+}
+
+/* The E4M3 code nearest to x: ties go to the code with an even mantissa (the
+ * last bit clear), magnitudes past the largest finite value (448) give +-448,
+ * NaN gives 0x7F.  Found by comparing with every finite code's value. */
+uint8_t orc_to_e4m3(double x) {
+  if (x != x) return 0x7F;
+  const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  int best = 0;
+  double best_err = a;  /* code 0 is +0 */
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double err = fabs(orc_e4m3((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* One indexer key entry i: the compressor's steps at width Dk (pool, RMSNorm
+ * with the key compressor's weight, RoPE on the last R channels at position
+ * m*i), then the Hadamard rotation, then E4M3.  pre receives the rotated
+ * values before rounding, codes the stored bytes. */
+void orc_index_key_entry(int m, int Dk, int R, double theta, double eps,
+                         int64_t i, const uint16_t *Ca, const uint16_t *Za,
+                         const uint16_t *Cb, const uint16_t *Zb,
+                         const uint16_t *Ba, const uint16_t *Bb,
+                         const uint16_t *w, double *pre, uint8_t *codes) {
+  double *x = (double *)malloc(sizeof(double) * (size_t)Dk);
+  double *y = (double *)malloc(sizeof(double) * (size_t)Dk);
+  orc_compress_pool(m, Dk, i > 0, Ca, Za, Cb, Zb, Ba, Bb, x);
+  orc_rmsnorm(Dk, x, w, eps, y);
+  orc_rope(Dk, R, theta, (double)m * (double)i, y);
+  orc_hadamard(Dk, y, pre);
+  for (int d = 0; d < Dk; ++d) codes[d] = orc_to_e4m3(pre[d]);
+  free(x);
+  free(y);
+}
+
 /* ---- visibility ([KV 压缩] §9.8) ---------------------------------------- */
 
 /* Entry s covers tokens up to m*s + m - 1, so the query at position t sees

@@ -414,3 +414,48 @@ def test_inverse_rope_recovers_the_output_of_unrotated_rows():
     wts /= wts.sum(1, keepdims=True)
     rotated = np.stack([oracle.rope(r, 64, 1e4, t) for r in rows])
     np.testing.assert_allclose(oracle.inverse_rope(wts @ rotated, t), wts @ rows, rtol=0, atol=1e-9)
+
+
+# ---- indexer keys ([hca_csa] "CSA：轻压缩 + 稀疏选择") --------------------------
+
+def test_hadamard_matches_the_kronecker_construction_and_is_an_involution():
+    import synthetic as syn
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(128)
+    H = syn.hadamard(128).double().numpy() / np.sqrt(128.0)  # H_2k = [[H_k, H_k], [H_k, -H_k]] built by blocks
+    np.testing.assert_allclose(oracle.hadamard(x), H @ x, atol=1e-12)
+    np.testing.assert_allclose(oracle.hadamard(oracle.hadamard(x)), x, atol=1e-12)
+    assert np.linalg.norm(oracle.hadamard(x)) == pytest.approx(np.linalg.norm(x), rel=1e-12)
+
+
+def test_e4m3_encoding_round_trips_and_agrees_with_torch_in_range():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_to_f64(codes)
+    back = oracle.to_e4m3(vals)
+    assert np.array_equal(back[codes != 0x80], codes[codes != 0x80])  # -0 and +0 decode alike
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(4000) * s for s in (1e-3, 0.05, 1.0, 30.0, 140.0)])
+    x = x[np.abs(x) <= 448].astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.to_e4m3(x.astype(np.float64)), want)
+
+
+def test_e4m3_ties_go_to_the_even_code_and_large_values_saturate():
+    pos = np.arange(1, 0x7E, dtype=np.uint8)  # neighbouring finite positive codes c, c+1
+    lo, hi = oracle.e4m3_to_f64(pos), oracle.e4m3_to_f64(pos + 1)
+    got = oracle.to_e4m3((lo + hi) / 2)
+    want = np.where(pos % 2 == 0, pos, pos + 1)
+    assert np.array_equal(got, want)
+    assert list(oracle.to_e4m3(np.array([1e4, -1e4, 449.0]))) == [0x7E, 0xFE, 0x7E]
+    assert oracle.to_e4m3(np.array([np.nan]))[0] == 0x7F
+
+
+def test_index_key_entry_is_the_compressor_entry_at_width_128_rotated_then_rounded():
+    m, D = 4, 128
+    Ca, Za, Cb, Zb, Ba, Bb = (rand_bf16((m, D)) for _ in range(6))
+    w = bf16_bits(torch.tensor(1 + 0.1 * RNG.standard_normal(D)).to(torch.bfloat16).double().numpy())
+    for i in (0, 5, 70000):
+        pre, codes = oracle.index_key_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w)
+        ent = oracle.compress_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w)
+        np.testing.assert_allclose(pre, oracle.hadamard(ent), atol=1e-12)
+        assert np.array_equal(codes, oracle.to_e4m3(pre))
