@@ -349,7 +349,27 @@ def prefill_profile(csa, torch, dev):
            "attn_tflops": attn_flops / (st[3] * 1e-3) / 1e12,
            "attn_tc_frac_of_bf16_peak": attn_flops / (st[3] * 1e-3) / 1e12 / bf16,
            "index_fp8_tflops": index_flops / (st[1] * 1e-3) / 1e12}
-    del x, kv, idx, out, lse, ws
+    # the chunk's indexer keys (the indexer's own compressor, width 128)
+    n_new = Q // w.m
+    xk = syn.indexer_compressor_inputs(w.config, B, Q, m=w.m, device=dev)
+    kI = torch.empty(B, x["n_cap"], 128, dtype=torch.uint8, device=dev)
+
+    def keys():
+        csa.csa_compress_indexer_keys(p, B, n_new, w.pos0 // w.m, xk["CIa"], xk["ZIa"], xk["CIb"], xk["ZIb"],
+                                      xk["CIb_prev"], xk["ZIb_prev"], xk["BIa"], xk["BIb"], xk["rms_wI"], kI,
+                                      x["n_cap"] * 128)
+    for _ in range(3):
+        keys()
+    e0.record()
+    for _ in range(n):
+        keys()
+    e1.record()
+    torch.cuda.synchronize()
+    kms = e0.elapsed_time(e1) / n
+    kbytes = B * n_new * (4 * w.m * 128 * 2 + 128)
+    res["indexer_keys"] = {"entries": B * n_new, "ms": kms, "gbs": kbytes / (kms * 1e-3) / 1e9,
+                           "hbm_frac": kbytes / (kms * 1e-3) / 1e9 / hbm}
+    del x, xk, kv, kI, idx, out, lse, ws
     torch.cuda.empty_cache()
     return res
 

@@ -59,6 +59,7 @@ _lib.csa_default_params.restype = None
 _lib.csa_workspace_size.argtypes = [_i32, _P, _i32, _i32, _i64]
 _lib.csa_workspace_size.restype = _sz
 _lib.csa_compress.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64, _vp]
+_lib.csa_compress_indexer_keys.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64, _vp]
 _lib.csa_index_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_static.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]
 _lib.csa_index_topk_static.restype = ctypes.c_int
@@ -66,7 +67,7 @@ _lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, 
                                  _vp, _sz, _vp]
 _lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
 _lib.csa_layer_prefill.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
-for _f in ("csa_compress", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode", "csa_layer_prefill"):
+for _f in ("csa_compress", "csa_compress_indexer_keys", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode", "csa_layer_prefill"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.csa_set_trace_events.argtypes = [ctypes.POINTER(_vp), _i32]
 _lib.csa_set_trace_events.restype = ctypes.c_int
@@ -124,6 +125,14 @@ def csa_compress(params, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba,
     _check(_lib.csa_compress(ctypes.byref(params), B, n_new, entry0, _ptr(Ca), _ptr(Za), _ptr(Cb), _ptr(Zb),
                              _ptr(Cb_prev), _ptr(Zb_prev), _ptr(Ba), _ptr(Bb), _ptr(rms_w), _ptr(kv_out),
                              kv_stride_b, _stream(stream)), "csa_compress")
+
+
+def csa_compress_indexer_keys(params, B, n_new, entry0, CIa, ZIa, CIb, ZIb, CIb_prev, ZIb_prev, BIa, BIb, rms_wI,
+                              kI_out, kI_stride_b, stream=None):
+    _check(_lib.csa_compress_indexer_keys(ctypes.byref(params), B, n_new, entry0, _ptr(CIa), _ptr(ZIa), _ptr(CIb),
+                                          _ptr(ZIb), _ptr(CIb_prev), _ptr(ZIb_prev), _ptr(BIa), _ptr(BIb),
+                                          _ptr(rms_wI), _ptr(kI_out), kI_stride_b, _stream(stream)),
+           "csa_compress_indexer_keys")
 
 
 def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, ws, stream=None):

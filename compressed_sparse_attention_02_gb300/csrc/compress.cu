@@ -1,6 +1,15 @@
 // The compressor as a kernel of its own: one 64-thread CTA per (entry,
 // sequence), 8 channels per thread (the entry routine is in compress.cuh).
 // Decode calls run the same routine inside the top-k launch instead.
+//
+// The indexer's key compressor ([hca_csa] "CSA：轻压缩 + 稀疏选择": its own
+// compressor at head_dim 128, then a Hadamard rotation so that the keys
+// quantise well to FP8): the same steps at width 128, one warp per entry
+// with 4 channels per lane, then H_128/sqrt(128) as butterflies (two stages
+// in registers, five across lanes), then E4M3 with round-to-nearest-even
+// and saturation at +-448.
+#include <cuda_fp8.h>
+
 #include "compress.cuh"
 
 namespace csa {
@@ -14,6 +23,46 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
   pdl_wait();
   __shared__ float red[kThreads / 32];
   compress_entry<M, 8>(a, blockIdx.y, blockIdx.x, threadIdx.x, red, [] { __syncthreads(); });
+}
+
+constexpr int kKeyWarps = 4;  // entries per CTA of the key kernel
+
+template <int M>
+__global__ void __launch_bounds__(32 * kKeyWarps) index_key_kernel(const CompressArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float red[kKeyWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * kKeyWarps + warp;
+  if (e >= a.n_new) return;  // warp-uniform
+  float y[4];
+  int64_t i;
+  if (!compress_values<M, 4, kIdxDim>(a, blockIdx.y, e, lane, red + warp, [] { __syncwarp(); }, y, &i)) return;
+  // H_128 x: butterflies (a, b) -> (a + b, a - b) over channel distance 1, 2
+  // (within the lane's 4 channels), then 4 .. 64 (lanes 1 .. 16 apart)
+  {
+    const float s0 = y[0] + y[1], d0 = y[0] - y[1], s1 = y[2] + y[3], d1 = y[2] - y[3];
+    y[0] = s0 + s1;
+    y[1] = d0 + d1;
+    y[2] = s0 - s1;
+    y[3] = d0 - d1;
+  }
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const bool upper = (lane >> st) & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[j], 1 << st);
+      y[j] = upper ? o - y[j] : y[j] + o;
+    }
+  }
+  constexpr float kInvSqrt128 = 0.088388347648318440550f;
+  uint32_t codes = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    codes |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(y[j] * kInvSqrt128, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+  *reinterpret_cast<uint32_t*>(a.key_out + static_cast<int64_t>(blockIdx.y) * a.kv_stride_b + i * kIdxDim +
+                               4 * lane) = codes;
 }
 
 }  // namespace
@@ -33,6 +82,26 @@ cudaError_t launch_compress(const CompressArgs& args, cudaStream_t stream) {
     case 2: return launch_pdl(compress_kernel<2>, grid, dim3(kThreads), 0, stream, a);
     case 4: return launch_pdl(compress_kernel<4>, grid, dim3(kThreads), 0, stream, a);
     case 8: return launch_pdl(compress_kernel<8>, grid, dim3(kThreads), 0, stream, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace csa
+
+namespace csa {
+
+cudaError_t launch_index_keys(const CompressArgs& args, cudaStream_t stream) {
+  if (args.B <= 0 || args.n_new <= 0) return cudaSuccess;
+  if (args.mode != 0) return cudaErrorInvalidValue;
+  CompressArgs a = args;
+  fill_inv_freq(&a);
+  const dim3 grid(static_cast<unsigned>((a.n_new + kKeyWarps - 1) / kKeyWarps), static_cast<unsigned>(a.B));
+  const dim3 block(32 * kKeyWarps);
+  switch (a.m) {
+    case 1: return launch_pdl(index_key_kernel<1>, grid, block, 0, stream, a);
+    case 2: return launch_pdl(index_key_kernel<2>, grid, block, 0, stream, a);
+    case 4: return launch_pdl(index_key_kernel<4>, grid, block, 0, stream, a);
+    case 8: return launch_pdl(index_key_kernel<8>, grid, block, 0, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -45,6 +45,20 @@ struct Bf16Vec<8> {
   }
 };
 template <>
+struct Bf16Vec<4> {
+  using T = uint2;
+  static __device__ __forceinline__ void unpack(const T u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ T pack(const float (&v)[4]) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+  }
+};
+template <>
 struct Bf16Vec<2> {
   using T = uint32_t;
   static __device__ __forceinline__ void unpack(const T u, float (&v)[2]) {
@@ -57,15 +71,18 @@ struct Bf16Vec<2> {
   }
 };
 
-// Computes entry (e-th of the chunk in bulk mode; the one completing at
-// q_pos[b] in ring mode) of sequence b.  `red` holds one float per warp of
-// the group; sync() is a barrier over exactly the group's threads.  Every
-// thread of the group must call this with the same (b, e).
-template <int M, int CPT, class Sync>
-__device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync) {
+// The values of entry (e-th of the chunk in bulk mode; the one completing at
+// q_pos[b] in ring mode) of sequence b at width D (rows of D channels, RoPE
+// on the last kRope of them): thread t's channels CPT*t .. CPT*t+CPT-1 into
+// y, the entry's index into *entry.  Returns false when there is no entry
+// (ring mode between block boundaries, or past the cache).  `red` holds one
+// float per warp of the group; sync() is a barrier over exactly the group's
+// threads.  Every thread of the group must call this with the same (b, e).
+template <int M, int CPT, int D, class Sync>
+__device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync,
+                                float (&y)[CPT], int64_t* entry) {
   using V = Bf16Vec<CPT>;
   using L = typename V::T;
-  constexpr int D = kDim;
   constexpr int NT = D / CPT;
   const int d0 = t * CPT;
 
@@ -96,11 +113,11 @@ __device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, f
     }
   } else {
     const int64_t tp = a.q_pos[b];
-    if (tp < 0 || (tp + 1) % M != 0) return;  // no block completes at this step
+    if (tp < 0 || (tp + 1) % M != 0) return false;  // no block completes at this step
     i = (tp + 1) / M - 1;
     if (i >= a.n_cap) {
       if (t == 0) record_error(a.status, kErrIndexRange);
-      return;
+      return false;
     }
     has_prev = i > 0;
     const int64_t ring = static_cast<int64_t>(b) * 2 * M * D;
@@ -185,7 +202,6 @@ __device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, f
   const float inv = rsqrtf(total / static_cast<float>(D) + a.rms_eps);
   float w[CPT];
   V::unpack(wr, w);
-  float y[CPT];
 #pragma unroll
   for (int j = 0; j < CPT; ++j) y[j] = x[j] * inv * w[j];
 
@@ -207,7 +223,19 @@ __device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, f
     }
   }
 
-  *reinterpret_cast<L*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * D + d0) = V::pack(y);
+  *entry = i;
+  return true;
+}
+
+// Entry of the main compressor (width 512), stored as bf16 into kv_out.
+template <int M, int CPT, class Sync>
+__device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync) {
+  using V = Bf16Vec<CPT>;
+  float y[CPT];
+  int64_t i;
+  if (!compress_values<M, CPT, kDim>(a, b, e, t, red, sync, y, &i)) return;
+  *reinterpret_cast<typename V::T*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + t * CPT) =
+      V::pack(y);
 }
 
 // theta^(-2j/R) for the 32 rotated pairs, in fp64 on the host.

@@ -339,6 +339,31 @@ csa_status csa_compress(const csa_params* p, int32_t B, int32_t n_new, int64_t e
                       kv_stride_b, entry0 + n_new, nullptr, static_cast<cudaStream_t>(stream));
 }
 
+csa_status csa_compress_indexer_keys(const csa_params* p, int32_t B, int32_t n_new, int64_t entry0,
+                                     const uint16_t* CIa, const uint16_t* ZIa, const uint16_t* CIb,
+                                     const uint16_t* ZIb, const uint16_t* CIb_prev, const uint16_t* ZIb_prev,
+                                     const uint16_t* BIa, const uint16_t* BIb, const uint16_t* rms_wI,
+                                     uint8_t* kI_out, int64_t kI_stride_b, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return CSA_OK;
+  if (!ok_ptr(CIa) || !ok_ptr(ZIa) || !ok_ptr(CIb) || !ok_ptr(ZIb) || !ok_ptr(BIa) || !ok_ptr(BIb) ||
+      !ok_ptr(rms_wI) || !ok_ptr(kI_out))
+    return CSA_ERR_INVALID_ARG;
+  if ((entry0 > 0) != (CIb_prev != nullptr) || (CIb_prev == nullptr) != (ZIb_prev == nullptr) ||
+      !ok_opt(CIb_prev) || !ok_opt(ZIb_prev))
+    return CSA_ERR_INVALID_ARG;
+  if (kI_stride_b < (entry0 + n_new) * csa::kIdxDim && B > 1) return CSA_ERR_INVALID_ARG;
+  if (kI_stride_b % 16 != 0) return CSA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  csa::CompressArgs ca = compress_args(p, 0, B, n_new, entry0, CIa, ZIa, CIb, ZIb, CIb_prev, ZIb_prev, BIa, BIb,
+                                       rms_wI, nullptr, kI_stride_b, entry0 + n_new, nullptr, status);
+  ca.key_out = kI_out;
+  return cuda_status(csa::launch_index_keys(ca, static_cast<cudaStream_t>(stream)));
+}
+
 csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
                           const uint16_t* wI, const uint8_t* kI, int64_t n_cap, int32_t* idx_out, float* score_out,
                           void* workspace, size_t workspace_bytes, void* stream) {

@@ -75,8 +75,12 @@ struct CompressArgs {
   float rms_eps;
   unsigned* status;
   double inv_freq[kRope / 2];  // theta^(-2j/R), filled by launch_compress
+  uint8_t* key_out;            // indexer keys (launch_index_keys): E4M3 rows of kIdxDim
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
+// Indexer keys from 128-wide compressor rows (bulk mode): the compressor's
+// steps at width kIdxDim, the Hadamard rotation, E4M3 codes into key_out.
+cudaError_t launch_index_keys(const CompressArgs& a, cudaStream_t stream);
 
 // ---- lightning indexer scores (tcgen05, FP8) -------------------------------------
 struct IndexArgs {

@@ -123,6 +123,36 @@ csa_status csa_compress(const csa_params *p, int32_t B, int32_t n_new,
                         int64_t kv_stride_b, void *stream);
 
 /*
+ * csa_compress_indexer_keys — the lightning indexer's own key compressor,
+ * bulk form.  [hca_csa] "CSA：轻压缩 + 稀疏选择": the indexer keeps a
+ * compressed K of its own (head_dim 128, one entry per m tokens at the same
+ * entry numbering as the main cache), rotated by a Hadamard matrix after
+ * compression so that it quantises well to FP8.
+ *
+ * For every sequence b and entry i in [entry0, entry0 + n_new): the steps of
+ * csa_compress at width 128 (the 2m-slot softmax pooling of CIa/CIb by the
+ * logits ZIa+BIa / ZIb+BIb, RMSNorm with rms_wI and eps = p->rms_eps, RoPE
+ * on the last rope_dim channels in interleaved pairs at position m*i), then
+ * y = H_128 x / sqrt(128) with H the Sylvester Hadamard matrix (entry (r, c)
+ * = (-1)^popcount(r & c)), then each y_d stored as the nearest FP8 E4M3 code
+ * (ties to the even code, magnitudes past 448 saturate to +-448, no scale).
+ *
+ * CIa, ZIa, CIb, ZIb : [B][m*n_new][128] bf16, row j of sequence b is token
+ *                      m*entry0 + j.
+ * CIb_prev, ZIb_prev : [B][m][128] bf16 rows of block entry0-1, NULL iff
+ *                      entry0 == 0.
+ * BIa, BIb : [m][128] bf16.   rms_wI : [128] bf16.
+ * kI_out   : entry e of sequence b at kI_out + b*kI_stride_b + e*128 (E4M3
+ *            bytes, the layout csa_index_topk reads); rows entry0.. only.
+ */
+csa_status csa_compress_indexer_keys(
+    const csa_params *p, int32_t B, int32_t n_new, int64_t entry0,
+    const uint16_t *CIa, const uint16_t *ZIa, const uint16_t *CIb,
+    const uint16_t *ZIb, const uint16_t *CIb_prev, const uint16_t *ZIb_prev,
+    const uint16_t *BIa, const uint16_t *BIb, const uint16_t *rms_wI,
+    uint8_t *kI_out, int64_t kI_stride_b, void *stream);
+
+/*
  * csa_index_topk — lightning indexer + top-k over the causally visible entries.
  * Score: [hca_csa] "CSA：轻压缩 + 稀疏选择", equation I_{t,s}; also
  * [结构对比] DSA section.  Visibility: [KV 压缩] §9.8 (entry s is visible to

@@ -29,7 +29,8 @@ import torch
 # which other tensors are drawn.
 _IDS = {name: i for i, name in enumerate([
     "Ca", "Za", "Cb", "Zb", "Ba", "Bb", "rms_w", "q", "qI", "wI", "kI", "sink", "kv", "swa",
-    "Cb_prev", "Zb_prev", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb"])}
+    "Cb_prev", "Zb_prev", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb",
+    "CIa", "ZIa", "CIb", "ZIb", "CIb_prev", "ZIb_prev", "BIa", "BIb", "rms_wI"])}
 
 D, H, HI, DI, R = 512, 64, 64, 128, 64
 
@@ -112,6 +113,19 @@ def _per_seq(B, config, name, shape, device, make):
 def compressor_rows(config: int, B: int, T: int, device="cpu", names=("Ca", "Za", "Cb", "Zb")) -> dict:
     """[B, T, D] bf16 N(0,1) compressor inputs for T consecutive tokens."""
     return {n: _per_seq(B, config, n, (T, D), device, bf16) for n in names}
+
+
+def indexer_compressor_inputs(config: int, B: int, T: int, m: int = 4, device="cpu") -> dict:
+    """The indexer key compressor's inputs (width 128): rows CIa, ZIa, CIb,
+    ZIb [B, T, 128] and the m rows before the chunk, N(0,1) bf16; block biases
+    BIa, BIb [m, 128] N(0,1) bf16; RMSNorm weight 1 + 0.1*N(0,1)."""
+    s = 1000 * config
+    out = {n: _per_seq(B, config, n, (T, DI), device, bf16) for n in ("CIa", "ZIa", "CIb", "ZIb")}
+    out.update({n: _per_seq(B, config, n, (m, DI), device, bf16) for n in ("CIb_prev", "ZIb_prev")})
+    out["BIa"] = bf16(normal((m, DI), s, "BIa", device))
+    out["BIb"] = bf16(normal((m, DI), s, "BIb", device))
+    out["rms_wI"] = bf16(1.0 + 0.1 * normal((DI,), s, "rms_wI", device))
+    return out
 
 
 def indexer_query(config: int, B: int, Q: int, device="cpu") -> dict:

@@ -119,3 +119,46 @@ def test_decode_emission_from_ring(csa):
         others = np.ones(n_cap, bool)
         others[i] = False
         np.testing.assert_array_equal(got[b, others], ref[b, others])
+
+
+def check_key_codes(got, pre, codes, what):
+    """Equal E4M3 codes, except where the oracle's value sits within a relative
+    1e-4 of the midpoint between two neighbouring codes: there the kernel's
+    fp32 rounding may land on either side (both codes are then accepted)."""
+    got = np.asarray(got, dtype=np.uint8).ravel()
+    codes = np.asarray(codes, dtype=np.uint8).ravel()
+    pre = np.asarray(pre, dtype=np.float64).ravel()
+    diff = np.nonzero(got != codes)[0]
+    for j in diff:
+        a, b = oracle.e4m3_to_f64(np.array([got[j], codes[j]], dtype=np.uint8))
+        mid = (a + b) / 2
+        assert abs(int(got[j] & 0x7F) - int(codes[j] & 0x7F)) <= 1 and (got[j] & 0x80) == (codes[j] & 0x80), \
+            "%s: element %d code %#x vs %#x" % (what, j, got[j], codes[j])
+        assert abs(pre[j] - mid) <= 1e-4 * abs(mid) + 1e-9, "%s: element %d not at a rounding midpoint" % (what, j)
+    return len(diff)
+
+
+@pytest.mark.parametrize("m,B,n_new,entry0", [(4, 2, 37, 0), (4, 3, 29, 1021), (8, 1, 9, 3), (1, 2, 50, 7)])
+def test_indexer_key_compressor_bulk(csa, m, B, n_new, entry0):
+    """Ragged entry counts (CTAs of four entries), the first block (no previous
+    rows) and a chunk far into the sequence (RoPE angles near 4100 rad)."""
+    x = syn.indexer_compressor_inputs(20 + m, B, m * n_new, m=m)
+    p = csa.csa_default_params(m=m)
+    n_cap = entry0 + n_new + 3
+    kI = torch.full((B, n_cap, 128), 0x55, dtype=torch.uint8, device=DEV)
+    prev = entry0 > 0
+    g = {k: v.to(DEV) for k, v in x.items()}
+    csa.csa_compress_indexer_keys(p, B, n_new, entry0, g["CIa"], g["ZIa"], g["CIb"], g["ZIb"],
+                                  g["CIb_prev"] if prev else None, g["ZIb_prev"] if prev else None, g["BIa"],
+                                  g["BIb"], g["rms_wI"], kI, n_cap * 128)
+    assert csa.csa_check_status() == 0
+    kI = kI.cpu().numpy()
+    near = 0
+    for b in range(B):
+        pre, codes = oracle.index_keys(entry0, n_new, bits(x["CIa"][b]), bits(x["ZIa"][b]), bits(x["CIb"][b]),
+                                       bits(x["ZIb"][b]), bits(x["CIb_prev"][b]) if prev else None,
+                                       bits(x["ZIb_prev"][b]) if prev else None, bits(x["BIa"]), bits(x["BIb"]),
+                                       bits(x["rms_wI"]), m=m)
+        near += check_key_codes(kI[b, entry0:entry0 + n_new], pre, codes, "keys b=%d" % b)
+        assert np.all(kI[b, :entry0] == 0x55) and np.all(kI[b, entry0 + n_new:] == 0x55), "rows outside the chunk"
+    assert near <= 0.01 * B * n_new * 128
