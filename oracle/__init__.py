@@ -196,6 +196,59 @@ def topk(scores, k: int) -> np.ndarray:
     return idx
 
 
+# ---- hierarchical indexer ---------------------------------------------------
+# [CSA2 详解] §11 "Hierarchical Sparse Indexer": the Full layer scores every
+# visible entry; entries are grouped in blocks of 8 consecutive ones, a
+# block's score is the largest score among its entries, and at most 2048
+# blocks with the largest block scores form the candidate pool (at most 16384
+# entries).  A Reindex layer scores only the pool's entries with its own q^I
+# and head weights and takes its own top-k among them (§11.1; §20.1: the
+# candidates are gathered first, so the cost is fixed by the pool size).
+
+POOL_BLOCK = 8
+
+
+def block_scores(scores, block: int = POOL_BLOCK) -> np.ndarray:
+    """Scores of the ceil(V/block) blocks of V visible entries: block j holds
+    entries j*block .. j*block+block-1 below V, its score is their largest."""
+    s = np.asarray(scores, dtype=np.float64)
+    V = s.size
+    nb = (V + block - 1) // block
+    out = np.empty(nb, np.float64)
+    for j in range(nb):
+        out[j] = s[j * block:min(V, (j + 1) * block)].max()
+    return out
+
+
+def candidate_pool(scores, n_blocks: int = 2048, block: int = POOL_BLOCK) -> np.ndarray:
+    """The Full layer's pool: the min(n_blocks, ceil(V/block)) blocks with the
+    largest block scores (equal scores: the smaller block first), in
+    ascending block order, then -1 up to n_blocks slots."""
+    return topk(block_scores(scores, block), n_blocks)
+
+
+def pool_entries(pool, V: int, block: int = POOL_BLOCK) -> np.ndarray:
+    """Entries of the pool's blocks (-1 slots skipped) that are visible
+    (below V), in ascending order."""
+    out = [b * block + r for b in np.asarray(pool) if b >= 0 for r in range(block) if b * block + r < V]
+    return np.asarray(out, dtype=np.int64)
+
+
+def reindex_topk(qI, wI, kI, pool, V: int, k: int, block: int = POOL_BLOCK):
+    """A Reindex layer over the pool: its own scores I_s for the pool's
+    entries s only, then the min(k, |pool|) largest (equal scores: the
+    smaller entry first), returned as entry indices in ascending order and
+    -1 up to k slots.  Returns (idx [k], the pool's entries, their scores)."""
+    ent = pool_entries(pool, V, block)
+    kI = np.asarray(kI)
+    sc = index_scores(qI, wI, kI[ent]) if ent.size else np.empty(0, np.float64)
+    slots = topk(sc, k)
+    idx = np.full(k, -1, np.int32)
+    n = int((slots >= 0).sum())
+    idx[:n] = ent[slots[:n]]
+    return idx, ent, sc
+
+
 # ---- attention ------------------------------------------------------------
 
 def attend(q, rows, sink, sm_scale):

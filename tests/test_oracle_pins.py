@@ -459,3 +459,92 @@ def test_index_key_entry_is_the_compressor_entry_at_width_128_rotated_then_round
         ent = oracle.compress_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w)
         np.testing.assert_allclose(pre, oracle.hadamard(ent), atol=1e-12)
         assert np.array_equal(codes, oracle.to_e4m3(pre))
+
+
+# ---- hierarchical indexer ([CSA2 详解] §11) ------------------------------------
+
+def test_block_scores_worked_example():
+    """21 entries in blocks of 8: blocks {0..7}, {8..15}, {16..20}.  Rising
+    scores put each block's maximum on its last visible entry, falling scores
+    on its first one (values written out by hand)."""
+    rising = np.arange(21, dtype=np.float64)
+    np.testing.assert_array_equal(oracle.block_scores(rising), [7.0, 15.0, 20.0])
+    np.testing.assert_array_equal(oracle.block_scores(rising[::-1].copy()), [20.0, 12.0, 4.0])
+    np.testing.assert_array_equal(oracle.block_scores(np.array([3.0])), [3.0])
+    assert oracle.block_scores(np.zeros(0)).size == 0
+
+
+def test_candidate_pool_separates_chosen_from_unchosen_entries():
+    """Every entry of an unchosen block scores at most the smallest chosen
+    block's best entry; pools are ascending, unique and -1 padded; when every
+    visible block fits, the pool is all of them."""
+    for trial in range(100):
+        V = int(RNG.integers(1, 200))
+        nb = int(RNG.integers(1, 30))
+        s = RNG.integers(-5, 6, V).astype(np.float64)  # many ties
+        pool = oracle.candidate_pool(s, nb)
+        n_vis = (V + 7) // 8
+        n = min(nb, n_vis)
+        assert pool.shape == (nb,)
+        assert np.all(pool[n:] == -1)
+        chosen = pool[:n]
+        assert np.all(np.diff(chosen) > 0) and chosen.min() >= 0 and chosen.max() < n_vis
+        if n == n_vis:
+            np.testing.assert_array_equal(chosen, np.arange(n_vis))
+            continue
+        best_in = [s[8 * b:min(V, 8 * b + 8)].max() for b in chosen]
+        out_entries = [s[e] for e in range(V) if e // 8 not in set(chosen.tolist())]
+        assert min(best_in) >= max(out_entries)
+        # ties between a chosen and an unchosen block: the chosen one is smaller
+        floor = min(best_in)
+        tied_out = [b for b in range(n_vis) if b not in set(chosen.tolist()) and s[8 * b:min(V, 8 * b + 8)].max() == floor]
+        tied_in = [b for b in chosen if s[8 * b:min(V, 8 * b + 8)].max() == floor]
+        if tied_out:
+            assert max(tied_in) < min(tied_out)
+
+
+def test_pool_entries_drop_the_invisible_tail_of_the_last_block():
+    # V = 59: block 7 holds entries 56..58 only
+    np.testing.assert_array_equal(oracle.pool_entries([2, 7, -1], 59), list(range(16, 24)) + [56, 57, 58])
+    assert oracle.pool_entries([-1, -1], 59).size == 0
+
+
+def test_reindex_with_the_full_layers_query_reproduces_the_full_topk():
+    """A position of the full top-k has a block score at least its own score,
+    and at most k blocks can score above it, so with n_blocks >= k the pool
+    holds the whole full top-k: a Reindex layer using the Full layer's own
+    q^I / w^I must then return exactly the full top-k."""
+    V, k, nb = 2000, 64, 64
+    q, w, kI = rand_e4m3((64, 128)), rand_bf16(64, 1 / 90.0), rand_e4m3((V, 128))
+    full = oracle.index_scores(q, w, kI)
+    top = np.sort(full)[::-1][:k + 1]
+    assert np.all(np.diff(top) < 0), "the seed must give distinct leading scores"
+    pool = oracle.candidate_pool(full, nb)
+    assert (pool >= 0).sum() == nb and oracle.pool_entries(pool, V).size == 8 * nb < V
+    idx, ent, sc = oracle.reindex_topk(q, w, kI, pool, V, k)
+    np.testing.assert_array_equal(idx, oracle.topk(full, k))
+
+
+def test_reindex_equals_masking_the_full_scores_outside_the_pool():
+    """Scoring the gathered pool equals scoring every entry and masking the
+    entries outside the pool to -inf before the top-k (the two forms of
+    [CSA2 详解] §20.1), with a second layer's own query."""
+    V, k, nb = 777, 40, 12
+    q1, w1 = rand_e4m3((64, 128)), rand_bf16(64, 1 / 90.0)
+    q2, w2 = rand_e4m3((64, 128)), rand_bf16(64, 1 / 90.0)
+    kI = rand_e4m3((V, 128))
+    pool = oracle.candidate_pool(oracle.index_scores(q1, w1, kI), nb)
+    idx, ent, sc = oracle.reindex_topk(q2, w2, kI, pool, V, k)
+    masked = np.full(V, -np.inf)
+    keep = oracle.pool_entries(pool, V)
+    masked[keep] = oracle.index_scores(q2, w2, kI)[keep]
+    np.testing.assert_array_equal(idx, oracle.topk(masked, k)[:k])
+    np.testing.assert_array_equal(sc, masked[ent])
+
+
+def test_reindex_returns_the_whole_pool_when_k_covers_it():
+    V = 59
+    kI = rand_e4m3((V, 128))
+    q, w = rand_e4m3((64, 128)), rand_bf16(64, 1 / 90.0)
+    idx, ent, sc = oracle.reindex_topk(q, w, kI, [0, 7, -1, -1], V, 16)
+    np.testing.assert_array_equal(idx, list(range(8)) + [56, 57, 58] + [-1] * 5)
