@@ -32,7 +32,9 @@ _lib = ctypes.CDLL(LIBRARY_PATH)
 CSA_OK = 0
 STATUS_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA",
                 4: "CSA_ERR_TIMEOUT", 5: "CSA_ERR_INDEX_RANGE", 6: "CSA_ERR_WORKSPACE"}
-CSA_OP_COMPRESS, CSA_OP_INDEX_TOPK, CSA_OP_SPARSE_ATTN, CSA_OP_LAYER_DECODE, CSA_OP_LAYER_PREFILL = range(5)
+(CSA_OP_COMPRESS, CSA_OP_INDEX_TOPK, CSA_OP_SPARSE_ATTN, CSA_OP_LAYER_DECODE, CSA_OP_LAYER_PREFILL,
+ CSA_OP_INDEX_TOPK_POOL, CSA_OP_REINDEX_TOPK) = range(7)
+CSA_POOL_BLOCK = 8
 
 
 class CsaParams(ctypes.Structure):
@@ -63,6 +65,10 @@ _lib.csa_compress_indexer_keys.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [
 _lib.csa_index_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_static.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]
 _lib.csa_index_topk_static.restype = ctypes.c_int
+_lib.csa_index_topk_pool.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]
+_lib.csa_index_topk_pool.restype = ctypes.c_int
+_lib.csa_reindex_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]
+_lib.csa_reindex_topk.restype = ctypes.c_int
 _lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]
 _lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
@@ -139,6 +145,20 @@ def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, w
     _check(_lib.csa_index_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
                                _ptr(idx_out), _ptr(score_out), _ptr(ws), 0 if ws is None else ws.numel(),
                                _stream(stream)), "csa_index_topk")
+
+
+def csa_index_topk_pool(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, pool_blocks, pool_out, ws,
+                        stream=None):
+    _check(_lib.csa_index_topk_pool(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
+                                    _ptr(idx_out), _ptr(score_out), pool_blocks, _ptr(pool_out), _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream(stream)), "csa_index_topk_pool")
+
+
+def csa_reindex_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, pool, pool_blocks, idx_out, score_out, ws,
+                     stream=None):
+    _check(_lib.csa_reindex_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
+                                 _ptr(pool), pool_blocks, _ptr(idx_out), _ptr(score_out), _ptr(ws),
+                                 0 if ws is None else ws.numel(), _stream(stream)), "csa_reindex_topk")
 
 
 STATIC_SCRATCH_BYTES = 16 << 20

@@ -125,24 +125,75 @@ bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
 
 csa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
-// Shared body of csa_index_topk and the layer calls.
+// The hierarchical indexer's side of a call: a pool to score (Reindex layer)
+// or a pool to produce (Full layer), of `blocks` blocks.
+struct PoolSpec {
+  const int32_t* in = nullptr;
+  int32_t* out = nullptr;
+  int blocks = 0;
+};
+
+// Full layer scratch: the entries' indexer scratch, then the same layout for
+// the ceil(n_cap/8) block scores.
+bool pool_workspace(int64_t rows, int64_t n_cap, IndexWs* w, IndexWs* wb, size_t* total) {
+  if (!index_workspace(rows, n_cap, 0, w) || !index_workspace(rows, (n_cap + 7) / 8, 0, wb)) return false;
+  *total = w->total + wb->total;
+  return true;
+}
+
+bool pool_blocks_ok(int32_t blocks) {
+  return blocks >= csa::kPoolTileBlocks && blocks <= csa::kMaxTopk && blocks % csa::kPoolTileBlocks == 0;
+}
+
+// Fills the top-k arguments that point into one IndexWs.
+void topk_scratch(csa::TopkArgs* ta, uint8_t* base, const IndexWs& w) {
+  ta->scores = reinterpret_cast<const float*>(base + w.scores_off);
+  ta->score_ld = w.score_ld;
+  ta->hist = reinterpret_cast<const uint32_t*>(base + w.hist_off);
+  ta->bits = reinterpret_cast<uint32_t*>(base + w.bits_off);
+  ta->ties = reinterpret_cast<uint32_t*>(base + w.ties_off);
+  ta->bits_ld = w.bits_ld;
+  ta->cand_count = reinterpret_cast<unsigned*>(base + w.count_off);
+  ta->row_done = reinterpret_cast<unsigned*>(base + w.done_off);
+  ta->cand_key = reinterpret_cast<uint32_t*>(base + w.cand_key_off);
+  ta->cand_idx = reinterpret_cast<int32_t*>(base + w.cand_idx_off);
+  ta->cand_cap = csa::kTopkCandCap;
+}
+
+// Shared body of csa_index_topk, the hierarchical indexer calls and the
+// layer calls.
 csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
                           const uint8_t* qI, const uint16_t* wI, const uint8_t* kI, int64_t n_cap,
                           int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes, cudaStream_t st,
                           bool traced = false, bool zeroed = false,
-                          const csa::CompressArgs* ride_along = nullptr) {
-  IndexWs w;
-  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < w.total || !aligned16(ws)) return CSA_ERR_WORKSPACE;
+                          const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr) {
+  const int64_t rows = static_cast<int64_t>(B) * Q;
+  IndexWs w, wb;
+  size_t need = 0;
+  bool sized;
+  if (pool && pool->in) {
+    sized = index_workspace(rows, static_cast<int64_t>(pool->blocks) * csa::kPoolBlock, p->topk, &w);
+    need = w.total;
+  } else if (pool && pool->out) {
+    sized = pool_workspace(rows, n_cap, &w, &wb, &need);
+  } else {
+    sized = index_workspace(rows, n_cap, p->topk, &w);
+    need = w.total;
+  }
+  if (!sized) return CSA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < need || !aligned16(ws)) return CSA_ERR_WORKSPACE;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   unsigned* status = status_ptr();
   if (!enc || !status) return CSA_ERR_CUDA;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
+  uint8_t* wsb_blk = wsb + w.total;  // Full layer: the block scores' scratch
   float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + w.hist_off);
   if (!zeroed && cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (pool && pool->out && cudaMemsetAsync(wsb_blk + wb.hist_off, 0, wb.zero_bytes, st) != cudaSuccess)
+    return CSA_ERR_CUDA;
 
-  csa::IndexArgs ia;
+  csa::IndexArgs ia = {};
   ia.qI = qI;
   ia.wI = wI;
   ia.kI = kI;
@@ -155,15 +206,23 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ia.scores = scores;
   ia.score_ld = w.score_ld;
   ia.hist = hist;
+  if (pool && pool->in) {
+    ia.pool = pool->in;
+    ia.pool_blocks = pool->blocks;
+    ia.pool_ld = pool->blocks;
+  }
+  if (pool && pool->out) {
+    ia.block_scores = reinterpret_cast<float*>(wsb_blk + wb.scores_off);
+    ia.block_ld = wb.score_ld;
+    ia.block_hist = reinterpret_cast<uint32_t*>(wsb_blk + wb.hist_off);
+  }
   ia.status = status;
   csa_status s = cuda_status(csa::launch_index_scores(ia, enc, st));
   if (s != CSA_OK) return s;
   if (traced) trace(2, st);
 
-  csa::TopkArgs ta;
-  ta.scores = scores;
-  ta.score_ld = w.score_ld;
-  ta.hist = hist;
+  csa::TopkArgs ta = {};
+  topk_scratch(&ta, wsb, w);
   ta.q_pos = q_pos;
   ta.pos_base = pos_base;
   ta.B = B;
@@ -173,16 +232,23 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ta.n_cap = n_cap;
   ta.idx_out = idx_out;
   ta.score_out = score_out;
-  ta.bits = reinterpret_cast<uint32_t*>(wsb + w.bits_off);
-  ta.ties = reinterpret_cast<uint32_t*>(wsb + w.ties_off);
-  ta.bits_ld = w.bits_ld;
-  ta.cand_count = reinterpret_cast<unsigned*>(wsb + w.count_off);
-  ta.row_done = reinterpret_cast<unsigned*>(wsb + w.done_off);
-  ta.cand_key = reinterpret_cast<uint32_t*>(wsb + w.cand_key_off);
-  ta.cand_idx = reinterpret_cast<int32_t*>(wsb + w.cand_idx_off);
-  ta.cand_cap = csa::kTopkCandCap;
+  if (pool && pool->in) {
+    ta.pool = pool->in;
+    ta.pool_blocks = pool->blocks;
+    ta.pool_ld = pool->blocks;
+  }
   ta.status = status;
-  return cuda_status(csa::launch_topk(ta, ride_along, st));
+  s = cuda_status(csa::launch_topk(ta, ride_along, st));
+  if (s != CSA_OK || !(pool && pool->out)) return s;
+
+  // the pool: the top `blocks` block scores, block ids ascending
+  csa::TopkArgs tb = ta;
+  topk_scratch(&tb, wsb_blk, wb);
+  tb.k = pool->blocks;
+  tb.vis_shift = 3;
+  tb.idx_out = pool->out;
+  tb.score_out = nullptr;
+  return cuda_status(csa::launch_topk(tb, nullptr, st));
 }
 
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
@@ -192,7 +258,7 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   unsigned* status = status_ptr();
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!status || !enc) return CSA_ERR_CUDA;
-  csa::AttnArgs aa;
+  csa::AttnArgs aa = {};
   aa.q_pos = q_pos;
   aa.pos_base = pos_base;
   aa.q = q;
@@ -314,6 +380,16 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
       return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w) ? w.total : 0;
     case CSA_OP_LAYER_DECODE:
       return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w) ? w.total : 0;
+    case CSA_OP_INDEX_TOPK_POOL: {
+      IndexWs wb;
+      size_t total = 0;
+      return pool_workspace(static_cast<int64_t>(B) * Q, n_cap, &w, &wb, &total) ? total : 0;
+    }
+    case CSA_OP_REINDEX_TOPK:  // sized for the largest pool
+      return index_workspace(static_cast<int64_t>(B) * Q, static_cast<int64_t>(csa::kMaxTopk) * csa::kPoolBlock,
+                             p->topk, &w)
+                 ? w.total
+                 : 0;
     default:
       return 0;
   }
@@ -393,6 +469,44 @@ csa_status csa_index_topk_static(const csa_params* p, int32_t B, int32_t Q, cons
   if (!scratch) return CSA_ERR_CUDA;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, scratch,
                         CSA_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_index_topk_pool(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
+                               const uint16_t* wI, const uint8_t* kI, int64_t n_cap, int32_t* idx_out,
+                               float* score_out, int32_t pool_blocks, int32_t* pool_out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (!pool_blocks_ok(pool_blocks)) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || Q == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(idx_out) || !ok_opt(score_out) ||
+      !ok_ptr(pool_out))
+    return CSA_ERR_INVALID_ARG;
+  PoolSpec ps;
+  ps.out = pool_out;
+  ps.blocks = pool_blocks;
+  return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
+                        static_cast<cudaStream_t>(stream), false, false, nullptr, &ps);
+}
+
+csa_status csa_reindex_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
+                            const uint16_t* wI, const uint8_t* kI, int64_t n_cap, const int32_t* pool,
+                            int32_t pool_blocks, int32_t* idx_out, float* score_out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (!pool_blocks_ok(pool_blocks)) return CSA_ERR_UNSUPPORTED;
+  if (B == 0 || Q == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(pool) || !ok_ptr(idx_out) ||
+      !ok_opt(score_out))
+    return CSA_ERR_INVALID_ARG;
+  PoolSpec ps;
+  ps.in = pool;
+  ps.blocks = pool_blocks;
+  return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
+                        static_cast<cudaStream_t>(stream), false, false, nullptr, &ps);
 }
 
 csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint16_t* q,

@@ -25,6 +25,16 @@
 //               the top-k to go straight to the digit holding the k-th).
 // Every wait is bounded; a timeout records the error, the roles drain their
 // own in-flight work and the CTA releases TMEM and exits.
+//
+// Hierarchical indexer ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §11, and
+// §20.1: the candidates are gathered before they are scored).  Full layer:
+// the epilogue also takes the maximum over each block of 8 consecutive keys
+// (three shuffles: a block is 8 adjacent lanes) and stores it with its own
+// first-digit histogram, for the top-k that picks the pool's blocks.
+// Reindex layer: a tile is 16 pool blocks instead of 128 consecutive keys;
+// the producer loads each block (8 keys, 1 KiB, one 128-byte swizzle atom)
+// with its own TMA box into the tile's atom slot, so the MMA and the epilogue
+// run unchanged, and scores are stored by pool slot.
 #include <cuda_bf16.h>
 
 #include "keys.cuh"
@@ -37,6 +47,7 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr uint32_t kKeyTileBytes = kTileKeys * kIdxDim;   // 16 KiB
 constexpr uint32_t kQBytes = kIdxHeads * kIdxDim;         // 8 KiB per query
+static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool blocks");
 
 // Shape of the decode (one query per group) configuration.
 #ifndef CSA_INDEX_DECODE_STAGES
@@ -71,7 +82,8 @@ struct IndexCfg {
 // q^I is then loaded into the other of two q^I buffers.  Tiles past a group's
 // last visible key are skipped by every role alike.
 struct GroupInfo {
-  int64_t vis[4];   // visible entries of each query of the group
+  int64_t vis[4];   // visible entries (pool mode: pool slots to score) of each query of the group
+  int64_t vent[4];  // visible entries of each query of the group
   int64_t vmax;
   int b, q0;
 };
@@ -91,6 +103,11 @@ __device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, int64_t g, i
                                 : a.pos_base + q;
       V = t >= 0 ? (t + 1) / a.m : 0;
       if (V > a.n_cap) V = a.n_cap;
+    }
+    gi.vent[j] = V;
+    if (a.pool) {  // the pool holds min(pool_blocks, ceil(V/8)) blocks
+      const int64_t nb = (V + kPoolBlock - 1) / kPoolBlock;
+      V = (nb < a.pool_blocks ? nb : a.pool_blocks) * kPoolBlock;
     }
     gi.vis[j] = V;
     gi.vmax = V > gi.vmax ? V : gi.vmax;
@@ -211,7 +228,28 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
         if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
         mbar_arrive_expect_tx(&full[s], kKeyTileBytes);
-        tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s], pol);
+        if (a.pool) {
+          // 16 blocks of 8 keys, each into its own 1 KiB swizzle atom; slots
+          // without a block (or with an id outside the cache) load block 0,
+          // which the epilogue does not score
+          const int4* ids = reinterpret_cast<const int4*>(a.pool + (static_cast<int64_t>(gi.b) * a.Q + gi.q0) * a.pool_ld +
+                                                          tile * kPoolTileBlocks);
+          const int64_t n_blk = (a.n_cap + kPoolBlock - 1) / kPoolBlock;
+#pragma unroll
+          for (int v = 0; v < kPoolTileBlocks / 4; ++v) {
+            const int4 q4 = __ldg(ids + v);
+            const int32_t id[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int32_t blk = (id[e] >= 0 && id[e] < n_blk) ? id[e] : 0;
+              tma_load_3d(k_s + s * kKeyTileBytes + (4 * v + e) * (kPoolBlock * kIdxDim), &tm_k, 0,
+                          blk * kPoolBlock, gi.b, &full[s], pol);
+            }
+          }
+        } else {
+          tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s],
+                      pol);
+        }
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | ((use & 1u) << s);
         ++it;
@@ -344,9 +382,29 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
           }
         }
         const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        const bool valid = s_idx < gi.vis[j];
+        const bool in_row = s_idx < gi.vis[j];
+        bool valid = in_row;
         const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
-        if (valid) a.scores[row_off * a.score_ld + s_idx] = score;
+        if (a.pool && in_row) {  // slot s_idx holds entry 8*pool[s_idx/8] + s_idx%8
+          const int32_t blk = __ldg(a.pool + row_off * a.pool_ld + (s_idx >> 3));
+          const int64_t nb = (gi.vent[j] + kPoolBlock - 1) / kPoolBlock;
+          if (blk >= nb && (row & 7) == 0) record_error(a.status, kErrIndexRange);
+          valid = blk >= 0 && static_cast<int64_t>(blk) * kPoolBlock + (row & 7) < gi.vent[j];
+          a.scores[row_off * a.score_ld + s_idx] = valid ? score : -INFINITY;
+        } else if (valid) {
+          a.scores[row_off * a.score_ld + s_idx] = score;
+        }
+        if (a.block_scores) {  // the block's largest score: 8 adjacent lanes
+          float bm = valid ? score : -INFINITY;
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+          const bool lead = valid && (lane & 7) == 0;  // the block's first entry is visible
+          if (lead) a.block_scores[row_off * a.block_ld + (s_idx >> 3)] = bm;
+          const int bbin = lead ? static_cast<int>(score_key(bm) >> kKeyBinShift) : -1;
+          const unsigned bpeers = __match_any_sync(0xffffffffu, bbin);
+          if (lead && lane == __ffs(bpeers) - 1) atomicAdd(a.block_hist + row_off * kKeyBins + bbin, __popc(bpeers));
+        }
         if (a.hist) {  // first-digit histogram of the row, one atomic per distinct digit per warp
           const int bin = valid ? static_cast<int>(score_key(score) >> kKeyBinShift) : -1;
           const unsigned peers = __match_any_sync(0xffffffffu, bin);
@@ -372,11 +430,12 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
 
 bool encode_maps(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, int qpc, CUtensorMap* tm_k,
                  CUtensorMap* tm_q) {
-  // K^I: [B][n_cap][128] bytes, box = 128 keys x 128 bytes of one sequence.
+  // K^I: [B][n_cap][128] bytes, box = 128 keys x 128 bytes of one sequence
+  // (pool mode: one block of 8 keys).
   cuuint64_t kdim[3] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(a.n_cap),
                         static_cast<cuuint64_t>(a.B)};
   cuuint64_t kstride[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(a.n_cap) * kIdxDim};
-  cuuint32_t kbox[3] = {static_cast<cuuint32_t>(kIdxDim), static_cast<cuuint32_t>(kTileKeys), 1};
+  cuuint32_t kbox[3] = {static_cast<cuuint32_t>(kIdxDim), static_cast<cuuint32_t>(a.pool ? kPoolBlock : kTileKeys), 1};
   cuuint32_t ones[3] = {1, 1, 1};
   if (encode(tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kI), kdim, kstride, kbox, ones,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -405,7 +464,8 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int per_sm = Cfg::CTAS_PER_SM;
-  const int64_t tiles_per_group = (a.n_cap + kTileKeys - 1) / kTileKeys;
+  const int64_t tiles_per_group =
+      a.pool ? a.pool_blocks / kPoolTileBlocks : (a.n_cap + kTileKeys - 1) / kTileKeys;
   const int64_t groups_per_seq = (a.Q + QPC - 1) / QPC;
   const int64_t units = tiles_per_group * groups_per_seq * a.B;
   // One wave of CTAs that all stay resident; each takes an equal range.
@@ -420,7 +480,9 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
                                 cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  if (a.Q >= 4) return launch_qpc<4>(a, encode, stream);
+  if (a.pool && (a.pool_blocks <= 0 || a.pool_blocks % kPoolTileBlocks != 0 || a.pool_ld % 4 != 0))
+    return cudaErrorInvalidValue;
+  if (a.Q >= 4 && !a.pool) return launch_qpc<4>(a, encode, stream);  // a pool is per query: one query per tile
   return launch_qpc<1>(a, encode, stream);
 }
 

@@ -58,6 +58,8 @@ constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
 constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k row keeps
+constexpr int kPoolBlock = 8;         // entries per block of the hierarchical indexer's pool
+constexpr int kPoolTileBlocks = 16;   // pool blocks per 128-key indexer tile
 
 // ---- compressor --------------------------------------------------------------
 struct CompressArgs {
@@ -94,6 +96,18 @@ struct IndexArgs {
   float* scores;            // [B*Q][score_ld]
   int64_t score_ld;
   uint32_t* hist;           // [B*Q][2048] key top-digit counts (zeroed by the caller) or null
+  // Full layer of the hierarchical indexer: per row, the largest score of
+  // each block of kPoolBlock entries with a visible first entry, and the
+  // first-digit counts of those block scores (zeroed by the caller).
+  float* block_scores;      // [B*Q][block_ld] or null
+  int64_t block_ld;
+  uint32_t* block_hist;     // [B*Q][2048] or null
+  // Reindex layer: score only the entries of the row's pool blocks (ascending
+  // block ids, -1 padded); scores are then indexed by pool slot (8*j + r is
+  // entry 8*pool[j] + r), -inf for slots that hold no visible entry.
+  const int32_t* pool;      // [B*Q][pool_ld] or null
+  int pool_blocks;          // a multiple of kPoolTileBlocks
+  int64_t pool_ld;          // a multiple of 4
   unsigned* status;
 };
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
@@ -118,6 +132,13 @@ struct TopkArgs {
   uint32_t* cand_key;       // [B*Q][cand_cap]
   int32_t* cand_idx;        // [B*Q][cand_cap]
   int cand_cap;             // <= kTopkCandCap
+  // Row extent: the visible entries V(t) by default; with vis_shift = s the
+  // ceil(V/2^s) blocks of 2^s entries (block scores); with a pool the row's
+  // valid pool slots, and the output positions map to entries through it.
+  int vis_shift;
+  const int32_t* pool;      // [B*Q][pool_ld] or null
+  int pool_blocks;
+  int64_t pool_ld;
   unsigned* status;
 };
 // Words per row of the top-k position bitmaps (a multiple of 4).

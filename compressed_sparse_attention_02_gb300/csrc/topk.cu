@@ -31,6 +31,11 @@
 //
 // A decode step's compressor entry (compress.cuh) can ride along: one extra
 // CTA per sequence computes it, so its latency hides behind the selection.
+//
+// The same kernel selects the hierarchical indexer's pool blocks (over the
+// block scores, ceil(V/8) of them) and a Reindex layer's entries (over the
+// pool's slots, mapped back to entries through the pool when written out);
+// "DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §11.
 #include "compress.cuh"
 #include "keys.cuh"
 #include "kernels.h"
@@ -212,10 +217,36 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-__device__ __forceinline__ int64_t visible_entries(const TopkArgs& a, int b, int q) {
-  const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[static_cast<int64_t>(b) * a.Q + q]) : a.pos_base + q;
+// The number of keys of the row: its visible entries; or their blocks
+// (vis_shift); or, with a pool, its valid slots: the pool holds
+// nb = min(pool_blocks, ceil(V/8)) ascending blocks, all entries visible but
+// those of block ceil(V/8)-1 past V, which can only be the pool's last.
+// *ventries receives V.
+__device__ __forceinline__ int64_t row_extent(const TopkArgs& a, int b, int q, int64_t* ventries) {
+  const int64_t row = static_cast<int64_t>(b) * a.Q + q;
+  const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row]) : a.pos_base + q;
   int64_t V = t >= 0 ? (t + 1) / a.m : 0;
-  return V > a.n_cap ? a.n_cap : V;
+  V = V > a.n_cap ? a.n_cap : V;
+  *ventries = V;
+  if (a.vis_shift) return (V + (int64_t(1) << a.vis_shift) - 1) >> a.vis_shift;
+  if (a.pool) {
+    const int64_t nvb = (V + kPoolBlock - 1) / kPoolBlock;
+    const int64_t nb = nvb < a.pool_blocks ? nvb : a.pool_blocks;
+    if (nb == 0) return 0;
+    const int32_t last = __ldg(a.pool + row * a.pool_ld + nb - 1);
+    return nb * kPoolBlock - (last == nvb - 1 ? nvb * kPoolBlock - V : 0);
+  }
+  return V;
+}
+
+// The entry a selected position stands for: itself, or with a pool the
+// entry in the slot's block; -1 where that is no visible entry (only a pool
+// that is not the Full layer's for this query leads there).
+__device__ __forceinline__ int32_t out_entry(const TopkArgs& a, int64_t row, int64_t ventries, int32_t p) {
+  if (!a.pool || p < 0) return p;
+  const int32_t blk = __ldg(a.pool + row * a.pool_ld + (p / kPoolBlock));
+  const int64_t e = static_cast<int64_t>(blk) * kPoolBlock + (p % kPoolBlock);
+  return (blk < 0 || e >= ventries) ? -1 : static_cast<int32_t>(e);
 }
 
 // The `need` lowest positions of the tie bitmap go to the extra list.
@@ -238,7 +269,8 @@ __device__ void take_ties(const uint32_t* ties, int64_t nwords, int need, Smem& 
 }
 
 // The finish of one row, run by the last of its CTAs.
-__device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Crossing& c, Smem& sm) {
+__device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
+                           Smem& sm) {
   const float* src = a.scores + row * a.score_ld;
   const uint32_t* bits = a.bits + row * a.bits_ld;
   uint32_t* ties = a.ties + row * a.bits_ld;
@@ -403,7 +435,7 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, const Cros
   float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
   for (int j = threadIdx.x; j < a.k; j += kThreads) {
     const int32_t p = j < out ? sm.u.c.sel[j] : -1;
-    idx[j] = p;
+    idx[j] = out_entry(a, row, ventries, p);
     if (sc) sc[j] = p >= 0 ? __ldg(src + p) + 0.0f : -INFINITY;
   }
 }
@@ -430,12 +462,13 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, con
   }
   const int b = blockIdx.z, q = blockIdx.y;
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
-  const int64_t V = visible_entries(a, b, q);
+  int64_t ventries;
+  const int64_t V = row_extent(a, b, q, &ventries);
   const float* src = a.scores + row * a.score_ld;
   if (V <= a.k) {  // every visible entry is selected; the row's first CTA writes it
     if (blockIdx.x != 0) return;
     for (int j = threadIdx.x; j < a.k; j += kThreads) {
-      a.idx_out[row * a.k + j] = j < V ? j : -1;
+      a.idx_out[row * a.k + j] = j < V ? out_entry(a, row, ventries, j) : -1;
       if (a.score_out) a.score_out[row * a.k + j] = j < V ? __ldg(src + j) + 0.0f : -INFINITY;
     }
     return;
@@ -537,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, con
   }
   __syncthreads();
   if (!sm.last) return;
-  finish_row(a, row, V, c, sm);
+  finish_row(a, row, V, ventries, c, sm);
 }
 
 }  // namespace
@@ -556,7 +589,10 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
     c = *ride_along;
     fill_inv_freq(&c);
   }
-  const int64_t chunks = (a.n_cap + kItems - 1) / kItems + (ride_along ? 1 : 0);
+  if (a.pool && (a.pool_blocks <= 0 || a.vis_shift)) return cudaErrorInvalidValue;
+  const int64_t extent = a.vis_shift ? (a.n_cap + (int64_t(1) << a.vis_shift) - 1) >> a.vis_shift
+                                     : (a.pool ? static_cast<int64_t>(a.pool_blocks) * kPoolBlock : a.n_cap);
+  const int64_t chunks = (extent + kItems - 1) / kItems + (ride_along ? 1 : 0);
   return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(chunks), a.Q, a.B), dim3(kThreads), 0, stream, a, c);
 }
 

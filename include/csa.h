@@ -81,7 +81,9 @@ enum {
   CSA_OP_INDEX_TOPK = 1,
   CSA_OP_SPARSE_ATTN = 2,
   CSA_OP_LAYER_DECODE = 3,
-  CSA_OP_LAYER_PREFILL = 4
+  CSA_OP_LAYER_PREFILL = 4,
+  CSA_OP_INDEX_TOPK_POOL = 5,
+  CSA_OP_REINDEX_TOPK = 6
 };
 
 /* Bytes of workspace the call `op` needs for B sequences of Q queries over a
@@ -210,6 +212,61 @@ csa_status csa_index_topk_static(const csa_params *p, int32_t B, int32_t Q,
                                  const uint16_t *wI, const uint8_t *kI,
                                  int64_t n_cap, int32_t *idx_out,
                                  float *score_out, void *stream);
+
+/*
+ * Hierarchical indexer ([CSA2 详解] §11 "Hierarchical Sparse Indexer"; §11.1
+ * on why the pool is larger than top-k; §20.1: a Reindex layer gathers the
+ * candidates before it scores them).  A Full layer scores every visible
+ * entry, keeps its own top-k, and hands on a candidate pool: entries grouped
+ * in blocks of CSA_POOL_BLOCK consecutive ones, a block scored by the largest
+ * score among its visible entries, the pool_blocks best blocks kept.  A
+ * Reindex layer scores only the pool's entries, with its own qI and wI, and
+ * takes its own top-k among them.
+ *
+ * csa_index_topk_pool — a Full layer: everything csa_index_topk does, plus
+ *   pool_out[b,q,:] = the min(pool_blocks, ceil(V/8)) block ids j (block j =
+ *   entries 8j .. 8j+7, those below V(t) counted) with the largest block
+ *   scores max_{s in block j, s < V} I[b,q,s], in ascending order, then -1.
+ *   Equal block scores: the smaller block id first.
+ *   pool_blocks : 16..2048, a multiple of 16 (the pages use 2048: at most
+ *                 16384 candidates).
+ *   pool_out    : [B][Q][pool_blocks] int32.
+ *   Workspace   : csa_workspace_size(CSA_OP_INDEX_TOPK_POOL, p, B, Q, n_cap).
+ *
+ * csa_reindex_topk — a Reindex layer over the pool a Full layer made for the
+ *   same q_pos (same B, Q, n_cap and pool_blocks):
+ *     I[b,q,s] = sum_h wI[b,q,h] * max(0, sum_c qI[b,q,h,c] * kI[b,s,c])
+ *   for the entries s of the pool's blocks with s < V(t) only; idx_out[b,q,:]
+ *   receives the min(topk, #pool entries) entries with the largest I in
+ *   ascending entry order (equal scores: the smaller entry), then -1;
+ *   score_out (optional) their fp32 scores, -inf in the -1 slots.  The key
+ *   rows read are those of the pool's blocks (1 KiB each, 16 per tensor-core
+ *   tile), so the cost is fixed by pool_blocks, not by V.
+ *   pool        : [B][Q][pool_blocks] int32 as csa_index_topk_pool wrote it.
+ *                 A pool from other inputs gives unspecified selections but
+ *                 no access outside kI (block ids past the cache record
+ *                 CSA_ERR_INDEX_RANGE and are not scored).
+ *   Workspace   : csa_workspace_size(CSA_OP_REINDEX_TOPK, p, B, Q, n_cap)
+ *                 (sized for pool_blocks = 2048).
+ *
+ * Other arguments, layouts, accuracy and errors are those of csa_index_topk.
+ * pool_blocks outside its range returns CSA_ERR_UNSUPPORTED.
+ */
+#define CSA_POOL_BLOCK 8
+csa_status csa_index_topk_pool(const csa_params *p, int32_t B, int32_t Q,
+                               const int32_t *q_pos, const uint8_t *qI,
+                               const uint16_t *wI, const uint8_t *kI,
+                               int64_t n_cap, int32_t *idx_out,
+                               float *score_out, int32_t pool_blocks,
+                               int32_t *pool_out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
+                            const int32_t *q_pos, const uint8_t *qI,
+                            const uint16_t *wI, const uint8_t *kI,
+                            int64_t n_cap, const int32_t *pool,
+                            int32_t pool_blocks, int32_t *idx_out,
+                            float *score_out, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * csa_sparse_attn — shared-KV MQA over [SWA rows || selected entries || sink].

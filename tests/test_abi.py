@@ -91,3 +91,36 @@ def test_host_validation_rejects_before_launch(lib):
     # empty batch is a no-op
     assert raw.csa_compress(P, 0, 4, i64(0), None, None, None, None, None, None, None, None, None, None, i64(0),
                             None) == 0
+
+
+def test_pool_calls_validate_and_size_their_workspace(lib):
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    raw.csa_index_topk_pool.restype = ctypes.c_int
+    raw.csa_reindex_topk.restype = ctypes.c_int
+    p = lib.csa_default_params()
+    P = ctypes.byref(p)
+    fake = ctypes.c_void_p(0x10000)
+    i64, sz = ctypes.c_int64, ctypes.c_size_t
+    big = sz(1 << 40)
+    # pool_blocks: 16..2048, a multiple of 16
+    for nb in (0, 8, 24, 2064):
+        assert raw.csa_index_topk_pool(P, 1, 1, fake, fake, fake, fake, i64(4096), fake, None, nb, fake, fake, big,
+                                       None) == 2
+        assert raw.csa_reindex_topk(P, 1, 1, fake, fake, fake, fake, i64(4096), fake, nb, fake, None, fake, big,
+                                    None) == 2
+    # a missing pool / pool output is an argument error
+    assert raw.csa_index_topk_pool(P, 1, 1, fake, fake, fake, fake, i64(4096), fake, None, 64, None, fake, big,
+                                   None) == 1
+    assert raw.csa_reindex_topk(P, 1, 1, fake, fake, fake, fake, i64(4096), None, 64, fake, None, fake, big,
+                                None) == 1
+    # workspace too small
+    assert raw.csa_index_topk_pool(P, 1, 1, fake, fake, fake, fake, i64(4096), fake, None, 64, fake, fake, sz(16),
+                                   None) == 6
+    assert raw.csa_reindex_topk(P, 1, 1, fake, fake, fake, fake, i64(4096), fake, 64, fake, None, fake, sz(16),
+                                None) == 6
+    # the Full layer's scratch holds the entries' and the blocks' selections
+    full = lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, p, 64, 1, 32768)
+    pool = lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK_POOL, p, 64, 1, 32768)
+    assert pool > full + 64 * (32768 // 8) * 4
+    # the Reindex layer's scratch holds 16384 slot scores per query
+    assert lib.csa_workspace_size(lib.CSA_OP_REINDEX_TOPK, p, 64, 1, 32768) >= 64 * 16384 * 4
