@@ -225,6 +225,7 @@ def run_ours(args, rank, world, local_rank):
         result.update(stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args))
         result["attn"].update(attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream))
         result["prefill"] = prefill_profile(csa, torch, dev)
+        result["hierarchical"] = [hierarchical_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -370,6 +371,70 @@ def prefill_profile(csa, torch, dev):
     res["indexer_keys"] = {"entries": B * n_new, "ms": kms, "gbs": kbytes / (kms * 1e-3) / 1e9,
                            "hbm_frac": kbytes / (kms * 1e-3) / 1e9 / hbm}
     del x, xk, kv, kI, idx, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
+    """The hierarchical indexer on a decode workload ("DeepSeek-V4 CSA/HCA 与
+    DeepSeek-V4.1 CSA2" §11): a Full layer (indexer + top-k + pool of 2048
+    blocks, 16384 candidates) against the plain indexer + top-k, and a
+    Reindex layer over the pool.  Query sets rotate (4 sets, each with its own
+    pool), so consecutive calls gather different key blocks."""
+    import synthetic as syn
+    hbm, _, _ = peaks()
+    w = syn.WORKLOADS[cfg]
+    B = w.B
+    kI = syn.indexer_keys(w.config, B, w.n_cap, device=dev, hadamard_rows=w.hadamard_kI)
+    pos = torch.full((B, 1), w.t, dtype=torch.int32, device=dev)
+    p = csa.csa_default_params(topk=w.topk)
+    qs = [syn.indexer_query(w.config + 2000 + 100 * r, B, 1, device=dev) for r in range(sets)]
+    q2 = [syn.indexer_query(w.config + 3000 + 100 * r, B, 1, device=dev) for r in range(sets)]
+    idx = torch.empty(B, 1, w.topk, dtype=torch.int32, device=dev)
+    pools = [torch.empty(B, 1, pool_blocks, dtype=torch.int32, device=dev) for _ in range(sets)]
+    ws_full = csa.workspace(csa.CSA_OP_INDEX_TOPK_POOL, p, B, 1, w.n_cap, device=dev)
+    ws_plain = csa.workspace(csa.CSA_OP_INDEX_TOPK, p, B, 1, w.n_cap, device=dev)
+    ws_re = csa.workspace(csa.CSA_OP_REINDEX_TOPK, p, B, 1, w.n_cap, device=dev)
+
+    def full(i):
+        q = qs[i % sets]
+        csa.csa_index_topk_pool(p, B, 1, pos, q["qI"], q["wI"], kI, w.n_cap, idx, None, pool_blocks,
+                                pools[i % sets], ws_full)
+
+    def plain(i):
+        q = qs[i % sets]
+        csa.csa_index_topk(p, B, 1, pos, q["qI"], q["wI"], kI, w.n_cap, idx, None, ws_plain)
+
+    def reindex(i):
+        q = q2[i % sets]
+        csa.csa_reindex_topk(p, B, 1, pos, q["qI"], q["wI"], kI, w.n_cap, pools[i % sets], pool_blocks, idx, None,
+                             ws_re)
+
+    def timed(fn, n=200):
+        for i in range(2 * sets):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    res = {"workload": w.name, "pool_blocks": pool_blocks, "candidates": pool_blocks * 8,
+           "full_layer_ms": timed(full), "index_topk_ms": timed(plain), "reindex_ms": timed(reindex)}
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the hierarchical indexer")
+    V = (w.t + 1) // w.m
+    cand = min(pool_blocks, (V + 7) // 8) * 8
+    rbytes = B * (cand * 128 + 64 * 128 + 64 * 2)
+    res["reindex_gbs"] = rbytes / (res["reindex_ms"] * 1e-3) / 1e9
+    res["reindex_hbm_frac"] = res["reindex_gbs"] / hbm
+    res["reindex_bytes"] = rbytes
+    res["note"] = ("reindex bytes = the pool's key rows (1 KiB blocks gathered) + q^I + w^I per query; "
+                   "full_layer_ms includes the block-score top-k")
+    del kI, qs, q2, pools, ws_full, ws_plain, ws_re
     torch.cuda.empty_cache()
     return res
 

@@ -90,6 +90,7 @@ struct IndexWs {
   size_t scores_off, hist_off, count_off, done_off, bits_off, ties_off, cand_key_off, cand_idx_off, total;
   size_t zero_bytes;  // hist, candidate counts and row counters, cleared before each call
   int64_t score_ld, bits_ld;
+  int cand_cap;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -103,6 +104,7 @@ bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
   if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
   w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 4));
   w->bits_ld = csa::topk_bits_ld(n_cap);
+  w->cand_cap = csa::topk_cand_cap(n_cap);
   const size_t R = static_cast<size_t>(rows);
   w->scores_off = 0;
   size_t off = round_up(R * w->score_ld * 4, 256);
@@ -116,9 +118,9 @@ bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
   w->ties_off = off;
   off = round_up(off + R * w->bits_ld * 4, 256);
   w->cand_key_off = off;
-  off = round_up(off + R * csa::kTopkCandCap * 4, 256);
+  off = round_up(off + R * w->cand_cap * 4, 256);
   w->cand_idx_off = off;
-  off = round_up(off + R * csa::kTopkCandCap * 4, 256);
+  off = round_up(off + R * w->cand_cap * 4, 256);
   w->total = off;
   return true;
 }
@@ -157,7 +159,7 @@ void topk_scratch(csa::TopkArgs* ta, uint8_t* base, const IndexWs& w) {
   ta->row_done = reinterpret_cast<unsigned*>(base + w.done_off);
   ta->cand_key = reinterpret_cast<uint32_t*>(base + w.cand_key_off);
   ta->cand_idx = reinterpret_cast<int32_t*>(base + w.cand_idx_off);
-  ta->cand_cap = csa::kTopkCandCap;
+  ta->cand_cap = w.cand_cap;
 }
 
 // Shared body of csa_index_topk, the hierarchical indexer calls and the

@@ -57,7 +57,8 @@ constexpr int kIdxHeads = 64;   // indexer heads
 constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
-constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k row keeps
+constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k finish stages in shared memory
+constexpr int kTopkCandCapMax = 16384;  // the longest global candidate list of a row
 constexpr int kPoolBlock = 8;         // entries per block of the hierarchical indexer's pool
 constexpr int kPoolTileBlocks = 16;   // pool blocks per 128-key indexer tile
 
@@ -131,7 +132,7 @@ struct TopkArgs {
   unsigned* row_done;       // [B*Q], zeroed by the caller
   uint32_t* cand_key;       // [B*Q][cand_cap]
   int32_t* cand_idx;        // [B*Q][cand_cap]
-  int cand_cap;             // <= kTopkCandCap
+  int cand_cap;             // kTopkCandCap .. kTopkCandCapMax (topk_cand_cap)
   // Row extent: the visible entries V(t) by default; with vis_shift = s the
   // ceil(V/2^s) blocks of 2^s entries (block scores); with a pool the row's
   // valid pool slots, and the output positions map to entries through it.
@@ -143,6 +144,8 @@ struct TopkArgs {
 };
 // Words per row of the top-k position bitmaps (a multiple of 4).
 int64_t topk_bits_ld(int64_t n_cap);
+// Length of a row's candidate list for rows of up to n_cap keys.
+int topk_cand_cap(int64_t n_cap);
 // ride_along: optional decode-mode (mode 1) compressor arguments for the same
 // B sequences, computed by extra CTAs of the same launch (m for which
 // topk_can_carry_compress holds).

@@ -49,6 +49,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kItems = 4096;     // keys per CTA: 16 consecutive keys per thread
 constexpr int kLocalCap = 2048;  // candidates one CTA gathers before the row falls back
 constexpr int kEmitWords = 8;    // bitmap words a thread reads per round of the read-out
+constexpr int kBatch = 8;        // global loads a thread issues before using them (passes over global lists)
 constexpr int kRoundWords = kThreads * kEmitWords;
 static_assert(kItems == 16 * kThreads, "a thread covers half a bitmap word");
 static_assert(kTopkCandCap == kRoundWords && kLocalCap == kTopkCandCap && kRoundWords >= kMaxTopk,
@@ -182,9 +183,18 @@ __device__ uint32_t resolve_threshold(uint32_t dstar, int64_t n, KeyAt key_at, S
     const uint32_t mask = pass == 0 ? 0xFFE00000u : 0xFFFFFC00u;
     for (int i = threadIdx.x; i < nb; i += kThreads) sm.h.hist[i] = 0;
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t k = key_at(i);
-      if ((k & mask) == prefix) atomicAdd(&sm.h.hist[(k >> shift) & (nb - 1)], 1);
+    for (int64_t i0 = 0; i0 < n; i0 += kBatch * kThreads) {  // kBatch independent loads in flight
+      uint32_t kk[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = i0 + u * kThreads + threadIdx.x;
+        kk[u] = i < n ? key_at(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t i = i0 + u * kThreads + threadIdx.x;
+        if (i < n && (kk[u] & mask) == prefix) atomicAdd(&sm.h.hist[(kk[u] >> shift) & (nb - 1)], 1);
+      }
     }
     __syncthreads();
     const Crossing c = find_crossing(nb, *need, sm);
@@ -268,6 +278,36 @@ __device__ void take_ties(const uint32_t* ties, int64_t nwords, int need, Smem& 
   }
 }
 
+// Calls f(key, position) for each of the row's nc candidates: from shared
+// memory where the list is staged there, else from the global list, kBatch
+// independent loads per thread at a time.  A position outside [0, V) (never
+// written by this row's filter) reads as key 0 at position 0, the lowest key.
+template <class F>
+__device__ __forceinline__ void for_candidates(bool staged, int nc, const Smem& sm, const uint32_t* gkey,
+                                               const int32_t* gpos, int64_t V, F f) {
+  if (staged) {
+    for (int i = threadIdx.x; i < nc; i += kThreads) f(sm.u.c.ckey[i], sm.u.c.cpos[i]);
+    return;
+  }
+  for (int i0 = 0; i0 < nc; i0 += kBatch * kThreads) {
+    uint32_t kk[kBatch];
+    int32_t pp[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kThreads + static_cast<int>(threadIdx.x);
+      kk[u] = i < nc ? __ldcg(gkey + i) : 0u;
+      pp[u] = i < nc ? __ldcg(gpos + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kThreads + static_cast<int>(threadIdx.x);
+      if (i >= nc) continue;
+      const bool ok = pp[u] >= 0 && pp[u] < V;
+      f(ok ? kk[u] : 0u, ok ? pp[u] : 0);
+    }
+  }
+}
+
 // The finish of one row, run by the last of its CTAs.
 __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
                            Smem& sm) {
@@ -306,35 +346,40 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
     int n_eq = 0;
     if (ncu <= static_cast<unsigned>(a.cand_cap)) {
       const int nc = static_cast<int>(ncu);
-      for (int i = threadIdx.x; i < nc; i += kThreads) {
-        const int32_t p = __ldcg(a.cand_idx + row * a.cand_cap + i);
-        const bool ok = p >= 0 && p < V;  // positions come from this row's filter; checked all the same
-        sm.u.c.ckey[i] = ok ? __ldcg(a.cand_key + row * a.cand_cap + i) : 0u;
-        sm.u.c.cpos[i] = ok ? p : 0;
+      const uint32_t* gkey = a.cand_key + row * a.cand_cap;
+      const int32_t* gpos = a.cand_idx + row * a.cand_cap;
+      const bool staged = nc <= kTopkCandCap;  // a longer list is read from global memory in each pass
+      if (staged) {
+        for (int i = threadIdx.x; i < nc; i += kThreads) {
+          const int32_t p = __ldcg(gpos + i);
+          const bool ok = p >= 0 && p < V;  // positions come from this row's filter; checked all the same
+          sm.u.c.ckey[i] = ok ? __ldcg(gkey + i) : 0u;
+          sm.u.c.cpos[i] = ok ? p : 0;
+        }
       }
       // the next 11 bits of the candidates' keys
       for (int i = threadIdx.x; i < 2048; i += kThreads) sm.h.hist[i] = 0;
       if (threadIdx.x == 0) sm.nsmall = 0;
       __syncthreads();
-      for (int i = threadIdx.x; i < nc; i += kThreads)
-        atomicAdd(&sm.h.hist[(sm.u.c.ckey[i] >> 10) & 2047], 1);
+      for_candidates(staged, nc, sm, gkey, gpos, V,
+                     [&](uint32_t k, int32_t) { atomicAdd(&sm.h.hist[(k >> 10) & 2047], 1); });
       __syncthreads();
       const Crossing cc = find_crossing(2048, need, sm);
       const uint32_t p22 = (dstar << 11) | static_cast<uint32_t>(cc.bin);  // the crossing bin's top 22 bits
       const int need2 = need - cc.above;
       if (cc.in_bin <= 32) {
         // keys above the bin are taken; the bin's keys are ranked by one warp
-        for (int i = threadIdx.x; i < nc; i += kThreads) {
-          const uint32_t k22 = sm.u.c.ckey[i] >> 10;
-          if (k22 > p22) mark(sm, sm.u.c.cpos[i]);
+        for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t p) {
+          const uint32_t k22 = k >> 10;
+          if (k22 > p22) mark(sm, p);
           if (k22 == p22) {
             const int slot = atomicAdd(&sm.nsmall, 1);
             if (slot < 32) {
-              sm.small_key[slot] = sm.u.c.ckey[i];
-              sm.small_pos[slot] = sm.u.c.cpos[i];
+              sm.small_key[slot] = k;
+              sm.small_pos[slot] = p;
             }
           }
-        }
+        });
         __syncthreads();
         if (threadIdx.x < 32) {
           const int nb = min(sm.nsmall, 32);
@@ -355,10 +400,9 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
         {
           for (int i = threadIdx.x; i < 1024; i += kThreads) sm.h.hist[i] = 0;
           __syncthreads();
-          for (int i = threadIdx.x; i < nc; i += kThreads) {
-            const uint32_t k = sm.u.c.ckey[i];
+          for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t) {
             if ((k >> 10) == p22) atomicAdd(&sm.h.hist[k & 1023], 1);
-          }
+          });
           __syncthreads();
           const Crossing c2 = find_crossing(1024, need2, sm);
           thr = (p22 << 10) | static_cast<uint32_t>(c2.bin);
@@ -366,12 +410,10 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
           n_eq = c2.in_bin;
         }
         const bool all_eq = n_eq == need;  // every key equal to thr is taken
-        for (int i = threadIdx.x; i < nc; i += kThreads) {
-          const uint32_t k = sm.u.c.ckey[i];
-          const int p = sm.u.c.cpos[i];
+        for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t p) {
           if (k > thr || (k == thr && all_eq)) mark(sm, p);
           if (k == thr && !all_eq) atomicOr(ties + (p >> 5), 1u << (p & 31));
-        }
+        });
         if (!all_eq) take_ties(ties, nwords, need, sm);
       }
     } else {
@@ -379,13 +421,22 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
       const uint32_t thr =
           resolve_threshold(dstar, V, [&](int64_t i) { return score_key(__ldg(src + i)); }, sm, &need, &n_eq);
       const bool all_eq = n_eq == need;
-      for (int64_t base = 0; base < V; base += kThreads) {
-        const int64_t i = base + threadIdx.x;
-        const uint32_t k = i < V ? score_key(__ldg(src + i)) : 0u;
-        const bool in = i < V && (k >> kKeyBinShift) == dstar;
-        if (in && (k > thr || (k == thr && all_eq))) mark(sm, static_cast<int32_t>(i));
-        const unsigned em = __ballot_sync(0xffffffffu, in && k == thr && !all_eq);
-        if (lane == 0 && em) atomicOr(ties + ((i - lane) >> 5), em);
+      for (int64_t i0 = 0; i0 < V; i0 += kBatch * kThreads) {
+        float xv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t i = i0 + u * kThreads + threadIdx.x;
+          xv[u] = i < V ? __ldg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t i = i0 + u * kThreads + threadIdx.x;
+          const uint32_t k = i < V ? score_key(xv[u]) : 0u;
+          const bool in = i < V && (k >> kKeyBinShift) == dstar;
+          if (in && (k > thr || (k == thr && all_eq))) mark(sm, static_cast<int32_t>(i));
+          const unsigned em = __ballot_sync(0xffffffffu, in && k == thr && !all_eq);
+          if (lane == 0 && em) atomicOr(ties + ((i - lane) >> 5), em);
+        }
       }
       if (!all_eq) take_ties(ties, nwords, need, sm);
     }
@@ -579,9 +630,18 @@ bool topk_can_carry_compress(int m) { return m == 1 || m == 2 || m == 4; }
 
 int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + kEmitWords - 1) / kEmitWords * kEmitWords; }
 
+// A sixteenth of the row, in whole 256-entry steps, within the staged size
+// and the largest list: the crossing digit (a quarter octave of scores) holds
+// a small fraction of a long row, and past the list the row is resolved from
+// its scores.
+int topk_cand_cap(int64_t n_cap) {
+  const int64_t c = (n_cap / 16 + 255) / 256 * 256;
+  return static_cast<int>(c < kTopkCandCap ? kTopkCandCap : (c > kTopkCandCapMax ? kTopkCandCapMax : c));
+}
+
 cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  if (a.cand_cap > kTopkCandCap) return cudaErrorInvalidValue;
+  if (a.cand_cap < kTopkCandCap || a.cand_cap > kTopkCandCapMax) return cudaErrorInvalidValue;
   CompressArgs c = {};
   if (ride_along) {
     if (ride_along->mode != 1 || ride_along->B != a.B || !topk_can_carry_compress(ride_along->m))

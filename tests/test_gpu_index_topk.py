@@ -111,7 +111,7 @@ def test_position_beyond_cache_is_reported(csa):
                                                              bits(kI[0])), 16)
 
 
-@pytest.mark.parametrize("cfg,samples", [(1, [0, 31]), (2, [0, 29, 63]), (3, [5])])
+@pytest.mark.parametrize("cfg,samples", [(1, [0, 31]), (2, [0, 29, 63]), (3, [5, 7])])
 def test_full_size_decode_configs_sampled(csa, cfg, samples):
     """The decode configurations at full size in the launch configuration the
     benchmark times; every sequence runs, sampled sequences are checked."""
@@ -167,3 +167,22 @@ def test_selection_is_exactly_the_keys_of_one_score(csa):
     idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
     assert np.array_equal(idx[0, 0], np.arange(0, n_cap, 16))
     check_row(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, what="one score")
+
+
+@pytest.mark.parametrize("period,k", [(100, 1500), (80, 1000), (600, 2000), (15, 2048)])
+def test_long_candidate_list_read_from_global_memory(csa, period, k):
+    """80000 visible entries whose keys repeat with a period: with periods
+    100, 80 and 600 the crossing digit holds 3200, 4000 and 2532 candidates,
+    more than a finish stages in shared memory (2048) but within the row's
+    list (5120), so every pass reads them from global memory (period 100: 800
+    equal keys at the threshold, 500 of them taken; period 80: the 1000 equal
+    keys at the threshold are exactly the keys still needed).  Period 37 puts
+    6486 candidates in the digit, past the list: the row is resolved from its
+    scores."""
+    n_cap = 80000
+    x = syn.indexer_query(8, 1, 1)
+    kI = periodic_keys(8, n_cap, period)
+    p = csa.csa_default_params(topk=k)
+    t = 4 * n_cap - 1
+    idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
+    check_row(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, what="period %d" % period)
