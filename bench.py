@@ -422,8 +422,19 @@ def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
+    def stages(fn, n=100):  # indexer kernel / top-k launches, from the call's trace events
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for i in range(n):
+            csa.csa_set_trace_events(evs[i])
+            fn(i)
+        csa.csa_set_trace_events(None)
+        torch.cuda.synchronize()
+        return [sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(n)) / n for s in (1, 2)]
+
     res = {"workload": w.name, "pool_blocks": pool_blocks, "candidates": pool_blocks * 8,
            "full_layer_ms": timed(full), "index_topk_ms": timed(plain), "reindex_ms": timed(reindex)}
+    res["full_layer_stages_ms"] = dict(zip(("index_scores", "topk_and_pool"), stages(full)))
+    res["reindex_stages_ms"] = dict(zip(("index_scores", "topk"), stages(reindex)))
     if csa.csa_check_status() != 0:
         raise RuntimeError("device status after the hierarchical indexer")
     V = (w.t + 1) // w.m
@@ -431,9 +442,14 @@ def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
     rbytes = B * (cand * 128 + 64 * 128 + 64 * 2)
     res["reindex_gbs"] = rbytes / (res["reindex_ms"] * 1e-3) / 1e9
     res["reindex_hbm_frac"] = res["reindex_gbs"] / hbm
+    kms = res["reindex_stages_ms"]["index_scores"]
+    res["reindex_kernel_gbs"] = rbytes / (kms * 1e-3) / 1e9
+    res["reindex_kernel_hbm_frac"] = res["reindex_kernel_gbs"] / hbm
     res["reindex_bytes"] = rbytes
     res["note"] = ("reindex bytes = the pool's key rows (1 KiB blocks gathered) + q^I + w^I per query; "
-                   "full_layer_ms includes the block-score top-k")
+                   "full_layer_ms includes the block-score top-k; *_stages_ms from events between the "
+                   "launches (which break their programmatic overlap); reindex_kernel_* = the indexer "
+                   "kernel alone")
     del kI, qs, q2, pools, ws_full, ws_plain, ws_re
     torch.cuda.empty_cache()
     return res

@@ -100,11 +100,10 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // count and the count of CTAs done with the row (contiguous, so one memset
 // clears them); the two position bitmaps; the candidate keys and positions.
 bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
-  (void)k;
   if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
   w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 4));
   w->bits_ld = csa::topk_bits_ld(n_cap);
-  w->cand_cap = csa::topk_cand_cap(n_cap);
+  w->cand_cap = csa::topk_cand_cap(n_cap, k);
   const size_t R = static_cast<size_t>(rows);
   w->scores_off = 0;
   size_t off = round_up(R * w->score_ld * 4, 256);
@@ -137,8 +136,10 @@ struct PoolSpec {
 
 // Full layer scratch: the entries' indexer scratch, then the same layout for
 // the ceil(n_cap/8) block scores.
-bool pool_workspace(int64_t rows, int64_t n_cap, IndexWs* w, IndexWs* wb, size_t* total) {
-  if (!index_workspace(rows, n_cap, 0, w) || !index_workspace(rows, (n_cap + 7) / 8, 0, wb)) return false;
+bool pool_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w, IndexWs* wb, size_t* total) {
+  // (the block selection is sized for the largest pool, 2048 blocks)
+  if (!index_workspace(rows, n_cap, k, w) || !index_workspace(rows, (n_cap + 7) / 8, csa::kMaxTopk, wb))
+    return false;
   *total = w->total + wb->total;
   return true;
 }
@@ -177,7 +178,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     sized = index_workspace(rows, static_cast<int64_t>(pool->blocks) * csa::kPoolBlock, p->topk, &w);
     need = w.total;
   } else if (pool && pool->out) {
-    sized = pool_workspace(rows, n_cap, &w, &wb, &need);
+    sized = pool_workspace(rows, n_cap, p->topk, &w, &wb, &need);
   } else {
     sized = index_workspace(rows, n_cap, p->topk, &w);
     need = w.total;
@@ -194,6 +195,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   if (!zeroed && cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
   if (pool && pool->out && cudaMemsetAsync(wsb_blk + wb.hist_off, 0, wb.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
+  if (traced && pool) trace(1, st);  // the hierarchical calls' own trace starts at the indexer
 
   csa::IndexArgs ia = {};
   ia.qI = qI;
@@ -240,17 +242,18 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     ta.pool_ld = pool->blocks;
   }
   ta.status = status;
-  s = cuda_status(csa::launch_topk(ta, ride_along, st));
-  if (s != CSA_OK || !(pool && pool->out)) return s;
-
-  // the pool: the top `blocks` block scores, block ids ascending
-  csa::TopkArgs tb = ta;
-  topk_scratch(&tb, wsb_blk, wb);
-  tb.k = pool->blocks;
-  tb.vis_shift = 3;
-  tb.idx_out = pool->out;
-  tb.score_out = nullptr;
-  return cuda_status(csa::launch_topk(tb, nullptr, st));
+  csa::TopkArgs tb = {};
+  if (pool && pool->out) {  // the pool, in the same launch: the top `blocks` block scores, ids ascending
+    tb = ta;
+    topk_scratch(&tb, wsb_blk, wb);
+    tb.k = pool->blocks;
+    tb.vis_shift = 3;
+    tb.idx_out = pool->out;
+    tb.score_out = nullptr;
+  }
+  s = cuda_status(csa::launch_topk(ta, ride_along, st, pool && pool->out ? &tb : nullptr));
+  if (s == CSA_OK && traced && pool) trace(3, st);
+  return s;
 }
 
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
@@ -385,7 +388,7 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
     case CSA_OP_INDEX_TOPK_POOL: {
       IndexWs wb;
       size_t total = 0;
-      return pool_workspace(static_cast<int64_t>(B) * Q, n_cap, &w, &wb, &total) ? total : 0;
+      return pool_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w, &wb, &total) ? total : 0;
     }
     case CSA_OP_REINDEX_TOPK:  // sized for the largest pool
       return index_workspace(static_cast<int64_t>(B) * Q, static_cast<int64_t>(csa::kMaxTopk) * csa::kPoolBlock,
@@ -489,7 +492,7 @@ csa_status csa_index_topk_pool(const csa_params* p, int32_t B, int32_t Q, const 
   ps.out = pool_out;
   ps.blocks = pool_blocks;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
-                        static_cast<cudaStream_t>(stream), false, false, nullptr, &ps);
+                        static_cast<cudaStream_t>(stream), g_trace_on, false, nullptr, &ps);
 }
 
 csa_status csa_reindex_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
@@ -508,7 +511,7 @@ csa_status csa_reindex_topk(const csa_params* p, int32_t B, int32_t Q, const int
   ps.in = pool;
   ps.blocks = pool_blocks;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
-                        static_cast<cudaStream_t>(stream), false, false, nullptr, &ps);
+                        static_cast<cudaStream_t>(stream), g_trace_on, false, nullptr, &ps);
 }
 
 csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint16_t* q,

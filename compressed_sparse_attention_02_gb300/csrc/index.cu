@@ -189,7 +189,88 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && a.pool && QPC == 1) {
+    // ---------------- TMA producer, Reindex layer (whole warp) ----------------
+    // A tile is 16 pool blocks of 8 keys; lane l < 16 loads slot l's block
+    // into its 1 KiB swizzle atom with its own TMA box.  Unit u's block ids
+    // are pool[16u .. 16u+15] (one query per group, pool_ld == pool_blocks);
+    // every lane keeps its slot's ids for the next kAhead units in flight.
+    // A slot without a block, or with an id outside the cache, loads block 0,
+    // which the epilogue does not score.
+    constexpr int kAhead = 4;
+    const int64_t n_blk = (a.n_cap + kPoolBlock - 1) / kPoolBlock;
+    const int32_t* ids = a.pool + (lane & (kPoolTileBlocks - 1));
+    int32_t ring[kAhead];
+#pragma unroll
+    for (int d = 0; d < kAhead; ++d) ring[d] = u0 + d < u1 ? __ldg(ids + kPoolTileBlocks * (u0 + d)) : 0;
+    if (lane == 0) {
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_q);
+    }
+    const uint64_t pol = policy_evict_first();
+    uint32_t issued = 0, parity = 0;
+    uint32_t q_uses[2] = {0, 0};
+    int64_t seen_g = -1;
+    bool active = false;
+    GroupInfo gi{};
+    int qb = 1, it = 0;
+    bool ok = true;
+    int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
+    for (int64_t u = u0; u < u1 && ok; ++u) {
+      const int32_t id = ring[0];
+#pragma unroll
+      for (int d = 0; d + 1 < kAhead; ++d) ring[d] = ring[d + 1];
+      ring[kAhead - 1] = u + kAhead < u1 ? __ldg(ids + kPoolTileBlocks * (u + kAhead)) : 0;
+      if (++tile == tiles_per_group) {
+        tile = 0;
+        ++g;
+      }
+      if (g != seen_g) {
+        gi = group_info<QPC>(a, g, groups_per_seq);
+        seen_g = g;
+        active = gi.vmax > tile * kTileKeys;
+        if (active) {
+          qb ^= 1;
+          if (lane == 0) {
+            if (q_uses[qb] > 0) ok = mbar_wait(&q_empty[qb], (q_uses[qb] - 1) & 1u, a.status);
+            if (ok) {
+              mbar_arrive_expect_tx(&q_full[qb], kQBytes);
+              tma_load_2d(q_s + qb * kQBytes, &tm_q, 0,
+                          static_cast<int32_t>((static_cast<int64_t>(gi.b) * a.Q + gi.q0) * kIdxHeads), &q_full[qb]);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          ++q_uses[qb];
+        }
+      }
+      if (!active || tile * kTileKeys >= gi.vmax) continue;
+      const int st = it % STAGES;
+      const uint32_t use = static_cast<uint32_t>(it / STAGES);
+      if (lane == 0) {
+        if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, a.status);
+        if (ok) mbar_arrive_expect_tx(&full[st], kKeyTileBytes);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < kPoolTileBlocks) {
+        const int32_t blk = (id >= 0 && id < n_blk) ? id : 0;
+        tma_load_3d(k_s + st * kKeyTileBytes + lane * (kPoolBlock * kIdxDim), &tm_k, 0, blk * kPoolBlock, gi.b,
+                    &full[st], pol);
+      }
+      issued |= 1u << st;
+      parity = (parity & ~(1u << st)) | ((use & 1u) << st);
+      ++it;
+    }
+    // Our own copies must have landed before the CTA may exit.
+    if (lane == 0) {
+      for (int x = 0; x < STAGES; ++x)
+        if (issued & (1u << x)) mbar_wait(&full[x], (parity >> x) & 1u, a.status);
+      for (int x = 0; x < 2; ++x)
+        if (q_uses[x]) mbar_wait(&q_full[x], (q_uses[x] - 1) & 1u, a.status);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
@@ -228,28 +309,7 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
         if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
         mbar_arrive_expect_tx(&full[s], kKeyTileBytes);
-        if (a.pool) {
-          // 16 blocks of 8 keys, each into its own 1 KiB swizzle atom; slots
-          // without a block (or with an id outside the cache) load block 0,
-          // which the epilogue does not score
-          const int4* ids = reinterpret_cast<const int4*>(a.pool + (static_cast<int64_t>(gi.b) * a.Q + gi.q0) * a.pool_ld +
-                                                          tile * kPoolTileBlocks);
-          const int64_t n_blk = (a.n_cap + kPoolBlock - 1) / kPoolBlock;
-#pragma unroll
-          for (int v = 0; v < kPoolTileBlocks / 4; ++v) {
-            const int4 q4 = __ldg(ids + v);
-            const int32_t id[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int32_t blk = (id[e] >= 0 && id[e] < n_blk) ? id[e] : 0;
-              tma_load_3d(k_s + s * kKeyTileBytes + (4 * v + e) * (kPoolBlock * kIdxDim), &tm_k, 0,
-                          blk * kPoolBlock, gi.b, &full[s], pol);
-            }
-          }
-        } else {
-          tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s],
-                      pol);
-        }
+        tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s], pol);
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | ((use & 1u) << s);
         ++it;
@@ -480,7 +540,7 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
                                 cudaStream_t stream) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  if (a.pool && (a.pool_blocks <= 0 || a.pool_blocks % kPoolTileBlocks != 0 || a.pool_ld % 4 != 0))
+  if (a.pool && (a.pool_blocks <= 0 || a.pool_blocks % kPoolTileBlocks != 0 || a.pool_ld != a.pool_blocks))
     return cudaErrorInvalidValue;
   if (a.Q >= 4 && !a.pool) return launch_qpc<4>(a, encode, stream);  // a pool is per query: one query per tile
   return launch_qpc<1>(a, encode, stream);

@@ -144,13 +144,16 @@ struct TopkArgs {
 };
 // Words per row of the top-k position bitmaps (a multiple of 4).
 int64_t topk_bits_ld(int64_t n_cap);
-// Length of a row's candidate list for rows of up to n_cap keys.
-int topk_cand_cap(int64_t n_cap);
+// Length of a row's candidate list for a top-k of rows of up to n_cap keys.
+int topk_cand_cap(int64_t n_cap, int k);
 // ride_along: optional decode-mode (mode 1) compressor arguments for the same
 // B sequences, computed by extra CTAs of the same launch (m for which
 // topk_can_carry_compress holds).
 bool topk_can_carry_compress(int m);
-cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream);
+// second: an optional independent selection run by the same launch (its
+// sequences after a's along the grid); not together with a ride-along.
+cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream,
+                        const TopkArgs* second = nullptr);
 
 // ---- sparse attention (tcgen05, bf16) ------------------------------------------------
 struct AttnArgs {

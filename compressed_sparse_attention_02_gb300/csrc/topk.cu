@@ -503,7 +503,11 @@ __device__ void compress_ride_along(const CompressArgs& c, int b, Smem& sm) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, const CompressArgs comp) {
+// Grid: x the 4096-key chunks of a row (plus the ride-along column), y the
+// queries, z the sequences of problem a0 and then those of problem a1 (a
+// second, independent selection over other scores, e.g. the pool's blocks).
+__global__ void __launch_bounds__(kThreads, 4)
+    topk_kernel(const __grid_constant__ TopkArgs a0, const __grid_constant__ TopkArgs a1, const CompressArgs comp) {
   __shared__ Smem sm;
   pdl_launch_dependents();
   pdl_wait();
@@ -511,7 +515,10 @@ __global__ void __launch_bounds__(kThreads, 4) topk_kernel(const TopkArgs a, con
     if (blockIdx.y == 0) compress_ride_along(comp, blockIdx.z, sm);
     return;
   }
-  const int b = blockIdx.z, q = blockIdx.y;
+  const bool second = static_cast<int>(blockIdx.z) >= a0.B;
+  const TopkArgs& a = second ? a1 : a0;
+  const int b = static_cast<int>(blockIdx.z) - (second ? a0.B : 0), q = blockIdx.y;
+  if (q >= a.Q) return;
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   int64_t ventries;
   const int64_t V = row_extent(a, b, q, &ventries);
@@ -630,30 +637,57 @@ bool topk_can_carry_compress(int m) { return m == 1 || m == 2 || m == 4; }
 
 int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + kEmitWords - 1) / kEmitWords * kEmitWords; }
 
-// A sixteenth of the row, in whole 256-entry steps, within the staged size
-// and the largest list: the crossing digit (a quarter octave of scores) holds
-// a small fraction of a long row, and past the list the row is resolved from
-// its scores.
-int topk_cand_cap(int64_t n_cap) {
-  const int64_t c = (n_cap / 16 + 255) / 256 * 256;
+// The larger of a sixteenth of the row and four times k (the crossing digit,
+// a quarter octave of scores, holds a small fraction of a long row, or a few
+// times k where k is a large part of it), at most the row, in whole 256-entry
+// steps within the staged size and the largest list.  Past the list a row is
+// resolved from its scores.
+int topk_cand_cap(int64_t n_cap, int k) {
+  int64_t c = n_cap / 16 > 4 * static_cast<int64_t>(k) ? n_cap / 16 : 4 * static_cast<int64_t>(k);
+  c = c < n_cap ? c : n_cap;
+  c = (c + 255) / 256 * 256;
   return static_cast<int>(c < kTopkCandCap ? kTopkCandCap : (c > kTopkCandCapMax ? kTopkCandCapMax : c));
 }
 
-cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream) {
+namespace {
+
+// The longest row of a selection: the cache's entries, their blocks, or the
+// pool's slots.
+int64_t topk_extent(const TopkArgs& a) {
+  return a.vis_shift ? (a.n_cap + (int64_t(1) << a.vis_shift) - 1) >> a.vis_shift
+                     : (a.pool ? static_cast<int64_t>(a.pool_blocks) * kPoolBlock : a.n_cap);
+}
+
+bool topk_args_ok(const TopkArgs& a) {
+  return a.cand_cap >= kTopkCandCap && a.cand_cap <= kTopkCandCapMax && !(a.pool && (a.pool_blocks <= 0 || a.vis_shift));
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaStream_t stream,
+                        const TopkArgs* second) {
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
-  if (a.cand_cap < kTopkCandCap || a.cand_cap > kTopkCandCapMax) return cudaErrorInvalidValue;
+  if (!topk_args_ok(a)) return cudaErrorInvalidValue;
   CompressArgs c = {};
   if (ride_along) {
-    if (ride_along->mode != 1 || ride_along->B != a.B || !topk_can_carry_compress(ride_along->m))
+    if (ride_along->mode != 1 || ride_along->B != a.B || !topk_can_carry_compress(ride_along->m) || second)
       return cudaErrorInvalidValue;
     c = *ride_along;
     fill_inv_freq(&c);
   }
-  if (a.pool && (a.pool_blocks <= 0 || a.vis_shift)) return cudaErrorInvalidValue;
-  const int64_t extent = a.vis_shift ? (a.n_cap + (int64_t(1) << a.vis_shift) - 1) >> a.vis_shift
-                                     : (a.pool ? static_cast<int64_t>(a.pool_blocks) * kPoolBlock : a.n_cap);
-  const int64_t chunks = (extent + kItems - 1) / kItems + (ride_along ? 1 : 0);
-  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(chunks), a.Q, a.B), dim3(kThreads), 0, stream, a, c);
+  TopkArgs b = {};  // no second problem: B = 0
+  int64_t chunks = (topk_extent(a) + kItems - 1) / kItems;
+  int q = a.Q;
+  if (second && second->B > 0 && second->Q > 0) {
+    if (!topk_args_ok(*second)) return cudaErrorInvalidValue;
+    b = *second;
+    const int64_t c2 = (topk_extent(b) + kItems - 1) / kItems;
+    chunks = c2 > chunks ? c2 : chunks;
+    q = b.Q > q ? b.Q : q;
+  }
+  chunks += ride_along ? 1 : 0;
+  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(chunks), q, a.B + b.B), dim3(kThreads), 0, stream, a,
+                    b, c);
 }
 
 }  // namespace csa
