@@ -174,7 +174,7 @@ csa_status csa_compress_indexer_keys(
  *         exceed n_cap (else CSA_ERR_INDEX_RANGE is recorded and V is clamped).
  * qI    : [B][Q][64][128] e4m3.      wI : [B][Q][64] bf16 (scale included).
  * kI    : [B][n_cap][128] e4m3 indexer keys, entry numbering shared with the
- *         main compressed KV ([hca_csa] "K^IComp 与主压缩 KV 一一对应").
+ *         main compressed KV (one indexer key per compressed entry, [hca_csa]).
  * idx_out: [B][Q][topk] int32.  score_out: [B][Q][topk] fp32 or NULL.
  * Accuracy: FP8 products are exact; they are accumulated in fp32 by the tensor
  * cores and the head sum is fp32.

@@ -243,7 +243,7 @@ static int orc_by_index(const void *pa, const void *pb) {
 
 /* The min(k, V) entries with the largest scores (ties toward the smaller
  * index), written in ascending entry order, then -1 up to k slots.  Returns
- * the number of selected entries.  Sorting "按位置" follows [结构对比] CSA2. */
+ * the number of selected entries.  The ascending (position) order follows [结构对比]'s CSA2 section. */
 int orc_topk(int64_t V, int k, const double *scores, int32_t *idx) {
   orc_scored *all = (orc_scored *)malloc(sizeof(orc_scored) * (size_t)(V > 0 ? V : 1));
   for (int64_t s = 0; s < V; ++s) {
