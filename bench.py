@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
+    ap.add_argument("--section", choices=["decode", "reindex"], default="decode",
+                    help="reindex: only the hierarchical indexer's Reindex layer on --workload (4 Full-layer "
+                         "calls make the pools, then --warmup and --steps Reindex calls; for profiling)")
     return ap.parse_args()
 
 
@@ -455,6 +458,49 @@ def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
     return res
 
 
+def reindex_section(args, pool_blocks=2048, sets=4):
+    """The Reindex layer alone (for profiling captures): the Full layer makes
+    one pool per query set (4 calls), then warm-up and timed Reindex calls
+    rotate over the sets."""
+    import torch
+
+    import compressed_sparse_attention_02_gb300 as csa
+    import synthetic as syn
+    dev = torch.device("cuda", 0)
+    w = syn.WORKLOADS[args.workload]
+    B = args.batch or w.B
+    kI = syn.indexer_keys(w.config, B, w.n_cap, device=dev, hadamard_rows=w.hadamard_kI)
+    pos = torch.full((B, 1), w.t, dtype=torch.int32, device=dev)
+    p = csa.csa_default_params(topk=w.topk)
+    qs = [syn.indexer_query(w.config + 2000 + 100 * r, B, 1, device=dev) for r in range(sets)]
+    q2 = [syn.indexer_query(w.config + 3000 + 100 * r, B, 1, device=dev) for r in range(sets)]
+    idx = torch.empty(B, 1, w.topk, dtype=torch.int32, device=dev)
+    pools = [torch.empty(B, 1, pool_blocks, dtype=torch.int32, device=dev) for _ in range(sets)]
+    ws_full = csa.workspace(csa.CSA_OP_INDEX_TOPK_POOL, p, B, 1, w.n_cap, device=dev)
+    ws_re = csa.workspace(csa.CSA_OP_REINDEX_TOPK, p, B, 1, w.n_cap, device=dev)
+    for r in range(sets):
+        csa.csa_index_topk_pool(p, B, 1, pos, qs[r]["qI"], qs[r]["wI"], kI, w.n_cap, idx, None, pool_blocks, pools[r],
+                                ws_full)
+
+    def reindex(i):
+        q = q2[i % sets]
+        csa.csa_reindex_topk(p, B, 1, pos, q["qI"], q["wI"], kI, w.n_cap, pools[i % sets], pool_blocks, idx, None,
+                             ws_re)
+    for i in range(args.warmup):
+        reindex(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        reindex(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the Reindex calls")
+    return {"section": "reindex", "workload": w.name, "batch": B, "pool_blocks": pool_blocks,
+            "ms_per_call": e0.elapsed_time(e1) / max(args.steps, 1)}
+
+
 def _traffic_from_profile():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary (scaled from the captured batch to the full launch), or None when
@@ -662,6 +708,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.section == "reindex":
+        if rank == 0:
+            print(json.dumps(reindex_section(args)), flush=True)
         return
     if world > 1:
         import torch
