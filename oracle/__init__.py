@@ -60,6 +60,8 @@ def _load():
         lib.orc_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, _f64p]
         lib.orc_compress_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
                                            + [_u16p] * 7 + [_f64p])
+        lib.orc_compress_single_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
+                                                  + [_u16p] * 4 + [_f64p])
         lib.orc_hadamard.argtypes = [ctypes.c_int, _f64p, _f64p]
         lib.orc_to_e4m3.restype = ctypes.c_uint8
         lib.orc_to_e4m3.argtypes = [ctypes.c_double]
@@ -147,6 +149,32 @@ def compress_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, *, rope_dim=64, theta=1e4, eps=
     _load().orc_compress_entry(m, D, rope_dim, theta, eps, int(i), _ptr(Ca, _u16p), _ptr(Za, _u16p),
                                _ptr(Cb, _u16p), _ptr(Zb, _u16p), _ptr(Ba, _u16p), _ptr(Bb, _u16p),
                                _ptr(w, _u16p), _ptr(out, _f64p))
+    return out
+
+
+def compress_single_entry(i, C, Z, B, w, *, rope_dim=64, theta=1e4, eps=1e-6) -> np.ndarray:
+    """Non-overlapped compressor ([hca_csa] "HCA：同一个算子，关掉重叠"; [CSA2
+    详解] §7.2, §7.5): entry i from the m rows C/Z of its own block, B the
+    [m, D] position bias or None (CSA2 has none); RoPE(Norm(pool)) at m*i."""
+    C, Z, w = (_c(a, np.uint16) for a in (C, Z, w))
+    B = None if B is None else _c(B, np.uint16)
+    m, D = C.shape
+    out = np.empty(D, np.float64)
+    _load().orc_compress_single_entry(m, D, rope_dim, theta, eps, int(i), _ptr(C, _u16p), _ptr(Z, _u16p),
+                                      _ptr(B, _u16p), _ptr(w, _u16p), _ptr(out, _f64p))
+    return out
+
+
+def compress_single(entry0, n_new, C, Z, B, w, *, m, rope_dim=64, theta=1e4, eps=1e-6) -> np.ndarray:
+    """Bulk non-overlapped form for one sequence: C/Z hold the chunk's m*n_new
+    token rows (row j is token m*entry0 + j); returns entries entry0.. as
+    [n_new, D] doubles."""
+    C, Z = _c(C, np.uint16), _c(Z, np.uint16)
+    D = C.shape[1]
+    out = np.empty((n_new, D), np.float64)
+    for e in range(n_new):
+        rows = slice(m * e, m * (e + 1))
+        out[e] = compress_single_entry(entry0 + e, C[rows], Z[rows], B, w, rope_dim=rope_dim, theta=theta, eps=eps)
     return out
 
 

@@ -129,6 +129,43 @@ void orc_compress_entry(int m, int D, int R, double theta, double eps,
   free(x);
 }
 
+/* ---- non-overlapped compressor ([hca_csa] "HCA：同一个算子，关掉重叠";
+ * [CSA2 详解] §7.2 and §7.5) ----------------------------------------------- */
+
+/*
+ * Entry i from the m rows of its own block only: for each channel d the m
+ * logits are Z[r][d] + B[r][d] (HCA; B == NULL: no position bias, as in
+ * CSA2), Softmax_row normalises over them and weights the C rows; then
+ * RMSNorm and RoPE at position m*i as for the overlapped compressor.  With
+ * m = 1 the one softmax weight is 1 and the entry is RoPE(Norm(C)).
+ *   C, Z : [m][D] rows of block i;  B : [m][D] or NULL;  out : [D].
+ */
+void orc_compress_single_entry(int m, int D, int R, double theta, double eps,
+                               int64_t i, const uint16_t *C, const uint16_t *Z,
+                               const uint16_t *B, const uint16_t *w,
+                               double *out) {
+  double *x = (double *)malloc(sizeof(double) * (size_t)D);
+  double *logit = (double *)malloc(sizeof(double) * (size_t)m);
+  for (int d = 0; d < D; ++d) {
+    double mx = -INFINITY;
+    for (int r = 0; r < m; ++r) {
+      logit[r] = orc_bf16(Z[r * D + d]) + (B ? orc_bf16(B[r * D + d]) : 0.0);
+      if (logit[r] > mx) mx = logit[r];
+    }
+    double num = 0.0, den = 0.0;
+    for (int r = 0; r < m; ++r) {
+      double e = exp(logit[r] - mx);
+      num += e * orc_bf16(C[r * D + d]);
+      den += e;
+    }
+    x[d] = num / den;
+  }
+  orc_rmsnorm(D, x, w, eps, out);
+  orc_rope(D, R, theta, (double)m * (double)i, out);
+  free(logit);
+  free(x);
+}
+
 /* ---- indexer keys ([hca_csa] "CSA：轻压缩 + 稀疏选择": the indexer has a
  * compressor of its own at head_dim 128, followed by a Hadamard rotation so
  * that the keys quantise well to FP8) ------------------------------------- */

@@ -548,3 +548,64 @@ def test_reindex_returns_the_whole_pool_when_k_covers_it():
     q, w = rand_e4m3((64, 128)), rand_bf16(64, 1 / 90.0)
     idx, ent, sc = oracle.reindex_topk(q, w, kI, [0, 7, -1, -1], V, 16)
     np.testing.assert_array_equal(idx, list(range(8)) + [56, 57, 58] + [-1] * 5)
+
+
+# ---- non-overlapped compressor (HCA, CSA2) ----------------------------------
+
+def test_single_stream_entry_zero_is_the_overlapped_entry_zero():
+    """[hca_csa]: HCA is the CSA compressor with one stream and no block i-1;
+    the overlapped entry 0 has no block i-1 either, so the two agree exactly."""
+    m, D = 4, 512
+    C, Z, B = rand_bf16((m, D)), rand_bf16((m, D)), rand_bf16((m, D))
+    w = bf16_bits(torch.tensor(1 + 0.1 * RNG.standard_normal(D)).to(torch.bfloat16).double().numpy())
+    junk = rand_bf16((m, D))
+    want = oracle.compress_entry(0, C, Z, junk, junk, B, junk, w)
+    np.testing.assert_array_equal(oracle.compress_single_entry(0, C, Z, B, w), want)
+
+
+def test_single_stream_flat_logits_and_no_bias_are_mean_pooling():
+    m, D = 128, 512
+    C = rand_bf16((m, D))
+    Z = np.full((m, D), bf16_bits([0.75])[0], np.uint16)
+    w = bf16_bits(np.ones(D))
+    mean = oracle.bf16_to_f64(C).mean(axis=0)
+    want = oracle.rope(oracle.rmsnorm(mean, w, 1e-6), 64, 1e4, 128 * 3)
+    np.testing.assert_allclose(oracle.compress_single_entry(3, C, Z, None, w), want, rtol=1e-12, atol=1e-12)
+
+
+def test_single_stream_ratio_one_is_norm_of_the_row():
+    """[CSA2 详解] §7.5: with one token per group the softmax weight is 1, so
+    the entry is RoPE(Norm(C)) of that token's row."""
+    D = 512
+    C, Z, B = rand_bf16((1, D)), rand_bf16((1, D)), rand_bf16((1, D))
+    w = bf16_bits(torch.tensor(1 + 0.1 * RNG.standard_normal(D)).to(torch.bfloat16).double().numpy())
+    want = oracle.rope(oracle.rmsnorm(oracle.bf16_to_f64(C[0]), w, 1e-6), 64, 1e4, 37)
+    np.testing.assert_array_equal(oracle.compress_single_entry(37, C, Z, B, w), want)
+    np.testing.assert_array_equal(oracle.compress_single_entry(37, C, Z, None, w), want)
+
+
+def test_single_stream_dominant_logit_selects_its_row_per_channel():
+    """A logit 60 above the others takes the whole softmax weight of its
+    channel: channel d picks row d % m."""
+    m, D = 128, 512
+    C = rand_bf16((m, D))
+    Z = np.zeros((m, D), np.uint16)
+    hot = bf16_bits([60.0])[0]
+    for d in range(D):
+        Z[d % m, d] = hot
+    w = bf16_bits(np.ones(D))
+    Cf = oracle.bf16_to_f64(C)
+    picked = np.array([Cf[d % m, d] for d in range(D)])
+    want = oracle.rope(oracle.rmsnorm(picked, w, 1e-6), 64, 1e4, 0)
+    np.testing.assert_allclose(oracle.compress_single_entry(0, C, Z, None, w), want, rtol=1e-12, atol=1e-12)
+
+
+def test_single_stream_rope_position_is_m_times_i():
+    """The same rows as entry i or entry 0 differ only by RoPE at m*i."""
+    m, D, i = 128, 512, 77
+    C, Z, B = rand_bf16((m, D)), rand_bf16((m, D)), rand_bf16((m, D))
+    w = bf16_bits(np.ones(D))
+    e0 = oracle.compress_single_entry(0, C, Z, B, w)
+    ei = oracle.compress_single_entry(i, C, Z, B, w)
+    np.testing.assert_allclose(oracle.rope(e0, 64, 1e4, m * i), ei, rtol=1e-9, atol=1e-12)
+    np.testing.assert_array_equal(ei[:448], e0[:448])
