@@ -65,6 +65,10 @@ _lib.csa_compress_indexer_keys.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [
 _lib.csa_index_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_static.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp]
 _lib.csa_index_topk_static.restype = ctypes.c_int
+_lib.csa_compress_single.argtypes = [_P, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp]
+_lib.csa_compress_single.restype = ctypes.c_int
+_lib.csa_compress_single_step.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp]
+_lib.csa_compress_single_step.restype = ctypes.c_int
 _lib.csa_index_topk_pool.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_pool.restype = ctypes.c_int
 _lib.csa_reindex_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]
@@ -139,6 +143,17 @@ def csa_compress_indexer_keys(params, B, n_new, entry0, CIa, ZIa, CIb, ZIb, CIb_
                                           _ptr(ZIb), _ptr(CIb_prev), _ptr(ZIb_prev), _ptr(BIa), _ptr(BIb),
                                           _ptr(rms_wI), _ptr(kI_out), kI_stride_b, _stream(stream)),
            "csa_compress_indexer_keys")
+
+
+def csa_compress_single(params, B, n_new, entry0, C, Z, bias, rms_w, kv_out, kv_stride_b, stream=None):
+    _check(_lib.csa_compress_single(ctypes.byref(params), B, n_new, entry0, _ptr(C), _ptr(Z), _ptr(bias), _ptr(rms_w),
+                                    _ptr(kv_out), kv_stride_b, _stream(stream)), "csa_compress_single")
+
+
+def csa_compress_single_step(params, B, q_pos, C, Z, bias, rms_w, state, kv_out, kv_stride_b, n_cap, stream=None):
+    _check(_lib.csa_compress_single_step(ctypes.byref(params), B, _ptr(q_pos), _ptr(C), _ptr(Z), _ptr(bias),
+                                         _ptr(rms_w), _ptr(state), _ptr(kv_out), kv_stride_b, n_cap, _stream(stream)),
+           "csa_compress_single_step")
 
 
 def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, ws, stream=None):

@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Compact the selected entries (drop -1, flag out-of-range indices).
-  {
+  // Dense (HCA): the rows are the visible entries 0 .. V(t)-1, no list.
+  if (!a.dense) {
     const int32_t* ig = a.idx + row_q * a.k;
     const int per = (a.k + kThreads - 1) / kThreads;
     const int lo = min(a.k, tid * per), hi = min(a.k, lo + per);
@@ -214,7 +215,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == kThreads - 1) flags[0] = before;
   }
   __syncthreads();
-  const int n_sel = flags[0];
+  int n_sel;
+  if (a.dense) {
+    int64_t V = t >= 0 ? (t + 1) / a.m : 0;
+    if (V > a.n_cap) {
+      if (tid == 0 && rank == 0) record_error(a.status, kErrIndexRange);
+      V = a.n_cap;
+    }
+    n_sel = static_cast<int>(V);
+  } else {
+    n_sel = flags[0];
+  }
   const int n_rows = n_swa + n_sel;
   // this CTA's slice of the row set [window rows || selected rows]
   const int per_cta = (n_rows + split - 1) / split;
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Address of row j of the query's row set (null: absent / skipped).
   auto row_at = [&](int j) -> const uint16_t* {
     if (j < n_swa) return swa_row(j);
-    if (j < n_rows) return kv_b + static_cast<int64_t>(sel_s[j - n_swa]) * kDim;
+    if (j < n_rows) return kv_b + static_cast<int64_t>(a.dense ? j - n_swa : sel_s[j - n_swa]) * kDim;
     return nullptr;
   };
   // Put every row of the slice in flight towards L2.

@@ -71,6 +71,48 @@ struct Bf16Vec<2> {
   }
 };
 
+// RMSNorm of the pooled entry x over its D channels (thread t holds channels
+// CPT*t .. CPT*t+CPT-1; `red` one float per warp of the D/CPT threads, sync()
+// a barrier over exactly them), times the weight w, then partial RoPE on the
+// last kRope channels in interleaved pairs at position pos, into y.
+template <int CPT, int D, class Sync>
+__device__ __forceinline__ void norm_rope(const CompressArgs& a, const float (&x)[CPT], const float (&w)[CPT], int t,
+                                          double pos, float* red, Sync sync, float (&y)[CPT]) {
+  constexpr int NT = D / CPT;
+  const int d0 = t * CPT;
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) ss = fmaf(x[j], x[j], ss);
+  // warp sums, then the group's warps combine
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((t & 31) == 0) red[t >> 5] = ss;
+  sync();
+  float total = 0.f;
+#pragma unroll
+  for (int wi = 0; wi < NT / 32; ++wi) total += red[wi];
+  const float inv = rsqrtf(total / static_cast<float>(D) + a.rms_eps);
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) y[j] = x[j] * inv * w[j];
+
+  // Partial RoPE on channels D-R .. D-1, interleaved pairs.
+  if (d0 >= D - kRope) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+#pragma unroll
+    for (int pr = 0; pr < CPT / 2; ++pr) {
+      const int jp = (d0 + 2 * pr - (D - kRope)) / 2;
+      double phi = pos * a.inv_freq[jp];
+      phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
+      float s, c;
+      sincosf(static_cast<float>(phi), &s, &c);
+      const float u = y[2 * pr], v = y[2 * pr + 1];
+      y[2 * pr] = u * c - v * s;
+      y[2 * pr + 1] = u * s + v * c;
+    }
+  }
+}
+
 // The values of entry (e-th of the chunk in bulk mode; the one completing at
 // q_pos[b] in ring mode) of sequence b at width D (rows of D channels, RoPE
 // on the last kRope of them): thread t's channels CPT*t .. CPT*t+CPT-1 into
@@ -83,7 +125,6 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
                                 float (&y)[CPT], int64_t* entry) {
   using V = Bf16Vec<CPT>;
   using L = typename V::T;
-  constexpr int NT = D / CPT;
   const int d0 = t * CPT;
 
   // Locate entry i and the rows of block i (a stream) and block i-1 (b stream).
@@ -184,45 +225,11 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
     }
   }
   float x[CPT];
-  float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < CPT; ++j) {
-    x[j] = num[j] / den[j];
-    ss = fmaf(x[j], x[j], ss);
-  }
-
-  // RMSNorm over the 512 channels: warp sums, then the group's warps combine.
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((t & 31) == 0) red[t >> 5] = ss;
-  sync();
-  float total = 0.f;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) total += red[w];
-  const float inv = rsqrtf(total / static_cast<float>(D) + a.rms_eps);
+  for (int j = 0; j < CPT; ++j) x[j] = num[j] / den[j];
   float w[CPT];
   V::unpack(wr, w);
-#pragma unroll
-  for (int j = 0; j < CPT; ++j) y[j] = x[j] * inv * w[j];
-
-  // Partial RoPE on channels D-R .. D-1, interleaved pairs, position M*i.
-  if (d0 >= D - kRope) {
-    const double pos = static_cast<double>(M) * static_cast<double>(i);
-    const double two_pi = 6.283185307179586476925286766559;
-    const double inv_two_pi = 0.15915494309189533576888376337251;
-#pragma unroll
-    for (int pr = 0; pr < CPT / 2; ++pr) {
-      const int jp = (d0 + 2 * pr - (D - kRope)) / 2;
-      double phi = pos * a.inv_freq[jp];
-      phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
-      float s, c;
-      sincosf(static_cast<float>(phi), &s, &c);
-      const float u = y[2 * pr], v = y[2 * pr + 1];
-      y[2 * pr] = u * c - v * s;
-      y[2 * pr + 1] = u * s + v * c;
-    }
-  }
-
+  norm_rope<CPT, D>(a, x, w, t, static_cast<double>(M) * static_cast<double>(i), red, sync, y);
   *entry = i;
   return true;
 }

@@ -1,0 +1,179 @@
+// The non-overlapped compressor of HCA and CSA2 layers.  Page "CSA / HCA"
+// (zdszero, hca_csa), section "HCA：同一个算子，关掉重叠" (one stream C, Z, B;
+// Softmax_row over the m slots of the entry's own block, then Norm and
+// RoPE); "DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §7.2 (CSA2: the same
+// pooling without the slot bias) and §7.5 (ratio 1: the softmax weight is 1);
+// RoPE at the first token of the block (§7.4).  The decode form keeps, per
+// sequence and channel, a running (max, sum, weighted sum) over the block's
+// tokens so far, the online-softmax state of the HCA compressor described in
+// "CSA / HCA", section "KV cache：成品与原料", instead of a ring of raw rows.
+//
+// Bulk: one 256-thread CTA per (entry, sequence); four groups of 64 threads
+// take every fourth row of the block (m up to 128) with an online softmax in
+// fp32, group 0 merges the four partial states and finishes the entry
+// (RMSNorm, RoPE, bf16 store).  Step: one 64-thread CTA per sequence updates
+// its state with the step's token and, when the token closes a block,
+// finishes the entry.
+#include "compress.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kGroupThreads = kDim / 8;  // 64: 8 channels per thread
+constexpr int kRowGroups = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Folds one row's logits and values into the running state of 8 channels.
+__device__ __forceinline__ void online_add(const float (&logit)[8], const float (&c)[8], float (&mx)[8],
+                                           float (&den)[8], float (&num)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float nm = fmaxf(mx[j], logit[j]);
+    const float sc = exp2f((mx[j] - nm) * kLog2e);  // 0 while the state is empty (mx = -inf)
+    const float p = exp2f((logit[j] - nm) * kLog2e);
+    num[j] = fmaf(num[j], sc, p * c[j]);
+    den[j] = fmaf(den[j], sc, p);
+    mx[j] = nm;
+  }
+}
+
+// The logits Z (+ bias) and values C of 8 channels of one row.
+__device__ __forceinline__ void load_row(const uint16_t* C, const uint16_t* Z, const uint16_t* bias, float (&logit)[8],
+                                         float (&c)[8]) {
+  using V = Bf16Vec<8>;
+  V::unpack(__ldg(reinterpret_cast<const uint4*>(Z)), logit);
+  V::unpack(__ldg(reinterpret_cast<const uint4*>(C)), c);
+  if (bias) {
+    float bv[8];
+    V::unpack(__ldg(reinterpret_cast<const uint4*>(bias)), bv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) logit[j] += bv[j];
+  }
+}
+
+__device__ __forceinline__ void group0_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kGroupThreads * kRowGroups) compress_single_kernel(const CompressArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float part[kRowGroups - 1][3][kDim];  // groups 1..3: max, sum, weighted sum
+  __shared__ float red[kGroupThreads / 32];
+  const int g = threadIdx.x / kGroupThreads, t = threadIdx.x % kGroupThreads, d0 = 8 * t;
+  const int b = blockIdx.y;
+  const int64_t e = blockIdx.x, i = a.entry0 + e;
+  const int m = a.m;
+  const int64_t row0 = (static_cast<int64_t>(b) * m * a.n_new + static_cast<int64_t>(m) * e) * kDim + d0;
+  float mx[8], den[8], num[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mx[j] = -INFINITY, den[j] = 0.f, num[j] = 0.f;
+#pragma unroll 4
+  for (int r = g; r < m; r += kRowGroups) {
+    float logit[8], c[8];
+    load_row(a.Ca + row0 + static_cast<int64_t>(r) * kDim, a.Za + row0 + static_cast<int64_t>(r) * kDim,
+             a.Ba ? a.Ba + r * kDim + d0 : nullptr, logit, c);
+    online_add(logit, c, mx, den, num);
+  }
+  if (g > 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      part[g - 1][0][d0 + j] = mx[j];
+      part[g - 1][1][d0 + j] = den[j];
+      part[g - 1][2][d0 + j] = num[j];
+    }
+  }
+  __syncthreads();
+  if (g > 0) return;
+  // group 0 has at least one row (m >= 1), so its maximum is finite
+#pragma unroll
+  for (int h = 0; h < kRowGroups - 1; ++h) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float mh = part[h][0][d0 + j];
+      const float nm = fmaxf(mx[j], mh);
+      const float s0 = exp2f((mx[j] - nm) * kLog2e), s1 = exp2f((mh - nm) * kLog2e);  // s1 = 0: no rows
+      num[j] = fmaf(num[j], s0, part[h][2][d0 + j] * s1);
+      den[j] = fmaf(den[j], s0, part[h][1][d0 + j] * s1);
+      mx[j] = nm;
+    }
+  }
+  float x[8], w[8], y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
+  Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
+  norm_rope<8, kDim>(a, x, w, t, static_cast<double>(m) * static_cast<double>(i), red, [] { group0_sync(); }, y);
+  *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
+      Bf16Vec<8>::pack(y);
+}
+
+// state: [B][3][kDim] fp32 (max, sum, weighted sum of the block's tokens so far).
+__global__ void __launch_bounds__(kGroupThreads) compress_single_step_kernel(const CompressArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float red[kGroupThreads / 32];
+  const int b = blockIdx.x, t = threadIdx.x, d0 = 8 * t;
+  const int64_t tp = a.q_pos[b];
+  if (tp < 0) return;
+  const int m = a.m;
+  const int r = static_cast<int>(tp % m);  // the token's slot in its block
+  float logit[8], c[8];
+  load_row(a.Ca + static_cast<int64_t>(b) * kDim + d0, a.Za + static_cast<int64_t>(b) * kDim + d0,
+           a.Ba ? a.Ba + r * kDim + d0 : nullptr, logit, c);
+  float* st = a.state + static_cast<int64_t>(b) * 3 * kDim + d0;
+  float mx[8], den[8], num[8];
+  if (r == 0) {  // a block starts: the state is this token alone
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx[j] = logit[j], den[j] = 1.f, num[j] = c[j];
+  } else {
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      const float4 m4 = reinterpret_cast<const float4*>(st)[v];
+      const float4 s4 = reinterpret_cast<const float4*>(st + kDim)[v];
+      const float4 n4 = reinterpret_cast<const float4*>(st + 2 * kDim)[v];
+      mx[4 * v] = m4.x, mx[4 * v + 1] = m4.y, mx[4 * v + 2] = m4.z, mx[4 * v + 3] = m4.w;
+      den[4 * v] = s4.x, den[4 * v + 1] = s4.y, den[4 * v + 2] = s4.z, den[4 * v + 3] = s4.w;
+      num[4 * v] = n4.x, num[4 * v + 1] = n4.y, num[4 * v + 2] = n4.z, num[4 * v + 3] = n4.w;
+    }
+    online_add(logit, c, mx, den, num);
+  }
+  if (r < m - 1) {  // the block goes on: keep the state
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      reinterpret_cast<float4*>(st)[v] = make_float4(mx[4 * v], mx[4 * v + 1], mx[4 * v + 2], mx[4 * v + 3]);
+      reinterpret_cast<float4*>(st + kDim)[v] =
+          make_float4(den[4 * v], den[4 * v + 1], den[4 * v + 2], den[4 * v + 3]);
+      reinterpret_cast<float4*>(st + 2 * kDim)[v] =
+          make_float4(num[4 * v], num[4 * v + 1], num[4 * v + 2], num[4 * v + 3]);
+    }
+    return;
+  }
+  const int64_t i = (tp + 1) / m - 1;  // the block is complete: entry i
+  if (i >= a.n_cap) {
+    if (t == 0) record_error(a.status, kErrIndexRange);
+    return;
+  }
+  float x[8], w[8], y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
+  Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
+  norm_rope<8, kDim>(a, x, w, t, static_cast<double>(m) * static_cast<double>(i), red, [] { __syncthreads(); }, y);
+  *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
+      Bf16Vec<8>::pack(y);
+}
+
+}  // namespace
+
+cudaError_t launch_compress_single(const CompressArgs& args, cudaStream_t stream) {
+  if (args.B <= 0) return cudaSuccess;
+  if (args.m < 1 || args.m > kMaxSingleM) return cudaErrorInvalidValue;
+  CompressArgs a = args;
+  fill_inv_freq(&a);
+  if (a.mode == 0) {
+    if (a.n_new <= 0) return cudaSuccess;
+    return launch_pdl(compress_single_kernel, dim3(static_cast<unsigned>(a.n_new), static_cast<unsigned>(a.B)),
+                      dim3(kGroupThreads * kRowGroups), 0, stream, a);
+  }
+  if (!a.state || !a.q_pos) return cudaErrorInvalidValue;
+  return launch_pdl(compress_single_step_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kGroupThreads), 0, stream, a);
+}
+
+}  // namespace csa

@@ -72,13 +72,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 
+// The overlapped compressor (and the layer calls that run it) exist for the
+// CSA block sizes 1..8.
+csa_status check_overlapped(const csa_params* p) { return p->m <= 8 ? CSA_OK : CSA_ERR_UNSUPPORTED; }
+
 // Dimensions the kernels are built for; anything else is unsupported.
 csa_status check_params(const csa_params* p) {
   if (!p) return CSA_ERR_INVALID_ARG;
   if (p->n_heads != csa::kHeads || p->head_dim != csa::kDim || p->rope_dim != csa::kRope ||
       p->idx_heads != csa::kIdxHeads || p->idx_dim != csa::kIdxDim)
     return CSA_ERR_UNSUPPORTED;
-  if (!(p->m == 1 || p->m == 2 || p->m == 4 || p->m == 8)) return CSA_ERR_UNSUPPORTED;
+  // block sizes: the overlapped CSA compressor 1..8 (checked by its calls),
+  // the single-stream HCA / CSA2 compressor up to 128
+  if (p->m < 1 || p->m > csa::kMaxSingleM || (p->m & (p->m - 1)) != 0) return CSA_ERR_UNSUPPORTED;
   if (p->topk < 1 || p->topk > csa::kMaxTopk) return CSA_ERR_UNSUPPORTED;
   if (p->swa_window < 1 || p->swa_window > csa::kMaxWindow) return CSA_ERR_UNSUPPORTED;
   if (!(p->rope_theta > 0.f) || !(p->rms_eps >= 0.f) || !isfinite(p->sm_scale)) return CSA_ERR_INVALID_ARG;
@@ -259,7 +265,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
                     const uint16_t* q, const uint16_t* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
                     int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
-                    const float* sink, uint16_t* out, float* lse, cudaStream_t st) {
+                    const float* sink, uint16_t* out, float* lse, cudaStream_t st, bool dense = false) {
   unsigned* status = status_ptr();
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!status || !enc) return CSA_ERR_CUDA;
@@ -271,6 +277,8 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.n_cap = n_cap;
   aa.idx = idx;
   aa.k = p->topk;
+  aa.dense = dense ? 1 : 0;
+  aa.m = p->m;
   aa.swa = swa;
   aa.swa_mode = swa_mode;
   aa.swa_len = swa_len;
@@ -406,6 +414,7 @@ csa_status csa_compress(const csa_params* p, int32_t B, int32_t n_new, int64_t e
                         uint16_t* kv_out, int64_t kv_stride_b, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
   if (B == 0 || n_new == 0) return CSA_OK;
   if (!ok_ptr(Ca) || !ok_ptr(Za) || !ok_ptr(Cb) || !ok_ptr(Zb) || !ok_ptr(Ba) || !ok_ptr(Bb) ||
@@ -427,6 +436,7 @@ csa_status csa_compress_indexer_keys(const csa_params* p, int32_t B, int32_t n_n
                                      uint8_t* kI_out, int64_t kI_stride_b, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
   if (B == 0 || n_new == 0) return CSA_OK;
   if (!ok_ptr(CIa) || !ok_ptr(ZIa) || !ok_ptr(CIb) || !ok_ptr(ZIb) || !ok_ptr(BIa) || !ok_ptr(BIb) ||
@@ -443,6 +453,43 @@ csa_status csa_compress_indexer_keys(const csa_params* p, int32_t B, int32_t n_n
                                        rms_wI, nullptr, kI_stride_b, entry0 + n_new, nullptr, status);
   ca.key_out = kI_out;
   return cuda_status(csa::launch_index_keys(ca, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_single(const csa_params* p, int32_t B, int32_t n_new, int64_t entry0, const uint16_t* C,
+                               const uint16_t* Z, const uint16_t* bias, const uint16_t* rms_w, uint16_t* kv_out,
+                               int64_t kv_stride_b, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return CSA_OK;
+  if (!ok_ptr(C) || !ok_ptr(Z) || !ok_opt(bias) || !ok_ptr(rms_w) || !ok_ptr(kv_out)) return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b < (entry0 + n_new) * csa::kDim && B > 1) return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b % 8 != 0) return CSA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  csa::CompressArgs ca = compress_args(p, 0, B, n_new, entry0, C, Z, nullptr, nullptr, nullptr, nullptr, bias, nullptr,
+                                       rms_w, kv_out, kv_stride_b, entry0 + n_new, nullptr, status);
+  return cuda_status(csa::launch_compress_single(ca, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_single_step(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* C,
+                                    const uint16_t* Z, const uint16_t* bias, const uint16_t* rms_w, float* state,
+                                    uint16_t* kv_out, int64_t kv_stride_b, int64_t n_cap, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(C) || !ok_ptr(Z) || !ok_opt(bias) || !ok_ptr(rms_w) || !ok_ptr(state) ||
+      !ok_ptr(kv_out))
+    return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b < n_cap * csa::kDim && B > 1) return CSA_ERR_INVALID_ARG;
+  if (kv_stride_b % 8 != 0) return CSA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  csa::CompressArgs ca = compress_args(p, 1, B, 0, 0, C, Z, nullptr, nullptr, nullptr, nullptr, bias, nullptr, rms_w,
+                                       kv_out, kv_stride_b, n_cap, q_pos, status);
+  ca.state = state;
+  return cuda_status(csa::launch_compress_single(ca, static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
@@ -524,7 +571,7 @@ csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int3
   if (s != CSA_OK) return s;
   if (B < 0 || Q < 0 || B > 65535 || Q > 2147483647 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
   if (B == 0 || Q == 0) return CSA_OK;
-  if (!ok_ptr(q_pos) || !ok_ptr(q) || !ok_ptr(kv_comp) || !ok_ptr(idx) || !ok_ptr(swa) || !ok_ptr(sink) ||
+  if (!ok_ptr(q_pos) || !ok_ptr(q) || !ok_ptr(kv_comp) || !ok_opt(idx) || !ok_ptr(swa) || !ok_ptr(sink) ||
       !ok_ptr(out) || !ok_opt(lse))
     return CSA_ERR_INVALID_ARG;
   if (swa_mode == 0) {
@@ -535,7 +582,7 @@ csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int3
     return CSA_ERR_INVALID_ARG;
   }
   return run_attn(p, B, Q, q_pos, 0, q, kv_comp, n_cap, idx, swa, swa_mode, swa_len, swa_pos0, 0, sink, out, lse,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), idx == nullptr);
 }
 
 csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
@@ -546,6 +593,7 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
                             uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
   if (B == 0) return CSA_OK;
   if (!ok_ptr(q_pos) || !ok_ptr(ring_Ca) || !ok_ptr(ring_Za) || !ok_ptr(ring_Cb) || !ok_ptr(ring_Zb) ||
@@ -593,6 +641,7 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
                              size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || pos0 < 0 || pos0 % p->m != 0 || !n_cap_ok(n_cap))
     return CSA_ERR_INVALID_ARG;
   if (B == 0 || Q == 0) return CSA_OK;

@@ -79,8 +79,15 @@ struct CompressArgs {
   unsigned* status;
   double inv_freq[kRope / 2];  // theta^(-2j/R), filled by launch_compress
   uint8_t* key_out;            // indexer keys (launch_index_keys): E4M3 rows of kIdxDim
+  float* state;                // single-stream step: [B][3][kDim] running (max, sum, weighted sum)
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
+// The non-overlapped (single-stream) compressor, block size a.m (1..128):
+// mode 0 bulk over Ca / Za (the stream's C / Z rows) with the optional slot
+// bias Ba; mode 1 one decode token per sequence, Ca / Za [B][kDim], folded
+// into a.state and finished into kv_out when it closes a block.
+constexpr int kMaxSingleM = 128;
+cudaError_t launch_compress_single(const CompressArgs& a, cudaStream_t stream);
 // Indexer keys from 128-wide compressor rows (bulk mode): the compressor's
 // steps at width kIdxDim, the Hadamard rotation, E4M3 codes into key_out.
 cudaError_t launch_index_keys(const CompressArgs& a, cudaStream_t stream);
@@ -162,8 +169,10 @@ struct AttnArgs {
   const uint16_t* q;        // [B][Q][64][512]
   const uint16_t* kv;       // [B][n_cap][512]
   int64_t n_cap;
-  const int32_t* idx;       // [B][Q][k]
+  const int32_t* idx;       // [B][Q][k] (sparse)
   int k;
+  int dense;                // 1: the rows are every visible entry 0 .. V(t)-1 (idx unused)
+  int m;                    // dense: V(t) = floor((t+1)/m), at most n_cap
   const uint16_t* swa;
   int swa_mode;             // 0 ring [B][W][512]; 1 linear [B][swa_len][512]
   int64_t swa_len;

@@ -57,7 +57,10 @@ typedef enum {
 
 /* Hyper-parameters of one CSA layer. */
 typedef struct {
-  int32_t m;          /* compression ratio: one entry per m tokens (4)        */
+  int32_t m;          /* compression ratio: one entry per m tokens (4); a
+                         power of two, 1..8 for the overlapped CSA compressor
+                         and the layer calls, up to 128 for the single-stream
+                         compressor and dense attention (HCA: 128)          */
   int32_t n_heads;    /* query heads (64)                                    */
   int32_t head_dim;   /* shared K=V latent width (512)                        */
   int32_t rope_dim;   /* trailing channels that carry RoPE (64)               */
@@ -153,6 +156,57 @@ csa_status csa_compress_indexer_keys(
     const uint16_t *ZIb, const uint16_t *CIb_prev, const uint16_t *ZIb_prev,
     const uint16_t *BIa, const uint16_t *BIb, const uint16_t *rms_wI,
     uint8_t *kI_out, int64_t kI_stride_b, void *stream);
+
+/*
+ * csa_compress_single — the non-overlapped compressor of HCA and CSA2 layers,
+ * bulk form.  [hca_csa] "HCA：同一个算子，关掉重叠" (one stream C, Z and
+ * slot bias B, Softmax_row over the m slots of the entry's own block);
+ * [CSA2 详解] §7.2 (CSA2: the same pooling without the slot bias) and §7.5
+ * (m = 1: the softmax weight is 1, the entry is RoPE(Norm(C))).  m = p->m,
+ * a power of two up to 128 (HCA uses 128).
+ *
+ * For every sequence b and entry i in [entry0, entry0 + n_new), per channel
+ * d: softmax over the m logits Z[b, m*(i-entry0) + r, d] + bias[r, d]
+ * (bias NULL: no bias) weighting the rows C[b, m*(i-entry0) + r, :]; then
+ * RMSNorm (p->rms_eps) times rms_w and RoPE on the last 64 channels in
+ * interleaved pairs at position m*i, as csa_compress does.
+ *
+ * C, Z   : [B][m*n_new][512] bf16, row j of sequence b is token m*entry0 + j.
+ * bias   : [m][512] bf16 or NULL.          rms_w : [512] bf16.
+ * kv_out : entry e of sequence b at kv_out + b*kv_stride_b + e*512 (bf16).
+ * m above 128 or not a power of two: CSA_ERR_UNSUPPORTED.
+ */
+csa_status csa_compress_single(const csa_params *p, int32_t B, int32_t n_new,
+                               int64_t entry0, const uint16_t *C,
+                               const uint16_t *Z, const uint16_t *bias,
+                               const uint16_t *rms_w, uint16_t *kv_out,
+                               int64_t kv_stride_b, void *stream);
+
+/*
+ * csa_compress_single_step — the same compressor at decode, one token per
+ * sequence per call, with an online softmax: per channel the block's tokens
+ * so far are held as a running (max logit, sum of e^(logit - max), sum of
+ * e^(logit - max) * C) instead of their rows ([hca_csa] "KV cache：成品与
+ * 原料": the HCA compressor's state shrinks to one (max, sum, kv) slot).
+ *
+ * For each b with t = q_pos[b] >= 0 and slot r = t mod m: the token's logit
+ * Z[b,:] + bias[r,:] and row C[b,:] start the state (r == 0) or are folded
+ * into it; when r == m-1 the block is complete and entry i = (t+1)/m - 1 is
+ * written to kv_out + b*kv_stride_b + i*512 (RMSNorm, RoPE at m*i); an i at
+ * or past n_cap records CSA_ERR_INDEX_RANGE.  The result equals
+ * csa_compress_single over the same block up to fp32 rounding.
+ *
+ * C, Z  : [B][512] bf16, this step's token.      bias : [m][512] or NULL.
+ * state : [B][3][512] fp32, owned by the caller, read and written by every
+ *         call; a sequence must be stepped through its positions in order
+ *         (its state is valid only after the first token of a block).
+ */
+csa_status csa_compress_single_step(const csa_params *p, int32_t B,
+                                    const int32_t *q_pos, const uint16_t *C,
+                                    const uint16_t *Z, const uint16_t *bias,
+                                    const uint16_t *rms_w, float *state,
+                                    uint16_t *kv_out, int64_t kv_stride_b,
+                                    int64_t n_cap, void *stream);
 
 /*
  * csa_index_topk — lightning indexer + top-k over the causally visible entries.
@@ -284,6 +338,11 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  * q      : [B][Q][64][512] bf16.        kv_comp : [B][n_cap][512] bf16.
  * idx    : [B][Q][topk] int32, -1 marks an empty slot; any other value outside
  *          [0, n_cap) records CSA_ERR_INDEX_RANGE and the slot is skipped.
+ *          NULL: dense attention, the HCA read path ([hca_csa] "HCA：同一个
+ *          算子，关掉重叠"; [CSA2 详解] §9: a layer without an indexer reads
+ *          every causally visible compressed entry): the compressed rows are
+ *          kv_comp[b, 0 .. V(t)-1] with V(t) = floor((t+1)/p->m) (a V(t) past
+ *          n_cap records CSA_ERR_INDEX_RANGE and is clamped).
  * swa    : swa_mode 0 (decode ring): [B][W][512], position u in slot u mod W.
  *          swa_mode 1 (linear):      [B][swa_len][512], row j holds position
  *          swa_pos0[b] + j (swa_pos0 is a [B] int32 device array); a needed

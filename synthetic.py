@@ -30,7 +30,8 @@ import torch
 _IDS = {name: i for i, name in enumerate([
     "Ca", "Za", "Cb", "Zb", "Ba", "Bb", "rms_w", "q", "qI", "wI", "kI", "sink", "kv", "swa",
     "Cb_prev", "Zb_prev", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb",
-    "CIa", "ZIa", "CIb", "ZIb", "CIb_prev", "ZIb_prev", "BIa", "BIb", "rms_wI"])}
+    "CIa", "ZIa", "CIb", "ZIb", "CIb_prev", "ZIb_prev", "BIa", "BIb", "rms_wI",
+    "C", "Z", "B"])}
 
 D, H, HI, DI, R = 512, 64, 64, 128, 64
 
@@ -149,6 +150,16 @@ def main_query(config: int, B: int, Q: int, device="cpu") -> torch.Tensor:
 def cache_rows(config: int, B: int, n: int, device="cpu", name="kv") -> torch.Tensor:
     """Existing compressed cache / raw window rows: unit-RMS N(0,1) rows, bf16."""
     return _per_seq(B, config, name, (n, D), device, lambda x: bf16(unit_rms_rows(x)))
+
+
+def single_stream_inputs(config: int, B: int, T: int, m: int, bias: bool = True, device="cpu") -> dict:
+    """The single-stream (HCA / CSA2) compressor's inputs: rows C, Z [B, T,
+    512] N(0,1) bf16; slot bias B [m, 512] N(0,1) bf16 (None without bias);
+    RMSNorm weight 1 + 0.1*N(0,1)."""
+    s = 1000 * config
+    return {"C": _per_seq(B, config, "C", (T, D), device, bf16), "Z": _per_seq(B, config, "Z", (T, D), device, bf16),
+            "B": bf16(normal((m, D), s, "B", device)) if bias else None,
+            "rms_w": bf16(1.0 + 0.1 * normal((D,), s, "rms_w", device))}
 
 
 def decode_inputs(w: Workload, device="cpu", B: int | None = None) -> dict:

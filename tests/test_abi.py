@@ -124,3 +124,27 @@ def test_pool_calls_validate_and_size_their_workspace(lib):
     assert pool > full + 64 * (32768 // 8) * 4
     # the Reindex layer's scratch holds 16384 slot scores per query
     assert lib.csa_workspace_size(lib.CSA_OP_REINDEX_TOPK, p, 64, 1, 32768) >= 64 * 16384 * 4
+
+
+def test_block_sizes_and_single_stream_calls_validate(lib):
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    for n in ("csa_compress", "csa_compress_single", "csa_compress_single_step", "csa_layer_decode"):
+        getattr(raw, n).restype = ctypes.c_int
+    fake = ctypes.c_void_p(0x10000)
+    i64 = ctypes.c_int64
+    # m: a power of two up to 128
+    for m in (3, 256, 0):
+        p = lib.csa_default_params(m=m)
+        assert raw.csa_compress_single(ctypes.byref(p), 1, 1, i64(0), fake, fake, None, fake, fake, i64(512),
+                                       None) == 2
+    p128 = lib.csa_default_params(m=128)
+    # the overlapped compressor and the layer calls stop at 8
+    assert raw.csa_compress(ctypes.byref(p128), 1, 4, i64(0), fake, fake, fake, fake, None, None, fake, fake, fake,
+                            fake, i64(4096), None) == 2
+    # single stream: bias optional, state required for the step form
+    assert raw.csa_compress_single(ctypes.byref(p128), 1, 1, i64(0), fake, None, None, fake, fake, i64(512),
+                                   None) == 1
+    assert raw.csa_compress_single_step(ctypes.byref(p128), 1, fake, fake, fake, None, fake, None, fake, i64(512),
+                                        i64(1), None) == 1
+    assert raw.csa_compress_single(ctypes.byref(p128), 0, 1, i64(0), None, None, None, None, None, i64(0),
+                                   None) == 0
