@@ -229,6 +229,7 @@ def run_ours(args, rank, world, local_rank):
         result["attn"].update(attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream))
         result["prefill"] = prefill_profile(csa, torch, dev)
         result["hierarchical"] = [hierarchical_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
+        result["hca"] = hca_profile(csa, torch, dev)
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -454,6 +455,74 @@ def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
                    "launches (which break their programmatic overlap); reindex_kernel_* = the indexer "
                    "kernel alone")
     del kI, qs, q2, pools, ws_full, ws_plain, ws_re
+    torch.cuda.empty_cache()
+    return res
+
+
+def hca_profile(csa, torch, dev, m=128):
+    """The HCA layer's path (block size 128, no indexer): dense decode
+    attention over the window and every visible compressed entry at 128K
+    (64 sequences, 1024 entries) and 1M (8 sequences, 8192 entries) context,
+    and the single-stream compressor over a prefill chunk.  Query sets rotate
+    (4), caches are larger than L2 at 1M."""
+    import synthetic as syn
+    hbm, bf16, _ = peaks()
+    p = csa.csa_default_params(m=m)
+    res = {"block": m, "attention": []}
+    for name, B, t in (("hca-decode-b64-128k", 64, 131071), ("hca-decode-b8-1m", 8, 1048575)):
+        n_cap = (t + 1) // m
+        kv = syn.cache_rows(100, B, n_cap, device=dev)
+        swa = syn.cache_rows(100, B, 128, device=dev, name="swa")
+        sink = syn.normal((64,), 100000, "sink", dev).float()
+        qs = [syn.main_query(100 + 1000 * r, B, 1, device=dev) for r in range(4)]
+        pos = torch.full((B, 1), t, dtype=torch.int32, device=dev)
+        out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=dev)
+
+        def attn(i):
+            csa.csa_sparse_attn(p, B, 1, pos, qs[i % 4], kv, n_cap, None, swa, 0, 128, None, sink, out, None)
+        for i in range(8):
+            attn(i)
+        torch.cuda.synchronize()
+        n = 100
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            attn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        if csa.csa_check_status() != 0:
+            raise RuntimeError("device status after the HCA attention")
+        ms = e0.elapsed_time(e1) / n
+        rows = 128 + n_cap
+        flops = B * 4.0 * 64 * 512 * rows
+        byts = B * (rows * 1024 + 2 * 64 * 1024)
+        res["attention"].append({"workload": name, "batch": B, "entries": n_cap, "rows_per_query": rows, "ms": ms,
+                                 "queries_per_s": B / (ms * 1e-3), "gbs": byts / (ms * 1e-3) / 1e9,
+                                 "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm,
+                                 "tflops": flops / (ms * 1e-3) / 1e12,
+                                 "binding_roofline_frac": max(byts / (hbm * 1e9), flops / (bf16 * 1e12)) / (ms * 1e-3)})
+        del kv, swa, qs, out
+    # the compressor over a 16384-token chunk of 8 sequences: 128 entries each
+    B, T = 8, 16384
+    x = syn.single_stream_inputs(101, B, T, m, True, device=dev)
+    kvc = torch.empty(B, T // m, 512, dtype=torch.bfloat16, device=dev)
+
+    def comp():
+        csa.csa_compress_single(p, B, T // m, 0, x["C"], x["Z"], x["B"], x["rms_w"], kvc, (T // m) * 512)
+    for _ in range(3):
+        comp()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        comp()
+    e1.record()
+    torch.cuda.synchronize()
+    cms = e0.elapsed_time(e1) / 20
+    cbytes = B * T * 2 * 1024 + B * (T // m) * 1024
+    res["compressor"] = {"workload": "hca-compress-b8-16k-tokens", "entries": B * T // m, "ms": cms,
+                         "gbs": cbytes / (cms * 1e-3) / 1e9, "hbm_frac": cbytes / (cms * 1e-3) / 1e9 / hbm}
+    del x, kvc
     torch.cuda.empty_cache()
     return res
 
