@@ -478,8 +478,10 @@ def hca_profile(csa, torch, dev, m=128):
         pos = torch.full((B, 1), t, dtype=torch.int32, device=dev)
         out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=dev)
 
+        wsa = csa.workspace(csa.CSA_OP_SPARSE_ATTN, p, B, 1, n_cap, device=dev)  # split-KV partials (B <= 16)
+
         def attn(i):
-            csa.csa_sparse_attn(p, B, 1, pos, qs[i % 4], kv, n_cap, None, swa, 0, 128, None, sink, out, None)
+            csa.csa_sparse_attn(p, B, 1, pos, qs[i % 4], kv, n_cap, None, swa, 0, 128, None, sink, out, None, wsa)
         for i in range(8):
             attn(i)
         torch.cuda.synchronize()
@@ -501,7 +503,7 @@ def hca_profile(csa, torch, dev, m=128):
                                  "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm,
                                  "tflops": flops / (ms * 1e-3) / 1e12,
                                  "binding_roofline_frac": max(byts / (hbm * 1e9), flops / (bf16 * 1e12)) / (ms * 1e-3)})
-        del kv, swa, qs, out
+        del kv, swa, qs, out, wsa
     # the compressor over a 16384-token chunk of 8 sequences: 128 entries each
     B, T = 8, 16384
     x = syn.single_stream_inputs(101, B, T, m, True, device=dev)

@@ -114,7 +114,8 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a, const int split) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a, const int split,
+                       const int gsplit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = base;                                          // [8 blocks][64 heads][128 B]
@@ -148,8 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // before any global access and before TMEM is taken
   const int quad = warp & 3;         // TMEM lane quadrant == 32 tile rows
   const int hw0 = (warp >> 2) * HW;  // first head of this warp
-  const int qi = blockIdx.x / split;
-  const int rank = blockIdx.x % split;  // == the CTA's rank in its cluster
+  // the query's row set is cut into `split` slices combined in the cluster,
+  // or `gsplit` slices combined by attn_combine_kernel (one of them is 1)
+  const int slices = split > 1 ? split : gsplit;
+  const int qi = blockIdx.x / slices;
+  const int rank = blockIdx.x % slices;  // == the CTA's rank in its cluster when split > 1
   const int b = blockIdx.y;
   const int64_t row_q = static_cast<int64_t>(b) * a.Q + qi;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + qi;
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n_rows = n_swa + n_sel;
   // this CTA's slice of the row set [window rows || selected rows]
-  const int per_cta = (n_rows + split - 1) / split;
+  const int per_cta = (n_rows + slices - 1) / slices;
   const int r_lo = min(n_rows, rank * per_cta);
   const int r_hi = min(n_rows, r_lo + per_cta);
   const int n_tiles = (r_hi - r_lo + kTileRows - 1) / kTileRows;
@@ -433,7 +437,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (a.lse && rank == 0) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
   };
-  if (split == 1) {
+  if (gsplit > 1) {
+    // this slice's raw O^T and (reference max, sum) per head, fp32, for the
+    // combine kernel: for a head, a warp's lanes hold 32 consecutive channels
+    float* po = a.part_o + (row_q * gsplit + rank) * kHeads * kDim;
+    float* pml = a.part_ml + (row_q * gsplit + rank) * 2 * kHeads;
+    if (tid < kHeads) {
+      pml[tid] = m_ref[tid];
+      pml[kHeads + tid] = l_sum[tid];
+    }
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      const int chn = blk * 128 + quad * 32 + lane;
+      uint32_t v[32];
+      if (live) {
+        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) v[h] = 0u;
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) po[(hw0 + h) * kDim + chn] = __uint_as_float(v[h]);
+    }
+  } else if (split == 1) {
     if (tid < kHeads) factors(tid, m_ref, l_sum, 0, 1, alpha);
     __syncthreads();
     // O^T from TMEM straight to global: for a head, a warp's lanes hold 32
@@ -557,6 +584,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The slices of a query split with gsplit > 1 merged: per head, the joint
+// maximum M over the slices' reference maxima and the sink (log2 units), the
+// denominator 2^(sink - M) + sum_s l_s 2^(m_s - M), and the output
+// sum_s O_s 2^(m_s - M) / den (the merge the cluster does on chip).  One CTA
+// per (query, head): one warp reduces the slices' (max, sum), then thread c
+// loads channels 4c .. 4c+3 of every slice at once (independent loads) and
+// sums them; the inverse RoPE rotates its two channel pairs in place.
+__global__ void __launch_bounds__(kDim / 4) attn_combine_kernel(const AttnArgs a, const int gsplit) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float fs[kMaxGSplit];
+  const int64_t row_q = blockIdx.x;
+  const int h = blockIdx.y, tid = threadIdx.x;
+  if (tid < 32) {
+    const float* ml = a.part_ml + row_q * gsplit * 2 * kHeads;
+    const float sk = a.sink[h] * kLog2e;
+    const float ms = tid < gsplit ? ml[tid * 2 * kHeads + h] : -INFINITY;
+    const float ls = tid < gsplit ? ml[tid * 2 * kHeads + kHeads + h] : 0.f;
+    float M = fmaxf(sk, ms);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float den = (M == -INFINITY || ms == -INFINITY) ? 0.f : ls * exp2f(ms - M);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    den += M == -INFINITY ? 0.f : exp2f(sk - M);
+    if (tid < gsplit) fs[tid] = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M) / den;
+    if (tid == 0 && a.lse) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
+  }
+  __syncthreads();
+  const int c0 = 4 * tid;
+  float4 o[kMaxGSplit];
+#pragma unroll
+  for (int s = 0; s < kMaxGSplit; ++s)
+    if (s < gsplit) o[s] = *reinterpret_cast<const float4*>(a.part_o + ((row_q * gsplit + s) * kHeads + h) * kDim + c0);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kMaxGSplit; ++s) {
+    if (s < gsplit) {
+      const float f = fs[s];
+      acc[0] = fmaf(f, o[s].x, acc[0]);
+      acc[1] = fmaf(f, o[s].y, acc[1]);
+      acc[2] = fmaf(f, o[s].z, acc[2]);
+      acc[3] = fmaf(f, o[s].w, acc[3]);
+    }
+  }
+  if (a.inverse_rope && c0 >= kDim - kRope) {  // pairs (c0, c0+1), (c0+2, c0+3): (u, v) -> (u cos + v sin, -u sin + v cos)
+    const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + row_q % a.Q;
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      float rs, rc;
+      rope_angle(c0 + 2 * pr, t, a, &rs, &rc);
+      const float u = acc[2 * pr], v = acc[2 * pr + 1];
+      acc[2 * pr] = fmaf(u, rc, v * rs);
+      acc[2 * pr + 1] = fmaf(v, rc, -u * rs);
+    }
+  }
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
+  *reinterpret_cast<uint2*>(a.out + (row_q * kHeads + h) * kDim + c0) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
 // The largest cluster size (a power of two up to kMaxSplit) that the device
 // can schedule for this kernel at all, found once per device.
 int max_split(int dev) {
@@ -615,9 +703,30 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int split = choose_split(static_cast<int64_t>(a.B) * a.Q, sms, max_split(dev));
+  const int64_t queries = static_cast<int64_t>(a.B) * a.Q;
+  const int cluster_max = max_split(dev);
+  // Few queries with long row sets: more slices than a cluster holds, merged
+  // by a second kernel through the caller's workspace (at most one slice per
+  // 128-row tile of the longest row set).
+  int gsplit = 1;
+  if (a.part_o && a.part_ml && queries <= kGSplitMaxQueries) {
+    const int64_t rows_max = a.W + (a.dense ? a.n_cap : a.k);
+    int64_t g = sms / queries;
+    g = g < kMaxGSplit ? g : kMaxGSplit;
+    const int64_t tiles = (rows_max + kTileRows - 1) / kTileRows;
+    g = g < tiles ? g : tiles;
+    if (g > cluster_max) gsplit = static_cast<int>(g);
+  }
+  if (gsplit > 1) {
+    e = launch_pdl(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,
+                   stream, tm_q, a, 1, gsplit);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(queries), kHeads), dim3(kDim / 4), 0, stream, a,
+                      gsplit);
+  }
+  const int split = choose_split(queries, sms, cluster_max);
   return launch_pdl_cluster(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
-                            kSmemBytes, stream, static_cast<unsigned>(split), tm_q, a, split);
+                            kSmemBytes, stream, static_cast<unsigned>(split), tm_q, a, split, 1);
 }
 
 }  // namespace csa

@@ -265,7 +265,8 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
                     const uint16_t* q, const uint16_t* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
                     int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
-                    const float* sink, uint16_t* out, float* lse, cudaStream_t st, bool dense = false) {
+                    const float* sink, uint16_t* out, float* lse, cudaStream_t st, bool dense = false,
+                    void* split_ws = nullptr, size_t split_ws_bytes = 0) {
   unsigned* status = status_ptr();
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!status || !enc) return CSA_ERR_CUDA;
@@ -279,6 +280,13 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.k = p->topk;
   aa.dense = dense ? 1 : 0;
   aa.m = p->m;
+  // the split-KV path for few queries, when the workspace holds its partials
+  const int64_t queries = static_cast<int64_t>(B) * Q;
+  const size_t need = csa::attn_split_bytes(queries);
+  if (need > 0 && split_ws && split_ws_bytes >= need && aligned16(split_ws)) {
+    aa.part_o = static_cast<float*>(split_ws);
+    aa.part_ml = aa.part_o + queries * csa::kMaxGSplit * csa::kHeads * csa::kDim;
+  }
   aa.swa = swa;
   aa.swa_mode = swa_mode;
   aa.swa_len = swa_len;
@@ -386,13 +394,21 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
   IndexWs w;
   switch (op) {
     case CSA_OP_COMPRESS:
-    case CSA_OP_SPARSE_ATTN:
       return 16;  // no scratch needed; a non-zero size keeps callers uniform
+    case CSA_OP_SPARSE_ATTN: {  // the split-KV partials for few queries
+      const size_t a = csa::attn_split_bytes(static_cast<int64_t>(B) * Q);
+      return a > 16 ? a : 16;
+    }
     case CSA_OP_INDEX_TOPK:
-    case CSA_OP_LAYER_PREFILL:
       return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w) ? w.total : 0;
+    case CSA_OP_LAYER_PREFILL:  // the indexer's scratch, then the attention's
+      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)
+                 ? round_up(w.total, 256) + csa::attn_split_bytes(static_cast<int64_t>(B) * Q)
+                 : 0;
     case CSA_OP_LAYER_DECODE:
-      return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w) ? w.total : 0;
+      return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w)
+                 ? round_up(w.total, 256) + csa::attn_split_bytes(B)
+                 : 0;
     case CSA_OP_INDEX_TOPK_POOL: {
       IndexWs wb;
       size_t total = 0;
@@ -582,7 +598,7 @@ csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int3
     return CSA_ERR_INVALID_ARG;
   }
   return run_attn(p, B, Q, q_pos, 0, q, kv_comp, n_cap, idx, swa, swa_mode, swa_len, swa_pos0, 0, sink, out, lse,
-                  static_cast<cudaStream_t>(stream), idx == nullptr);
+                  static_cast<cudaStream_t>(stream), idx == nullptr, workspace, workspace_bytes);
 }
 
 csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
@@ -626,8 +642,10 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   if (s != CSA_OK) return s;
   trace(3, st);
   // 3. sparse attention over the window ring and the selection
+  const size_t attn_off = round_up(w.total, 256);
   s = run_attn(p, B, 1, q_pos, 0, q, kv_comp, n_cap, idx_out, swa_ring, 0, p->swa_window, nullptr, 0, sink, out,
-               lse, st);
+               lse, st, false, static_cast<uint8_t*>(workspace) + attn_off,
+               workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
   trace(4, st);
   return s;
 }
@@ -689,8 +707,10 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   if (s != CSA_OK) return s;
   trace(3, st);
   // 3. sparse attention with the linear window (row j = position pos0-(W-1)+j)
+  const size_t attn_off = round_up(w.total, 256);
   s = run_attn(p, B, Q, nullptr, pos0, q, kv_comp, n_cap, idx_out, swa, 1, static_cast<int64_t>(p->swa_window) - 1 + Q,
-               nullptr, pos0 - (p->swa_window - 1), sink, out, lse, st);
+               nullptr, pos0 - (p->swa_window - 1), sink, out, lse, st, false,
+               static_cast<uint8_t*>(workspace) + attn_off, workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
   trace(4, st);
   return s;
 }

@@ -184,10 +184,22 @@ struct AttnArgs {
   float* lse;               // [B][Q][64] or null
   int B, Q;
   float sm_scale;
+  // Workspace of the split-KV path (few queries): per query kMaxGSplit
+  // slices of raw O [64][512] fp32 and (max, sum) [2][64] fp32; null: no
+  // such path.
+  float* part_o;
+  float* part_ml;
   int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
   double inv_freq[kRope / 2];  // theta^(-2j/R), host fp64
   unsigned* status;
 };
+constexpr int kMaxGSplit = 16;          // split-KV slices per query at most
+constexpr int kGSplitMaxQueries = 16;   // the split-KV path serves launches of up to this many queries
+// Bytes of the split-KV workspace for `queries` queries (0 past the limit).
+inline size_t attn_split_bytes(int64_t queries) {
+  return queries > kGSplitMaxQueries ? 0
+                                     : static_cast<size_t>(queries) * kMaxGSplit * (kHeads * kDim + 2 * kHeads) * 4;
+}
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream);
 
 }  // namespace csa

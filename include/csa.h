@@ -350,6 +350,13 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  *          skipped.
  * sink   : [64] fp32.   out : [B][Q][64][512] bf16.   lse : [B][Q][64] or NULL.
  *
+ * workspace: optional.  With csa_workspace_size(CSA_OP_SPARSE_ATTN, p, B, Q,
+ *          n_cap) bytes (more than a token amount only for B*Q <= 16), a
+ *          call with few queries cuts each query's rows into up to 16 slices
+ *          on as many CTAs and merges them in a second kernel (the same
+ *          result up to fp32 summation order); NULL or fewer bytes: one
+ *          launch, at most a thread-block cluster's slices per query.
+ *
  * With p->inverse_rope = 1 each head's output then gets the inverse of the
  * RoPE the rows carry, at the query position ([CSA2 详解] §12.1 "Partial RoPE
  * 与 inverse RoPE"; [KV 压缩] §9.6 kernel note): channels (448+2j, 449+2j)

@@ -86,13 +86,15 @@ def dense_inputs(cfg, B, n_cap, W=128):
             "sink": syn.normal((64,), 1000 * cfg, "sink", "cpu").float()}
 
 
-def run_dense(csa, p, x, pos, n_cap):
+def run_dense(csa, p, x, pos, n_cap, split_ws=True):
+    """split_ws: pass the workspace, so few queries take the split-KV path."""
     B = x["q"].shape[0]
     out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(B, 1, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_SPARSE_ATTN, p, B, 1, n_cap) if split_ws else None
     csa.csa_sparse_attn(p, B, 1, torch.tensor(pos, dtype=torch.int32, device=DEV).view(B, 1), x["q"].to(DEV),
                         x["kv"].to(DEV), n_cap, None, x["swa"].to(DEV), 0, p.swa_window, None, x["sink"].to(DEV),
-                        out, lse)
+                        out, lse, ws)
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
@@ -103,9 +105,10 @@ def oracle_dense(p, x, b, t, m, n_cap):
                                lambda u: ring[u % 128], bits(x["sink"]), W=128, sm_scale=p.sm_scale)
 
 
+@pytest.mark.parametrize("split_ws", [True, False])
 @pytest.mark.parametrize("m,ts", [(128, [131071, 128 * 700 + 5]), (128, [100, 127]), (2, [999, 1500]),
                                   (16, [16 * 333 - 1, 40])])
-def test_dense_attention_over_every_visible_entry(csa, m, ts):
+def test_dense_attention_over_every_visible_entry(csa, m, ts, split_ws):
     """HCA's read path: window rows + all floor((t+1)/m) entries + sink;
     at m = 128, V = 1024 and 700, then V = 0 (t = 100: the window alone) and
     V = 1 (t = 127); the CSA2 block size 2 and 16."""
@@ -113,11 +116,11 @@ def test_dense_attention_over_every_visible_entry(csa, m, ts):
     n_cap = max((t + 1) // m for t in ts) + 3
     x = dense_inputs(80 + m, B, n_cap)
     p = params(csa, m)
-    out, lse = run_dense(csa, p, x, ts, n_cap)
+    out, lse = run_dense(csa, p, x, ts, n_cap, split_ws)
     assert csa.csa_check_status() == 0
     for b, t in enumerate(ts):
         o, l = oracle_dense(p, x, b, t, m, n_cap)
-        assert_close(out[b, 0], o, "dense m=%d t=%d" % (m, t))
+        assert_close(out[b, 0], o, "dense m=%d t=%d split=%s" % (m, t, split_ws))
         np.testing.assert_allclose(lse[b, 0], l, rtol=1e-3, atol=1e-3)
 
 
@@ -126,7 +129,7 @@ def test_dense_attention_equals_the_sparse_call_with_every_entry_listed(csa):
     V = (t + 1) // m
     x = dense_inputs(91, 1, V)
     p = params(csa, m)
-    dense, _ = run_dense(csa, p, x, [t], V)
+    dense, _ = run_dense(csa, p, x, [t], V, split_ws=False)
     pk = csa.csa_default_params(m=m, topk=512)
     idx = torch.cat([torch.arange(V, dtype=torch.int32), torch.full((512 - V,), -1, dtype=torch.int32)]).view(1, 1, -1)
     out = torch.empty(1, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
@@ -161,3 +164,29 @@ def test_hca_decode_at_1m_context_sampled(csa):
     for b in (0, 5):
         o, l = oracle_dense(p, x, b, t, m, n_cap)
         assert_close(out[b, 0], o, "1m b=%d" % b)
+
+
+@pytest.mark.parametrize("inverse_rope", [0, 1])
+def test_split_kv_path_with_inverse_rope_and_sparse_selection(csa, inverse_rope):
+    """Few queries with a sparse selection (the 1M CSA shape: k = 1024 of
+    262144 entries, 8 sequences) through the split-KV path, with and without
+    the inverse RoPE epilogue (applied by the merge kernel)."""
+    B, n_cap, k, t = 8, 262144, 1024, 1048575
+    x = {"q": syn.main_query(94, B, 1), "kv": syn.cache_rows(94, B, n_cap, device=DEV),
+         "swa": syn.cache_rows(94, B, 128, name="swa"), "sink": syn.normal((64,), 94000, "sink", "cpu").float()}
+    g = torch.Generator().manual_seed(94)
+    sel = torch.stack([torch.sort(torch.randperm(n_cap, generator=g)[:k])[0] for _ in range(B)]).to(torch.int32)
+    p = csa.csa_default_params(topk=k, inverse_rope=inverse_rope)
+    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, 1, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_SPARSE_ATTN, p, B, 1, n_cap)
+    csa.csa_sparse_attn(p, B, 1, torch.full((B, 1), t, dtype=torch.int32, device=DEV), x["q"].to(DEV), x["kv"],
+                        n_cap, sel.view(B, 1, k).to(DEV), x["swa"].to(DEV), 0, 128, None, x["sink"].to(DEV), out, lse,
+                        ws)
+    assert csa.csa_check_status() == 0
+    for b in (0, 7):
+        ring = bits(x["swa"][b])
+        o, l = oracle.attend_query(t, bits(x["q"][b, 0]), sel[b].numpy(), bits(x["kv"][b]), lambda u: ring[u % 128],
+                                   bits(x["sink"]), W=128, sm_scale=p.sm_scale, inverse_rope_out=bool(inverse_rope))
+        assert_close(out[b, 0].float().cpu().numpy(), o, "split-kv b=%d" % b)
+        np.testing.assert_allclose(lse[b, 0].cpu().numpy(), l, rtol=1e-3, atol=1e-3)
