@@ -67,6 +67,12 @@ def _load():
         lib.orc_to_e4m3.argtypes = [ctypes.c_double]
         lib.orc_index_key_entry.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_double] * 2 + [ctypes.c_int64]
                                             + [_u16p] * 7 + [_f64p, _u8p])
+        lib.orc_e2m1.restype = ctypes.c_double
+        lib.orc_e2m1.argtypes = [ctypes.c_uint8]
+        lib.orc_to_e2m1.restype = ctypes.c_uint8
+        lib.orc_to_e2m1.argtypes = [ctypes.c_double]
+        lib.orc_quantize_kv_fp4.argtypes = [ctypes.c_int, _u16p, _u8p]
+        lib.orc_dequantize_kv_fp4.argtypes = [ctypes.c_int, _u8p, _f64p]
         lib.orc_visible.restype = ctypes.c_int64
         lib.orc_visible.argtypes = [ctypes.c_int64, ctypes.c_int]
         lib.orc_index_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _f64p]
@@ -304,6 +310,47 @@ def to_e4m3(x) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
     lib = _load()
     return np.array([lib.orc_to_e4m3(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def e2m1_to_f64(codes) -> np.ndarray:
+    """Values of E2M1 codes (the low 4 bits of each element)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.orc_e2m1(int(c) & 0xF) for c in codes.ravel()], np.float64).reshape(codes.shape)
+
+
+def to_e2m1(x) -> np.ndarray:
+    """Nearest E2M1 codes (ties to even, saturating at +-6, sign kept) of doubles."""
+    x = np.asarray(x, dtype=np.float64)
+    lib = _load()
+    return np.array([lib.orc_to_e2m1(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def quantize_kv_fp4(rows) -> np.ndarray:
+    """bf16 rows [n, D] -> FP4 entries [n, D/2 + D/16] bytes ([CSA2 详解] §16.1)."""
+    rows = _c(rows, np.uint16)
+    rows2 = rows.reshape(-1, rows.shape[-1])
+    D = rows2.shape[1]
+    out = np.empty((rows2.shape[0], D // 2 + D // 16), np.uint8)
+    for i in range(rows2.shape[0]):
+        r = np.ascontiguousarray(rows2[i])
+        o = np.empty(D // 2 + D // 16, np.uint8)
+        _load().orc_quantize_kv_fp4(D, _ptr(r, _u16p), _ptr(o, _u8p))
+        out[i] = o
+    return out.reshape(rows.shape[:-1] + (D // 2 + D // 16,))
+
+
+def dequantize_kv_fp4(entries, D: int = 512) -> np.ndarray:
+    """FP4 entries [n, D/2 + D/16] bytes -> their values [n, D] (doubles)."""
+    entries = _c(entries, np.uint8)
+    e2 = entries.reshape(-1, entries.shape[-1])
+    out = np.empty((e2.shape[0], D), np.float64)
+    for i in range(e2.shape[0]):
+        r = np.ascontiguousarray(e2[i])
+        o = np.empty(D, np.float64)
+        _load().orc_dequantize_kv_fp4(D, _ptr(r, _u8p), _ptr(o, _f64p))
+        out[i] = o
+    return out.reshape(entries.shape[:-1] + (D,))
 
 
 def index_key_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, *, rope_dim=64, theta=1e4, eps=1e-6):

@@ -228,6 +228,76 @@ void orc_index_key_entry(int m, int Dk, int R, double theta, double eps,
   free(y);
 }
 
+/* ---- FP4 cache entries ([CSA2 详解] §16.1: a Main KV entry is 512 FP4
+ * values with one 1-byte E4M3 scale per 16 values, 288 bytes) ------------- */
+
+/* Value of an E2M1 code: bit 3 the sign, bits 2..1 the exponent (bias 1),
+ * bit 0 the mantissa; exponent 0 is subnormal.  Magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6. */
+double orc_e2m1(uint8_t code) {
+  const int e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (code & 8) ? -mag : mag;
+}
+
+/* The E2M1 code nearest to x: ties go to the code with an even mantissa,
+ * magnitudes past 6 give +-6, the sign is kept (a small negative x gives
+ * -0).  Found by comparing with every code's value. */
+uint8_t orc_to_e2m1(double x) {
+  const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 8 : 0;
+  const double a = fabs(x);
+  int best = 0;
+  double best_err = a;
+  for (int c = 1; c <= 7; ++c) {
+    const double err = fabs(orc_e2m1((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/*
+ * One Main KV entry of D bf16 values in the FP4 layout.  Bytes 0 .. D/2-1:
+ * the E2M1 codes, channel 2j in the low nibble of byte j and channel 2j+1 in
+ * the high nibble; bytes D/2 .. D/2 + D/16 - 1: the E4M3 scales, scale g for
+ * channels 16g .. 16g+15.  Scale of a group: the E4M3 code nearest to
+ * amax / 6 (amax the group's largest magnitude), the quotient formed in
+ * binary32, as the kernel forms it, because it decides a code; code of a
+ * channel: E2M1 of x / s, the quotient again in binary32; a group whose
+ * scale is zero gets zero codes.  The stored value is s * e2m1(code).
+ */
+void orc_quantize_kv_fp4(int D, const uint16_t *x, uint8_t *out) {
+  for (int g = 0; g < D / 16; ++g) {
+    float amax = 0.0f;
+    for (int c = 16 * g; c < 16 * g + 16; ++c) {
+      const float v = (float)fabs(orc_bf16(x[c]));
+      if (v > amax) amax = v;
+    }
+    const float q = amax / 6.0f;
+    const uint8_t sc = orc_to_e4m3((double)q);
+    out[D / 2 + g] = sc;
+    const float s = (float)orc_e4m3(sc);
+    for (int c = 16 * g; c < 16 * g + 16; c += 2) {
+      uint8_t lo = 0, hi = 0;
+      if (s != 0.0f) {
+        lo = orc_to_e2m1((double)((float)orc_bf16(x[c]) / s));
+        hi = orc_to_e2m1((double)((float)orc_bf16(x[c + 1]) / s));
+      }
+      out[c / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+/* The D values an FP4 entry stands for: s * e2m1(code). */
+void orc_dequantize_kv_fp4(int D, const uint8_t *in, double *x) {
+  for (int c = 0; c < D; ++c) {
+    const uint8_t code = (uint8_t)((in[c / 2] >> (4 * (c & 1))) & 0xF);
+    x[c] = orc_e4m3(in[D / 2 + c / 16]) * orc_e2m1(code);
+  }
+}
+
 /* ---- visibility ([KV 压缩] §9.8) ---------------------------------------- */
 
 /* Entry s covers tokens up to m*s + m - 1, so the query at position t sees

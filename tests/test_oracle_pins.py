@@ -609,3 +609,62 @@ def test_single_stream_rope_position_is_m_times_i():
     ei = oracle.compress_single_entry(i, C, Z, B, w)
     np.testing.assert_allclose(oracle.rope(e0, 64, 1e4, m * i), ei, rtol=1e-9, atol=1e-12)
     np.testing.assert_array_equal(ei[:448], e0[:448])
+
+
+# ---- FP4 cache entries ([CSA2 详解] §16.1) ------------------------------------
+
+def test_e2m1_values_of_all_codes():
+    """The E2M1 grid (sign, 2 exponent bits with bias 1, 1 mantissa bit)."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    np.testing.assert_array_equal(oracle.e2m1_to_f64(np.arange(8)), mags)
+    np.testing.assert_array_equal(oracle.e2m1_to_f64(np.arange(8, 16)), [-m for m in mags])
+    assert math.copysign(1.0, oracle.e2m1_to_f64(np.array([8]))[0]) == -1.0
+
+
+def test_e2m1_rounding_is_nearest_with_ties_to_even_and_saturates():
+    codes = np.arange(16, dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.to_e2m1(oracle.e2m1_to_f64(codes))[1:], codes[1:])  # round trip (+0 / -0 apart)
+    ties = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}
+    for x, want in ties.items():
+        assert oracle.e2m1_to_f64(oracle.to_e2m1(np.array([x])))[0] == want, x
+        assert oracle.e2m1_to_f64(oracle.to_e2m1(np.array([-x])))[0] == -want, -x
+    np.testing.assert_array_equal(oracle.e2m1_to_f64(oracle.to_e2m1(np.array([6.5, 100.0, -7.0]))), [6.0, 6.0, -6.0])
+    grid = oracle.e2m1_to_f64(np.arange(16))
+    x = RNG.uniform(-7, 7, 2000)
+    got = oracle.e2m1_to_f64(oracle.to_e2m1(x))
+    err = np.abs(got - x)
+    assert np.all(err <= np.min(np.abs(grid[None, :] - x[:, None]), axis=1) + 1e-15)  # nearest by brute force
+
+
+def test_fp4_entry_layout_worked_example():
+    """Group 0 holds 6, -0.5, 3, 0 ... (scale E4M3(6/6) = 1.0, code 0x38): byte 0
+    = (code(-0.5) << 4) | code(6) = 0x97, byte 1 = 0x05 (3, then +0); other
+    groups are zero (scale code 0, zero codes)."""
+    x = np.zeros(512)
+    x[:4] = [6.0, -0.5, 3.0, 0.0]
+    e = oracle.quantize_kv_fp4(bf16_bits(x))
+    assert e.shape == (288,)
+    assert e[0] == 0x97 and e[1] == 0x05 and not e[2:256].any()
+    assert e[256] == 0x38 and not e[257:].any()
+    np.testing.assert_array_equal(oracle.dequantize_kv_fp4(e), x)
+
+
+def test_fp4_entries_on_the_grid_round_trip_and_others_round_to_the_nearest_code():
+    # rows that are exactly s * e2m1 with amax = 6 s round-trip
+    s = oracle.e4m3_to_f64(np.array([0x30, 0x38, 0x41, 0x2A], np.uint8))  # 0.5, 1, 2.25, 0.3125
+    vals = oracle.e2m1_to_f64(RNG.integers(0, 16, 512).astype(np.uint8))
+    vals[::16] = 6.0
+    x = vals * np.repeat(np.resize(s, 32), 16)
+    np.testing.assert_array_equal(oracle.dequantize_kv_fp4(oracle.quantize_kv_fp4(bf16_bits(x))), x)
+    # general rows: the scale is E4M3(amax/6), each code the nearest grid point of x/s
+    x = oracle.bf16_to_f64(rand_bf16(512, 2.0))
+    e = oracle.quantize_kv_fp4(bf16_bits(x))
+    deq = oracle.dequantize_kv_fp4(e)
+    grid = oracle.e2m1_to_f64(np.arange(16))
+    for g in range(32):
+        sc = oracle.e4m3_to_f64(e[256 + g:257 + g])[0]
+        amax = np.abs(x[16 * g:16 * g + 16]).max()
+        assert abs(sc - amax / 6) <= 0.0625 * amax / 6 + 1e-12  # E4M3: 3 mantissa bits
+        q = x[16 * g:16 * g + 16] / sc
+        best = np.min(np.abs(grid[None, :] - q[:, None]), axis=1)
+        assert np.all(np.abs(deq[16 * g:16 * g + 16] / sc - q) <= best + 1e-9)
