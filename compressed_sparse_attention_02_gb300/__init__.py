@@ -35,6 +35,7 @@ STATUS_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED",
 (CSA_OP_COMPRESS, CSA_OP_INDEX_TOPK, CSA_OP_SPARSE_ATTN, CSA_OP_LAYER_DECODE, CSA_OP_LAYER_PREFILL,
  CSA_OP_INDEX_TOPK_POOL, CSA_OP_REINDEX_TOPK) = range(7)
 CSA_POOL_BLOCK = 8
+CSA_FP4_ENTRY_BYTES = 288
 
 
 class CsaParams(ctypes.Structure):
@@ -42,7 +43,8 @@ class CsaParams(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("swa_window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
-                ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float), ("inverse_rope", ctypes.c_int32)]
+                ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float), ("inverse_rope", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 class CsaError(RuntimeError):
@@ -69,6 +71,8 @@ _lib.csa_compress_single.argtypes = [_P, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _
 _lib.csa_compress_single.restype = ctypes.c_int
 _lib.csa_compress_single_step.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp]
 _lib.csa_compress_single_step.restype = ctypes.c_int
+_lib.csa_quantize_kv_fp4.argtypes = [_i64, _vp, _i64, _vp, _i64, _vp]
+_lib.csa_quantize_kv_fp4.restype = ctypes.c_int
 _lib.csa_index_topk_pool.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_pool.restype = ctypes.c_int
 _lib.csa_reindex_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]
@@ -160,6 +164,11 @@ def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, w
     _check(_lib.csa_index_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
                                _ptr(idx_out), _ptr(score_out), _ptr(ws), 0 if ws is None else ws.numel(),
                                _stream(stream)), "csa_index_topk")
+
+
+def csa_quantize_kv_fp4(n_rows, inp, in_stride, out, out_stride, stream=None):
+    _check(_lib.csa_quantize_kv_fp4(n_rows, _ptr(inp), in_stride, _ptr(out), out_stride, _stream(stream)),
+           "csa_quantize_kv_fp4")
 
 
 def csa_index_topk_pool(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, pool_blocks, pool_out, ws,

@@ -17,7 +17,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libcsa.so")
-SOURCES = ["csa_api.cu", "compress.cu", "compress_single.cu", "index.cu", "topk.cu", "attn.cu"]
+SOURCES = ["csa_api.cu", "compress.cu", "compress_single.cu", "index.cu", "topk.cu", "attn.cu", "fp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

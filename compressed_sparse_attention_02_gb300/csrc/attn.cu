@@ -34,6 +34,8 @@
 // prefetches), so the HBM reads of the whole batch are in flight at once and
 // the tile gathers that follow mostly hit L2.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -57,7 +59,8 @@ constexpr int HW = kHeads / 2;                            // heads per warp (two
 constexpr int kMaxSplit = 4;  // the exchange below needs 2*(split-1)/split of 192 KiB
 static_assert(kKVBytes == kHeads * kDim * 4, "the KV buffer stages the fp32 partial output");
 
-constexpr size_t kSmemBytes = 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
+constexpr size_t kLutBytes = 256 * 4;  // FP4 rows: byte -> two bf16 E2M1 values
+constexpr size_t kSmemBytes = kLutBytes + 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
                               4 * kHeads * 4 + 2 * kMaxSplit * kHeads * 4 + 64;
 static_assert(kQBytes + kKVBytes == 192 * 1024, "the output exchange uses the Q and KV buffers");
 
@@ -86,6 +89,21 @@ __device__ __forceinline__ float inverse_rope(float x, int chn, float s, float c
   const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
   // pair (u, v) -> (u cos + v sin, -u sin + v cos)
   return (chn & 1) ? fmaf(x, c, -partner * s) : fmaf(x, c, partner * s);
+}
+
+// Two E2M1 codes (the low nibble first) as a bf16 pair: the E2M1 grid
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6 with the sign in bit 3.
+__device__ __forceinline__ uint32_t e2m1_pair_bf16(uint32_t byte) {
+  constexpr uint16_t kMag[8] = {0x0000, 0x3F00, 0x3F80, 0x3FC0, 0x4000, 0x4040, 0x4080, 0x40C0};
+  const uint32_t lo = kMag[byte & 7u] | ((byte & 8u) << 12), hi = kMag[(byte >> 4) & 7u] | ((byte & 0x80u) << 8);
+  return lo | (hi << 16);
+}
+
+// An E4M3 scale as a bf16 pair (E4M3 values are exact in bf16).
+__device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+  const float f = __half2float(__half(h));
+  return __floats2bfloat162_rn(f, f);
 }
 
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block.
@@ -134,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = recv_bar + 1;   // the Q tile (TMA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
+  uint32_t* lut = reinterpret_cast<uint32_t*>(flags + 4);        // [256] (FP4 rows)
 
   pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -241,14 +260,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Address of row j of the query's row set (null: absent / skipped).
   auto row_at = [&](int j) -> const uint16_t* {
     if (j < n_swa) return swa_row(j);
-    if (j < n_rows) return kv_b + static_cast<int64_t>(a.dense ? j - n_swa : sel_s[j - n_swa]) * kDim;
+    if (j < n_rows) {
+      const int64_t e = a.dense ? j - n_swa : sel_s[j - n_swa];
+      if (a.kv_fp4)  // an FP4 entry: its address, read as bytes by the gather
+        return reinterpret_cast<const uint16_t*>(a.kv_fp4 + (static_cast<int64_t>(b) * a.n_cap + e) * kFp4Entry);
+      return kv_b + e * kDim;
+    }
     return nullptr;
   };
-  // Put every row of the slice in flight towards L2.
+  // Put every row of the slice in flight towards L2 (an FP4 entry spans at
+  // most four 128-byte lines).
   for (int j = r_lo + tid; j < r_hi; j += kThreads) {
     const uint16_t* src = row_at(j);
-    if (src) prefetch_row_l2(src);
+    if (!src) continue;
+    if (a.kv_fp4 && j >= n_swa) {
+      const uint8_t* e = reinterpret_cast<const uint8_t*>(src);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(e) : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + 128) : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + 256) : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + kFp4Entry - 1) : "memory");
+    } else {
+      prefetch_row_l2(src);
+    }
   }
+  if (a.kv_fp4) lut[tid] = e2m1_pair_bf16(tid);  // kThreads == 256: one entry per thread
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -273,7 +308,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- gather 128 rows: thread tid copies 16-byte chunk (tid & 7) of
     //      channel block (tid >> 3) & 7 of rows (tid >> 6) + 4i, so a warp
     //      covers 512 contiguous bytes of a row
-    {
+    if (a.kv_fp4) {
+      // FP4 rows: 16 threads per row; thread `part` owns channels 32*part ..
+      // 32*part+31 (16 code bytes and 2 scales of the entry; 64 bytes =
+      // chunks 4*(part&1) .. +3 of channel block part>>1 of the tile), loads
+      // all of its rows first, then writes them as bf16 (value * scale is
+      // exact in bf16).  Window rows (bf16) take the same 64 bytes by cp.async.
+      const int part = tid & 15, pblk = part >> 1, c0 = (part & 1) * 4;
+      uint8_t* blk_s = kv_s + pblk * kKVBlock;
+      constexpr int kRowsPer = kTileRows * 16 / kThreads;  // 8
+      uint4 nib[kRowsPer];
+      uint32_t scl[kRowsPer];
+#pragma unroll
+      for (int i = 0; i < kRowsPer; ++i) {
+        const int r = (tid >> 4) + i * (kThreads / 16);
+        const uint8_t* e = reinterpret_cast<const uint8_t*>(row_src[r]);
+        const bool packed = e && r0 + r >= n_swa;
+        nib[i] = packed ? __ldg(reinterpret_cast<const uint4*>(e + 16 * part)) : make_uint4(0u, 0u, 0u, 0u);
+        scl[i] = packed ? __ldg(reinterpret_cast<const unsigned short*>(e + kDim / 2 + 2 * part)) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kRowsPer; ++i) {
+        const int r = (tid >> 4) + i * (kThreads / 16);
+        const uint16_t* src = row_src[r];
+        if (src && r0 + r < n_swa) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cp_async_16(blk_s + swz(r, c0 + k), src + pblk * 64 + (c0 + k) * 8);
+          continue;
+        }
+        const __nv_bfloat162 s_lo = e4m3_bf16x2(scl[i] & 0xFFu), s_hi = e4m3_bf16x2(scl[i] >> 8);
+        const uint32_t w[4] = {nib[i].x, nib[i].y, nib[i].z, nib[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // chunk k: code bytes 4k .. 4k+3 (8 channels)
+          const __nv_bfloat162 sc = k < 2 ? s_lo : s_hi;
+          uint32_t o[4];
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t v = lut[(w[k] >> (8 * bb)) & 0xFFu];
+            const __nv_bfloat162 x = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), sc);
+            o[bb] = *reinterpret_cast<const uint32_t*>(&x);
+          }
+          *reinterpret_cast<uint4*>(blk_s + swz(r, c0 + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else {
       const int pblk = (tid >> 3) & 7, pc = tid & 7;
       uint8_t* blk_s = kv_s + pblk * kKVBlock;
 #pragma unroll

@@ -76,6 +76,9 @@ bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 // CSA block sizes 1..8.
 csa_status check_overlapped(const csa_params* p) { return p->m <= 8 ? CSA_OK : CSA_ERR_UNSUPPORTED; }
 
+// Calls that write or read the cache as bf16 rows.
+csa_status check_bf16_cache(const csa_params* p) { return p->kv_format == 0 ? CSA_OK : CSA_ERR_UNSUPPORTED; }
+
 // Dimensions the kernels are built for; anything else is unsupported.
 csa_status check_params(const csa_params* p) {
   if (!p) return CSA_ERR_INVALID_ARG;
@@ -89,6 +92,7 @@ csa_status check_params(const csa_params* p) {
   if (p->swa_window < 1 || p->swa_window > csa::kMaxWindow) return CSA_ERR_UNSUPPORTED;
   if (!(p->rope_theta > 0.f) || !(p->rms_eps >= 0.f) || !isfinite(p->sm_scale)) return CSA_ERR_INVALID_ARG;
   if (p->inverse_rope != 0 && p->inverse_rope != 1) return CSA_ERR_INVALID_ARG;
+  if (p->kv_format != 0 && p->kv_format != 1) return CSA_ERR_UNSUPPORTED;
   return CSA_OK;
 }
 
@@ -263,7 +267,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
 }
 
 csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, int64_t pos_base,
-                    const uint16_t* q, const uint16_t* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
+                    const uint16_t* q, const void* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
                     int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
                     const float* sink, uint16_t* out, float* lse, cudaStream_t st, bool dense = false,
                     void* split_ws = nullptr, size_t split_ws_bytes = 0) {
@@ -274,7 +278,10 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.q_pos = q_pos;
   aa.pos_base = pos_base;
   aa.q = q;
-  aa.kv = kv;
+  if (p->kv_format == 1)
+    aa.kv_fp4 = static_cast<const uint8_t*>(kv);
+  else
+    aa.kv = static_cast<const uint16_t*>(kv);
   aa.n_cap = n_cap;
   aa.idx = idx;
   aa.k = p->topk;
@@ -387,6 +394,7 @@ void csa_default_params(csa_params* p) {
   p->rms_eps = 1e-6f;
   p->sm_scale = 0.044194173824159216f;  // 1/sqrt(512)
   p->inverse_rope = 0;
+  p->kv_format = 0;
 }
 
 size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {
@@ -430,6 +438,7 @@ csa_status csa_compress(const csa_params* p, int32_t B, int32_t n_new, int64_t e
                         uint16_t* kv_out, int64_t kv_stride_b, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
   if (B == 0 || n_new == 0) return CSA_OK;
@@ -476,6 +485,7 @@ csa_status csa_compress_single(const csa_params* p, int32_t B, int32_t n_new, in
                                int64_t kv_stride_b, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
   if (B == 0 || n_new == 0) return CSA_OK;
   if (!ok_ptr(C) || !ok_ptr(Z) || !ok_opt(bias) || !ok_ptr(rms_w) || !ok_ptr(kv_out)) return CSA_ERR_INVALID_ARG;
@@ -493,6 +503,7 @@ csa_status csa_compress_single_step(const csa_params* p, int32_t B, const int32_
                                     uint16_t* kv_out, int64_t kv_stride_b, int64_t n_cap, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
   if (B == 0) return CSA_OK;
   if (!ok_ptr(q_pos) || !ok_ptr(C) || !ok_ptr(Z) || !ok_opt(bias) || !ok_ptr(rms_w) || !ok_ptr(state) ||
@@ -506,6 +517,17 @@ csa_status csa_compress_single_step(const csa_params* p, int32_t B, const int32_
                                        kv_out, kv_stride_b, n_cap, q_pos, status);
   ca.state = state;
   return cuda_status(csa::launch_compress_single(ca, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_quantize_kv_fp4(int64_t n_rows, const uint16_t* in, int64_t in_stride, uint8_t* out,
+                               int64_t out_stride, void* stream) {
+  if (n_rows < 0 || n_rows > (int64_t(1) << 40)) return CSA_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA_OK;
+  if (!ok_ptr(in) || !ok_ptr(out)) return CSA_ERR_INVALID_ARG;
+  if (in_stride < csa::kDim || in_stride % 8 != 0 || out_stride < csa::kFp4Entry || out_stride % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  return cuda_status(csa::launch_quantize_kv_fp4(n_rows, in, in_stride, out, out_stride,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,
@@ -578,7 +600,7 @@ csa_status csa_reindex_topk(const csa_params* p, int32_t B, int32_t Q, const int
 }
 
 csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint16_t* q,
-                           const uint16_t* kv_comp, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
+                           const void* kv_comp, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
                            int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, const float* sink,
                            uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   (void)workspace;
@@ -609,6 +631,7 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
                             uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
   if (B == 0) return CSA_OK;
@@ -659,6 +682,7 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
                              size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || pos0 < 0 || pos0 % p->m != 0 || !n_cap_ok(n_cap))
     return CSA_ERR_INVALID_ARG;

@@ -1,0 +1,72 @@
+// FP4 cache entries ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §16.1: a
+// Main KV entry of 512 FP4 values with one 1-byte E4M3 scale per 16 values,
+// 288 bytes).  Layout of an entry: bytes 0..255 the E2M1 codes (channel 2j
+// in the low nibble of byte j), bytes 256..287 the E4M3 scales (scale g for
+// channels 16g..16g+15).  A group's scale is the E4M3 code nearest to
+// amax/6 and a channel's code the E2M1 code nearest to x/scale, saturating,
+// both quotients in binary32.
+//
+// One warp per entry, one lane per 16-channel group: two 16-byte loads, the
+// group maximum, the scale, eight paired conversions, one 8-byte store of
+// codes and one scale byte.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kRowsPerCta = 8;
+
+__global__ void __launch_bounds__(32 * kRowsPerCta) quantize_kv_fp4_kernel(const int64_t n_rows, const uint16_t* in,
+                                                                          const int64_t in_stride, uint8_t* out,
+                                                                          const int64_t out_stride) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  const int g = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(in + row * in_stride + 16 * g);
+  const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float x[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    x[2 * j] = __uint_as_float(w[j] << 16);
+    x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+  }
+  const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
+  const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+  uint32_t codes[2] = {0u, 0u};
+  if (s != 0.f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_fp4x2_storage_t pr =
+          __nv_cvt_float2_to_fp4x2(make_float2(__fdiv_rn(x[2 * j], s), __fdiv_rn(x[2 * j + 1], s)), __NV_E2M1,
+                                   cudaRoundNearest);
+      codes[j >> 2] |= static_cast<uint32_t>(pr) << (8 * (j & 3));
+    }
+  }
+  uint8_t* dst = out + row * out_stride;
+  *reinterpret_cast<uint2*>(dst + 8 * g) = make_uint2(codes[0], codes[1]);
+  dst[kDim / 2 + g] = sc;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_kv_fp4(int64_t n_rows, const uint16_t* in, int64_t in_stride, uint8_t* out,
+                                   int64_t out_stride, cudaStream_t stream) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int64_t ctas = (n_rows + kRowsPerCta - 1) / kRowsPerCta;
+  if (ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_pdl(quantize_kv_fp4_kernel, dim3(static_cast<unsigned>(ctas)), dim3(32 * kRowsPerCta), 0, stream,
+                    n_rows, in, in_stride, out, out_stride);
+}
+
+}  // namespace csa

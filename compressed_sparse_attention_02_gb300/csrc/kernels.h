@@ -59,6 +59,7 @@ constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
 constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k finish stages in shared memory
 constexpr int kTopkCandCapMax = 16384;  // the longest global candidate list of a row
+constexpr int kFp4Entry = kDim / 2 + kDim / 16;  // 288: E2M1 codes + one E4M3 scale per 16 values
 constexpr int kPoolBlock = 8;         // entries per block of the hierarchical indexer's pool
 constexpr int kPoolTileBlocks = 16;   // pool blocks per 128-key indexer tile
 
@@ -167,7 +168,8 @@ struct AttnArgs {
   const int32_t* q_pos;     // [B][Q] or null (then pos_base + q)
   int64_t pos_base;
   const uint16_t* q;        // [B][Q][64][512]
-  const uint16_t* kv;       // [B][n_cap][512]
+  const uint16_t* kv;       // [B][n_cap][512] bf16 (unused with kv_fp4)
+  const uint8_t* kv_fp4;    // [B][n_cap][kFp4Entry] FP4 entries, or null
   int64_t n_cap;
   const int32_t* idx;       // [B][Q][k] (sparse)
   int k;
@@ -201,5 +203,11 @@ inline size_t attn_split_bytes(int64_t queries) {
                                      : static_cast<size_t>(queries) * kMaxGSplit * (kHeads * kDim + 2 * kHeads) * 4;
 }
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream);
+
+// ---- FP4 cache entries -------------------------------------------------------------
+// bf16 rows of kDim (row r at in + r*in_stride) -> FP4 entries of kFp4Entry
+// bytes (entry r at out + r*out_stride).
+cudaError_t launch_quantize_kv_fp4(int64_t n_rows, const uint16_t* in, int64_t in_stride, uint8_t* out,
+                                   int64_t out_stride, cudaStream_t stream);
 
 }  // namespace csa

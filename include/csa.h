@@ -73,7 +73,12 @@ typedef struct {
   float sm_scale;     /* logit scale applied to q·kv (1/sqrt(512))            */
   int32_t inverse_rope; /* 1: rotate the output's last rope_dim channels back
                            by the query position (see csa_sparse_attn); 0    */
+  int32_t kv_format;  /* compressed cache entries: 0 bf16 (512 x 2 B), 1 FP4
+                         (CSA_FP4_ENTRY_BYTES, see csa_quantize_kv_fp4); the
+                         layer calls and the compressors write bf16 only    */
 } csa_params;
+
+#define CSA_FP4_ENTRY_BYTES 288
 
 /* Fills *p with the V4-Flash CSA values listed above (topk = 512). */
 void csa_default_params(csa_params *p);
@@ -268,6 +273,24 @@ csa_status csa_index_topk_static(const csa_params *p, int32_t B, int32_t Q,
                                  float *score_out, void *stream);
 
 /*
+ * csa_quantize_kv_fp4 — compressed cache entries to the FP4 layout ([CSA2 详解]
+ * §16.1: 512 FP4 values and one 1-byte E4M3 scale per 16 values, 288 bytes).
+ * Entry layout: bytes 0..255 the E2M1 codes, channel 2j in the low nibble of
+ * byte j and 2j+1 in the high nibble; bytes 256..287 the E4M3 scales, scale g
+ * for channels 16g..16g+15.  Scale of a group: the E4M3 code nearest to
+ * amax/6 (amax its largest magnitude); code of a channel: the E2M1 code
+ * nearest to x/scale (ties to the even code, saturating at +-6, the sign
+ * kept); both quotients are formed in binary32; a zero scale gives zero
+ * codes.  The entry stands for scale * e2m1(code).
+ *
+ * in  : n_rows rows of 512 bf16, row r at in + r*in_stride (elements).
+ * out : entry r at out + r*out_stride (bytes, a multiple of 16, >= 288).
+ */
+csa_status csa_quantize_kv_fp4(int64_t n_rows, const uint16_t *in,
+                               int64_t in_stride, uint8_t *out,
+                               int64_t out_stride, void *stream);
+
+/*
  * Hierarchical indexer ([CSA2 详解] §11 "Hierarchical Sparse Indexer"; §11.1
  * on why the pool is larger than top-k; §20.1: a Reindex layer gathers the
  * candidates before it scores them).  A Full layer scores every visible
@@ -335,7 +358,11 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  * The sink enters the denominator only and is not scaled by sm_scale.
  * lse[b,q,h] (optional) = log(sum_j e^{l_hj} + e^{sink[h]}).
  *
- * q      : [B][Q][64][512] bf16.        kv_comp : [B][n_cap][512] bf16.
+ * q      : [B][Q][64][512] bf16.
+ * kv_comp: p->kv_format 0: [B][n_cap][512] bf16; 1: [B][n_cap][288] FP4
+ *          entries (csa_quantize_kv_fp4), gathered at 288 B per row and
+ *          expanded to bf16 on chip (value * scale is exact in bf16).  The
+ *          window rows are bf16 either way.
  * idx    : [B][Q][topk] int32, -1 marks an empty slot; any other value outside
  *          [0, n_cap) records CSA_ERR_INDEX_RANGE and the slot is skipped.
  *          NULL: dense attention, the HCA read path ([hca_csa] "HCA：同一个
@@ -366,7 +393,7 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  */
 csa_status csa_sparse_attn(const csa_params *p, int32_t B, int32_t Q,
                            const int32_t *q_pos, const uint16_t *q,
-                           const uint16_t *kv_comp, int64_t n_cap,
+                           const void *kv_comp, int64_t n_cap,
                            const int32_t *idx, const uint16_t *swa,
                            int32_t swa_mode, int64_t swa_len,
                            const int32_t *swa_pos0, const float *sink,
