@@ -230,6 +230,7 @@ def run_ours(args, rank, world, local_rank):
         result["prefill"] = prefill_profile(csa, torch, dev)
         result["hierarchical"] = [hierarchical_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
         result["hca"] = hca_profile(csa, torch, dev)
+        result["fp4_cache"] = fp4_profile(csa, torch, dev, x, w)
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -457,6 +458,65 @@ def hierarchical_profile(csa, torch, dev, cfg, pool_blocks=2048, sets=4):
     del kI, qs, q2, pools, ws_full, ws_plain, ws_re
     torch.cuda.empty_cache()
     return res
+
+
+def fp4_profile(csa, torch, dev, x, w, sets=4):
+    """The FP4 cache ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §16.1, 288 B
+    per entry) on the decode workload: the quantizer over the whole cache, and
+    the sparse attention alone over the bf16 and the FP4 cache with the same
+    selections (4 sets of 512 random entries per query, rotated)."""
+    hbm, bf16, _ = peaks()
+    B, n_cap, k = w.B, w.n_cap, w.topk
+    kv = x["kv"]
+    fp4 = torch.empty(B, n_cap, 288, dtype=torch.uint8, device=dev)
+
+    def quant():
+        csa.csa_quantize_kv_fp4(B * n_cap, kv, 512, fp4, 288)
+    quant()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        quant()
+    e1.record()
+    torch.cuda.synchronize()
+    qms = e0.elapsed_time(e1) / 10
+    qbytes = B * n_cap * (1024 + 288)
+    g = torch.Generator().manual_seed(7)
+    sels = [torch.stack([torch.sort(torch.randperm(n_cap, generator=g)[:k])[0] for _ in range(B)])
+            .to(torch.int32).view(B, 1, k).to(dev) for _ in range(sets)]
+    qs = [syn_main_query(w, B, r, dev) for r in range(sets)]
+    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=dev)
+    res = {"workload": w.name, "quantize": {"entries": B * n_cap, "ms": qms, "gbs": qbytes / (qms * 1e-3) / 1e9,
+                                            "hbm_frac": qbytes / (qms * 1e-3) / 1e9 / hbm}}
+    for fmt, cache in (("bf16", kv), ("fp4", fp4)):
+        p = csa.csa_default_params(topk=k, kv_format=1 if fmt == "fp4" else 0)
+
+        def attn(i):
+            csa.csa_sparse_attn(p, B, 1, x["q_pos"], qs[i % sets], cache, n_cap, sels[i % sets], x["swa"], 0, w.W,
+                                None, x["sink"], out, None)
+        for i in range(8):
+            attn(i)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(200):
+            attn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 200
+        row = 288 if fmt == "fp4" else 1024
+        byts = B * (k * row + w.W * 1024 + 2 * 64 * 1024)
+        res["attention_" + fmt] = {"ms": ms, "gbs": byts / (ms * 1e-3) / 1e9, "bytes": byts}
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the FP4 section")
+    del fp4, sels, qs, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def syn_main_query(w, B, r, dev):
+    import synthetic as syn
+    return syn.main_query(w.config + 5000 + 1000 * r, B, 1, device=dev)
 
 
 def hca_profile(csa, torch, dev, m=128):
