@@ -44,7 +44,7 @@ class CsaParams(ctypes.Structure):
                 ("rope_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("swa_window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float), ("inverse_rope", ctypes.c_int32),
-                ("kv_format", ctypes.c_int32)]
+                ("kv_format", ctypes.c_int32), ("bf16_scores", ctypes.c_int32)]
 
 
 class CsaError(RuntimeError):

@@ -93,6 +93,7 @@ csa_status check_params(const csa_params* p) {
   if (!(p->rope_theta > 0.f) || !(p->rms_eps >= 0.f) || !isfinite(p->sm_scale)) return CSA_ERR_INVALID_ARG;
   if (p->inverse_rope != 0 && p->inverse_rope != 1) return CSA_ERR_INVALID_ARG;
   if (p->kv_format != 0 && p->kv_format != 1) return CSA_ERR_UNSUPPORTED;
+  if (p->bf16_scores != 0 && p->bf16_scores != 1) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 
@@ -111,7 +112,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // clears them); the two position bitmaps; the candidate keys and positions.
 bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
   if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
-  w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 4));
+  w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 8));  // 16-byte rows as bf16 too
   w->bits_ld = csa::topk_bits_ld(n_cap);
   w->cand_cap = csa::topk_cand_cap(n_cap, k);
   const size_t R = static_cast<size_t>(rows);
@@ -219,6 +220,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ia.n_cap = n_cap;
   ia.scores = scores;
   ia.score_ld = w.score_ld;
+  ia.bf16_scores = p->bf16_scores;
   ia.hist = hist;
   if (pool && pool->in) {
     ia.pool = pool->in;
@@ -237,6 +239,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
 
   csa::TopkArgs ta = {};
   topk_scratch(&ta, wsb, w);
+  ta.bf16_scores = p->bf16_scores;
   ta.q_pos = q_pos;
   ta.pos_base = pos_base;
   ta.B = B;
@@ -258,6 +261,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     topk_scratch(&tb, wsb_blk, wb);
     tb.k = pool->blocks;
     tb.vis_shift = 3;
+    tb.bf16_scores = 0;  // the block scores stay fp32
     tb.idx_out = pool->out;
     tb.score_out = nullptr;
   }
@@ -395,6 +399,7 @@ void csa_default_params(csa_params* p) {
   p->sm_scale = 0.044194173824159216f;  // 1/sqrt(512)
   p->inverse_rope = 0;
   p->kv_format = 0;
+  p->bf16_scores = 0;
 }
 
 size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {

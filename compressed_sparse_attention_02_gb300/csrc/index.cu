@@ -115,6 +115,14 @@ __device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, int64_t g, i
   return gi;
 }
 
+// A score into the row array: fp32, or its bf16 bits (already rounded).
+__device__ __forceinline__ void store_score(const IndexArgs& a, int64_t at, float v) {
+  if (a.bf16_scores)
+    reinterpret_cast<uint16_t*>(a.scores)[at] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
+  else
+    a.scores[at] = v;
+}
+
 // True if a query of the group sits past what the cache holds (V(t) > n_cap).
 template <int QPC>
 __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const GroupInfo& gi) {
@@ -441,7 +449,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
             }
           }
         }
-        const float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        // bf16 scores: every use below (store, digit counts, block maxima)
+        // sees the rounded value
+        if (a.bf16_scores) score = __bfloat162float(__float2bfloat16_rn(score));
         const bool in_row = s_idx < gi.vis[j];
         bool valid = in_row;
         const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
@@ -450,9 +461,9 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
           const int64_t nb = (gi.vent[j] + kPoolBlock - 1) / kPoolBlock;
           if (blk >= nb && (row & 7) == 0) record_error(a.status, kErrIndexRange);
           valid = blk >= 0 && static_cast<int64_t>(blk) * kPoolBlock + (row & 7) < gi.vent[j];
-          a.scores[row_off * a.score_ld + s_idx] = valid ? score : -INFINITY;
+          store_score(a, row_off * a.score_ld + s_idx, valid ? score : -INFINITY);
         } else if (valid) {
-          a.scores[row_off * a.score_ld + s_idx] = score;
+          store_score(a, row_off * a.score_ld + s_idx, score);
         }
         if (a.block_scores) {  // the block's largest score: 8 adjacent lanes
           float bm = valid ? score : -INFINITY;

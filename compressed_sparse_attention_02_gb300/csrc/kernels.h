@@ -102,8 +102,9 @@ struct IndexArgs {
   int64_t pos_base;
   int B, Q, m;
   int64_t n_cap;
-  float* scores;            // [B*Q][score_ld]
-  int64_t score_ld;
+  float* scores;            // [B*Q][score_ld] fp32, or bf16 (uint16) with bf16_scores
+  int64_t score_ld;         // elements (a multiple of 8)
+  int bf16_scores;          // 1: scores rounded to bf16 and stored as 2 bytes
   uint32_t* hist;           // [B*Q][2048] key top-digit counts (zeroed by the caller) or null
   // Full layer of the hierarchical indexer: per row, the largest score of
   // each block of kPoolBlock entries with a visible first entry, and the
@@ -124,8 +125,9 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
 
 // ---- top-k -------------------------------------------------------------------------
 struct TopkArgs {
-  const float* scores;
+  const float* scores;      // fp32, or bf16 (uint16) with bf16_scores
   int64_t score_ld;
+  int bf16_scores;
   const uint32_t* hist;     // [B*Q][2048] key first-digit counts from the indexer
   const int32_t* q_pos;
   int64_t pos_base;

@@ -232,6 +232,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // nb = min(pool_blocks, ceil(V/8)) ascending blocks, all entries visible but
 // those of block ceil(V/8)-1 past V, which can only be the pool's last.
 // *ventries receives V.
+// Score i of a row (fp32, or bf16 bits widened exactly).
+__device__ __forceinline__ float row_score(const TopkArgs& a, int64_t row, int64_t i) {
+  if (a.bf16_scores)
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(a.scores) +
+                                                      row * a.score_ld + i))
+                           << 16);
+  return __ldg(a.scores + row * a.score_ld + i);
+}
+
 __device__ __forceinline__ int64_t row_extent(const TopkArgs& a, int b, int q, int64_t* ventries) {
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row]) : a.pos_base + q;
@@ -311,7 +320,6 @@ __device__ __forceinline__ void for_candidates(bool staged, int nc, const Smem& 
 // The finish of one row, run by the last of its CTAs.
 __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
                            Smem& sm) {
-  const float* src = a.scores + row * a.score_ld;
   const uint32_t* bits = a.bits + row * a.bits_ld;
   uint32_t* ties = a.ties + row * a.bits_ld;
   const int lane = threadIdx.x & 31;
@@ -419,14 +427,14 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
     } else {
       // the candidate list overflowed: the same digits counted over the row's scores
       const uint32_t thr =
-          resolve_threshold(dstar, V, [&](int64_t i) { return score_key(__ldg(src + i)); }, sm, &need, &n_eq);
+          resolve_threshold(dstar, V, [&](int64_t i) { return score_key(row_score(a, row, i)); }, sm, &need, &n_eq);
       const bool all_eq = n_eq == need;
       for (int64_t i0 = 0; i0 < V; i0 += kBatch * kThreads) {
         float xv[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int64_t i = i0 + u * kThreads + threadIdx.x;
-          xv[u] = i < V ? __ldg(src + i) : 0.f;
+          xv[u] = i < V ? row_score(a, row, i) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
@@ -487,7 +495,7 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
   for (int j = threadIdx.x; j < a.k; j += kThreads) {
     const int32_t p = j < out ? sm.u.c.sel[j] : -1;
     idx[j] = out_entry(a, row, ventries, p);
-    if (sc) sc[j] = p >= 0 ? __ldg(src + p) + 0.0f : -INFINITY;
+    if (sc) sc[j] = p >= 0 ? row_score(a, row, p) + 0.0f : -INFINITY;
   }
 }
 
@@ -522,12 +530,11 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   int64_t ventries;
   const int64_t V = row_extent(a, b, q, &ventries);
-  const float* src = a.scores + row * a.score_ld;
   if (V <= a.k) {  // every visible entry is selected; the row's first CTA writes it
     if (blockIdx.x != 0) return;
     for (int j = threadIdx.x; j < a.k; j += kThreads) {
       a.idx_out[row * a.k + j] = j < V ? out_entry(a, row, ventries, j) : -1;
-      if (a.score_out) a.score_out[row * a.k + j] = j < V ? __ldg(src + j) + 0.0f : -INFINITY;
+      if (a.score_out) a.score_out[row * a.k + j] = j < V ? row_score(a, row, j) + 0.0f : -INFINITY;
     }
     return;
   }
@@ -537,14 +544,16 @@ __global__ void __launch_bounds__(kThreads, 4)
   // the row's digit counts and the chunk's scores, one bulk copy each on
   // barriers of their own: the crossing search starts once the counts land
   if (threadIdx.x == 0) {
-    const uint32_t vbytes = static_cast<uint32_t>((n_in * 4 + 15) & ~15);  // score rows are padded to 16 B
+    const int esz = a.bf16_scores ? 2 : 4;
+    const uint32_t vbytes = static_cast<uint32_t>((n_in * esz + 15) & ~15);  // score rows are padded to 16 B
     mbar_init(&sm.hist_bar, 1);
     mbar_init(&sm.vals_bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&sm.hist_bar, kKeyBins * 4);
     bulk_load(sm.h.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
     mbar_arrive_expect_tx(&sm.vals_bar, vbytes);
-    bulk_load(sm.u.f.vals, src + i0, vbytes, &sm.vals_bar);
+    bulk_load(sm.u.f.vals, reinterpret_cast<const uint8_t*>(a.scores) + (row * a.score_ld + i0) * esz, vbytes,
+              &sm.vals_bar);
     sm.n_local = 0;
   }
   __syncthreads();
@@ -565,8 +574,15 @@ __global__ void __launch_bounds__(kThreads, 4)
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int jj = (j + (t >> 1)) & 3;
-    const float4 x = reinterpret_cast<const float4*>(sm.u.f.vals)[4 * t + jj];
-    const float xs[4] = {x.x, x.y, x.z, x.w};
+    float xs[4];
+    if (a.bf16_scores) {  // the chunk holds bf16 bits: keys 16t .. 16t+15 are 32 bytes
+      const uint2 h = reinterpret_cast<const uint2*>(sm.u.f.vals)[4 * t + jj];
+      xs[0] = __uint_as_float(h.x << 16), xs[1] = __uint_as_float(h.x & 0xFFFF0000u);
+      xs[2] = __uint_as_float(h.y << 16), xs[3] = __uint_as_float(h.y & 0xFFFF0000u);
+    } else {
+      const float4 x = reinterpret_cast<const float4*>(sm.u.f.vals)[4 * t + jj];
+      xs[0] = x.x, xs[1] = x.y, xs[2] = x.z, xs[3] = x.w;
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int bit = 4 * jj + e;
@@ -593,7 +609,12 @@ __global__ void __launch_bounds__(kThreads, 4)
       const int bit = __ffs(cmask) - 1;
       cmask &= cmask - 1;
       if (slot < kLocalCap) {
-        sm.u.f.lkey[slot] = score_key(sm.u.f.vals[16 * t + bit]);
+        const float v = a.bf16_scores
+                            ? __uint_as_float(static_cast<uint32_t>(
+                                                  reinterpret_cast<const unsigned short*>(sm.u.f.vals)[16 * t + bit])
+                                              << 16)
+                            : sm.u.f.vals[16 * t + bit];
+        sm.u.f.lkey[slot] = score_key(v);
         sm.u.f.lpos[slot] = static_cast<int32_t>(i0 + 16 * t + bit);
       }
       ++slot;

@@ -76,6 +76,13 @@ typedef struct {
   int32_t kv_format;  /* compressed cache entries: 0 bf16 (512 x 2 B), 1 FP4
                          (CSA_FP4_ENTRY_BYTES, see csa_quantize_kv_fp4); the
                          layer calls and the compressors write bf16 only    */
+  int32_t bf16_scores; /* 1: the indexer rounds each score to bf16 (nearest,
+                           ties to even) and the top-k selects on the rounded
+                           values, ties to the smaller entry as always;
+                           score_out returns the rounded values.  Halves the
+                           score traffic ([KV 压缩] §7, "Oracle top-k vs
+                           learned top-k": BF16 scores for the selector).
+                           0: fp32 scores                                 */
 } csa_params;
 
 #define CSA_FP4_ENTRY_BYTES 288

@@ -39,7 +39,7 @@ def test_default_params_and_status_strings(lib):
     assert (p.m, p.n_heads, p.head_dim, p.rope_dim, p.idx_heads, p.idx_dim, p.topk, p.swa_window) == \
         (4, 64, 512, 64, 64, 128, 512, 128)
     assert abs(p.sm_scale - 512 ** -0.5) < 1e-7 and p.rope_theta == 1e4
-    assert p.inverse_rope == 0 and p.kv_format == 0 and ctypes.sizeof(p) == 13 * 4
+    assert p.inverse_rope == 0 and p.kv_format == 0 and p.bf16_scores == 0 and ctypes.sizeof(p) == 14 * 4
     for s in range(7):
         assert lib.csa_status_string(s).startswith(lib.STATUS_NAMES[s])
 

@@ -186,3 +186,57 @@ def test_long_candidate_list_read_from_global_memory(csa, period, k):
     t = 4 * n_cap - 1
     idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
     check_row(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, what="period %d" % period)
+
+
+def check_row_bf16(idx, sc, qI, wI, kI, t, k, what):
+    """bf16 scores: the returned scores are bf16 values within one bf16 step
+    of the oracle's; every entry left out scores (in bf16) at most the
+    lowest selected one, up to that step; ascending, -1 padded."""
+    V = oracle.visible(t)
+    s = oracle.index_scores(bits(qI), bits(wI), bits(kI)[:V])
+    r = oracle.bf16_to_f64(oracle.f64_to_bf16_bits(s))
+    n = min(k, V)
+    sel = idx[:n]
+    assert np.all(idx[n:] == -1), what + ": padding"
+    assert np.all(np.diff(sel) > 0) and (n == 0 or (sel.min() >= 0 and sel.max() < V)), what + ": order / range"
+    got = sc[:n].astype(np.float64)
+    assert np.array_equal(oracle.bf16_to_f64(oracle.f64_to_bf16_bits(got)), got), what + ": not bf16 values"
+    step = 2.0 ** -7 * np.abs(r[sel]) + 1e-30
+    assert np.all(np.abs(got - r[sel]) <= step), what + ": scores"
+    if n < V and n > 0:
+        kth = got.min()
+        out = np.setdiff1d(np.arange(V), sel)
+        assert np.all(r[out] <= kth + 2.0 ** -7 * abs(kth)), what + ": a left-out entry outranks the selection"
+    assert np.all(np.isneginf(sc[n:]))
+
+
+@pytest.mark.parametrize("cfg,samples", [(2, [0, 40]), (3, [1])])
+def test_bf16_scores_full_size(csa, cfg, samples):
+    w = syn.WORKLOADS[cfg]
+    x = syn.indexer_query(cfg, w.B, 1, device=DEV)
+    kI = syn.indexer_keys(cfg, w.B, w.n_cap, device=DEV, hadamard_rows=w.hadamard_kI)
+    p = csa.csa_default_params(topk=w.topk, bf16_scores=1)
+    idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.full((w.B, 1), w.t, dtype=torch.int32), w.n_cap)
+    for b in samples:
+        check_row_bf16(idx[b, 0], sc[b, 0], x["qI"][b, 0], x["wI"][b, 0], kI[b], w.t, w.topk, "c%d b=%d" % (cfg, b))
+
+
+@pytest.mark.parametrize("period,k,t", [(37, 700, 4 * 20000 - 1), (1, 512, 4 * 20000 - 1), (5, 64, 4 * 1000 - 1),
+                                        (600, 2048, 4 * 80000 - 1)])
+def test_bf16_scores_with_ties_go_to_the_smaller_entries(csa, period, k, t):
+    """Repeated keys: every bf16 score occurs many times, so the tie rule
+    decides most of the selection; the k lowest positions among equal scores
+    win (period 1: exactly 0..k-1)."""
+    n_cap = (t + 1) // 4
+    x = syn.indexer_query(9, 1, 1)
+    kI = periodic_keys(9, n_cap, period)
+    p = csa.csa_default_params(topk=k, bf16_scores=1)
+    idx, sc = run(csa, p, x["qI"], x["wI"], kI, torch.tensor([[t]], dtype=torch.int32), n_cap)
+    check_row_bf16(idx[0, 0], sc[0, 0], x["qI"][0, 0], x["wI"][0, 0], kI[0], t, k, "period %d" % period)
+    V = oracle.visible(t)
+    r = oracle.bf16_to_f64(oracle.f64_to_bf16_bits(oracle.index_scores(bits(x["qI"][0, 0]), bits(x["wI"][0, 0]),
+                                                                       bits(kI[0])[:V])))
+    want = oracle.topk(r, k)  # ties toward the smaller entry on the bf16 values
+    assert np.array_equal(idx[0, 0], want), "tie order"
+    if period == 1:
+        assert np.array_equal(idx[0, 0], np.arange(k))
