@@ -231,6 +231,7 @@ def run_ours(args, rank, world, local_rank):
         result["hierarchical"] = [hierarchical_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
         result["hca"] = hca_profile(csa, torch, dev)
         result["fp4_cache"] = fp4_profile(csa, torch, dev, x, w)
+        result["bf16_scores"] = [scores_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -510,6 +511,51 @@ def fp4_profile(csa, torch, dev, x, w, sets=4):
     if csa.csa_check_status() != 0:
         raise RuntimeError("device status after the FP4 section")
     del fp4, sels, qs, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def scores_profile(csa, torch, dev, cfg, sets=4):
+    """The indexer + top-k with fp32 and with bf16 scores ([KV 压缩] §7: BF16
+    scores for the selector): stage durations from the call's trace events
+    (indexer kernel, top-k launch) and the whole call, query sets rotated."""
+    import synthetic as syn
+    w = syn.WORKLOADS[cfg]
+    B = w.B
+    kI = syn.indexer_keys(w.config, B, w.n_cap, device=dev, hadamard_rows=w.hadamard_kI)
+    pos = torch.full((B, 1), w.t, dtype=torch.int32, device=dev)
+    qs = [syn.indexer_query(w.config + 4000 + 100 * r, B, 1, device=dev) for r in range(sets)]
+    idx = torch.empty(B, 1, w.topk, dtype=torch.int32, device=dev)
+    res = {"workload": w.name}
+    for name, flag in (("fp32", 0), ("bf16", 1)):
+        p = csa.csa_default_params(topk=w.topk, bf16_scores=flag)
+        ws = csa.workspace(csa.CSA_OP_INDEX_TOPK, p, B, 1, w.n_cap, device=dev)
+
+        def call(i):
+            q = qs[i % sets]
+            csa.csa_index_topk(p, B, 1, pos, q["qI"], q["wI"], kI, w.n_cap, idx, None, ws)
+        for i in range(8):
+            call(i)
+        torch.cuda.synchronize()
+        n = 100
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            call(i)
+        e1.record()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for i in range(n):
+            csa.csa_set_trace_events(evs[i])
+            call(i)
+        csa.csa_set_trace_events(None)
+        torch.cuda.synchronize()
+        st = [sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(n)) / n for s in (1, 2)]
+        res[name] = {"call_ms": e0.elapsed_time(e1) / n, "index_scores_ms": st[0], "topk_ms": st[1]}
+        del ws
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the score-format section")
+    del kI, qs, idx
     torch.cuda.empty_cache()
     return res
 

@@ -180,7 +180,8 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
                           const uint8_t* qI, const uint16_t* wI, const uint8_t* kI, int64_t n_cap,
                           int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes, cudaStream_t st,
                           bool traced = false, bool zeroed = false,
-                          const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr) {
+                          const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr,
+                          bool standalone = false) {
   const int64_t rows = static_cast<int64_t>(B) * Q;
   IndexWs w, wb;
   size_t need = 0;
@@ -206,7 +207,9 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   if (!zeroed && cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
   if (pool && pool->out && cudaMemsetAsync(wsb_blk + wb.hist_off, 0, wb.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
-  if (traced && pool) trace(1, st);  // the hierarchical calls' own trace starts at the indexer
+  // a call of its own (not inside a layer call) traces from its indexer on
+  const bool own = traced && (pool || standalone);
+  if (own) trace(1, st);
 
   csa::IndexArgs ia = {};
   ia.qI = qI;
@@ -266,7 +269,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     tb.score_out = nullptr;
   }
   s = cuda_status(csa::launch_topk(ta, ride_along, st, pool && pool->out ? &tb : nullptr));
-  if (s == CSA_OK && traced && pool) trace(3, st);
+  if (s == CSA_OK && own) trace(3, st);
   return s;
 }
 
@@ -545,7 +548,7 @@ csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(idx_out) || !ok_opt(score_out))
     return CSA_ERR_INVALID_ARG;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, workspace, workspace_bytes,
-                        static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream), g_trace_on, false, nullptr, nullptr, true);
 }
 
 csa_status csa_index_topk_static(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos,

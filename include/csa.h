@@ -472,7 +472,7 @@ csa_status csa_layer_prefill(
  * cudaEvent_t handles passed as void*), every csa_layer_decode and
  * csa_layer_prefill call records events[0] on its stream before its first
  * kernel and events[s] after stage s: 1 compressor, 2 indexer scores, 3 top-k,
- * 4 sparse attention.  csa_index_topk_pool and csa_reindex_topk record
+ * 4 sparse attention.  csa_index_topk, csa_index_topk_pool and csa_reindex_topk record
  * events[1] before their indexer kernel (after clearing their workspace),
  * events[2] after it and events[3] after their top-k launches.  events ==
  * NULL turns tracing off.  The setting is process-wide; set it only while no
