@@ -131,6 +131,9 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
   }
 }
 
+// kFp4: the compressed rows are FP4 entries (a.kv_fp4); a template
+// argument, so that the bf16 kernel carries none of that code.
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a, const int split,
                        const int gsplit) {
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (j < n_swa) return swa_row(j);
     if (j < n_rows) {
       const int64_t e = a.dense ? j - n_swa : sel_s[j - n_swa];
-      if (a.kv_fp4)  // an FP4 entry: its address, read as bytes by the gather
+      if constexpr (kFp4)  // an FP4 entry: its address, read as bytes by the gather
         return reinterpret_cast<const uint16_t*>(a.kv_fp4 + (static_cast<int64_t>(b) * a.n_cap + e) * kFp4Entry);
       return kv_b + e * kDim;
     }
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int j = r_lo + tid; j < r_hi; j += kThreads) {
     const uint16_t* src = row_at(j);
     if (!src) continue;
-    if (a.kv_fp4 && j >= n_swa) {
+    if (kFp4 && j >= n_swa) {
       const uint8_t* e = reinterpret_cast<const uint8_t*>(src);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(e) : "memory");
       asm volatile("prefetch.global.L2 [%0];" ::"l"(e + 128) : "memory");
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_row_l2(src);
     }
   }
-  if (a.kv_fp4) lut[tid] = e2m1_pair_bf16(tid);  // kThreads == 256: one entry per thread
+  if constexpr (kFp4) lut[tid] = e2m1_pair_bf16(tid);  // kThreads == 256: one entry per thread
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- gather 128 rows: thread tid copies 16-byte chunk (tid & 7) of
     //      channel block (tid >> 3) & 7 of rows (tid >> 6) + 4i, so a warp
     //      covers 512 contiguous bytes of a row
-    if (a.kv_fp4) {
+    if constexpr (kFp4) {
       // FP4 rows: 16 threads per row; thread `part` owns channels 32*part ..
       // 32*part+31 (16 code bytes and 2 scales of the entry; 64 bytes =
       // chunks 4*(part&1) .. +3 of channel block part>>1 of the tile), loads
@@ -743,7 +746,7 @@ int max_split(int dev) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_attn_kernel, &cfg) == cudaSuccess && n > 0) break;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_attn_kernel<false>, &cfg) == cudaSuccess && n > 0) break;
     cudaGetLastError();  // a refused size is not an error of the launch
   }
   if (dev >= 0 && dev < kDevices) cached[dev] = split;
@@ -778,7 +781,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = a.kv_fp4 ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int64_t queries = static_cast<int64_t>(a.B) * a.Q;
@@ -796,14 +800,14 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
     if (g > cluster_max) gsplit = static_cast<int>(g);
   }
   if (gsplit > 1) {
-    e = launch_pdl(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,
+    e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,
                    stream, tm_q, a, 1, gsplit);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(queries), kHeads), dim3(kDim / 4), 0, stream, a,
                       gsplit);
   }
   const int split = choose_split(queries, sms, cluster_max);
-  return launch_pdl_cluster(sparse_attn_kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
+  return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
                             kSmemBytes, stream, static_cast<unsigned>(split), tm_q, a, split, 1);
 }
 
