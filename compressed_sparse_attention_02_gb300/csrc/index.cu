@@ -60,6 +60,11 @@ static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool bloc
 #define CSA_INDEX_DECODE_CTAS_PER_SM 2
 #endif
 
+// Kernel variants (template bits): the Reindex layer's pool gathers, the
+// Full layer's block maxima, bf16 score stores.  Each launch runs the one
+// variant it needs, so the decode kernel carries none of the others.
+constexpr int kModePool = 1, kModeBlocks = 2, kModeBf16 = 4;
+
 template <int QPC>
 struct IndexCfg {
   static constexpr int N = kIdxHeads * QPC;
@@ -116,8 +121,9 @@ __device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, int64_t g, i
 }
 
 // A score into the row array: fp32, or its bf16 bits (already rounded).
+template <bool kBf16>
 __device__ __forceinline__ void store_score(const IndexArgs& a, int64_t at, float v) {
-  if (a.bf16_scores)
+  if constexpr (kBf16)
     reinterpret_cast<uint16_t*>(a.scores)[at] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
   else
     a.scores[at] = v;
@@ -139,7 +145,7 @@ __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const Group
   return past;
 }
 
-template <int QPC>
+template <int QPC, int kMode>
 __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PER_SM)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
@@ -197,7 +203,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && a.pool && QPC == 1) {
+  constexpr bool kPool = (kMode & kModePool) != 0, kBlocks = (kMode & kModeBlocks) != 0,
+                 kBf16 = (kMode & kModeBf16) != 0;
+  static_assert(!kPool || QPC == 1, "a pool belongs to one query");
+  if (kPool && warp == 0) {
     // ---------------- TMA producer, Reindex layer (whole warp) ----------------
     // A tile is 16 pool blocks of 8 keys; lane l < 16 loads slot l's block
     // into its 1 KiB swizzle atom with its own TMA box.  Unit u's block ids
@@ -452,20 +461,20 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
         float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         // bf16 scores: every use below (store, digit counts, block maxima)
         // sees the rounded value
-        if (a.bf16_scores) score = __bfloat162float(__float2bfloat16_rn(score));
+        if constexpr (kBf16) score = __bfloat162float(__float2bfloat16_rn(score));
         const bool in_row = s_idx < gi.vis[j];
         bool valid = in_row;
         const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
-        if (a.pool && in_row) {  // slot s_idx holds entry 8*pool[s_idx/8] + s_idx%8
+        if (kPool && in_row) {  // slot s_idx holds entry 8*pool[s_idx/8] + s_idx%8
           const int32_t blk = __ldg(a.pool + row_off * a.pool_ld + (s_idx >> 3));
           const int64_t nb = (gi.vent[j] + kPoolBlock - 1) / kPoolBlock;
           if (blk >= nb && (row & 7) == 0) record_error(a.status, kErrIndexRange);
           valid = blk >= 0 && static_cast<int64_t>(blk) * kPoolBlock + (row & 7) < gi.vent[j];
-          store_score(a, row_off * a.score_ld + s_idx, valid ? score : -INFINITY);
+          store_score<kBf16>(a, row_off * a.score_ld + s_idx, valid ? score : -INFINITY);
         } else if (valid) {
-          store_score(a, row_off * a.score_ld + s_idx, score);
+          store_score<kBf16>(a, row_off * a.score_ld + s_idx, score);
         }
-        if (a.block_scores) {  // the block's largest score: 8 adjacent lanes
+        if constexpr (kBlocks) {  // the block's largest score: 8 adjacent lanes
           float bm = valid ? score : -INFINITY;
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
@@ -523,12 +532,12 @@ bool encode_maps(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, i
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int QPC>
+template <int QPC, int kMode>
 cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
   using Cfg = IndexCfg<QPC>;
   CUtensorMap tm_k, tm_q;
   if (!encode_maps(a, encode, QPC, &tm_k, &tm_q)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::SMEM));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
@@ -542,7 +551,7 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   // One wave of CTAs that all stay resident; each takes an equal range.
   int64_t ctas = static_cast<int64_t>(sms) * per_sm;
   if (ctas > units) ctas = units;
-  return launch_pdl(index_score_kernel<QPC>, dim3(static_cast<unsigned>(ctas)), dim3(Cfg::THREADS), Cfg::SMEM,
+  return launch_pdl(index_score_kernel<QPC, kMode>, dim3(static_cast<unsigned>(ctas)), dim3(Cfg::THREADS), Cfg::SMEM,
                     stream, tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
 }
 
@@ -553,8 +562,25 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
   if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
   if (a.pool && (a.pool_blocks <= 0 || a.pool_blocks % kPoolTileBlocks != 0 || a.pool_ld != a.pool_blocks))
     return cudaErrorInvalidValue;
-  if (a.Q >= 4 && !a.pool) return launch_qpc<4>(a, encode, stream);  // a pool is per query: one query per tile
-  return launch_qpc<1>(a, encode, stream);
+  const int mode = (a.pool ? kModePool : 0) | (a.block_scores ? kModeBlocks : 0) | (a.bf16_scores ? kModeBf16 : 0);
+  if (a.Q >= 4 && !a.pool) {  // a pool is per query: one query per tile
+    switch (mode) {
+      case 0: return launch_qpc<4, 0>(a, encode, stream);
+      case kModeBlocks: return launch_qpc<4, kModeBlocks>(a, encode, stream);
+      case kModeBf16: return launch_qpc<4, kModeBf16>(a, encode, stream);
+      case kModeBlocks | kModeBf16: return launch_qpc<4, kModeBlocks | kModeBf16>(a, encode, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (mode) {
+    case 0: return launch_qpc<1, 0>(a, encode, stream);
+    case kModePool: return launch_qpc<1, kModePool>(a, encode, stream);
+    case kModeBlocks: return launch_qpc<1, kModeBlocks>(a, encode, stream);
+    case kModeBf16: return launch_qpc<1, kModeBf16>(a, encode, stream);
+    case kModePool | kModeBf16: return launch_qpc<1, kModePool | kModeBf16>(a, encode, stream);
+    case kModeBlocks | kModeBf16: return launch_qpc<1, kModeBlocks | kModeBf16>(a, encode, stream);
+    default: return cudaErrorInvalidValue;  // a pool with block outputs is not a call of this library
+  }
 }
 
 }  // namespace csa
