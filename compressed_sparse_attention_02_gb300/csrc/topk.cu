@@ -317,8 +317,48 @@ __device__ __forceinline__ void for_candidates(bool staged, int nc, const Smem& 
   }
 }
 
+// Reads the staged round of the bitmap out in position order: thread t takes
+// words W*t .. W*t+W-1, one block scan of their bit counts gives each thread
+// its first output slot, and it writes its positions (the first k of the
+// row) to sm.u.c.sel.  Returns the running count.
+template <int W>
+__device__ __forceinline__ int emit_round(Smem& sm, int64_t w0, int out, int k) {
+  uint32_t wd[W];
+  const uint32_t* src = sm.u.c.bm + W * threadIdx.x;
+  if constexpr (W == 8) {
+    const uint4 lo = reinterpret_cast<const uint4*>(src)[0], hi = reinterpret_cast<const uint4*>(src)[1];
+    wd[0] = lo.x, wd[1] = lo.y, wd[2] = lo.z, wd[3] = lo.w;
+    wd[4] = hi.x, wd[5] = hi.y, wd[6] = hi.z, wd[7] = hi.w;
+  } else if constexpr (W == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    wd[0] = v.x, wd[1] = v.y, wd[2] = v.z, wd[3] = v.w;
+  } else if constexpr (W == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    wd[0] = v.x, wd[1] = v.y;
+  } else {
+    wd[0] = *src;
+  }
+  int cnt = 0;
+#pragma unroll
+  for (int e = 0; e < W; ++e) cnt += __popc(wd[e]);
+  int total;
+  int slot = out + block_prefix(cnt, sm, &total);
+  const int64_t wb = w0 + W * threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < W; ++e) {
+    uint32_t word = wd[e];
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      word &= word - 1;
+      if (slot < k) sm.u.c.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
+      ++slot;
+    }
+  }
+  return out + total;
+}
+
 // The finish of one row, run by the last of its CTAs.
-__device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
+__device__ __forceinline__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
                            Smem& sm) {
   const uint32_t* bits = a.bits + row * a.bits_ld;
   uint32_t* ties = a.ties + row * a.bits_ld;
@@ -358,10 +398,11 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
       const int32_t* gpos = a.cand_idx + row * a.cand_cap;
       const bool staged = nc <= kTopkCandCap;  // a longer list is read from global memory in each pass
       if (staged) {
-        for (int i = threadIdx.x; i < nc; i += kThreads) {
+        for (int i = threadIdx.x; i < nc; i += kThreads) {  // both loads in flight at once
           const int32_t p = __ldcg(gpos + i);
+          const uint32_t key = __ldcg(gkey + i);
           const bool ok = p >= 0 && p < V;  // positions come from this row's filter; checked all the same
-          sm.u.c.ckey[i] = ok ? __ldcg(gkey + i) : 0u;
+          sm.u.c.ckey[i] = ok ? key : 0u;
           sm.u.c.cpos[i] = ok ? p : 0;
         }
       }
@@ -456,7 +497,8 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
   // round.  Later rounds (rows longer than 65536 entries) are loaded here and
   // get their selected candidates from the list.
   int out = 0;
-  for (int64_t w0 = 0; w0 < nwords && out < a.k; w0 += kRoundWords) {
+  const int k = a.k;
+  for (int64_t w0 = 0; w0 < nwords && out < k; w0 += kRoundWords) {
     if (w0 > 0) {
       __syncthreads();  // the previous round is read out
       load_round(w0);
@@ -468,26 +510,17 @@ __device__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ve
       }
       __syncthreads();
     }
-    const int64_t wb = w0 + kEmitWords * threadIdx.x;
-    const uint4 lo = reinterpret_cast<const uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x)[0];
-    const uint4 hi = reinterpret_cast<const uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x)[1];
-    const uint32_t wd[kEmitWords] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    int cnt = 0;
-#pragma unroll
-    for (int e = 0; e < kEmitWords; ++e) cnt += __popc(wd[e]);
-    int total;
-    int slot = out + block_prefix(cnt, sm, &total);
-#pragma unroll
-    for (int e = 0; e < kEmitWords; ++e) {
-      uint32_t word = wd[e];
-      while (word) {
-        const int bit = __ffs(word) - 1;
-        word &= word - 1;
-        if (slot < a.k) sm.u.c.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
-        ++slot;
-      }
-    }
-    out += total;
+    // a row that fits one round spreads its words over all the threads
+    // (fewer set bits to walk per thread); longer rows take 8 words each
+    const int64_t left = nwords - w0;
+    if (left <= kThreads)
+      out = emit_round<1>(sm, w0, out, k);
+    else if (left <= 2 * kThreads)
+      out = emit_round<2>(sm, w0, out, k);
+    else if (left <= 4 * kThreads)
+      out = emit_round<4>(sm, w0, out, k);
+    else
+      out = emit_round<kEmitWords>(sm, w0, out, k);
   }
   __syncthreads();
   int32_t* idx = a.idx_out + row * a.k;
@@ -524,7 +557,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     return;
   }
   const bool second = static_cast<int>(blockIdx.z) >= a0.B;
-  const TopkArgs& a = second ? a1 : a0;
+  // a local copy: the compiler keeps the fields it needs in registers (a
+  // reference into the parameter space may alias shared memory, and every
+  // shared store would force the fields to be read again)
+  const TopkArgs a = second ? a1 : a0;
   const int b = static_cast<int>(blockIdx.z) - (second ? a0.B : 0), q = blockIdx.y;
   if (q >= a.Q) return;
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
