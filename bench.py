@@ -604,12 +604,34 @@ def hca_profile(csa, torch, dev, m=128):
         rows = 128 + n_cap
         flops = B * 4.0 * 64 * 512 * rows
         byts = B * (rows * 1024 + 2 * 64 * 1024)
-        res["attention"].append({"workload": name, "batch": B, "entries": n_cap, "rows_per_query": rows, "ms": ms,
-                                 "queries_per_s": B / (ms * 1e-3), "gbs": byts / (ms * 1e-3) / 1e9,
-                                 "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm,
-                                 "tflops": flops / (ms * 1e-3) / 1e12,
-                                 "binding_roofline_frac": max(byts / (hbm * 1e9), flops / (bf16 * 1e12)) / (ms * 1e-3)})
-        del kv, swa, qs, out, wsa
+        entry = {"workload": name, "batch": B, "entries": n_cap, "rows_per_query": rows, "ms": ms,
+                 "queries_per_s": B / (ms * 1e-3), "gbs": byts / (ms * 1e-3) / 1e9,
+                 "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm, "tflops": flops / (ms * 1e-3) / 1e12,
+                 "binding_roofline_frac": max(byts / (hbm * 1e9), flops / (bf16 * 1e12)) / (ms * 1e-3)}
+        # the whole HCA decode step (csa_hca_layer_decode): the compressor
+        # state update (this position closes a block, so the entry is
+        # written every step) and the dense attention
+        x1 = syn.single_stream_inputs(102, B, 1, m, True, device=dev)
+        state = torch.zeros(B, 3, 512, dtype=torch.float32, device=dev)
+        wsl = csa.workspace(csa.CSA_OP_HCA_LAYER_DECODE, p, B, 1, n_cap, device=dev)
+        C1, Z1 = x1["C"][:, 0].contiguous(), x1["Z"][:, 0].contiguous()
+
+        def layer(i):
+            csa.csa_hca_layer_decode(p, B, pos, C1, Z1, x1["B"], x1["rms_w"], state, kv, n_cap, qs[i % 4], swa, sink,
+                                     out, None, wsl)
+        for i in range(8):
+            layer(i)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(n):
+            layer(i)
+        e1.record()
+        torch.cuda.synchronize()
+        lms = e0.elapsed_time(e1) / n
+        entry["layer_step_ms"] = lms
+        entry["layer_queries_per_s"] = B / (lms * 1e-3)
+        res["attention"].append(entry)
+        del kv, swa, qs, out, wsa, wsl, state
     # the compressor over a 16384-token chunk of 8 sequences: 128 entries each
     B, T = 8, 16384
     x = syn.single_stream_inputs(101, B, T, m, True, device=dev)

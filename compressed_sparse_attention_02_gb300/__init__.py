@@ -33,7 +33,7 @@ CSA_OK = 0
 STATUS_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA",
                 4: "CSA_ERR_TIMEOUT", 5: "CSA_ERR_INDEX_RANGE", 6: "CSA_ERR_WORKSPACE"}
 (CSA_OP_COMPRESS, CSA_OP_INDEX_TOPK, CSA_OP_SPARSE_ATTN, CSA_OP_LAYER_DECODE, CSA_OP_LAYER_PREFILL,
- CSA_OP_INDEX_TOPK_POOL, CSA_OP_REINDEX_TOPK) = range(7)
+ CSA_OP_INDEX_TOPK_POOL, CSA_OP_REINDEX_TOPK, CSA_OP_HCA_LAYER_DECODE) = range(8)
 CSA_POOL_BLOCK = 8
 CSA_FP4_ENTRY_BYTES = 288
 
@@ -71,6 +71,8 @@ _lib.csa_compress_single.argtypes = [_P, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _
 _lib.csa_compress_single.restype = ctypes.c_int
 _lib.csa_compress_single_step.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp]
 _lib.csa_compress_single_step.restype = ctypes.c_int
+_lib.csa_hca_layer_decode.argtypes = [_P, _i32] + [_vp] * 6 + [_vp, _i64] + [_vp] * 5 + [_vp, _sz, _vp]
+_lib.csa_hca_layer_decode.restype = ctypes.c_int
 _lib.csa_quantize_kv_fp4.argtypes = [_i64, _vp, _i64, _vp, _i64, _vp]
 _lib.csa_quantize_kv_fp4.restype = ctypes.c_int
 _lib.csa_index_topk_pool.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]
@@ -164,6 +166,14 @@ def csa_index_topk(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, w
     _check(_lib.csa_index_topk(ctypes.byref(params), B, Q, _ptr(q_pos), _ptr(qI), _ptr(wI), _ptr(kI), n_cap,
                                _ptr(idx_out), _ptr(score_out), _ptr(ws), 0 if ws is None else ws.numel(),
                                _stream(stream)), "csa_index_topk")
+
+
+def csa_hca_layer_decode(params, B, q_pos, C, Z, bias, rms_w, state, kv_comp, n_cap, q, swa_ring, sink, out, lse,
+                         ws, stream=None):
+    _check(_lib.csa_hca_layer_decode(ctypes.byref(params), B, _ptr(q_pos), _ptr(C), _ptr(Z), _ptr(bias), _ptr(rms_w),
+                                     _ptr(state), _ptr(kv_comp), n_cap, _ptr(q), _ptr(swa_ring), _ptr(sink), _ptr(out),
+                                     _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "csa_hca_layer_decode")
 
 
 def csa_quantize_kv_fp4(n_rows, inp, in_stride, out, out_stride, stream=None):

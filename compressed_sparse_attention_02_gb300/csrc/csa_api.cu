@@ -425,6 +425,10 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
       return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w)
                  ? round_up(w.total, 256) + csa::attn_split_bytes(B)
                  : 0;
+    case CSA_OP_HCA_LAYER_DECODE: {  // the attention's split-KV partials (B <= 16)
+      const size_t a = csa::attn_split_bytes(B);
+      return a > 16 ? a : 16;
+    }
     case CSA_OP_INDEX_TOPK_POOL: {
       IndexWs wb;
       size_t total = 0;
@@ -743,6 +747,38 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   s = run_attn(p, B, Q, nullptr, pos0, q, kv_comp, n_cap, idx_out, swa, 1, static_cast<int64_t>(p->swa_window) - 1 + Q,
                nullptr, pos0 - (p->swa_window - 1), sink, out, lse, st, false,
                static_cast<uint8_t*>(workspace) + attn_off, workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
+  trace(4, st);
+  return s;
+}
+
+csa_status csa_hca_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* C,
+                                const uint16_t* Z, const uint16_t* bias, const uint16_t* rms_w, float* state,
+                                uint16_t* kv_comp, int64_t n_cap, const uint16_t* q, const uint16_t* swa_ring,
+                                const float* sink, uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
+  if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
+  if (B == 0) return CSA_OK;
+  if (!ok_ptr(q_pos) || !ok_ptr(C) || !ok_ptr(Z) || !ok_opt(bias) || !ok_ptr(rms_w) || !ok_ptr(state) ||
+      !ok_ptr(kv_comp) || !ok_ptr(q) || !ok_ptr(swa_ring) || !ok_ptr(sink) || !ok_ptr(out) || !ok_opt(lse))
+    return CSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
+  trace(0, st);
+  // 1. the step's token into the compressor state; a completed block's entry into the cache
+  csa::CompressArgs ca = compress_args(p, 1, B, 0, 0, C, Z, nullptr, nullptr, nullptr, nullptr, bias, nullptr, rms_w,
+                                       kv_comp, n_cap * csa::kDim, n_cap, q_pos, status);
+  ca.state = state;
+  if ((s = cuda_status(csa::launch_compress_single(ca, st))) != CSA_OK) return s;
+  trace(1, st);
+  trace(2, st);
+  trace(3, st);
+  // 2. dense attention: the ring window and every visible entry (the new one included)
+  s = run_attn(p, B, 1, q_pos, 0, q, kv_comp, n_cap, nullptr, swa_ring, 0, p->swa_window, nullptr, 0, sink, out, lse,
+               st, true, workspace, workspace_bytes);
   trace(4, st);
   return s;
 }

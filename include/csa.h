@@ -98,7 +98,8 @@ enum {
   CSA_OP_LAYER_DECODE = 3,
   CSA_OP_LAYER_PREFILL = 4,
   CSA_OP_INDEX_TOPK_POOL = 5,
-  CSA_OP_REINDEX_TOPK = 6
+  CSA_OP_REINDEX_TOPK = 6,
+  CSA_OP_HCA_LAYER_DECODE = 7
 };
 
 /* Bytes of workspace the call `op` needs for B sequences of Q queries over a
@@ -466,6 +467,31 @@ csa_status csa_layer_prefill(
     const uint16_t *wI, const uint16_t *q, const uint16_t *swa,
     const float *sink, int32_t *idx_out, uint16_t *out, float *lse,
     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * csa_hca_layer_decode — one decode step of an HCA layer (block size p->m,
+ * 128 in the pages; no indexer) for B sequences ([hca_csa] "HCA：同一个算子，
+ * 关掉重叠"; [CSA2 详解] §9: the layer reads every causally visible entry):
+ *   1. csa_compress_single_step with the step's token rows C, Z: the token
+ *      joins its block's online state, and a token that completes block i
+ *      writes entry i to kv_comp;
+ *   2. csa_sparse_attn with idx = NULL over the ring window swa_ring and the
+ *      entries 0 .. floor((t+1)/m)-1, the one just written included.
+ * Arguments are those of the two calls (kv_comp: [B][n_cap][512] bf16,
+ * kv_stride_b = n_cap*512).  Workspace: csa_workspace_size(
+ * CSA_OP_HCA_LAYER_DECODE, p, B, 1, n_cap) bytes or NULL (see
+ * csa_sparse_attn).  Stage events (csa_set_trace_events): 1 after the
+ * compressor, 4 after the attention (2 and 3 with 1).
+ */
+csa_status csa_hca_layer_decode(const csa_params *p, int32_t B,
+                                const int32_t *q_pos, const uint16_t *C,
+                                const uint16_t *Z, const uint16_t *bias,
+                                const uint16_t *rms_w, float *state,
+                                uint16_t *kv_comp, int64_t n_cap,
+                                const uint16_t *q, const uint16_t *swa_ring,
+                                const float *sink, uint16_t *out, float *lse,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
 
 /*
  * Optional stage tracing, for profiling.  With events != NULL (n_events == 5

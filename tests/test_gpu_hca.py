@@ -190,3 +190,52 @@ def test_split_kv_path_with_inverse_rope_and_sparse_selection(csa, inverse_rope)
                                    bits(x["sink"]), W=128, sm_scale=p.sm_scale, inverse_rope_out=bool(inverse_rope))
         assert_close(out[b, 0].float().cpu().numpy(), o, "split-kv b=%d" % b)
         np.testing.assert_allclose(lse[b, 0].cpu().numpy(), l, rtol=1e-3, atol=1e-3)
+
+
+@pytest.mark.parametrize("m,B,steps,check_every", [(8, 2, 20, 1), (128, 3, 130, 43)])
+def test_hca_layer_decode_steps(csa, m, B, steps, check_every):
+    """csa_hca_layer_decode stepped from a block start over a block boundary:
+    each completed block's entry equals the bulk definition, and every
+    step's output is the oracle's attention over the ring window and all
+    entries visible at that step (the one just completed included)."""
+    cfg = 120 + m
+    i0 = 5                      # entries 0..4 exist before the first step
+    t0 = m * i0                 # the first token of block 5
+    n_cap = i0 + steps // m + 2
+    x = syn.single_stream_inputs(cfg, B, steps, m, True)
+    kv = syn.cache_rows(cfg, B, n_cap)
+    kv[:, i0:] = 0
+    ring = syn.cache_rows(cfg, B, 128, name="swa")
+    sink = syn.normal((64,), 1000 * cfg, "sink", "cpu").float()
+    q = syn.main_query(cfg, B, steps)
+    p = params(csa, m)
+    kvd, ringd, sinkd = kv.to(DEV), ring.to(DEV), sink.to(DEV)
+    C, Z, bias, w = x["C"].to(DEV), x["Z"].to(DEV), x["B"].to(DEV), x["rms_w"].to(DEV)
+    state = torch.empty(B, 3, 512, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_HCA_LAYER_DECODE, p, B, 1, n_cap)
+    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, 1, 64, dtype=torch.float32, device=DEV)
+    kv_host = bits(kv).copy()
+    for s in range(steps):
+        t = t0 + s
+        pos = torch.full((B, 1), t, dtype=torch.int32, device=DEV)
+        csa.csa_hca_layer_decode(p, B, pos, C[:, s].contiguous(), Z[:, s].contiguous(), bias, w, state, kvd, n_cap,
+                                 q[:, s:s + 1].contiguous().to(DEV), ringd, sinkd, out, lse, ws)
+        if (t + 1) % m == 0:  # the oracle's cache gains the block's entry
+            e = (t + 1) // m - 1
+            blk = slice(s + 1 - m, s + 1)
+            for b in range(B):
+                ent = oracle.compress_single_entry(e, bits(x["C"][b, blk]), bits(x["Z"][b, blk]), bits(x["B"]),
+                                                   bits(x["rms_w"]))
+                got = kvd[b, e].float().cpu().numpy()
+                assert_close(got, ent, "entry %d b=%d" % (e, b))
+                kv_host[b, e] = bits(kvd[b, e])  # the attention reads the stored bf16 entry
+        if s % check_every == 0 or s == steps - 1:
+            assert csa.csa_check_status() == 0
+            V = (t + 1) // m
+            for b in range(B):
+                rb = bits(ring[b])
+                o, l = oracle.attend_query(t, bits(q[b, s]), np.arange(V, dtype=np.int32), kv_host[b],
+                                           lambda u: rb[u % 128], bits(sink), W=128, sm_scale=p.sm_scale)
+                assert_close(out[b, 0].float().cpu().numpy(), o, "step t=%d b=%d" % (t, b))
+    assert csa.csa_check_status() == 0
