@@ -508,6 +508,29 @@ def fp4_profile(csa, torch, dev, x, w, sets=4):
         row = 288 if fmt == "fp4" else 1024
         byts = B * (k * row + w.W * 1024 + 2 * 64 * 1024)
         res["attention_" + fmt] = {"ms": ms, "gbs": byts / (ms * 1e-3) / 1e9, "bytes": byts}
+    # the whole decode step (csa_layer_decode) over each cache, the same query rotation
+    for fmt, cache in (("bf16", kv.clone()), ("fp4", fp4)):
+        p = csa.csa_default_params(topk=k, kv_format=1 if fmt == "fp4" else 0)
+        idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+        ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, n_cap, device=dev)
+        qi = [syn_indexer_query(w, B, r, dev) for r in range(sets)]
+
+        def step(i):
+            qq = qi[i % sets]
+            csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"],
+                                 x["Bb"], x["rms_w"], cache, n_cap, x["kI"], qq["qI"], qq["wI"], qs[i % sets],
+                                 x["swa"], x["sink"], idx, out.view(B, 64, 512), None, ws)
+        for i in range(8):
+            step(i)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(200):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        res["layer_step_ms_" + fmt] = e0.elapsed_time(e1) / 200
+        del ws, qi
+    res["cache_bytes_per_entry"] = {"bf16": 1024, "fp4": 288}
     if csa.csa_check_status() != 0:
         raise RuntimeError("device status after the FP4 section")
     del fp4, sels, qs, out
@@ -558,6 +581,11 @@ def scores_profile(csa, torch, dev, cfg, sets=4):
     del kI, qs, idx
     torch.cuda.empty_cache()
     return res
+
+
+def syn_indexer_query(w, B, r, dev):
+    import synthetic as syn
+    return syn.indexer_query(w.config + 5000 + 1000 * r, B, 1, device=dev)
 
 
 def syn_main_query(w, B, r, dev):

@@ -16,6 +16,7 @@
 
 #include <cuda_bf16.h>
 
+#include "fp4.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -234,15 +235,43 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
   return true;
 }
 
-// Entry of the main compressor (width 512), stored as bf16 into kv_out.
+// Entry of the main compressor (width 512), stored as bf16 into kv_out, or
+// (kv_fp4_out set) as the FP4 entry of its bf16 values: a 16-channel group
+// is 16/CPT adjacent threads, whose maximum is taken by shuffles.
 template <int M, int CPT, class Sync>
 __device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync) {
   using V = Bf16Vec<CPT>;
   float y[CPT];
   int64_t i;
   if (!compress_values<M, CPT, kDim>(a, b, e, t, red, sync, y, &i)) return;
-  *reinterpret_cast<typename V::T*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + t * CPT) =
-      V::pack(y);
+  if (!a.kv_fp4_out) {
+    *reinterpret_cast<typename V::T*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + t * CPT) =
+        V::pack(y);
+    return;
+  }
+  static_assert(CPT >= 2 && 16 % CPT == 0, "a group of 16 channels spans whole threads");
+  constexpr int kGroupThreads = 16 / CPT;
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    y[j] = __bfloat162float(__float2bfloat16_rn(y[j]));  // the entry's bf16 values are what is quantised
+    amax = fmaxf(amax, fabsf(y[j]));
+  }
+#pragma unroll
+  for (int off = 1; off < kGroupThreads; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  float s;
+  const uint8_t sc = fp4_scale_code(amax, &s);
+  uint8_t* dst = a.kv_fp4_out + static_cast<int64_t>(b) * a.fp4_stride_b + i * kFp4Entry;
+  uint32_t codes = 0u;
+#pragma unroll
+  for (int j = 0; j < CPT / 2; ++j) codes |= fp4_pair_code(y[2 * j], y[2 * j + 1], s) << (8 * j);
+  if constexpr (CPT == 8)
+    *reinterpret_cast<uint32_t*>(dst + 4 * t) = codes;
+  else if constexpr (CPT == 4)
+    *reinterpret_cast<uint16_t*>(dst + 2 * t) = static_cast<uint16_t>(codes);
+  else
+    dst[t] = static_cast<uint8_t>(codes);
+  if (t % kGroupThreads == 0) dst[kDim / 2 + t * CPT / 16] = sc;
 }
 
 // theta^(-2j/R) for the 32 rotated pairs, in fp64 on the host.

@@ -354,11 +354,14 @@ csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new,
                         const uint16_t* Ca, const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
                         const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
                         const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
-                        int64_t n_cap, const int32_t* q_pos, cudaStream_t st) {
+                        int64_t n_cap, const int32_t* q_pos, cudaStream_t st, uint8_t* fp4_out = nullptr,
+                        int64_t fp4_stride_b = 0) {
   unsigned* status = status_ptr();
   if (!status) return CSA_ERR_CUDA;
-  const csa::CompressArgs ca = compress_args(p, mode, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb,
-                                             rms_w, kv_out, kv_stride_b, n_cap, q_pos, status);
+  csa::CompressArgs ca = compress_args(p, mode, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w,
+                                       kv_out, kv_stride_b, n_cap, q_pos, status);
+  ca.kv_fp4_out = fp4_out;
+  ca.fp4_stride_b = fp4_stride_b;
   return cuda_status(csa::launch_compress(ca, st));
 }
 
@@ -637,13 +640,12 @@ csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int3
 
 csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
                             const uint16_t* ring_Za, const uint16_t* ring_Cb, const uint16_t* ring_Zb,
-                            const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_comp,
+                            const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp,
                             int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
                             const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
                             uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
-  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || B > 65535 || !n_cap_ok(n_cap)) return CSA_ERR_INVALID_ARG;
   if (B == 0) return CSA_OK;
@@ -665,8 +667,14 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   // 1. emission of the entry that completes at this step (if any).  Only the
   //    attention reads it, so it is computed by extra CTAs of the top-k launch
   //    where that kernel can carry it, else by its own kernel first.
-  const csa::CompressArgs ca = compress_args(p, 1, B, 1, 0, ring_Ca, ring_Za, ring_Cb, ring_Zb, nullptr, nullptr, Ba,
-                                             Bb, rms_w, kv_comp, n_cap * csa::kDim, n_cap, q_pos, status);
+  // the cache holds bf16 rows or FP4 entries (p->kv_format); the compressor writes the same
+  uint16_t* kv16 = p->kv_format ? nullptr : static_cast<uint16_t*>(kv_comp);
+  csa::CompressArgs ca = compress_args(p, 1, B, 1, 0, ring_Ca, ring_Za, ring_Cb, ring_Zb, nullptr, nullptr, Ba, Bb,
+                                       rms_w, kv16, n_cap * csa::kDim, n_cap, q_pos, status);
+  if (p->kv_format) {
+    ca.kv_fp4_out = static_cast<uint8_t*>(kv_comp);
+    ca.fp4_stride_b = n_cap * csa::kFp4Entry;
+  }
   const bool ride_along = csa::topk_can_carry_compress(p->m);
   trace(0, st);
   if (!ride_along && (s = cuda_status(csa::launch_compress(ca, st))) != CSA_OK) return s;
@@ -688,13 +696,12 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
 csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
                              const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb, const uint16_t* Cb_prev,
                              const uint16_t* Zb_prev, const uint16_t* Ba, const uint16_t* Bb,
-                             const uint16_t* rms_w, uint16_t* kv_comp, int64_t n_cap, const uint8_t* kI,
+                             const uint16_t* rms_w, void* kv_comp, int64_t n_cap, const uint8_t* kI,
                              const uint8_t* qI, const uint16_t* wI, const uint16_t* q, const uint16_t* swa,
                              const float* sink, int32_t* idx_out, uint16_t* out, float* lse, void* workspace,
                              size_t workspace_bytes, void* stream) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
-  if ((s = check_bf16_cache(p)) != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || pos0 < 0 || pos0 % p->m != 0 || !n_cap_ok(n_cap))
     return CSA_ERR_INVALID_ARG;
@@ -716,6 +723,8 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
   trace(0, st);
+  uint16_t* kv16 = p->kv_format ? nullptr : static_cast<uint16_t*>(kv_comp);
+  uint8_t* kv8 = p->kv_format ? static_cast<uint8_t*>(kv_comp) : nullptr;
   // 1. compress the chunk's complete blocks.  Rows are [B][Q][D]; the
   //    compressor reads m*n_new of them per sequence with a stride of Q rows.
   if (n_new > 0) {
@@ -726,13 +735,14 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
         const int64_t poff = static_cast<int64_t>(b) * p->m * csa::kDim;
         s = run_compress(p, 0, 1, n_new, entry0, Ca + off, Za + off, Cb + off, Zb + off,
                          Cb_prev ? Cb_prev + poff : nullptr, Zb_prev ? Zb_prev + poff : nullptr, Ba, Bb, rms_w,
-                         kv_comp + static_cast<int64_t>(b) * n_cap * csa::kDim, n_cap * csa::kDim, n_cap, nullptr,
-                         st);
+                         kv16 ? kv16 + static_cast<int64_t>(b) * n_cap * csa::kDim : nullptr, n_cap * csa::kDim, n_cap,
+                         nullptr, st, kv8 ? kv8 + static_cast<int64_t>(b) * n_cap * csa::kFp4Entry : nullptr,
+                         n_cap * csa::kFp4Entry);
         if (s != CSA_OK) return s;
       }
     } else {
-      s = run_compress(p, 0, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp,
-                       n_cap * csa::kDim, n_cap, nullptr, st);
+      s = run_compress(p, 0, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv16,
+                       n_cap * csa::kDim, n_cap, nullptr, st, kv8, n_cap * csa::kFp4Entry);
       if (s != CSA_OK) return s;
     }
   }

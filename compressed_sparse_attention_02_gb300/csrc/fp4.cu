@@ -14,6 +14,7 @@
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
+#include "fp4.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -41,18 +42,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) quantize_kv_fp4_kernel(const
     x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
   }
-  const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
-  const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+  float s;
+  const uint8_t sc = fp4_scale_code(amax, &s);
   uint32_t codes[2] = {0u, 0u};
-  if (s != 0.f) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const __nv_fp4x2_storage_t pr =
-          __nv_cvt_float2_to_fp4x2(make_float2(__fdiv_rn(x[2 * j], s), __fdiv_rn(x[2 * j + 1], s)), __NV_E2M1,
-                                   cudaRoundNearest);
-      codes[j >> 2] |= static_cast<uint32_t>(pr) << (8 * (j & 3));
-    }
-  }
+  for (int j = 0; j < 8; ++j) codes[j >> 2] |= fp4_pair_code(x[2 * j], x[2 * j + 1], s) << (8 * (j & 3));
   uint8_t* dst = out + row * out_stride;
   *reinterpret_cast<uint2*>(dst + 8 * g) = make_uint2(codes[0], codes[1]);
   dst[kDim / 2 + g] = sc;

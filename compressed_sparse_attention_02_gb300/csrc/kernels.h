@@ -81,6 +81,8 @@ struct CompressArgs {
   double inv_freq[kRope / 2];  // theta^(-2j/R), filled by launch_compress
   uint8_t* key_out;            // indexer keys (launch_index_keys): E4M3 rows of kIdxDim
   float* state;                // single-stream step: [B][3][kDim] running (max, sum, weighted sum)
+  uint8_t* kv_fp4_out;         // main compressor: entries in the FP4 layout instead of kv_out
+  int64_t fp4_stride_b;        // bytes between sequences of kv_fp4_out
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
 // The non-overlapped (single-stream) compressor, block size a.m (1..128):

@@ -74,8 +74,12 @@ typedef struct {
   int32_t inverse_rope; /* 1: rotate the output's last rope_dim channels back
                            by the query position (see csa_sparse_attn); 0    */
   int32_t kv_format;  /* compressed cache entries: 0 bf16 (512 x 2 B), 1 FP4
-                         (CSA_FP4_ENTRY_BYTES, see csa_quantize_kv_fp4); the
-                         layer calls and the compressors write bf16 only    */
+                         (CSA_FP4_ENTRY_BYTES, see csa_quantize_kv_fp4).
+                         csa_layer_decode / csa_layer_prefill read and
+                         write their kv_comp in this format (the compressor
+                         stores the FP4 entry of its bf16 values);
+                         csa_compress and the single-stream calls write
+                         bf16 only                                       */
   int32_t bf16_scores; /* 1: the indexer rounds each score to bf16 (nearest,
                            ties to even) and the top-k selects on the rounded
                            values, ties to the smaller entry as always;
@@ -432,7 +436,7 @@ csa_status csa_layer_decode(
     const csa_params *p, int32_t B, const int32_t *q_pos,
     const uint16_t *ring_Ca, const uint16_t *ring_Za, const uint16_t *ring_Cb,
     const uint16_t *ring_Zb, const uint16_t *Ba, const uint16_t *Bb,
-    const uint16_t *rms_w, uint16_t *kv_comp, int64_t n_cap,
+    const uint16_t *rms_w, void *kv_comp, int64_t n_cap,
     const uint8_t *kI, const uint8_t *qI, const uint16_t *wI,
     const uint16_t *q, const uint16_t *swa_ring, const float *sink,
     int32_t *idx_out, uint16_t *out, float *lse, void *workspace,
@@ -463,7 +467,7 @@ csa_status csa_layer_prefill(
     const uint16_t *Ca, const uint16_t *Za, const uint16_t *Cb,
     const uint16_t *Zb, const uint16_t *Cb_prev, const uint16_t *Zb_prev,
     const uint16_t *Ba, const uint16_t *Bb, const uint16_t *rms_w,
-    uint16_t *kv_comp, int64_t n_cap, const uint8_t *kI, const uint8_t *qI,
+    void *kv_comp, int64_t n_cap, const uint8_t *kI, const uint8_t *qI,
     const uint16_t *wI, const uint16_t *q, const uint16_t *swa,
     const float *sink, int32_t *idx_out, uint16_t *out, float *lse,
     void *workspace, size_t workspace_bytes, void *stream);

@@ -98,7 +98,7 @@ def test_attention_over_the_fp4_cache(csa, B, split_ws, dense):
         np.testing.assert_allclose(l4[b, 0], l, rtol=1e-3, atol=1e-3)
 
 
-def test_layer_calls_and_compressors_refuse_the_fp4_cache(csa):
+def test_bulk_compressor_refuses_the_fp4_cache(csa):
     p4 = csa.csa_default_params(kv_format=1)
     with pytest.raises(csa.CsaError) as e:
         csa.csa_compress(p4, 1, 1, 0, *([torch.zeros(4, 512, dtype=torch.bfloat16, device=DEV)] * 4), None, None,
@@ -107,3 +107,73 @@ def test_layer_calls_and_compressors_refuse_the_fp4_cache(csa):
                          torch.ones(512, dtype=torch.bfloat16, device=DEV),
                          torch.zeros(1, 512, dtype=torch.bfloat16, device=DEV), 512)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("B", [3, 40])
+def test_layer_decode_on_the_fp4_cache(csa, B):
+    """A decode step on the FP4 cache leaves exactly the FP4 entries of the
+    bf16 step's cache (the emitted entry included), selects the same entries,
+    and outputs exactly the bf16 attention over the dequantized cache."""
+    n_cap, k = 2048, 512
+    t = 4 * n_cap - 1  # the step emits entry n_cap - 1
+    w = syn.Workload("fp4-layer", 96, "decode", B=B, t=t, topk=k, n_cap=n_cap)
+    x = syn.decode_inputs(w, device=DEV)
+    p16 = csa.csa_default_params(topk=k)
+    p4 = csa.csa_default_params(topk=k, kv_format=1)
+    outs = {}
+    for name, p, cache in (("bf16", p16, x["kv"].clone()), ("fp4", p4, quantize(csa, x["kv"].view(-1, 512)))):
+        idx = torch.empty(B, k, dtype=torch.int32, device=DEV)
+        out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(B, 64, dtype=torch.float32, device=DEV)
+        ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, n_cap)
+        csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"],
+                             x["Bb"], x["rms_w"], cache, n_cap, x["kI"], x["qI"], x["wI"], x["q"], x["swa"],
+                             x["sink"], idx, out, lse, ws)
+        assert csa.csa_check_status() == 0
+        outs[name] = (cache, idx, out, lse)
+    kv16, idx16, _, _ = outs["bf16"]
+    kv4, idx4, out4, lse4 = outs["fp4"]
+    assert torch.equal(idx4, idx16)
+    want4 = quantize(csa, kv16.view(-1, 512)).view(B, n_cap, 288)
+    assert torch.equal(kv4.view(B, n_cap, 288), want4), "the FP4 cache after the step"
+    deq = dequantized_bf16(kv4.view(B, n_cap, 288).cpu().numpy()).view(B, n_cap, 512)
+    o16, l16 = run_attn(csa, p16, x["q"].view(B, 1, 64, 512), deq, n_cap, idx4.view(B, 1, k), x["swa"], x["sink"],
+                        [t] * B, csa.workspace(csa.CSA_OP_SPARSE_ATTN, p16, B, 1, n_cap))
+    np.testing.assert_array_equal(out4.view(B, 1, 64, 512).float().cpu().numpy(), o16)
+    np.testing.assert_array_equal(lse4.view(B, 1, 64).cpu().numpy(), l16)
+
+
+def test_layer_prefill_on_the_fp4_cache(csa):
+    """A prefill chunk on the FP4 cache writes exactly the FP4 entries of the
+    bf16 chunk's new entries and leaves the others as they were."""
+    B, Q, pos0, k = 2, 64, 512, 64
+    w = syn.Workload("fp4-prefill", 97, "prefill", B=B, t=pos0 + Q - 1, topk=k, n_cap=(pos0 + Q) // 4 + 8, Q=Q,
+                     pos0=pos0)
+    x = syn.prefill_inputs(w, device=DEV)
+    n_cap = x["n_cap"]
+    p16 = csa.csa_default_params(topk=k)
+    p4 = csa.csa_default_params(topk=k, kv_format=1)
+    res = {}
+    for name, p, cache in (("bf16", p16, x["kv"].clone()), ("fp4", p4, quantize(csa, x["kv"].view(-1, 512)))):
+        idx = torch.empty(B, Q, k, dtype=torch.int32, device=DEV)
+        out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+        ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, n_cap)
+        csa.csa_layer_prefill(p, B, Q, pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"], x["Zb_prev"],
+                              x["Ba"], x["Bb"], x["rms_w"], cache, n_cap, x["kI"], x["qI"], x["wI"], x["q"], x["swa"],
+                              x["sink"], idx, out, None, ws)
+        assert csa.csa_check_status() == 0
+        res[name] = (cache, idx, out)
+    kv16, idx16, out16 = res["bf16"]
+    kv4, idx4, out4 = res["fp4"]
+    assert torch.equal(idx4, idx16)
+    assert torch.equal(kv4.view(B, n_cap, 288), quantize(csa, kv16.view(-1, 512)).view(B, n_cap, 288))
+    # the output is the bf16 attention over the dequantized cache, bit for bit
+    deq = dequantized_bf16(kv4.view(B, n_cap, 288).cpu().numpy()).view(B, n_cap, 512).to(DEV)
+    W = p16.swa_window
+    q_pos = (pos0 + torch.arange(Q, dtype=torch.int32, device=DEV)).view(1, Q).repeat(B, 1).contiguous()
+    swa_pos0 = torch.full((B,), pos0 - (W - 1), dtype=torch.int32, device=DEV)
+    o16 = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    csa.csa_sparse_attn(p16, B, Q, q_pos, x["q"], deq, n_cap, idx4, x["swa"], 1, W - 1 + Q, swa_pos0, x["sink"], o16,
+                        None, csa.workspace(csa.CSA_OP_SPARSE_ATTN, p16, B, Q, n_cap))
+    assert csa.csa_check_status() == 0
+    assert torch.equal(out4, o16)
