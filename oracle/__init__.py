@@ -73,6 +73,14 @@ def _load():
         lib.orc_to_e2m1.argtypes = [ctypes.c_double]
         lib.orc_quantize_kv_fp4.argtypes = [ctypes.c_int, _u16p, _u8p]
         lib.orc_dequantize_kv_fp4.argtypes = [ctypes.c_int, _u8p, _f64p]
+        lib.orc_e8m0_scale.restype = ctypes.c_uint8
+        lib.orc_e8m0_scale.argtypes = [ctypes.c_double]
+        lib.orc_e8m0.restype = ctypes.c_double
+        lib.orc_e8m0.argtypes = [ctypes.c_uint8]
+        lib.orc_quantize_index_fp4.argtypes = [ctypes.c_int, _u16p, _u8p, _u8p]
+        lib.orc_dequantize_index_fp4.argtypes = [ctypes.c_int, _u8p, _u8p, _f64p]
+        lib.orc_index_scores_f64.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f64p, _u16p, _f64p,
+                                             _f64p]
         lib.orc_visible.restype = ctypes.c_int64
         lib.orc_visible.argtypes = [ctypes.c_int64, ctypes.c_int]
         lib.orc_index_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _u8p, _u16p, _u8p, _f64p]
@@ -351,6 +359,70 @@ def dequantize_kv_fp4(entries, D: int = 512) -> np.ndarray:
         _load().orc_dequantize_kv_fp4(D, _ptr(r, _u8p), _ptr(o, _f64p))
         out[i] = o
     return out.reshape(entries.shape[:-1] + (D,))
+
+
+# ---- FP4 indexer keys and queries ([CSA2 详解] §16.2) -----------------------
+# 128 E2M1 values and one E8M0 scale per 32 of them.  Scale rounding (the
+# pages leave it open): the smallest power of two s with 6 * s >= the block's
+# largest magnitude; see orc_e8m0_scale.
+
+def e8m0_scale(amax: float) -> int:
+    """E8M0 byte of a block whose largest magnitude is ``amax``."""
+    return int(_load().orc_e8m0_scale(float(amax)))
+
+
+def e8m0_to_f64(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.orc_e8m0(int(v)) for v in b.ravel()], np.float64).reshape(b.shape)
+
+
+def quantize_index_fp4(rows):
+    """bf16 rows [..., D] -> (codes [..., D/2] u8, scales [..., D/32] u8): per
+    row, channel 2j in the low nibble of code byte j, scale g for channels
+    32g .. 32g+31."""
+    rows = _c(rows, np.uint16)
+    r2 = rows.reshape(-1, rows.shape[-1])
+    D = r2.shape[1]
+    codes = np.empty((r2.shape[0], D // 2), np.uint8)
+    scales = np.empty((r2.shape[0], D // 32), np.uint8)
+    for i in range(r2.shape[0]):
+        r = np.ascontiguousarray(r2[i])
+        c = np.empty(D // 2, np.uint8)
+        s = np.empty(D // 32, np.uint8)
+        _load().orc_quantize_index_fp4(D, _ptr(r, _u16p), _ptr(c, _u8p), _ptr(s, _u8p))
+        codes[i], scales[i] = c, s
+    lead = rows.shape[:-1]
+    return codes.reshape(lead + (D // 2,)), scales.reshape(lead + (D // 32,))
+
+
+def dequantize_index_fp4(codes, scales) -> np.ndarray:
+    """(codes [..., D/2], scales [..., D/32]) -> values [..., D] (doubles)."""
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    D = codes.shape[-1] * 2
+    c2, s2 = codes.reshape(-1, D // 2), scales.reshape(-1, D // 32)
+    out = np.empty((c2.shape[0], D), np.float64)
+    for i in range(c2.shape[0]):
+        c, s = np.ascontiguousarray(c2[i]), np.ascontiguousarray(s2[i])
+        o = np.empty(D, np.float64)
+        _load().orc_dequantize_index_fp4(D, _ptr(c, _u8p), _ptr(s, _u8p), _ptr(o, _f64p))
+        out[i] = o
+    return out.reshape(codes.shape[:-1] + (D,))
+
+
+def index_scores_fp4(q_codes, q_scales, wI, k_codes, k_scales) -> np.ndarray:
+    """The indexer score over FP4 queries and keys: q [H, Dk/2] + [H, Dk/32],
+    wI [H] bf16, k [V, Dk/2] + [V, Dk/32] -> scores [V] (fp64); the products
+    of the decoded values, as index_scores forms them for E4M3."""
+    q = np.ascontiguousarray(dequantize_index_fp4(q_codes, q_scales))
+    k = np.ascontiguousarray(dequantize_index_fp4(k_codes, k_scales)) if len(k_codes) else np.empty((0, q.shape[1]))
+    wI = _c(wI, np.uint16)
+    H, Dk = q.shape
+    V = k.shape[0]
+    out = np.empty(V, np.float64)
+    if V:
+        _load().orc_index_scores_f64(H, Dk, V, _ptr(q, _f64p), _ptr(wI, _u16p), _ptr(k, _f64p), _ptr(out, _f64p))
+    return out
 
 
 def index_key_entry(i, Ca, Za, Cb, Zb, Ba, Bb, w, *, rope_dim=64, theta=1e4, eps=1e-6):

@@ -298,6 +298,49 @@ void orc_dequantize_kv_fp4(int D, const uint8_t *in, double *x) {
   }
 }
 
+/* ---- FP4 indexer keys and queries ([CSA2 详解] §16.2) --------------------
+ * The CSA2 indexer holds its keys (and forms its queries) as 128 FP4 E2M1
+ * values with one 1-byte E8M0 scale per 32 values (68 bytes a key).  The
+ * pages do not say how the power-of-two scale is rounded; the reading here:
+ * the smallest power of two s with 6 * s >= amax (6 is E2M1's largest value),
+ * so every x / s lies within E2M1's range and no code saturates. */
+
+/* E8M0 byte of a block whose largest magnitude is amax: e + 127 for the
+ * smallest e in -127..127 with 6 * 2^e >= amax (a zero block: byte 0). */
+uint8_t orc_e8m0_scale(double amax) {
+  int e = -127;
+  while (e < 127 && 6.0 * ldexp(1.0, e) < amax) ++e;
+  return (uint8_t)(e + 127);
+}
+
+/* Value of an E8M0 byte (255, the format's NaN, is never produced here). */
+double orc_e8m0(uint8_t b) { return ldexp(1.0, (int)b - 127); }
+
+/* One row of D bf16 values: codes[j] holds channel 2j in its low nibble and
+ * 2j+1 in its high nibble; scales[g] is the E8M0 byte of channels
+ * 32g .. 32g+31; a channel's code is the E2M1 code nearest to x / s (ties to
+ * the even code, sign kept; the quotient is exact, s being a power of two). */
+void orc_quantize_index_fp4(int D, const uint16_t *x, uint8_t *codes, uint8_t *scales) {
+  for (int g = 0; g < D / 32; ++g) {
+    double amax = 0.0;
+    for (int c = 32 * g; c < 32 * g + 32; ++c)
+      if (fabs(orc_bf16(x[c])) > amax) amax = fabs(orc_bf16(x[c]));
+    scales[g] = orc_e8m0_scale(amax);
+    const double s = orc_e8m0(scales[g]);
+    for (int c = 32 * g; c < 32 * g + 32; c += 2) {
+      const uint8_t lo = orc_to_e2m1(orc_bf16(x[c]) / s);
+      const uint8_t hi = orc_to_e2m1(orc_bf16(x[c + 1]) / s);
+      codes[c / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+/* The D values such a row stands for: e8m0(scale of the block) * e2m1(code). */
+void orc_dequantize_index_fp4(int D, const uint8_t *codes, const uint8_t *scales, double *x) {
+  for (int c = 0; c < D; ++c)
+    x[c] = orc_e8m0(scales[c / 32]) * orc_e2m1((uint8_t)((codes[c / 2] >> (4 * (c & 1))) & 0xF));
+}
+
 /* ---- visibility ([KV 压缩] §9.8) ---------------------------------------- */
 
 /* Entry s covers tokens up to m*s + m - 1, so the query at position t sees
@@ -326,6 +369,21 @@ void orc_index_scores(int H, int Dk, int64_t V, const uint8_t *q,
   }
   free(kd);
   free(qd);
+}
+
+/* The same score over values already decoded to doubles (the FP4 indexer):
+ *   q : [H][Dk];  w : [H] bf16;  k : [V][Dk]. */
+void orc_index_scores_f64(int H, int Dk, int64_t V, const double *q, const uint16_t *w, const double *k,
+                          double *scores) {
+  for (int64_t s = 0; s < V; ++s) {
+    double total = 0.0;
+    for (int h = 0; h < H; ++h) {
+      double dot = 0.0;
+      for (int c = 0; c < Dk; ++c) dot += q[h * Dk + c] * k[s * Dk + c];
+      total += orc_bf16(w[h]) * (dot > 0.0 ? dot : 0.0);
+    }
+    scores[s] = total;
+  }
 }
 
 /* ---- top-k ---------------------------------------------------------------- */

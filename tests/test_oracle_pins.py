@@ -668,3 +668,84 @@ def test_fp4_entries_on_the_grid_round_trip_and_others_round_to_the_nearest_code
         q = x[16 * g:16 * g + 16] / sc
         best = np.min(np.abs(grid[None, :] - q[:, None]), axis=1)
         assert np.all(np.abs(deq[16 * g:16 * g + 16] / sc - q) <= best + 1e-9)
+
+
+# ---- FP4 indexer keys and queries ------------------------------------------
+
+def test_e8m0_scale_bytes_worked_by_hand():
+    """Smallest 2^e with 6 * 2^e >= amax, byte e + 127: 6 = 6 * 2^0 -> 127;
+    the next bf16 above 6 needs 2^1 -> 128; 1 lies in (6 * 2^-3, 6 * 2^-2] ->
+    125; 0.75 = 6 * 2^-3 -> 124; 3 = 6 * 2^-1 -> 126; 1e38 in
+    (6 * 2^123, 6 * 2^124] -> 251; the largest bf16 (about 3.39e38) in
+    (6 * 2^125, 6 * 2^126] -> 253; zero and anything at or below
+    6 * 2^-127 -> 0 (the format's smallest scale)."""
+    cases = {6.0: 127, 6.0234375: 128, 1.0: 125, 0.75: 124, 3.0: 126, 1e38: 251, 3.3895313892515355e38: 253,
+             0.0: 0, 2.0 ** -133: 0, 6.0 * 2.0 ** -127: 0, 2.0 ** -124: 1}
+    for amax, want in cases.items():
+        assert oracle.e8m0_scale(amax) == want, amax
+    np.testing.assert_array_equal(oracle.e8m0_to_f64(np.array([0, 126, 127, 128, 254], np.uint8)),
+                                  [2.0 ** -127, 0.5, 1.0, 2.0, 2.0 ** 127])
+
+
+def test_fp4_index_row_layout_worked_example():
+    """Block 0 = [2.5, 5, 0.25, 0.75, -2.5, 1.25, 1.75, 3.5, 6, 0 ...] has amax 6,
+    scale byte 127 (s = 1); the codes by hand (ties to the even code):
+    2.5 -> 2 (0x4), 5 -> 4 (0x6), 0.25 -> 0 (0x0), 0.75 -> 1 (0x2),
+    -2.5 -> -2 (0xC), 1.25 -> 1 (0x2), 1.75 -> 2 (0x4), 3.5 -> 4 (0x6), 6 (0x7);
+    byte j = code(2j) | code(2j+1) << 4.  Block 1 = 12 at channel 32: scale
+    2 (byte 128), code 6 (0x7).  Blocks 2, 3 are zero: byte 0, zero codes."""
+    x = np.zeros(128)
+    x[:9] = [2.5, 5.0, 0.25, 0.75, -2.5, 1.25, 1.75, 3.5, 6.0]
+    x[32] = 12.0
+    codes, scales = oracle.quantize_index_fp4(bf16_bits(x))
+    assert codes.shape == (64,) and scales.shape == (4,)
+    assert list(codes[:5]) == [0x64, 0x20, 0x2C, 0x64, 0x07]
+    assert not codes[5:16].any() and codes[16] == 0x07 and not codes[17:].any()
+    assert list(scales) == [127, 128, 0, 0]
+    np.testing.assert_array_equal(oracle.dequantize_index_fp4(codes, scales)[:9],
+                                  [2.0, 4.0, 0.0, 1.0, -2.0, 1.0, 2.0, 4.0, 6.0])
+
+
+def test_fp4_index_rows_on_the_grid_round_trip_and_others_round_to_the_nearest_code():
+    # a block of e2m1 values times 2^k with amax 6 * 2^k or 4 * 2^k has scale 2^k and round-trips
+    for top in (6.0, 4.0):
+        k = RNG.integers(-20, 20, 4)
+        vals = oracle.e2m1_to_f64(RNG.integers(0, 16, 128).astype(np.uint8))
+        vals = np.clip(vals, -top, top)
+        vals[::32] = top
+        x = vals * np.repeat(2.0 ** k, 32)
+        codes, scales = oracle.quantize_index_fp4(bf16_bits(x))
+        np.testing.assert_array_equal(scales, k + 127)
+        np.testing.assert_array_equal(oracle.dequantize_index_fp4(codes, scales), x)
+    # general rows: |x| / s within E2M1's range, each value the nearest grid point of x / s
+    grid = oracle.e2m1_to_f64(np.arange(16))
+    for scale in (1e-3, 1.0, 300.0):
+        x = oracle.bf16_to_f64(rand_bf16(128, scale))
+        codes, scales = oracle.quantize_index_fp4(bf16_bits(x))
+        deq = oracle.dequantize_index_fp4(codes, scales)
+        for g in range(4):
+            s = 2.0 ** (int(scales[g]) - 127)
+            blk = x[32 * g:32 * g + 32]
+            assert 3 * s < np.abs(blk).max() <= 6 * s  # the smallest power of two that fits
+            q = blk / s
+            best = np.min(np.abs(grid[None, :] - q[:, None]), axis=1)
+            assert np.all(np.abs(deq[32 * g:32 * g + 32] / s - q) <= best + 1e-12)
+
+
+def test_fp4_index_scores_equal_the_e4m3_scores_of_the_same_values():
+    """Values e2m1 * 2^k with k in -6..4 are exact in E4M3 too: the FP4 scorer
+    (E8M0 scales per 32 channels, nibble codes) and the E4M3 scorer must give
+    the same scores, block scales differing across a row."""
+    H, V = 8, 40
+    def rows(n):
+        codes = RNG.integers(0, 256, (n, 64)).astype(np.uint8)
+        scales = RNG.integers(121, 132, (n, 4)).astype(np.uint8)
+        return codes, scales
+    qc, qs = rows(H)
+    kc, ks = rows(V)
+    w = rand_bf16(H)
+    fp4 = oracle.index_scores_fp4(qc, qs, w, kc, ks)
+    q8 = e4m3_bits(oracle.dequantize_index_fp4(qc, qs))
+    k8 = e4m3_bits(oracle.dequantize_index_fp4(kc, ks))
+    np.testing.assert_array_equal(fp4, oracle.index_scores(q8, w, k8))
+    assert np.count_nonzero(fp4) > V // 2
