@@ -44,7 +44,7 @@ class CsaParams(ctypes.Structure):
                 ("rope_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("swa_window", ctypes.c_int32), ("rope_theta", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("sm_scale", ctypes.c_float), ("inverse_rope", ctypes.c_int32),
-                ("kv_format", ctypes.c_int32), ("bf16_scores", ctypes.c_int32)]
+                ("kv_format", ctypes.c_int32), ("bf16_scores", ctypes.c_int32), ("index_format", ctypes.c_int32)]
 
 
 class CsaError(RuntimeError):
@@ -75,6 +75,10 @@ _lib.csa_hca_layer_decode.argtypes = [_P, _i32] + [_vp] * 6 + [_vp, _i64] + [_vp
 _lib.csa_hca_layer_decode.restype = ctypes.c_int
 _lib.csa_quantize_kv_fp4.argtypes = [_i64, _vp, _i64, _vp, _i64, _vp]
 _lib.csa_quantize_kv_fp4.restype = ctypes.c_int
+_lib.csa_quantize_index_keys_fp4.argtypes = [_i32, _i32, _i64, _vp, _i64, _vp, _i64, _vp]
+_lib.csa_quantize_index_keys_fp4.restype = ctypes.c_int
+_lib.csa_quantize_index_query_fp4.argtypes = [_i64, _vp, _vp, _vp]
+_lib.csa_quantize_index_query_fp4.restype = ctypes.c_int
 _lib.csa_index_topk_pool.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]
 _lib.csa_index_topk_pool.restype = ctypes.c_int
 _lib.csa_reindex_topk.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _vp, _sz, _vp]
@@ -179,6 +183,26 @@ def csa_hca_layer_decode(params, B, q_pos, C, Z, bias, rms_w, state, kv_comp, n_
 def csa_quantize_kv_fp4(n_rows, inp, in_stride, out, out_stride, stream=None):
     _check(_lib.csa_quantize_kv_fp4(n_rows, _ptr(inp), in_stride, _ptr(out), out_stride, _stream(stream)),
            "csa_quantize_kv_fp4")
+
+
+def csa_quantize_index_keys_fp4(B, n_new, entry0, inp, in_stride_b, kI, n_cap, stream=None):
+    _check(_lib.csa_quantize_index_keys_fp4(B, n_new, entry0, _ptr(inp), in_stride_b, _ptr(kI), n_cap,
+                                            _stream(stream)), "csa_quantize_index_keys_fp4")
+
+
+def csa_quantize_index_query_fp4(n_q, inp, qI, stream=None):
+    _check(_lib.csa_quantize_index_query_fp4(n_q, _ptr(inp), _ptr(qI), _stream(stream)),
+           "csa_quantize_index_query_fp4")
+
+
+def index_keys_fp4_bytes(B: int, n_cap: int) -> int:
+    """Bytes of an FP4 indexer key cache (CSA_FP4_INDEX_KEYS_BYTES)."""
+    return B * (n_cap * 64 + (n_cap + 127) // 128 * 512)
+
+
+def index_query_fp4_bytes(n_q: int) -> int:
+    """Bytes of n_q FP4 indexer query records (CSA_FP4_INDEX_QUERY_BYTES)."""
+    return n_q * 4608
 
 
 def csa_index_topk_pool(params, B, Q, q_pos, qI, wI, kI, n_cap, idx_out, score_out, pool_blocks, pool_out, ws,

@@ -94,6 +94,7 @@ csa_status check_params(const csa_params* p) {
   if (p->inverse_rope != 0 && p->inverse_rope != 1) return CSA_ERR_INVALID_ARG;
   if (p->kv_format != 0 && p->kv_format != 1) return CSA_ERR_UNSUPPORTED;
   if (p->bf16_scores != 0 && p->bf16_scores != 1) return CSA_ERR_INVALID_ARG;
+  if (p->index_format != 0 && p->index_format != 1) return CSA_ERR_UNSUPPORTED;
   return CSA_OK;
 }
 
@@ -183,6 +184,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
                           const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr,
                           bool standalone = false) {
   const int64_t rows = static_cast<int64_t>(B) * Q;
+  if (pool && pool->in && p->index_format != 0) return CSA_ERR_UNSUPPORTED;  // the pool gathers read E4M3 keys
   IndexWs w, wb;
   size_t need = 0;
   bool sized;
@@ -225,6 +227,12 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   ia.score_ld = w.score_ld;
   ia.bf16_scores = p->bf16_scores;
   ia.hist = hist;
+  if (p->index_format == 1) {  // FP4: the scale planes follow the code planes
+    ia.fp4 = 1;
+    ia.kI_sf = kI + static_cast<int64_t>(B) * n_cap * (csa::kIdxDim / 2);
+    ia.kI_sf_ld = (n_cap + 127) / 128 * 512;
+    ia.qI_sf = qI + rows * csa::kIdxHeads * (csa::kIdxDim / 2);
+  }
   if (pool && pool->in) {
     ia.pool = pool->in;
     ia.pool_blocks = pool->blocks;
@@ -406,6 +414,7 @@ void csa_default_params(csa_params* p) {
   p->inverse_rope = 0;
   p->kv_format = 0;
   p->bf16_scores = 0;
+  p->index_format = 0;
 }
 
 size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {
@@ -477,6 +486,7 @@ csa_status csa_compress_indexer_keys(const csa_params* p, int32_t B, int32_t n_n
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
+  if (p->index_format != 0) return CSA_ERR_UNSUPPORTED;  // this compressor writes E4M3 keys
   if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535) return CSA_ERR_INVALID_ARG;
   if (B == 0 || n_new == 0) return CSA_OK;
   if (!ok_ptr(CIa) || !ok_ptr(ZIa) || !ok_ptr(CIb) || !ok_ptr(ZIb) || !ok_ptr(BIa) || !ok_ptr(BIb) ||
@@ -543,6 +553,44 @@ csa_status csa_quantize_kv_fp4(int64_t n_rows, const uint16_t* in, int64_t in_st
     return CSA_ERR_INVALID_ARG;
   return cuda_status(csa::launch_quantize_kv_fp4(n_rows, in, in_stride, out, out_stride,
                                                  static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_quantize_index_keys_fp4(int32_t B, int32_t n_new, int64_t entry0, const uint16_t* in,
+                                       int64_t in_stride_b, uint8_t* kI, int64_t n_cap, void* stream) {
+  if (B < 0 || n_new < 0 || entry0 < 0 || B > 65535 || !n_cap_ok(n_cap) || entry0 + n_new > n_cap)
+    return CSA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return CSA_OK;
+  if (!ok_ptr(in) || !ok_ptr(kI) || in_stride_b % 8 != 0 ||
+      (B > 1 && in_stride_b < static_cast<int64_t>(n_new) * csa::kIdxDim))
+    return CSA_ERR_INVALID_ARG;
+  csa::IndexFp4Rows a = {};
+  a.in = in;
+  a.in_stride_b = in_stride_b;
+  a.B = B;
+  a.n_rows = n_new;
+  a.entry0 = entry0;
+  a.codes = kI;
+  a.codes_stride_b = n_cap * (csa::kIdxDim / 2);
+  a.sf = kI + static_cast<int64_t>(B) * n_cap * (csa::kIdxDim / 2);
+  a.sf_stride_b = (n_cap + 127) / 128 * 512;
+  return cuda_status(csa::launch_quantize_index_fp4(a, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_quantize_index_query_fp4(int64_t n_q, const uint16_t* in, uint8_t* qI, void* stream) {
+  if (n_q < 0 || n_q > (int64_t(1) << 31) - 1) return CSA_ERR_INVALID_ARG;
+  if (n_q == 0) return CSA_OK;
+  if (!ok_ptr(in) || !ok_ptr(qI)) return CSA_ERR_INVALID_ARG;
+  csa::IndexFp4Rows a = {};  // a query is a "sequence" of 64 head rows sharing one atom
+  a.in = in;
+  a.in_stride_b = static_cast<int64_t>(csa::kIdxHeads) * csa::kIdxDim;
+  a.B = static_cast<int>(n_q);
+  a.n_rows = csa::kIdxHeads;
+  a.codes = qI;
+  a.codes_stride_b = csa::kIdxHeads * (csa::kIdxDim / 2);
+  a.sf = qI + n_q * csa::kIdxHeads * (csa::kIdxDim / 2);
+  a.sf_stride_b = 512;
+  a.zero_pad = 1;
+  return cuda_status(csa::launch_quantize_index_fp4(a, static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,

@@ -45,8 +45,7 @@ namespace csa {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr uint32_t kKeyTileBytes = kTileKeys * kIdxDim;   // 16 KiB
-constexpr uint32_t kQBytes = kIdxHeads * kIdxDim;         // 8 KiB per query
+constexpr uint32_t kSfBytes = 512;  // FP4: a key tile's scale atom, a query's scale record
 static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool blocks");
 
 // Shape of the decode (one query per group) configuration.
@@ -59,26 +58,43 @@ static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool bloc
 #ifndef CSA_INDEX_DECODE_CTAS_PER_SM
 #define CSA_INDEX_DECODE_CTAS_PER_SM 2
 #endif
+#ifndef CSA_INDEX_DECODE_STAGES_FP4
+#define CSA_INDEX_DECODE_STAGES_FP4 8
+#endif
 
 // Kernel variants (template bits): the Reindex layer's pool gathers, the
-// Full layer's block maxima, bf16 score stores.  Each launch runs the one
-// variant it needs, so the decode kernel carries none of the others.
-constexpr int kModePool = 1, kModeBlocks = 2, kModeBf16 = 4;
+// Full layer's block maxima, bf16 score stores, FP4 keys and queries.  Each
+// launch runs the one variant it needs, so the decode kernel carries none of
+// the others.
+constexpr int kModePool = 1, kModeBlocks = 2, kModeBf16 = 4, kModeFp4 = 8;
 
-template <int QPC>
+template <int QPC, bool kFp4 = false>
 struct IndexCfg {
   static constexpr int N = kIdxHeads * QPC;
   // Epilogue groups of 4 warps (one per TMEM lane quadrant).  One query per
-  // group: the groups take tiles in turn; four queries: a group per query.
-  static constexpr int GROUPS = QPC == 1 ? CSA_INDEX_DECODE_GROUPS : 4;
+  // group: the groups take tiles in turn; more queries: a group per query.
+  static constexpr int GROUPS = QPC == 1 ? CSA_INDEX_DECODE_GROUPS : QPC;
   static constexpr int EPI_WARPS = 4 * GROUPS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int CTAS_PER_SM = QPC == 1 ? CSA_INDEX_DECODE_CTAS_PER_SM : 1;
-  static constexpr int STAGES = QPC == 1 ? CSA_INDEX_DECODE_STAGES : 8;
+  static constexpr int STAGES =
+      QPC == 1 ? (kFp4 ? CSA_INDEX_DECODE_STAGES_FP4 : CSA_INDEX_DECODE_STAGES) : (kFp4 ? 16 : 8);
   static constexpr int NBUF = QPC == 1 ? (GROUPS < 2 ? 2 : GROUPS) : 2;  // TMEM accumulators; tile n: n % NBUF
-  static constexpr uint32_t TMEM_COLS = NBUF * N <= 32 ? 32 : (NBUF * N <= 64 ? 64 : (NBUF * N <= 128 ? 128 : (NBUF * N <= 256 ? 256 : 512)));
-  static constexpr size_t SMEM = 1024 + 2 * QPC * kQBytes + STAGES * kKeyTileBytes + EPI_WARPS * kIdxHeads * 4 +
-                                 (2 * STAGES + 2 * NBUF + 5) * 8 + 16;
+  // Operand rows: 128 E4M3 bytes, or 64 bytes of E2M1 codes (plus scales).
+  static constexpr uint32_t ROW = kFp4 ? kIdxDim / 2 : kIdxDim;
+  static constexpr uint32_t KEY_TILE = kTileKeys * ROW;  // 16 or 8 KiB
+  static constexpr uint32_t QBYTES = kIdxHeads * ROW;    // 8 or 4 KiB per query
+  static constexpr uint32_t SF = kFp4 ? kSfBytes : 0;
+  // TMEM columns: NBUF accumulators of N; FP4: 4 scale columns per
+  // accumulator (the key tile's atom) and per query of either q^I buffer.
+  static constexpr uint32_t SFA_COL = NBUF * N;
+  static constexpr uint32_t SFB_COL = SFA_COL + 4 * NBUF;
+  static constexpr uint32_t COLS = kFp4 ? SFB_COL + 4 * 2 * QPC : NBUF * N;
+  static_assert(COLS <= 512, "TMEM holds 512 columns");
+  static constexpr uint32_t TMEM_COLS =
+      COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : (COLS <= 256 ? 256 : 512)));
+  static constexpr size_t SMEM = 1024 + 2 * QPC * (QBYTES + SF) + STAGES * (KEY_TILE + SF) +
+                                 EPI_WARPS * kIdxHeads * 4 + (2 * STAGES + 2 * NBUF + 5) * 8 + 16;
 };
 
 // Work split: the flattened (query group, key tile) space is cut into
@@ -149,20 +165,25 @@ template <int QPC, int kMode>
 __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PER_SM)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
-  using Cfg = IndexCfg<QPC>;
+  constexpr bool kPool = (kMode & kModePool) != 0, kBlocks = (kMode & kModeBlocks) != 0,
+                 kBf16 = (kMode & kModeBf16) != 0, kFp4 = (kMode & kModeFp4) != 0;
+  using Cfg = IndexCfg<QPC, kFp4>;
   constexpr int N = Cfg::N;
   constexpr int STAGES = Cfg::STAGES;
+  constexpr uint32_t kKeyTileBytes = Cfg::KEY_TILE, kQBytes = Cfg::QBYTES;
   pdl_launch_dependents();
   pdl_wait();  // before any global access and before TMEM is taken
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = base;                                   // [2][QPC * 8 KiB]
-  uint8_t* k_s = q_s + 2 * QPC * kQBytes;                // [STAGES][16 KiB]
+  uint8_t* q_s = base;                                   // [2][QPC][QBYTES]
+  uint8_t* k_s = q_s + 2 * QPC * kQBytes;                // [STAGES][KEY_TILE]
+  uint8_t* ksf_s = k_s + STAGES * kKeyTileBytes;         // FP4: [STAGES][512] scale atoms
+  uint8_t* qsf_s = ksf_s + STAGES * Cfg::SF;             // FP4: [2][QPC][512] query scale records
   constexpr int NBUF = Cfg::NBUF;
   constexpr int kEpiWarps = Cfg::EPI_WARPS;
   constexpr int kEpiGroups = Cfg::GROUPS;
-  float* w_s = reinterpret_cast<float*>(k_s + STAGES * kKeyTileBytes);  // [epilogue warps][64]
+  float* w_s = reinterpret_cast<float*>(qsf_s + 2 * QPC * Cfg::SF);  // [epilogue warps][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(w_s + kEpiWarps * kIdxHeads);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;   // [NBUF]
@@ -203,9 +224,8 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  constexpr bool kPool = (kMode & kModePool) != 0, kBlocks = (kMode & kModeBlocks) != 0,
-                 kBf16 = (kMode & kModeBf16) != 0;
   static_assert(!kPool || QPC == 1, "a pool belongs to one query");
+  static_assert(!(kPool && kFp4), "the pool gathers read E4M3 keys");
   if (kPool && warp == 0) {
     // ---------------- TMA producer, Reindex layer (whole warp) ----------------
     // A tile is 16 pool blocks of 8 keys; lane l < 16 loads slot l's block
@@ -313,11 +333,16 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
           if (active) {
             qb ^= 1;
             if (q_uses[qb] > 0 && !(ok = mbar_wait(&q_empty[qb], (q_uses[qb] - 1) & 1u, a.status))) break;
-            mbar_arrive_expect_tx(&q_full[qb], QPC * kQBytes);
-            for (int j = 0; j < QPC; ++j)
-              tma_load_2d(q_s + (qb * QPC + j) * kQBytes, &tm_q, 0,
-                          static_cast<int32_t>((static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j) * kIdxHeads),
+            mbar_arrive_expect_tx(&q_full[qb], QPC * (kQBytes + Cfg::SF));
+            for (int j = 0; j < QPC; ++j) {
+              const int64_t r = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
+              tma_load_2d(q_s + (qb * QPC + j) * kQBytes, &tm_q, 0, static_cast<int32_t>(r * kIdxHeads),
                           &q_full[qb]);
+              if constexpr (kFp4) {  // a query past the last one reads the last record (not scored)
+                const int64_t rc = r < static_cast<int64_t>(a.B) * a.Q ? r : static_cast<int64_t>(a.B) * a.Q - 1;
+                bulk_load(qsf_s + (qb * QPC + j) * kSfBytes, a.qI_sf + rc * kSfBytes, kSfBytes, &q_full[qb]);
+              }
+            }
             ++q_uses[qb];
           }
         }
@@ -325,8 +350,11 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
         const int s = it % STAGES;
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
         if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
-        mbar_arrive_expect_tx(&full[s], kKeyTileBytes);
+        mbar_arrive_expect_tx(&full[s], kKeyTileBytes + Cfg::SF);
         tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s], pol);
+        if constexpr (kFp4)
+          bulk_load(ksf_s + s * kSfBytes, a.kI_sf + static_cast<int64_t>(gi.b) * a.kI_sf_ld + tile * kSfBytes, kSfBytes,
+                    &full[s], pol);
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | ((use & 1u) << s);
         ++it;
@@ -341,6 +369,9 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = instr_desc(kTileKeys, N, 0, 0, 0, 0);
+      // FP4: the scale atoms go to TMEM by tcgen05.cp, source described as
+      // 32 contiguous 16-byte lines
+      const auto sf_desc = [](const uint8_t* p) { return smem_desc(smem_u32(p), 128, 128, kSwizzleNone); };
       uint32_t q_uses[2] = {0, 0};
       int64_t seen_g = -1;
       bool active = false;
@@ -362,6 +393,11 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
             qb ^= 1;
             if (!(ok = mbar_wait(&q_full[qb], q_uses[qb] & 1u, a.status))) break;
             ++q_uses[qb];
+            if constexpr (kFp4) {
+              tc_fence_after();
+              for (int j = 0; j < QPC; ++j)
+                tc_cp_32x128b_warpx4(tmem + Cfg::SFB_COL + 4 * (qb * QPC + j), sf_desc(qsf_s + (qb * QPC + j) * kSfBytes));
+            }
           }
         }
         if (!active || tile * kTileKeys >= gi.vmax) continue;
@@ -374,11 +410,28 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
         tc_fence_after();
         const uint32_t kb = smem_u32(k_s + s * kKeyTileBytes);
         const uint32_t qbase = smem_u32(q_s + qb * QPC * kQBytes);
+        if constexpr (kFp4) {
+          // K = 128 as two block-scaled MMAs of 64 (scale bytes 0-1, then
+          // 2-3); one MMA per query, each with its own scale columns
+          const uint32_t sfa = tmem + Cfg::SFA_COL + 4 * x;
+          tc_cp_32x128b_warpx4(sfa, sf_desc(ksf_s + s * kSfBytes));
 #pragma unroll
-        for (int kk = 0; kk < kIdxDim / 32; ++kk) {
-          const uint64_t ad = smem_desc(kb + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(qbase + kk * 32, 16, 1024, kSwizzle128B);
-          mma_f8(tmem + x * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t ad = smem_desc(kb + kk * 32, 16, 512, kSwizzle64B);
+#pragma unroll
+            for (int j = 0; j < QPC; ++j) {
+              const uint64_t bd = smem_desc(qbase + j * kQBytes + kk * 32, 16, 512, kSwizzle64B);
+              mma_mxf4(tmem + x * N + j * kIdxHeads, ad, bd, instr_desc_mxf4(kTileKeys, kIdxHeads, 2 * kk, 2 * kk),
+                       sfa, tmem + Cfg::SFB_COL + 4 * (qb * QPC + j), kk > 0 ? 1u : 0u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kIdxDim / 32; ++kk) {
+            const uint64_t ad = smem_desc(kb + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(qbase + kk * 32, 16, 1024, kSwizzle128B);
+            mma_f8(tmem + x * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(&empty[s]);
         tc_commit(&acc_full[x]);
@@ -508,35 +561,36 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   }
 }
 
-bool encode_maps(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, int qpc, CUtensorMap* tm_k,
+bool encode_maps(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* tm_k,
                  CUtensorMap* tm_q) {
-  // K^I: [B][n_cap][128] bytes, box = 128 keys x 128 bytes of one sequence
-  // (pool mode: one block of 8 keys).
-  cuuint64_t kdim[3] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(a.n_cap),
-                        static_cast<cuuint64_t>(a.B)};
-  cuuint64_t kstride[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(a.n_cap) * kIdxDim};
-  cuuint32_t kbox[3] = {static_cast<cuuint32_t>(kIdxDim), static_cast<cuuint32_t>(a.pool ? kPoolBlock : kTileKeys), 1};
+  // Rows of 128 E4M3 bytes (128-byte swizzle) or of 64 bytes of E2M1 codes
+  // (64-byte swizzle).
+  const cuuint64_t row = a.fp4 ? kIdxDim / 2 : kIdxDim;
+  const CUtensorMapSwizzle swz = a.fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  // K^I: [B][n_cap][row] bytes, box = 128 keys of one sequence (pool mode:
+  // one block of 8 keys).
+  cuuint64_t kdim[3] = {row, static_cast<cuuint64_t>(a.n_cap), static_cast<cuuint64_t>(a.B)};
+  cuuint64_t kstride[2] = {row, static_cast<cuuint64_t>(a.n_cap) * row};
+  cuuint32_t kbox[3] = {static_cast<cuuint32_t>(row), static_cast<cuuint32_t>(a.pool ? kPoolBlock : kTileKeys), 1};
   cuuint32_t ones[3] = {1, 1, 1};
   if (encode(tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kI), kdim, kstride, kbox, ones,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
-  // q^I: [B*Q*64 rows][128 bytes], box = the 64 heads of one query.
-  cuuint64_t qdim[2] = {static_cast<cuuint64_t>(kIdxDim),
-                        static_cast<cuuint64_t>(a.B) * static_cast<cuuint64_t>(a.Q) * kIdxHeads};
-  cuuint64_t qstride[1] = {static_cast<cuuint64_t>(kIdxDim)};
-  cuuint32_t qbox[2] = {static_cast<cuuint32_t>(kIdxDim), static_cast<cuuint32_t>(kIdxHeads)};
-  (void)qpc;
+  // q^I: [B*Q*64 rows][row bytes], box = the 64 heads of one query.
+  cuuint64_t qdim[2] = {row, static_cast<cuuint64_t>(a.B) * static_cast<cuuint64_t>(a.Q) * kIdxHeads};
+  cuuint64_t qstride[1] = {row};
+  cuuint32_t qbox[2] = {static_cast<cuuint32_t>(row), static_cast<cuuint32_t>(kIdxHeads)};
   return encode(tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.qI), qdim, qstride, qbox, ones,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int QPC, int kMode>
 cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
-  using Cfg = IndexCfg<QPC>;
+  using Cfg = IndexCfg<QPC, (kMode & kModeFp4) != 0>;
   CUtensorMap tm_k, tm_q;
-  if (!encode_maps(a, encode, QPC, &tm_k, &tm_q)) return cudaErrorInvalidValue;
+  if (!encode_maps(a, encode, &tm_k, &tm_q)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::SMEM));
   if (e != cudaSuccess) return e;
@@ -563,6 +617,26 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
   if (a.pool && (a.pool_blocks <= 0 || a.pool_blocks % kPoolTileBlocks != 0 || a.pool_ld != a.pool_blocks))
     return cudaErrorInvalidValue;
   const int mode = (a.pool ? kModePool : 0) | (a.block_scores ? kModeBlocks : 0) | (a.bf16_scores ? kModeBf16 : 0);
+  if (a.fp4) {  // FP4 keys and queries: one query per CTA, or three (TMEM holds two accumulators of 3 x 64)
+    if (a.pool || !a.kI_sf || !a.qI_sf) return cudaErrorInvalidValue;
+    constexpr int F = kModeFp4, L = kModeBlocks, H = kModeBf16;
+    if (a.Q >= 3) {
+      switch (mode) {
+        case 0: return launch_qpc<3, F>(a, encode, stream);
+        case L: return launch_qpc<3, F | L>(a, encode, stream);
+        case H: return launch_qpc<3, F | H>(a, encode, stream);
+        case L | H: return launch_qpc<3, F | L | H>(a, encode, stream);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    switch (mode) {
+      case 0: return launch_qpc<1, F>(a, encode, stream);
+      case L: return launch_qpc<1, F | L>(a, encode, stream);
+      case H: return launch_qpc<1, F | H>(a, encode, stream);
+      case L | H: return launch_qpc<1, F | L | H>(a, encode, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (a.Q >= 4 && !a.pool) {  // a pool is per query: one query per tile
     switch (mode) {
       case 0: return launch_qpc<4, 0>(a, encode, stream);

@@ -97,9 +97,17 @@ cudaError_t launch_index_keys(const CompressArgs& a, cudaStream_t stream);
 
 // ---- lightning indexer scores (tcgen05, FP8) -------------------------------------
 struct IndexArgs {
-  const uint8_t* qI;        // [B][Q][64][128]
+  const uint8_t* qI;        // [B][Q][64][128] E4M3; FP4: [B][Q][64][64] E2M1 codes
   const uint16_t* wI;       // [B][Q][64]
-  const uint8_t* kI;        // [B][n_cap][128]
+  const uint8_t* kI;        // [B][n_cap][128] E4M3; FP4: [B][n_cap][64] E2M1 codes
+  // FP4 indexer (CSA2): E8M0 scales of 32 channels.  Keys: per sequence, one
+  // 512-byte atom per 128 entries (entry e at byte 16*(e%32) + 4*((e%128)/32)
+  // + block of atom e/128); queries: one 512-byte record per query (head h at
+  // byte 16*(h%32) + 4*(h/32) + block, bytes 8..15 of each line unused).
+  int fp4;
+  const uint8_t* kI_sf;     // [B][kI_sf_ld]
+  int64_t kI_sf_ld;         // bytes between sequences: 512 * ceil(n_cap / 128)
+  const uint8_t* qI_sf;     // [B*Q][512]
   const int32_t* q_pos;     // [B][Q] or null (then pos_base + q)
   int64_t pos_base;
   int B, Q, m;
@@ -211,6 +219,23 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
 // ---- FP4 cache entries -------------------------------------------------------------
 // bf16 rows of kDim (row r at in + r*in_stride) -> FP4 entries of kFp4Entry
 // bytes (entry r at out + r*out_stride).
+// bf16 rows of 128 (row j of sequence b at in + b*in_stride_b + j*128) ->
+// FP4 indexer rows: codes at codes + b*codes_stride_b + e*64 and E8M0 scales
+// in 512-byte atoms at sf + b*sf_stride_b (e = entry0 + j, layout of
+// IndexArgs::kI_sf); zero_pad: also zero bytes 8..15 of each atom line (the
+// query records, whose 64 rows fill half an atom).
+struct IndexFp4Rows {
+  const uint16_t* in;
+  int64_t in_stride_b;
+  int B, n_rows;
+  int64_t entry0;
+  uint8_t* codes;
+  int64_t codes_stride_b;
+  uint8_t* sf;
+  int64_t sf_stride_b;
+  int zero_pad;
+};
+cudaError_t launch_quantize_index_fp4(const IndexFp4Rows& a, cudaStream_t stream);
 cudaError_t launch_quantize_kv_fp4(int64_t n_rows, const uint16_t* in, int64_t in_stride, uint8_t* out,
                                    int64_t out_stride, cudaStream_t stream);
 

@@ -174,6 +174,25 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// The same with an L2 cache policy.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -232,6 +251,30 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D(tmem) (+)= (A * SFA) x (B * SFB): packed E2M1 operands (K = 64 per
+// instruction), one E8M0 scale per 32 values of a row from TMEM.  Scale
+// layout: row r of A at TMEM lane r, column sfa + r/32; row n of B at column
+// sfb + n/32 and lane n%32 of every lane quadrant; the two bytes of a row's
+// two 32-value blocks are bytes id, id+1 of the 32-bit cell (id from the
+// instruction descriptor, 0 or 2).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 lines of 16 bytes (shared memory, described by s_desc) into TMEM
+// columns taddr .. taddr+3 of lanes l, 32+l, 64+l, 96+l (line l in every lane
+// quadrant): the scale layout mma_mxf4 reads.  Issued by the MMA thread,
+// ordered with its MMAs.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // D(tmem) (+)= A(smem desc) x B(smem desc), 16-bit inputs, fp32 accumulate.
@@ -302,7 +345,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 //  - MN-major: 128-byte lines run along M/N, 8 lines (consecutive K) form an
 //    atom; lbo = distance between 128-byte chunks along M/N, sbo = distance
 //    between 8-line groups along K.
-enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2 };
+enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4 };
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t layout) {
@@ -327,6 +370,19 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t M, uint32_t N, uint32
          | (b_mn << 16)         // B major
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::mxf4 (E2M1 x E2M1, E8M0 scales, fp32
+// accumulation, both operands K-major); sfa_id / sfb_id pick the scale bytes
+// (0: bytes 0-1, 2: bytes 2-3 of each scale cell).
+__host__ __device__ constexpr uint32_t instr_desc_mxf4(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4)          // B scale bytes
+         | (1u << 7)            // A format: E2M1
+         | (1u << 10)           // B format: E2M1
+         | ((N >> 3) << 17)     // N / 8
+         | (1u << 23)           // scale format: E8M0
+         | ((M >> 4) << 24)     // M / 16
+         | (sfa_id << 29);      // A scale bytes
 }
 
 }  // namespace csa

@@ -87,6 +87,11 @@ typedef struct {
                            score traffic ([KV 压缩] §7, "Oracle top-k vs
                            learned top-k": BF16 scores for the selector).
                            0: fp32 scores                                 */
+  int32_t index_format; /* the indexer's keys kI and queries qI: 0 E4M3
+                           codes (kI [B][n_cap][128], qI [B][Q][64][128]);
+                           1 FP4 (E2M1 codes, one E8M0 scale per 32 values,
+                           the layouts of csa_quantize_index_keys_fp4 and
+                           csa_quantize_index_query_fp4)                  */
 } csa_params;
 
 #define CSA_FP4_ENTRY_BYTES 288
@@ -301,6 +306,57 @@ csa_status csa_index_topk_static(const csa_params *p, int32_t B, int32_t Q,
 csa_status csa_quantize_kv_fp4(int64_t n_rows, const uint16_t *in,
                                int64_t in_stride, uint8_t *out,
                                int64_t out_stride, void *stream);
+
+/*
+ * FP4 indexer keys and queries ([CSA2 详解] §16.2 "一份 Indexer K": a key of
+ * 128 FP4 values and one 1-byte E8M0 scale per 32 values, 68 bytes; the
+ * indexer's query is FP4 too, [结构对比] CSA2 figure; [KV 压缩] §7.2 "Oracle
+ * top-k vs learned top-k": the CSA indexer's QK path in FP4).  A block of 32
+ * values with largest magnitude amax gets the scale s = 2^e, e the smallest
+ * integer in -127..127 with 6 * 2^e >= amax (the pages leave the rounding
+ * open; this one keeps every x/s within E2M1's range, so no code saturates);
+ * each value x gets the E2M1 code nearest to x/s (the quotient is exact; ties
+ * to the even code; the sign is kept, so a small negative value gives -0).
+ * The value stands for s * e2m1(code).  Inputs must be finite.
+ *
+ * Key cache of B sequences of n_cap entries (CSA_FP4_INDEX_KEYS_BYTES bytes):
+ *   codes  : entry e of sequence b at kI + (b*n_cap + e)*64; byte j holds
+ *            channel 2j in its low nibble and 2j+1 in its high nibble.
+ *   scales : after all codes, 512 bytes per 128 entries of each sequence:
+ *            the scale of channels 32g..32g+31 of entry e of sequence b at
+ *            kI + B*n_cap*64 + b*512*ceil(n_cap/128) + 512*(e/128)
+ *               + 16*(e%32) + 4*((e%128)/32) + g
+ *            (the order in which the tensor cores read them).
+ * Query records, one per query, n_q = B*Q of them (CSA_FP4_INDEX_QUERY_BYTES):
+ *   codes  : head h of query r at qI + (64*r + h)*64, same nibble order.
+ *   scales : after all codes, 512 bytes per query: block g of head h of
+ *            query r at qI + n_q*4096 + 512*r + 16*(h%32) + 4*(h/32) + g;
+ *            bytes 8..15 of every 16-byte line are zero.
+ */
+#define CSA_FP4_INDEX_KEYS_BYTES(B, n_cap) \
+  ((size_t)(B) * ((size_t)(n_cap) * 64u + (((size_t)(n_cap) + 127u) / 128u) * 512u))
+#define CSA_FP4_INDEX_QUERY_BYTES(n_q) ((size_t)(n_q) * 4608u)
+
+/*
+ * csa_quantize_index_keys_fp4 — bf16 indexer keys into the FP4 key cache.
+ * in : row j (128 bf16) of sequence b at in + b*in_stride_b + j*128 for
+ *      j < n_new (in_stride_b a multiple of 8 and >= n_new*128 when B > 1).
+ * kI : the FP4 key cache (B sequences of n_cap entries, layout above);
+ *      entries entry0 .. entry0+n_new-1 are written (entry0 + n_new <=
+ *      n_cap), all others are left as they are.
+ * Device pointers, 16-byte aligned.  No workspace.
+ */
+csa_status csa_quantize_index_keys_fp4(int32_t B, int32_t n_new,
+                                       int64_t entry0, const uint16_t *in,
+                                       int64_t in_stride_b, uint8_t *kI,
+                                       int64_t n_cap, void *stream);
+
+/*
+ * csa_quantize_index_query_fp4 — bf16 indexer queries [n_q][64][128] (n_q =
+ * B*Q, contiguous) into n_q FP4 query records at qI (layout above).
+ */
+csa_status csa_quantize_index_query_fp4(int64_t n_q, const uint16_t *in,
+                                        uint8_t *qI, void *stream);
 
 /*
  * Hierarchical indexer ([CSA2 详解] §11 "Hierarchical Sparse Indexer"; §11.1

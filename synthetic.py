@@ -143,6 +143,19 @@ def indexer_keys(config: int, B: int, n: int, device="cpu", hadamard_rows: bool 
     return _per_seq(B, config, "kI", (n, DI), device, e4m3)
 
 
+def indexer_query_bf16(config: int, B: int, Q: int, device="cpu") -> dict:
+    """indexer_query's draws as bf16 rows (the FP4 indexer quantizes them)."""
+    return {
+        "qI": _per_seq(B, config, "qI", (Q, HI, DI), device, bf16),
+        "wI": _per_seq(B, config, "wI", (Q, HI), device, lambda x: bf16(x / math.sqrt(DI * HI))),
+    }
+
+
+def indexer_keys_bf16(config: int, B: int, n: int, device="cpu") -> torch.Tensor:
+    """indexer_keys' draws as bf16 rows (the FP4 indexer quantizes them)."""
+    return _per_seq(B, config, "kI", (n, DI), device, bf16)
+
+
 def main_query(config: int, B: int, Q: int, device="cpu") -> torch.Tensor:
     return _per_seq(B, config, "q", (Q, H, D), device, bf16)
 

@@ -56,3 +56,54 @@ def check_topk(got_idx, scores, k, what="top-k"):
 def bits(t):
     import synthetic
     return synthetic.bits(t)
+
+
+# ---- FP4 indexer layouts (include/csa.h, csa_quantize_index_keys_fp4) -------
+# Pure byte placement: codes planes first, then the E8M0 scales in 512-byte
+# atoms (entry e of a key sequence at 16*(e%32) + 4*((e%128)/32) + block of
+# atom e/128; head h of a query record at 16*(h%32) + 4*(h/32) + block).
+
+def pack_index_keys_fp4(codes, scales, n_cap):
+    """codes [B][n][64] u8, scales [B][n][4] u8 (n <= n_cap) -> FP4 key cache
+    bytes; entries n.. are zero."""
+    codes, scales = np.asarray(codes, np.uint8), np.asarray(scales, np.uint8)
+    B, n = codes.shape[:2]
+    A = (n_cap + 127) // 128
+    buf = np.zeros(B * (n_cap * 64 + A * 512), np.uint8)
+    buf[:B * n_cap * 64].reshape(B, n_cap, 64)[:, :n] = codes
+    sp = buf[B * n_cap * 64:].reshape(B, A, 32, 4, 4)
+    e = np.arange(n)
+    for b in range(B):
+        sp[b, e // 128, e % 32, (e % 128) // 32, :] = scales[b]
+    return buf
+
+
+def unpack_index_keys_fp4(buf, B, n_cap):
+    """FP4 key cache bytes -> (codes [B][n_cap][64], scales [B][n_cap][4])."""
+    buf = np.asarray(buf, np.uint8).reshape(-1)
+    A = (n_cap + 127) // 128
+    codes = buf[:B * n_cap * 64].reshape(B, n_cap, 64)
+    sp = buf[B * n_cap * 64:B * (n_cap * 64 + A * 512)].reshape(B, A, 32, 4, 4)
+    e = np.arange(n_cap)
+    return codes, np.stack([sp[b, e // 128, e % 32, (e % 128) // 32, :] for b in range(B)])
+
+
+def pack_index_query_fp4(codes, scales):
+    """codes [n_q][64][64] u8, scales [n_q][64][4] u8 -> FP4 query records."""
+    codes, scales = np.asarray(codes, np.uint8), np.asarray(scales, np.uint8)
+    nq = codes.shape[0]
+    buf = np.zeros(nq * 4608, np.uint8)
+    buf[:nq * 4096] = codes.reshape(-1)
+    sp = buf[nq * 4096:].reshape(nq, 32, 16)
+    sp[:, :, 0:4] = scales[:, :32]
+    sp[:, :, 4:8] = scales[:, 32:]
+    return buf
+
+
+def unpack_index_query_fp4(buf, nq):
+    """FP4 query records -> (codes [n_q][64][64], scales [n_q][64][4], the
+    unused bytes 8..15 of every line [n_q][32][8])."""
+    buf = np.asarray(buf, np.uint8).reshape(-1)
+    codes = buf[:nq * 4096].reshape(nq, 64, 64)
+    sp = buf[nq * 4096:nq * 4608].reshape(nq, 32, 16)
+    return codes, np.concatenate([sp[:, :, 0:4], sp[:, :, 4:8]], axis=1), sp[:, :, 8:]

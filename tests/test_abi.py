@@ -39,7 +39,8 @@ def test_default_params_and_status_strings(lib):
     assert (p.m, p.n_heads, p.head_dim, p.rope_dim, p.idx_heads, p.idx_dim, p.topk, p.swa_window) == \
         (4, 64, 512, 64, 64, 128, 512, 128)
     assert abs(p.sm_scale - 512 ** -0.5) < 1e-7 and p.rope_theta == 1e4
-    assert p.inverse_rope == 0 and p.kv_format == 0 and p.bf16_scores == 0 and ctypes.sizeof(p) == 14 * 4
+    assert p.inverse_rope == 0 and p.kv_format == 0 and p.bf16_scores == 0 and p.index_format == 0
+    assert ctypes.sizeof(p) == 15 * 4
     for s in range(7):
         assert lib.csa_status_string(s).startswith(lib.STATUS_NAMES[s])
 
@@ -148,3 +149,27 @@ def test_block_sizes_and_single_stream_calls_validate(lib):
                                         i64(1), None) == 1
     assert raw.csa_compress_single(ctypes.byref(p128), 0, 1, i64(0), None, None, None, None, None, i64(0),
                                    None) == 0
+
+
+def test_fp4_indexer_argument_checks(lib):
+    """FP4 indexer rows: sizes of the layouts, and host-side refusals (no launch)."""
+    assert lib.index_keys_fp4_bytes(2, 300) == 2 * (300 * 64 + 3 * 512)
+    assert lib.index_query_fp4_bytes(5) == 5 * (64 * 64 + 512)
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    for fn in ("csa_quantize_index_keys_fp4", "csa_quantize_index_query_fp4", "csa_reindex_topk",
+               "csa_compress_indexer_keys"):
+        getattr(raw, fn).restype = ctypes.c_int
+    fake = ctypes.c_void_p(0x10000)
+    i64 = ctypes.c_int64
+    # entries past the cache, a stride that is not a multiple of 8, a null input
+    assert raw.csa_quantize_index_keys_fp4(1, 8, i64(100), fake, i64(1024), fake, i64(104), None) == 1
+    assert raw.csa_quantize_index_keys_fp4(2, 8, i64(0), fake, i64(1028), fake, i64(104), None) == 1
+    assert raw.csa_quantize_index_query_fp4(i64(3), None, fake, None) == 1
+    assert raw.csa_quantize_index_query_fp4(i64(0), None, None, None) == 0  # nothing to do
+    # formats: only 0 and 1; the Reindex gathers and the E4M3 key compressor take no FP4
+    assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, lib.csa_default_params(index_format=2), 1, 1, 1024) == 0
+    p4 = lib.csa_default_params(index_format=1)
+    assert raw.csa_reindex_topk(ctypes.byref(p4), 1, 1, fake, fake, fake, fake, i64(4096), fake, 2048, fake, None,
+                                fake, ctypes.c_size_t(1 << 30), None) == 2
+    assert raw.csa_compress_indexer_keys(ctypes.byref(p4), 1, 4, i64(0), *([fake] * 4), None, None,
+                                         *([fake] * 4), i64(512), None) == 2
