@@ -40,9 +40,10 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
-    ap.add_argument("--section", choices=["decode", "reindex"], default="decode",
+    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index"], default="decode",
                     help="reindex: only the hierarchical indexer's Reindex layer on --workload (4 Full-layer "
-                         "calls make the pools, then --warmup and --steps Reindex calls; for profiling)")
+                         "calls make the pools, then --warmup and --steps Reindex calls; for profiling); "
+                         "fp4_index: only the FP4 indexer section on --workload")
     return ap.parse_args()
 
 
@@ -232,6 +233,9 @@ def run_ours(args, rank, world, local_rank):
         result["hca"] = hca_profile(csa, torch, dev)
         result["fp4_cache"] = fp4_profile(csa, torch, dev, x, w)
         result["bf16_scores"] = [scores_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
+        result["fp4_index"] = [index_fp4_profile(csa, torch, dev, cfg,
+                                                 x=x if cfg == args.workload and B == w.B else None)
+                               for cfg in (2, 3)]
         result["e2e"] = end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args)
         result["cpu_baseline"] = cpu_baseline(w, x, seconds=12.0)
     return result
@@ -579,6 +583,103 @@ def scores_profile(csa, torch, dev, cfg, sets=4):
     if csa.csa_check_status() != 0:
         raise RuntimeError("device status after the score-format section")
     del kI, qs, idx
+    torch.cuda.empty_cache()
+    return res
+
+
+def _ms_per_call(torch, fn, n, warm=8):
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def _index_stages(csa, torch, fn, n):
+    """Mean indexer-kernel and top-k durations of n calls, from the calls'
+    trace events (csa_set_trace_events: events 1-2 bracket the indexer, 2-3
+    the top-k)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    for i in range(n):
+        csa.csa_set_trace_events(evs[i])
+        fn(i)
+    csa.csa_set_trace_events(None)
+    torch.cuda.synchronize()
+    return [sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(n)) / n for s in (1, 2)]
+
+
+def index_fp4_profile(csa, torch, dev, cfg, x=None, sets=4, n=100):
+    """The FP4 indexer ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §16.2:
+    68-byte keys, E2M1 with an E8M0 scale per 32 values; "DeepSeek-V4 的 KV
+    压缩" §7.2: FP4 QK path and BF16 scores for the selector) beside the E4M3
+    indexer on the same workload: the key quantizer, the indexer kernel and
+    the top-k from the calls' trace events, the indexer's algorithmic HBM
+    rate, the whole call, and (given the decode inputs x) the whole decode
+    step with either indexer format.  Query sets rotate."""
+    import synthetic as syn
+    hbm, _, _ = peaks()
+    w = syn.WORKLOADS[cfg]
+    B, n_cap, t, k = w.B, w.n_cap, w.t, w.topk
+    kbf = syn.indexer_keys_bf16(w.config, B, n_cap, device=dev)
+    k4 = torch.empty(csa.index_keys_fp4_bytes(B, n_cap), dtype=torch.uint8, device=dev)
+    qms = _ms_per_call(torch, lambda i: csa.csa_quantize_index_keys_fp4(B, n_cap, 0, kbf, n_cap * 128, k4, n_cap),
+                       10, warm=1)
+    del kbf
+    k8 = syn.indexer_keys(w.config, B, n_cap, device=dev, hadamard_rows=w.hadamard_kI)
+    pos = torch.full((B, 1), t, dtype=torch.int32, device=dev)
+    qsets = []
+    for r in range(sets):
+        qb = syn.indexer_query_bf16(w.config + 4000 + 100 * r, B, 1, device=dev)
+        q4 = torch.empty(csa.index_query_fp4_bytes(B), dtype=torch.uint8, device=dev)
+        csa.csa_quantize_index_query_fp4(B, qb["qI"], q4)
+        qsets.append({"e4m3": qb["qI"].to(torch.float8_e4m3fn), "fp4": q4, "wI": qb["wI"]})
+    idx = torch.empty(B, 1, k, dtype=torch.int32, device=dev)
+    V = min((t + 1) // w.m, n_cap)
+    nbytes = {"e4m3": B * (V * 128 + 64 * 128 + 64 * 2),
+              "fp4": B * (V * 64 + (V + 127) // 128 * 512 + 4608 + 64 * 2)}
+    res = {"workload": w.name, "key_bytes_per_entry": {"e4m3": 128, "fp4": 68},
+           "quantize_keys": {"entries": B * n_cap, "ms": qms,
+                             "gbs": B * n_cap * (256 + 68) / (qms * 1e-3) / 1e9}}
+    for name, fmt, sflag in (("e4m3", "e4m3", 0), ("fp4", "fp4", 0), ("fp4_bf16_scores", "fp4", 1)):
+        p = csa.csa_default_params(topk=k, index_format=1 if fmt == "fp4" else 0, bf16_scores=sflag)
+        ws = csa.workspace(csa.CSA_OP_INDEX_TOPK, p, B, 1, n_cap, device=dev)
+        kI = k4 if fmt == "fp4" else k8
+
+        def call(i):
+            q = qsets[i % sets]
+            csa.csa_index_topk(p, B, 1, pos, q[fmt], q["wI"], kI, n_cap, idx, None, ws)
+        call_ms = _ms_per_call(torch, call, n)
+        st = _index_stages(csa, torch, call, n)
+        gbs = nbytes[fmt] / (st[0] * 1e-3) / 1e9
+        res[name] = {"call_ms": call_ms, "index_scores_ms": st[0], "topk_ms": st[1], "index_bytes": nbytes[fmt],
+                     "index_gbs": gbs, "index_hbm_frac": gbs / hbm}
+        del ws
+    if x is not None:  # the whole decode step (csa_layer_decode) with either indexer format
+        qs = [syn_main_query(w, B, r, dev) for r in range(sets)]
+        out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev)
+        idx2 = torch.empty(B, k, dtype=torch.int32, device=dev)
+        kv = x["kv"].clone()
+        for fmt in ("e4m3", "fp4"):
+            p = csa.csa_default_params(topk=k, index_format=1 if fmt == "fp4" else 0)
+            ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, n_cap, device=dev)
+            kI = k4 if fmt == "fp4" else k8
+
+            def step(i):
+                q = qsets[i % sets]
+                csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"],
+                                     x["Ba"], x["Bb"], x["rms_w"], kv, n_cap, kI, q[fmt], q["wI"], qs[i % sets],
+                                     x["swa"], x["sink"], idx2, out, None, ws)
+            res["layer_step_ms_" + fmt] = _ms_per_call(torch, step, 200)
+            del ws
+        del qs, out, kv
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the FP4 indexer section")
+    del k4, k8, qsets, idx
     torch.cuda.empty_cache()
     return res
 
@@ -939,6 +1040,14 @@ def main():
     if args.section == "reindex":
         if rank == 0:
             print(json.dumps(reindex_section(args)), flush=True)
+        return
+    if args.section == "fp4_index":
+        if rank == 0:
+            import torch
+
+            import compressed_sparse_attention_02_gb300 as csa
+            print(json.dumps(index_fp4_profile(csa, torch, torch.device("cuda", 0), args.workload,
+                                               n=max(args.steps, 1))), flush=True)
         return
     if world > 1:
         import torch

@@ -184,7 +184,6 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
                           const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr,
                           bool standalone = false) {
   const int64_t rows = static_cast<int64_t>(B) * Q;
-  if (pool && pool->in && p->index_format != 0) return CSA_ERR_UNSUPPORTED;  // the pool gathers read E4M3 keys
   IndexWs w, wb;
   size_t need = 0;
   bool sized;

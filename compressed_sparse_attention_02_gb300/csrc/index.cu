@@ -225,7 +225,6 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
   const uint32_t tmem = *tmem_slot;
 
   static_assert(!kPool || QPC == 1, "a pool belongs to one query");
-  static_assert(!(kPool && kFp4), "the pool gathers read E4M3 keys");
   if (kPool && warp == 0) {
     // ---------------- TMA producer, Reindex layer (whole warp) ----------------
     // A tile is 16 pool blocks of 8 keys; lane l < 16 loads slot l's block
@@ -234,12 +233,33 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
     // every lane keeps its slot's ids for the next kAhead units in flight.
     // A slot without a block, or with an id outside the cache, loads block 0,
     // which the epilogue does not score.
+    // FP4: the tile's scale atom is assembled here.  Block blk's 8 scale
+    // words lie on lines 8*(blk%4) .. +7, word (blk%16)/4, of the sequence's
+    // atom blk/16; slot l's go to lines 8*(l%4) .. +7, word l/4 of the
+    // stage's atom.  Lane l loads them kAhead units ahead (its ids are read
+    // 2*kAhead units ahead), stores them when the stage is free and fences
+    // them for the tensor cores before lane 0 arrives on the stage.
     constexpr int kAhead = 4;
+    constexpr int kIdAhead = kFp4 ? 2 * kAhead : kAhead;
     const int64_t n_blk = (a.n_cap + kPoolBlock - 1) / kPoolBlock;
     const int32_t* ids = a.pool + (lane & (kPoolTileBlocks - 1));
-    int32_t ring[kAhead];
+    int32_t ring[kIdAhead];
 #pragma unroll
-    for (int d = 0; d < kAhead; ++d) ring[d] = u0 + d < u1 ? __ldg(ids + kPoolTileBlocks * (u0 + d)) : 0;
+    for (int d = 0; d < kIdAhead; ++d) ring[d] = u0 + d < u1 ? __ldg(ids + kPoolTileBlocks * (u0 + d)) : 0;
+    uint32_t sw[kFp4 ? kAhead : 1][8];
+    const auto load_scales = [&](int64_t up, int32_t id, uint32_t(&w)[8]) {
+      const bool live = lane < kPoolTileBlocks && up < u1;
+      const int32_t blk = (id >= 0 && id < n_blk) ? id : 0;
+      const int64_t bp = live ? up / tiles_per_group / groups_per_seq : 0;
+      const uint8_t* src = a.kI_sf + bp * a.kI_sf_ld + (blk >> 4) * static_cast<int64_t>(kSfBytes) + (blk & 3) * 128 +
+                           ((blk & 15) >> 2) * 4;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = live ? __ldg(reinterpret_cast<const uint32_t*>(src + 16 * k)) : 0u;
+    };
+    if constexpr (kFp4) {
+#pragma unroll
+      for (int d = 0; d < kAhead; ++d) load_scales(u0 + d, ring[d], sw[d]);
+    }
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_q);
@@ -256,8 +276,18 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
     for (int64_t u = u0; u < u1 && ok; ++u) {
       const int32_t id = ring[0];
 #pragma unroll
-      for (int d = 0; d + 1 < kAhead; ++d) ring[d] = ring[d + 1];
-      ring[kAhead - 1] = u + kAhead < u1 ? __ldg(ids + kPoolTileBlocks * (u + kAhead)) : 0;
+      for (int d = 0; d + 1 < kIdAhead; ++d) ring[d] = ring[d + 1];
+      ring[kIdAhead - 1] = u + kIdAhead < u1 ? __ldg(ids + kPoolTileBlocks * (u + kIdAhead)) : 0;
+      uint32_t cur[8];
+      if constexpr (kFp4) {  // this unit's scale words; load those of unit u + kAhead
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cur[k] = sw[0][k];
+#pragma unroll
+        for (int d = 0; d + 1 < kAhead; ++d)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sw[d][k] = sw[d + 1][k];
+        load_scales(u + kAhead, ring[kAhead - 1], sw[kAhead - 1]);
+      }
       if (++tile == tiles_per_group) {
         tile = 0;
         ++g;
@@ -271,9 +301,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
           if (lane == 0) {
             if (q_uses[qb] > 0) ok = mbar_wait(&q_empty[qb], (q_uses[qb] - 1) & 1u, a.status);
             if (ok) {
-              mbar_arrive_expect_tx(&q_full[qb], kQBytes);
-              tma_load_2d(q_s + qb * kQBytes, &tm_q, 0,
-                          static_cast<int32_t>((static_cast<int64_t>(gi.b) * a.Q + gi.q0) * kIdxHeads), &q_full[qb]);
+              const int64_t r = static_cast<int64_t>(gi.b) * a.Q + gi.q0;
+              mbar_arrive_expect_tx(&q_full[qb], kQBytes + Cfg::SF);
+              tma_load_2d(q_s + qb * kQBytes, &tm_q, 0, static_cast<int32_t>(r * kIdxHeads), &q_full[qb]);
+              if constexpr (kFp4) bulk_load(qsf_s + qb * kSfBytes, a.qI_sf + r * kSfBytes, kSfBytes, &q_full[qb]);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -284,15 +315,22 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
       if (!active || tile * kTileKeys >= gi.vmax) continue;
       const int st = it % STAGES;
       const uint32_t use = static_cast<uint32_t>(it / STAGES);
-      if (lane == 0) {
-        if (use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, a.status);
-        if (ok) mbar_arrive_expect_tx(&full[st], kKeyTileBytes);
-      }
+      if (lane == 0 && use > 0) ok = mbar_wait(&empty[st], (use - 1) & 1u, a.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      if constexpr (kFp4) {
+        if (lane < kPoolTileBlocks) {
+          uint8_t* dst = ksf_s + st * kSfBytes + (lane & 3) * 128 + (lane >> 2) * 4;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint32_t*>(dst + 16 * k) = cur[k];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kKeyTileBytes);
       if (lane < kPoolTileBlocks) {
         const int32_t blk = (id >= 0 && id < n_blk) ? id : 0;
-        tma_load_3d(k_s + st * kKeyTileBytes + lane * (kPoolBlock * kIdxDim), &tm_k, 0, blk * kPoolBlock, gi.b,
+        tma_load_3d(k_s + st * kKeyTileBytes + lane * (kPoolBlock * Cfg::ROW), &tm_k, 0, blk * kPoolBlock, gi.b,
                     &full[st], pol);
       }
       issued |= 1u << st;
@@ -618,9 +656,9 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
     return cudaErrorInvalidValue;
   const int mode = (a.pool ? kModePool : 0) | (a.block_scores ? kModeBlocks : 0) | (a.bf16_scores ? kModeBf16 : 0);
   if (a.fp4) {  // FP4 keys and queries: one query per CTA, or three (TMEM holds two accumulators of 3 x 64)
-    if (a.pool || !a.kI_sf || !a.qI_sf) return cudaErrorInvalidValue;
-    constexpr int F = kModeFp4, L = kModeBlocks, H = kModeBf16;
-    if (a.Q >= 3) {
+    if (!a.kI_sf || !a.qI_sf) return cudaErrorInvalidValue;
+    constexpr int F = kModeFp4, L = kModeBlocks, H = kModeBf16, P = kModePool;
+    if (a.Q >= 3 && !a.pool) {
       switch (mode) {
         case 0: return launch_qpc<3, F>(a, encode, stream);
         case L: return launch_qpc<3, F | L>(a, encode, stream);
@@ -634,6 +672,8 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
       case L: return launch_qpc<1, F | L>(a, encode, stream);
       case H: return launch_qpc<1, F | H>(a, encode, stream);
       case L | H: return launch_qpc<1, F | L | H>(a, encode, stream);
+      case P: return launch_qpc<1, F | P>(a, encode, stream);
+      case P | H: return launch_qpc<1, F | P | H>(a, encode, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -79,6 +79,8 @@ def _load():
         lib.orc_e8m0.argtypes = [ctypes.c_uint8]
         lib.orc_quantize_index_fp4.argtypes = [ctypes.c_int, _u16p, _u8p, _u8p]
         lib.orc_dequantize_index_fp4.argtypes = [ctypes.c_int, _u8p, _u8p, _f64p]
+        lib.orc_quantize_index_fp4_rows.argtypes = [ctypes.c_int64, ctypes.c_int, _u16p, _u8p, _u8p]
+        lib.orc_dequantize_index_fp4_rows.argtypes = [ctypes.c_int64, ctypes.c_int, _u8p, _u8p, _f64p]
         lib.orc_index_scores_f64.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f64p, _u16p, _f64p,
                                              _f64p]
         lib.orc_visible.restype = ctypes.c_int64
@@ -382,16 +384,11 @@ def quantize_index_fp4(rows):
     row, channel 2j in the low nibble of code byte j, scale g for channels
     32g .. 32g+31."""
     rows = _c(rows, np.uint16)
-    r2 = rows.reshape(-1, rows.shape[-1])
+    r2 = np.ascontiguousarray(rows.reshape(-1, rows.shape[-1]))
     D = r2.shape[1]
     codes = np.empty((r2.shape[0], D // 2), np.uint8)
     scales = np.empty((r2.shape[0], D // 32), np.uint8)
-    for i in range(r2.shape[0]):
-        r = np.ascontiguousarray(r2[i])
-        c = np.empty(D // 2, np.uint8)
-        s = np.empty(D // 32, np.uint8)
-        _load().orc_quantize_index_fp4(D, _ptr(r, _u16p), _ptr(c, _u8p), _ptr(s, _u8p))
-        codes[i], scales[i] = c, s
+    _load().orc_quantize_index_fp4_rows(r2.shape[0], D, _ptr(r2, _u16p), _ptr(codes, _u8p), _ptr(scales, _u8p))
     lead = rows.shape[:-1]
     return codes.reshape(lead + (D // 2,)), scales.reshape(lead + (D // 32,))
 
@@ -400,13 +397,11 @@ def dequantize_index_fp4(codes, scales) -> np.ndarray:
     """(codes [..., D/2], scales [..., D/32]) -> values [..., D] (doubles)."""
     codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
     D = codes.shape[-1] * 2
-    c2, s2 = codes.reshape(-1, D // 2), scales.reshape(-1, D // 32)
+    c2 = np.ascontiguousarray(codes.reshape(-1, D // 2))
+    s2 = np.ascontiguousarray(scales.reshape(-1, D // 32))
     out = np.empty((c2.shape[0], D), np.float64)
-    for i in range(c2.shape[0]):
-        c, s = np.ascontiguousarray(c2[i]), np.ascontiguousarray(s2[i])
-        o = np.empty(D, np.float64)
-        _load().orc_dequantize_index_fp4(D, _ptr(c, _u8p), _ptr(s, _u8p), _ptr(o, _f64p))
-        out[i] = o
+    if c2.shape[0]:
+        _load().orc_dequantize_index_fp4_rows(c2.shape[0], D, _ptr(c2, _u8p), _ptr(s2, _u8p), _ptr(out, _f64p))
     return out.reshape(codes.shape[:-1] + (D,))
 
 

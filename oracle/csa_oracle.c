@@ -335,10 +335,22 @@ void orc_quantize_index_fp4(int D, const uint16_t *x, uint8_t *codes, uint8_t *s
   }
 }
 
+/* n such rows, row r at x + r*D, codes + r*D/2, scales + r*D/32. */
+void orc_quantize_index_fp4_rows(int64_t n, int D, const uint16_t *x, uint8_t *codes, uint8_t *scales) {
+  for (int64_t r = 0; r < n; ++r)
+    orc_quantize_index_fp4(D, x + r * D, codes + r * (D / 2), scales + r * (D / 32));
+}
+
 /* The D values such a row stands for: e8m0(scale of the block) * e2m1(code). */
 void orc_dequantize_index_fp4(int D, const uint8_t *codes, const uint8_t *scales, double *x) {
   for (int c = 0; c < D; ++c)
     x[c] = orc_e8m0(scales[c / 32]) * orc_e2m1((uint8_t)((codes[c / 2] >> (4 * (c & 1))) & 0xF));
+}
+
+/* n such rows decoded, row r at x + r*D. */
+void orc_dequantize_index_fp4_rows(int64_t n, int D, const uint8_t *codes, const uint8_t *scales, double *x) {
+  for (int64_t r = 0; r < n; ++r)
+    orc_dequantize_index_fp4(D, codes + r * (D / 2), scales + r * (D / 32), x + r * D);
 }
 
 /* ---- visibility ([KV 压缩] §9.8) ---------------------------------------- */

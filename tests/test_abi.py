@@ -156,8 +156,7 @@ def test_fp4_indexer_argument_checks(lib):
     assert lib.index_keys_fp4_bytes(2, 300) == 2 * (300 * 64 + 3 * 512)
     assert lib.index_query_fp4_bytes(5) == 5 * (64 * 64 + 512)
     raw = ctypes.CDLL(lib.LIBRARY_PATH)
-    for fn in ("csa_quantize_index_keys_fp4", "csa_quantize_index_query_fp4", "csa_reindex_topk",
-               "csa_compress_indexer_keys"):
+    for fn in ("csa_quantize_index_keys_fp4", "csa_quantize_index_query_fp4", "csa_compress_indexer_keys"):
         getattr(raw, fn).restype = ctypes.c_int
     fake = ctypes.c_void_p(0x10000)
     i64 = ctypes.c_int64
@@ -166,10 +165,22 @@ def test_fp4_indexer_argument_checks(lib):
     assert raw.csa_quantize_index_keys_fp4(2, 8, i64(0), fake, i64(1028), fake, i64(104), None) == 1
     assert raw.csa_quantize_index_query_fp4(i64(3), None, fake, None) == 1
     assert raw.csa_quantize_index_query_fp4(i64(0), None, None, None) == 0  # nothing to do
-    # formats: only 0 and 1; the Reindex gathers and the E4M3 key compressor take no FP4
+    # formats: only 0 and 1; the E4M3 key compressor takes no FP4
     assert lib.csa_workspace_size(lib.CSA_OP_INDEX_TOPK, lib.csa_default_params(index_format=2), 1, 1, 1024) == 0
     p4 = lib.csa_default_params(index_format=1)
-    assert raw.csa_reindex_topk(ctypes.byref(p4), 1, 1, fake, fake, fake, fake, i64(4096), fake, 2048, fake, None,
-                                fake, ctypes.c_size_t(1 << 30), None) == 2
     assert raw.csa_compress_indexer_keys(ctypes.byref(p4), 1, 4, i64(0), *([fake] * 4), None, None,
                                          *([fake] * 4), i64(512), None) == 2
+
+
+def test_fp4_layouts_give_the_890_bytes_per_token_of_the_csa2_accounting():
+    """[CSA2 详解] §16: a Main KV entry is 288 B and an indexer key 68 B; at
+    2.5 entries per token (three ratio-2 encoder sources, one ratio-1 decoder
+    source) that is 890 B per token.  The library's layouts take exactly those
+    bytes per entry (the scale atoms of 128 keys amortised)."""
+    import re as _re
+    text = open(HEADER).read()
+    main = int(_re.search(r"#define CSA_FP4_ENTRY_BYTES (\d+)", text).group(1))
+    import compressed_sparse_attention_02_gb300 as csa
+    key = csa.index_keys_fp4_bytes(1, 128 * 1000) / (128 * 1000)
+    assert (main, key) == (288, 68)
+    assert (main + key) * (3 * 0.5 + 1 * 1.0) == 890

@@ -74,11 +74,12 @@ def test_query_quantizer_matches_the_oracle_bit_for_bit(csa):
 class Fp4Inputs:
     """Indexer inputs quantized by the oracle and packed into the device layouts."""
 
-    def __init__(self, seed, B, Q, n_cap):
+    def __init__(self, seed, B, Q, n_cap, key_seed=None):
         q = syn.indexer_query_bf16(seed, B, Q)
         self.wI = q["wI"]
         self.qc, self.qs = oracle.quantize_index_fp4(bits(q["qI"]))      # [B][Q][64][64], [B][Q][64][4]
-        self.kc, self.ks = oracle.quantize_index_fp4(bits(syn.indexer_keys_bf16(seed, B, n_cap)))
+        ks = seed if key_seed is None else key_seed
+        self.kc, self.ks = oracle.quantize_index_fp4(bits(syn.indexer_keys_bf16(ks, B, n_cap)))
         self.kI = torch.from_numpy(pack_index_keys_fp4(self.kc, self.ks, n_cap))
         self.qI = torch.from_numpy(pack_index_query_fp4(self.qc.reshape(B * Q, 64, 64), self.qs.reshape(B * Q, 64, 4)))
         self.n_cap = n_cap
@@ -165,11 +166,12 @@ def test_fp4_queries_with_bf16_scores(csa):
         assert np.all(r[out] <= kth + 2.0 ** -7 * abs(kth)), "a left-out entry outranks the selection"
 
 
-def test_full_size_decode_sampled_rows(csa):
-    """decode-b64-128k with FP4 keys and queries (quantized on the device by
-    the library's own quantizers); rows 0 and 63 against the oracle, which
-    quantizes those sequences' bf16 rows itself."""
-    w = syn.WORKLOADS[1]
+@pytest.mark.parametrize("cfg,samples", [(2, (0, 63)), (3, (5,))])
+def test_full_size_decode_sampled_rows(csa, cfg, samples):
+    """decode-b64-128k and v4pro-decode-b8-1m with FP4 keys and queries
+    (quantized on the device by the library's own quantizers); sampled rows
+    against the oracle, which quantizes those sequences' bf16 rows itself."""
+    w = syn.WORKLOADS[cfg]
     B, n_cap, k, t = w.B, w.n_cap, w.topk, w.t
     q = syn.indexer_query_bf16(w.config, B, 1, device=DEV)
     keys = syn.indexer_keys_bf16(w.config, B, n_cap, device=DEV)
@@ -185,7 +187,7 @@ def test_full_size_decode_sampled_rows(csa):
                        sc, ws)
     assert csa.csa_check_status() == 0
     idx, sc = idx.cpu().numpy(), sc.cpu().numpy()
-    for b in (0, B - 1):
+    for b in samples:
         qc, qs = oracle.quantize_index_fp4(bits(q["qI"][b, 0]))
         kc, ks = oracle.quantize_index_fp4(bits(keys[b]))
         V = oracle.visible(t)
@@ -213,6 +215,81 @@ def test_full_layer_pool_on_fp4_keys(csa):
     pool = pool.cpu().numpy()
     for b in range(B):  # the pool is a valid top-`blocks` of the oracle's block scores
         check_topk(pool[b, 0], oracle.block_scores(x.scores(b, 0, t)), blocks, "pool b=%d" % b)
+
+
+def reindex_fp4(csa, p, x, pos, pool, nb):
+    B, Q = pos.shape
+    idx = torch.full((B, Q, p.topk), -7, dtype=torch.int32, device=DEV)
+    sc = torch.empty((B, Q, p.topk), dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_REINDEX_TOPK, p, B, Q, x.n_cap)
+    csa.csa_reindex_topk(p, B, Q, pos.to(DEV), x.qI.to(DEV), x.wI.to(DEV), x.kI.to(DEV), x.n_cap,
+                         torch.as_tensor(pool, dtype=torch.int32).to(DEV), nb, idx, sc, ws)
+    return idx.cpu().numpy(), sc.cpu().numpy()
+
+
+def check_reindex_row(idx, sc, pool, x, b, t, k, what):
+    """The Reindex selection over FP4 keys, as positions in the pool's entry
+    list, is a valid top-k of the oracle's FP4 scores of the pool's entries
+    (the pool's visible entries, then the scores of those entries only)."""
+    V = oracle.visible(t)
+    ent = oracle.pool_entries(pool, V)
+    esc = oracle.index_scores_fp4(x.qc[b, 0], x.qs[b, 0], bits(x.wI[b, 0]), x.kc[b, ent], x.ks[b, ent])
+    n = min(k, ent.size)
+    assert np.all(idx[n:] == -1), what + ": padding"
+    assert np.all(np.isin(idx[:n], ent)), what + ": an entry outside the pool"
+    slots = np.searchsorted(ent, idx[:n])
+    got = np.full(k, -1, np.int64)
+    got[:n] = slots
+    check_topk(got, esc, k, what)
+    tol = 1e-5 * (np.abs(esc).max() if esc.size else 0.0) + 1e-5 * np.abs(esc[slots])
+    assert np.all(np.abs(sc[:n] - esc[slots]) <= tol), what + ": selected scores"
+    assert np.all(np.isneginf(sc[n:]))
+    return ent[np.sort(oracle.topk(esc, k)[:n])] if n else np.empty(0, np.int64)
+
+
+@pytest.mark.parametrize("t", [4 * 6000 - 1, 2047])
+def test_reindex_on_fp4_keys(csa, t):
+    """A Reindex layer on FP4 keys: the pool comes from the Full layer of
+    another FP4 query set over the same keys (its slots gathered 16 blocks to
+    a tile, with the scale words assembled in the producer), and the Reindex
+    top-k is checked against the oracle's FP4 scores of the pool's entries.
+    t = 2047: 64 visible blocks for 256 pool slots (-1 slots)."""
+    B, n_cap, k, nb = 3, 6000, 256, 256
+    xf = Fp4Inputs(47, B, 1, n_cap)
+    xr = Fp4Inputs(48, B, 1, n_cap, key_seed=47)
+    p = csa.csa_default_params(topk=k, index_format=1)
+    q_pos = torch.full((B, 1), t, dtype=torch.int32, device=DEV)
+    idx = torch.empty((B, 1, k), dtype=torch.int32, device=DEV)
+    pool = torch.empty((B, 1, nb), dtype=torch.int32, device=DEV)
+    csa.csa_index_topk_pool(p, B, 1, q_pos, xf.qI.to(DEV), xf.wI.to(DEV), xf.kI.to(DEV), n_cap, idx, None, nb, pool,
+                            csa.workspace(csa.CSA_OP_INDEX_TOPK_POOL, p, B, 1, n_cap))
+    assert csa.csa_check_status() == 0
+    pool = pool.cpu().numpy()
+    ridx, rsc = reindex_fp4(csa, p, xr, q_pos.cpu(), pool, nb)
+    assert csa.csa_check_status() == 0
+    for b in range(B):
+        check_reindex_row(ridx[b, 0], rsc[b, 0], pool[b, 0], xr, b, t, k, "reindex b=%d" % b)
+
+
+def test_reindex_on_fp4_keys_partial_block_and_foreign_ids(csa):
+    """The partial last block (V = 8*40 + 3) is scored up to V only; a block
+    id past the cache is reported and nothing invisible is returned."""
+    n_cap, nb, k = 1024, 16, 128
+    V = 8 * 40 + 3
+    t = 4 * V + 2
+    x = Fp4Inputs(49, 1, 1, n_cap)
+    p = csa.csa_default_params(topk=k, index_format=1)
+    pool = np.array([[[0, 3, 5, 8, 13, 21, 22, 23, 24, 25, 26, 27, 28, 34, 39, 40]]], dtype=np.int32)
+    pos = torch.tensor([[t]], dtype=torch.int32)
+    ridx, rsc = reindex_fp4(csa, p, x, pos, pool, nb)
+    assert csa.csa_check_status() == 0
+    want = check_reindex_row(ridx[0, 0], rsc[0, 0], pool[0, 0], x, 0, t, k, "partial")
+    assert np.array_equal(ridx[0, 0][:len(want)], want) and (ridx[0, 0] >= 0).sum() == 15 * 8 + 3
+    pool[0, 0, 8] = 5000  # past the 1024-entry cache
+    ridx, _ = reindex_fp4(csa, p, x, pos, pool, nb)
+    assert csa.csa_check_status() == 5  # CSA_ERR_INDEX_RANGE
+    got = ridx[0, 0]
+    assert set(got[got >= 0]) <= set(oracle.pool_entries(pool[0, 0], V))
 
 
 def gpu_fp4_rows(csa, config, B, Q, n_cap):
