@@ -659,6 +659,35 @@ def index_fp4_profile(csa, torch, dev, cfg, x=None, sets=4, n=100):
         res[name] = {"call_ms": call_ms, "index_scores_ms": st[0], "topk_ms": st[1], "index_bytes": nbytes[fmt],
                      "index_gbs": gbs, "index_hbm_frac": gbs / hbm}
         del ws
+    # the hierarchical indexer with either key format: Full layers make one
+    # 2048-block pool per query set, then Reindex layers with other queries
+    nb = 2048
+    pools = [torch.empty(B, 1, nb, dtype=torch.int32, device=dev) for _ in range(sets)]
+    cand = min(nb, (V + 7) // 8) * 8
+    for fmt in ("e4m3", "fp4"):
+        p = csa.csa_default_params(topk=k, index_format=1 if fmt == "fp4" else 0)
+        kI = k4 if fmt == "fp4" else k8
+        ws_full = csa.workspace(csa.CSA_OP_INDEX_TOPK_POOL, p, B, 1, n_cap, device=dev)
+        ws_re = csa.workspace(csa.CSA_OP_REINDEX_TOPK, p, B, 1, n_cap, device=dev)
+
+        def full(i):
+            q = qsets[i % sets]
+            csa.csa_index_topk_pool(p, B, 1, pos, q[fmt], q["wI"], kI, n_cap, idx, None, nb, pools[i % sets],
+                                    ws_full)
+
+        def reindex(i):
+            q = qsets[(i + 1) % sets]
+            csa.csa_reindex_topk(p, B, 1, pos, q[fmt], q["wI"], kI, n_cap, pools[i % sets], nb, idx, None, ws_re)
+        full_ms = _ms_per_call(torch, full, n)
+        re_ms = _ms_per_call(torch, reindex, n)
+        re_st = _index_stages(csa, torch, reindex, n)
+        rbytes = B * (cand * (68 if fmt == "fp4" else 128) + (4608 if fmt == "fp4" else 8192) + 64 * 2)
+        res["hierarchical_" + fmt] = {"full_layer_ms": full_ms, "reindex_ms": re_ms, "reindex_index_ms": re_st[0],
+                                      "reindex_topk_ms": re_st[1], "reindex_bytes": rbytes,
+                                      "reindex_kernel_gbs": rbytes / (re_st[0] * 1e-3) / 1e9,
+                                      "reindex_kernel_hbm_frac": rbytes / (re_st[0] * 1e-3) / 1e9 / hbm}
+        del ws_full, ws_re
+    del pools
     if x is not None:  # the whole decode step (csa_layer_decode) with either indexer format
         qs = [syn_main_query(w, B, r, dev) for r in range(sets)]
         out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev)

@@ -136,13 +136,13 @@ __device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, int64_t g, i
   return gi;
 }
 
-// A score into the row array: fp32, or its bf16 bits (already rounded).
+// A score into its row: fp32, or its bf16 bits (already rounded).
 template <bool kBf16>
-__device__ __forceinline__ void store_score(const IndexArgs& a, int64_t at, float v) {
+__device__ __forceinline__ void store_score(uint8_t* row, int64_t i, float v) {
   if constexpr (kBf16)
-    reinterpret_cast<uint16_t*>(a.scores)[at] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
+    reinterpret_cast<uint16_t*>(row)[i] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
   else
-    a.scores[at] = v;
+    reinterpret_cast<float*>(row)[i] = v;
 }
 
 // True if a query of the group sits past what the cache holds (V(t) > n_cap).
@@ -162,7 +162,7 @@ __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const Group
 }
 
 template <int QPC, int kMode>
-__global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PER_SM)
+__global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, IndexCfg<QPC, (kMode & 8) != 0>::CTAS_PER_SM)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
   constexpr bool kPool = (kMode & kModePool) != 0, kBlocks = (kMode & kModeBlocks) != 0,
@@ -480,90 +480,90 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
-    // Four groups of 4 warps; in a group, warp w reads TMEM lane quadrant
-    // w % 4 (keys 32*(w%4) .. +31 of the tile).  With one query per tile the
-    // groups take tiles in turn; with four, every group takes every tile and
-    // scores its own query.
+    // Groups of 4 warps; in a group, warp w reads TMEM lane quadrant w % 4
+    // (keys 32*(w%4) .. +31 of the tile).  With one query per tile the groups
+    // take tiles in turn; with more, every group takes every tile and scores
+    // its own query.
+    // The CTA's unit range is walked group by group: a group's active tiles
+    // are the prefix of its tiles below its last visible key, so the running
+    // tile count `it` (the MMA thread's accumulator numbering) advances by a
+    // group's active tiles at once, and a warp visits only its own tiles.
     const int ew = warp - 2;
     const int grp = ew >> 2;
     const int sub = warp & 3;
     const int row = sub * 32 + lane;
-    constexpr int kMyQ = QPC == 1 ? 1 : 1;  // queries scored per tile by one group
-    const int jq = QPC == 1 ? 0 : grp;       // the query this group scores
-    float4* w_mine = reinterpret_cast<float4*>(w_s + ew * kIdxHeads);  // this warp's copy of the head weights
-    int64_t seen_g = -1;
-    bool active = false;
-    GroupInfo gi{};
+    const int jq = QPC == 1 ? 0 : grp;  // the query this group scores
+    float* w_mine = w_s + ew * kIdxHeads;  // this warp's copy of the head weights
+    const uint32_t w_addr = smem_u32(w_mine);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(sub * 32) << 16) + jq * kIdxHeads;
+    constexpr int kStep = QPC == 1 ? kEpiGroups : 1;
     int it = 0;
-    int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
-    for (int64_t u = u0; u < u1; ++u) {
-      if (++tile == tiles_per_group) {
-        tile = 0;
-        ++g;
+    bool ok = true;
+    for (int64_t g = u0 / tiles_per_group; ok && g * tiles_per_group < u1; ++g) {
+      const int64_t gu = g * tiles_per_group;
+      const int ta = gu < u0 ? static_cast<int>(u0 - gu) : 0;
+      const int te = u1 - gu < tiles_per_group ? static_cast<int>(u1 - gu) : tiles_per_group;
+      const GroupInfo gi = group_info<QPC>(a, g, groups_per_seq);
+      const int64_t n_vis_tiles = (gi.vmax + kTileKeys - 1) / kTileKeys;
+      const int tb = n_vis_tiles < te ? static_cast<int>(n_vis_tiles) : te;
+      if (tb <= ta) continue;
+      if (ta == 0 && warp == 2 && lane == 0 && group_past_cache<QPC>(a, gi)) record_error(a.status, kErrIndexRange);
+      // this group's query: head weights, output rows, visible counts
+      const int q = gi.q0 + jq;
+      const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + q;
+      __syncwarp();  // the warp is done with the previous group's weights
+      for (int e = lane; e < kIdxHeads; e += 32) {
+        const uint16_t wb = q < a.Q ? a.wI[row_off * kIdxHeads + e] : uint16_t(0);
+        w_mine[e] = __uint_as_float(static_cast<uint32_t>(wb) << 16);
       }
-      if (g != seen_g) {
-        gi = group_info<QPC>(a, g, groups_per_seq);
-        seen_g = g;
-        active = gi.vmax > tile * kTileKeys;
-        if (active) {
-          __syncwarp();  // the warp is done with the previous group's weights
-          const int q = gi.q0 + jq;
-          float* wf = reinterpret_cast<float*>(w_mine);
-          for (int e = lane; e < kIdxHeads; e += 32) {
-            const uint16_t wb = q < a.Q ? a.wI[(static_cast<int64_t>(gi.b) * a.Q + q) * kIdxHeads + e] : uint16_t(0);
-            wf[e] = __uint_as_float(static_cast<uint32_t>(wb) << 16);
-          }
-          __syncwarp();
+      __syncwarp();
+      const int64_t vis = gi.vis[jq], vent = gi.vent[jq];
+      uint8_t* srow = reinterpret_cast<uint8_t*>(a.scores) + row_off * a.score_ld * (kBf16 ? 2 : 4);
+      uint32_t* hrow = a.hist ? a.hist + row_off * kKeyBins : nullptr;
+      const int32_t* prow = kPool ? a.pool + row_off * a.pool_ld : nullptr;
+      const int64_t n_blk_vis = (vent + kPoolBlock - 1) / kPoolBlock;
+      int t = ta;
+      if constexpr (kStep > 1) t += ((grp - it) % kStep + kStep) % kStep;
+      for (; t < tb; t += kStep) {
+        const int my_it = it + (t - ta);
+        const int x = my_it % NBUF;
+        const uint32_t xuse = static_cast<uint32_t>(my_it / NBUF);
+        // every lane waits; the warp leaves together if any lane gave up
+        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[x], xuse & 1u, a.status))) {
+          ok = false;
+          break;
         }
-      }
-      if (!active || tile * kTileKeys >= gi.vmax) continue;
-      if (tile == 0 && warp == 2 && lane == 0 && group_past_cache<QPC>(a, gi)) record_error(a.status, kErrIndexRange);
-      const int my_it = it++;
-      if (QPC == 1 && (my_it % kEpiGroups) != grp) continue;  // another group's tile
-      const int x = my_it % NBUF;
-      const uint32_t xuse = static_cast<uint32_t>(my_it / NBUF);
-      // every lane waits; the warp leaves together if any lane gave up
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[x], xuse & 1u, a.status))) break;
-      tc_fence_after();
-      const int64_t s_idx = tile * kTileKeys + row;
-#pragma unroll
-      for (int jj = 0; jj < kMyQ; ++jj) {
-        const int j = jq;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(sub * 32) << 16) + x * N + j * kIdxHeads;
+        tc_fence_after();
+        const int64_t s_idx = static_cast<int64_t>(t) * kTileKeys + row;
+        const uint32_t taddr = t_lane + x * N;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // 32 heads at a time keeps registers low
-          uint32_t r[2][16];
-          tmem_ld16(taddr + 32 * half, r[0]);
-          tmem_ld16(taddr + 32 * half + 16, r[1]);
+          uint32_t r[32];
+          tmem_ld32(taddr + 32 * half, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float4 w4 = w_mine[half * 8 + c * 4 + v];
-              const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                acc[e] = fmaf(wv[e], fmaxf(__uint_as_float(r[c][4 * v + e]), 0.f), acc[e]);
-            }
+          for (int v = 0; v < 8; ++v) {
+            const float4 w4 = lds_f32x4(w_addr + 16 * (8 * half + v));
+            acc[0] = fmaf(w4.x, fmaxf(__uint_as_float(r[4 * v + 0]), 0.f), acc[0]);
+            acc[1] = fmaf(w4.y, fmaxf(__uint_as_float(r[4 * v + 1]), 0.f), acc[1]);
+            acc[2] = fmaf(w4.z, fmaxf(__uint_as_float(r[4 * v + 2]), 0.f), acc[2]);
+            acc[3] = fmaf(w4.w, fmaxf(__uint_as_float(r[4 * v + 3]), 0.f), acc[3]);
           }
         }
         float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         // bf16 scores: every use below (store, digit counts, block maxima)
         // sees the rounded value
         if constexpr (kBf16) score = __bfloat162float(__float2bfloat16_rn(score));
-        const bool in_row = s_idx < gi.vis[j];
+        const bool in_row = s_idx < vis;
         bool valid = in_row;
-        const int64_t row_off = static_cast<int64_t>(gi.b) * a.Q + gi.q0 + j;
         if (kPool && in_row) {  // slot s_idx holds entry 8*pool[s_idx/8] + s_idx%8
-          const int32_t blk = __ldg(a.pool + row_off * a.pool_ld + (s_idx >> 3));
-          const int64_t nb = (gi.vent[j] + kPoolBlock - 1) / kPoolBlock;
-          if (blk >= nb && (row & 7) == 0) record_error(a.status, kErrIndexRange);
-          valid = blk >= 0 && static_cast<int64_t>(blk) * kPoolBlock + (row & 7) < gi.vent[j];
-          store_score<kBf16>(a, row_off * a.score_ld + s_idx, valid ? score : -INFINITY);
+          const int32_t blk = __ldg(prow + (s_idx >> 3));
+          if (blk >= n_blk_vis && (row & 7) == 0) record_error(a.status, kErrIndexRange);
+          valid = blk >= 0 && static_cast<int64_t>(blk) * kPoolBlock + (row & 7) < vent;
+          store_score<kBf16>(srow, s_idx, valid ? score : -INFINITY);
         } else if (valid) {
-          store_score<kBf16>(a, row_off * a.score_ld + s_idx, score);
+          store_score<kBf16>(srow, s_idx, score);
         }
         if constexpr (kBlocks) {  // the block's largest score: 8 adjacent lanes
           float bm = valid ? score : -INFINITY;
@@ -576,15 +576,16 @@ __global__ void __launch_bounds__(IndexCfg<QPC>::THREADS, IndexCfg<QPC>::CTAS_PE
           const unsigned bpeers = __match_any_sync(0xffffffffu, bbin);
           if (lead && lane == __ffs(bpeers) - 1) atomicAdd(a.block_hist + row_off * kKeyBins + bbin, __popc(bpeers));
         }
-        if (a.hist) {  // first-digit histogram of the row, one atomic per distinct digit per warp
+        if (hrow) {  // first-digit histogram of the row, one atomic per distinct digit per warp
           const int bin = valid ? static_cast<int>(score_key(score) >> kKeyBinShift) : -1;
           const unsigned peers = __match_any_sync(0xffffffffu, bin);
-          if (valid && lane == __ffs(peers) - 1) atomicAdd(a.hist + row_off * kKeyBins + bin, __popc(peers));
+          if (valid && lane == __ffs(peers) - 1) atomicAdd(hrow + bin, __popc(peers));
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[x]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[x]);
+      it += tb - ta;
     }
   }
 

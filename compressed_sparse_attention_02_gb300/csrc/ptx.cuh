@@ -146,6 +146,14 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   return v;
 }
 
+// ---- shared memory ------------------------------------------------------------
+
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 // ---- proxy fences -----------------------------------------------------------
 
 // Makes generic-proxy shared-memory writes visible to the async proxy (TMA,
