@@ -93,7 +93,11 @@ struct IndexCfg {
   static_assert(COLS <= 512, "TMEM holds 512 columns");
   static constexpr uint32_t TMEM_COLS =
       COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : (COLS <= 256 ? 256 : 512)));
-  static constexpr size_t SMEM = 1024 + 2 * QPC * (QBYTES + SF) + STAGES * (KEY_TILE + SF) +
+  // one query per CTA: each epilogue group gathers the row's first-digit
+  // counts in shared memory and adds them to the global row once per query
+  // group
+  static constexpr uint32_t HIST = QPC == 1 ? GROUPS * kKeyBins * 4 : 0;
+  static constexpr size_t SMEM = 1024 + 2 * QPC * (QBYTES + SF) + STAGES * (KEY_TILE + SF) + HIST +
                                  EPI_WARPS * kIdxHeads * 4 + (2 * STAGES + 2 * NBUF + 5) * 8 + 16;
 };
 
@@ -183,7 +187,8 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
   constexpr int NBUF = Cfg::NBUF;
   constexpr int kEpiWarps = Cfg::EPI_WARPS;
   constexpr int kEpiGroups = Cfg::GROUPS;
-  float* w_s = reinterpret_cast<float*>(qsf_s + 2 * QPC * Cfg::SF);  // [epilogue warps][64]
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(qsf_s + 2 * QPC * Cfg::SF);  // QPC 1: [GROUPS][2048] digit counts
+  float* w_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(hist_s) + Cfg::HIST);  // [epilogue warps][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(w_s + kEpiWarps * kIdxHeads);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;   // [NBUF]
@@ -497,9 +502,22 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
     const uint32_t w_addr = smem_u32(w_mine);
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(sub * 32) << 16) + jq * kIdxHeads;
     constexpr int kStep = QPC == 1 ? kEpiGroups : 1;
+    // One query per CTA, many CTAs per row (a.hist_private): each epilogue
+    // group counts digits in its own hist_s row and adds it to the global
+    // row once it is done with the query group, instead of many CTAs'
+    // atomics meeting on the same bins.  The group's 4 warps meet at named
+    // barrier 1 + grp around each flush; a warp whose wait gave up still
+    // walks the groups (doing no work) so that no barrier hangs.
+    const bool priv = QPC == 1 && a.hist_private && a.hist;
+    const uint32_t et = threadIdx.x - 64 - 128 * grp;  // thread index within the epilogue group
+    uint32_t* hist_mine = hist_s + grp * kKeyBins;
+    if (priv) {
+      for (uint32_t i = et; i < kKeyBins; i += 128) hist_mine[i] = 0u;
+      named_bar_sync(1 + grp, 128);
+    }
     int it = 0;
     bool ok = true;
-    for (int64_t g = u0 / tiles_per_group; ok && g * tiles_per_group < u1; ++g) {
+    for (int64_t g = u0 / tiles_per_group; g * tiles_per_group < u1; ++g) {
       const int64_t gu = g * tiles_per_group;
       const int ta = gu < u0 ? static_cast<int>(u0 - gu) : 0;
       const int te = u1 - gu < tiles_per_group ? static_cast<int>(u1 - gu) : tiles_per_group;
@@ -524,7 +542,7 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
       const int64_t n_blk_vis = (vent + kPoolBlock - 1) / kPoolBlock;
       int t = ta;
       if constexpr (kStep > 1) t += ((grp - it) % kStep + kStep) % kStep;
-      for (; t < tb; t += kStep) {
+      for (; ok && t < tb; t += kStep) {
         const int my_it = it + (t - ta);
         const int x = my_it % NBUF;
         const uint32_t xuse = static_cast<uint32_t>(my_it / NBUF);
@@ -579,13 +597,29 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
         if (hrow) {  // first-digit histogram of the row, one atomic per distinct digit per warp
           const int bin = valid ? static_cast<int>(score_key(score) >> kKeyBinShift) : -1;
           const unsigned peers = __match_any_sync(0xffffffffu, bin);
-          if (valid && lane == __ffs(peers) - 1) atomicAdd(hrow + bin, __popc(peers));
+          if (valid && lane == __ffs(peers) - 1) {
+            if (priv)
+              atomicAdd(hist_mine + bin, __popc(peers));  // shared
+            else
+              atomicAdd(hrow + bin, __popc(peers));  // global
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[x]);
       }
       it += tb - ta;
+      if (priv) {  // this group is done with the query: add its counts to the row
+        named_bar_sync(1 + grp, 128);
+        for (uint32_t i = et; i < kKeyBins; i += 128) {
+          const uint32_t c = hist_mine[i];
+          if (c) {
+            atomicAdd(hrow + i, c);
+            hist_mine[i] = 0u;
+          }
+        }
+        named_bar_sync(1 + grp, 128);
+      }
     }
   }
 
@@ -644,8 +678,13 @@ cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 enc
   // One wave of CTAs that all stay resident; each takes an equal range.
   int64_t ctas = static_cast<int64_t>(sms) * per_sm;
   if (ctas > units) ctas = units;
+  // shared-memory digit counts pay off when many CTAs share a row and each
+  // has many tiles to count
+  IndexArgs ka = a;
+  const int64_t rows = static_cast<int64_t>(a.B) * a.Q;
+  ka.hist_private = QPC == 1 && ctas >= 8 * rows && units >= 16 * ctas;
   return launch_pdl(index_score_kernel<QPC, kMode>, dim3(static_cast<unsigned>(ctas)), dim3(Cfg::THREADS), Cfg::SMEM,
-                    stream, tm_k, tm_q, a, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
+                    stream, tm_k, tm_q, ka, static_cast<int>(tiles_per_group), static_cast<int>(groups_per_seq));
 }
 
 }  // namespace

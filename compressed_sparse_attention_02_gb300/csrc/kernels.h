@@ -116,6 +116,7 @@ struct IndexArgs {
   int64_t score_ld;         // elements (a multiple of 8)
   int bf16_scores;          // 1: scores rounded to bf16 and stored as 2 bytes
   uint32_t* hist;           // [B*Q][2048] key top-digit counts (zeroed by the caller) or null
+  int hist_private;         // set by the launcher: count in shared memory, add to hist per query group
   // Full layer of the hierarchical indexer: per row, the largest score of
   // each block of kPoolBlock entries with a visible first entry, and the
   // first-digit counts of those block scores (zeroed by the caller).

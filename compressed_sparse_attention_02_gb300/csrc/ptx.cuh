@@ -146,6 +146,11 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
   return v;
 }
 
+// Barrier `id` (1..15) over `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---- shared memory ------------------------------------------------------------
 
 __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
