@@ -787,17 +787,21 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
   if (e != cudaSuccess) return e;
   const int64_t queries = static_cast<int64_t>(a.B) * a.Q;
   const int cluster_max = max_split(dev);
-  // Few queries with long row sets: more slices than a cluster holds, merged
-  // by a second kernel through the caller's workspace (at most one slice per
-  // 128-row tile of the longest row set).
+  // With the caller's workspace: split each query's rows over separate CTAs
+  // (one wave, at most one slice per 128-row tile of the longest row set, at
+  // most what the workspace holds), merged by a second kernel.  Taken when
+  // it gives more slices than a cluster holds, or slices of at most 3 tiles;
+  // with longer slices the cluster's on-chip merge was measured faster
+  // (64 queries: 2 slices of 2.5 tiles, decode step 100.5 against 101.5 us;
+  // 2 slices of 4.5 tiles, 47.5 against 43.9 us).
   int gsplit = 1;
-  if (a.part_o && a.part_ml && queries <= kGSplitMaxQueries) {
+  if (a.part_o && a.part_ml && a.gsplit_cap >= 2) {
     const int64_t rows_max = a.W + (a.dense ? a.n_cap : a.k);
     int64_t g = sms / queries;
-    g = g < kMaxGSplit ? g : kMaxGSplit;
+    g = g < a.gsplit_cap ? g : a.gsplit_cap;
     const int64_t tiles = (rows_max + kTileRows - 1) / kTileRows;
     g = g < tiles ? g : tiles;
-    if (g > cluster_max) gsplit = static_cast<int>(g);
+    if (g >= 2 && (g > cluster_max || (tiles + g - 1) / g <= 3)) gsplit = static_cast<int>(g);
   }
   if (gsplit > 1) {
     e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,

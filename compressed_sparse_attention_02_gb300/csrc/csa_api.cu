@@ -301,12 +301,16 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.k = p->topk;
   aa.dense = dense ? 1 : 0;
   aa.m = p->m;
-  // the split-KV path for few queries, when the workspace holds its partials
+  // the split-KV path, with as many slices per query as the workspace holds
   const int64_t queries = static_cast<int64_t>(B) * Q;
-  const size_t need = csa::attn_split_bytes(queries);
-  if (need > 0 && split_ws && split_ws_bytes >= need && aligned16(split_ws)) {
-    aa.part_o = static_cast<float*>(split_ws);
-    aa.part_ml = aa.part_o + queries * csa::kMaxGSplit * csa::kHeads * csa::kDim;
+  if (split_ws && aligned16(split_ws) && queries > 0) {
+    int64_t cap = static_cast<int64_t>(split_ws_bytes / (static_cast<size_t>(queries) * csa::kGSplitSliceBytes));
+    cap = cap < csa::kMaxGSplit ? cap : csa::kMaxGSplit;
+    if (cap >= 2) {
+      aa.part_o = static_cast<float*>(split_ws);
+      aa.part_ml = aa.part_o + queries * cap * csa::kHeads * csa::kDim;
+      aa.gsplit_cap = static_cast<int>(cap);
+    }
   }
   aa.swa = swa;
   aa.swa_mode = swa_mode;
@@ -416,28 +420,41 @@ void csa_default_params(csa_params* p) {
   p->index_format = 0;
 }
 
+// SMs of the current device (0 without one): the split-KV scratch is sized
+// for one wave of its slices.
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return sms;
+}
+
 size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q, int64_t n_cap) {
   if (check_params(p) != CSA_OK || B < 0 || Q < 0 || !n_cap_ok(n_cap)) return 0;
   IndexWs w;
+  const int sms = device_sms();
   switch (op) {
     case CSA_OP_COMPRESS:
       return 16;  // no scratch needed; a non-zero size keeps callers uniform
-    case CSA_OP_SPARSE_ATTN: {  // the split-KV partials for few queries
-      const size_t a = csa::attn_split_bytes(static_cast<int64_t>(B) * Q);
+    case CSA_OP_SPARSE_ATTN: {  // the split-KV partials
+      const size_t a = csa::attn_split_bytes(static_cast<int64_t>(B) * Q, sms);
       return a > 16 ? a : 16;
     }
     case CSA_OP_INDEX_TOPK:
       return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w) ? w.total : 0;
     case CSA_OP_LAYER_PREFILL:  // the indexer's scratch, then the attention's
       return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)
-                 ? round_up(w.total, 256) + csa::attn_split_bytes(static_cast<int64_t>(B) * Q)
+                 ? round_up(w.total, 256) + csa::attn_split_bytes(static_cast<int64_t>(B) * Q, sms)
                  : 0;
     case CSA_OP_LAYER_DECODE:
       return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w)
-                 ? round_up(w.total, 256) + csa::attn_split_bytes(B)
+                 ? round_up(w.total, 256) + csa::attn_split_bytes(B, sms)
                  : 0;
-    case CSA_OP_HCA_LAYER_DECODE: {  // the attention's split-KV partials (B <= 16)
-      const size_t a = csa::attn_split_bytes(B);
+    case CSA_OP_HCA_LAYER_DECODE: {  // the attention's split-KV partials
+      const size_t a = csa::attn_split_bytes(B, sms);
       return a > 16 ? a : 16;
     }
     case CSA_OP_INDEX_TOPK_POOL: {

@@ -199,21 +199,28 @@ struct AttnArgs {
   float* lse;               // [B][Q][64] or null
   int B, Q;
   float sm_scale;
-  // Workspace of the split-KV path (few queries): per query kMaxGSplit
-  // slices of raw O [64][512] fp32 and (max, sum) [2][64] fp32; null: no
-  // such path.
+  // Workspace of the split-KV path: per query gsplit_cap slices of raw
+  // O [64][512] fp32, then per query gsplit_cap (max, sum) [2][64] fp32;
+  // null: no such path.
   float* part_o;
   float* part_ml;
+  int gsplit_cap;
   int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
   double inv_freq[kRope / 2];  // theta^(-2j/R), host fp64
   unsigned* status;
 };
-constexpr int kMaxGSplit = 16;          // split-KV slices per query at most
-constexpr int kGSplitMaxQueries = 16;   // the split-KV path serves launches of up to this many queries
-// Bytes of the split-KV workspace for `queries` queries (0 past the limit).
-inline size_t attn_split_bytes(int64_t queries) {
-  return queries > kGSplitMaxQueries ? 0
-                                     : static_cast<size_t>(queries) * kMaxGSplit * (kHeads * kDim + 2 * kHeads) * 4;
+constexpr int kMaxGSplit = 16;  // split-KV slices per query at most
+constexpr size_t kGSplitSliceBytes = static_cast<size_t>(kHeads * kDim + 2 * kHeads) * 4;  // raw O + (max, sum)
+// Slices per query of the split-KV path for `queries` queries on a GPU of
+// `sms` SMs: one wave of one CTA per slice, at most kMaxGSplit; 0 when fewer
+// than 2 fit (the cluster path then serves the launch).
+inline int attn_split_slices(int64_t queries, int sms) {
+  if (queries <= 0 || sms <= 0) return 0;
+  const int64_t g = sms / queries < kMaxGSplit ? sms / queries : kMaxGSplit;
+  return g >= 2 ? static_cast<int>(g) : 0;
+}
+inline size_t attn_split_bytes(int64_t queries, int sms) {
+  return static_cast<size_t>(queries) * attn_split_slices(queries, sms) * kGSplitSliceBytes;
 }
 cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream);
 

@@ -112,7 +112,10 @@ enum {
 };
 
 /* Bytes of workspace the call `op` needs for B sequences of Q queries over a
- * cache of n_cap entries.  Returns 0 for an invalid combination. */
+ * cache of n_cap entries.  Returns 0 for an invalid combination.  The
+ * attention's share (CSA_OP_SPARSE_ATTN and the layer calls) is sized for
+ * the current device: one wave of split-KV slices, min(16, SMs / (B*Q))
+ * per query, none when fewer than 2 fit. */
 size_t csa_workspace_size(int32_t op, const csa_params *p, int32_t B, int32_t Q,
                           int64_t n_cap);
 
@@ -446,11 +449,12 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  * sink   : [64] fp32.   out : [B][Q][64][512] bf16.   lse : [B][Q][64] or NULL.
  *
  * workspace: optional.  With csa_workspace_size(CSA_OP_SPARSE_ATTN, p, B, Q,
- *          n_cap) bytes (more than a token amount only for B*Q <= 16), a
- *          call with few queries cuts each query's rows into up to 16 slices
- *          on as many CTAs and merges them in a second kernel (the same
- *          result up to fp32 summation order); NULL or fewer bytes: one
- *          launch, at most a thread-block cluster's slices per query.
+ *          n_cap) bytes (a token amount when B*Q > SMs/2), each query's rows
+ *          are cut into as many slices as the workspace holds and one wave
+ *          of CTAs allows (up to 16, at most one per 128 rows), one CTA
+ *          each, merged by a second kernel (the same result up to fp32
+ *          summation order); NULL or too few bytes: one launch, at most a
+ *          thread-block cluster's slices per query, merged on chip.
  *
  * With p->inverse_rope = 1 each head's output then gets the inverse of the
  * RoPE the rows carry, at the query position ([CSA2 详解] §12.1 "Partial RoPE
