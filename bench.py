@@ -884,6 +884,8 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
     The copies run on their own streams one step ahead of / behind the layer
     call (two staging buffers and two output buffers), as a serving loop
     would overlap them; the timed region spans every step's copies."""
+    stream = torch.cuda.Stream()  # a stream of its own (the legacy default stream cannot be captured)
+    torch.cuda.synchronize()
     names = ["q", "qI", "wI", "q_pos", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb", "swa_row", "kI_row"]
     slot = w.t % w.W
     entry = (w.t + 1) // w.m - 1
@@ -939,16 +941,17 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
     def compute(i):
         s_ = i % 2
         v = sviews[s_]
-        stream.wait_event(in_ready[s_])
-        if i >= 2:
-            stream.wait_event(out_free[s_])
-        x["swa"][:, slot].copy_(v["swa_row"], non_blocking=True)
-        x["kI"][:, entry].copy_(v["kI_row"], non_blocking=True)
-        csa.csa_layer_decode(p, B, v["q_pos"], v["ring_Ca"], v["ring_Za"], v["ring_Cb"], v["ring_Zb"], x["Ba"],
-                             x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], v["qI"], v["wI"], v["q"], x["swa"],
-                             x["sink"], idxs[s_], outs[s_], lse, ws)
-        stage_free[s_].record(stream)
-        out_ready[s_].record(stream)
+        with torch.cuda.stream(stream):
+            stream.wait_event(in_ready[s_])
+            if i >= 2:
+                stream.wait_event(out_free[s_])
+            x["swa"][:, slot].copy_(v["swa_row"], non_blocking=True)
+            x["kI"][:, entry].copy_(v["kI_row"], non_blocking=True)
+            csa.csa_layer_decode(p, B, v["q_pos"], v["ring_Ca"], v["ring_Za"], v["ring_Cb"], v["ring_Zb"], x["Ba"],
+                                 x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], v["qI"], v["wI"], v["q"], x["swa"],
+                                 x["sink"], idxs[s_], outs[s_], lse, ws)
+            stage_free[s_].record(stream)
+            out_ready[s_].record(stream)
 
     def copy_out(i):
         s_ = i % 2
@@ -971,18 +974,53 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
 
     run(3)
     torch.cuda.synchronize()
-    n = min(args.steps, 500)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    h2d_s.wait_event(e0)
-    d2h_s.wait_event(e0)
-    run(n)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    return {"value": B * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "copies": "one packed H2D and two D2H per step, on two copy streams overlapping the "
-                                  "neighbouring steps' layer calls"}
+
+    def timed(fn, n_steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d_s.wait_event(e0)
+        d2h_s.wait_event(e0)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return B * n_steps / (e0.elapsed_time(e1) / 1e3)
+
+    n = min(args.steps, 512)
+    eager = timed(lambda: run(n), n)
+    # A serving loop replays captured steps: G consecutive steps (their copies
+    # and the overlap between neighbours included) in one CUDA graph.
+    G = 16
+    graph, why = None, None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            h2d_s.wait_event(fork)
+            d2h_s.wait_event(fork)
+            run(G)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # report the eager loop alone
+        graph, why = None, "graph capture failed: %s" % str(exc).splitlines()[0][:120]
+    res = {"unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "copies": "one packed H2D and two D2H per step, on two copy streams overlapping the neighbouring "
+                     "steps' layer calls", "eager_value": eager}
+    if graph is not None:
+        reps = max(n // G, 1)
+
+        def replay():  # on the stream the timing events are recorded on
+            with torch.cuda.stream(stream):
+                for _ in range(reps):
+                    graph.replay()
+        res.update({"value": timed(replay, reps * G), "steps": reps * G,
+                    "launch": "CUDA graphs of %d steps (copies included), replayed" % G})
+    else:
+        res.update({"value": eager, "steps": n, "launch": "eager: " + why})
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the end-to-end section")
+    return res
 
 
 # ---------------------------------------------------------------------------
