@@ -554,7 +554,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
         tc_fence_after();
         const int64_t s_idx = static_cast<int64_t>(t) * kTileKeys + row;
         const uint32_t taddr = t_lane + x * N;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+        // four independent chains (head h into chain h % 4); where the
+        // epilogue's issue rate bounds the kernel (FP4 keys, several queries
+        // a tile) two chains go through one packed FMA, the same roundings
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // 32 heads at a time keeps registers low
           uint32_t r[32];
@@ -563,10 +566,21 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             const float4 w4 = lds_f32x4(w_addr + 16 * (8 * half + v));
-            acc[0] = fmaf(w4.x, fmaxf(__uint_as_float(r[4 * v + 0]), 0.f), acc[0]);
-            acc[1] = fmaf(w4.y, fmaxf(__uint_as_float(r[4 * v + 1]), 0.f), acc[1]);
-            acc[2] = fmaf(w4.z, fmaxf(__uint_as_float(r[4 * v + 2]), 0.f), acc[2]);
-            acc[3] = fmaf(w4.w, fmaxf(__uint_as_float(r[4 * v + 3]), 0.f), acc[3]);
+            const float x0 = fmaxf(__uint_as_float(r[4 * v + 0]), 0.f), x1 = fmaxf(__uint_as_float(r[4 * v + 1]), 0.f);
+            const float x2 = fmaxf(__uint_as_float(r[4 * v + 2]), 0.f), x3 = fmaxf(__uint_as_float(r[4 * v + 3]), 0.f);
+            if constexpr (kFp4 || QPC > 1) {
+              const float2 a01 = ffma2(make_float2(w4.x, w4.y), make_float2(x0, x1), make_float2(acc[0], acc[1]));
+              const float2 a23 = ffma2(make_float2(w4.z, w4.w), make_float2(x2, x3), make_float2(acc[2], acc[3]));
+              acc[0] = a01.x;
+              acc[1] = a01.y;
+              acc[2] = a23.x;
+              acc[3] = a23.y;
+            } else {
+              acc[0] = fmaf(w4.x, x0, acc[0]);
+              acc[1] = fmaf(w4.y, x1, acc[1]);
+              acc[2] = fmaf(w4.z, x2, acc[2]);
+              acc[3] = fmaf(w4.w, x3, acc[3]);
+            }
           }
         }
         float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
