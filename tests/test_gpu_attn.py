@@ -201,3 +201,35 @@ def test_inverse_rope_flag_is_validated(csa):
                             torch.full((1, 1, p.topk), -1, dtype=torch.int32, device=DEV),
                             torch.zeros(1, 128, 512, dtype=torch.bfloat16, device=DEV), 0, 128, None,
                             torch.zeros(64, device=DEV), out)
+
+
+def test_split_kv_slices_follow_the_workspace(csa):
+    """The split-KV form takes as many slices per query as the workspace
+    holds: a workspace for 2 slices (where the GPU alone would take 16), one
+    sized by csa_workspace_size, and one too small for any (the cluster form)
+    all give the oracle's result, and the split forms agree with each other
+    to fp32 summation order."""
+    n_cap, k, B = 4096, 512, 4
+    t = 4 * n_cap - 1
+    x = syn.decode_inputs(syn.Workload("split-ws", 71, "decode", B=B, t=t, topk=k, n_cap=n_cap))
+    p = csa.csa_default_params(topk=k)
+    g = torch.Generator().manual_seed(71)
+    idx = torch.stack([torch.sort(torch.randperm(n_cap, generator=g)[:k])[0] for _ in range(B)]).to(torch.int32)
+    idx = idx.view(B, 1, k)
+    slice_bytes = (64 * 512 + 2 * 64) * 4
+    full = csa.workspace(csa.CSA_OP_SPARSE_ATTN, p, B, 1, n_cap)
+    two = torch.empty(B * 2 * slice_bytes, dtype=torch.uint8, device=DEV)
+    small = torch.empty(B * slice_bytes, dtype=torch.uint8, device=DEV)
+    outs = {}
+    for name, ws in (("full", full), ("two", two), ("small", small)):
+        out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=DEV)
+        csa.csa_sparse_attn(p, B, 1, torch.full((B, 1), t, dtype=torch.int32, device=DEV), x["q"].to(DEV),
+                            x["kv"].to(DEV), n_cap, idx.to(DEV), x["swa"].to(DEV), 0, 128, None, x["sink"].to(DEV),
+                            out, None, ws)
+        assert csa.csa_check_status() == 0
+        outs[name] = out.float().cpu().numpy()
+    for b in (0, B - 1):
+        o, _ = oracle_ring(p, x["q"][b, 0], x["kv"][b], idx[b, 0].numpy(), x["swa"][b], x["sink"], t)
+        for name in outs:
+            assert_close(outs[name][b, 0], o, "%s b=%d" % (name, b))
+    np.testing.assert_allclose(outs["two"], outs["full"], rtol=2e-2, atol=2e-3)
