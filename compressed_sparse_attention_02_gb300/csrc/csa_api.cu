@@ -205,8 +205,8 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   uint8_t* wsb_blk = wsb + w.total;  // Full layer: the block scores' scratch
   float* scores = reinterpret_cast<float*>(wsb + w.scores_off);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + w.hist_off);
-  if (!zeroed && cudaMemsetAsync(hist, 0, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
-  if (pool && pool->out && cudaMemsetAsync(wsb_blk + wb.hist_off, 0, wb.zero_bytes, st) != cudaSuccess)
+  if (!zeroed && csa::launch_zero(hist, w.zero_bytes, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (pool && pool->out && csa::launch_zero(wsb_blk + wb.hist_off, wb.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
   // a call of its own (not inside a layer call) traces from its indexer on
   const bool own = traced && (pool || standalone);
@@ -724,7 +724,7 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
   // the top-k counters are cleared first, so that the kernels follow one
   // another directly (programmatic launches)
-  if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
+  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
   unsigned* status = status_ptr();
   if (!status) return CSA_ERR_CUDA;
@@ -784,7 +784,7 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   IndexWs w;
   if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
-  if (cudaMemsetAsync(static_cast<uint8_t*>(workspace) + w.hist_off, 0, w.zero_bytes, st) != cudaSuccess)
+  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
   trace(0, st);
   uint16_t* kv16 = p->kv_format ? nullptr : static_cast<uint16_t*>(kv_comp);

@@ -133,6 +133,9 @@ struct IndexArgs {
 };
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,
                                 cudaStream_t stream);
+// Zeroes `bytes` (a multiple of 4) at a 16-byte aligned device pointer, as a
+// kernel on the programmatic-launch chain.
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream);
 
 // ---- top-k -------------------------------------------------------------------------
 struct TopkArgs {

@@ -747,4 +747,32 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
                     b, c);
 }
 
+// Clears `bytes` (a multiple of 4, 16-byte aligned) at p: the indexer's and
+// the top-k's per-call counters.  A kernel on the programmatic-launch chain
+// (it signals its dependents on entry and waits for its predecessor before
+// writing), so that the launches around it still overlap, which a memset node
+// would not allow.
+namespace {
+__global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t words) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t n4 = words / 4;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint4* p4 = reinterpret_cast<uint4*>(p);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += step)
+    p4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = n4 * 4 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words; i += step)
+    p[i] = 0u;
+}
+}  // namespace
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream) {
+  const int64_t words = static_cast<int64_t>(bytes / 4);
+  if (words <= 0) return cudaSuccess;
+  int64_t blocks = (words / 4 + 255) / 256;
+  blocks = blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks);
+  return launch_pdl(zero_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, static_cast<uint32_t*>(p),
+                    words);
+}
+
 }  // namespace csa
