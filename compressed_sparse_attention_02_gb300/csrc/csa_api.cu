@@ -109,8 +109,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch of the indexer and top-k: scores [rows][score_ld] fp32; per row the
 // counts of the 2048 score-key first digits, the crossing-digit candidate
-// count and the count of CTAs done with the row (contiguous, so one memset
-// clears them); the two position bitmaps; the candidate keys and positions.
+// count and the count of CTAs done with the row (contiguous, so one zeroing
+// launch clears them); the two position bitmaps; the candidate keys and positions.
 bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
   if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
   w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 8));  // 16-byte rows as bf16 too
