@@ -242,6 +242,7 @@ def run_ours(args, rank, world, local_rank):
         result.update(stage_profile(csa, torch, w, x, p, B, step, kv, out, idx, lse, ws, stream, args))
         result["attn"].update(attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream))
         result["prefill"] = prefill_profile(csa, torch, dev)
+        result["compressor"] = compressor_profile(csa, torch, dev)
         result["hierarchical"] = [hierarchical_profile(csa, torch, dev, cfg) for cfg in (2, 3)]
         result["hca"] = hca_profile(csa, torch, dev)
         result["fp4_cache"] = fp4_profile(csa, torch, dev, x, w)
@@ -394,6 +395,35 @@ def prefill_profile(csa, torch, dev):
     res["indexer_keys"] = {"entries": B * n_new, "ms": kms, "gbs": kbytes / (kms * 1e-3) / 1e9,
                            "hbm_frac": kbytes / (kms * 1e-3) / 1e9 / hbm}
     del x, xk, kv, kI, idx, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def compressor_profile(csa, torch, dev):
+    """The overlapped compressor in bulk form on v4flash-decode-b32-8k: 32
+    sequences of 8192 tokens into 2048 entries each.  Algorithmic bytes: every
+    input row read once (C^a, Z^a, C^b, Z^b: 4 x 8192 rows of 1 KiB per
+    sequence, 1 GiB in all, larger than L2) and every entry written once."""
+    import synthetic as syn
+    hbm, _, _ = peaks()
+    w = syn.WORKLOADS[1]
+    B, T, m = w.B, w.t + 1, w.m
+    n_new = T // m
+    rows = syn.compressor_rows(w.config, B, T, device=dev)
+    sp = syn.shared_params(w.config, m, dev)
+    kv = torch.empty(B, n_new, 512, dtype=torch.bfloat16, device=dev)
+    p = csa.csa_default_params(topk=w.topk, m=m)
+
+    def call(i):
+        csa.csa_compress(p, B, n_new, 0, rows["Ca"], rows["Za"], rows["Cb"], rows["Zb"], None, None, sp["Ba"],
+                         sp["Bb"], sp["rms_w"], kv, n_new * 512)
+    ms = _ms_per_call(torch, call, 20, warm=3)
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the compressor section")
+    byts = B * (4 * T + n_new) * 1024
+    res = {"workload": w.name, "tokens": B * T, "entries": B * n_new, "ms": ms, "bytes": byts,
+           "gbs": byts / (ms * 1e-3) / 1e9, "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm}
+    del rows, kv
     torch.cuda.empty_cache()
     return res
 
