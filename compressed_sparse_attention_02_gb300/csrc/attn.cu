@@ -29,10 +29,7 @@
 // buffer, and then sums one channel slice over the cluster's buffers and
 // writes it.  Decode (few queries) splits so that about one CTA per SM runs;
 // every row is then gathered once.  Prefill runs one CTA per query.
-//
-// Before its first tile every CTA asks L2 for all of its rows (plain line
-// prefetches), so the HBM reads of the whole batch are in flight at once and
-// the tile gathers that follow mostly hit L2.
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -63,13 +60,6 @@ constexpr size_t kLutBytes = 256 * 4;  // FP4 rows: byte -> two bf16 E2M1 values
 constexpr size_t kSmemBytes = kLutBytes + 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
                               4 * kHeads * 4 + 2 * kMaxSplit * kHeads * 4 + 64;
 static_assert(kQBytes + kKVBytes == 192 * 1024, "the output exchange uses the Q and KV buffers");
-
-// Asks L2 to fetch one 1 KiB row: eight 128-byte lines, plain prefetches
-// (cheap to issue from every thread, unlike one bulk prefetch per row).
-__device__ __forceinline__ void prefetch_row_l2(const uint16_t* row) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c * 64) : "memory");
-}
 
 // Inverse partial RoPE of the output: channel chn's pair (D-R+2j, D-R+2j+1)
 // is turned by -t * theta^(-2j/R).  rope_angle gives (sin, cos) of t *
@@ -271,21 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return nullptr;
   };
-  // Put every row of the slice in flight towards L2 (an FP4 entry spans at
-  // most four 128-byte lines).
-  for (int j = r_lo + tid; j < r_hi; j += kThreads) {
-    const uint16_t* src = row_at(j);
-    if (!src) continue;
-    if (kFp4 && j >= n_swa) {
-      const uint8_t* e = reinterpret_cast<const uint8_t*>(src);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(e) : "memory");
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + 128) : "memory");
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + 256) : "memory");
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(e + kFp4Entry - 1) : "memory");
-    } else {
-      prefetch_row_l2(src);
-    }
-  }
   if constexpr (kFp4) lut[tid] = e2m1_pair_bf16(tid);  // kThreads == 256: one entry per thread
   tc_fence_before();
   __syncthreads();
