@@ -923,7 +923,8 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
     pinned host memory and its results read back: the step's queries, indexer
     queries and weights, positions, compressor staging rows, the new token's
     window row and the new entry's indexer key travel host -> device in one
-    packed copy, and the attention output and the selection travel back.
+    packed copy (the layer call's first kernel stores those two rows into the
+    caches), and the attention output and the selection travel back.
     The copies run on their own streams one step ahead of / behind the layer
     call (two staging buffers and two output buffers), as a serving loop
     would overlap them; the timed region spans every step's copies."""
@@ -988,11 +989,10 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
             stream.wait_event(in_ready[s_])
             if i >= 2:
                 stream.wait_event(out_free[s_])
-            x["swa"][:, slot].copy_(v["swa_row"], non_blocking=True)
-            x["kI"][:, entry].copy_(v["kI_row"], non_blocking=True)
-            csa.csa_layer_decode(p, B, v["q_pos"], v["ring_Ca"], v["ring_Za"], v["ring_Cb"], v["ring_Zb"], x["Ba"],
-                                 x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], v["qI"], v["wI"], v["q"], x["swa"],
-                                 x["sink"], idxs[s_], outs[s_], lse, ws)
+            csa.csa_layer_decode_append(p, B, v["q_pos"], v["swa_row"], v["kI_row"], v["ring_Ca"], v["ring_Za"],
+                                        v["ring_Cb"], v["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap,
+                                        x["kI"], v["qI"], v["wI"], v["q"], x["swa"], x["sink"], idxs[s_], outs[s_],
+                                        lse, ws)
             stage_free[s_].record(stream)
             out_ready[s_].record(stream)
 
@@ -1057,8 +1057,15 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
             with torch.cuda.stream(stream):
                 for _ in range(reps):
                     graph.replay()
-        res.update({"value": timed(replay, reps * G), "steps": reps * G,
-                    "launch": "CUDA graphs of %d steps (copies included), replayed" % G})
+        g_val = timed(replay, reps * G)
+        res["graph_value"] = g_val
+        # a serving loop takes the faster of the two launch forms
+        if g_val >= eager:
+            res.update({"value": g_val, "steps": reps * G,
+                        "launch": "CUDA graphs of %d steps (copies included), replayed" % G})
+        else:
+            res.update({"value": eager, "steps": n,
+                        "launch": "eager stream launches (faster here than CUDA graphs of %d steps)" % G})
     else:
         res.update({"value": eager, "steps": n, "launch": "eager: " + why})
     if csa.csa_check_status() != 0:

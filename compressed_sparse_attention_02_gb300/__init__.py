@@ -86,8 +86,10 @@ _lib.csa_reindex_topk.restype = ctypes.c_int
 _lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp,
                                  _vp, _sz, _vp]
 _lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
+_lib.csa_layer_decode_append.argtypes = [_P, _i32, _vp] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
 _lib.csa_layer_prefill.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
-for _f in ("csa_compress", "csa_compress_indexer_keys", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode", "csa_layer_prefill"):
+for _f in ("csa_compress", "csa_compress_indexer_keys", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode",
+           "csa_layer_decode_append", "csa_layer_prefill"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.csa_set_trace_events.argtypes = [ctypes.POINTER(_vp), _i32]
 _lib.csa_set_trace_events.restype = ctypes.c_int
@@ -247,6 +249,16 @@ def csa_layer_decode(params, B, q_pos, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, B
                                  n_cap, _ptr(kI), _ptr(qI), _ptr(wI), _ptr(q), _ptr(swa_ring), _ptr(sink),
                                  _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
                                  _stream(stream)), "csa_layer_decode")
+
+
+def csa_layer_decode_append(params, B, q_pos, swa_new, kI_new, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w,
+                            kv_comp, n_cap, kI, qI, wI, q, swa_ring, sink, idx_out, out, lse, ws, stream=None):
+    _check(_lib.csa_layer_decode_append(ctypes.byref(params), B, _ptr(q_pos), _ptr(swa_new), _ptr(kI_new),
+                                        _ptr(ring_Ca), _ptr(ring_Za), _ptr(ring_Cb), _ptr(ring_Zb), _ptr(Ba),
+                                        _ptr(Bb), _ptr(rms_w), _ptr(kv_comp), n_cap, _ptr(kI), _ptr(qI), _ptr(wI),
+                                        _ptr(q), _ptr(swa_ring), _ptr(sink), _ptr(idx_out), _ptr(out), _ptr(lse),
+                                        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "csa_layer_decode_append")
 
 
 def csa_layer_prefill(params, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI,

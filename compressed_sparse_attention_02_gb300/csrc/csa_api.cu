@@ -702,12 +702,16 @@ csa_status csa_sparse_attn(const csa_params* p, int32_t B, int32_t Q, const int3
                   static_cast<cudaStream_t>(stream), idx == nullptr, workspace, workspace_bytes);
 }
 
-csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
-                            const uint16_t* ring_Za, const uint16_t* ring_Cb, const uint16_t* ring_Zb,
-                            const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp,
-                            int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
-                            const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
-                            uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// One decode step; with `append`, the step's first kernel also writes the new
+// window row and indexer key into the caches.
+csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
+                        const uint16_t* ring_Za, const uint16_t* ring_Cb, const uint16_t* ring_Zb,
+                        const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp,
+                        int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
+                        const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
+                        uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                        const csa::DecodeAppend* append) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
@@ -724,7 +728,7 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
   // the top-k counters are cleared first, so that the kernels follow one
   // another directly (programmatic launches)
-  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st) != cudaSuccess)
+  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st, append) != cudaSuccess)
     return CSA_ERR_CUDA;
   unsigned* status = status_ptr();
   if (!status) return CSA_ERR_CUDA;
@@ -755,6 +759,42 @@ csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos
                workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
   trace(4, st);
   return s;
+}
+}  // namespace
+
+csa_status csa_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* ring_Ca,
+                            const uint16_t* ring_Za, const uint16_t* ring_Cb, const uint16_t* ring_Zb,
+                            const uint16_t* Ba, const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp,
+                            int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
+                            const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
+                            uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return layer_decode(p, B, q_pos, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI, wI, q,
+                      swa_ring, sink, idx_out, out, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+csa_status csa_layer_decode_append(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* swa_new,
+                                   const uint8_t* kI_new, const uint16_t* ring_Ca, const uint16_t* ring_Za,
+                                   const uint16_t* ring_Cb, const uint16_t* ring_Zb, const uint16_t* Ba,
+                                   const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp, int64_t n_cap,
+                                   uint8_t* kI, const uint8_t* qI, const uint16_t* wI, const uint16_t* q,
+                                   uint16_t* swa_ring, const float* sink, int32_t* idx_out, uint16_t* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (!ok_ptr(swa_new) || !ok_opt(kI_new)) return CSA_ERR_INVALID_ARG;
+  if (kI_new && p->index_format != 0) return CSA_ERR_UNSUPPORTED;  // E4M3 index keys only
+  csa::DecodeAppend ap = {};
+  ap.q_pos = q_pos;
+  ap.B = B;
+  ap.W = p->swa_window;
+  ap.m = p->m;
+  ap.swa_new = swa_new;
+  ap.swa_ring = swa_ring;
+  ap.kI_new = kI_new;
+  ap.kI = kI;
+  ap.n_cap = n_cap;
+  return layer_decode(p, B, q_pos, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI, wI, q,
+                      swa_ring, sink, idx_out, out, lse, workspace, workspace_bytes, stream, &ap);
 }
 
 csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,

@@ -135,7 +135,21 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
                                 cudaStream_t stream);
 // Zeroes `bytes` (a multiple of 4) at a 16-byte aligned device pointer, as a
 // kernel on the programmatic-launch chain.
-cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream);
+// A decode step's new rows, written into the caches by the step's first
+// kernel (the counters' zeroing) so that they cost no launch of their own:
+// the window row of position t = q_pos[b] into ring slot t mod W, and, where
+// (t+1) mod m == 0, the indexer key of entry (t+1)/m - 1 (kI_new optional).
+// Sequences with t < 0 are skipped, and so is an entry past n_cap.
+struct DecodeAppend {
+  const int32_t* q_pos;
+  int B, W, m;
+  const uint16_t* swa_new;  // [B][kDim] bf16
+  uint16_t* swa_ring;       // [B][W][kDim] bf16
+  const uint8_t* kI_new;    // [B][kIdxDim] e4m3, or null
+  uint8_t* kI;              // [B][n_cap][kIdxDim] e4m3
+  int64_t n_cap;
+};
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append = nullptr);
 
 // ---- top-k -------------------------------------------------------------------------
 struct TopkArgs {

@@ -751,13 +751,35 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
 // the top-k's per-call counters.  A kernel on the programmatic-launch chain
 // (it signals its dependents on entry and waits for its predecessor before
 // writing), so that the launches around it still overlap, which a memset node
-// would not allow.
+// would not allow.  With a DecodeAppend, B more CTAs (one per sequence) write
+// the step's new window row and indexer key into the caches.
 namespace {
-__global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t words) {
+__global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t words, const int zero_blocks,
+                                                   const DecodeAppend ap) {
   pdl_launch_dependents();
   pdl_wait();
+  if (static_cast<int>(blockIdx.x) >= zero_blocks) {  // one CTA per sequence: its new rows
+    const int b = static_cast<int>(blockIdx.x) - zero_blocks;
+    const int64_t t = ap.q_pos[b];
+    if (t < 0) return;
+    const int c = threadIdx.x;
+    constexpr int kRowChunks = kDim * 2 / 16, kKeyChunks = kIdxDim / 16;
+    if (c < kRowChunks) {
+      const uint4* src = reinterpret_cast<const uint4*>(ap.swa_new + static_cast<int64_t>(b) * kDim);
+      uint4* dst = reinterpret_cast<uint4*>(ap.swa_ring + (static_cast<int64_t>(b) * ap.W + t % ap.W) * kDim);
+      dst[c] = src[c];
+    } else if (ap.kI_new && c < kRowChunks + kKeyChunks && (t + 1) % ap.m == 0) {
+      const int64_t i = (t + 1) / ap.m - 1;
+      if (i < ap.n_cap) {
+        const uint4* src = reinterpret_cast<const uint4*>(ap.kI_new + static_cast<int64_t>(b) * kIdxDim);
+        uint4* dst = reinterpret_cast<uint4*>(ap.kI + (static_cast<int64_t>(b) * ap.n_cap + i) * kIdxDim);
+        dst[c - kRowChunks] = src[c - kRowChunks];
+      }
+    }
+    return;
+  }
   const int64_t n4 = words / 4;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t step = static_cast<int64_t>(zero_blocks) * blockDim.x;
   uint4* p4 = reinterpret_cast<uint4*>(p);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += step)
     p4[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -766,13 +788,16 @@ __global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t wo
 }
 }  // namespace
 
-cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream) {
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append) {
   const int64_t words = static_cast<int64_t>(bytes / 4);
-  if (words <= 0) return cudaSuccess;
-  int64_t blocks = (words / 4 + 255) / 256;
-  blocks = blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks);
-  return launch_pdl(zero_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, static_cast<uint32_t*>(p),
-                    words);
+  const int rows = append ? append->B : 0;
+  if (words <= 0 && rows == 0) return cudaSuccess;
+  int64_t blocks = words > 0 ? (words / 4 + 255) / 256 : 0;
+  blocks = words <= 0 ? 0 : (blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks));
+  static_assert(kDim * 2 / 16 + kIdxDim / 16 <= 256, "one CTA copies a sequence's new rows");
+  return launch_pdl(zero_kernel, dim3(static_cast<unsigned>(blocks + rows)), dim3(256), 0, stream,
+                    static_cast<uint32_t*>(p), words, static_cast<int>(blocks),
+                    append ? *append : DecodeAppend{});
 }
 
 }  // namespace csa

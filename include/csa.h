@@ -503,6 +503,36 @@ csa_status csa_layer_decode(
     size_t workspace_bytes, void *stream);
 
 /*
+ * csa_layer_decode_append — csa_layer_decode whose first kernel also stores
+ * the step's new rows into the caches it then reads (a serving loop's
+ * per-step cache append, without launches of its own):
+ *
+ *   swa_new [B][512] bf16: the window row of position t = q_pos[b], stored
+ *           into swa_ring slot t mod W before the attention reads the ring;
+ *   kI_new  [B][128] e4m3, or NULL: where (t+1) % m == 0, the indexer key of
+ *           the entry completing at t, i = (t+1)/m - 1, stored into kI[b, i]
+ *           before the indexer reads it (other rows of kI_new are not read;
+ *           an i >= n_cap is not stored and is reported by step 1 as for
+ *           csa_layer_decode).
+ *
+ * Sequences with q_pos[b] < 0 store nothing.  swa_ring and kI are written,
+ * hence not const here; every other argument and the result are as for
+ * csa_layer_decode.  Errors: CSA_ERR_INVALID_ARG for a NULL or unaligned
+ * swa_new or an unaligned kI_new; CSA_ERR_UNSUPPORTED for kI_new with
+ * index_format 1 (FP4 index keys live in planes, see above).
+ */
+csa_status csa_layer_decode_append(
+    const csa_params *p, int32_t B, const int32_t *q_pos,
+    const uint16_t *swa_new, const uint8_t *kI_new,
+    const uint16_t *ring_Ca, const uint16_t *ring_Za, const uint16_t *ring_Cb,
+    const uint16_t *ring_Zb, const uint16_t *Ba, const uint16_t *Bb,
+    const uint16_t *rms_w, void *kv_comp, int64_t n_cap,
+    uint8_t *kI, const uint8_t *qI, const uint16_t *wI,
+    const uint16_t *q, uint16_t *swa_ring, const float *sink,
+    int32_t *idx_out, uint16_t *out, float *lse, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
  * csa_layer_prefill — one chunk of Q query tokens at positions pos0..pos0+Q-1
  * (pos0 a multiple of m, given on the host), causal per query.
  * [hca_csa] "在 SGLang 里的落点" (large-batch prefill has the decode

@@ -151,6 +151,23 @@ def test_block_sizes_and_single_stream_calls_validate(lib):
                                    None) == 0
 
 
+def test_layer_decode_append_argument_checks(lib):
+    """The append form refuses on the host, before any launch: swa_new missing
+    or misaligned, kI_new misaligned, kI_new with FP4 index keys."""
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    raw.csa_layer_decode_append.restype = ctypes.c_int
+    fake, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+
+    def call(p, swa_new, kI_new):
+        return raw.csa_layer_decode_append(ctypes.byref(p), 1, fake, swa_new, kI_new, *([fake] * 8),
+                                           ctypes.c_int64(4096), *([fake] * 9), fake, ctypes.c_size_t(1 << 30), None)
+    p = lib.csa_default_params()
+    assert call(p, None, fake) == 1
+    assert call(p, odd, fake) == 1
+    assert call(p, fake, odd) == 1
+    assert call(lib.csa_default_params(index_format=1), fake, fake) == 2
+
+
 def test_fp4_indexer_argument_checks(lib):
     """FP4 indexer rows: sizes of the layouts, and host-side refusals (no launch)."""
     assert lib.index_keys_fp4_bytes(2, 300) == 2 * (300 * 64 + 3 * 512)

@@ -77,6 +77,48 @@ def test_layer_decode_other_compression_ratios(csa, m, t):
         check_decode_seq(w, x, b, bits(x["kv"][b]), kv[b].float().cpu().numpy(), idx[b], out[b], lse[b])
 
 
+@pytest.mark.parametrize("t", [1023, 1022])
+def test_layer_decode_append_stores_the_new_rows(csa, t):
+    """csa_layer_decode_append: the new window row and the completing entry's
+    indexer key, stored by the step's first kernel, give the same step (bit
+    for bit) as storing them first and calling csa_layer_decode; the caches
+    hold them afterwards; a sequence at position -1 stores nothing; at
+    t = 1022 no entry completes and kI is left as it was."""
+    w = syn.Workload("decode-append", 0, "decode", B=3, t=t, topk=64, n_cap=400, m=4)
+    x = syn.decode_inputs(w, device=DEV)
+    x["q_pos"][2] = -1
+    p = csa.csa_default_params(topk=w.topk)
+    swa_new = x["swa"][:, 5].roll(1, dims=0).contiguous()   # bf16 rows unlike the slots they go to
+    kI_new = x["kI"][:, 17].view(torch.uint8).roll(1, dims=0).contiguous()  # valid e4m3 rows
+    ref = {k: x[k].clone() for k in ("kv", "swa", "kI")}
+    for b in range(2):
+        ref["swa"][b, t % w.W] = swa_new[b]
+        if (t + 1) % w.m == 0:
+            ref["kI"][b, (t + 1) // w.m - 1].view(torch.uint8).copy_(kI_new[b])
+    got = {k: x[k].clone() for k in ("kv", "swa", "kI")}
+    res = []
+    for form, c in (("plain", ref), ("append", got)):
+        idx = torch.empty(w.B, p.topk, dtype=torch.int32, device=DEV)
+        out = torch.empty(w.B, 64, 512, dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty(w.B, 64, dtype=torch.float32, device=DEV)
+        ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, w.B, 1, w.n_cap)
+        common = (x["Ba"], x["Bb"], x["rms_w"], c["kv"], w.n_cap, c["kI"], x["qI"], x["wI"], x["q"], c["swa"],
+                  x["sink"], idx, out, lse, ws)
+        rings = (x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"])
+        if form == "plain":
+            csa.csa_layer_decode(p, w.B, x["q_pos"], *rings, *common)
+        else:
+            csa.csa_layer_decode_append(p, w.B, x["q_pos"], swa_new, kI_new, *rings, *common)
+        st = csa.csa_check_status()
+        assert st == 0, csa.csa_status_string(st)
+        res.append((idx.cpu(), bits(out), lse.cpu()))
+    for k in ("kv", "swa", "kI"):
+        assert torch.equal(got[k].view(torch.uint8), ref[k].view(torch.uint8)), k
+    assert torch.equal(res[0][0], res[1][0])
+    assert np.array_equal(res[0][1], res[1][1])
+    assert torch.equal(res[0][2], res[1][2])
+
+
 def test_layer_decode_v4flash_cache_from_the_compressor(csa):
     """Batch 32 x 8192 tokens: the cache is built by the bulk compressor over
     the whole context, then one decode step at t = 8191 re-emits the last
