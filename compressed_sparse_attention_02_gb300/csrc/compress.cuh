@@ -121,9 +121,12 @@ __device__ __forceinline__ void norm_rope(const CompressArgs& a, const float (&x
 // (ring mode between block boundaries, or past the cache).  `red` holds one
 // float per warp of the group; sync() is a barrier over exactly the group's
 // threads.  Every thread of the group must call this with the same (b, e).
-template <int M, int CPT, int D, class Sync>
+// kStaged (bulk mode only): the entry's source rows are already in shared
+// memory at `stage` (block i's M rows of Z, its M rows of C, then block
+// i-1's Z and C rows; D channels each) and are read where they are used.
+template <int M, int CPT, int D, class Sync, bool kStaged = false>
 __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync,
-                                float (&y)[CPT], int64_t* entry) {
+                                float (&y)[CPT], int64_t* entry, const uint16_t* stage = nullptr) {
   using V = Bf16Vec<CPT>;
   using L = typename V::T;
   const int d0 = t * CPT;
@@ -174,19 +177,35 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
     }
   }
 
-  // Issue every load of the entry first (one memory round trip), then math.
-  L zr[2 * M], cr[2 * M], br[2 * M];
+  // Issue every load of the entry first (one memory round trip), then math;
+  // staged rows (and then the slot biases, cache-resident) are read at use.
+  L zr[kStaged ? 1 : 2 * M], cr[kStaged ? 1 : 2 * M], br[kStaged ? 1 : 2 * M];
+  if constexpr (!kStaged) {
 #pragma unroll
-  for (int r = 0; r < M; ++r) {
-    zr[r] = __ldg(reinterpret_cast<const L*>(za[r] + d0));
-    cr[r] = __ldg(reinterpret_cast<const L*>(ca[r] + d0));
-    br[r] = __ldg(reinterpret_cast<const L*>(a.Ba + r * D + d0));
-    if (has_prev) {
-      zr[M + r] = __ldg(reinterpret_cast<const L*>(zb[r] + d0));
-      cr[M + r] = __ldg(reinterpret_cast<const L*>(cb[r] + d0));
-      br[M + r] = __ldg(reinterpret_cast<const L*>(a.Bb + r * D + d0));
+    for (int r = 0; r < M; ++r) {
+      zr[r] = __ldg(reinterpret_cast<const L*>(za[r] + d0));
+      cr[r] = __ldg(reinterpret_cast<const L*>(ca[r] + d0));
+      br[r] = __ldg(reinterpret_cast<const L*>(a.Ba + r * D + d0));
+      if (has_prev) {
+        zr[M + r] = __ldg(reinterpret_cast<const L*>(zb[r] + d0));
+        cr[M + r] = __ldg(reinterpret_cast<const L*>(cb[r] + d0));
+        br[M + r] = __ldg(reinterpret_cast<const L*>(a.Bb + r * D + d0));
+      }
     }
   }
+  const auto z_at = [&](int r) -> L {
+    if constexpr (kStaged) return *reinterpret_cast<const L*>(stage + ((r < M ? 0 : 2 * M) + r % M) * D + d0);
+    else return zr[r];
+  };
+  const auto c_at = [&](int r) -> L {
+    if constexpr (kStaged) return *reinterpret_cast<const L*>(stage + ((r < M ? M : 3 * M) + r % M) * D + d0);
+    else return cr[r];
+  };
+  const auto b_at = [&](int r) -> L {
+    if constexpr (kStaged)
+      return __ldg(reinterpret_cast<const L*>((r < M ? a.Ba + r * D : a.Bb + (r - M) * D) + d0));
+    else return br[r];
+  };
   const L wr = __ldg(reinterpret_cast<const L*>(a.rms_w + d0));
   const int slots = has_prev ? 2 * M : M;  // block i-1 slots are absent for entry 0
 
@@ -198,8 +217,8 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
   for (int r = 0; r < 2 * M; ++r) {
     if (r < slots) {
       float z[CPT], bias[CPT];
-      V::unpack(zr[r], z);
-      V::unpack(br[r], bias);
+      V::unpack(z_at(r), z);
+      V::unpack(b_at(r), bias);
 #pragma unroll
       for (int j = 0; j < CPT; ++j) mx[j] = fmaxf(mx[j], z[j] + bias[j]);
     }
@@ -214,9 +233,9 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
   for (int r = 0; r < 2 * M; ++r) {
     if (r < slots) {
       float z[CPT], bias[CPT], c[CPT];
-      V::unpack(zr[r], z);
-      V::unpack(br[r], bias);
-      V::unpack(cr[r], c);
+      V::unpack(z_at(r), z);
+      V::unpack(b_at(r), bias);
+      V::unpack(c_at(r), c);
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
         const float w = exp2f((z[j] + bias[j] - mx[j]) * kLog2e);
@@ -238,12 +257,13 @@ __device__ bool compress_values(const CompressArgs& a, int b, int64_t e, int t, 
 // Entry of the main compressor (width 512), stored as bf16 into kv_out, or
 // (kv_fp4_out set) as the FP4 entry of its bf16 values: a 16-channel group
 // is 16/CPT adjacent threads, whose maximum is taken by shuffles.
-template <int M, int CPT, class Sync>
-__device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync) {
+template <int M, int CPT, class Sync, bool kStaged = false>
+__device__ void compress_entry(const CompressArgs& a, int b, int64_t e, int t, float* red, Sync sync,
+                               const uint16_t* stage = nullptr) {
   using V = Bf16Vec<CPT>;
   float y[CPT];
   int64_t i;
-  if (!compress_values<M, CPT, kDim>(a, b, e, t, red, sync, y, &i)) return;
+  if (!compress_values<M, CPT, kDim, Sync, kStaged>(a, b, e, t, red, sync, y, &i, stage)) return;
   if (!a.kv_fp4_out) {
     *reinterpret_cast<typename V::T*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + t * CPT) =
         V::pack(y);

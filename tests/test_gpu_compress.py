@@ -55,6 +55,22 @@ def test_chunk_after_previous_block_ragged_batch(csa):
         assert np.all(got[b, :entry0] == 0) and np.all(got[b, entry0 + n_new:] == 0)
 
 
+@pytest.mark.parametrize("m,entry0", [(4, 0), (4, 7), (8, 7), (1, 3)])
+def test_staged_form_from_2048_entries(csa, m, entry0):
+    """Launches of at least 2048 entries stage each entry's rows in shared
+    memory by bulk copies (fewer use the register form): every entry of two
+    sequences of 1100, with and without a previous block."""
+    B, n_new = 2, 1100
+    x = syn.compressor_rows(21 + m, B, m * n_new)
+    x.update({k: syn.shared_params(21 + m, m)[k] for k in ("Ba", "Bb", "rms_w")})
+    prev = syn.compressor_rows(31 + m, B, m, names=("Cb_prev", "Zb_prev")) if entry0 else None
+    p = csa.csa_default_params(m=m)
+    got = run_bulk(csa, p, x, B, n_new, entry0, prev, entry0 + n_new + 2)
+    for b in range(B):
+        assert_close(got[b, entry0:entry0 + n_new], oracle_bulk(x, b, n_new, entry0, prev, m=m), "b=%d" % b)
+        assert np.all(got[b, :entry0] == 0) and np.all(got[b, entry0 + n_new:] == 0)
+
+
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_other_ratios(csa, m):
     n_new = 9
