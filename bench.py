@@ -40,10 +40,11 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
-    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index"], default="decode",
+    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index", "compressor"], default="decode",
                     help="reindex: only the hierarchical indexer's Reindex layer on --workload (4 Full-layer "
                          "calls make the pools, then --warmup and --steps Reindex calls; for profiling); "
-                         "fp4_index: only the FP4 indexer section on --workload")
+                         "fp4_index: only the FP4 indexer section on --workload; compressor: only the bulk "
+                         "compressor section")
     return ap.parse_args()
 
 
@@ -1187,6 +1188,13 @@ def main():
             import compressed_sparse_attention_02_gb300 as csa
             print(json.dumps(index_fp4_profile(csa, torch, torch.device("cuda", 0), args.workload,
                                                n=max(args.steps, 1))), flush=True)
+        return
+    if args.section == "compressor":
+        if rank == 0:
+            import torch
+
+            import compressed_sparse_attention_02_gb300 as csa
+            print(json.dumps(compressor_profile(csa, torch, torch.device("cuda", 0))), flush=True)
         return
     if world > 1:
         import torch
