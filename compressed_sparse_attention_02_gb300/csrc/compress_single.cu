@@ -53,7 +53,7 @@ __device__ __forceinline__ void load_row(const uint16_t* C, const uint16_t* Z, c
 
 __device__ __forceinline__ void group0_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kGroupThreads * kRowGroups) compress_single_kernel(const CompressArgs a) {
+__global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single_kernel(const CompressArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float part[kRowGroups - 1][3][kDim];  // groups 1..3: max, sum, weighted sum
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kGroupThreads * kRowGroups) compress_single_ke
   float mx[8], den[8], num[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx[j] = -INFINITY, den[j] = 0.f, num[j] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int r = g; r < m; r += kRowGroups) {
     float logit[8], c[8];
     load_row(a.Ca + row0 + static_cast<int64_t>(r) * kDim, a.Za + row0 + static_cast<int64_t>(r) * kDim,
