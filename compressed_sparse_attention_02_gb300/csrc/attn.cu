@@ -644,15 +644,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // maximum M over the slices' reference maxima and the sink (log2 units), the
 // denominator 2^(sink - M) + sum_s l_s 2^(m_s - M), and the output
 // sum_s O_s 2^(m_s - M) / den (the merge the cluster does on chip).  One CTA
-// per (query, head): one warp reduces the slices' (max, sum), then thread c
-// loads channels 4c .. 4c+3 of every slice at once (independent loads) and
-// sums them; the inverse RoPE rotates its two channel pairs in place.
+// per (query, head): thread c loads channels 4c .. 4c+3 of every slice at
+// once (independent loads) while one warp reduces the slices' (max, sum),
+// then sums them; the inverse RoPE rotates its two channel pairs in place.  G is
+// a bound on gsplit (2, 4, 8 or 16), so that a launch with few slices keeps
+// few registers and many CTAs per SM.
+template <int G>
 __global__ void __launch_bounds__(kDim / 4) attn_combine_kernel(const AttnArgs a, const int gsplit) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float fs[kMaxGSplit];
+  __shared__ float fs[G];
   const int64_t row_q = blockIdx.x;
   const int h = blockIdx.y, tid = threadIdx.x;
+  // the slices' outputs do not depend on the factors: their loads go out first
+  const int c0 = 4 * tid;
+  float4 o[G];
+#pragma unroll
+  for (int s = 0; s < G; ++s)
+    if (s < gsplit) o[s] = *reinterpret_cast<const float4*>(a.part_o + ((row_q * gsplit + s) * kHeads + h) * kDim + c0);
   if (tid < 32) {
     const float* ml = a.part_ml + row_q * gsplit * 2 * kHeads;
     const float sk = a.sink[h] * kLog2e;
@@ -669,14 +678,9 @@ __global__ void __launch_bounds__(kDim / 4) attn_combine_kernel(const AttnArgs a
     if (tid == 0 && a.lse) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
   }
   __syncthreads();
-  const int c0 = 4 * tid;
-  float4 o[kMaxGSplit];
-#pragma unroll
-  for (int s = 0; s < kMaxGSplit; ++s)
-    if (s < gsplit) o[s] = *reinterpret_cast<const float4*>(a.part_o + ((row_q * gsplit + s) * kHeads + h) * kDim + c0);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < kMaxGSplit; ++s) {
+  for (int s = 0; s < G; ++s) {
     if (s < gsplit) {
       const float f = fs[s];
       acc[0] = fmaf(f, o[s].x, acc[0]);
@@ -782,8 +786,12 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
     e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,
                    stream, tm_q, a, 1, gsplit);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(queries), kHeads), dim3(kDim / 4), 0, stream, a,
-                      gsplit);
+    const dim3 grid(static_cast<unsigned>(queries), kHeads), block(kDim / 4);
+    static_assert(kMaxGSplit == 16, "the merge kernel is instantiated for bounds up to 16");
+    if (gsplit <= 2) return launch_pdl(attn_combine_kernel<2>, grid, block, 0, stream, a, gsplit);
+    if (gsplit <= 4) return launch_pdl(attn_combine_kernel<4>, grid, block, 0, stream, a, gsplit);
+    if (gsplit <= 8) return launch_pdl(attn_combine_kernel<8>, grid, block, 0, stream, a, gsplit);
+    return launch_pdl(attn_combine_kernel<16>, grid, block, 0, stream, a, gsplit);
   }
   const int split = choose_split(queries, sms, cluster_max);
   return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
