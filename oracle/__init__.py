@@ -471,8 +471,9 @@ def inverse_rope(o, t, *, rope_dim=64, theta=1e4) -> np.ndarray:
 
 
 def window_positions(t: int, W: int) -> np.ndarray:
-    """Raw window of the query at t: positions max(0, t-W+1) .. t, the current
-    token included (reading recorded in the design doc)."""
+    """Raw window of the query at t: positions max(0, t-W+1) .. t.  The pages
+    do not say whether the window holds the current token; it is read as
+    included (W positions ending at t)."""
     return np.arange(max(0, t - W + 1), t + 1, dtype=np.int64)
 
 
