@@ -77,13 +77,14 @@ def test_layer_decode_other_compression_ratios(csa, m, t):
         check_decode_seq(w, x, b, bits(x["kv"][b]), kv[b].float().cpu().numpy(), idx[b], out[b], lse[b])
 
 
-@pytest.mark.parametrize("t", [1023, 1022])
-def test_layer_decode_append_stores_the_new_rows(csa, t):
+@pytest.mark.parametrize("t,with_key", [(1023, True), (1022, True), (1023, False)])
+def test_layer_decode_append_stores_the_new_rows(csa, t, with_key):
     """csa_layer_decode_append: the new window row and the completing entry's
     indexer key, stored by the step's first kernel, give the same step (bit
     for bit) as storing them first and calling csa_layer_decode; the caches
     hold them afterwards; a sequence at position -1 stores nothing; at
-    t = 1022 no entry completes and kI is left as it was."""
+    t = 1022 no entry completes and kI is left as it was; without kI_new only
+    the window row is stored."""
     w = syn.Workload("decode-append", 0, "decode", B=3, t=t, topk=64, n_cap=400, m=4)
     x = syn.decode_inputs(w, device=DEV)
     x["q_pos"][2] = -1
@@ -93,7 +94,7 @@ def test_layer_decode_append_stores_the_new_rows(csa, t):
     ref = {k: x[k].clone() for k in ("kv", "swa", "kI")}
     for b in range(2):
         ref["swa"][b, t % w.W] = swa_new[b]
-        if (t + 1) % w.m == 0:
+        if with_key and (t + 1) % w.m == 0:
             ref["kI"][b, (t + 1) // w.m - 1].view(torch.uint8).copy_(kI_new[b])
     got = {k: x[k].clone() for k in ("kv", "swa", "kI")}
     res = []
@@ -108,7 +109,7 @@ def test_layer_decode_append_stores_the_new_rows(csa, t):
         if form == "plain":
             csa.csa_layer_decode(p, w.B, x["q_pos"], *rings, *common)
         else:
-            csa.csa_layer_decode_append(p, w.B, x["q_pos"], swa_new, kI_new, *rings, *common)
+            csa.csa_layer_decode_append(p, w.B, x["q_pos"], swa_new, kI_new if with_key else None, *rings, *common)
         st = csa.csa_check_status()
         assert st == 0, csa.csa_status_string(st)
         res.append((idx.cpu(), bits(out), lse.cpu()))
