@@ -75,8 +75,8 @@ typedef struct {
                            by the query position (see csa_sparse_attn); 0    */
   int32_t kv_format;  /* compressed cache entries: 0 bf16 (512 x 2 B), 1 FP4
                          (CSA_FP4_ENTRY_BYTES, see csa_quantize_kv_fp4).
-                         csa_layer_decode / csa_layer_prefill read and
-                         write their kv_comp in this format (the compressor
+                         csa_layer_decode(_append) / csa_layer_prefill read
+                         and write their kv_comp in this format (the compressor
                          stores the FP4 entry of its bf16 values);
                          csa_compress and the single-stream calls write
                          bf16 only                                       */
