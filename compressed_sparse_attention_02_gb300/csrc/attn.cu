@@ -5,30 +5,48 @@
 // 预算检索" §9.5–9.6; flash-style running max / running sum with a fused sink
 // ("DeepSeek-V4 CSA/HCA 与 DeepSeek-V4.1 CSA2" §19.3).
 //
-// A query's rows are shared by `split` CTAs (1, 2, 4 or 8; a thread-block
-// cluster when above 1), each holding all 64 heads and a contiguous slice of
-// the query's row set.  The 64 heads share every K=V row, so both products
-// run with the gathered rows on the MMA's M side:
+// A query's rows are shared by `split` CTAs (1, 2 or 4; a thread-block
+// cluster when above 1) or `gsplit` CTAs (split-KV, merged by a second
+// kernel), each holding all 64 heads and a contiguous slice of the query's
+// row set.  The 64 heads share every K=V row, so both products run with the
+// gathered rows on the MMA's M side (M = 128: an N = 64 product costs the
+// same ~52 clocks at M = 64 as at M = 128, so smaller tiles would double the
+// first product's cost):
 //   S^T[row, head]  = KV_tile[128 x 512] . Q^T[512 x 64]   (K-major A and B)
 //   O^T[ch, head]  += V^T[512 x 128] . P^T[128 x 64]       (MN-major A and B)
-// The same 128-byte-swizzled KV tile in shared memory serves as the K-major A
-// operand of the first product and the MN-major A operand of the second.  S^T
-// (64 TMEM columns) and O^T (4 x 64 columns, one per 128-channel block) live in
-// TMEM.  Two warps share each TMEM lane quadrant (32 tile rows) and split the
-// heads between them: a thread owns one tile row and 32 heads, reads their
-// logits with one tcgen05.ld, and per-head maxima and sums over rows use a
-// warp reduce-scatter plus a 4-quadrant combine in shared memory.  The
-// reference maximum only moves when a tile exceeds it by more than 2^8, so
-// O^T is rarely rescaled; the final division uses the same reference, so the
-// result does not depend on when it moved.
+// The same 128-byte-swizzled KV tile in shared memory is the K-major A
+// operand of the first product and the MN-major A operand of the second.
+// S^T (64 TMEM columns) and O^T (4 x 64 columns, one per 128-channel block)
+// live in TMEM.
+//
+// The CTA is warp-specialised and pipelined within its one KV buffer (the
+// 64 KiB Q tile and a 128 KiB tile leave no room for a second):
+//   warp 8 (one thread) issues the MMAs: S of a tile granule by granule (a
+//     granule is a 128-channel quarter of the tile) as each lands, then,
+//     once P is written, O one 128-channel block at a time, committing each
+//     block to its own barrier;
+//   warps 0-7 gather the next tile's granule g into the buffer as soon as
+//     O has finished with channel block g (16-byte cp.async per row piece,
+//     or, for a tile of 128 consecutive present rows of the window buffer or
+//     of a dense cache run, two TMA boxes), so the gather overlaps the O
+//     product and the next S product overlaps the gather; then they run the
+//     softmax of the tile: a thread owns one tile row (its TMEM lane) and 32
+//     heads.  The reference maximum of a head moves only when a logit
+//     exceeds it by more than 2^8, found by a barrier OR over the threads'
+//     checks; only then are the per-head tile maxima reduced across rows and
+//     O^T rescaled.  Row sums are kept per thread and reduced once after the
+//     last tile.  The final division uses the same reference, so the result
+//     does not depend on when it moved.
+// Every wait is bounded; a wait that gives up raises a CTA-wide abort flag
+// that ends every other wait, so all roles leave their loops together.
 //
 // With split > 1 each CTA ends with its slice's (O^T, reference max, sum) per
 // head.  The cluster combines them through distributed shared memory: every
 // CTA reads all CTAs' maxima and sums, scales its own O^T by its share of the
 // joint softmax (sink included once), stages it as fp32 in its (now free) KV
 // buffer, and then sums one channel slice over the cluster's buffers and
-// writes it.  Decode (few queries) splits so that about one CTA per SM runs;
-// every row is then gathered once.  Prefill runs one CTA per query.
+// writes it.  With gsplit > 1 the slices' raw O^T and (max, sum) go to the
+// workspace and attn_combine_kernel merges them.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,11 +58,16 @@
 namespace csa {
 namespace {
 
-constexpr int kThreads = 256;  // 8 warps: two per TMEM lane quadrant
+constexpr int kWorkers = 256;             // warps 0-7: gather, softmax, epilogue
+constexpr int kMmaWarp = kWorkers / 32;   // warp 8: TMA of Q and MMA issue
+constexpr int kThreads = kWorkers + 32;
+constexpr uint32_t kBarWorkers = 1;       // named barrier over the workers
 constexpr int kTileRows = 128;
+constexpr int kGranules = 4;              // 128-channel quarters of a tile
 constexpr uint32_t kKVBytes = kTileRows * kDim * 2;       // 128 KiB: [8 blocks][128 rows][128 B]
 constexpr uint32_t kPBytes = kTileRows * kHeads * 2;      // 16 KiB: [128 rows][64 heads]
 constexpr uint32_t kKVBlock = kTileRows * 128;            // 16 KiB per 64-channel block of KV
+constexpr uint32_t kGranuleBytes = 2 * kKVBlock;          // 32 KiB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 64;                            // O^T columns start here
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,14 +75,18 @@ constexpr float kRescaleSlack = 8.0f;                     // log2 units
 
 constexpr uint32_t kQBytes = kHeads * kDim * 2;           // 64 KiB: [8 blocks][64 heads][128 B]
 constexpr uint32_t kQBlock = kHeads * 128;                // 8 KiB per 64-channel block of Q
-constexpr int HW = kHeads / 2;                            // heads per warp (two warps share a TMEM quadrant)
+constexpr int HW = kHeads / 2;                            // heads per worker warp (two share a TMEM quadrant)
 constexpr int kMaxSplit = 4;  // the exchange below needs 2*(split-1)/split of 192 KiB
 static_assert(kKVBytes == kHeads * kDim * 4, "the KV buffer stages the fp32 partial output");
-
-constexpr size_t kLutBytes = 256 * 4;  // FP4 rows: byte -> two bf16 E2M1 values
-constexpr size_t kSmemBytes = kLutBytes + 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + kTileRows * 8 + 4 * kHeads * 4 +
-                              4 * kHeads * 4 + 2 * kMaxSplit * kHeads * 4 + 64;
 static_assert(kQBytes + kKVBytes == 192 * 1024, "the output exchange uses the Q and KV buffers");
+
+// How a tile's rows reach shared memory.
+enum : int { kTileGather = 0, kTileTmaWindow = 1, kTileTmaEntries = 2 };
+
+constexpr int kNumBars = 5 + 3 * kGranules;
+constexpr size_t kLutBytes = 256 * 4;  // FP4 rows: byte -> two bf16 E2M1 values
+constexpr size_t kSmemBytes = 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4 + 4 * kHeads * 4 +
+                              4 * kHeads * 4 + 2 * kMaxSplit * kHeads * 4 + kNumBars * 8 + 16 + kLutBytes;
 
 // Inverse partial RoPE of the output: channel chn's pair (D-R+2j, D-R+2j+1)
 // is turned by -t * theta^(-2j/R).  rope_angle gives (sin, cos) of t *
@@ -96,6 +123,21 @@ __device__ __forceinline__ __nv_bfloat162 e4m3_bf16x2(uint32_t code) {
   return __floats2bfloat162_rn(f, f);
 }
 
+// bf16 bits of x rounded to nearest, ties to even, by integer arithmetic
+// (the conversion instruction is slow here; x finite or NaN, which stays NaN).
+__device__ __forceinline__ uint32_t bf16_bits_rn(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t r = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC0u : r;
+}
+
+// 2^x (MUFU; subnormal results flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
@@ -121,34 +163,61 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
   }
 }
 
+// A bounded wait that also ends when another thread of the CTA has raised
+// the abort flag; a wait that runs out records kErrTimeout and raises it.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_error(status, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // kFp4: the compressed rows are FP4 entries (a.kv_fp4); a template
 // argument, so that the bf16 kernel carries none of that code.
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a, const int split,
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_swa,
+                       const __grid_constant__ CUtensorMap tm_kv, const AttnArgs a, const int split,
                        const int gsplit) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (offset from smem_raw, not an integer round trip: the pointers keep the
+  // shared address space, so their accesses are shared-memory instructions)
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* q_s = base;                                          // [8 blocks][64 heads][128 B]
   uint8_t* kv_s = q_s + kQBytes;                                // [8 blocks][128 rows][128 B]
   uint8_t* p_s = kv_s + kKVBytes;                               // [128 rows][64 heads] bf16
   int32_t* sel_s = reinterpret_cast<int32_t*>(p_s + kPBytes);
-  const uint16_t** row_src = reinterpret_cast<const uint16_t**>(sel_s + kMaxTopk);  // [128]
-  float* red_s = reinterpret_cast<float*>(row_src + kTileRows);  // [4 row quadrants][64]
-  float* m_ref = red_s + 4 * kHeads;                             // running reference max (log2 units)
-  float* l_sum = m_ref + kHeads;                                 // running denominator
-  float* alpha = l_sum + kHeads;                                 // per-tile rescale factor
-  float* fin = alpha + kHeads;                                   // final per-head output scale
+  float* red_s = reinterpret_cast<float*>(sel_s + kMaxTopk);    // [4 row quadrants][64]
+  float* m_ref = red_s + 4 * kHeads;                            // running reference max (log2 units)
+  float* l_sum = m_ref + kHeads;                                // the denominator after the last tile
+  float* alpha = l_sum + kHeads;                                // per-head rescale factor
+  float* fin = alpha + kHeads;                                  // the sink logit
   float* ml_s = fin + kHeads;  // [split][2][64]: every slice's reference max and sum (split > 1)
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(ml_s + 2 * kMaxSplit * kHeads);
-  uint64_t* recv_bar = mma_bar + 1;  // incoming output slices (split > 1)
-  uint64_t* q_full = recv_bar + 1;   // the Q tile (TMA)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale
-  uint32_t* lut = reinterpret_cast<uint32_t*>(flags + 4);        // [256] (FP4 rows)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ml_s + 2 * kMaxSplit * kHeads);
+  uint64_t* q_full = bars;          // the Q tile (TMA)
+  uint64_t* recv_bar = bars + 1;    // incoming output slices (split > 1)
+  uint64_t* s_full = bars + 2;      // S of the tile is in TMEM (MMA commit)
+  uint64_t* p_full = bars + 3;      // P of the tile is written (every worker)
+  uint64_t* drain_bar = bars + 4;   // MMAs in flight when a wait gave up
+  uint64_t* landed = bars + 5;      // [4] granule gathered by the workers (every worker)
+  uint64_t* tma_bar = landed + kGranules;  // [4] granule loaded by TMA (bytes)
+  uint64_t* o_done = tma_bar + kGranules;  // [4] O has read channel block g (MMA commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);            // [0] n_sel, [1] rescale, [2] abort
+  uint32_t* lut = reinterpret_cast<uint32_t*>(flags + 3);        // [256] (FP4 rows)
+  volatile int* abort_flag = flags + 2;
 
   pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool worker = tid < kWorkers;
   if (split > 1) {
     if (tid == 0) {  // expects the (split-1) output slices the peers will send
       mbar_init(recv_bar, 1);
@@ -160,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   pdl_wait();  // before any global access and before TMEM is taken
   const int quad = warp & 3;         // TMEM lane quadrant == 32 tile rows
-  const int hw0 = (warp >> 2) * HW;  // first head of this warp
+  const int hw0 = (warp >> 2) * HW;  // first head of this worker warp
   // the query's row set is cut into `split` slices combined in the cluster,
   // or `gsplit` slices combined by attn_combine_kernel (one of them is 1)
   const int slices = split > 1 ? split : gsplit;
@@ -170,18 +239,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row_q = static_cast<int64_t>(b) * a.Q + qi;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + qi;
 
-  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
-    mbar_init(mma_bar, 1);
     mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kWorkers);
+    mbar_init(drain_bar, 1);
+    for (int g = 0; g < kGranules; ++g) {
+      mbar_init(landed + g, kWorkers);
+      mbar_init(tma_bar + g, 1);
+      mbar_init(o_done + g, 1);
+    }
     fence_mbar_init();
     flags[1] = 0;
-    // Q tile: 8 boxes of [64 heads][64 channels] into [8 blocks][64 heads][128 B], swizzled
-    prefetch_tensormap(&tm_q);
-    mbar_arrive_expect_tx(q_full, kHeads * kDim * 2);
-#pragma unroll
-    for (int blk = 0; blk < 8; ++blk)
-      tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
+    flags[2] = 0;
   }
   if (tid < kHeads) {
     m_ref[tid] = -INFINITY;
@@ -192,11 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
   const uint16_t* kv_b = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
   const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
+  const int64_t swa_first = t - n_swa + 1;  // position of window row 0
+  const int slot0 = a.swa_mode == 0 ? static_cast<int>(swa_first % a.W) : 0;  // its ring slot
   // Address of window row j (0 <= j < n_swa), null if the window buffer lacks it.
   auto swa_row = [&](int j) -> const uint16_t* {
-    const int64_t u = t - n_swa + 1 + j;  // window position
-    if (a.swa_mode == 0) return a.swa + (static_cast<int64_t>(b) * a.W + u % a.W) * kDim;
-    const int64_t rr = u - swa_pos0;
+    if (a.swa_mode == 0) {
+      const int slot = slot0 + j < a.W ? slot0 + j : slot0 + j - a.W;  // j < n_swa <= W
+      return a.swa + (static_cast<int64_t>(b) * a.W + slot) * kDim;
+    }
+    const int64_t rr = swa_first + j - swa_pos0;
     if (rr >= 0 && rr < a.swa_len) return a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
     return nullptr;
   };
@@ -261,223 +336,354 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return nullptr;
   };
-  if constexpr (kFp4) lut[tid] = e2m1_pair_bf16(tid);  // kThreads == 256: one entry per thread
+  // Tile j's 128 rows by TMA when they are all present and consecutive in
+  // one buffer: the whole window (linear buffer, or the W = 128 ring, whose
+  // slots then hold exactly the window, in slot order, which the softmax
+  // does not see), or a run of consecutive entries of a dense (bf16) cache.
+  // Returns the mode and the TMA row coordinate.
+  auto tile_mode = [&](int j, int32_t* y) -> int {
+    const int r0 = r_lo + j * kTileRows;
+    if (r0 + kTileRows > r_hi) return kTileGather;
+    if (r0 + kTileRows <= n_swa) {
+      if (!a.tma_swa) return kTileGather;
+      if (a.swa_mode == 0) {
+        *y = 0;
+        return a.W == kTileRows && n_swa == kTileRows ? kTileTmaWindow : kTileGather;
+      }
+      const int64_t rr0 = swa_first + r0 - swa_pos0;
+      *y = static_cast<int32_t>(rr0);
+      return rr0 >= 0 && rr0 + kTileRows <= a.swa_len ? kTileTmaWindow : kTileGather;
+    }
+    if (!kFp4 && a.dense && a.tma_kv && r0 >= n_swa) {
+      *y = r0 - n_swa;
+      return kTileTmaEntries;
+    }
+    return kTileGather;
+  };
+  if constexpr (kFp4)
+    if (worker) lut[tid] = e2m1_pair_bf16(tid);  // one entry per worker
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tlane = tmem + (static_cast<uint32_t>(quad * 32) << 16);  // this warp's TMEM quadrant
 
-  constexpr uint32_t idesc_s = instr_desc(kTileRows, kHeads, 1, 1, 0, 0);  // bf16, K-major A/B
-  constexpr uint32_t idesc_o = instr_desc(kTileRows, kHeads, 1, 1, 1, 1);  // bf16, MN-major A/B
-  uint32_t phase = 0;
-  bool ok = true;
-
-  for (int tile = 0; tile < n_tiles && ok; ++tile) {
-    const int r0 = r_lo + tile * kTileRows;
-    // ---- resolve the tile's 128 row addresses
-    if (tid < kTileRows) {
-      const int j = r0 + tid;
-      const uint16_t* src = j < r_hi ? row_at(j) : nullptr;
-      if (!src && j < n_swa && j < r_hi) record_error(a.status, kErrIndexRange);
-      row_src[tid] = src;
-    }
-    __syncthreads();
-    // ---- gather 128 rows: thread tid copies 16-byte chunk (tid & 7) of
-    //      channel block (tid >> 3) & 7 of rows (tid >> 6) + 4i, so a warp
-    //      covers 512 contiguous bytes of a row
-    if constexpr (kFp4) {
-      // FP4 rows: 16 threads per row; thread `part` owns channels 32*part ..
-      // 32*part+31 (16 code bytes and 2 scales of the entry; 64 bytes =
-      // chunks 4*(part&1) .. +3 of channel block part>>1 of the tile), loads
-      // all of its rows first, then writes them as bf16 (value * scale is
-      // exact in bf16).  Window rows (bf16) take the same 64 bytes by cp.async.
-      const int part = tid & 15, pblk = part >> 1, c0 = (part & 1) * 4;
-      uint8_t* blk_s = kv_s + pblk * kKVBlock;
-      constexpr int kRowsPer = kTileRows * 16 / kThreads;  // 8
-      uint4 nib[kRowsPer];
-      uint32_t scl[kRowsPer];
-#pragma unroll
-      for (int i = 0; i < kRowsPer; ++i) {
-        const int r = (tid >> 4) + i * (kThreads / 16);
-        const uint8_t* e = reinterpret_cast<const uint8_t*>(row_src[r]);
-        const bool packed = e && r0 + r >= n_swa;
-        nib[i] = packed ? __ldg(reinterpret_cast<const uint4*>(e + 16 * part)) : make_uint4(0u, 0u, 0u, 0u);
-        scl[i] = packed ? __ldg(reinterpret_cast<const unsigned short*>(e + kDim / 2 + 2 * part)) : 0u;
-      }
-#pragma unroll
-      for (int i = 0; i < kRowsPer; ++i) {
-        const int r = (tid >> 4) + i * (kThreads / 16);
-        const uint16_t* src = row_src[r];
-        if (src && r0 + r < n_swa) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) cp_async_16(blk_s + swz(r, c0 + k), src + pblk * 64 + (c0 + k) * 8);
-          continue;
-        }
-        const __nv_bfloat162 s_lo = e4m3_bf16x2(scl[i] & 0xFFu), s_hi = e4m3_bf16x2(scl[i] >> 8);
-        const uint32_t w[4] = {nib[i].x, nib[i].y, nib[i].z, nib[i].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // chunk k: code bytes 4k .. 4k+3 (8 channels)
-          const __nv_bfloat162 sc = k < 2 ? s_lo : s_hi;
-          uint32_t o[4];
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const uint32_t v = lut[(w[k] >> (8 * bb)) & 0xFFu];
-            const __nv_bfloat162 x = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), sc);
-            o[bb] = *reinterpret_cast<const uint32_t*>(&x);
-          }
-          *reinterpret_cast<uint4*>(blk_s + swz(r, c0 + k)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-    } else {
-      const int pblk = (tid >> 3) & 7, pc = tid & 7;
-      uint8_t* blk_s = kv_s + pblk * kKVBlock;
-#pragma unroll
-      for (int i = 0; i < kTileRows * 64 / kThreads; ++i) {
-        const int r = (tid >> 6) + i * (kThreads / 64);
-        const uint16_t* src = row_src[r];
-        uint8_t* dst = blk_s + swz(r, pc);
-        if (src) cp_async_16(dst, src + pblk * 64 + pc * 8);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    cp_async_commit_wait_all();
-    fence_proxy_async_smem();
-    if (tile == 0 && !__syncthreads_and(mbar_wait(q_full, 0, a.status))) {  // Q has landed
-      ok = false;
-      break;
-    }
-    __syncthreads();
-
-    // ---- S^T = KV . Q^T  (32 MMAs of K = 16)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kvb = smem_u32(kv_s), qb = smem_u32(q_s);
+  if (warp == kMmaWarp) {
+    // ---------------- Q by TMA, then the MMAs of every tile ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      mbar_arrive_expect_tx(q_full, kQBytes);
 #pragma unroll
       for (int blk = 0; blk < 8; ++blk)
+        tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
+      // (waited for even without a tile: the epilogue may reuse the Q buffer)
+      bool ok = wait_or_abort(q_full, 0, abort_flag, a.status);
+      constexpr uint32_t idesc_s = instr_desc(kTileRows, kHeads, 1, 1, 0, 0);  // bf16, K-major A/B
+      constexpr uint32_t idesc_o = instr_desc(kTileRows, kHeads, 1, 1, 1, 1);  // bf16, MN-major A/B
+      const uint32_t kvb = smem_u32(kv_s), qb = smem_u32(q_s), pb = smem_u32(p_s);
+      int n_gather = 0, n_tma = 0;  // tiles so far of each kind: the phases of landed / tma_bar
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        int32_t y;
+        const bool tma = tile_mode(j, &y) != kTileGather;
+        const uint32_t par = static_cast<uint32_t>(tma ? n_tma++ : n_gather++) & 1u;
+        // S^T = KV . Q^T, granule by granule as each lands (8 MMAs of K = 16 each)
+        for (int g = 0; g < kGranules && ok; ++g) {
+          ok = wait_or_abort(tma ? tma_bar + g : landed + g, par, abort_flag, a.status);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = smem_desc(kvb + blk * kKVBlock + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(qb + blk * kQBlock + kk * 32, 16, 1024, kSwizzle128B);
-          mma_f16(tmem, ad, bd, idesc_s, (blk | kk) ? 1u : 0u);
+          for (int bb = 0; bb < 2; ++bb) {
+            const int blk = 2 * g + bb;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(kvb + blk * kKVBlock + kk * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bd = smem_desc(qb + blk * kQBlock + kk * 32, 16, 1024, kSwizzle128B);
+              mma_f16(tmem, ad, bd, idesc_s, (blk | kk) ? 1u : 0u);
+            }
+          }
         }
-      tc_commit(mma_bar);
+        if (!ok) break;
+        tc_commit(s_full);
+        ok = wait_or_abort(p_full, static_cast<uint32_t>(j) & 1u, abort_flag, a.status);
+        if (!ok) break;
+        tc_fence_after();
+        // O^T += V^T . P^T, one 128-channel block (8 K-steps of 16 rows) per commit
+#pragma unroll
+        for (int g = 0; g < kGranules; ++g) {
+#pragma unroll
+          for (int ks = 0; ks < kTileRows / 16; ++ks) {
+            const uint64_t ad = smem_desc(kvb + 2 * g * kKVBlock + ks * 2048, kKVBlock, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(pb + ks * 2048, kPBytes, 1024, kSwizzle128B);
+            mma_f16(tmem + kOCol + g * 64, ad, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(o_done + g);
+        }
+      }
+      if (!ok) {  // whatever was issued finishes before TMEM is released
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0, a.status);
+      }
     }
     __syncwarp();
-    // block-uniform: every thread waits, all leave together if one gave up
-    if (!__syncthreads_and(mbar_wait(mma_bar, phase, a.status))) { ok = false; break; }
-    phase ^= 1u;
-    tc_fence_after();
-
-    // ---- logits of this thread's row (its warp's 32 heads), per-head tile max
-    const int r = quad * 32 + lane;  // TMEM lane == tile row
-    const bool valid = row_src[r] != nullptr;
-    float l[HW];
-    {
-      uint32_t v[32];
-      tmem_ld32(tlane + hw0, v);
-      tmem_wait_ld();
+  } else {
+    // ---------------- workers: gather, softmax ----------------
+    const int r = quad * 32 + lane;  // TMEM lane == tile row of this thread's softmax
+    float lpart[HW];                 // this thread's partial row sums of its warp's heads
 #pragma unroll
-      for (int h = 0; h < 32; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
-    }
-    {
-      float tmp[HW];
-#pragma unroll
-      for (int h = 0; h < HW; ++h) tmp[h] = l[h];
-      warp_reduce_scatter<true>(tmp);
-      red_s[quad * kHeads + hw0 + lane] = tmp[0];
-    }
-    __syncthreads();
-    if (tid < kHeads) {
-      const float tmax = fmaxf(fmaxf(red_s[tid], red_s[kHeads + tid]),
-                               fmaxf(red_s[2 * kHeads + tid], red_s[3 * kHeads + tid]));
-      const float mo = m_ref[tid];
-      float al = 1.f;
-      if (tmax > mo + kRescaleSlack) {  // also taken on the first tile (mo = -inf)
-        al = (mo == -INFINITY) ? 0.f : exp2f(mo - tmax);
-        m_ref[tid] = tmax;
-        l_sum[tid] *= al;
-        if (tile > 0 && al != 1.f) flags[1] = 1;
+    for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
+    int tma_tiles = 0;           // thread 0: TMA tiles issued (the phase of tma_bar)
+    uint32_t tma_pending = 0u;   // thread 0: granules of its last TMA tile
+    // Tile j's rows into the KV buffer, granule g once O has read channel
+    // block g of the previous tile (wait_o, phase opar).  Gathered tiles:
+    // each worker then signals `landed[g]` once its own copies of g are done.
+    // A wait of the whole warp taken by its lane 0 alone (the others wait at
+    // the shuffle, not on the barrier's shared-memory word, which the tensor
+    // cores' operand reads share).
+    auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      bool w = true;
+      if (lane == 0) w = wait_or_abort(bar, par, abort_flag, a.status);
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    auto gather = [&](int j, bool wait_o, uint32_t opar) -> bool {
+      const int r0 = r_lo + j * kTileRows;
+      int32_t y = 0;
+      const int mode = tile_mode(j, &y);
+      if (mode != kTileGather) {
+        if (tid == 0) {
+          const CUtensorMap* map = mode == kTileTmaWindow ? &tm_swa : &tm_kv;
+          const uint32_t par = static_cast<uint32_t>(tma_tiles++) & 1u;
+          tma_pending = 0u;
+          for (int g = 0; g < kGranules; ++g) {
+            if (wait_o && !wait_or_abort(o_done + g, opar, abort_flag, a.status)) return false;
+            mbar_arrive_expect_tx(tma_bar + g, kGranuleBytes);
+            tma_load_3d(kv_s + 2 * g * kKVBlock, map, 2 * g * 64, y, b, tma_bar + g);
+            tma_load_3d(kv_s + (2 * g + 1) * kKVBlock, map, (2 * g + 1) * 64, y, b, tma_bar + g);
+            tma_pending = (tma_pending | (1u << g)) | (par << 8);
+          }
+        }
+        return true;
       }
-      alpha[tid] = al;
-    }
-    __syncthreads();
+      if constexpr (!kFp4) {
+        // thread tid copies 16-byte chunk tid & 7 of block 2g + ((tid >> 3) & 1)
+        // of rows (tid >> 4) + 16i: a half-warp covers a row's 256 bytes of the granule
+        const uint16_t* src[kTileRows / 16];
+#pragma unroll
+        for (int i = 0; i < kTileRows / 16; ++i) {
+          const int jr = r0 + (tid >> 4) + 16 * i;
+          src[i] = jr < r_hi ? row_at(jr) : nullptr;
+          if (!src[i] && jr < n_swa && jr < r_hi && (tid & 15) == 0) record_error(a.status, kErrIndexRange);
+        }
+        const int bb = (tid >> 3) & 1, c = tid & 7;
+        for (int g = 0; g < kGranules; ++g) {
+          if (wait_o && !warp_wait(o_done + g, opar)) {
+            cp_async_wait_pending(0);
+            return false;
+          }
+          const int blk = 2 * g + bb;
+          uint8_t* blk_s = kv_s + blk * kKVBlock;
+#pragma unroll
+          for (int i = 0; i < kTileRows / 16; ++i) {
+            uint8_t* dst = blk_s + swz((tid >> 4) + 16 * i, c);
+            if (src[i]) cp_async_16(dst, src[i] + blk * 64 + c * 8);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          cp_async_commit();
+          if (g > 0) {  // the previous granule's copies of this thread are done
+            cp_async_wait_pending(1);
+            fence_proxy_async_smem();
+            mbar_arrive(landed + g - 1);
+          }
+        }
+      } else {
+        // FP4 rows: thread tid takes rows (tid >> 2) + 64i and, in granule g,
+        // channels 32*part .. 32*part+31 with part = 4g + (tid & 3) (16 code
+        // bytes and 2 scales of the entry; chunks 4*(part&1) .. +3 of block
+        // part>>1).  All codes are loaded first, ahead of the O product; the
+        // bf16 values (value * scale is exact in bf16) are written once the
+        // granule is free.  Window rows (bf16) take the same 64 bytes by cp.async.
+        constexpr int kRowsPer = kTileRows * 4 / kWorkers;  // 2
+        const uint16_t* src[kRowsPer];
+        bool packed[kRowsPer];
+        uint4 nib[kGranules][kRowsPer];
+        uint32_t scl[kGranules][kRowsPer];
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+          const int jr = r0 + (tid >> 2) + 64 * i;
+          src[i] = jr < r_hi ? row_at(jr) : nullptr;
+          if (!src[i] && jr < n_swa && jr < r_hi && (tid & 3) == 0) record_error(a.status, kErrIndexRange);
+          packed[i] = src[i] && jr >= n_swa;
+          const uint8_t* e = reinterpret_cast<const uint8_t*>(src[i]);
+#pragma unroll
+          for (int g = 0; g < kGranules; ++g) {
+            const int part = 4 * g + (tid & 3);
+            nib[g][i] = packed[i] ? __ldg(reinterpret_cast<const uint4*>(e + 16 * part)) : make_uint4(0u, 0u, 0u, 0u);
+            scl[g][i] = packed[i] ? __ldg(reinterpret_cast<const unsigned short*>(e + kDim / 2 + 2 * part)) : 0u;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < kGranules; ++g) {
+          if (wait_o && !warp_wait(o_done + g, opar)) {
+            cp_async_wait_pending(0);
+            return false;
+          }
+          const int part = 4 * g + (tid & 3), pblk = part >> 1, c0 = (part & 1) * 4;
+          uint8_t* blk_s = kv_s + pblk * kKVBlock;
+#pragma unroll
+          for (int i = 0; i < kRowsPer; ++i) {
+            const int rr = (tid >> 2) + 64 * i;
+            if (src[i] && !packed[i]) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) cp_async_16(blk_s + swz(rr, c0 + k), src[i] + pblk * 64 + (c0 + k) * 8);
+              continue;
+            }
+            const __nv_bfloat162 s_lo = e4m3_bf16x2(scl[g][i] & 0xFFu), s_hi = e4m3_bf16x2(scl[g][i] >> 8);
+            const uint32_t w[4] = {nib[g][i].x, nib[g][i].y, nib[g][i].z, nib[g][i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // chunk k: code bytes 4k .. 4k+3 (8 channels)
+              const __nv_bfloat162 sc = k < 2 ? s_lo : s_hi;
+              uint32_t o[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t v = lut[(w[k] >> (8 * q)) & 0xFFu];
+                const __nv_bfloat162 x = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), sc);
+                o[q] = *reinterpret_cast<const uint32_t*>(&x);
+              }
+              *reinterpret_cast<uint4*>(blk_s + swz(rr, c0 + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          cp_async_commit();
+          if (g > 0) {
+            cp_async_wait_pending(1);
+            fence_proxy_async_smem();
+            mbar_arrive(landed + g - 1);
+          }
+        }
+      }
+      cp_async_wait_pending(0);
+      fence_proxy_async_smem();
+      mbar_arrive(landed + kGranules - 1);
+      return true;
+    };
 
-    // ---- rescale the O^T columns of this warp's heads when a reference moved
-    if (flags[1]) {
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
+    bool ok = n_tiles == 0 || gather(0, false, 0u);
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = warp_wait(s_full, static_cast<uint32_t>(j) & 1u) && ok;
+      if (!named_bar_and(kBarWorkers, kWorkers, ok)) {  // every worker leaves together
+        ok = false;
+        break;
+      }
+      __syncwarp();  // converged for the warp-wide TMEM loads
+      tc_fence_after();
+      // ---- logits of this thread's row (its warp's 32 heads)
+      const int jr = r_lo + j * kTileRows + r;
+      const bool valid = jr < r_hi && (jr >= n_swa || swa_row(jr) != nullptr);
+      float l[HW];
+      auto load_logits = [&] {
         uint32_t v[32];
-        tmem_ld32(taddr, v);
+        tmem_ld32(tlane + hw0, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
-        tmem_st32(taddr, v);
+        for (int h = 0; h < HW; ++h) l[h] = valid ? __uint_as_float(v[h]) * scale2 : -INFINITY;
+      };
+      load_logits();
+      // the warp's heads' reference maxima (m_ref changes only below, between barriers)
+      float mref[HW];
+#pragma unroll
+      for (int h = 0; h < HW; h += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(m_ref + hw0 + h);
+        mref[h] = m4.x, mref[h + 1] = m4.y, mref[h + 2] = m4.z, mref[h + 3] = m4.w;
       }
-      tmem_wait_st();
-    }
-
-    // ---- P = 2^(l - m_ref) as bf16 into the swizzled P tile; row sums
-    {
-      float pf[HW];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < HW; ++h) need |= l[h] > mref[h] + kRescaleSlack;
+      if (named_bar_or(kBarWorkers, kWorkers, need)) {
+        // ---- a reference maximum moves: per-head tile maxima over the rows
+        //      (the reduction consumes l, read again from TMEM afterwards)
+        warp_reduce_scatter<true>(l);
+        red_s[quad * kHeads + hw0 + lane] = l[0];
+        named_bar_sync_any(kBarWorkers, kWorkers);
+        if (tid < kHeads) {
+          const float tmax = fmaxf(fmaxf(red_s[tid], red_s[kHeads + tid]),
+                                   fmaxf(red_s[2 * kHeads + tid], red_s[3 * kHeads + tid]));
+          const float mo = m_ref[tid];
+          float al = 1.f;
+          if (tmax > mo + kRescaleSlack) {  // also taken on the first tile (mo = -inf)
+            al = (mo == -INFINITY) ? 0.f : exp2f(mo - tmax);
+            m_ref[tid] = tmax;
+            if (j > 0 && al != 1.f) flags[1] = 1;
+          }
+          alpha[tid] = al;
+        }
+        named_bar_sync_any(kBarWorkers, kWorkers);
+        const bool rescale = flags[1] != 0;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          lpart[h] *= alpha[hw0 + h];
+          mref[h] = m_ref[hw0 + h];
+        }
+        if (rescale) {  // O^T columns of this warp's heads (O of the previous tile is complete)
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint32_t taddr = tlane + kOCol + blk * 64 + hw0;
+            uint32_t v[32];
+            tmem_ld32(taddr, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[hw0 + h]);
+            tmem_st32(taddr, v);
+          }
+          tmem_wait_st();
+        }
+        named_bar_sync_any(kBarWorkers, kWorkers);  // flags[1] and red_s read by every worker
+        if (tid == 0) flags[1] = 0;
+        __syncwarp();
+        load_logits();
+      }
+      // ---- P = 2^(l - m_ref) as bf16 into the swizzled P tile; partial row sums
 #pragma unroll
       for (int c = 0; c < HW / 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int h = c * 8 + 2 * i;
-          const float m0 = m_ref[hw0 + h], m1 = m_ref[hw0 + h + 1];
-          const float ref0 = m0 == -INFINITY ? 0.f : m0;
-          const float ref1 = m1 == -INFINITY ? 0.f : m1;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(l[h] - ref0), exp2f(l[h + 1] - ref1));
-          pf[h] = __low2float(pb);
-          pf[h + 1] = __high2float(pb);
-          w[i] = *reinterpret_cast<const uint32_t*>(&pb);
+          const uint32_t b0 = valid ? bf16_bits_rn(ex2(l[h] - mref[h])) : 0u;
+          const uint32_t b1 = valid ? bf16_bits_rn(ex2(l[h + 1] - mref[h + 1])) : 0u;
+          lpart[h] += __uint_as_float(b0 << 16);
+          lpart[h + 1] += __uint_as_float(b1 << 16);
+          w[i] = b0 | (b1 << 16);
         }
         *reinterpret_cast<uint4*>(p_s + swz(r, hw0 / 8 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      warp_reduce_scatter<false>(pf);
-      __syncthreads();  // everyone is done reading red_s (tile max) and flags
-      red_s[quad * kHeads + hw0 + lane] = pf[0];
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(p_full);
+      // ---- the next tile's rows, granule by granule as O frees them
+      if (j + 1 < n_tiles) ok = gather(j + 1, true, static_cast<uint32_t>(j) & 1u);
+      __syncwarp();
     }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid < kHeads) {
-      l_sum[tid] += (red_s[tid] + red_s[kHeads + tid]) + (red_s[2 * kHeads + tid] + red_s[3 * kHeads + tid]);
-      if (tid == 0) flags[1] = 0;
-    }
-
-    // ---- O^T += V^T . P^T  (4 channel blocks x 8 K-steps of 16 rows)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kvb = smem_u32(kv_s), pb = smem_u32(p_s);
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-        for (int ks = 0; ks < kTileRows / 16; ++ks) {
-          const uint64_t ad = smem_desc(kvb + 2 * blk * kKVBlock + ks * 2048, kKVBlock, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(pb + ks * 2048, kPBytes, 1024, kSwizzle128B);
-          mma_f16(tmem + kOCol + blk * 64, ad, bd, idesc_o, (tile > 0 || ks > 0) ? 1u : 0u);
-        }
-      tc_commit(mma_bar);
-    }
+    // O of the last tile is complete before the epilogue reads TMEM
+    if (ok && n_tiles > 0) ok = warp_wait(o_done + kGranules - 1, static_cast<uint32_t>(n_tiles - 1) & 1u);
+    cp_async_wait_pending(0);  // no copy of this thread's stays in flight
+    if (tid == 0)              // nor a TMA box (bounded, whatever happened to the other waits)
+      for (int g = 0; g < kGranules; ++g)
+        if (tma_pending & (1u << g)) mbar_wait(tma_bar + g, (tma_pending >> 8) & 1u, a.status);
     __syncwarp();
-    if (!__syncthreads_and(mbar_wait(mma_bar, phase, a.status))) { ok = false; break; }
-    phase ^= 1u;
-    tc_fence_after();
-    __syncthreads();  // kv_s / p_s may be overwritten by the next tile
+    // the denominator of each head over the CTA's rows
+    warp_reduce_scatter<false>(lpart);
+    red_s[quad * kHeads + hw0 + lane] = lpart[0];
+    named_bar_sync_any(kBarWorkers, kWorkers);
+    if (tid < kHeads)
+      l_sum[tid] = (red_s[tid] + red_s[kHeads + tid]) + (red_s[2 * kHeads + tid] + red_s[3 * kHeads + tid]);
   }
+  tc_fence_before();
   __syncthreads();
-  // with no tile the Q tile's copy may still be in flight: its buffer is reused below
-  if (n_tiles == 0 && !__syncthreads_and(mbar_wait(q_full, 0, a.status))) ok = false;
-  const bool live = ok && n_tiles > 0;  // TMEM holds this CTA's O^T
+  tc_fence_after();
+  const bool live = *abort_flag == 0 && n_tiles > 0;  // TMEM holds this CTA's O^T
   uint16_t* og = a.out + row_q * kHeads * kDim;
 
   // ---- epilogue: out = sum over the slices s of O_s^T * 2^(m_s - M) / den,
   //      M the joint maximum (sink included), den = sum_s l_s 2^(m_s - M) +
-  //      2^(sink*log2e - M).  `share(s, h)` is slice s's factor for head h.
+  //      2^(sink*log2e - M).  `factors` gives slice s's factor for head h.
   auto factors = [&](int h, const float* mvals, const float* lvals, int stride, int n, float* out_f) {
     const float sk = fin[h];
     float M = sk;
@@ -502,42 +708,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       pml[tid] = m_ref[tid];
       pml[kHeads + tid] = l_sum[tid];
     }
+    // staged as [64 heads][512] fp32 in the (free) KV buffer, then one bulk copy
+    float* stage = reinterpret_cast<float*>(kv_s);
+    if (worker) {
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      const int chn = blk * 128 + quad * 32 + lane;
-      uint32_t v[32];
-      if (live) {
-        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
-        tmem_wait_ld();
-      } else {
+      for (int blk = 0; blk < 4; ++blk) {
+        const int chn = blk * 128 + quad * 32 + lane;
+        uint32_t v[32];
+        if (live) {
+          tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) v[h] = 0u;
+          for (int h = 0; h < 32; ++h) v[h] = 0u;
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) stage[(hw0 + h) * kDim + chn] = __uint_as_float(v[h]);
       }
-#pragma unroll
-      for (int h = 0; h < 32; ++h) po[(hw0 + h) * kDim + chn] = __uint_as_float(v[h]);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(po, stage, kHeads * kDim * 4);
+      bulk_commit_group();
+      bulk_wait_read_all();
     }
   } else if (split == 1) {
     if (tid < kHeads) factors(tid, m_ref, l_sum, 0, 1, alpha);
     __syncthreads();
-    // O^T from TMEM straight to global: for a head, a warp's lanes hold 32
-    // consecutive channels (one 64-byte store).
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      const int chn = blk * 128 + quad * 32 + lane;
-      uint32_t v[32];
-      if (live) {
-        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
-        tmem_wait_ld();
-      }
-      const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
-      float rs = 0.f, rc = 1.f;
-      if (rot) rope_angle(chn, t, a, &rs, &rc);
+    // O^T from TMEM into a [64 heads][512] bf16 staging tile in the (free) Q
+    // buffer (for a head, a warp's lanes hold 32 consecutive channels), then
+    // one bulk copy to the output
+    uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
+    if (worker) {
+      // this warp's 32 head factors, read before any staging store (which
+      // the compiler could not otherwise move them past)
+      float fa[32];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        float o = live ? __uint_as_float(v[h]) * alpha[hw0 + h] : 0.f;
-        if (rot) o = inverse_rope(o, chn, rs, rc);
-        og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      for (int h = 0; h < 32; h += 4) {
+        const float4 f4 = *reinterpret_cast<const float4*>(alpha + hw0 + h);
+        fa[h] = f4.x, fa[h + 1] = f4.y, fa[h + 2] = f4.z, fa[h + 3] = f4.w;
       }
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        const int chn = blk * 128 + quad * 32 + lane;
+        uint32_t v[32];
+        if (live) {
+          tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
+          tmem_wait_ld();
+        }
+        const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
+        float rs = 0.f, rc = 1.f;
+        if (rot) rope_angle(chn, t, a, &rs, &rc);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          float o = live ? __uint_as_float(v[h]) * fa[h] : 0.f;
+          if (rot) o = inverse_rope(o, chn, rs, rc);
+          stage[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(bf16_bits_rn(o));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(og, stage, kHeads * kDim * 2);
+      bulk_commit_group();
+      bulk_wait_read_all();
     }
   } else {
     // Channel slice c (cw channels, whole 128-channel blocks) of the output
@@ -560,19 +796,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsmem_st_f32(dsmem_addr(&ml_s[(rank * 2 + 1) * kHeads + tid], s), l_sum[tid]);
       }
     }
+    if (worker) {
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      if (blk >= own_blk0 && blk < own_blk0 + own_blks) continue;
-      const int chn = blk * 128 + quad * 32 + lane;
-      const int owner = chn / cw, c = chn - owner * cw;
-      uint32_t v[32];
-      if (live) {
-        tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
-        tmem_wait_ld();
-      }
-      float* dst = reinterpret_cast<float*>(xbuf + slot(owner) * slab) + hw0 * cw + c;
+      for (int blk = 0; blk < 4; ++blk) {
+        if (blk >= own_blk0 && blk < own_blk0 + own_blks) continue;
+        const int chn = blk * 128 + quad * 32 + lane;
+        const int owner = chn / cw, c = chn - owner * cw;
+        uint32_t v[32];
+        if (live) {
+          tmem_ld32(tlane + kOCol + blk * 64 + hw0, v);
+          tmem_wait_ld();
+        }
+        float* dst = reinterpret_cast<float*>(xbuf + slot(owner) * slab) + hw0 * cw + c;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) dst[h * cw] = live ? __uint_as_float(v[h]) : 0.f;
+        for (int h = 0; h < 32; ++h) dst[h * cw] = live ? __uint_as_float(v[h]) : 0.f;
+      }
     }
     fence_proxy_async_smem();
     cluster_sync();  // all slices done: (max, sum) delivered, staging complete, receiving slots free
@@ -586,55 +824,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bulk_commit_group();
     }
-    // every slice's factor per head (alpha is free: [split][64] factors in ml's place)
-    float* fs = red_s;  // [split <= 4][64]
+    // every slice's factor per head (red_s is free: [split <= 4][64] factors)
+    float* fs = red_s;
     if (tid < kHeads) factors(tid, ml_s, ml_s + kHeads, 2 * kHeads, split, fs);
     // own share from TMEM while the slices travel
     float acc[2][32];
+    if (worker) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (k >= own_blks) break;
-      uint32_t v[32];
-      if (live) {
-        tmem_ld32(tlane + kOCol + (own_blk0 + k) * 64 + hw0, v);
-        tmem_wait_ld();
+      for (int k = 0; k < 2; ++k) {
+        if (k >= own_blks) break;
+        uint32_t v[32];
+        if (live) {
+          tmem_ld32(tlane + kOCol + (own_blk0 + k) * 64 + hw0, v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int h = 0; h < 32; ++h) acc[k][h] = live ? __uint_as_float(v[h]) : 0.f;
       }
-#pragma unroll
-      for (int h = 0; h < 32; ++h) acc[k][h] = live ? __uint_as_float(v[h]) : 0.f;
     }
     const bool got = __syncthreads_and(mbar_wait(recv_bar, 0, a.status));
+    if (worker) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (k >= own_blks) break;
-      const int chn = (own_blk0 + k) * 128 + quad * 32 + lane;
-      const int c = chn - rank * cw;
+      for (int k = 0; k < 2; ++k) {
+        if (k >= own_blks) break;
+        const int chn = (own_blk0 + k) * 128 + quad * 32 + lane;
+        const int c = chn - rank * cw;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) acc[k][h] *= fs[rank * kHeads + hw0 + h];
-      for (int s = 0; s < split && got; ++s) {
-        if (s == rank) continue;
-        const float* src = reinterpret_cast<const float*>(xbuf + (split - 1 + slot(s)) * slab) + hw0 * cw + c;
+        for (int h = 0; h < 32; ++h) acc[k][h] *= fs[rank * kHeads + hw0 + h];
+        for (int s = 0; s < split && got; ++s) {
+          if (s == rank) continue;
+          const float* src = reinterpret_cast<const float*>(xbuf + (split - 1 + slot(s)) * slab) + hw0 * cw + c;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) acc[k][h] = fmaf(src[h * cw], fs[s * kHeads + hw0 + h], acc[k][h]);
-      }
-      const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
-      float rs = 0.f, rc = 1.f;
-      if (rot) rope_angle(chn, t, a, &rs, &rc);
+          for (int h = 0; h < 32; ++h) acc[k][h] = fmaf(src[h * cw], fs[s * kHeads + hw0 + h], acc[k][h]);
+        }
+        const bool rot = a.inverse_rope && chn - lane >= kDim - kRope;  // warp-uniform
+        float rs = 0.f, rc = 1.f;
+        if (rot) rope_angle(chn, t, a, &rs, &rc);
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        const float o = rot ? inverse_rope(acc[k][h], chn, rs, rc) : acc[k][h];
-        og[(hw0 + h) * kDim + chn] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        for (int h = 0; h < 32; ++h) {
+          const float o = rot ? inverse_rope(acc[k][h], chn, rs, rc) : acc[k][h];
+          og[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(bf16_bits_rn(o));
+        }
       }
     }
     if (tid == 0) bulk_wait_all();  // this CTA's sends have left its shared memory
     cluster_sync();                 // and every CTA has received before any leaves
   }
 
-  // A timed-out wait leaves MMAs possibly in flight: give them a bounded
-  // chance to finish before TMEM is released.
-  if (!ok && tid == 0) mbar_wait(mma_bar, phase, a.status);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -740,10 +979,26 @@ int choose_split(int64_t queries, int sms, int limit) {
   return split;
 }
 
+// A 3-D map over bf16 rows of kDim channels, [seqs][rows][kDim], read in
+// boxes of one 64-channel block of kTileRows consecutive rows of one
+// sequence (128-byte swizzle, the KV tile's layout).
+bool encode_rows_map(CUtensorMap* m, PFN_cuTensorMapEncodeTiled_v12000 encode, const uint16_t* base, int64_t rows,
+                     int64_t seqs) {
+  if (!encode || !base || rows < kTileRows || seqs <= 0) return false;
+  cuuint64_t dim[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(seqs)};
+  cuuint64_t stride[2] = {static_cast<cuuint64_t>(kDim) * 2, static_cast<cuuint64_t>(rows) * kDim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileRows), 1};
+  cuuint32_t ones[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dim, stride, box, ones,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
-  if (a.B <= 0 || a.Q <= 0) return cudaSuccess;
+cudaError_t launch_sparse_attn(const AttnArgs& args, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
+  if (args.B <= 0 || args.Q <= 0) return cudaSuccess;
+  AttnArgs a = args;
   // q: [B*Q*64 rows][512 bf16]; a box is one 64-channel block of one query's 64 heads
   CUtensorMap tm_q;
   {
@@ -757,6 +1012,12 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // the window buffer ([B][W] ring or [B][swa_len] linear rows) and, for
+  // dense attention over a bf16 cache, the cache: tiles of consecutive rows
+  // by TMA (a map that cannot be made leaves those tiles to the gather)
+  CUtensorMap tm_swa = {}, tm_kv = {};
+  a.tma_swa = encode_rows_map(&tm_swa, encode, a.swa, a.swa_mode == 0 ? a.W : a.swa_len, a.B) ? 1 : 0;
+  a.tma_kv = !a.kv_fp4 && a.dense && encode_rows_map(&tm_kv, encode, a.kv, a.n_cap, a.B) ? 1 : 0;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -770,9 +1031,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
   // (one wave, at most one slice per 128-row tile of the longest row set, at
   // most what the workspace holds), merged by a second kernel.  Taken when
   // it gives more slices than a cluster holds, or slices of at most 3 tiles;
-  // with longer slices the cluster's on-chip merge was measured faster
-  // (64 queries: 2 slices of 2.5 tiles, decode step 100.5 against 101.5 us;
-  // 2 slices of 4.5 tiles, 47.5 against 43.9 us).
+  // with longer slices the cluster's on-chip merge was measured faster.
   int gsplit = 1;
   if (a.part_o && a.part_ml && a.gsplit_cap >= 2) {
     const int64_t rows_max = a.W + (a.dense ? a.n_cap : a.k);
@@ -783,8 +1042,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
     if (g >= 2 && (g > cluster_max || (tiles + g - 1) / g <= 3)) gsplit = static_cast<int>(g);
   }
   if (gsplit > 1) {
-    e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes,
-                   stream, tm_q, a, 1, gsplit);
+    e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes, stream, tm_q,
+                   tm_swa, tm_kv, a, 1, gsplit);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(queries), kHeads), block(kDim / 4);
     static_assert(kMaxGSplit == 16, "the merge kernel is instantiated for bounds up to 16");
@@ -794,8 +1053,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, PFN_cuTensorMapEncodeTiled_v12
     return launch_pdl(attn_combine_kernel<16>, grid, block, 0, stream, a, gsplit);
   }
   const int split = choose_split(queries, sms, cluster_max);
-  return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads),
-                            kSmemBytes, stream, static_cast<unsigned>(split), tm_q, a, split, 1);
+  return launch_pdl_cluster(kernel, dim3(static_cast<unsigned>(a.Q) * split, a.B), dim3(kThreads), kSmemBytes,
+                            stream, static_cast<unsigned>(split), tm_q, tm_swa, tm_kv, a, split, 1);
 }
 
 }  // namespace csa

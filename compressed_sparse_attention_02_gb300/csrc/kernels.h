@@ -225,6 +225,9 @@ struct AttnArgs {
   int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
   double inv_freq[kRope / 2];  // theta^(-2j/R), host fp64
   unsigned* status;
+  // set by launch_sparse_attn: tensor maps of the window buffer and of the
+  // bf16 cache exist, so tiles of 128 consecutive present rows load by TMA
+  int tma_swa, tma_kv;
 };
 constexpr int kMaxGSplit = 16;  // split-KV slices per query at most
 constexpr size_t kGSplitSliceBytes = static_cast<size_t>(kHeads * kDim + 2 * kHeads) * 4;  // raw O + (max, sum)

@@ -127,6 +127,16 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* s
                "r"(smem_u32(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
+// Contiguous copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from this CTA's shared memory to global memory, in the calling
+// thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+// Waits until this thread's committed bulk copies have finished reading
+// their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until this thread's committed bulk copies have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -149,6 +159,35 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
 // Barrier `id` (1..15) over `threads` threads (a multiple of 32) of the CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier `id` over `threads` threads, non-aligned form (see below).
+__device__ __forceinline__ void named_bar_sync_any(uint32_t id, uint32_t threads) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier `id` over `threads` threads that returns the OR (resp. AND) of
+// the threads' predicates.  Non-aligned forms: the threads of a warp may
+// reach them at different times (each thread counts once).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\t"
+      "barrier.red.or.pred po, %2, %3, pi;\n\tselp.b32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\t"
+      "barrier.red.and.pred po, %2, %3, pi;\n\tselp.b32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
 }
 
 // Two independent fp32 fused multiply-adds in one instruction, a * b + c per
@@ -199,6 +238,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global to this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -232,6 +280,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most `n` of this thread's committed cp.async groups are
+// still pending (n = 0..3).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+  }
 }
 
 __device__ __forceinline__ void cp_async_commit_wait_all() {
