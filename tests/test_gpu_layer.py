@@ -46,9 +46,19 @@ def check_decode_seq(w, x, b, kv_in, kv_gpu, idx, out, lse):
         assert_close(kv_gpu[i], oracle.bf16_to_f64(kv_o[i]), "emitted entry b=%d" % b)
     V = oracle.visible(w.t, w.m)
     scores = oracle.index_scores(bits(x["qI"][b, 0]), bits(x["wI"][b, 0]), bits(x["kI"][b])[:V])
-    check_topk(idx, scores, w.topk, "b=%d" % b)
-    assert_close(out, out_o, "out b=%d" % b)
-    np.testing.assert_allclose(lse, lse_o, rtol=1e-3, atol=1e-3)
+    n_diff = check_topk(idx, scores, w.topk, "b=%d" % b)
+    # the attention is judged over the GPU's own selection (a legal near-tie
+    # swap changes the rows, not the kernel's correctness) ...
+    swa = bits(x["swa"][b])
+    out_g, lse_g = oracle.attend_query(w.t, bits(x["q"][b, 0]), idx, kv_o, lambda u: swa[u % w.W], bits(x["sink"]),
+                                       W=w.W)
+    assert_close(out, out_g, "out b=%d" % b)
+    np.testing.assert_allclose(lse, lse_g, rtol=1e-3, atol=1e-3)
+    # ... and the whole step against the oracle's own composition when the
+    # selections agree
+    if n_diff == 0:
+        assert_close(out, out_o, "layer step b=%d" % b)
+        np.testing.assert_allclose(lse, lse_o, rtol=1e-3, atol=1e-3)
 
 
 @pytest.mark.parametrize("cfg,samples", [(0, [0]), (2, [0, 41, 63]), (3, [3])])
@@ -181,12 +191,14 @@ def check_prefill(w, x, kv_gpu, idx, out, lse, b, queries):
         t = pos0 + j
         V = oracle.visible(t, m)
         scores = oracle.index_scores(bits(x["qI"][b, j]), bits(x["wI"][b, j]), kI[:V])
-        check_topk(idx[b, j], scores, w.topk, "q=%d" % j)
-        sel = oracle.topk(scores, w.topk)
-        o, l = oracle.attend_query(t, bits(x["q"][b, j]), sel, kv_o, lambda u: lin[u - (pos0 - (W - 1))],
-                                   bits(x["sink"]), W=W)
-        assert_close(out[b, j].float().cpu().numpy(), o, "prefill out q=%d" % j)
-        np.testing.assert_allclose(lse[b, j], l, rtol=1e-3, atol=1e-3)
+        n_diff = check_topk(idx[b, j], scores, w.topk, "q=%d" % j)
+        # attention over the GPU's selection; the oracle's own when they agree
+        sels = [idx[b, j]] + ([oracle.topk(scores, w.topk)] if n_diff == 0 else [])
+        for sel in sels:
+            o, l = oracle.attend_query(t, bits(x["q"][b, j]), sel, kv_o, lambda u: lin[u - (pos0 - (W - 1))],
+                                       bits(x["sink"]), W=W)
+            assert_close(out[b, j].float().cpu().numpy(), o, "prefill out q=%d" % j)
+            np.testing.assert_allclose(lse[b, j], l, rtol=1e-3, atol=1e-3)
 
 
 @pytest.mark.parametrize("B,Q,pos0,k", [(2, 64, 512, 64), (1, 70, 0, 16), (1, 45, 8, 32)])
