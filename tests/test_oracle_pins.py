@@ -670,6 +670,51 @@ def test_fp4_entries_on_the_grid_round_trip_and_others_round_to_the_nearest_code
         assert np.all(np.abs(deq[16 * g:16 * g + 16] / sc - q) <= best + 1e-9)
 
 
+def test_fp4_entry_binary32_quotients_choose_the_fp64_codes_on_every_input():
+    """The FP4 entry's two quotients (amax/6 for the scale, x/s for a code) are
+    formed in binary32, the kernel's precision; the pages fix no rounding.
+    This reading is harmless: for every bf16 amax and every (bf16 x, E4M3
+    scale s) pair the binary32 and fp64 quotients have no E2M1 / E4M3 rounding
+    midpoint between them (an exact midpoint is representable in binary32 and
+    is then the same in both), so both readings give the same codes; and the
+    oracle's entries equal the ones built from fp64 quotients."""
+    u = np.arange(1, 0x7F80, dtype=np.uint32)                      # every positive finite bf16
+    x = (u << 16).view(np.float32).astype(np.float64)
+    e4 = oracle.e4m3_to_f64(np.arange(0, 127, dtype=np.uint8))     # 0 .. 448, ascending
+    mid4 = (e4[:-1] + e4[1:]) / 2
+    mid2 = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])        # between E2M1 magnitudes
+
+    def crossing(q64, q32, mids):
+        lo, hi = np.minimum(q64, q32), np.maximum(q64, q32)
+        k = np.searchsorted(mids, lo, side="left")                  # first midpoint >= lo
+        return (q64 != q32) & (k < len(mids)) & (mids[np.minimum(k, len(mids) - 1)] <= hi)
+
+    # the scale quotient, every bf16 amax
+    q64 = x / 6.0
+    q32 = (x.astype(np.float32) / np.float32(6.0)).astype(np.float64)
+    assert not crossing(q64, q32, mid4).any()
+    # the code quotient, every bf16 x against every non-zero E4M3 scale
+    for s in e4[1:]:
+        q64 = x / s
+        q32 = (x.astype(np.float32) / np.float32(s)).astype(np.float64)
+        assert not crossing(q64, q32, mid2).any(), s
+    # the oracle's entries equal those of the fp64 reading (random rows and
+    # groups whose amax sits at E4M3 midpoints times 6)
+    rows = oracle.bf16_to_f64(rand_bf16((24, 512), 2.0))
+    rows[:, ::16] = np.resize(oracle.bf16_to_f64(bf16_bits(mid4[40:100] * 6.0)), (24, 32))
+    for r in rows:
+        e = oracle.quantize_kv_fp4(bf16_bits(r))
+        rb = oracle.bf16_to_f64(bf16_bits(r))
+        for g in range(32):
+            grp = rb[16 * g:16 * g + 16]
+            sc = oracle.to_e4m3(np.array([np.abs(grp).max() / 6.0]))[0]
+            assert e[256 + g] == sc
+            sv = oracle.e4m3_to_f64(np.array([sc], np.uint8))[0]
+            codes = oracle.to_e2m1(grp / sv) if sv != 0 else np.zeros(16, np.uint8)
+            want = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+            np.testing.assert_array_equal(e[8 * g:8 * g + 8], want)
+
+
 # ---- FP4 indexer keys and queries ------------------------------------------
 
 def test_e8m0_scale_bytes_worked_by_hand():
