@@ -637,7 +637,8 @@ csa_status csa_index_topk_static(const csa_params* p, int32_t B, int32_t Q, cons
   void* scratch = static_scratch();
   if (!scratch) return CSA_ERR_CUDA;
   return run_index_topk(p, B, Q, q_pos, 0, qI, wI, kI, n_cap, idx_out, score_out, scratch,
-                        CSA_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+                        CSA_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream), g_trace_on, false, nullptr,
+                        nullptr, true);
 }
 
 csa_status csa_index_topk_pool(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_pos, const uint8_t* qI,

@@ -658,15 +658,19 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
   __syncthreads();
   const int n_local = sm.n_local;
-  if (n_local > 0) {
-    // a CTA whose list overflowed pushes the row's count past the cap: the
-    // finish then counts from the scores
-    const unsigned add = n_local > kLocalCap ? static_cast<unsigned>(a.cand_cap) + 1u : static_cast<unsigned>(n_local);
-    if (threadIdx.x == 0) sm.cand_base = atomicAdd(a.cand_count + row, add);
+  const unsigned cap = static_cast<unsigned>(a.cand_cap);
+  if (n_local > kLocalCap) {
+    // this CTA's candidates overflowed its local list: the row's count is
+    // raised past the cap, so the finish counts from the scores.  A maximum,
+    // not an add, so that many overflowing CTAs of one row cannot wrap the
+    // count below the cap (the adds below sum to at most the row's length).
+    if (threadIdx.x == 0) atomicMax(a.cand_count + row, cap + 1u);
+  } else if (n_local > 0) {
+    if (threadIdx.x == 0) sm.cand_base = atomicAdd(a.cand_count + row, static_cast<unsigned>(n_local));
     __syncthreads();
     // unsigned throughout: slots at or past the cap are dropped, whatever the count holds
-    const unsigned base = sm.cand_base, cap = static_cast<unsigned>(a.cand_cap);
-    for (int j = threadIdx.x; j < n_local && j < kLocalCap; j += kThreads) {
+    const unsigned base = sm.cand_base;
+    for (int j = threadIdx.x; j < n_local; j += kThreads) {
       if (base < cap && static_cast<unsigned>(j) < cap - base) {
         a.cand_key[row * a.cand_cap + base + j] = sm.u.f.lkey[j];
         a.cand_idx[row * a.cand_cap + base + j] = sm.u.f.lpos[j];

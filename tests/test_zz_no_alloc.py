@@ -4,7 +4,8 @@ cudaMalloc's host blocking / device synchronisation is not allowed where they
 call).  Its scratch is libcsa's fixed device array instead of a workspace.
 
 Checked through the C ABI against csa_index_topk with a workspace, on two
-calls in a row (the array keeps the previous call's contents).  This file is
+calls in a row after a larger call with other keys (the array keeps the
+previous call's contents).  This file is
 collected last so that a run stopping at the first failure has already run
 every other test; it also passes alone in a fresh process.
 """
@@ -37,6 +38,18 @@ def test_static_scratch_matches_workspace_entry_point_on_two_calls(csa):
     sc_ref = torch.empty(B, 1, k, dtype=torch.float32, device=DEV)
     ws = csa.workspace(csa.CSA_OP_INDEX_TOPK, p, B, 1, n_cap)
     csa.csa_index_topk(p, B, 1, pos, x["qI"], x["wI"], kI, n_cap, idx_ref, sc_ref, ws)
+    assert csa.csa_check_status() == 0
+
+    # a larger call with other keys first: longer rows and more sequences
+    # leave scores, candidate lists and tie bits in the shared array that the
+    # calls below must not pick up
+    B2, n2 = 12, 98304
+    assert csa.csa_workspace_size(csa.CSA_OP_INDEX_TOPK, p, B2, 1, n2) <= csa.STATIC_SCRATCH_BYTES
+    x2 = syn.indexer_query(61, B2, 1, device=DEV)
+    kI2 = syn.indexer_keys(61, B2, n2, device=DEV)
+    pos2 = torch.full((B2, 1), 4 * n2 - 1, dtype=torch.int32, device=DEV)
+    idx2 = torch.empty(B2, 1, k, dtype=torch.int32, device=DEV)
+    csa.csa_index_topk_static(p, B2, 1, pos2, x2["qI"], x2["wI"], kI2, n2, idx2, None)
     assert csa.csa_check_status() == 0
 
     for call in range(2):
