@@ -163,14 +163,88 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32]) {
   }
 }
 
+// The row set of one query, [window rows || selected (or, dense, all
+// visible) entries], and the addresses of its rows.  Plain values and
+// force-inlined functions: nothing of it lives in local memory, which (with
+// the shared memory this kernel takes) would be an L2 round trip per access.
+struct RowSet {
+  const uint16_t* swa;     // this sequence's window buffer: [W] ring or [swa_len] linear rows
+  const uint16_t* kv;      // this sequence's bf16 cache
+  const uint8_t* kv_fp4;   // this sequence's FP4 cache
+  uint32_t sel;            // the compacted selection (shared-memory address)
+  int64_t swa_rel0;        // linear window: buffer row of window row 0
+  int64_t swa_len;
+  int W, swa_mode, n_swa, n_rows, slot0, dense;
+};
+
+// Address of window row j (0 <= j < n_swa), null if the window buffer lacks it.
+__device__ __forceinline__ const uint16_t* window_row(const RowSet& s, int j) {
+  if (s.swa_mode == 0) {
+    const int slot = s.slot0 + j < s.W ? s.slot0 + j : s.slot0 + j - s.W;  // j < n_swa <= W
+    return s.swa + static_cast<int64_t>(slot) * kDim;
+  }
+  const int64_t rr = s.swa_rel0 + j;
+  return rr >= 0 && rr < s.swa_len ? s.swa + rr * kDim : nullptr;
+}
+
+// Address of row j of the row set (null: absent or past the set); an FP4
+// entry's address is returned for its bytes.
+template <bool kFp4>
+__device__ __forceinline__ const uint16_t* row_addr(const RowSet& s, int j) {
+  if (j < s.n_swa) return window_row(s, j);
+  if (j >= s.n_rows) return nullptr;
+  int64_t e = j - s.n_swa;
+  if (!s.dense) {
+    int32_t v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(s.sel + 4u * static_cast<uint32_t>(j - s.n_swa)));
+    e = v;
+  }
+  if constexpr (kFp4) return reinterpret_cast<const uint16_t*>(s.kv_fp4 + e * kFp4Entry);
+  return s.kv + e * kDim;
+}
+
+// Whether the tile of rows r0 .. r0+127 loads by TMA: all present and
+// consecutive in one buffer, i.e. the whole window (linear buffer, or the
+// W = 128 ring, whose slots then hold exactly the window, in slot order,
+// which the softmax does not see), or a run of consecutive entries of a
+// dense bf16 cache.  y: the TMA row coordinate.
+struct TileLoad {
+  int mode;
+  int32_t y;
+};
+template <bool kFp4>
+__device__ __forceinline__ TileLoad tile_load(const RowSet& s, int r0, int r_hi, const AttnArgs& a) {
+  TileLoad t = {kTileGather, 0};
+  if (r0 + kTileRows > r_hi) return t;
+  if (r0 + kTileRows <= s.n_swa) {
+    if (!a.tma_swa) return t;
+    if (s.swa_mode == 0) {
+      if (s.W == kTileRows && s.n_swa == kTileRows) t.mode = kTileTmaWindow;
+      return t;
+    }
+    const int64_t rr0 = s.swa_rel0 + r0;
+    if (rr0 >= 0 && rr0 + kTileRows <= s.swa_len) {
+      t.mode = kTileTmaWindow;
+      t.y = static_cast<int32_t>(rr0);
+    }
+    return t;
+  }
+  if (!kFp4 && s.dense && a.tma_kv && r0 >= s.n_swa) {
+    t.mode = kTileTmaEntries;
+    t.y = r0 - s.n_swa;
+  }
+  return t;
+}
+
 // A bounded wait that also ends when another thread of the CTA has raised
 // the abort flag; a wait that runs out records kErrTimeout and raises it.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned* status) {
+  constexpr uint32_t kSleepNs = 20000;  // the thread wakes when the phase completes
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       record_error(status, kErrTimeout);
@@ -261,20 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int n_swa = static_cast<int>(t < 0 ? 0 : min(static_cast<int64_t>(a.W), t + 1));
-  const uint16_t* kv_b = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
-  const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
-  const int64_t swa_first = t - n_swa + 1;  // position of window row 0
-  const int slot0 = a.swa_mode == 0 ? static_cast<int>(swa_first % a.W) : 0;  // its ring slot
-  // Address of window row j (0 <= j < n_swa), null if the window buffer lacks it.
-  auto swa_row = [&](int j) -> const uint16_t* {
-    if (a.swa_mode == 0) {
-      const int slot = slot0 + j < a.W ? slot0 + j : slot0 + j - a.W;  // j < n_swa <= W
-      return a.swa + (static_cast<int64_t>(b) * a.W + slot) * kDim;
-    }
-    const int64_t rr = swa_first + j - swa_pos0;
-    if (rr >= 0 && rr < a.swa_len) return a.swa + (static_cast<int64_t>(b) * a.swa_len + rr) * kDim;
-    return nullptr;
-  };
+  RowSet rs;
+  rs.swa = a.swa + static_cast<int64_t>(b) * (a.swa_mode == 0 ? a.W : a.swa_len) * kDim;
+  rs.kv = a.kv + static_cast<int64_t>(b) * a.n_cap * kDim;
+  rs.kv_fp4 = a.kv_fp4 + static_cast<int64_t>(b) * a.n_cap * kFp4Entry;
+  rs.sel = smem_u32(sel_s);
+  {
+    const int64_t swa_first = t - n_swa + 1;  // position of window row 0
+    const int64_t swa_pos0 = a.swa_mode == 1 ? (a.swa_pos0 ? a.swa_pos0[b] : a.swa_pos0_base) : 0;
+    rs.swa_rel0 = swa_first - swa_pos0;
+    rs.slot0 = a.swa_mode == 0 ? static_cast<int>(swa_first % a.W) : 0;  // its ring slot
+  }
+  rs.swa_len = a.swa_len;
+  rs.W = a.W;
+  rs.swa_mode = a.swa_mode;
+  rs.n_swa = n_swa;
+  rs.dense = a.dense;
 
   // Compact the selected entries (drop -1, flag out-of-range indices).
   // Dense (HCA): the rows are the visible entries 0 .. V(t)-1, no list.
@@ -325,41 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (r_hi - r_lo + kTileRows - 1) / kTileRows;
   const float scale2 = a.sm_scale * kLog2e;
 
-  // Address of row j of the query's row set (null: absent / skipped).
-  auto row_at = [&](int j) -> const uint16_t* {
-    if (j < n_swa) return swa_row(j);
-    if (j < n_rows) {
-      const int64_t e = a.dense ? j - n_swa : sel_s[j - n_swa];
-      if constexpr (kFp4)  // an FP4 entry: its address, read as bytes by the gather
-        return reinterpret_cast<const uint16_t*>(a.kv_fp4 + (static_cast<int64_t>(b) * a.n_cap + e) * kFp4Entry);
-      return kv_b + e * kDim;
-    }
-    return nullptr;
-  };
-  // Tile j's 128 rows by TMA when they are all present and consecutive in
-  // one buffer: the whole window (linear buffer, or the W = 128 ring, whose
-  // slots then hold exactly the window, in slot order, which the softmax
-  // does not see), or a run of consecutive entries of a dense (bf16) cache.
-  // Returns the mode and the TMA row coordinate.
-  auto tile_mode = [&](int j, int32_t* y) -> int {
-    const int r0 = r_lo + j * kTileRows;
-    if (r0 + kTileRows > r_hi) return kTileGather;
-    if (r0 + kTileRows <= n_swa) {
-      if (!a.tma_swa) return kTileGather;
-      if (a.swa_mode == 0) {
-        *y = 0;
-        return a.W == kTileRows && n_swa == kTileRows ? kTileTmaWindow : kTileGather;
-      }
-      const int64_t rr0 = swa_first + r0 - swa_pos0;
-      *y = static_cast<int32_t>(rr0);
-      return rr0 >= 0 && rr0 + kTileRows <= a.swa_len ? kTileTmaWindow : kTileGather;
-    }
-    if (!kFp4 && a.dense && a.tma_kv && r0 >= n_swa) {
-      *y = r0 - n_swa;
-      return kTileTmaEntries;
-    }
-    return kTileGather;
-  };
+  rs.n_rows = n_rows;
   if constexpr (kFp4)
     if (worker) lut[tid] = e2m1_pair_bf16(tid);  // one entry per worker
   tc_fence_before();
@@ -383,8 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kvb = smem_u32(kv_s), qb = smem_u32(q_s), pb = smem_u32(p_s);
       int n_gather = 0, n_tma = 0;  // tiles so far of each kind: the phases of landed / tma_bar
       for (int j = 0; j < n_tiles && ok; ++j) {
-        int32_t y;
-        const bool tma = tile_mode(j, &y) != kTileGather;
+        const bool tma = tile_load<kFp4>(rs, r_lo + j * kTileRows, r_hi, a).mode != kTileGather;
         const uint32_t par = static_cast<uint32_t>(tma ? n_tma++ : n_gather++) & 1u;
         // S^T = KV . Q^T, granule by granule as each lands (8 MMAs of K = 16 each)
         for (int g = 0; g < kGranules && ok; ++g) {
@@ -446,8 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto gather = [&](int j, bool wait_o, uint32_t opar) -> bool {
       const int r0 = r_lo + j * kTileRows;
-      int32_t y = 0;
-      const int mode = tile_mode(j, &y);
+      const TileLoad tl = tile_load<kFp4>(rs, r0, r_hi, a);
+      const int mode = tl.mode;
+      const int32_t y = tl.y;
       if (mode != kTileGather) {
         if (tid == 0) {
           const CUtensorMap* map = mode == kTileTmaWindow ? &tm_swa : &tm_kv;
@@ -465,14 +507,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (!kFp4) {
         // thread tid copies 16-byte chunk tid & 7 of block 2g + ((tid >> 3) & 1)
-        // of rows (tid >> 4) + 16i: a half-warp covers a row's 256 bytes of the granule
+        // of rows (tid >> 4) + 16i: a half-warp covers a row's 256 bytes of
+        // the granule.  The warp's 16 rows are looked up once, one per lane
+        // (lane l: row 2w + (l & 1) + 16 (l >> 1)), and taken by shuffles: a
+        // row's address may need the selection in shared memory, and lookups
+        // interleaved with the copies would each wait behind the previous copy.
+        const int jl = r0 + 2 * warp + (lane & 1) + 16 * ((lane >> 1) & 7);
+        const uint16_t* mine = lane < 16 && jl < r_hi ? row_addr<kFp4>(rs, jl) : nullptr;
+        if (lane < 16 && !mine && jl < n_swa && jl < r_hi) record_error(a.status, kErrIndexRange);
+        const uint64_t mine_u = reinterpret_cast<uint64_t>(mine);
         const uint16_t* src[kTileRows / 16];
 #pragma unroll
-        for (int i = 0; i < kTileRows / 16; ++i) {
-          const int jr = r0 + (tid >> 4) + 16 * i;
-          src[i] = jr < r_hi ? row_at(jr) : nullptr;
-          if (!src[i] && jr < n_swa && jr < r_hi && (tid & 15) == 0) record_error(a.status, kErrIndexRange);
-        }
+        for (int i = 0; i < kTileRows / 16; ++i)
+          src[i] = reinterpret_cast<const uint16_t*>(__shfl_sync(0xffffffffu, mine_u, (lane >> 4) + 2 * i));
         const int bb = (tid >> 3) & 1, c = tid & 7;
         for (int g = 0; g < kGranules; ++g) {
           if (wait_o && !warp_wait(o_done + g, opar)) {
@@ -484,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kTileRows / 16; ++i) {
             uint8_t* dst = blk_s + swz((tid >> 4) + 16 * i, c);
-            if (src[i]) cp_async_16(dst, src[i] + blk * 64 + c * 8);
+            if (src[i]) cp_async_16_free(dst, src[i] + blk * 64 + c * 8);
             else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
           }
           cp_async_commit();
@@ -509,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           const int jr = r0 + (tid >> 2) + 64 * i;
-          src[i] = jr < r_hi ? row_at(jr) : nullptr;
+          src[i] = jr < r_hi ? row_addr<kFp4>(rs, jr) : nullptr;
           if (!src[i] && jr < n_swa && jr < r_hi && (tid & 3) == 0) record_error(a.status, kErrIndexRange);
           packed[i] = src[i] && jr >= n_swa;
           const uint8_t* e = reinterpret_cast<const uint8_t*>(src[i]);
@@ -533,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rr = (tid >> 2) + 64 * i;
             if (src[i] && !packed[i]) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) cp_async_16(blk_s + swz(rr, c0 + k), src[i] + pblk * 64 + (c0 + k) * 8);
+              for (int k = 0; k < 4; ++k) cp_async_16_free(blk_s + swz(rr, c0 + k), src[i] + pblk * 64 + (c0 + k) * 8);
               continue;
             }
             const __nv_bfloat162 s_lo = e4m3_bf16x2(scl[g][i] & 0xFFu), s_hi = e4m3_bf16x2(scl[g][i] >> 8);
@@ -576,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // ---- logits of this thread's row (its warp's 32 heads)
       const int jr = r_lo + j * kTileRows + r;
-      const bool valid = jr < r_hi && (jr >= n_swa || swa_row(jr) != nullptr);
+      const bool valid = jr < r_hi && (jr >= n_swa || window_row(rs, jr) != nullptr);
       float l[HW];
       auto load_logits = [&] {
         uint32_t v[32];
