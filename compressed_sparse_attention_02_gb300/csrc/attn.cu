@@ -687,17 +687,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_logits();
       }
       // ---- P = 2^(l - m_ref) as bf16 into the swizzled P tile; partial row sums
+      //      (one packed conversion per pair of heads; an invalid row
+      //      contributes zeros, whatever its logits and references give)
 #pragma unroll
       for (int c = 0; c < HW / 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int h = c * 8 + 2 * i;
-          const uint32_t b0 = valid ? bf16_bits_rn(ex2(l[h] - mref[h])) : 0u;
-          const uint32_t b1 = valid ? bf16_bits_rn(ex2(l[h + 1] - mref[h + 1])) : 0u;
-          lpart[h] += __uint_as_float(b0 << 16);
-          lpart[h + 1] += __uint_as_float(b1 << 16);
-          w[i] = b0 | (b1 << 16);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2(l[h] - mref[h]), ex2(l[h + 1] - mref[h + 1]));
+          const uint32_t u = valid ? *reinterpret_cast<const uint32_t*>(&pb) : 0u;
+          lpart[h] += __uint_as_float(u << 16);
+          lpart[h + 1] += __uint_as_float(u & 0xFFFF0000u);
+          w[i] = u;
         }
         *reinterpret_cast<uint4*>(p_s + swz(r, hw0 / 8 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -808,10 +810,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs = 0.f, rc = 1.f;
         if (rot) rope_angle(chn, t, a, &rs, &rc);
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          float o = live ? __uint_as_float(v[h]) * fa[h] : 0.f;
-          if (rot) o = inverse_rope(o, chn, rs, rc);
-          stage[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(bf16_bits_rn(o));
+        for (int h = 0; h < 32; h += 2) {  // one packed conversion per pair of heads
+          float o0 = live ? __uint_as_float(v[h]) * fa[h] : 0.f;
+          float o1 = live ? __uint_as_float(v[h + 1]) * fa[h + 1] : 0.f;
+          if (rot) {
+            o0 = inverse_rope(o0, chn, rs, rc);
+            o1 = inverse_rope(o1, chn, rs, rc);
+          }
+          const __nv_bfloat162 ob = __floats2bfloat162_rn(o0, o1);
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(&ob);
+          stage[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(u);
+          stage[(hw0 + h + 1) * kDim + chn] = static_cast<uint16_t>(u >> 16);
         }
       }
     }
