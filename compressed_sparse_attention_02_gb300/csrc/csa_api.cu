@@ -99,39 +99,29 @@ csa_status check_params(const csa_params* p) {
 }
 
 struct IndexWs {
-  size_t scores_off, hist_off, count_off, done_off, bits_off, ties_off, cand_key_off, cand_idx_off, total;
-  size_t zero_bytes;  // hist, candidate counts and row counters, cleared before each call
+  size_t scores_off, hist_off, bits_off, total;
+  size_t zero_bytes;  // the digit counts, cleared before each call
   int64_t score_ld, bits_ld;
-  int cand_cap;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch of the indexer and top-k: scores [rows][score_ld] fp32; per row the
-// counts of the 2048 score-key first digits, the crossing-digit candidate
-// count and the count of CTAs done with the row (contiguous, so one zeroing
-// launch clears them); the two position bitmaps; the candidate keys and positions.
-bool index_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w) {
+// counts of the 2048 score-key first digits (cleared by one launch before
+// the indexer adds to them); the position bitmaps of rows too long for the
+// top-k's on-chip bitmaps.
+bool index_workspace(int64_t rows, int64_t n_cap, IndexWs* w) {
   if (rows < 0 || n_cap < 0 || static_cast<double>(rows) * static_cast<double>(n_cap) > 1e13) return false;
   w->score_ld = static_cast<int64_t>(round_up(static_cast<size_t>(n_cap), 8));  // 16-byte rows as bf16 too
   w->bits_ld = csa::topk_bits_ld(n_cap);
-  w->cand_cap = csa::topk_cand_cap(n_cap, k);
   const size_t R = static_cast<size_t>(rows);
   w->scores_off = 0;
   size_t off = round_up(R * w->score_ld * 4, 256);
   w->hist_off = off;
-  w->count_off = off + R * 2048 * 4;
-  w->done_off = w->count_off + R * 4;
-  w->zero_bytes = R * 2048 * 4 + R * 8;
+  w->zero_bytes = R * 2048 * 4;
   off = round_up(off + w->zero_bytes, 256);
   w->bits_off = off;
   off = round_up(off + R * w->bits_ld * 4, 256);
-  w->ties_off = off;
-  off = round_up(off + R * w->bits_ld * 4, 256);
-  w->cand_key_off = off;
-  off = round_up(off + R * w->cand_cap * 4, 256);
-  w->cand_idx_off = off;
-  off = round_up(off + R * w->cand_cap * 4, 256);
   w->total = off;
   return true;
 }
@@ -148,9 +138,8 @@ struct PoolSpec {
 
 // Full layer scratch: the entries' indexer scratch, then the same layout for
 // the ceil(n_cap/8) block scores.
-bool pool_workspace(int64_t rows, int64_t n_cap, int k, IndexWs* w, IndexWs* wb, size_t* total) {
-  // (the block selection is sized for the largest pool, 2048 blocks)
-  if (!index_workspace(rows, n_cap, k, w) || !index_workspace(rows, (n_cap + 7) / 8, csa::kMaxTopk, wb))
+bool pool_workspace(int64_t rows, int64_t n_cap, IndexWs* w, IndexWs* wb, size_t* total) {
+  if (!index_workspace(rows, n_cap, w) || !index_workspace(rows, (n_cap + 7) / 8, wb))
     return false;
   *total = w->total + wb->total;
   return true;
@@ -166,13 +155,7 @@ void topk_scratch(csa::TopkArgs* ta, uint8_t* base, const IndexWs& w) {
   ta->score_ld = w.score_ld;
   ta->hist = reinterpret_cast<const uint32_t*>(base + w.hist_off);
   ta->bits = reinterpret_cast<uint32_t*>(base + w.bits_off);
-  ta->ties = reinterpret_cast<uint32_t*>(base + w.ties_off);
   ta->bits_ld = w.bits_ld;
-  ta->cand_count = reinterpret_cast<unsigned*>(base + w.count_off);
-  ta->row_done = reinterpret_cast<unsigned*>(base + w.done_off);
-  ta->cand_key = reinterpret_cast<uint32_t*>(base + w.cand_key_off);
-  ta->cand_idx = reinterpret_cast<int32_t*>(base + w.cand_idx_off);
-  ta->cand_cap = w.cand_cap;
 }
 
 // Shared body of csa_index_topk, the hierarchical indexer calls and the
@@ -188,12 +171,12 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
   size_t need = 0;
   bool sized;
   if (pool && pool->in) {
-    sized = index_workspace(rows, static_cast<int64_t>(pool->blocks) * csa::kPoolBlock, p->topk, &w);
+    sized = index_workspace(rows, static_cast<int64_t>(pool->blocks) * csa::kPoolBlock, &w);
     need = w.total;
   } else if (pool && pool->out) {
-    sized = pool_workspace(rows, n_cap, p->topk, &w, &wb, &need);
+    sized = pool_workspace(rows, n_cap, &w, &wb, &need);
   } else {
-    sized = index_workspace(rows, n_cap, p->topk, &w);
+    sized = index_workspace(rows, n_cap, &w);
     need = w.total;
   }
   if (!sized) return CSA_ERR_UNSUPPORTED;
@@ -444,13 +427,13 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
       return a > 16 ? a : 16;
     }
     case CSA_OP_INDEX_TOPK:
-      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w) ? w.total : 0;
+      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, &w) ? w.total : 0;
     case CSA_OP_LAYER_PREFILL:  // the indexer's scratch, then the attention's
-      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)
+      return index_workspace(static_cast<int64_t>(B) * Q, n_cap, &w)
                  ? round_up(w.total, 256) + csa::attn_split_bytes(static_cast<int64_t>(B) * Q, sms)
                  : 0;
     case CSA_OP_LAYER_DECODE:
-      return index_workspace(static_cast<int64_t>(B), n_cap, p->topk, &w)
+      return index_workspace(static_cast<int64_t>(B), n_cap, &w)
                  ? round_up(w.total, 256) + csa::attn_split_bytes(B, sms)
                  : 0;
     case CSA_OP_HCA_LAYER_DECODE: {  // the attention's split-KV partials
@@ -460,11 +443,10 @@ size_t csa_workspace_size(int32_t op, const csa_params* p, int32_t B, int32_t Q,
     case CSA_OP_INDEX_TOPK_POOL: {
       IndexWs wb;
       size_t total = 0;
-      return pool_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w, &wb, &total) ? total : 0;
+      return pool_workspace(static_cast<int64_t>(B) * Q, n_cap, &w, &wb, &total) ? total : 0;
     }
     case CSA_OP_REINDEX_TOPK:  // sized for the largest pool
-      return index_workspace(static_cast<int64_t>(B) * Q, static_cast<int64_t>(csa::kMaxTopk) * csa::kPoolBlock,
-                             p->topk, &w)
+      return index_workspace(static_cast<int64_t>(B) * Q, static_cast<int64_t>(csa::kMaxTopk) * csa::kPoolBlock, &w)
                  ? w.total
                  : 0;
     default:
@@ -632,7 +614,7 @@ csa_status csa_index_topk_static(const csa_params* p, int32_t B, int32_t Q, cons
   if (!ok_ptr(q_pos) || !ok_ptr(qI) || !ok_ptr(wI) || !ok_ptr(kI) || !ok_ptr(idx_out) || !ok_opt(score_out))
     return CSA_ERR_INVALID_ARG;
   IndexWs w;
-  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, &w)) return CSA_ERR_UNSUPPORTED;
   if (w.total > CSA_STATIC_SCRATCH_BYTES) return CSA_ERR_WORKSPACE;  // beyond the fixed array
   void* scratch = static_scratch();
   if (!scratch) return CSA_ERR_CUDA;
@@ -725,7 +707,7 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
     return CSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   IndexWs w;
-  if (!index_workspace(B, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!index_workspace(B, n_cap, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
   // the top-k counters are cleared first, so that the kernels follow one
   // another directly (programmatic launches)
@@ -823,7 +805,7 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
     return CSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   IndexWs w;
-  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, p->topk, &w)) return CSA_ERR_UNSUPPORTED;
+  if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
   if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;

@@ -57,8 +57,6 @@ constexpr int kIdxHeads = 64;   // indexer heads
 constexpr int kIdxDim = 128;    // indexer width (bytes of one e4m3 key row)
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxWindow = 1024;
-constexpr int kTopkCandCap = 2048;    // crossing-digit candidates a top-k finish stages in shared memory
-constexpr int kTopkCandCapMax = 16384;  // the longest global candidate list of a row
 constexpr int kFp4Entry = kDim / 2 + kDim / 16;  // 288: E2M1 codes + one E4M3 scale per 16 values
 constexpr int kPoolBlock = 8;         // entries per block of the hierarchical indexer's pool
 constexpr int kPoolTileBlocks = 16;   // pool blocks per 128-key indexer tile
@@ -163,14 +161,9 @@ struct TopkArgs {
   int64_t n_cap;
   int32_t* idx_out;         // [B][Q][k]
   float* score_out;         // [B][Q][k] or null
-  uint32_t* bits;           // [B*Q][bits_ld] selected-position bitmap (scratch)
-  uint32_t* ties;           // [B*Q][bits_ld] threshold-tie bitmap (scratch)
+  uint32_t* bits;           // [B*Q][bits_ld] selected-position bitmap of rows longer than the
+                            // on-chip bitmaps hold (scratch, never read before it is written)
   int64_t bits_ld;          // topk_bits_ld(n_cap)
-  unsigned* cand_count;     // [B*Q], zeroed by the caller
-  unsigned* row_done;       // [B*Q], zeroed by the caller
-  uint32_t* cand_key;       // [B*Q][cand_cap]
-  int32_t* cand_idx;        // [B*Q][cand_cap]
-  int cand_cap;             // kTopkCandCap .. kTopkCandCapMax (topk_cand_cap)
   // Row extent: the visible entries V(t) by default; with vis_shift = s the
   // ceil(V/2^s) blocks of 2^s entries (block scores); with a pool the row's
   // valid pool slots, and the output positions map to entries through it.
@@ -182,8 +175,6 @@ struct TopkArgs {
 };
 // Words per row of the top-k position bitmaps (a multiple of 4).
 int64_t topk_bits_ld(int64_t n_cap);
-// Length of a row's candidate list for a top-k of rows of up to n_cap keys.
-int topk_cand_cap(int64_t n_cap, int k);
 // ride_along: optional decode-mode (mode 1) compressor arguments for the same
 // B sequences, computed by extra CTAs of the same launch (m for which
 // topk_can_carry_compress holds).

@@ -130,6 +130,21 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
                : "memory");
 }
+// Adds v to a 32-bit counter in the shared memory of a CTA of the cluster,
+// completing 4 bytes of the transaction count of its mbarrier `bar` (both
+// cluster addresses in that CTA).
+__device__ __forceinline__ void red_async_add_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.add.u32 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "r"(v), "r"(bar)
+               : "memory");
+}
+// Arrives on an mbarrier of a CTA of the cluster (cluster address) and adds
+// `bytes` to the transaction count its phase waits for; no memory ordering.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v), "r"(bar)
                : "memory");
@@ -172,10 +187,40 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
 // Split halves of cluster_sync: arrive early, wait before the first access
 // to another CTA's shared memory (which must not precede the peer's start).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+// Arrival without memory ordering: for a barrier that only keeps the CTAs of
+// the cluster alive until every one has arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 __device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_u32x2(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+
+// Adds v to a 32-bit counter in the shared memory of a CTA of the cluster
+// (no value returned).
+__device__ __forceinline__ void dsmem_red_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 dsmem_ld_u32x4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // Bulk copy of `bytes` (a multiple of 16, 16-byte aligned ends) from this

@@ -7,30 +7,34 @@
 // Scores are compared as order-preserving 32-bit keys (keys.cuh).  While it
 // scores, the indexer counts each row's keys by their top 11 bits (the
 // "digit"), so the digit d* that holds the k-th largest key is known without
-// another pass over the row.  One kernel then selects, one CTA per 4096 keys
-// of a row:
-//   filter  a key whose digit is above d* is selected.  Each thread reads 16
-//           consecutive keys from shared memory and builds their half of a
-//           32-bit word of the row's position bitmap.  A key whose digit is
-//           d* is a candidate: the CTA gathers its candidates in shared
-//           memory and appends them, with their positions, to the row's list
-//           (one global atomic per CTA).
-//   finish  the last CTA of the row to finish its filter (release/acquire on
-//           a per-row counter; no CTA waits for another) loads the row's
-//           bitmap and candidates together and resolves the candidates
-//           exactly: the next 11 bits of their keys give the crossing bin;
-//           when that bin holds at most 32 keys one warp ranks them by (key,
-//           position), else a last 10-bit digit gives the threshold key and
-//           the keys equal to it are taken in position order from a tie
-//           bitmap.  The selected candidates are OR-ed into the bitmap, which
-//           is then read out in position order (the ascending output), and
-//           the selected scores are gathered last.
-// When d* alone holds exactly the keys still needed, the filter selects all of
-// d* and the finish only reads the bitmap out.  A row whose candidate list
-// overflows is resolved from its scores in global memory (slower, exact).
+// another pass over the row.  One thread-block cluster of G <= 8 CTAs selects
+// a row; CTA g owns a contiguous range of the row's 4096-key chunks, whose
+// scores it stages on chip with bulk copies (two in flight):
+//   filter   a key whose digit is above d* is selected outright: each thread
+//            reads 16 consecutive keys and builds half of a 32-bit word of
+//            the CTA's position bitmap (on chip for up to 8 chunks).  A key
+//            whose digit is d* is a candidate; the CTA lists its candidates
+//            in position order.
+//   resolve  the candidates' next 11 bits, then (unless the crossing bin is
+//            taken whole) their last 10 bits, are counted into the shared
+//            memory of the cluster's rank-0 CTA (remote atomic adds) and read
+//            back by every CTA after a cluster barrier: every CTA finds the
+//            same exact threshold key T and how many keys equal to T are
+//            taken (the first ones by position).
+//   emit     each CTA counts its keys above T and equal to T and sends both
+//            counts to every CTA of the cluster; one more barrier gives each
+//            its offset in the row's output and its share of the ties.  It
+//            ORs its selected candidates into its bitmap and writes its own
+//            positions, ascending, at that offset.
+// No CTA waits for another outside the cluster's hardware barriers, and no
+// count or list goes through global memory.  A CTA whose candidates outnumber
+// its list reads its keys again instead (slower, exact).  When d* alone holds
+// exactly the keys still needed, the filter selects all of d* and only the
+// counts are exchanged.
 //
-// A decode step's compressor entry (compress.cuh) can ride along: one extra
-// CTA per sequence computes it, so its latency hides behind the selection.
+// A decode step's compressor entry (compress.cuh) can ride along: extra CTAs
+// of the same launch compute one sequence's entry each, so their latency
+// hides behind the selection.
 //
 // The same kernel selects the hierarchical indexer's pool blocks (over the
 // block scores, ceil(V/8) of them) and a Reindex layer's entries (over the
@@ -46,72 +50,44 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 4096;     // keys per CTA: 16 consecutive keys per thread
-constexpr int kLocalCap = 2048;  // candidates one CTA gathers before the row falls back
-constexpr int kEmitWords = 8;    // bitmap words a thread reads per round of the read-out
-constexpr int kBatch = 8;        // global loads a thread issues before using them (passes over global lists)
-constexpr int kRoundWords = kThreads * kEmitWords;
+constexpr int kItems = 4096;                // keys per chunk: 16 consecutive keys per thread
+constexpr int kChunkWords = kItems / 32;    // bitmap words per chunk
+constexpr int kMaxCluster = 16;             // CTAs that share a row (8 where larger clusters are refused)
+constexpr int kMaxSlots = 4;                // chunks of scores in flight per CTA
+constexpr int kSmemWords = 1024;            // bitmap words a CTA keeps on chip (8 chunks)
+constexpr int kListCap = 2 * kThreads;      // candidates a CTA lists (two per thread when ranked)
+constexpr int kEmitWords = 4;               // bitmap words a thread reads per emission round
 static_assert(kItems == 16 * kThreads, "a thread covers half a bitmap word");
-static_assert(kTopkCandCap == kRoundWords && kLocalCap == kTopkCandCap && kRoundWords >= kMaxTopk,
-              "shared-memory reuse");
+static_assert(kSmemWords == kEmitWords * kThreads, "one emission round covers the on-chip bitmap");
+static_assert(kKeyBins == 2048, "first digit: 11 bits");
 
 struct Crossing {
   int bin, above, in_bin;  // the bin, the count in higher bins, the count in it
 };
 
+// The dynamic shared memory: this struct, then (at kValsOff) the CTA's score
+// slots of kItems fp32 each (bf16 rows fill the first half of a slot): one
+// for launches whose CTAs hold one chunk, up to kMaxSlots in flight for
+// longer rows.
 struct __align__(16) Smem {
-  union {
-    struct {
-      float vals[kItems];        // the CTA's scores
-      uint32_t lkey[kLocalCap];  // its candidates
-      int32_t lpos[kLocalCap];
-    } f;
-    struct {
-      uint32_t ckey[kTopkCandCap];  // the row's candidates
-      int32_t cpos[kTopkCandCap];
-      uint32_t bm[kRoundWords];     // one read-out round of the row's position bitmap
-      int32_t sel[kMaxTopk];        // the selected positions, ascending
-    } c;
-  } u;
-  union {
-    int hist[2048];           // digit counts
-    int32_t xpos[kMaxTopk];   // extra selected positions (unordered)
-  } h;
+  int hist[kKeyBins];             // the row's first-digit counts, then the second-digit counts
+  int h3[1024];                   // third-digit counts
+  uint32_t bm[kSmemWords];        // this CTA's part of the row's position bitmap
+  uint32_t lkey[kListCap];        // its candidates, in position order
+  int32_t lpos[kListCap];
+  uint4 peer[kMaxCluster];        // per CTA of the cluster: keys above the threshold, keys equal to it
+  uint4 res[2];                   // rank 0's results: the second digit's crossing, then the third's
+  uint4 lead;                     // rank 0's d*, the count still needed at it, whether it is taken whole
+  int wscan[2][kWarps];           // warp totals of block scans (two buffers, used in turn)
   int wsum[kWarps];
   int wval[kWarps];
   float red[kWarps];
-  int wtotal;
   Crossing out;
-  int n_local, last, nx, nsmall;
-  unsigned cand_base;
-  uint32_t small_key[32];  // the keys of a small crossing bin
-  int32_t small_pos[32];
-  uint64_t hist_bar, vals_bar;
+  uint64_t hist_bar, vals_bar[kMaxSlots];
+  uint64_t sum_bar;               // rank 0: one arrival per warp of the cluster per digit (two phases)
+  uint64_t res_bar[2];            // rank 0's results landed
+  uint64_t peer_bar;              // every CTA's counts landed
 };
-
-// Exclusive scan over the warps of the block of one value per warp (every
-// lane of a warp passes the same v); returns the warp's prefix, *total the sum.
-__device__ int warps_scan(int v, Smem& sm, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) sm.wval[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    const int x = lane < kWarps ? sm.wval[lane] : 0;
-    int incl = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane < kWarps) sm.wval[lane] = incl - x;
-    if (lane == 31) sm.wtotal = incl;
-  }
-  __syncthreads();
-  const int r = sm.wval[warp];
-  *total = sm.wtotal;
-  __syncthreads();
-  return r;
-}
 
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
@@ -124,23 +100,77 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 }
 
 // The block-wide exclusive prefix of this thread's count; *total the sum.
-__device__ int block_prefix(int cnt, Smem& sm, int* total) {
+// One barrier: the warps' totals go to buffer `buf`, which the block flips
+// after each scan, so that no scan overwrites totals a thread may still be
+// reading from the scan before (a barrier of the scan between separates
+// them).
+__device__ int block_prefix(int cnt, Smem& sm, int* total, int& buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int incl = warp_incl_scan(cnt);
-  const int wbase = warps_scan(__shfl_sync(0xffffffffu, incl, 31), sm, total);
-  return wbase + incl - cnt;
+  if (lane == 31) sm.wscan[buf][warp] = incl;
+  __syncthreads();
+  int before = 0, sum = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = sm.wscan[buf][w];
+    before += w < warp ? v : 0;
+    sum += v;
+  }
+  buf ^= 1;
+  *total = sum;
+  return before + incl - cnt;
 }
 
-// Scanning the counts of nb (1024 or 2048) bins of sm.h.hist from the top bin
-// down, finds the bin in which the running count first reaches `need`.  Thread
-// t holds bins nb-1-per*t down to nb-per*(t+1); two barriers.  If the counts
-// never reach `need` the result is {0, 0, 0}.
-__device__ Crossing find_crossing(int nb, int need, Smem& sm) {
+// Waits (cluster-scope acquire) for a phase of a barrier that other CTAs of
+// the cluster complete; gives up after kWaitLimitNs (kErrTimeout recorded).
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, unsigned* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_error(status, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+// Block-wide sums of two per-thread counts; every thread gets both.
+__device__ void block_sum2(uint32_t* x, uint32_t* y, Smem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t a = *x, b = *y;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    b += __shfl_xor_sync(0xffffffffu, b, off);
+  }
+  if (lane == 0) {
+    sm.wsum[warp] = static_cast<int>(a);
+    sm.wval[warp] = static_cast<int>(b);
+  }
+  __syncthreads();
+  a = b = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    a += static_cast<uint32_t>(sm.wsum[w]);
+    b += static_cast<uint32_t>(sm.wval[w]);
+  }
+  __syncthreads();
+  *x = a;
+  *y = b;
+}
+
+// Scanning the counts of nb (1024 or 2048) bins from the top bin down, finds
+// the bin in which the running count first reaches `need`.  Thread t holds
+// bins nb-1-per*t down to nb-per*(t+1); two barriers.  If the counts never
+// reach `need` the result is {0, 0, 0}.
+__device__ Crossing find_crossing(const int* bins, int nb, int need, Smem& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = nb / kThreads;  // 4 or 8
   const int lo = nb - per * (static_cast<int>(threadIdx.x) + 1);
   int c[8];
-  const int4 v0 = *reinterpret_cast<const int4*>(sm.h.hist + lo + per - 4);
-  const int4 v1 = per == 8 ? *reinterpret_cast<const int4*>(sm.h.hist + lo) : make_int4(0, 0, 0, 0);
+  const int4 v0 = *reinterpret_cast<const int4*>(bins + lo + per - 4);
+  const int4 v1 = per == 8 ? *reinterpret_cast<const int4*>(bins + lo) : make_int4(0, 0, 0, 0);
   c[0] = v0.w, c[1] = v0.z, c[2] = v0.y, c[3] = v0.x;  // highest bin first
   c[4] = v1.w, c[5] = v1.z, c[6] = v1.y, c[7] = v1.x;
   int x = 0;
@@ -169,55 +199,6 @@ __device__ Crossing find_crossing(int nb, int need, Smem& sm) {
   return total >= need ? sm.out : Crossing{0, 0, 0};
 }
 
-// Resolves the key digits below the first, 11 then 10 bits, among keys whose
-// first digit is d*; key_at(i) for i < n gives the keys to count.  Returns the
-// exact threshold key; *need becomes how many keys equal to it are taken and
-// *n_eq how many there are.
-template <class KeyAt>
-__device__ uint32_t resolve_threshold(uint32_t dstar, int64_t n, KeyAt key_at, Smem& sm, int* need, int* n_eq) {
-  uint32_t prefix = dstar << kKeyBinShift;
-  int in_bin = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int shift = pass == 0 ? 10 : 0;
-    const int nb = pass == 0 ? 2048 : 1024;
-    const uint32_t mask = pass == 0 ? 0xFFE00000u : 0xFFFFFC00u;
-    for (int i = threadIdx.x; i < nb; i += kThreads) sm.h.hist[i] = 0;
-    __syncthreads();
-    for (int64_t i0 = 0; i0 < n; i0 += kBatch * kThreads) {  // kBatch independent loads in flight
-      uint32_t kk[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int64_t i = i0 + u * kThreads + threadIdx.x;
-        kk[u] = i < n ? key_at(i) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int64_t i = i0 + u * kThreads + threadIdx.x;
-        if (i < n && (kk[u] & mask) == prefix) atomicAdd(&sm.h.hist[(kk[u] >> shift) & (nb - 1)], 1);
-      }
-    }
-    __syncthreads();
-    const Crossing c = find_crossing(nb, *need, sm);
-    prefix |= static_cast<uint32_t>(c.bin) << shift;
-    *need -= c.above;
-    in_bin = c.in_bin;
-  }
-  *n_eq = in_bin;
-  return prefix;
-}
-
-__device__ __forceinline__ void push_extra(Smem& sm, int32_t pos) {
-  const int slot = atomicAdd(&sm.nx, 1);
-  if (slot < kMaxTopk) sm.h.xpos[slot] = pos;
-}
-
-// Selects position pos: in the staged first round of the bitmap, or in the
-// list of positions past it (rows longer than kRoundWords words).
-__device__ __forceinline__ void mark(Smem& sm, int32_t pos) {
-  if ((pos >> 5) < kRoundWords) atomicOr(&sm.u.c.bm[pos >> 5], 1u << (pos & 31));
-  else push_extra(sm, pos);
-}
-
 // One bulk async copy global -> shared completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -227,11 +208,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
-// The number of keys of the row: its visible entries; or their blocks
-// (vis_shift); or, with a pool, its valid slots: the pool holds
-// nb = min(pool_blocks, ceil(V/8)) ascending blocks, all entries visible but
-// those of block ceil(V/8)-1 past V, which can only be the pool's last.
-// *ventries receives V.
 // Score i of a row (fp32, or bf16 bits widened exactly).
 __device__ __forceinline__ float row_score(const TopkArgs& a, int64_t row, int64_t i) {
   if (a.bf16_scores)
@@ -241,6 +217,40 @@ __device__ __forceinline__ float row_score(const TopkArgs& a, int64_t row, int64
   return __ldg(a.scores + row * a.score_ld + i);
 }
 
+// Score i of a staged chunk.
+__device__ __forceinline__ float staged_score(const float* vals, bool bf16, int i) {
+  return bf16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(vals)[i]) << 16)
+              : vals[i];
+}
+
+// Calls f(key, bit) for the 16 keys 16t .. 16t+15 of a staged chunk (bit =
+// key - 16t), read as four 16-byte vectors (fp32) in a rotated order so that
+// the eight threads of a shared-memory phase hit distinct banks.
+template <class F>
+__device__ __forceinline__ void visit16(const float* vals, bool bf16, F f) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int jj = (j + (t >> 1)) & 3;
+    float xs[4];
+    if (bf16) {  // keys 16t .. 16t+15 are 32 bytes
+      const uint2 h = reinterpret_cast<const uint2*>(vals)[4 * t + jj];
+      xs[0] = __uint_as_float(h.x << 16), xs[1] = __uint_as_float(h.x & 0xFFFF0000u);
+      xs[2] = __uint_as_float(h.y << 16), xs[3] = __uint_as_float(h.y & 0xFFFF0000u);
+    } else {
+      const float4 x = reinterpret_cast<const float4*>(vals)[4 * t + jj];
+      xs[0] = x.x, xs[1] = x.y, xs[2] = x.z, xs[3] = x.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f(score_key(xs[e]), 4 * jj + e);
+  }
+}
+
+// The number of keys of the row: its visible entries; or their blocks
+// (vis_shift); or, with a pool, its valid slots: the pool holds
+// nb = min(pool_blocks, ceil(V/8)) ascending blocks, all entries visible but
+// those of block ceil(V/8)-1 past V, which can only be the pool's last.
+// *ventries receives V.
 __device__ __forceinline__ int64_t row_extent(const TopkArgs& a, int b, int q, int64_t* ventries) {
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row]) : a.pos_base + q;
@@ -268,270 +278,6 @@ __device__ __forceinline__ int32_t out_entry(const TopkArgs& a, int64_t row, int
   return (blk < 0 || e >= ventries) ? -1 : static_cast<int32_t>(e);
 }
 
-// The `need` lowest positions of the tie bitmap go to the extra list.
-__device__ void take_ties(const uint32_t* ties, int64_t nwords, int need, Smem& sm) {
-  __syncthreads();  // the tie bits of every thread are in the bitmap
-  int done = 0;
-  for (int64_t w0 = 0; w0 < nwords && done < need; w0 += kThreads) {
-    const int64_t w = w0 + threadIdx.x;
-    uint32_t word = w < nwords ? __ldcg(ties + w) : 0u;
-    int total;
-    int before = done + block_prefix(__popc(word), sm, &total);
-    while (word && before < need) {
-      const int bit = __ffs(word) - 1;
-      word &= word - 1;
-      mark(sm, static_cast<int32_t>(w * 32 + bit));
-      ++before;
-    }
-    done += total;
-  }
-}
-
-// Calls f(key, position) for each of the row's nc candidates: from shared
-// memory where the list is staged there, else from the global list, kBatch
-// independent loads per thread at a time.  A position outside [0, V) (never
-// written by this row's filter) reads as key 0 at position 0, the lowest key.
-template <class F>
-__device__ __forceinline__ void for_candidates(bool staged, int nc, const Smem& sm, const uint32_t* gkey,
-                                               const int32_t* gpos, int64_t V, F f) {
-  if (staged) {
-    for (int i = threadIdx.x; i < nc; i += kThreads) f(sm.u.c.ckey[i], sm.u.c.cpos[i]);
-    return;
-  }
-  for (int i0 = 0; i0 < nc; i0 += kBatch * kThreads) {
-    uint32_t kk[kBatch];
-    int32_t pp[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kThreads + static_cast<int>(threadIdx.x);
-      kk[u] = i < nc ? __ldcg(gkey + i) : 0u;
-      pp[u] = i < nc ? __ldcg(gpos + i) : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kThreads + static_cast<int>(threadIdx.x);
-      if (i >= nc) continue;
-      const bool ok = pp[u] >= 0 && pp[u] < V;
-      f(ok ? kk[u] : 0u, ok ? pp[u] : 0);
-    }
-  }
-}
-
-// Reads the staged round of the bitmap out in position order: thread t takes
-// words W*t .. W*t+W-1, one block scan of their bit counts gives each thread
-// its first output slot, and it writes its positions (the first k of the
-// row) to sm.u.c.sel.  Returns the running count.
-template <int W>
-__device__ __forceinline__ int emit_round(Smem& sm, int64_t w0, int out, int k) {
-  uint32_t wd[W];
-  const uint32_t* src = sm.u.c.bm + W * threadIdx.x;
-  if constexpr (W == 8) {
-    const uint4 lo = reinterpret_cast<const uint4*>(src)[0], hi = reinterpret_cast<const uint4*>(src)[1];
-    wd[0] = lo.x, wd[1] = lo.y, wd[2] = lo.z, wd[3] = lo.w;
-    wd[4] = hi.x, wd[5] = hi.y, wd[6] = hi.z, wd[7] = hi.w;
-  } else if constexpr (W == 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(src);
-    wd[0] = v.x, wd[1] = v.y, wd[2] = v.z, wd[3] = v.w;
-  } else if constexpr (W == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
-    wd[0] = v.x, wd[1] = v.y;
-  } else {
-    wd[0] = *src;
-  }
-  int cnt = 0;
-#pragma unroll
-  for (int e = 0; e < W; ++e) cnt += __popc(wd[e]);
-  int total;
-  int slot = out + block_prefix(cnt, sm, &total);
-  const int64_t wb = w0 + W * threadIdx.x;
-#pragma unroll
-  for (int e = 0; e < W; ++e) {
-    uint32_t word = wd[e];
-    while (word) {
-      const int bit = __ffs(word) - 1;
-      word &= word - 1;
-      if (slot < k) sm.u.c.sel[slot] = static_cast<int32_t>((wb + e) * 32 + bit);
-      ++slot;
-    }
-  }
-  return out + total;
-}
-
-// The finish of one row, run by the last of its CTAs.
-__device__ __forceinline__ void finish_row(const TopkArgs& a, int64_t row, int64_t V, int64_t ventries, const Crossing& c,
-                           Smem& sm) {
-  const uint32_t* bits = a.bits + row * a.bits_ld;
-  uint32_t* ties = a.ties + row * a.bits_ld;
-  const int lane = threadIdx.x & 31;
-  const int64_t nwords = (V + 31) >> 5;
-  const uint32_t dstar = static_cast<uint32_t>(c.bin);
-  int need = a.k - c.above;
-  if (threadIdx.x == 0) sm.nx = 0;
-  // Words [w0, w0 + kRoundWords) of the bitmap into sm.u.c.bm, eight
-  // consecutive words per thread (bits_ld is a multiple of 8: the vectors
-  // stay inside the row); words past the row read as zero.
-  auto load_round = [&](int64_t w0) {
-    const int64_t wb = w0 + kEmitWords * threadIdx.x;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (wb < nwords) {
-      lo = __ldcg(reinterpret_cast<const uint4*>(bits + wb));
-      hi = __ldcg(reinterpret_cast<const uint4*>(bits + wb + 4));
-      const uint32_t left = static_cast<uint32_t>(nwords - wb);
-      if (left < 8) {  // the row's last words: the rest of the group is not the row's
-        uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        for (uint32_t e = left; e < 8; ++e) v[e] = 0u;
-        lo = make_uint4(v[0], v[1], v[2], v[3]);
-        hi = make_uint4(v[4], v[5], v[6], v[7]);
-      }
-    }
-    uint4* dst = reinterpret_cast<uint4*>(sm.u.c.bm + kEmitWords * threadIdx.x);
-    dst[0] = lo;
-    dst[1] = hi;
-  };
-  load_round(0);  // in flight with the candidate loads below
-  if (c.in_bin != need) {
-    const unsigned ncu = __ldcg(a.cand_count + row);
-    int n_eq = 0;
-    if (ncu <= static_cast<unsigned>(a.cand_cap)) {
-      const int nc = static_cast<int>(ncu);
-      const uint32_t* gkey = a.cand_key + row * a.cand_cap;
-      const int32_t* gpos = a.cand_idx + row * a.cand_cap;
-      const bool staged = nc <= kTopkCandCap;  // a longer list is read from global memory in each pass
-      if (staged) {
-        for (int i = threadIdx.x; i < nc; i += kThreads) {  // both loads in flight at once
-          const int32_t p = __ldcg(gpos + i);
-          const uint32_t key = __ldcg(gkey + i);
-          const bool ok = p >= 0 && p < V;  // positions come from this row's filter; checked all the same
-          sm.u.c.ckey[i] = ok ? key : 0u;
-          sm.u.c.cpos[i] = ok ? p : 0;
-        }
-      }
-      // the next 11 bits of the candidates' keys
-      for (int i = threadIdx.x; i < 2048; i += kThreads) sm.h.hist[i] = 0;
-      if (threadIdx.x == 0) sm.nsmall = 0;
-      __syncthreads();
-      for_candidates(staged, nc, sm, gkey, gpos, V,
-                     [&](uint32_t k, int32_t) { atomicAdd(&sm.h.hist[(k >> 10) & 2047], 1); });
-      __syncthreads();
-      const Crossing cc = find_crossing(2048, need, sm);
-      const uint32_t p22 = (dstar << 11) | static_cast<uint32_t>(cc.bin);  // the crossing bin's top 22 bits
-      const int need2 = need - cc.above;
-      if (cc.in_bin <= 32) {
-        // keys above the bin are taken; the bin's keys are ranked by one warp
-        for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t p) {
-          const uint32_t k22 = k >> 10;
-          if (k22 > p22) mark(sm, p);
-          if (k22 == p22) {
-            const int slot = atomicAdd(&sm.nsmall, 1);
-            if (slot < 32) {
-              sm.small_key[slot] = k;
-              sm.small_pos[slot] = p;
-            }
-          }
-        });
-        __syncthreads();
-        if (threadIdx.x < 32) {
-          const int nb = min(sm.nsmall, 32);
-          const bool has = lane < nb;
-          const uint32_t kl = has ? sm.small_key[lane] : 0u;
-          const int32_t pl = has ? sm.small_pos[lane] : 0;
-          int rank = 0;  // keys of the bin before this one: larger, or equal at a smaller position
-          for (int j = 0; j < nb; ++j) {
-            const uint32_t kj = __shfl_sync(0xffffffffu, kl, j);
-            const int32_t pj = __shfl_sync(0xffffffffu, pl, j);
-            rank += (kj > kl) || (kj == kl && pj < pl);
-          }
-          if (has && rank < need2) mark(sm, pl);
-        }
-      } else {
-        // a crowded bin: one more digit (10 bits) gives the threshold key
-        uint32_t thr;
-        {
-          for (int i = threadIdx.x; i < 1024; i += kThreads) sm.h.hist[i] = 0;
-          __syncthreads();
-          for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t) {
-            if ((k >> 10) == p22) atomicAdd(&sm.h.hist[k & 1023], 1);
-          });
-          __syncthreads();
-          const Crossing c2 = find_crossing(1024, need2, sm);
-          thr = (p22 << 10) | static_cast<uint32_t>(c2.bin);
-          need = need2 - c2.above;
-          n_eq = c2.in_bin;
-        }
-        const bool all_eq = n_eq == need;  // every key equal to thr is taken
-        for_candidates(staged, nc, sm, gkey, gpos, V, [&](uint32_t k, int32_t p) {
-          if (k > thr || (k == thr && all_eq)) mark(sm, p);
-          if (k == thr && !all_eq) atomicOr(ties + (p >> 5), 1u << (p & 31));
-        });
-        if (!all_eq) take_ties(ties, nwords, need, sm);
-      }
-    } else {
-      // the candidate list overflowed: the same digits counted over the row's scores
-      const uint32_t thr =
-          resolve_threshold(dstar, V, [&](int64_t i) { return score_key(row_score(a, row, i)); }, sm, &need, &n_eq);
-      const bool all_eq = n_eq == need;
-      for (int64_t i0 = 0; i0 < V; i0 += kBatch * kThreads) {
-        float xv[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t i = i0 + u * kThreads + threadIdx.x;
-          xv[u] = i < V ? row_score(a, row, i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t i = i0 + u * kThreads + threadIdx.x;
-          const uint32_t k = i < V ? score_key(xv[u]) : 0u;
-          const bool in = i < V && (k >> kKeyBinShift) == dstar;
-          if (in && (k > thr || (k == thr && all_eq))) mark(sm, static_cast<int32_t>(i));
-          const unsigned em = __ballot_sync(0xffffffffu, in && k == thr && !all_eq);
-          if (lane == 0 && em) atomicOr(ties + ((i - lane) >> 5), em);
-        }
-      }
-      if (!all_eq) take_ties(ties, nwords, need, sm);
-    }
-  }
-  __syncthreads();
-  const int nx = min(sm.nx, kMaxTopk);  // selected positions past the first round
-  // Read the bitmap out in position order, rounds of kRoundWords words from
-  // shared memory: eight consecutive words per thread, one block scan per
-  // round.  Later rounds (rows longer than 65536 entries) are loaded here and
-  // get their selected candidates from the list.
-  int out = 0;
-  const int k = a.k;
-  for (int64_t w0 = 0; w0 < nwords && out < k; w0 += kRoundWords) {
-    if (w0 > 0) {
-      __syncthreads();  // the previous round is read out
-      load_round(w0);
-      __syncthreads();
-      for (int j = threadIdx.x; j < nx; j += kThreads) {
-        const int32_t p = sm.h.xpos[j];
-        const int64_t w = (p >> 5) - w0;
-        if (w >= 0 && w < kRoundWords) atomicOr(&sm.u.c.bm[w], 1u << (p & 31));
-      }
-      __syncthreads();
-    }
-    // a row that fits one round spreads its words over all the threads
-    // (fewer set bits to walk per thread); longer rows take 8 words each
-    const int64_t left = nwords - w0;
-    if (left <= kThreads)
-      out = emit_round<1>(sm, w0, out, k);
-    else if (left <= 2 * kThreads)
-      out = emit_round<2>(sm, w0, out, k);
-    else if (left <= 4 * kThreads)
-      out = emit_round<4>(sm, w0, out, k);
-    else
-      out = emit_round<kEmitWords>(sm, w0, out, k);
-  }
-  __syncthreads();
-  int32_t* idx = a.idx_out + row * a.k;
-  float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
-  for (int j = threadIdx.x; j < a.k; j += kThreads) {
-    const int32_t p = j < out ? sm.u.c.sel[j] : -1;
-    idx[j] = out_entry(a, row, ventries, p);
-    if (sc) sc[j] = p >= 0 ? row_score(a, row, p) + 0.0f : -INFINITY;
-  }
-}
-
 // The compressor entry of sequence b, 2 channels per thread (m <= 4: the
 // m = 8 routine would not fit this kernel's register budget).
 __device__ void compress_ride_along(const CompressArgs& c, int b, Smem& sm) {
@@ -544,16 +290,28 @@ __device__ void compress_ride_along(const CompressArgs& c, int b, Smem& sm) {
   }
 }
 
-// Grid: x the 4096-key chunks of a row (plus the ride-along column), y the
-// queries, z the sequences of problem a0 and then those of problem a1 (a
-// second, independent selection over other scores, e.g. the pool's blocks).
+// Grid: x the G CTAs of a row's cluster, y the queries, z the sequences of
+// problem a0 and then those of problem a1 (a second, independent selection
+// over other scores, e.g. the pool's blocks), then the ride-along CTAs (one
+// compressor entry each).  Every CTA of a cluster shares y and z, so a row
+// that needs no selection is left by the whole cluster at once, and every
+// decision between two cluster barriers is taken on values that all its CTAs
+// hold alike.
+constexpr size_t kValsOff = (sizeof(Smem) + 127) / 128 * 128;
+
 __global__ void __launch_bounds__(kThreads, 4)
-    topk_kernel(const __grid_constant__ TopkArgs a0, const __grid_constant__ TopkArgs a1, const CompressArgs comp) {
-  __shared__ Smem sm;
+    topk_kernel(const __grid_constant__ TopkArgs a0, const __grid_constant__ TopkArgs a1, const CompressArgs comp,
+                const int G, const int slot_shift) {
+  extern __shared__ __align__(128) uint8_t topk_smem[];
+  Smem& sm = *reinterpret_cast<Smem*>(topk_smem);
+  float* const vbase = reinterpret_cast<float*>(topk_smem + kValsOff);
   pdl_launch_dependents();
   pdl_wait();
-  if (comp.B > 0 && blockIdx.x == gridDim.x - 1) {  // the extra column: compressor entries
-    if (blockIdx.y == 0) compress_ride_along(comp, blockIdx.z, sm);
+  const int zsel = a0.B + a1.B;
+  if (static_cast<int>(blockIdx.z) >= zsel) {  // ride-along: one compressor entry per CTA
+    const int64_t s =
+        (static_cast<int64_t>(blockIdx.z - zsel) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    if (s < comp.B) compress_ride_along(comp, static_cast<int>(s), sm);
     return;
   }
   const bool second = static_cast<int>(blockIdx.z) >= a0.B;
@@ -566,149 +324,386 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
   int64_t ventries;
   const int64_t V = row_extent(a, b, q, &ventries);
-  if (V <= a.k) {  // every visible entry is selected; the row's first CTA writes it
-    if (blockIdx.x != 0) return;
-    for (int j = threadIdx.x; j < a.k; j += kThreads) {
+  const int t = threadIdx.x;
+  const int g = blockIdx.x;  // the rank in the cluster
+  if (V <= a.k) {  // every visible entry is selected; the cluster's first CTA writes the row
+    if (g != 0) return;
+    for (int j = t; j < a.k; j += kThreads) {
       a.idx_out[row * a.k + j] = j < V ? out_entry(a, row, ventries, j) : -1;
       if (a.score_out) a.score_out[row * a.k + j] = j < V ? row_score(a, row, j) + 0.0f : -INFINITY;
     }
     return;
   }
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kItems;
-  if (i0 >= V) return;
-  const int n_in = static_cast<int>(min(V - i0, static_cast<int64_t>(kItems)));
-  // the row's digit counts and the chunk's scores, one bulk copy each on
-  // barriers of their own: the crossing search starts once the counts land
-  if (threadIdx.x == 0) {
-    const int esz = a.bf16_scores ? 2 : 4;
-    const uint32_t vbytes = static_cast<uint32_t>((n_in * esz + 15) & ~15);  // score rows are padded to 16 B
+  // this CTA's chunks [c0, c0 + nmine) and keys [i_lo, i_hi)
+  const int64_t nch = (V + kItems - 1) / kItems;
+  const int64_t cpc = (nch + G - 1) / G;
+  const int64_t c0 = min(static_cast<int64_t>(g) * cpc, nch);
+  const int nmine = static_cast<int>(min(c0 + cpc, nch) - c0);
+  const int64_t i_lo = c0 * kItems;
+  const int64_t i_hi = nmine > 0 ? min(i_lo + static_cast<int64_t>(nmine) * kItems, V) : i_lo;
+  const bool resident = cpc == 1;  // the CTA's only chunk stays staged in slot 0 throughout
+  const bool bf16 = a.bf16_scores != 0;
+  const int esz = bf16 ? 2 : 4;
+  // the CTA's bitmap words: on chip, or (ranges of more than 8 chunks) the row's global scratch
+  uint32_t* bm = cpc * kChunkWords <= kSmemWords ? sm.bm : a.bits + row * a.bits_ld + c0 * kChunkWords;
+  const uint8_t* srow = reinterpret_cast<const uint8_t*>(a.scores) + row * a.score_ld * esz;
+  auto chunk_len = [&](int j) { return static_cast<int>(min(V - (c0 + j) * kItems, static_cast<int64_t>(kItems))); };
+  const int nslot = 1 << slot_shift;
+  auto vals = [&](int slot) { return vbase + slot * kItems; };
+  auto issue = [&](int slot, int j) {  // score rows are padded to 16 bytes
+    const uint32_t bytes = static_cast<uint32_t>((chunk_len(j) * esz + 15) & ~15);
+    mbar_arrive_expect_tx(&sm.vals_bar[slot], bytes);
+    bulk_load(vals(slot), srow + (c0 + j) * kItems * esz, bytes, &sm.vals_bar[slot]);
+  };
+  if (t == 0) {
     mbar_init(&sm.hist_bar, 1);
-    mbar_init(&sm.vals_bar, 1);
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&sm.vals_bar[i], 1);
+    mbar_init(&sm.sum_bar, G * kWarps);
+    mbar_init(&sm.res_bar[0], 1);
+    mbar_init(&sm.res_bar[1], 1);
+    mbar_init(&sm.peer_bar, 1);
     fence_mbar_init();
+    // the bytes other CTAs will store here (a result not sent leaves its phase open)
+    mbar_arrive_expect_tx(&sm.res_bar[0], 16);
+    mbar_arrive_expect_tx(&sm.res_bar[1], 16);
+    mbar_arrive_expect_tx(&sm.peer_bar, 16 * G);
     mbar_arrive_expect_tx(&sm.hist_bar, kKeyBins * 4);
-    bulk_load(sm.h.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
-    mbar_arrive_expect_tx(&sm.vals_bar, vbytes);
-    bulk_load(sm.u.f.vals, reinterpret_cast<const uint8_t*>(a.scores) + (row * a.score_ld + i0) * esz, vbytes,
-              &sm.vals_bar);
-    sm.n_local = 0;
+    bulk_load(sm.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
+    for (int j = 0; j < nslot && j < nmine; ++j) issue(j, j);
   }
+  for (int i = t; i < 1024; i += kThreads) sm.h3[i] = 0;
   __syncthreads();
-  if (!__syncthreads_and(mbar_wait(&sm.hist_bar, 0, a.status))) {
-    mbar_wait(&sm.vals_bar, 0, a.status);  // no copy of ours stays in flight
-    return;
-  }
-  const Crossing c = find_crossing(kKeyBins, a.k, sm);
-  if (!__syncthreads_and(mbar_wait(&sm.vals_bar, 0, a.status))) return;
+  // A wait that gives up (status recorded) leaves garbage behind but changes
+  // no barrier: every CTA still takes every cluster barrier the cluster takes.
+  bool ok = __syncthreads_and(mbar_wait(&sm.hist_bar, 0, a.status));
+  const Crossing c = find_crossing(sm.hist, kKeyBins, a.k, sm);
   const uint32_t dstar = static_cast<uint32_t>(c.bin);
-  const bool whole = c.in_bin == a.k - c.above;
-  const uint32_t dsel = whole ? dstar : dstar + 1;  // keys with digit >= dsel are selected outright
+  const int need = a.k - c.above;
+  const bool whole = c.in_bin == need;
+  for (int i = t; i < kKeyBins; i += kThreads) sm.hist[i] = 0;  // now the second-digit counts
+  if (g == 0 && t == 0) sm.lead = make_uint4(dstar, static_cast<uint32_t>(need), whole, 0u);
+  if (G > 1) cluster_arrive();  // barriers set up, counts cleared, rank 0's first digit published
 
-  // 16 consecutive keys per thread, read as four float4 in a rotated order so
-  // that the eight threads of a shared-memory phase hit distinct banks
-  const int t = threadIdx.x, lane = t & 31;
-  uint32_t smask = 0, cmask = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int jj = (j + (t >> 1)) & 3;
-    float xs[4];
-    if (a.bf16_scores) {  // the chunk holds bf16 bits: keys 16t .. 16t+15 are 32 bytes
-      const uint2 h = reinterpret_cast<const uint2*>(sm.u.f.vals)[4 * t + jj];
-      xs[0] = __uint_as_float(h.x << 16), xs[1] = __uint_as_float(h.x & 0xFFFF0000u);
-      xs[2] = __uint_as_float(h.y << 16), xs[3] = __uint_as_float(h.y & 0xFFFF0000u);
-    } else {
-      const float4 x = reinterpret_cast<const float4*>(sm.u.f.vals)[4 * t + jj];
-      xs[0] = x.x, xs[1] = x.y, xs[2] = x.z, xs[3] = x.w;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int bit = 4 * jj + e;
+  // ---- filter: outright selections and candidates.  A CTA with one chunk
+  // keeps both as masks of each thread's 16 keys in registers; with more,
+  // the selections go to the bitmap and the candidates to the list.
+  const uint32_t dsel = whole ? dstar : dstar + 1;  // keys with digit >= dsel are selected outright
+  uint32_t n_out = 0;                               // this thread's outright selections
+  uint32_t r_sel = 0, r_cand = 0;                   // one chunk: this thread's selections and candidates
+  int n_cand = 0;                                   // the CTA's candidates
+  int sb = 0;                                       // the block scans' buffer
+  for (int j = 0; j < nmine; ++j) {
+    const int slot = j & (nslot - 1);
+    const int n_in = chunk_len(j);
+    ok = __syncthreads_and(mbar_wait(&sm.vals_bar[slot], static_cast<uint32_t>(j >> slot_shift) & 1u, a.status)) && ok;
+    uint32_t smask = 0, cmask = 0;
+    visit16(vals(slot), bf16, [&](uint32_t key, int bit) {
       const bool in = 16 * t + bit < n_in;
-      const uint32_t d = score_key(xs[e]) >> kKeyBinShift;
+      const uint32_t d = key >> kKeyBinShift;
       smask |= static_cast<uint32_t>(in && d >= dsel) << bit;
       cmask |= static_cast<uint32_t>(in && !whole && d == dstar) << bit;
+    });
+    n_out += __popc(smask);
+    if (resident) {
+      r_sel = smask, r_cand = cmask;
+      break;  // the chunk stays staged
     }
-  }
-  // thread pairs (2u, 2u+1) make bitmap word u of the chunk
-  const uint32_t upper = __shfl_down_sync(0xffffffffu, smask, 1);
-  if ((t & 1) == 0 && 16 * t < n_in) {
-    const int64_t w = (i0 >> 5) + (t >> 1);
-    a.bits[row * a.bits_ld + w] = smask | (upper << 16);
-    a.ties[row * a.bits_ld + w] = 0u;
-  }
-  if (__any_sync(0xffffffffu, cmask != 0)) {
-    const int cnt = __popc(cmask);
-    const int incl = warp_incl_scan(cnt);
-    int base = 0;
-    if (lane == 31) base = atomicAdd(&sm.n_local, incl);
-    int slot = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-    while (cmask) {
-      const int bit = __ffs(cmask) - 1;
-      cmask &= cmask - 1;
-      if (slot < kLocalCap) {
-        const float v = a.bf16_scores
-                            ? __uint_as_float(static_cast<uint32_t>(
-                                                  reinterpret_cast<const unsigned short*>(sm.u.f.vals)[16 * t + bit])
-                                              << 16)
-                            : sm.u.f.vals[16 * t + bit];
-        sm.u.f.lkey[slot] = score_key(v);
-        sm.u.f.lpos[slot] = static_cast<int32_t>(i0 + 16 * t + bit);
+    // thread pairs (2u, 2u+1) make word u of the chunk
+    const uint32_t upper = __shfl_down_sync(0xffffffffu, smask, 1);
+    if ((t & 1) == 0 && 16 * t < n_in) bm[j * kChunkWords + (t >> 1)] = smask | (upper << 16);
+    if (!whole) {
+      int total;
+      int s = n_cand + block_prefix(__popc(cmask), sm, &total, sb);  // position order
+      while (cmask) {
+        const int bit = __ffs(cmask) - 1;
+        cmask &= cmask - 1;
+        if (s < kListCap) {
+          sm.lkey[s] = score_key(staged_score(vals(slot), bf16, 16 * t + bit));
+          sm.lpos[s] = static_cast<int32_t>(i_lo + static_cast<int64_t>(j) * kItems + 16 * t + bit);
+        }
+        ++s;
       }
-      ++slot;
+      n_cand += total;
+    }
+    __syncthreads();  // the slot is read
+    if (t == 0 && j + nslot < nmine) issue(slot, j + nslot);
+  }
+  // Whether the resolution runs is rank 0's decision (equal to this CTA's
+  // own unless a copy gave up waiting); the crossings are rank 0's.
+  uint32_t ldstar = dstar;
+  int lneed = need;
+  bool lwhole = whole;
+  if (G > 1) {
+    cluster_wait();  // every CTA of the cluster is set up
+    const uint4 l = dsmem_ld_u32x4(dsmem_addr(&sm.lead, 0));
+    ldstar = l.x, lneed = static_cast<int>(l.y), lwhole = l.z != 0;
+  }
+  const bool listed = n_cand <= kListCap;
+  // f(key, position) for each of this CTA's candidates: from the masks
+  // (one chunk), the list, or (a list that overflowed) the scores again
+  auto for_cands = [&](auto f) {
+    if (resident) {
+      uint32_t m = r_cand;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        f(score_key(staged_score(vals(0), bf16, 16 * t + bit)), static_cast<int32_t>(i_lo + 16 * t + bit));
+      }
+      return;
+    }
+    if (listed) {
+      for (int i = t; i < n_cand; i += kThreads) f(sm.lkey[i], sm.lpos[i]);
+      return;
+    }
+    for (int64_t i = i_lo + t; i < i_hi; i += kThreads) {
+      const uint32_t key = score_key(row_score(a, row, i));
+      if ((key >> kKeyBinShift) == ldstar) f(key, static_cast<int32_t>(i));
+    }
+  };
+  // One digit of the candidates' keys counted into rank 0's bins, which
+  // alone finds the crossing bin and sends it to every CTA.  G > 1: each add
+  // is a remote asynchronous add that completes 4 bytes of rank 0's sum_bar,
+  // and each warp arrives there announcing its adds (no fence on the way); a
+  // CTA whose list overflowed adds plainly and arrives after a barrier with
+  // release order instead (its adds could outgrow a transaction count).
+  auto resolve = [&](int* bins, int nb, int phase, int need_at, auto bin_of, auto result) -> uint4 {
+    if (G == 1) {
+      for_cands([&](uint32_t key, int32_t) {
+        const int bin = bin_of(key);
+        if (bin >= 0) atomicAdd(bins + bin, 1);
+      });
+      __syncthreads();
+      return result(find_crossing(bins, nb, need_at, sm));
+    }
+    const uint32_t b0 = dsmem_addr(bins, 0), sbar = dsmem_addr(&sm.sum_bar, 0);
+    if (resident || listed) {
+      uint32_t mine = 0;
+      for_cands([&](uint32_t key, int32_t) {
+        const int bin = bin_of(key);
+        if (bin < 0) return;
+        red_async_add_u32(b0 + 4u * static_cast<uint32_t>(bin), 1u, sbar);
+        ++mine;
+      });
+      const uint32_t wn = __reduce_add_sync(0xffffffffu, mine);
+      if ((t & 31) == 0) mbar_arrive_expect_tx_remote(sbar, 4u * wn);
+    } else {
+      for_cands([&](uint32_t key, int32_t) {
+        const int bin = bin_of(key);
+        if (bin >= 0) dsmem_red_add_u32(b0 + 4u * static_cast<uint32_t>(bin), 1u);
+      });
+      __syncthreads();
+      if ((t & 31) == 0) mbar_arrive_remote(sbar);  // orders the block's adds before it
+    }
+    if (g == 0) {
+      ok = __syncthreads_and(mbar_wait_cl(&sm.sum_bar, static_cast<uint32_t>(phase), a.status)) && ok;
+      const uint4 r = result(find_crossing(bins, nb, need_at, sm));
+      if (t < G) st_async_v4(dsmem_addr(&sm.res[phase], t), r, dsmem_addr(&sm.res_bar[phase], t));
+    }
+    ok = __syncthreads_and(mbar_wait_cl(&sm.res_bar[phase], 0, a.status)) && ok;
+    return sm.res[phase];
+  };
+
+  // ---- resolve: the exact threshold key among the candidates
+  uint32_t thr = ldstar << kKeyBinShift;  // selected: keys >= thr (all_eq), else keys > thr and the first ties
+  int need_eq = 0;
+  bool all_eq = true;
+  if (!lwhole) {
+    // the next 11 bits: res.x the crossing bin's top 22 bits, .y the count still needed, .z whole bin
+    const uint4 r2 = resolve(
+        sm.hist, 2048, 0, lneed, [&](uint32_t key) { return static_cast<int>((key >> 10) & 2047u); },
+        [&](const Crossing& cc) {
+          const int need2 = lneed - cc.above;
+          return make_uint4((ldstar << 11) | static_cast<uint32_t>(cc.bin), static_cast<uint32_t>(need2),
+                            cc.in_bin == need2, 0u);
+        });
+    const uint32_t p22 = r2.x;
+    thr = p22 << 10;
+    if (r2.z == 0) {  // the last 10 bits: res.x the threshold key, .y the ties taken, .z all of them
+      const uint4 r3 = resolve(
+          sm.h3, 1024, 1, static_cast<int>(r2.y), [&](uint32_t key) { return (key >> 10) == p22 ? static_cast<int>(key & 1023u) : -1; },
+          [&](const Crossing& c3) {
+            const int q3 = static_cast<int>(r2.y) - c3.above;
+            return make_uint4((p22 << 10) | static_cast<uint32_t>(c3.bin), static_cast<uint32_t>(q3),
+                              c3.in_bin == q3, 0u);
+          });
+      thr = r3.x;
+      need_eq = static_cast<int>(r3.y);
+      all_eq = r3.z != 0;
     }
   }
-  __syncthreads();
-  const int n_local = sm.n_local;
-  const unsigned cap = static_cast<unsigned>(a.cand_cap);
-  if (n_local > kLocalCap) {
-    // this CTA's candidates overflowed its local list: the row's count is
-    // raised past the cap, so the finish counts from the scores.  A maximum,
-    // not an add, so that many overflowing CTAs of one row cannot wrap the
-    // count below the cap (the adds below sum to at most the row's length).
-    if (threadIdx.x == 0) atomicMax(a.cand_count + row, cap + 1u);
-  } else if (n_local > 0) {
-    if (threadIdx.x == 0) sm.cand_base = atomicAdd(a.cand_count + row, static_cast<unsigned>(n_local));
+
+  // ---- counts: keys above the threshold and keys equal to it, sent to every CTA.
+  // One chunk: each thread's selected keys and ties as masks, whose counts one
+  // block scan gives both for the exchange and for the output slots.
+  uint32_t strict = r_sel, eqm = 0, above = n_out, eq = 0;
+  int pre_s = 0, pre_e = 0;
+  if (resident) {
+    if (!lwhole) {
+      uint32_t m = r_cand;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        const uint32_t key = score_key(staged_score(vals(0), bf16, 16 * t + bit));
+        if (all_eq ? key >= thr : key > thr)
+          strict |= 1u << bit;
+        else if (!all_eq && key == thr)
+          eqm |= 1u << bit;
+      }
+    }
+    int total;  // (a chunk's counts stay below 2^16)
+    const int packed = block_prefix(__popc(strict) | (__popc(eqm) << 16), sm, &total, sb);
+    pre_s = packed & 0xFFFF, pre_e = packed >> 16;
+    above = static_cast<uint32_t>(total & 0xFFFF), eq = static_cast<uint32_t>(total) >> 16;
+  } else {
+    if (!lwhole)
+      for_cands([&](uint32_t key, int32_t) {
+        above += all_eq ? key >= thr : key > thr;
+        eq += !all_eq && key == thr;
+      });
+    block_sum2(&above, &eq, sm);
+  }
+  if (G > 1) {
+    if (t < G) st_async_v4(dsmem_addr(&sm.peer[g], t), make_uint4(above, eq, 0u, 0u), dsmem_addr(&sm.peer_bar, t));
+    // the CTAs stay until every one has sent its last message (below, before leaving)
+    cluster_arrive_relaxed();
+    ok = __syncthreads_and(mbar_wait_cl(&sm.peer_bar, 0, a.status)) && ok;
+  } else {
+    if (t == 0) sm.peer[0] = make_uint4(above, eq, 0u, 0u);
     __syncthreads();
-    // unsigned throughout: slots at or past the cap are dropped, whatever the count holds
-    const unsigned base = sm.cand_base;
-    for (int j = threadIdx.x; j < n_local; j += kThreads) {
-      if (base < cap && static_cast<unsigned>(j) < cap - base) {
-        a.cand_key[row * a.cand_cap + base + j] = sm.u.f.lkey[j];
-        a.cand_idx[row * a.cand_cap + base + j] = sm.u.f.lpos[j];
+  }
+  // this CTA's first output slot, and how many of its keys equal to thr it
+  // takes (a row's counts stay below 2^31)
+  int off = 0, quota = 0, eq_before = 0;
+#pragma unroll
+  for (int r = 0; r < kMaxCluster; ++r) {
+    if (r < G) {
+      const int A = static_cast<int>(sm.peer[r].x), E = static_cast<int>(sm.peer[r].y);
+      const int take = all_eq ? 0 : min(max(need_eq - eq_before, 0), E);
+      off += r < g ? A + take : 0;
+      quota = r == g ? take : quota;
+      eq_before += E;
+    }
+  }
+  int32_t* idx = a.idx_out + row * a.k;
+  float* sc = a.score_out ? a.score_out + row * a.k : nullptr;
+  if (resident) {  // ---- emit: this thread's selected keys and its first ties, in order
+    int take = min(max(quota - pre_e, 0), __popc(eqm));
+    uint32_t sel = strict;
+    for (; take > 0; --take) {
+      const uint32_t low = eqm & (0u - eqm);
+      sel |= low;
+      eqm ^= low;
+    }
+    int s = off + pre_s + min(pre_e, quota);
+    while (sel) {
+      const int bit = __ffs(sel) - 1;
+      sel &= sel - 1;
+      if (s >= 0 && s < a.k) {
+        idx[s] = out_entry(a, row, ventries, static_cast<int32_t>(i_lo + 16 * t + bit));
+        if (sc) sc[s] = staged_score(vals(0), bf16, 16 * t + bit) + 0.0f;
+      }
+      ++s;
+    }
+    if (!ok && t == 0) {  // no copy of ours stays in flight past the CTA
+      mbar_wait(&sm.hist_bar, 0, a.status);
+      if (nmine > 0) mbar_wait(&sm.vals_bar[0], 0, a.status);
+    }
+    if (G > 1) cluster_wait();
+    return;
+  }
+
+  // ---- emit (several chunks): selected candidates into the bitmap, then the bitmap in order
+  auto mark = [&](int64_t pos) { atomicOr(bm + ((pos - i_lo) >> 5), 1u << (pos & 31)); };
+  if (!lwhole) {
+    if (listed) {  // list order is position order: ranks among the keys equal to thr
+      const int i0 = 2 * t;
+      const bool v0 = i0 < n_cand, v1 = i0 + 1 < n_cand;
+      const uint32_t k0 = v0 ? sm.lkey[i0] : 0u, k1 = v1 ? sm.lkey[i0 + 1] : 0u;
+      const bool e0 = v0 && !all_eq && k0 == thr, e1 = v1 && !all_eq && k1 == thr;
+      int total;
+      const int r0 = block_prefix(static_cast<int>(e0) + static_cast<int>(e1), sm, &total, sb);
+      if (v0 && (all_eq ? k0 >= thr : (k0 > thr || (e0 && r0 < quota)))) mark(sm.lpos[i0]);
+      if (v1 && (all_eq ? k1 >= thr : (k1 > thr || (e1 && r0 + static_cast<int>(e0) < quota))))
+        mark(sm.lpos[i0 + 1]);
+    } else {  // the keys again, chunk by chunk: 16 consecutive keys per thread
+      int ranked = 0;
+      for (int j = 0; j < nmine; ++j) {
+        const int n_in = chunk_len(j);
+        const int64_t base = i_lo + static_cast<int64_t>(j) * kItems + 16 * t;
+        uint32_t sel = 0, eqm = 0;
+        auto take = [&](uint32_t key, int bit) {
+          const bool in = 16 * t + bit < n_in && (key >> kKeyBinShift) == ldstar;
+          sel |= static_cast<uint32_t>(in && (all_eq ? key >= thr : key > thr)) << bit;
+          eqm |= static_cast<uint32_t>(in && !all_eq && key == thr) << bit;
+        };
+#pragma unroll 4
+        for (int e = 0; e < 16; ++e) take(16 * t + e < n_in ? score_key(row_score(a, row, base + e)) : 0u, e);
+        int total;
+        int r = ranked + block_prefix(__popc(eqm), sm, &total, sb);
+        while (eqm) {
+          const int bit = __ffs(eqm) - 1;
+          eqm &= eqm - 1;
+          if (r < quota) sel |= 1u << bit;
+          ++r;
+        }
+        ranked += total;
+        while (sel) {
+          const int bit = __ffs(sel) - 1;
+          sel &= sel - 1;
+          mark(base + bit);
+        }
       }
     }
   }
-  // The last CTA of the row to get here finishes it: the barrier orders this
-  // CTA's writes before thread 0's release, and its acquire (with the
-  // barrier after it) orders the other CTAs' writes before the finish reads.
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned n_ctas = static_cast<unsigned>((V + kItems - 1) / kItems);
-    unsigned prev;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.row_done + row) : "memory");
-    sm.last = prev == n_ctas - 1;
+  // the bitmap in position order: four consecutive words per thread, one
+  // block scan per round of 1024 words
+  const int64_t nw = (i_hi - i_lo + 31) >> 5;
+  int64_t run = off;
+  for (int64_t w0 = 0; w0 < nw; w0 += kEmitWords * kThreads) {
+    const int64_t wb = w0 + kEmitWords * t;
+    uint32_t wd[kEmitWords];
+    if (wb + kEmitWords <= nw) {
+      const uint4 v = *reinterpret_cast<const uint4*>(bm + wb);
+      wd[0] = v.x, wd[1] = v.y, wd[2] = v.z, wd[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < kEmitWords; ++e) wd[e] = wb + e < nw ? bm[wb + e] : 0u;
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kEmitWords; ++e) cnt += __popc(wd[e]);
+    int total;
+    int64_t s = run + block_prefix(cnt, sm, &total, sb);
+#pragma unroll
+    for (int e = 0; e < kEmitWords; ++e) {
+      uint32_t word = wd[e];
+      while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1;
+        const int64_t pos = i_lo + (wb + e) * 32 + bit;
+        if (s >= 0 && s < a.k) {
+          idx[s] = out_entry(a, row, ventries, static_cast<int32_t>(pos));
+          if (sc) sc[s] = row_score(a, row, pos) + 0.0f;
+        }
+        ++s;
+      }
+    }
+    run += total;
   }
-  __syncthreads();
-  if (!sm.last) return;
-  finish_row(a, row, V, ventries, c, sm);
+  if (!ok && t == 0) {  // no copy of ours stays in flight past the CTA
+    mbar_wait(&sm.hist_bar, 0, a.status);
+    for (int j = max(0, nmine - nslot); j < nmine; ++j)
+      mbar_wait(&sm.vals_bar[j & (nslot - 1)], static_cast<uint32_t>(j >> slot_shift) & 1u, a.status);
+  }
+  if (G > 1) cluster_wait();
 }
 
 }  // namespace
 
 bool topk_can_carry_compress(int m) { return m == 1 || m == 2 || m == 4; }
 
-int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + kEmitWords - 1) / kEmitWords * kEmitWords; }
-
-// The larger of a sixteenth of the row and four times k (the crossing digit,
-// a quarter octave of scores, holds a small fraction of a long row, or a few
-// times k where k is a large part of it), at most the row, in whole 256-entry
-// steps within the staged size and the largest list.  Past the list a row is
-// resolved from its scores.
-int topk_cand_cap(int64_t n_cap, int k) {
-  int64_t c = n_cap / 16 > 4 * static_cast<int64_t>(k) ? n_cap / 16 : 4 * static_cast<int64_t>(k);
-  c = c < n_cap ? c : n_cap;
-  c = (c + 255) / 256 * 256;
-  return static_cast<int>(c < kTopkCandCap ? kTopkCandCap : (c > kTopkCandCapMax ? kTopkCandCapMax : c));
-}
+int64_t topk_bits_ld(int64_t n_cap) { return ((n_cap + 31) / 32 + 7) / 8 * 8; }
 
 namespace {
 
@@ -719,8 +714,40 @@ int64_t topk_extent(const TopkArgs& a) {
                      : (a.pool ? static_cast<int64_t>(a.pool_blocks) * kPoolBlock : a.n_cap);
 }
 
-bool topk_args_ok(const TopkArgs& a) {
-  return a.cand_cap >= kTopkCandCap && a.cand_cap <= kTopkCandCapMax && !(a.pool && (a.pool_blocks <= 0 || a.vis_shift));
+bool topk_args_ok(const TopkArgs& a) { return !(a.pool && (a.pool_blocks <= 0 || a.vis_shift)); }
+
+// The largest cluster the device schedules with the kernel's largest shared
+// memory (16, else 8); sets the kernel's attributes on first use per device.
+// 0 if the attributes are refused.
+int max_cluster() {
+  constexpr int kDevices = 64;
+  static int cached[kDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kDevices && cached[dev] > 0) return cached[dev];
+  const size_t smem_max = kValsOff + size_t(kMaxSlots) * kItems * 4;
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max)) !=
+      cudaSuccess)
+    return 0;
+  int g = 8;
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMaxCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxCluster, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_max;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) == cudaSuccess && n > 0) g = kMaxCluster;
+  }
+  cudaGetLastError();  // a refused size is not an error of a launch
+  if (dev >= 0 && dev < kDevices) cached[dev] = g;
+  return g;
 }
 
 }  // namespace
@@ -746,9 +773,20 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
     chunks = c2 > chunks ? c2 : chunks;
     q = b.Q > q ? b.Q : q;
   }
-  chunks += ride_along ? 1 : 0;
-  return launch_pdl(topk_kernel, dim3(static_cast<unsigned>(chunks), q, a.B + b.B), dim3(kThreads), 0, stream, a,
-                    b, c);
+  // one CTA per chunk up to the largest cluster; longer rows give each CTA
+  // several, streamed through up to kMaxSlots slots
+  const int gmax = max_cluster();
+  if (gmax <= 0) return cudaErrorInvalidValue;
+  const int G = static_cast<int>(chunks < 1 ? 1 : (chunks > gmax ? gmax : chunks));
+  const int64_t cpc = (chunks + G - 1) / G;
+  const int slot_shift = cpc <= 1 ? 0 : (cpc == 2 ? 1 : 2);
+  const int64_t per_z = static_cast<int64_t>(G) * q;
+  const int64_t extra = ride_along ? (c.B + per_z - 1) / per_z : 0;
+  const int64_t z = static_cast<int64_t>(a.B) + b.B + extra;
+  if (z > 65535) return cudaErrorInvalidValue;
+  const size_t smem = kValsOff + (size_t(1) << slot_shift) * kItems * 4;
+  return launch_pdl_cluster(topk_kernel, dim3(static_cast<unsigned>(G), q, static_cast<unsigned>(z)), dim3(kThreads),
+                            smem, stream, static_cast<unsigned>(G), a, b, c, G, slot_shift);
 }
 
 // Clears `bytes` (a multiple of 4, 16-byte aligned) at p: the indexer's and
