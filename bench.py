@@ -1,9 +1,11 @@
 """Benchmark of the CSA layer hot path (decode step of the 128K-context
 workload: 64 sequences, 32768 compressed entries each, top-k 512, window 128).
 
-One step = one csa_layer_decode call over the batch: block-boundary emission
-of the new compressed entry, lightning indexer over every visible entry,
-top-k, and the sparse attention.  Prints one JSON line (rank 0).
+One step = one csa_layer_decode_with_keys call over the batch: the new
+token's window row into the ring, block-boundary emission of the new
+indexer key (from the key compressor's staging ring) and of the new
+compressed entry, lightning indexer over every visible entry, top-k, and the
+sparse attention.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -171,13 +173,16 @@ def run_ours(args, rank, world, local_rank):
     ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, w.n_cap, device=dev)
     stream = torch.cuda.current_stream()
     counter = [0]
+    keys = csa.index_key_src(x["ring_CIa"], x["ring_ZIa"], x["ring_CIb"], x["ring_ZIb"], x["BIa"], x["BIb"],
+                             x["rms_wI"])
+    swa_new = x["swa"][:, w.t % w.W].contiguous()
 
     def step():
         qs = qsets[counter[0] % QSETS]
         counter[0] += 1
-        csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"],
-                             x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], qs["qI"], qs["wI"], qs["q"], x["swa"],
-                             x["sink"], idx, out, lse, ws)
+        csa.csa_layer_decode_with_keys(p, B, x["q_pos"], swa_new, keys, x["ring_Ca"], x["ring_Za"], x["ring_Cb"],
+                                       x["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap, x["kI"], qs["qI"],
+                                       qs["wI"], qs["q"], x["swa"], x["sink"], idx, out, lse, ws)
 
     def barrier():
         if world > 1:
@@ -922,21 +927,21 @@ def _traffic_from_profile():
 def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, args):
     """Same metric through the same C-ABI call with every step's inputs in
     pinned host memory and its results read back: the step's queries, indexer
-    queries and weights, positions, compressor staging rows, the new token's
-    window row and the new entry's indexer key travel host -> device in one
-    packed copy (the layer call's first kernel stores those two rows into the
-    caches), and the attention output and the selection travel back.
+    queries and weights, positions, the staging rows of both compressors and
+    the new token's window row travel host -> device in one packed copy (the
+    layer call's first kernel stores the row into the window ring and
+    computes the new entry's indexer key), and the attention output and the
+    selection travel back.
     The copies run on their own streams one step ahead of / behind the layer
     call (two staging buffers and two output buffers), as a serving loop
     would overlap them; the timed region spans every step's copies."""
     stream = torch.cuda.Stream()  # a stream of its own (the legacy default stream cannot be captured)
     torch.cuda.synchronize()
-    names = ["q", "qI", "wI", "q_pos", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb", "swa_row", "kI_row"]
+    names = ["q", "qI", "wI", "q_pos", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb", "ring_CIa", "ring_ZIa",
+             "ring_CIb", "ring_ZIb", "swa_row"]
     slot = w.t % w.W
-    entry = (w.t + 1) // w.m - 1
-    parts = {k: x[k] for k in names[:8]}
+    parts = {k: x[k] for k in names[:12]}
     parts["swa_row"] = x["swa"][:, slot].contiguous()
-    parts["kI_row"] = x["kI"][:, entry].contiguous()
     layout, off = {}, 0
     for k in names:
         t = parts[k]
@@ -965,6 +970,8 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
     hsets = [pack({k: qs[k] for k in ("q", "qI", "wI")}) for qs in qsets]
     stage = [torch.empty(total, dtype=torch.uint8, device=kv.device) for _ in range(2)]
     sviews = [views(b) for b in stage]
+    vkeys = [csa.index_key_src(v["ring_CIa"], v["ring_ZIa"], v["ring_CIb"], v["ring_ZIb"], x["BIa"], x["BIb"],
+                               x["rms_wI"]) for v in sviews]
     outs = [out, torch.empty_like(out)]
     idxs = [idx, torch.empty_like(idx)]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -990,10 +997,10 @@ def end_to_end(csa, torch, w, x, qsets, p, B, kv, out, idx, lse, ws, stream, arg
             stream.wait_event(in_ready[s_])
             if i >= 2:
                 stream.wait_event(out_free[s_])
-            csa.csa_layer_decode_append(p, B, v["q_pos"], v["swa_row"], v["kI_row"], v["ring_Ca"], v["ring_Za"],
-                                        v["ring_Cb"], v["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap,
-                                        x["kI"], v["qI"], v["wI"], v["q"], x["swa"], x["sink"], idxs[s_], outs[s_],
-                                        lse, ws)
+            csa.csa_layer_decode_with_keys(p, B, v["q_pos"], v["swa_row"], vkeys[s_], v["ring_Ca"], v["ring_Za"],
+                                           v["ring_Cb"], v["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap,
+                                           x["kI"], v["qI"], v["wI"], v["q"], x["swa"], x["sink"], idxs[s_],
+                                           outs[s_], lse, ws)
             stage_free[s_].record(stream)
             out_ready[s_].record(stream)
 
@@ -1083,7 +1090,9 @@ def _oracle_step_inputs(w, x, b):
     return dict(t=w.t, ring_Ca=b16(x["ring_Ca"][b]), ring_Za=b16(x["ring_Za"][b]), ring_Cb=b16(x["ring_Cb"][b]),
                 ring_Zb=b16(x["ring_Zb"][b]), Ba=b16(x["Ba"]), Bb=b16(x["Bb"]), rms_w=b16(x["rms_w"]),
                 kv_comp=b16(x["kv"][b]), kI=b16(x["kI"][b]), qI=b16(x["qI"][b, 0]), wI=b16(x["wI"][b, 0]),
-                q=b16(x["q"][b, 0]), swa_ring=b16(x["swa"][b]), sink=b16(x["sink"]))
+                q=b16(x["q"][b, 0]), swa_ring=b16(x["swa"][b]), sink=b16(x["sink"]),
+                key_ring={k: b16(x["ring_" + k][b]) for k in ("CIa", "ZIa", "CIb", "ZIb")},
+                key_params={k: b16(x[k]) for k in ("BIa", "BIb", "rms_wI")})
 
 
 def _host_cores():
@@ -1097,7 +1106,9 @@ def _host_cores():
 def _oracle_units(w, inputs, threads):
     """Runs the oracle's full decode step of each input (one sequence) as one
     task, `threads` at a time: the oracle's C parts release the interpreter
-    lock, so the independent units run on separate host cores."""
+    lock, so the independent units run on separate host cores.  A step that
+    completes a block first computes the new entry's indexer key from the key
+    compressor's ring (as the GPU step does) and indexes with it."""
     import concurrent.futures
 
     import oracle
@@ -1105,7 +1116,16 @@ def _oracle_units(w, inputs, threads):
 
     def unit(a):
         a = dict(a)
-        oracle.layer_decode_one(a.pop("t"), **a, m=w.m, topk_k=w.topk, W=w.W)
+        t, ring, kp = a.pop("t"), a.pop("key_ring"), a.pop("key_params")
+        if (t + 1) % w.m == 0 and (t + 1) // w.m - 1 < len(a["kI"]):
+            i, m = (t + 1) // w.m - 1, w.m
+            sa = [(m * i + r) % (2 * m) for r in range(m)]
+            sb = [(m * (i - 1) + r) % (2 * m) for r in range(m)]
+            _, codes = oracle.index_key_entry(i, ring["CIa"][sa], ring["ZIa"][sa], ring["CIb"][sb], ring["ZIb"][sb],
+                                              kp["BIa"], kp["BIb"], kp["rms_wI"])
+            a["kI"] = a["kI"].copy()
+            a["kI"][i] = codes
+        oracle.layer_decode_one(t, **a, m=w.m, topk_k=w.topk, W=w.W)
     with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(unit, inputs))
 
@@ -1122,7 +1142,7 @@ def cpu_baseline(w, x, seconds):
         done += n
     dt = time.perf_counter() - t0
     return {"value": done / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%d of the %d sequences of one decode step (full step each: emission, indexer over %d "
+            "sample": "%d of the %d sequences of one decode step (full step each: key and entry emission, indexer over %d "
                       "entries, top-%d, attention over %d rows), fp64, one sequence per thread on %d threads"
                       % (done, w.B, (w.t + 1) // w.m, w.topk, min(w.W, w.t + 1) + w.topk, cores)}
 

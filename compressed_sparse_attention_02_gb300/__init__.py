@@ -47,6 +47,18 @@ class CsaParams(ctypes.Structure):
                 ("kv_format", ctypes.c_int32), ("bf16_scores", ctypes.c_int32), ("index_format", ctypes.c_int32)]
 
 
+class CsaIndexKeySrc(ctypes.Structure):
+    """Mirror of ``csa_index_key_src`` (device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("CIa", "ZIa", "CIb", "ZIb", "CIb_prev", "ZIb_prev", "BIa", "BIb",
+                                                "rms_wI")]
+
+
+def index_key_src(CIa, ZIa, CIb, ZIb, BIa, BIb, rms_wI, CIb_prev=None, ZIb_prev=None) -> CsaIndexKeySrc:
+    """A ``csa_index_key_src`` over device tensors (which the caller keeps alive)."""
+    return CsaIndexKeySrc(*[None if t is None else t.data_ptr()
+                            for t in (CIa, ZIa, CIb, ZIb, CIb_prev, ZIb_prev, BIa, BIb, rms_wI)])
+
+
 class CsaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -88,8 +100,14 @@ _lib.csa_sparse_attn.argtypes = [_P, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, 
 _lib.csa_layer_decode.argtypes = [_P, _i32, _vp] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
 _lib.csa_layer_decode_append.argtypes = [_P, _i32, _vp] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
 _lib.csa_layer_prefill.argtypes = [_P, _i32, _i32, _i64] + [_vp] * 9 + [_vp, _i64] + [_vp] * 9 + [_vp, _sz, _vp]
+_K = ctypes.POINTER(CsaIndexKeySrc)
+_lib.csa_layer_decode_with_keys.argtypes = ([_P, _i32, _vp, _vp, _K] + [_vp] * 7 + [_vp, _i64] + [_vp] * 9 +
+                                            [_vp, _sz, _vp])
+_lib.csa_layer_prefill_with_keys.argtypes = ([_P, _i32, _i32, _i64] + [_vp] * 9 + [_K, _vp, _i64] + [_vp] * 9 +
+                                             [_vp, _sz, _vp])
 for _f in ("csa_compress", "csa_compress_indexer_keys", "csa_index_topk", "csa_sparse_attn", "csa_layer_decode",
-           "csa_layer_decode_append", "csa_layer_prefill"):
+           "csa_layer_decode_append", "csa_layer_prefill", "csa_layer_decode_with_keys",
+           "csa_layer_prefill_with_keys"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.csa_set_trace_events.argtypes = [ctypes.POINTER(_vp), _i32]
 _lib.csa_set_trace_events.restype = ctypes.c_int
@@ -259,6 +277,30 @@ def csa_layer_decode_append(params, B, q_pos, swa_new, kI_new, ring_Ca, ring_Za,
                                         _ptr(q), _ptr(swa_ring), _ptr(sink), _ptr(idx_out), _ptr(out), _ptr(lse),
                                         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "csa_layer_decode_append")
+
+
+def csa_layer_decode_with_keys(params, B, q_pos, swa_new, keys, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w,
+                               kv_comp, n_cap, kI, qI, wI, q, swa_ring, sink, idx_out, out, lse, ws, stream=None):
+    """``keys``: a CsaIndexKeySrc (see index_key_src) over the key compressor's staging rings."""
+    _check(_lib.csa_layer_decode_with_keys(ctypes.byref(params), B, _ptr(q_pos), _ptr(swa_new),
+                                           None if keys is None else ctypes.byref(keys), _ptr(ring_Ca),
+                                           _ptr(ring_Za), _ptr(ring_Cb), _ptr(ring_Zb), _ptr(Ba), _ptr(Bb),
+                                           _ptr(rms_w), _ptr(kv_comp), n_cap, _ptr(kI), _ptr(qI), _ptr(wI), _ptr(q),
+                                           _ptr(swa_ring), _ptr(sink), _ptr(idx_out), _ptr(out), _ptr(lse),
+                                           _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "csa_layer_decode_with_keys")
+
+
+def csa_layer_prefill_with_keys(params, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, keys, kv_comp,
+                                n_cap, kI, qI, wI, q, swa, sink, idx_out, out, lse, ws, stream=None):
+    """``keys``: a CsaIndexKeySrc (see index_key_src) over the chunk's key compressor rows."""
+    _check(_lib.csa_layer_prefill_with_keys(ctypes.byref(params), B, Q, pos0, _ptr(Ca), _ptr(Za), _ptr(Cb),
+                                            _ptr(Zb), _ptr(Cb_prev), _ptr(Zb_prev), _ptr(Ba), _ptr(Bb), _ptr(rms_w),
+                                            None if keys is None else ctypes.byref(keys), _ptr(kv_comp), n_cap,
+                                            _ptr(kI), _ptr(qI), _ptr(wI), _ptr(q), _ptr(swa), _ptr(sink),
+                                            _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws),
+                                            0 if ws is None else ws.numel(), _stream(stream)),
+           "csa_layer_prefill_with_keys")
 
 
 def csa_layer_prefill(params, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI,

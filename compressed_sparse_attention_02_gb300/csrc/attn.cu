@@ -90,16 +90,11 @@ constexpr size_t kSmemBytes = 1024 + kQBytes + kKVBytes + kPBytes + kMaxTopk * 4
 
 // Inverse partial RoPE of the output: channel chn's pair (D-R+2j, D-R+2j+1)
 // is turned by -t * theta^(-2j/R).  rope_angle gives (sin, cos) of t *
-// theta^(-2j/R), formed and reduced modulo 2*pi in fp64 (positions reach
+// theta^(-2j/R) (the fixed-point angle of rope_sincos: positions reach
 // 2^20); inverse_rope turns one value, exchanging it with the pair's other
 // lane (adjacent lanes of a warp: every lane of the warp must call it).
 __device__ __forceinline__ void rope_angle(int chn, int64_t t, const AttnArgs& a, float* s, float* c) {
-  const int j = (chn - (kDim - kRope)) >> 1;
-  const double two_pi = 6.283185307179586476925286766559;
-  const double inv_two_pi = 0.15915494309189533576888376337251;
-  double phi = static_cast<double>(t) * a.inv_freq[j];
-  phi = fma(-two_pi, rint(phi * inv_two_pi), phi);
-  sincosf(static_cast<float>(phi), s, c);
+  rope_sincos(t, a.rope_turns[(chn - (kDim - kRope)) >> 1], s, c);
 }
 
 __device__ __forceinline__ float inverse_rope(float x, int chn, float s, float c) {

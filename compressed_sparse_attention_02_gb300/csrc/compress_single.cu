@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single
 #pragma unroll
   for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
   Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
-  norm_rope<8, kDim>(a, x, w, t, static_cast<double>(m) * static_cast<double>(i), red, [] { group0_sync(); }, y);
+  norm_rope<8, kDim>(a, x, w, t, static_cast<int64_t>(m) * i, red, [] { group0_sync(); }, y);
   *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
       Bf16Vec<8>::pack(y);
 }
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kGroupThreads) compress_single_step_kernel(con
 #pragma unroll
   for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
   Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
-  norm_rope<8, kDim>(a, x, w, t, static_cast<double>(m) * static_cast<double>(i), red, [] { __syncthreads(); }, y);
+  norm_rope<8, kDim>(a, x, w, t, static_cast<int64_t>(m) * i, red, [] { __syncthreads(); }, y);
   *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
       Bf16Vec<8>::pack(y);
 }
@@ -166,7 +166,7 @@ cudaError_t launch_compress_single(const CompressArgs& args, cudaStream_t stream
   if (args.B <= 0) return cudaSuccess;
   if (args.m < 1 || args.m > kMaxSingleM) return cudaErrorInvalidValue;
   CompressArgs a = args;
-  fill_inv_freq(&a);
+  fill_rope(&a);
   if (a.mode == 0) {
     if (a.n_new <= 0) return cudaSuccess;
     return launch_pdl(compress_single_kernel, dim3(static_cast<unsigned>(a.n_new), static_cast<unsigned>(a.B)),

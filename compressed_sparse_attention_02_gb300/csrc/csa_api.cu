@@ -308,8 +308,7 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.Q = Q;
   aa.sm_scale = p->sm_scale;
   aa.inverse_rope = p->inverse_rope;
-  for (int j = 0; j < csa::kRope / 2; ++j)
-    aa.inv_freq[j] = pow(static_cast<double>(p->rope_theta), -2.0 * j / static_cast<double>(csa::kRope));
+  csa::fill_rope_turns(static_cast<double>(p->rope_theta), aa.rope_turns);
   aa.status = status;
   return cuda_status(csa::launch_sparse_attn(aa, enc, st));
 }
@@ -349,14 +348,35 @@ csa_status run_compress(const csa_params* p, int mode, int32_t B, int64_t n_new,
                         const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
                         const uint16_t* Bb, const uint16_t* rms_w, uint16_t* kv_out, int64_t kv_stride_b,
                         int64_t n_cap, const int32_t* q_pos, cudaStream_t st, uint8_t* fp4_out = nullptr,
-                        int64_t fp4_stride_b = 0) {
+                        int64_t fp4_stride_b = 0, const csa::CompressArgs* keys = nullptr) {
   unsigned* status = status_ptr();
   if (!status) return CSA_ERR_CUDA;
   csa::CompressArgs ca = compress_args(p, mode, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w,
                                        kv_out, kv_stride_b, n_cap, q_pos, status);
   ca.kv_fp4_out = fp4_out;
   ca.fp4_stride_b = fp4_stride_b;
-  return cuda_status(csa::launch_compress(ca, st));
+  return cuda_status(csa::launch_compress(ca, st, keys));
+}
+
+// The key compressor's arguments for the layer calls: mode 1 (decode ring)
+// or 0 (a chunk's rows), E4M3 keys into kI [B][n_cap][128].
+csa::CompressArgs key_args(const csa_params* p, int mode, int32_t B, int64_t n_new, int64_t entry0,
+                           const csa_index_key_src& k, uint8_t* kI, int64_t n_cap, const int32_t* q_pos,
+                           unsigned* status) {
+  csa::CompressArgs ka = compress_args(p, mode, B, n_new, entry0, k.CIa, k.ZIa, k.CIb, k.ZIb,
+                                       mode == 0 ? k.CIb_prev : nullptr, mode == 0 ? k.ZIb_prev : nullptr, k.BIa,
+                                       k.BIb, k.rms_wI, nullptr, n_cap * csa::kIdxDim, n_cap, q_pos, status);
+  ka.key_out = kI;
+  return ka;
+}
+
+bool key_src_ok(const csa_index_key_src* k, bool prefill, int64_t pos0) {
+  if (!k || !ok_ptr(k->CIa) || !ok_ptr(k->ZIa) || !ok_ptr(k->CIb) || !ok_ptr(k->ZIb) || !ok_ptr(k->BIa) ||
+      !ok_ptr(k->BIb) || !ok_ptr(k->rms_wI))
+    return false;
+  if (!prefill) return true;
+  return (pos0 > 0) == (k->CIb_prev != nullptr) && (k->CIb_prev == nullptr) == (k->ZIb_prev == nullptr) &&
+         ok_opt(k->CIb_prev) && ok_opt(k->ZIb_prev);
 }
 
 bool n_cap_ok(int64_t n_cap) { return n_cap >= 1 && n_cap <= (int64_t(1) << 30); }
@@ -694,7 +714,8 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
                         int64_t n_cap, const uint8_t* kI, const uint8_t* qI, const uint16_t* wI,
                         const uint16_t* q, const uint16_t* swa_ring, const float* sink, int32_t* idx_out,
                         uint16_t* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
-                        const csa::DecodeAppend* append) {
+                        const csa::DecodeAppend* append, const csa_index_key_src* keys = nullptr,
+                        uint8_t* kI_out = nullptr) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
@@ -709,12 +730,17 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
   IndexWs w;
   if (!index_workspace(B, n_cap, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
-  // the top-k counters are cleared first, so that the kernels follow one
-  // another directly (programmatic launches)
-  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st, append) != cudaSuccess)
-    return CSA_ERR_CUDA;
   unsigned* status = status_ptr();
   if (!status) return CSA_ERR_CUDA;
+  // the top-k counters are cleared first, so that the kernels follow one
+  // another directly (programmatic launches); the same kernel stores the
+  // step's new rows and computes its indexer key
+  csa::CompressArgs ka = {};
+  if (keys) ka = key_args(p, 1, B, 1, 0, *keys, kI_out, n_cap, q_pos, status);
+  trace(0, st);
+  if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st, append,
+                       keys ? &ka : nullptr) != cudaSuccess)
+    return CSA_ERR_CUDA;
   // 1. emission of the entry that completes at this step (if any).  Only the
   //    attention reads it, so it is computed by extra CTAs of the top-k launch
   //    where that kernel can carry it, else by its own kernel first.
@@ -727,7 +753,6 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
     ca.fp4_stride_b = n_cap * csa::kFp4Entry;
   }
   const bool ride_along = csa::topk_can_carry_compress(p->m);
-  trace(0, st);
   if (!ride_along && (s = cuda_status(csa::launch_compress(ca, st))) != CSA_OK) return s;
   trace(1, st);
   // 2. indexer + top-k over the visible entries
@@ -780,18 +805,48 @@ csa_status csa_layer_decode_append(const csa_params* p, int32_t B, const int32_t
                       swa_ring, sink, idx_out, out, lse, workspace, workspace_bytes, stream, &ap);
 }
 
-csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
+csa_status csa_layer_decode_with_keys(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* swa_new,
+                                      const csa_index_key_src* keys, const uint16_t* ring_Ca, const uint16_t* ring_Za,
+                                      const uint16_t* ring_Cb, const uint16_t* ring_Zb, const uint16_t* Ba,
+                                      const uint16_t* Bb, const uint16_t* rms_w, void* kv_comp, int64_t n_cap,
+                                      uint8_t* kI, const uint8_t* qI, const uint16_t* wI, const uint16_t* q,
+                                      uint16_t* swa_ring, const float* sink, int32_t* idx_out, uint16_t* out,
+                                      float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status s = check_params(p);
+  if (s != CSA_OK) return s;
+  if (!ok_opt(swa_new) || !key_src_ok(keys, false, 0)) return CSA_ERR_INVALID_ARG;
+  if (p->index_format != 0) return CSA_ERR_UNSUPPORTED;  // E4M3 index keys only
+  csa::DecodeAppend ap = {};
+  ap.q_pos = q_pos;
+  ap.B = B;
+  ap.W = p->swa_window;
+  ap.m = p->m;
+  ap.swa_new = swa_new;
+  ap.swa_ring = swa_ring;
+  ap.kI = kI;
+  ap.n_cap = n_cap;
+  return layer_decode(p, B, q_pos, ring_Ca, ring_Za, ring_Cb, ring_Zb, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI, wI, q,
+                      swa_ring, sink, idx_out, out, lse, workspace, workspace_bytes, stream, &ap, keys, kI);
+}
+
+namespace {
+// One prefill chunk; with `keys`, the compressor launch also writes the
+// chunk's indexer keys into kI_out.
+csa_status layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
                              const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb, const uint16_t* Cb_prev,
                              const uint16_t* Zb_prev, const uint16_t* Ba, const uint16_t* Bb,
                              const uint16_t* rms_w, void* kv_comp, int64_t n_cap, const uint8_t* kI,
                              const uint8_t* qI, const uint16_t* wI, const uint16_t* q, const uint16_t* swa,
                              const float* sink, int32_t* idx_out, uint16_t* out, float* lse, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             size_t workspace_bytes, void* stream, const csa_index_key_src* keys = nullptr,
+                             uint8_t* kI_out = nullptr) {
   csa_status s = check_params(p);
   if (s != CSA_OK) return s;
   if ((s = check_overlapped(p)) != CSA_OK) return s;
   if (B < 0 || Q < 0 || B > 65535 || Q > 65535 || pos0 < 0 || pos0 % p->m != 0 || !n_cap_ok(n_cap))
     return CSA_ERR_INVALID_ARG;
+  if (keys && (!key_src_ok(keys, true, pos0) || !ok_ptr(kI_out))) return CSA_ERR_INVALID_ARG;
+  if (keys && p->index_format != 0) return CSA_ERR_UNSUPPORTED;
   if (B == 0 || Q == 0) return CSA_OK;
   const int64_t entry0 = pos0 / p->m;
   const int64_t n_new = (pos0 + Q) / p->m - entry0;
@@ -807,29 +862,43 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
   IndexWs w;
   if (!index_workspace(static_cast<int64_t>(B) * Q, n_cap, &w)) return CSA_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CSA_ERR_WORKSPACE;
+  trace(0, st);
   if (csa::launch_zero(static_cast<uint8_t*>(workspace) + w.hist_off, w.zero_bytes, st) != cudaSuccess)
     return CSA_ERR_CUDA;
-  trace(0, st);
   uint16_t* kv16 = p->kv_format ? nullptr : static_cast<uint16_t*>(kv_comp);
   uint8_t* kv8 = p->kv_format ? static_cast<uint8_t*>(kv_comp) : nullptr;
-  // 1. compress the chunk's complete blocks.  Rows are [B][Q][D]; the
-  //    compressor reads m*n_new of them per sequence with a stride of Q rows.
+  // 1. compress the chunk's complete blocks (and, with keys, their indexer
+  //    keys in the same launch).  Rows are [B][Q][D]; the compressor reads
+  //    m*n_new of them per sequence with a stride of Q rows.
+  unsigned* status = status_ptr();
+  if (!status) return CSA_ERR_CUDA;
   if (n_new > 0) {
     if (static_cast<int64_t>(Q) != n_new * p->m) {
       // Ragged chunk: compress sequence by sequence so the row stride is Q.
       for (int32_t b = 0; b < B; ++b) {
         const int64_t off = static_cast<int64_t>(b) * Q * csa::kDim;
         const int64_t poff = static_cast<int64_t>(b) * p->m * csa::kDim;
+        csa::CompressArgs ka = {};
+        if (keys) {
+          const int64_t ko = static_cast<int64_t>(b) * Q * csa::kIdxDim, kp = static_cast<int64_t>(b) * p->m * csa::kIdxDim;
+          csa_index_key_src kb = *keys;
+          kb.CIa += ko, kb.ZIa += ko, kb.CIb += ko, kb.ZIb += ko;
+          if (kb.CIb_prev) kb.CIb_prev += kp, kb.ZIb_prev += kp;
+          ka = key_args(p, 0, 1, n_new, entry0, kb, kI_out + static_cast<int64_t>(b) * n_cap * csa::kIdxDim, n_cap,
+                        nullptr, status);
+        }
         s = run_compress(p, 0, 1, n_new, entry0, Ca + off, Za + off, Cb + off, Zb + off,
                          Cb_prev ? Cb_prev + poff : nullptr, Zb_prev ? Zb_prev + poff : nullptr, Ba, Bb, rms_w,
                          kv16 ? kv16 + static_cast<int64_t>(b) * n_cap * csa::kDim : nullptr, n_cap * csa::kDim, n_cap,
                          nullptr, st, kv8 ? kv8 + static_cast<int64_t>(b) * n_cap * csa::kFp4Entry : nullptr,
-                         n_cap * csa::kFp4Entry);
+                         n_cap * csa::kFp4Entry, keys ? &ka : nullptr);
         if (s != CSA_OK) return s;
       }
     } else {
+      csa::CompressArgs ka = {};
+      if (keys) ka = key_args(p, 0, B, n_new, entry0, *keys, kI_out, n_cap, nullptr, status);
       s = run_compress(p, 0, B, n_new, entry0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv16,
-                       n_cap * csa::kDim, n_cap, nullptr, st, kv8, n_cap * csa::kFp4Entry);
+                       n_cap * csa::kDim, n_cap, nullptr, st, kv8, n_cap * csa::kFp4Entry, keys ? &ka : nullptr);
       if (s != CSA_OK) return s;
     }
   }
@@ -846,6 +915,31 @@ csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t 
                static_cast<uint8_t*>(workspace) + attn_off, workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
   trace(4, st);
   return s;
+}
+}  // namespace
+
+csa_status csa_layer_prefill(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
+                             const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb, const uint16_t* Cb_prev,
+                             const uint16_t* Zb_prev, const uint16_t* Ba, const uint16_t* Bb,
+                             const uint16_t* rms_w, void* kv_comp, int64_t n_cap, const uint8_t* kI,
+                             const uint8_t* qI, const uint16_t* wI, const uint16_t* q, const uint16_t* swa,
+                             const float* sink, int32_t* idx_out, uint16_t* out, float* lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return layer_prefill(p, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI, wI, q,
+                       swa, sink, idx_out, out, lse, workspace, workspace_bytes, stream);
+}
+
+csa_status csa_layer_prefill_with_keys(const csa_params* p, int32_t B, int32_t Q, int64_t pos0, const uint16_t* Ca,
+                                       const uint16_t* Za, const uint16_t* Cb, const uint16_t* Zb,
+                                       const uint16_t* Cb_prev, const uint16_t* Zb_prev, const uint16_t* Ba,
+                                       const uint16_t* Bb, const uint16_t* rms_w, const csa_index_key_src* keys,
+                                       void* kv_comp, int64_t n_cap, uint8_t* kI, const uint8_t* qI,
+                                       const uint16_t* wI, const uint16_t* q, const uint16_t* swa, const float* sink,
+                                       int32_t* idx_out, uint16_t* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (!keys) return CSA_ERR_INVALID_ARG;
+  return layer_prefill(p, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, Bb, rms_w, kv_comp, n_cap, kI, qI, wI, q,
+                       swa, sink, idx_out, out, lse, workspace, workspace_bytes, stream, keys, kI);
 }
 
 csa_status csa_hca_layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, const uint16_t* C,

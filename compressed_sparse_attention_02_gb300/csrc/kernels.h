@@ -61,6 +61,23 @@ constexpr int kFp4Entry = kDim / 2 + kDim / 16;  // 288: E2M1 codes + one E4M3 s
 constexpr int kPoolBlock = 8;         // entries per block of the hierarchical indexer's pool
 constexpr int kPoolTileBlocks = 16;   // pool blocks per 128-key indexer tile
 
+// RoPE angles as fixed-point fractions of a turn.  Frequency j of the
+// partial RoPE, theta^(-2j/R), is held as f_j / (2 pi) * 2^64 (fp64 on the
+// host, so its relative error is about 2^-52); the angle of an integer
+// position p is then p * f_j / (2 pi) turns, whose fractional part is the
+// low 64 bits of the integer product p * table[j] (a negative p wraps the
+// same way).  Exact integer arithmetic on the device: no angle needs fp64 or
+// a reduction modulo 2 pi; the angle, in [-pi, pi), goes to the hardware
+// sine and cosine (absolute error about 5e-7 there), and the error at
+// position 2^31 stays near 1e-6 rad in all.
+void fill_rope_turns(double theta, uint64_t (&table)[kRope / 2]);
+// sin and cos of position p's angle at the frequency whose table entry is turns.
+__device__ __forceinline__ void rope_sincos(int64_t p, uint64_t turns, float* s, float* c) {
+  const uint64_t frac = static_cast<uint64_t>(p) * turns;  // the angle modulo one turn, in 2^-64 turns
+  const int32_t half = static_cast<int32_t>(frac >> 32);    // in half-turns times 2^31, in [-2^31, 2^31)
+  __sincosf(static_cast<float>(half) * 1.4629180792671596e-09f, s, c);  // pi * 2^-31
+}
+
 // ---- compressor --------------------------------------------------------------
 struct CompressArgs {
   int mode;                 // 0: bulk chunk, 1: decode ring (one entry at most)
@@ -76,13 +93,16 @@ struct CompressArgs {
   double rope_theta;
   float rms_eps;
   unsigned* status;
-  double inv_freq[kRope / 2];  // theta^(-2j/R), filled by launch_compress
+  uint64_t rope_turns[kRope / 2];  // theta^(-2j/R) / (2 pi) * 2^64 (fill_rope_turns), by launch_compress
   uint8_t* key_out;            // indexer keys (launch_index_keys): E4M3 rows of kIdxDim
   float* state;                // single-stream step: [B][3][kDim] running (max, sum, weighted sum)
   uint8_t* kv_fp4_out;         // main compressor: entries in the FP4 layout instead of kv_out
   int64_t fp4_stride_b;        // bytes between sequences of kv_fp4_out
 };
-cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
+// keys: optional bulk-mode arguments of the indexer's key compressor for
+// the same entries (same B, m, n_new, entry0): warp 0 of each CTA writes the
+// entry's indexer key too.
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream, const CompressArgs* keys = nullptr);
 // The non-overlapped (single-stream) compressor, block size a.m (1..128):
 // mode 0 bulk over Ca / Za (the stream's C / Z rows) with the optional slot
 // bias Ba; mode 1 one decode token per sequence, Ca / Za [B][kDim], folded
@@ -135,19 +155,22 @@ cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v
 // kernel on the programmatic-launch chain.
 // A decode step's new rows, written into the caches by the step's first
 // kernel (the counters' zeroing) so that they cost no launch of their own:
-// the window row of position t = q_pos[b] into ring slot t mod W, and, where
-// (t+1) mod m == 0, the indexer key of entry (t+1)/m - 1 (kI_new optional).
-// Sequences with t < 0 are skipped, and so is an entry past n_cap.
+// the window row of position t = q_pos[b] into ring slot t mod W (swa_new
+// optional), and, where (t+1) mod m == 0, the indexer key of entry
+// (t+1)/m - 1: copied from kI_new, or computed by the key compressor from
+// its staging ring (`keys`, ring mode).  Sequences with t < 0 are skipped,
+// and so is an entry past n_cap.
 struct DecodeAppend {
   const int32_t* q_pos;
   int B, W, m;
-  const uint16_t* swa_new;  // [B][kDim] bf16
+  const uint16_t* swa_new;  // [B][kDim] bf16, or null
   uint16_t* swa_ring;       // [B][W][kDim] bf16
   const uint8_t* kI_new;    // [B][kIdxDim] e4m3, or null
   uint8_t* kI;              // [B][n_cap][kIdxDim] e4m3
   int64_t n_cap;
 };
-cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append = nullptr);
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append = nullptr,
+                        const CompressArgs* keys = nullptr);
 
 // ---- top-k -------------------------------------------------------------------------
 struct TopkArgs {
@@ -214,7 +237,7 @@ struct AttnArgs {
   float* part_ml;
   int gsplit_cap;
   int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
-  double inv_freq[kRope / 2];  // theta^(-2j/R), host fp64
+  uint64_t rope_turns[kRope / 2];  // theta^(-2j/R) / (2 pi) * 2^64 (fill_rope_turns)
   unsigned* status;
   // set by launch_sparse_attn: tensor maps of the window buffer and of the
   // bf16 cache exist, so tiles of 128 consecutive present rows load by TMA

@@ -761,7 +761,7 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
     if (ride_along->mode != 1 || ride_along->B != a.B || !topk_can_carry_compress(ride_along->m) || second)
       return cudaErrorInvalidValue;
     c = *ride_along;
-    fill_inv_freq(&c);
+    fill_rope(&c);
   }
   TopkArgs b = {};  // no second problem: B = 0
   int64_t chunks = (topk_extent(a) + kItems - 1) / kItems;
@@ -793,20 +793,31 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
 // the top-k's per-call counters.  A kernel on the programmatic-launch chain
 // (it signals its dependents on entry and waits for its predecessor before
 // writing), so that the launches around it still overlap, which a memset node
-// would not allow.  With a DecodeAppend, B more CTAs (one per sequence) write
-// the step's new window row and indexer key into the caches.
+// would not allow.  With a DecodeAppend, B more CTAs (one per sequence, the
+// grid's first, so that they are dispatched before the zeroing CTAs) write
+// the step's new window row and indexer key into the caches; the key
+// compressor (`key`, ring mode, B > 0) runs on warps 4..7 of those CTAs.
 namespace {
 __global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t words, const int zero_blocks,
-                                                   const DecodeAppend ap) {
+                                                   const DecodeAppend ap, const CompressArgs key) {
   pdl_launch_dependents();
   pdl_wait();
-  if (static_cast<int>(blockIdx.x) >= zero_blocks) {  // one CTA per sequence: its new rows
-    const int b = static_cast<int>(blockIdx.x) - zero_blocks;
+  const int seq_blocks = static_cast<int>(gridDim.x) - zero_blocks;
+  if (static_cast<int>(blockIdx.x) < seq_blocks) {  // one CTA per sequence: its new rows
+    __shared__ float red[4], xch[kIdxDim];
+    const int b = static_cast<int>(blockIdx.x);
+    const int c = threadIdx.x;
+    constexpr int kRowChunks = kDim * 2 / 16, kKeyChunks = kIdxDim / 16, kKeyThread0 = 128;
+    static_assert(kRowChunks + kKeyChunks <= kKeyThread0 && kKeyThread0 + kIdxDim == 256, "threads' roles");
+    if (c >= kKeyThread0) {  // (reads the position itself, with its other loads)
+      if (key.B > 0)
+        index_key_entry_wide_m(key, b, c - kKeyThread0, red, xch, [] { named_bar_sync(1, kIdxDim); });
+      return;
+    }
     const int64_t t = ap.q_pos[b];
     if (t < 0) return;
-    const int c = threadIdx.x;
-    constexpr int kRowChunks = kDim * 2 / 16, kKeyChunks = kIdxDim / 16;
     if (c < kRowChunks) {
+      if (!ap.swa_new) return;
       const uint4* src = reinterpret_cast<const uint4*>(ap.swa_new + static_cast<int64_t>(b) * kDim);
       uint4* dst = reinterpret_cast<uint4*>(ap.swa_ring + (static_cast<int64_t>(b) * ap.W + t % ap.W) * kDim);
       dst[c] = src[c];
@@ -822,24 +833,30 @@ __global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t wo
   }
   const int64_t n4 = words / 4;
   const int64_t step = static_cast<int64_t>(zero_blocks) * blockDim.x;
+  const int64_t zb = static_cast<int64_t>(blockIdx.x) - seq_blocks;
   uint4* p4 = reinterpret_cast<uint4*>(p);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += step)
-    p4[i] = make_uint4(0u, 0u, 0u, 0u);
-  for (int64_t i = n4 * 4 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < words; i += step)
-    p[i] = 0u;
+  for (int64_t i = zb * blockDim.x + threadIdx.x; i < n4; i += step) p4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = n4 * 4 + zb * blockDim.x + threadIdx.x; i < words; i += step) p[i] = 0u;
 }
 }  // namespace
 
-cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append) {
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream, const DecodeAppend* append,
+                        const CompressArgs* keys) {
   const int64_t words = static_cast<int64_t>(bytes / 4);
   const int rows = append ? append->B : 0;
+  CompressArgs k = {};  // B = 0: no key compressor
+  if (keys) {
+    if (!append || keys->mode != 1 || keys->B != append->B || keys->m != append->m) return cudaErrorInvalidValue;
+    k = *keys;
+    fill_rope(&k);
+  }
   if (words <= 0 && rows == 0) return cudaSuccess;
   int64_t blocks = words > 0 ? (words / 4 + 255) / 256 : 0;
   blocks = words <= 0 ? 0 : (blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks));
   static_assert(kDim * 2 / 16 + kIdxDim / 16 <= 256, "one CTA copies a sequence's new rows");
   return launch_pdl(zero_kernel, dim3(static_cast<unsigned>(blocks + rows)), dim3(256), 0, stream,
                     static_cast<uint32_t*>(p), words, static_cast<int>(blocks),
-                    append ? *append : DecodeAppend{});
+                    append ? *append : DecodeAppend{}, k);
 }
 
 }  // namespace csa

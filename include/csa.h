@@ -488,7 +488,7 @@ csa_status csa_sparse_attn(const csa_params *p, int32_t B, int32_t Q,
  *         token u sits in slot u mod 2m and the slots hold tokens t-2m+1..t.
  * kI    : [B][n_cap][128] e4m3 — must already hold entries 0..V(t)-1 (the
  *         indexer keys come from a separate compressor that is not part of
- *         this call).
+ *         this call; csa_layer_decode_with_keys computes the step's key).
  * swa_ring: [B][W][512] bf16 holding positions t-W+1..t (slot u mod W).
  * idx_out: [B][topk] int32 (the selection), out [B][64][512], lse [B][64] or NULL.
  */
@@ -533,6 +533,56 @@ csa_status csa_layer_decode_append(
     size_t workspace_bytes, void *stream);
 
 /*
+ * csa_index_key_src — the inputs of the lightning indexer's own key
+ * compressor (width 128; the steps of csa_compress_indexer_keys), for the
+ * layer calls that compute their indexer keys themselves.  [hca_csa]
+ * "CSA：轻压缩 + 稀疏选择": the indexer compresses its keys at its own width
+ * with the main cache's entry numbering, then rotates them by H_128/sqrt(128)
+ * and stores FP8 codes.
+ *
+ * Decode (csa_layer_decode_with_keys): CIa, ZIa, CIb, ZIb are staging rings
+ *   [B][2m][128] bf16 laid out as the main compressor's ring (the row of
+ *   token u in slot u mod 2m, holding tokens t-2m+1..t); CIb_prev and
+ *   ZIb_prev are not read.
+ * Prefill (csa_layer_prefill_with_keys): CIa, ZIa, CIb, ZIb are [B][Q][128]
+ *   bf16 rows of the chunk's tokens; CIb_prev, ZIb_prev [B][m][128] the rows
+ *   of the block before the chunk, NULL iff pos0 == 0.
+ * BIa, BIb [m][128] bf16 slot biases; rms_wI [128] bf16 RMSNorm weight.
+ * All pointers are device pointers owned by the caller, 16-byte aligned.
+ */
+typedef struct csa_index_key_src {
+  const uint16_t *CIa, *ZIa, *CIb, *ZIb;
+  const uint16_t *CIb_prev, *ZIb_prev;
+  const uint16_t *BIa, *BIb;
+  const uint16_t *rms_wI;
+} csa_index_key_src;
+
+/*
+ * csa_layer_decode_with_keys — csa_layer_decode_append whose indexer key is
+ * computed by the call instead of given: one decode step that needs nothing
+ * but the staging rings, the caches and the queries.  The step's first
+ * kernel (the one that clears the counters) stores swa_new (if not NULL)
+ * into swa_ring slot t mod W and, where (t+1) % m == 0, computes the key of
+ * entry i = (t+1)/m - 1 from the key compressor's ring (*keys) into kI[b, i]
+ * before the indexer reads it; then the steps of csa_layer_decode.  keys is
+ * a host pointer to the struct (read during the call); its arrays and every
+ * other pointer are as for csa_layer_decode_append, except that swa_new may
+ * be NULL.  Errors: those of csa_layer_decode; CSA_ERR_INVALID_ARG for a
+ * NULL keys or a NULL or unaligned array in it; CSA_ERR_UNSUPPORTED for
+ * index_format 1 (this compressor writes E4M3 keys).
+ */
+csa_status csa_layer_decode_with_keys(
+    const csa_params *p, int32_t B, const int32_t *q_pos,
+    const uint16_t *swa_new, const csa_index_key_src *keys,
+    const uint16_t *ring_Ca, const uint16_t *ring_Za, const uint16_t *ring_Cb,
+    const uint16_t *ring_Zb, const uint16_t *Ba, const uint16_t *Bb,
+    const uint16_t *rms_w, void *kv_comp, int64_t n_cap,
+    uint8_t *kI, const uint8_t *qI, const uint16_t *wI,
+    const uint16_t *q, uint16_t *swa_ring, const float *sink,
+    int32_t *idx_out, uint16_t *out, float *lse, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
  * csa_layer_prefill — one chunk of Q query tokens at positions pos0..pos0+Q-1
  * (pos0 a multiple of m, given on the host), causal per query.
  * [hca_csa] "在 SGLang 里的落点" (large-batch prefill has the decode
@@ -563,6 +613,27 @@ csa_status csa_layer_prefill(
     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * csa_layer_prefill_with_keys — csa_layer_prefill that also computes the
+ * chunk's indexer keys: the compressor launch of step 1 writes, beside each
+ * entry i = pos0/m .. (pos0+Q)/m - 1 of kv_comp, its indexer key into
+ * kI[b, i] from *keys (prefill layout, see csa_index_key_src), so that kI
+ * need only hold entries 0..pos0/m - 1 beforehand.  keys is a host pointer
+ * read during the call; kI is written, hence not const.  Errors: those of
+ * csa_layer_prefill; CSA_ERR_INVALID_ARG for a NULL keys, a NULL or
+ * unaligned array in it, or CIb_prev/ZIb_prev not NULL exactly when
+ * pos0 == 0; CSA_ERR_UNSUPPORTED for index_format 1.
+ */
+csa_status csa_layer_prefill_with_keys(
+    const csa_params *p, int32_t B, int32_t Q, int64_t pos0,
+    const uint16_t *Ca, const uint16_t *Za, const uint16_t *Cb,
+    const uint16_t *Zb, const uint16_t *Cb_prev, const uint16_t *Zb_prev,
+    const uint16_t *Ba, const uint16_t *Bb, const uint16_t *rms_w,
+    const csa_index_key_src *keys, void *kv_comp, int64_t n_cap, uint8_t *kI,
+    const uint8_t *qI, const uint16_t *wI, const uint16_t *q,
+    const uint16_t *swa, const float *sink, int32_t *idx_out, uint16_t *out,
+    float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * csa_hca_layer_decode — one decode step of an HCA layer (block size p->m,
  * 128 in the pages; no indexer) for B sequences ([hca_csa] "HCA：同一个算子，
  * 关掉重叠"; [CSA2 详解] §9: the layer reads every causally visible entry):
@@ -589,10 +660,11 @@ csa_status csa_hca_layer_decode(const csa_params *p, int32_t B,
 
 /*
  * Optional stage tracing, for profiling.  With events != NULL (n_events == 5
- * cudaEvent_t handles passed as void*), every csa_layer_decode and
- * csa_layer_prefill call records events[0] on its stream before its first
- * kernel and events[s] after stage s: 1 compressor, 2 indexer scores, 3 top-k,
- * 4 sparse attention.  csa_index_topk, csa_index_topk_pool and csa_reindex_topk record
+ * cudaEvent_t handles passed as void*), every csa_layer_decode(_append,
+ * _with_keys) and csa_layer_prefill(_with_keys) call records events[0] on
+ * its stream before its first kernel and events[s] after stage s: 1 the
+ * first kernel (counters cleared, new rows stored, indexer key computed) and
+ * the compressor, 2 indexer scores, 3 top-k, 4 sparse attention.  csa_index_topk, csa_index_topk_pool and csa_reindex_topk record
  * events[1] before their indexer kernel (after clearing their workspace),
  * events[2] after it and events[3] after their top-k launches.  events ==
  * NULL turns tracing off.  The setting is process-wide; set it only while no

@@ -31,7 +31,7 @@ _IDS = {name: i for i, name in enumerate([
     "Ca", "Za", "Cb", "Zb", "Ba", "Bb", "rms_w", "q", "qI", "wI", "kI", "sink", "kv", "swa",
     "Cb_prev", "Zb_prev", "ring_Ca", "ring_Za", "ring_Cb", "ring_Zb",
     "CIa", "ZIa", "CIb", "ZIb", "CIb_prev", "ZIb_prev", "BIa", "BIb", "rms_wI",
-    "C", "Z", "B"])}
+    "C", "Z", "B", "ring_CIa", "ring_ZIa", "ring_CIb", "ring_ZIb"])}
 
 D, H, HI, DI, R = 512, 64, 64, 128, 64
 
@@ -129,6 +129,20 @@ def indexer_compressor_inputs(config: int, B: int, T: int, m: int = 4, device="c
     return out
 
 
+def indexer_ring_inputs(config: int, B: int, m: int = 4, device="cpu") -> dict:
+    """The indexer key compressor's decode staging ring: ring_CIa, ring_ZIa,
+    ring_CIb, ring_ZIb [B, 2m, 128] N(0,1) bf16 (slot u mod 2m holds token
+    u's row), with the block biases and RMSNorm weight of
+    indexer_compressor_inputs."""
+    s = 1000 * config
+    out = {n: _per_seq(B, config, n, (2 * m, DI), device, bf16) for n in ("ring_CIa", "ring_ZIa", "ring_CIb",
+                                                                          "ring_ZIb")}
+    out["BIa"] = bf16(normal((m, DI), s, "BIa", device))
+    out["BIb"] = bf16(normal((m, DI), s, "BIb", device))
+    out["rms_wI"] = bf16(1.0 + 0.1 * normal((DI,), s, "rms_wI", device))
+    return out
+
+
 def indexer_query(config: int, B: int, Q: int, device="cpu") -> dict:
     return {
         "qI": _per_seq(B, config, "qI", (Q, HI, DI), device, e4m3),
@@ -180,8 +194,9 @@ def decode_inputs(w: Workload, device="cpu", B: int | None = None) -> dict:
 
     The cache holds entries 0..n_cap-1 as unit-RMS rows (the entry the step
     emits, V(t)-1 when (t+1) % m == 0, is overwritten by the step), the indexer
-    keys for all n_cap entries, the staging ring of the last 2m tokens'
-    compressor rows, the window ring and the queries.
+    keys for all n_cap entries, the staging rings of the last 2m tokens'
+    compressor rows (main and indexer-key compressors), the window ring and
+    the queries.
     """
     B = w.B if B is None else B
     c = w.config
@@ -194,6 +209,7 @@ def decode_inputs(w: Workload, device="cpu", B: int | None = None) -> dict:
     out.update({k: v for k, v in zip(
         ("ring_Ca", "ring_Za", "ring_Cb", "ring_Zb"),
         compressor_rows(c, B, 2 * w.m, device, names=("ring_Ca", "ring_Za", "ring_Cb", "ring_Zb")).values())})
+    out.update(indexer_ring_inputs(c, B, w.m, device))
     out["q_pos"] = torch.full((B, 1), w.t, dtype=torch.int32, device=device)
     return out
 
@@ -203,8 +219,10 @@ def prefill_inputs(w: Workload, device="cpu", Q: int | None = None) -> dict:
 
     The cache holds pos0/m existing entries (unit-RMS rows); the chunk's
     compressor rows produce the next Q/m entries.  Indexer keys are given for
-    every entry up to (pos0+Q)/m.  The window buffer is linear: row j is
-    position pos0-(W-1)+j.
+    every entry up to (pos0+Q)/m, and the indexer key compressor's rows of the
+    chunk (CIa..ZIb, CIb_prev, ZIb_prev) for the calls that compute the
+    chunk's keys.  The window buffer is linear: row j is position
+    pos0-(W-1)+j.
     """
     Q = w.Q if Q is None else Q
     c, B, m = w.config, w.B, w.m
@@ -218,6 +236,7 @@ def prefill_inputs(w: Workload, device="cpu", Q: int | None = None) -> dict:
     out["kv"] = cache_rows(c, B, n_cap, device)
     out["swa"] = cache_rows(c, B, w.W - 1 + Q, device, name="swa")
     out["q"] = main_query(c, B, Q, device)
+    out.update(indexer_compressor_inputs(c, B, Q, m, device))
     out["n_cap"] = n_cap
     return out
 

@@ -107,3 +107,21 @@ def unpack_index_query_fp4(buf, nq):
     codes = buf[:nq * 4096].reshape(nq, 64, 64)
     sp = buf[nq * 4096:nq * 4608].reshape(nq, 32, 16)
     return codes, np.concatenate([sp[:, :, 0:4], sp[:, :, 4:8]], axis=1), sp[:, :, 8:]
+
+
+def check_key_codes(got, pre, codes, what):
+    """Equal E4M3 codes, except where the oracle's value sits within a relative
+    1e-4 of the midpoint between two neighbouring codes: there the kernel's
+    fp32 rounding may land on either side (both codes are then accepted)."""
+    import oracle
+    got = np.asarray(got, dtype=np.uint8).ravel()
+    codes = np.asarray(codes, dtype=np.uint8).ravel()
+    pre = np.asarray(pre, dtype=np.float64).ravel()
+    diff = np.nonzero(got != codes)[0]
+    for j in diff:
+        a, b = oracle.e4m3_to_f64(np.array([got[j], codes[j]], dtype=np.uint8))
+        mid = (a + b) / 2
+        assert abs(int(got[j] & 0x7F) - int(codes[j] & 0x7F)) <= 1 and (got[j] & 0x80) == (codes[j] & 0x80), \
+            "%s: element %d code %#x vs %#x" % (what, j, got[j], codes[j])
+        assert abs(pre[j] - mid) <= 1e-4 * abs(mid) + 1e-9, "%s: element %d not at a rounding midpoint" % (what, j)
+    return len(diff)

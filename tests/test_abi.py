@@ -168,6 +168,49 @@ def test_layer_decode_append_argument_checks(lib):
     assert call(lib.csa_default_params(index_format=1), fake, fake) == 2
 
 
+def test_layer_calls_with_keys_argument_checks(lib):
+    """The layer calls that compute their own indexer keys refuse on the host,
+    before any launch: no key source, a null or misaligned array in it, the
+    previous-block rows not given exactly when the chunk does not start the
+    sequence, FP4 index keys; the size of the source struct is nine pointers."""
+    raw = ctypes.CDLL(lib.LIBRARY_PATH)
+    raw.csa_layer_decode_with_keys.restype = ctypes.c_int
+    raw.csa_layer_prefill_with_keys.restype = ctypes.c_int
+    assert ctypes.sizeof(lib.CsaIndexKeySrc) == 9 * ctypes.sizeof(ctypes.c_void_p)
+    fake, odd = 0x10000, 0x10008
+    i64 = ctypes.c_int64
+
+    def src(**kw):
+        f = {n: fake for n in ("CIa", "ZIa", "CIb", "ZIb", "BIa", "BIb", "rms_wI")}
+        f.update(kw)
+        return lib.CsaIndexKeySrc(**f)
+
+    def dec(p, keys):
+        return raw.csa_layer_decode_with_keys(ctypes.byref(p), 1, ctypes.c_void_p(fake), None,
+                                              None if keys is None else ctypes.byref(keys),
+                                              *([ctypes.c_void_p(fake)] * 7), i64(4096),
+                                              *([ctypes.c_void_p(fake)] * 9), ctypes.c_void_p(fake),
+                                              ctypes.c_size_t(1 << 30), None)
+
+    def pre(p, keys, pos0):
+        prev = [ctypes.c_void_p(fake) if pos0 else None] * 2
+        return raw.csa_layer_prefill_with_keys(ctypes.byref(p), 1, 16, i64(pos0), *([ctypes.c_void_p(fake)] * 4),
+                                               *prev, *([ctypes.c_void_p(fake)] * 3),
+                                               None if keys is None else ctypes.byref(keys), ctypes.c_void_p(fake),
+                                               i64(4096), *([ctypes.c_void_p(fake)] * 9), ctypes.c_void_p(fake),
+                                               ctypes.c_size_t(1 << 30), None)
+    p = lib.csa_default_params()
+    assert dec(p, None) == 1
+    assert dec(p, src(CIa=None)) == 1
+    assert dec(p, src(rms_wI=odd)) == 1
+    assert dec(lib.csa_default_params(index_format=1), src()) == 2
+    assert pre(p, None, 0) == 1
+    assert pre(p, src(BIb=None), 0) == 1
+    assert pre(p, src(CIb_prev=fake, ZIb_prev=fake), 0) == 1  # block -1 does not exist
+    assert pre(p, src(), 64) == 1  # its rows are needed past the first chunk
+    assert pre(lib.csa_default_params(index_format=1), src(), 0) == 2
+
+
 def test_fp4_indexer_argument_checks(lib):
     """FP4 indexer rows: sizes of the layouts, and host-side refusals (no launch)."""
     assert lib.index_keys_fp4_bytes(2, 300) == 2 * (300 * 64 + 3 * 512)

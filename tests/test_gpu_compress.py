@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synthetic as syn
-from _util import assert_close, bits
+from _util import assert_close, bits, check_key_codes
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -135,23 +135,6 @@ def test_decode_emission_from_ring(csa):
         others = np.ones(n_cap, bool)
         others[i] = False
         np.testing.assert_array_equal(got[b, others], ref[b, others])
-
-
-def check_key_codes(got, pre, codes, what):
-    """Equal E4M3 codes, except where the oracle's value sits within a relative
-    1e-4 of the midpoint between two neighbouring codes: there the kernel's
-    fp32 rounding may land on either side (both codes are then accepted)."""
-    got = np.asarray(got, dtype=np.uint8).ravel()
-    codes = np.asarray(codes, dtype=np.uint8).ravel()
-    pre = np.asarray(pre, dtype=np.float64).ravel()
-    diff = np.nonzero(got != codes)[0]
-    for j in diff:
-        a, b = oracle.e4m3_to_f64(np.array([got[j], codes[j]], dtype=np.uint8))
-        mid = (a + b) / 2
-        assert abs(int(got[j] & 0x7F) - int(codes[j] & 0x7F)) <= 1 and (got[j] & 0x80) == (codes[j] & 0x80), \
-            "%s: element %d code %#x vs %#x" % (what, j, got[j], codes[j])
-        assert abs(pre[j] - mid) <= 1e-4 * abs(mid) + 1e-9, "%s: element %d not at a rounding midpoint" % (what, j)
-    return len(diff)
 
 
 @pytest.mark.parametrize("m,B,n_new,entry0", [(4, 2, 37, 0), (4, 3, 29, 1021), (8, 1, 9, 3), (1, 2, 50, 7)])

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synthetic as syn
-from _util import assert_close, bits, check_topk
+from _util import assert_close, bits, check_key_codes, check_topk
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -222,3 +222,157 @@ def test_layer_prefill_chunk_of_4096_at_61440(csa):
     kv, idx, out, lse = run_prefill(csa, p, w, x)
     qs = sorted(set(list(range(8)) + list(range(w.Q - 8, w.Q)) + list(range(0, w.Q, 256))))
     check_prefill(w, x, kv, idx, out, lse, 0, qs)
+
+
+def decode_keys_src(csa, x):
+    return csa.index_key_src(x["ring_CIa"], x["ring_ZIa"], x["ring_CIb"], x["ring_ZIb"], x["BIa"], x["BIb"],
+                             x["rms_wI"])
+
+
+def oracle_ring_key(x, b, t, m):
+    """The oracle's indexer key of the entry completing at t, from sequence
+    b's staging ring (slot u mod 2m holds token u)."""
+    i = (t + 1) // m - 1
+    sa = [(m * i + r) % (2 * m) for r in range(m)]
+    sb = [(m * (i - 1) + r) % (2 * m) for r in range(m)]
+    return oracle.index_key_entry(i, bits(x["ring_CIa"][b])[sa], bits(x["ring_ZIa"][b])[sa],
+                                  bits(x["ring_CIb"][b])[sb], bits(x["ring_ZIb"][b])[sb], bits(x["BIa"]),
+                                  bits(x["BIb"]), bits(x["rms_wI"]))
+
+
+@pytest.mark.parametrize("cfg,m,t", [(0, 4, 1023), (None, 8, 2399), (None, 2, 598), (None, 1, 0)])
+def test_layer_decode_with_keys(csa, cfg, m, t):
+    """csa_layer_decode_with_keys computes the step's indexer key from the key
+    compressor's staging ring: the kI row it writes matches the oracle's key
+    (E4M3 codes equal but at rounding midpoints); no other row changes (and
+    none at a step that completes no block, or for a sequence at position
+    -1); the rest of the step is bit for bit csa_layer_decode over the kI and
+    window ring so written; and the step is the oracle's layer step over the
+    written keys (emission, selection, attention)."""
+    if cfg is not None:
+        w = syn.WORKLOADS[cfg]
+    else:
+        w = syn.Workload("decode-keys-m%d" % m, 30 + m, "decode", B=3, t=t, topk=32, n_cap=300 if m > 1 else 64, m=m)
+    x = syn.decode_inputs(w, device=DEV)
+    if w.B > 2:
+        x["q_pos"][2] = -1
+    p = csa.csa_default_params(topk=w.topk, m=w.m)
+    swa_new = x["swa"][:, 7].roll(1, dims=0).contiguous()
+    keys = decode_keys_src(csa, x)
+    kv, kI, swa = x["kv"].clone(), x["kI"].clone(), x["swa"].clone()
+    B = w.B
+    idx = torch.empty(B, p.topk, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, w.n_cap)
+    csa.csa_layer_decode_with_keys(p, B, x["q_pos"], swa_new, keys, x["ring_Ca"], x["ring_Za"], x["ring_Cb"],
+                                   x["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], kv, w.n_cap, kI, x["qI"], x["wI"],
+                                   x["q"], swa, x["sink"], idx, out, lse, ws)
+    st = csa.csa_check_status()
+    assert st == 0, csa.csa_status_string(st)
+    kI_g = kI.view(torch.uint8).cpu().numpy()
+    kI_0 = x["kI"].view(torch.uint8).cpu().numpy()
+    qp = x["q_pos"].view(-1).cpu().numpy()
+    for b in range(B):
+        others = np.ones(w.n_cap, bool)
+        if qp[b] >= 0 and (qp[b] + 1) % w.m == 0:
+            i = (qp[b] + 1) // w.m - 1
+            pre, codes = oracle_ring_key(x, b, int(qp[b]), w.m)
+            check_key_codes(kI_g[b, i], pre, codes, "decode key b=%d" % b)
+            others[i] = False
+        assert np.array_equal(kI_g[b, others], kI_0[b, others]), "kI rows other than the step's, b=%d" % b
+    # the same step through csa_layer_decode over the caches as written
+    kv2 = x["kv"].clone()
+    idx2, out2, lse2 = torch.empty_like(idx), torch.empty_like(out), torch.empty_like(lse)
+    csa.csa_layer_decode(p, B, x["q_pos"], x["ring_Ca"], x["ring_Za"], x["ring_Cb"], x["ring_Zb"], x["Ba"], x["Bb"],
+                         x["rms_w"], kv2, w.n_cap, kI, x["qI"], x["wI"], x["q"], swa, x["sink"], idx2, out2, lse2, ws)
+    assert csa.csa_check_status() == 0
+    assert torch.equal(idx, idx2) and torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2) and torch.equal(kv.view(torch.int16), kv2.view(torch.int16))
+    # the layer step against the oracle's, over the keys and window as written
+    xo = dict(x)
+    xo["kI"], xo["swa"] = kI, swa
+    idx_c, out_c, lse_c = idx.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+    kv_c = kv.float().cpu().numpy()
+    for b in range(min(B, 2)):
+        check_decode_seq(w, xo, b, bits(x["kv"][b]), kv_c[b], idx_c[b], out_c[b], lse_c[b])
+
+
+def run_prefill_with_keys(csa, p, w, x):
+    B, Q = w.B, w.Q
+    prev = w.pos0 > 0
+    keys = csa.index_key_src(x["CIa"], x["ZIa"], x["CIb"], x["ZIb"], x["BIa"], x["BIb"], x["rms_wI"],
+                             x["CIb_prev"] if prev else None, x["ZIb_prev"] if prev else None)
+    kv, kI = x["kv"].clone(), x["kI"].clone()
+    e0 = w.pos0 // w.m
+    kI[:, e0:] = 0  # the call writes the chunk's keys
+    idx = torch.empty(B, Q, p.topk, dtype=torch.int32, device=DEV)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=DEV)
+    ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, x["n_cap"])
+    csa.csa_layer_prefill_with_keys(p, B, Q, w.pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"],
+                                    x["Cb_prev"] if prev else None, x["Zb_prev"] if prev else None, x["Ba"],
+                                    x["Bb"], x["rms_w"], keys, kv, x["n_cap"], kI, x["qI"], x["wI"], x["q"],
+                                    x["swa"], x["sink"], idx, out, lse, ws)
+    st = csa.csa_check_status()
+    assert st == 0, csa.csa_status_string(st)
+    return kv, kI, idx, out, lse, ws
+
+
+def check_prefill_keys(csa, p, w, x, kv, kI, idx, out, lse, ws):
+    """The chunk's keys against the oracle's; rows before the chunk kept; the
+    step bit for bit csa_layer_prefill over the keys as written."""
+    m, Q, pos0, B = w.m, w.Q, w.pos0, w.B
+    e0, n_new = pos0 // m, (pos0 + Q) // m - pos0 // m
+    prev = pos0 > 0
+    kI_g = kI.view(torch.uint8).cpu().numpy()
+    kI_0 = x["kI"].view(torch.uint8).cpu().numpy()
+    near = 0
+    for b in range(B):
+        pre, codes = oracle.index_keys(e0, n_new, bits(x["CIa"][b])[: m * n_new], bits(x["ZIa"][b])[: m * n_new],
+                                       bits(x["CIb"][b])[: m * n_new], bits(x["ZIb"][b])[: m * n_new],
+                                       bits(x["CIb_prev"][b]) if prev else None,
+                                       bits(x["ZIb_prev"][b]) if prev else None, bits(x["BIa"]), bits(x["BIb"]),
+                                       bits(x["rms_wI"]), m=m)
+        near += check_key_codes(kI_g[b, e0:e0 + n_new], pre, codes, "prefill keys b=%d" % b)
+        assert np.array_equal(kI_g[b, :e0], kI_0[b, :e0]), "rows before the chunk b=%d" % b
+    assert near <= 0.01 * B * n_new * 128 + 1
+    kv2 = x["kv"].clone()
+    idx2, out2, lse2 = torch.empty_like(idx), torch.empty_like(out), torch.empty_like(lse)
+    csa.csa_layer_prefill(p, B, Q, pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"] if prev else None,
+                          x["Zb_prev"] if prev else None, x["Ba"], x["Bb"], x["rms_w"], kv2, x["n_cap"], kI, x["qI"],
+                          x["wI"], x["q"], x["swa"], x["sink"], idx2, out2, lse2, ws)
+    assert csa.csa_check_status() == 0
+    assert torch.equal(idx, idx2) and torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2) and torch.equal(kv.view(torch.int16), kv2.view(torch.int16))
+
+
+@pytest.mark.parametrize("B,Q,pos0,k", [(2, 64, 512, 64), (1, 70, 0, 16), (3, 45, 8, 32)])
+def test_layer_prefill_with_keys_small(csa, B, Q, pos0, k):
+    """Small chunks (the first block, and ragged chunks computed sequence by
+    sequence): the chunk's keys, then every query's selection and attention
+    against the oracle over the keys as written."""
+    w = syn.Workload("prefill-keys", 70 + Q, "prefill", B=B, t=pos0 + Q - 1, topk=k, n_cap=0, Q=Q, pos0=pos0)
+    x = syn.prefill_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=k)
+    kv, kI, idx, out, lse, ws = run_prefill_with_keys(csa, p, w, x)
+    check_prefill_keys(csa, p, w, x, kv, kI, idx, out, lse, ws)
+    xo = dict(x)
+    xo["kI"] = kI
+    idx_c, lse_c = idx.cpu().numpy(), lse.cpu().numpy()
+    for b in range(B):
+        check_prefill(w, xo, kv, idx_c, out, lse_c, b, range(Q))
+
+
+def test_layer_prefill_with_keys_chunk_of_4096_at_61440(csa):
+    """The chunked-prefill configuration at full size with the chunk's 1024
+    indexer keys computed by the call."""
+    w = syn.WORKLOADS[4]
+    x = syn.prefill_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=w.topk)
+    kv, kI, idx, out, lse, ws = run_prefill_with_keys(csa, p, w, x)
+    check_prefill_keys(csa, p, w, x, kv, kI, idx, out, lse, ws)
+    xo = dict(x)
+    xo["kI"] = kI
+    qs = [0, 1, 2047, 4095]
+    check_prefill(w, xo, kv, idx.cpu().numpy(), out, lse.cpu().numpy(), 0, qs)
