@@ -312,6 +312,16 @@ def csa_layer_prefill(params, B, Q, pos0, Ca, Za, Cb, Zb, Cb_prev, Zb_prev, Ba, 
                                   _stream(stream)), "csa_layer_prefill")
 
 
+CSA_TEST_FAULT_INDEXER, CSA_TEST_FAULT_TOPK, CSA_TEST_FAULT_ATTN = 1, 2, 4
+_lib.csa_test_set_wait_fault.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+_lib.csa_test_set_wait_fault.restype = ctypes.c_int
+
+
+def csa_test_set_wait_fault(wait_limit_us, faults):
+    """Test-only: device wait limit (us, 0 = default) and withheld signals (CSA_TEST_FAULT_*)."""
+    _check(_lib.csa_test_set_wait_fault(wait_limit_us, faults), "csa_test_set_wait_fault")
+
+
 def csa_check_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status."""
     return int(_lib.csa_check_status(_stream(stream)))

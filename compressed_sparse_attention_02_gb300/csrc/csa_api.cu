@@ -25,8 +25,10 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 namespace {
 
 // Device status word: kernels OR error bits into it, csa_check_status reads
-// and clears it.  One per device (module globals are per context).
-__device__ unsigned g_status_word;
+// and clears it.  One per device (module globals are per context).  The
+// words after it hold the test faults and test wait limit (see ptx.cuh),
+// zero unless csa_test_set_wait_fault set them.
+__device__ unsigned g_status_word[4];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -988,6 +990,19 @@ csa_status csa_set_trace_events(void* const* events, int32_t n_events) {
   }
   g_trace_on = true;
   return CSA_OK;
+}
+
+csa_status csa_test_set_wait_fault(uint32_t wait_limit_us, uint32_t faults) {
+  if (faults & ~(CSA_TEST_FAULT_INDEXER | CSA_TEST_FAULT_TOPK | CSA_TEST_FAULT_ATTN)) return CSA_ERR_INVALID_ARG;
+  if (faults && wait_limit_us == 0) return CSA_ERR_INVALID_ARG;  // a fault waits out the test limit only
+  unsigned* p = status_ptr();
+  if (!p) return CSA_ERR_CUDA;
+  static_assert(CSA_TEST_FAULT_INDEXER == csa::kFaultIndexer && CSA_TEST_FAULT_TOPK == csa::kFaultTopk &&
+                    CSA_TEST_FAULT_ATTN == csa::kFaultAttn,
+                "fault bits");
+  const unsigned words[2] = {faults, wait_limit_us};
+  if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;  // no kernel reads them meanwhile
+  return cudaMemcpy(p + 1, words, sizeof words, cudaMemcpyHostToDevice) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
 
 csa_status csa_check_status(void* stream) {

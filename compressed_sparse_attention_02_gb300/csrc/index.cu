@@ -332,6 +332,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
         fence_proxy_async_smem();
         __syncwarp();
       }
+      if (it == 0 && test_fault(a.status, kFaultIndexer)) {  // test fault: the first tile is never loaded (the MMA's wait gives up)
+        ++it;
+        continue;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&full[st], kKeyTileBytes);
       if (lane < kPoolTileBlocks) {
         const int32_t blk = (id >= 0 && id < n_blk) ? id : 0;
@@ -393,6 +397,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
         const int s = it % STAGES;
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
         if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
+        if (it == 0 && test_fault(a.status, kFaultIndexer)) {  // test fault: the first tile is never loaded (the MMA's wait gives up)
+          ++it;
+          continue;
+        }
         mbar_arrive_expect_tx(&full[s], kKeyTileBytes + Cfg::SF);
         tma_load_3d(k_s + s * kKeyTileBytes, &tm_k, 0, static_cast<int32_t>(tile * kTileKeys), gi.b, &full[s], pol);
         if constexpr (kFp4)

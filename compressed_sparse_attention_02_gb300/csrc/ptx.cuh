@@ -16,6 +16,18 @@ enum : unsigned { kErrTimeout = 1u << 0, kErrIndexRange = 1u << 1 };
 // kErrTimeout instead of spinning forever.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// The status word is the first of four: [1] holds test faults (bits below,
+// 0 outside tests) and [2] a test wait limit in microseconds (0: the default
+// above); both are set only through csa_test_set_wait_fault.
+enum : unsigned { kFaultIndexer = 1u << 0, kFaultTopk = 1u << 1, kFaultAttn = 1u << 2 };
+__device__ __forceinline__ uint64_t wait_limit_ns(const unsigned* status) {
+  const unsigned us = status ? __ldcg(status + 2) : 0u;
+  return us ? static_cast<uint64_t>(us) * 1000ull : kWaitLimitNs;
+}
+__device__ __forceinline__ bool test_fault(const unsigned* status, unsigned bit) {
+  return status && (__ldcg(status + 1) & bit) != 0u;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -62,13 +74,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the completion of the phase with the given parity.  Returns false
-// (and records kErrTimeout) if it has not completed within kWaitLimitNs.
+// (and records kErrTimeout) if it has not completed within the wait limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = global_timer_ns(), limit = wait_limit_ns(status);
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit) {
       record_error(status, kErrTimeout);
       return false;
     }

@@ -122,13 +122,13 @@ __device__ int block_prefix(int cnt, Smem& sm, int* total, int& buf) {
 }
 
 // Waits (cluster-scope acquire) for a phase of a barrier that other CTAs of
-// the cluster complete; gives up after kWaitLimitNs (kErrTimeout recorded).
+// the cluster complete; gives up after the wait limit (kErrTimeout recorded).
 __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, unsigned* status) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = global_timer_ns(), limit = wait_limit_ns(status);
   while (true) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit) {
       record_error(status, kErrTimeout);
       return false;
     }
@@ -372,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     for (int j = 0; j < nslot && j < nmine; ++j) issue(j, j);
   }
   for (int i = t; i < 1024; i += kThreads) sm.h3[i] = 0;
+  // rank 0's results, before they come: read alike by every CTA should a wait give up
+  if (t < 2) sm.res[t] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   // A wait that gives up (status recorded) leaves garbage behind but changes
   // no barrier: every CTA still takes every cluster barrier the cluster takes.
@@ -497,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 4)
     if (g == 0) {
       ok = __syncthreads_and(mbar_wait_cl(&sm.sum_bar, static_cast<uint32_t>(phase), a.status)) && ok;
       const uint4 r = result(find_crossing(bins, nb, need_at, sm));
-      if (t < G) st_async_v4(dsmem_addr(&sm.res[phase], t), r, dsmem_addr(&sm.res_bar[phase], t));
+      // (test fault: the first result is never sent; every CTA's wait gives up)
+      if (t < G && !(phase == 0 && test_fault(a.status, kFaultTopk)))
+        st_async_v4(dsmem_addr(&sm.res[phase], t), r, dsmem_addr(&sm.res_bar[phase], t));
     }
     ok = __syncthreads_and(mbar_wait_cl(&sm.res_bar[phase], 0, a.status)) && ok;
     return sm.res[phase];

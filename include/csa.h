@@ -682,6 +682,33 @@ uint64_t csa_launch_count(void);
  */
 csa_status csa_check_status(void *stream);
 
+/*
+ * csa_test_set_wait_fault — test-only switch for the failure path of the
+ * bounded device waits (failure detection: every wait of the library's
+ * kernels gives up after a limit, records CSA_ERR_TIMEOUT and lets its kernel
+ * finish; a CTA still releases its tensor memory and waits for its own copies
+ * in flight).  Off by default; nothing but this call turns it on.
+ *
+ * wait_limit_us: the limit of every device wait on the current device, in
+ *   microseconds; 0 restores the default (2 s).
+ * faults: OR of the CSA_TEST_FAULT_* bits, each withholding one signal in
+ *   the kernels of later calls so that a wait must give up:
+ *     INDEXER  the lightning indexer's producer never loads its first key
+ *              tile (csa_index_topk and the layer and pool calls);
+ *     TOPK     a top-k cluster's rank 0 never sends its first crossing (rows
+ *              of more than 4096 keys);
+ *     ATTN     the sparse attention's MMA thread never announces the first
+ *              tile's scores (every form: single CTA, cluster, split-KV).
+ *   A non-zero faults needs a non-zero wait_limit_us.
+ * Synchronises the device first.  Process-wide per device: set it only while
+ * no other call runs.  Errors: CSA_ERR_INVALID_ARG for unknown bits or faults
+ * without a limit; CSA_ERR_CUDA.
+ */
+#define CSA_TEST_FAULT_INDEXER 1u
+#define CSA_TEST_FAULT_TOPK 2u
+#define CSA_TEST_FAULT_ATTN 4u
+csa_status csa_test_set_wait_fault(uint32_t wait_limit_us, uint32_t faults);
+
 /* Static, human-readable name of a status code. */
 const char *csa_status_string(csa_status s);
 
