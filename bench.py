@@ -80,6 +80,44 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def bf16_sustained():
+    """The sustained dense bf16 rate (a kernel inside a long call), measured
+    copy if present, else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
+
+
+def fp8_peak(torch, dev):
+    """Dense FP8 E4M3 GEMM rate on this GPU, measured here: torch._scaled_mm
+    of 8192^3 (2*N^3 flops, unit scales, bf16 output), best of 10 after 3
+    warm-up calls.  None if the library call is unavailable."""
+    try:
+        n = 8192
+        g = torch.Generator(device=dev).manual_seed(5)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.ones((), device=dev)
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(10):
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -331,11 +369,16 @@ def attn_warm_l2(csa, torch, w, x, p, B, kv, out, idx, lse, stream):
 
 def prefill_profile(csa, torch, dev):
     """The chunked-prefill layer call of the 64K-context workload (4096 queries
-    at positions 61440..65535 over 16384 entries): stage durations, whole-call
-    time, and the attention's tensor-core rate (prefill attention is where the
-    bf16 tensor peak is the meaningful roofline)."""
+    at positions 61440..65535 over 16384 entries), the self-contained form that
+    also writes the chunk's indexer keys: stage durations, whole-call time, and
+    the tensor-core rates of its two contractions (prefill is where the tensor
+    peaks are the meaningful rooflines): the attention against the sustained
+    bf16 rate (a kernel inside a call of about 2 ms), the indexer's scoring
+    against an FP8 GEMM measured in this process."""
     import synthetic as syn
     hbm, bf16, _ = peaks()
+    bf16_s, bf16_s_src = bf16_sustained()
+    fp8 = fp8_peak(torch, dev)
     w = syn.WORKLOADS[4]
     B, Q = w.B, w.Q
     x = syn.prefill_inputs(w, device=dev)
@@ -345,11 +388,13 @@ def prefill_profile(csa, torch, dev):
     out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B, Q, 64, dtype=torch.float32, device=dev)
     ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, x["n_cap"], device=dev)
+    keys_src = csa.index_key_src(x["CIa"], x["ZIa"], x["CIb"], x["ZIb"], x["BIa"], x["BIb"], x["rms_wI"],
+                                 x["CIb_prev"], x["ZIb_prev"])
 
     def step():
-        csa.csa_layer_prefill(p, B, Q, w.pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"], x["Zb_prev"],
-                              x["Ba"], x["Bb"], x["rms_w"], kv, x["n_cap"], x["kI"], x["qI"], x["wI"], x["q"],
-                              x["swa"], x["sink"], idx, out, lse, ws)
+        csa.csa_layer_prefill_with_keys(p, B, Q, w.pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"],
+                                        x["Zb_prev"], x["Ba"], x["Bb"], x["rms_w"], keys_src, kv, x["n_cap"],
+                                        x["kI"], x["qI"], x["wI"], x["q"], x["swa"], x["sink"], idx, out, lse, ws)
     for _ in range(3):
         step()
     torch.cuda.synchronize()
@@ -375,32 +420,22 @@ def prefill_profile(csa, torch, dev):
     attn_flops = B * 4.0 * 64 * 512 * rows
     pairs = sum(min(x["n_cap"], (t + 1) // w.m) for t in range(w.pos0, w.pos0 + Q))
     index_flops = B * 2.0 * 64 * 128 * pairs
-    res = {"workload": w.name, "tokens_per_s": B * Q / (ms * 1e-3), "ms_per_call": ms,
-           "stages_ms": {"compress": st[0], "index_scores": st[1], "topk": st[2], "sparse_attn": st[3]},
-           "attn_tflops": attn_flops / (st[3] * 1e-3) / 1e12,
-           "attn_tc_frac_of_bf16_peak": attn_flops / (st[3] * 1e-3) / 1e12 / bf16,
-           "index_fp8_tflops": index_flops / (st[1] * 1e-3) / 1e12}
-    # the chunk's indexer keys (the indexer's own compressor, width 128)
+    attn_tf = attn_flops / (st[3] * 1e-3) / 1e12
+    index_tf = index_flops / (st[1] * 1e-3) / 1e12
     n_new = Q // w.m
-    xk = syn.indexer_compressor_inputs(w.config, B, Q, m=w.m, device=dev)
-    kI = torch.empty(B, x["n_cap"], 128, dtype=torch.uint8, device=dev)
-
-    def keys():
-        csa.csa_compress_indexer_keys(p, B, n_new, w.pos0 // w.m, xk["CIa"], xk["ZIa"], xk["CIb"], xk["ZIb"],
-                                      xk["CIb_prev"], xk["ZIb_prev"], xk["BIa"], xk["BIb"], xk["rms_wI"], kI,
-                                      x["n_cap"] * 128)
-    for _ in range(3):
-        keys()
-    e0.record()
-    for _ in range(n):
-        keys()
-    e1.record()
-    torch.cuda.synchronize()
-    kms = e0.elapsed_time(e1) / n
-    kbytes = B * n_new * (4 * w.m * 128 * 2 + 128)
-    res["indexer_keys"] = {"entries": B * n_new, "ms": kms, "gbs": kbytes / (kms * 1e-3) / 1e9,
-                           "hbm_frac": kbytes / (kms * 1e-3) / 1e9 / hbm}
-    del x, xk, kv, kI, idx, out, lse, ws
+    res = {"workload": w.name, "tokens_per_s": B * Q / (ms * 1e-3), "ms_per_call": ms,
+           "stages_ms": {"compress_and_keys": st[0], "index_scores": st[1], "topk": st[2], "sparse_attn": st[3]},
+           "attn_tflops": attn_tf,
+           "attn_tc_frac_of_bf16_peak": attn_tf / bf16,
+           "attn_tc_frac_of_bf16_sustained": attn_tf / bf16_s, "bf16_sustained_tflops": bf16_s,
+           "bf16_sustained_source": bf16_s_src,
+           "index_fp8_tflops": index_tf,
+           "fp8_peak_tflops": fp8, "fp8_peak_source": "torch._scaled_mm e4m3 8192^3, best of 10, this process",
+           "index_fp8_frac": (index_tf / fp8) if fp8 else None,
+           "compress_and_keys": {"entries": B * n_new, "bytes": B * n_new * (4 * w.m * (512 + 128) * 2 + 1024 + 128),
+                                 "note": "main entries (bf16) and indexer keys (E4M3) of the chunk in one launch; "
+                                         "stage time includes the first kernel (counters cleared)"}}
+    del x, kv, idx, out, lse, ws
     torch.cuda.empty_cache()
     return res
 
