@@ -402,7 +402,7 @@ __device__ __forceinline__ void index_key_entry_wide(const CompressArgs& a, int 
                                                      Sync sync) {
   float y[1];
   int64_t i;
-  if (!compress_values<M, 1, kIdxDim, Sync, false, true>(a, b, 0, t, red, sync, y, &i)) return;
+  if (!compress_values<M, 1, kIdxDim, Sync, false, (M <= 4)>(a, b, 0, t, red, sync, y, &i)) return;
   float v = y[0];
 #pragma unroll
   for (int st = 0; st < 5; ++st) {

@@ -299,6 +299,10 @@ __device__ void compress_ride_along(const CompressArgs& c, int b, Smem& sm) {
 // hold alike.
 constexpr size_t kValsOff = (sizeof(Smem) + 127) / 128 * 128;
 
+// kMulti: some rows of the launch give a CTA more than one chunk; without
+// it every CTA holds at most one (and the kernel carries none of the code of
+// the longer rows, a smaller instruction footprint for the common launches).
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 4)
     topk_kernel(const __grid_constant__ TopkArgs a0, const __grid_constant__ TopkArgs a1, const CompressArgs comp,
                 const int G, const int slot_shift) {
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int nmine = static_cast<int>(min(c0 + cpc, nch) - c0);
   const int64_t i_lo = c0 * kItems;
   const int64_t i_hi = nmine > 0 ? min(i_lo + static_cast<int64_t>(nmine) * kItems, V) : i_lo;
-  const bool resident = cpc == 1;  // the CTA's only chunk stays staged in slot 0 throughout
+  const bool resident = !kMulti || cpc == 1;  // the CTA's only chunk stays staged in slot 0 throughout
   const bool bf16 = a.bf16_scores != 0;
   const int esz = bf16 ? 2 : 4;
   // the CTA's bitmap words: on chip, or (ranges of more than 8 chunks) the row's global scratch
@@ -730,11 +734,13 @@ int max_cluster() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < kDevices && cached[dev] > 0) return cached[dev];
   const size_t smem_max = kValsOff + size_t(kMaxSlots) * kItems * 4;
-  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max)) !=
-      cudaSuccess)
-    return 0;
+  for (auto k : {topk_kernel<false>, topk_kernel<true>})
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max)) !=
+        cudaSuccess)
+      return 0;
   int g = 8;
-  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+  if (cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+      cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kMaxCluster;
@@ -747,7 +753,7 @@ int max_cluster() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) == cudaSuccess && n > 0) g = kMaxCluster;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_kernel<true>, &cfg) == cudaSuccess && n > 0) g = kMaxCluster;
   }
   cudaGetLastError();  // a refused size is not an error of a launch
   if (dev >= 0 && dev < kDevices) cached[dev] = g;
@@ -789,8 +795,9 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
   const int64_t z = static_cast<int64_t>(a.B) + b.B + extra;
   if (z > 65535) return cudaErrorInvalidValue;
   const size_t smem = kValsOff + (size_t(1) << slot_shift) * kItems * 4;
-  return launch_pdl_cluster(topk_kernel, dim3(static_cast<unsigned>(G), q, static_cast<unsigned>(z)), dim3(kThreads),
-                            smem, stream, static_cast<unsigned>(G), a, b, c, G, slot_shift);
+  return launch_pdl_cluster(slot_shift == 0 ? topk_kernel<false> : topk_kernel<true>,
+                            dim3(static_cast<unsigned>(G), q, static_cast<unsigned>(z)), dim3(kThreads), smem, stream,
+                            static_cast<unsigned>(G), a, b, c, G, slot_shift);
 }
 
 // Clears `bytes` (a multiple of 4, 16-byte aligned) at p: the indexer's and
@@ -802,7 +809,7 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
 // the step's new window row and indexer key into the caches; the key
 // compressor (`key`, ring mode, B > 0) runs on warps 4..7 of those CTAs.
 namespace {
-__global__ void __launch_bounds__(256) zero_kernel(uint32_t* p, const int64_t words, const int zero_blocks,
+__global__ void __launch_bounds__(256, 2) zero_kernel(uint32_t* p, const int64_t words, const int zero_blocks,
                                                    const DecodeAppend ap, const CompressArgs key) {
   pdl_launch_dependents();
   pdl_wait();
