@@ -42,11 +42,15 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
-    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index", "compressor"], default="decode",
+    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index", "compressor", "prefill"],
+                    default="decode",
                     help="reindex: only the hierarchical indexer's Reindex layer on --workload (4 Full-layer "
                          "calls make the pools, then --warmup and --steps Reindex calls; for profiling); "
                          "fp4_index: only the FP4 indexer section on --workload; compressor: only the bulk "
-                         "compressor section")
+                         "compressor section; prefill: only --warmup and --steps calls of the self-contained "
+                         "prefill layer call on the 64K-context chunk, the first --queries queries of it")
+    ap.add_argument("--queries", type=int, default=4096, help="prefill section: queries of the chunk (a multiple "
+                                                              "of 4, for profiling captures of fewer)")
     return ap.parse_args()
 
 
@@ -942,6 +946,46 @@ def reindex_section(args, pool_blocks=2048, sets=4):
             "ms_per_call": e0.elapsed_time(e1) / max(args.steps, 1)}
 
 
+def prefill_section(args):
+    """Timed calls of csa_layer_prefill_with_keys on the first --queries
+    queries of the 64K-context chunk (positions 61440..): for profiling."""
+    import torch
+
+    import compressed_sparse_attention_02_gb300 as csa
+    import synthetic as syn
+    dev = torch.device("cuda", 0)
+    w0 = syn.WORKLOADS[4]
+    Q = max(4, args.queries // 4 * 4)
+    w = syn.Workload(w0.name, w0.config, w0.kind, B=w0.B, t=w0.pos0 + Q - 1, topk=w0.topk, n_cap=w0.n_cap, Q=Q,
+                     pos0=w0.pos0)
+    x = syn.prefill_inputs(w, device=dev)
+    p = csa.csa_default_params(topk=w.topk)
+    B = w.B
+    idx = torch.empty(B, Q, p.topk, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Q, 64, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Q, 64, dtype=torch.float32, device=dev)
+    ws = csa.workspace(csa.CSA_OP_LAYER_PREFILL, p, B, Q, x["n_cap"], device=dev)
+    keys = csa.index_key_src(x["CIa"], x["ZIa"], x["CIb"], x["ZIb"], x["BIa"], x["BIb"], x["rms_wI"], x["CIb_prev"],
+                             x["ZIb_prev"])
+
+    def step():
+        csa.csa_layer_prefill_with_keys(p, B, Q, w.pos0, x["Ca"], x["Za"], x["Cb"], x["Zb"], x["Cb_prev"],
+                                        x["Zb_prev"], x["Ba"], x["Bb"], x["rms_w"], keys, x["kv"], x["n_cap"],
+                                        x["kI"], x["qI"], x["wI"], x["q"], x["swa"], x["sink"], idx, out, lse, ws)
+    for _ in range(args.warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if csa.csa_check_status() != 0:
+        raise RuntimeError("device status after the prefill calls")
+    return {"section": "prefill", "workload": w.name, "queries": Q,
+            "ms_per_call": e0.elapsed_time(e1) / max(args.steps, 1)}
+
+
 def _traffic_from_profile():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary (scaled from the captured batch to the full launch), or None when
@@ -1243,6 +1287,10 @@ def main():
             import compressed_sparse_attention_02_gb300 as csa
             print(json.dumps(index_fp4_profile(csa, torch, torch.device("cuda", 0), args.workload,
                                                n=max(args.steps, 1))), flush=True)
+        return
+    if args.section == "prefill":
+        if rank == 0:
+            print(json.dumps(prefill_section(args)), flush=True)
         return
     if args.section == "compressor":
         if rank == 0:
