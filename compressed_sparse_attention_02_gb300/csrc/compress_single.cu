@@ -8,12 +8,18 @@
 // tokens so far, the online-softmax state of the HCA compressor described in
 // "CSA / HCA", section "KV cache：成品与原料", instead of a ring of raw rows.
 //
-// Bulk: one 256-thread CTA per (entry, sequence); four groups of 64 threads
-// take every fourth row of the block (m up to 128) with an online softmax in
-// fp32, group 0 merges the four partial states and finishes the entry
-// (RMSNorm, RoPE, bf16 store).  Step: one 64-thread CTA per sequence updates
-// its state with the step's token and, when the token closes a block,
-// finishes the entry.
+// Bulk: one 256-thread CTA per (entry, sequence).  The rows of C and Z stream
+// through shared memory in stages of up to 8 rows (one bulk copy of each, a
+// ring of 4 stages in flight; the slot biases of the next stage are loaded
+// while one is computed); four groups of 64 threads take every fourth row of
+// a stage with an online softmax in fp32; group 0 merges the partial states
+// and finishes the entry (RMSNorm, RoPE, bf16 store).  (Two CTAs per entry,
+// each with half of the rows and a merge through distributed shared memory,
+// were measured slower at HCA's m = 128: 69 against 54 us for 1024 entries.)
+// Step: one 64-thread CTA per sequence updates its state with the step's
+// token and, when the token closes a block, finishes the entry.  The
+// exponentials and the final divide are the hardware approximations (a few
+// ulp, far inside the bf16 output's rounding).
 #include "compress.cuh"
 
 namespace csa {
@@ -22,6 +28,11 @@ namespace {
 constexpr int kGroupThreads = kDim / 8;  // 64: 8 channels per thread
 constexpr int kRowGroups = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kStageRows = 8;  // rows of C (and of Z) per stage
+constexpr int kStages = 4;     // stages in flight
+constexpr uint32_t kStageBytes = kStageRows * kDim * 2;
+constexpr size_t kBulkSmem = 2 * kStages * kStageBytes + kStages * sizeof(uint64_t);  // C and Z rings, barriers
+static_assert((kRowGroups - 1) * 3 * kDim * sizeof(float) <= kStages * kStageBytes, "merge states fit the C ring");
 
 // Folds one row's logits and values into the running state of 8 channels.
 __device__ __forceinline__ void online_add(const float (&logit)[8], const float (&c)[8], float (&mx)[8],
@@ -29,8 +40,8 @@ __device__ __forceinline__ void online_add(const float (&logit)[8], const float 
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float nm = fmaxf(mx[j], logit[j]);
-    const float sc = exp2f((mx[j] - nm) * kLog2e);  // 0 while the state is empty (mx = -inf)
-    const float p = exp2f((logit[j] - nm) * kLog2e);
+    const float sc = ex2_approx((mx[j] - nm) * kLog2e);  // 0 while the state is empty (mx = -inf)
+    const float p = ex2_approx((logit[j] - nm) * kLog2e);
     num[j] = fmaf(num[j], sc, p * c[j]);
     den[j] = fmaf(den[j], sc, p);
     mx[j] = nm;
@@ -54,31 +65,85 @@ __device__ __forceinline__ void load_row(const uint16_t* C, const uint16_t* Z, c
 __device__ __forceinline__ void group0_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single_kernel(const CompressArgs a) {
-  pdl_launch_dependents();
-  pdl_wait();
-  __shared__ float part[kRowGroups - 1][3][kDim];  // groups 1..3: max, sum, weighted sum
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* ring_c = reinterpret_cast<uint16_t*>(smem);                   // [kStages][kStageRows][kDim]
+  uint16_t* ring_z = ring_c + kStages * kStageRows * kDim;                // [kStages][kStageRows][kDim]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(ring_z + kStages * kStageRows * kDim);
+  float* part = reinterpret_cast<float*>(smem);  // after the rows: groups 1..3's (max, sum, weighted sum)
   __shared__ float red[kGroupThreads / 32];
+  pdl_launch_dependents();
   const int g = threadIdx.x / kGroupThreads, t = threadIdx.x % kGroupThreads, d0 = 8 * t;
   const int b = blockIdx.y;
   const int64_t e = blockIdx.x, i = a.entry0 + e;
   const int m = a.m;
-  const int64_t row0 = (static_cast<int64_t>(b) * m * a.n_new + static_cast<int64_t>(m) * e) * kDim + d0;
+  const int rows = m < kStageRows ? m : kStageRows;  // rows per stage (m is a power of two)
+  const int stages = m / rows;
+  const uint32_t bytes = static_cast<uint32_t>(rows) * kDim * 2;
+  const int64_t row0 = (static_cast<int64_t>(b) * m * a.n_new + static_cast<int64_t>(m) * e) * kDim;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  auto issue = [&](int slot, int j) {  // rows j*rows .. of the block: contiguous runs of C and of Z
+    mbar_arrive_expect_tx(&bar[slot], 2 * bytes);
+    const int64_t off = row0 + static_cast<int64_t>(j) * rows * kDim;
+    bulk_load(ring_c + slot * kStageRows * kDim, a.Ca + off, bytes, &bar[slot]);
+    bulk_load(ring_z + slot * kStageRows * kDim, a.Za + off, bytes, &bar[slot]);
+  };
+  if (threadIdx.x == 0)
+    for (int s = 0; s < kStages && s < stages; ++s) issue(s, s);
   float mx[8], den[8], num[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx[j] = -INFINITY, den[j] = 0.f, num[j] = 0.f;
-#pragma unroll 8
-  for (int r = g; r < m; r += kRowGroups) {
-    float logit[8], c[8];
-    load_row(a.Ca + row0 + static_cast<int64_t>(r) * kDim, a.Za + row0 + static_cast<int64_t>(r) * kDim,
-             a.Ba ? a.Ba + r * kDim + d0 : nullptr, logit, c);
-    online_add(logit, c, mx, den, num);
+  // the slot biases of this thread's rows (at most kStageRows / kRowGroups =
+  // 2 a stage), loaded one stage ahead so that no stage waits for them
+  constexpr int kMine = kStageRows / kRowGroups;
+  static_assert(kMine == 2, "two rows of a stage per group");
+  uint4 bcur[kMine], bnext[kMine];
+  auto load_bias = [&](int j, uint4 (&bv)[kMine]) {
+#pragma unroll
+    for (int u = 0; u < kMine; ++u) {
+      const int rr = g + kRowGroups * u;
+      bv[u] = (a.Ba && rr < rows && j < stages)
+                  ? __ldg(reinterpret_cast<const uint4*>(a.Ba + (j * rows + rr) * kDim + d0))
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load_bias(0, bnext);
+  bool ok = true;
+  for (int j = 0; j < stages; ++j) {
+    const int slot = j % kStages;
+#pragma unroll
+    for (int u = 0; u < kMine; ++u) bcur[u] = bnext[u];
+    load_bias(j + 1, bnext);
+    ok = __syncthreads_and(mbar_wait_sleep(&bar[slot], static_cast<uint32_t>(j / kStages) & 1u, a.status)) && ok;
+#pragma unroll
+    for (int u = 0; u < kMine; ++u) {
+      const int rr = g + kRowGroups * u;
+      if (rr >= rows) break;
+      float logit[8], c[8], bv[8];
+      using V = Bf16Vec<8>;
+      V::unpack(*reinterpret_cast<const uint4*>(ring_z + (slot * kStageRows + rr) * kDim + d0), logit);
+      V::unpack(*reinterpret_cast<const uint4*>(ring_c + (slot * kStageRows + rr) * kDim + d0), c);
+      V::unpack(bcur[u], bv);  // (zero without a bias)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) logit[q] += bv[q];
+      online_add(logit, c, mx, den, num);
+    }
+    __syncthreads();  // the slot is read
+    if (threadIdx.x == 0 && j + kStages < stages) issue(slot, j + kStages);
   }
-  if (g > 0) {
+  if (!ok && threadIdx.x == 0)  // no copy of ours stays in flight
+    for (int j = stages > kStages ? stages - kStages : 0; j < stages; ++j)
+      mbar_wait(&bar[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, a.status);
+  if (g > 0) {  // (the ring is free: every stage has been read)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      part[g - 1][0][d0 + j] = mx[j];
-      part[g - 1][1][d0 + j] = den[j];
-      part[g - 1][2][d0 + j] = num[j];
+      part[((g - 1) * 3 + 0) * kDim + d0 + j] = mx[j];
+      part[((g - 1) * 3 + 1) * kDim + d0 + j] = den[j];
+      part[((g - 1) * 3 + 2) * kDim + d0 + j] = num[j];
     }
   }
   __syncthreads();
@@ -88,17 +153,17 @@ __global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single
   for (int h = 0; h < kRowGroups - 1; ++h) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float mh = part[h][0][d0 + j];
+      const float mh = part[(h * 3 + 0) * kDim + d0 + j];
       const float nm = fmaxf(mx[j], mh);
-      const float s0 = exp2f((mx[j] - nm) * kLog2e), s1 = exp2f((mh - nm) * kLog2e);  // s1 = 0: no rows
-      num[j] = fmaf(num[j], s0, part[h][2][d0 + j] * s1);
-      den[j] = fmaf(den[j], s0, part[h][1][d0 + j] * s1);
+      const float s0 = ex2_approx((mx[j] - nm) * kLog2e), s1 = ex2_approx((mh - nm) * kLog2e);  // s1 = 0: no rows
+      num[j] = fmaf(num[j], s0, part[(h * 3 + 2) * kDim + d0 + j] * s1);
+      den[j] = fmaf(den[j], s0, part[(h * 3 + 1) * kDim + d0 + j] * s1);
       mx[j] = nm;
     }
   }
   float x[8], w[8], y[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
+  for (int j = 0; j < 8; ++j) x[j] = __fdividef(num[j], den[j]);
   Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
   norm_rope<8, kDim>(a, x, w, t, static_cast<int64_t>(m) * i, red, [] { group0_sync(); }, y);
   *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
@@ -153,7 +218,7 @@ __global__ void __launch_bounds__(kGroupThreads) compress_single_step_kernel(con
   }
   float x[8], w[8], y[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) x[j] = num[j] / den[j];
+  for (int j = 0; j < 8; ++j) x[j] = __fdividef(num[j], den[j]);
   Bf16Vec<8>::unpack(__ldg(reinterpret_cast<const uint4*>(a.rms_w + d0)), w);
   norm_rope<8, kDim>(a, x, w, t, static_cast<int64_t>(m) * i, red, [] { __syncthreads(); }, y);
   *reinterpret_cast<uint4*>(a.kv_out + static_cast<int64_t>(b) * a.kv_stride_b + i * kDim + d0) =
@@ -169,8 +234,11 @@ cudaError_t launch_compress_single(const CompressArgs& args, cudaStream_t stream
   fill_rope(&a);
   if (a.mode == 0) {
     if (a.n_new <= 0) return cudaSuccess;
+    const cudaError_t err = cudaFuncSetAttribute(compress_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kBulkSmem));
+    if (err != cudaSuccess) return err;
     return launch_pdl(compress_single_kernel, dim3(static_cast<unsigned>(a.n_new), static_cast<unsigned>(a.B)),
-                      dim3(kGroupThreads * kRowGroups), 0, stream, a);
+                      dim3(kGroupThreads * kRowGroups), kBulkSmem, stream, a);
   }
   if (!a.state || !a.q_pos) return cudaErrorInvalidValue;
   return launch_pdl(compress_single_step_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kGroupThreads), 0, stream, a);

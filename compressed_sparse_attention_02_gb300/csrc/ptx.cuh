@@ -87,6 +87,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 
+// mbar_wait for many threads at once: a thread whose phase is not complete
+// sleeps in the barrier (suspend-time hint) instead of polling it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns);
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, unsigned* status) {
+  constexpr uint32_t kSleepNs = 20000;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns(), limit = wait_limit_ns(status);
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (global_timer_ns() - t0 > limit) {
+      record_error(status, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // The same wait with cluster-scope acquire: for barriers that a peer CTA of
 // the cluster arrives on or completes bytes on (its writes become visible).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
