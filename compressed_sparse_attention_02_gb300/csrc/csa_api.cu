@@ -167,7 +167,7 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
                           int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes, cudaStream_t st,
                           bool traced = false, bool zeroed = false,
                           const csa::CompressArgs* ride_along = nullptr, const PoolSpec* pool = nullptr,
-                          bool standalone = false) {
+                          bool standalone = false, bool after_zero = false) {
   const int64_t rows = static_cast<int64_t>(B) * Q;
   IndexWs w, wb;
   size_t need = 0;
@@ -227,6 +227,9 @@ csa_status run_index_topk(const csa_params* p, int32_t B, int32_t Q, const int32
     ia.block_ld = wb.score_ld;
     ia.block_hist = reinterpret_cast<uint32_t*>(wsb_blk + wb.hist_off);
   }
+  // the indexer may start on its key tiles before the zeroing kernel right
+  // before it has finished (not across a trace event, not in pool mode)
+  ia.early = (!zeroed || after_zero) && !own && !(pool && pool->in);
   ia.status = status;
   csa_status s = cuda_status(csa::launch_index_scores(ia, enc, st));
   if (s != CSA_OK) return s;
@@ -759,7 +762,7 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
   trace(1, st);
   // 2. indexer + top-k over the visible entries
   s = run_index_topk(p, B, 1, q_pos, 0, qI, wI, kI, n_cap, idx_out, nullptr, workspace, workspace_bytes, st, true,
-                     true, ride_along ? &ca : nullptr);
+                     true, ride_along ? &ca : nullptr, nullptr, false, ride_along);
   if (s != CSA_OK) return s;
   trace(3, st);
   // 3. sparse attention over the window ring and the selection

@@ -61,6 +61,29 @@ static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool bloc
 #ifndef CSA_INDEX_DECODE_STAGES_FP4
 #define CSA_INDEX_DECODE_STAGES_FP4 8
 #endif
+// TMEM accumulators of the one-query configuration (E4M3, FP4)
+#ifndef CSA_INDEX_DECODE_NBUF
+#define CSA_INDEX_DECODE_NBUF 2
+#endif
+#ifndef CSA_INDEX_DECODE_NBUF_FP4
+#define CSA_INDEX_DECODE_NBUF_FP4 2
+#endif
+// Shape of the Reindex (pool gather) configuration
+#ifndef CSA_INDEX_POOL_STAGES
+#define CSA_INDEX_POOL_STAGES 4
+#endif
+#ifndef CSA_INDEX_POOL_STAGES_FP4
+#define CSA_INDEX_POOL_STAGES_FP4 8
+#endif
+#ifndef CSA_INDEX_POOL_GROUPS
+#define CSA_INDEX_POOL_GROUPS 2
+#endif
+#ifndef CSA_INDEX_POOL_CTAS_PER_SM
+#define CSA_INDEX_POOL_CTAS_PER_SM 2
+#endif
+#ifndef CSA_INDEX_POOL_NBUF
+#define CSA_INDEX_POOL_NBUF 2
+#endif
 
 // Kernel variants (template bits): the Reindex layer's pool gathers, the
 // Full layer's block maxima, bf16 score stores, FP4 keys and queries.  Each
@@ -68,18 +91,26 @@ static_assert(kPoolTileBlocks * kPoolBlock == kTileKeys, "a tile is 16 pool bloc
 // the others.
 constexpr int kModePool = 1, kModeBlocks = 2, kModeBf16 = 4, kModeFp4 = 8;
 
-template <int QPC, bool kFp4 = false>
+template <int QPC, int kMode>
 struct IndexCfg {
+  static constexpr bool kFp4 = (kMode & kModeFp4) != 0, kPool = (kMode & kModePool) != 0;
   static constexpr int N = kIdxHeads * QPC;
   // Epilogue groups of 4 warps (one per TMEM lane quadrant).  One query per
   // group: the groups take tiles in turn; more queries: a group per query.
-  static constexpr int GROUPS = QPC == 1 ? CSA_INDEX_DECODE_GROUPS : QPC;
+  static constexpr int GROUPS = QPC != 1 ? QPC : (kPool ? CSA_INDEX_POOL_GROUPS : CSA_INDEX_DECODE_GROUPS);
   static constexpr int EPI_WARPS = 4 * GROUPS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int CTAS_PER_SM = QPC == 1 ? CSA_INDEX_DECODE_CTAS_PER_SM : 1;
+  static constexpr int CTAS_PER_SM =
+      QPC != 1 ? 1 : (kPool ? CSA_INDEX_POOL_CTAS_PER_SM : CSA_INDEX_DECODE_CTAS_PER_SM);
   static constexpr int STAGES =
-      QPC == 1 ? (kFp4 ? CSA_INDEX_DECODE_STAGES_FP4 : CSA_INDEX_DECODE_STAGES) : (kFp4 ? 16 : 8);
-  static constexpr int NBUF = QPC == 1 ? (GROUPS < 2 ? 2 : GROUPS) : 2;  // TMEM accumulators; tile n: n % NBUF
+      QPC != 1 ? (kFp4 ? 16 : 8)
+               : kPool ? (kFp4 ? CSA_INDEX_POOL_STAGES_FP4 : CSA_INDEX_POOL_STAGES)
+                       : (kFp4 ? CSA_INDEX_DECODE_STAGES_FP4 : CSA_INDEX_DECODE_STAGES);
+  // TMEM accumulators; tile n uses accumulator n % NBUF
+  static constexpr int NBUF = QPC != 1 ? 2
+                              : kPool  ? CSA_INDEX_POOL_NBUF
+                                       : (kFp4 ? CSA_INDEX_DECODE_NBUF_FP4 : CSA_INDEX_DECODE_NBUF);
+  static_assert(QPC != 1 || NBUF >= GROUPS, "every epilogue group owns an accumulator");
   // Operand rows: 128 E4M3 bytes, or 64 bytes of E2M1 codes (plus scales).
   static constexpr uint32_t ROW = kFp4 ? kIdxDim / 2 : kIdxDim;
   static constexpr uint32_t KEY_TILE = kTileKeys * ROW;  // 16 or 8 KiB
@@ -93,6 +124,7 @@ struct IndexCfg {
   static_assert(COLS <= 512, "TMEM holds 512 columns");
   static constexpr uint32_t TMEM_COLS =
       COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : (COLS <= 256 ? 256 : 512)));
+  static_assert(TMEM_COLS * CTAS_PER_SM <= 512, "the resident CTAs' accumulators share an SM's TMEM");
   // one query per CTA: each epilogue group gathers the row's first-digit
   // counts in shared memory and adds them to the global row once per query
   // group
@@ -166,17 +198,24 @@ __device__ __forceinline__ bool group_past_cache(const IndexArgs& a, const Group
 }
 
 template <int QPC, int kMode>
-__global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, IndexCfg<QPC, (kMode & 8) != 0>::CTAS_PER_SM)
+__global__ void __launch_bounds__(IndexCfg<QPC, kMode>::THREADS, IndexCfg<QPC, kMode>::CTAS_PER_SM)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                        const IndexArgs a, const int tiles_per_group, const int groups_per_seq) {
   constexpr bool kPool = (kMode & kModePool) != 0, kBlocks = (kMode & kModeBlocks) != 0,
                  kBf16 = (kMode & kModeBf16) != 0, kFp4 = (kMode & kModeFp4) != 0;
-  using Cfg = IndexCfg<QPC, kFp4>;
+  using Cfg = IndexCfg<QPC, kMode>;
   constexpr int N = Cfg::N;
   constexpr int STAGES = Cfg::STAGES;
   constexpr uint32_t kKeyTileBytes = Cfg::KEY_TILE, kQBytes = Cfg::QBYTES;
   pdl_launch_dependents();
-  pdl_wait();  // before any global access and before TMEM is taken
+  // Without a.early: wait before any global access and before TMEM is
+  // taken.  With it the predecessor is the counters' zeroing kernel, whose
+  // own predecessor has completed (no other kernel of the stream holds TMEM
+  // or writes this launch's inputs): the producer streams key tiles before
+  // the wait, up to each query's last visible tile, and the epilogue waits
+  // before its first global access (the counters the zeroing kernel clears).
+  const bool early = !kPool && a.early != 0;
+  if (!early) pdl_wait();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -366,7 +405,7 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
       bool active = false;
       GroupInfo gi{};
       int qb = 1, it = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
       int64_t g = u0 / tiles_per_group, tile = u0 % tiles_per_group - 1;
       for (int64_t u = u0; u < u1 && ok; ++u) {
         if (++tile == tiles_per_group) {  // advance (group, tile) without dividing
@@ -394,6 +433,10 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
           }
         }
         if (!active || tile * kTileKeys >= gi.vmax) continue;
+        if (early && !waited && (tile + 1) * kTileKeys >= gi.vmax) {  // the tile may hold the new entry
+          pdl_wait();
+          waited = true;
+        }
         const int s = it % STAGES;
         const uint32_t use = static_cast<uint32_t>(it / STAGES);
         if (use > 0 && !(ok = mbar_wait(&empty[s], (use - 1) & 1u, a.status))) break;
@@ -501,6 +544,7 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
     // are the prefix of its tiles below its last visible key, so the running
     // tile count `it` (the MMA thread's accumulator numbering) advances by a
     // group's active tiles at once, and a warp visits only its own tiles.
+    if (early) pdl_wait();
     const int ew = warp - 2;
     const int grp = ew >> 2;
     const int sub = warp & 3;
@@ -565,32 +609,20 @@ __global__ void __launch_bounds__(IndexCfg<QPC, (kMode & 8) != 0>::THREADS, Inde
         // four independent chains (head h into chain h % 4); where the
         // epilogue's issue rate bounds the kernel (FP4 keys, several queries
         // a tile) two chains go through one packed FMA, the same roundings
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // four independent chains (head h into chain h % 4), two to a packed
+        // register: each step is fmaf(w_h, fmaxf(s_h, 0), chain) per head
+        uint64_t acc01 = 0ull, acc23 = 0ull;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // 32 heads at a time keeps registers low
           uint32_t r[32];
           tmem_ld32(taddr + 32 * half, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const float4 w4 = lds_f32x4(w_addr + 16 * (8 * half + v));
-            const float x0 = fmaxf(__uint_as_float(r[4 * v + 0]), 0.f), x1 = fmaxf(__uint_as_float(r[4 * v + 1]), 0.f);
-            const float x2 = fmaxf(__uint_as_float(r[4 * v + 2]), 0.f), x3 = fmaxf(__uint_as_float(r[4 * v + 3]), 0.f);
-            if constexpr (kFp4 || QPC > 1) {
-              const float2 a01 = ffma2(make_float2(w4.x, w4.y), make_float2(x0, x1), make_float2(acc[0], acc[1]));
-              const float2 a23 = ffma2(make_float2(w4.z, w4.w), make_float2(x2, x3), make_float2(acc[2], acc[3]));
-              acc[0] = a01.x;
-              acc[1] = a01.y;
-              acc[2] = a23.x;
-              acc[3] = a23.y;
-            } else {
-              acc[0] = fmaf(w4.x, x0, acc[0]);
-              acc[1] = fmaf(w4.y, x1, acc[1]);
-              acc[2] = fmaf(w4.z, x2, acc[2]);
-              acc[3] = fmaf(w4.w, x3, acc[3]);
-            }
-          }
+          for (int v = 0; v < 8; ++v)
+            relu_fma4(acc01, acc23, w_addr + 16 * (8 * half + v), r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
         }
+        const float acc[4] = {__uint_as_float(static_cast<uint32_t>(acc01)), __uint_as_float(static_cast<uint32_t>(acc01 >> 32)),
+                              __uint_as_float(static_cast<uint32_t>(acc23)), __uint_as_float(static_cast<uint32_t>(acc23 >> 32))};
         float score = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         // bf16 scores: every use below (store, digit counts, block maxima)
         // sees the rounded value
@@ -683,7 +715,7 @@ bool encode_maps(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, C
 
 template <int QPC, int kMode>
 cudaError_t launch_qpc(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
-  using Cfg = IndexCfg<QPC, (kMode & kModeFp4) != 0>;
+  using Cfg = IndexCfg<QPC, kMode>;
   CUtensorMap tm_k, tm_q;
   if (!encode_maps(a, encode, &tm_k, &tm_q)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(index_score_kernel<QPC, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,

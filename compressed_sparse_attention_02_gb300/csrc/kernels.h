@@ -147,6 +147,12 @@ struct IndexArgs {
   const int32_t* pool;      // [B*Q][pool_ld] or null
   int pool_blocks;          // a multiple of kPoolTileBlocks
   int64_t pool_ld;          // a multiple of 4
+  // 1: the launch directly follows a launch_zero kernel of the same stream
+  // (which lets its dependents start only once its own predecessor has
+  // completed), so the kernel may read its inputs before waiting for that
+  // kernel: q_pos, q^I and every key tile but each query's last visible one
+  // (which may hold the entry that kernel writes).  Not for pool mode.
+  int early;
   unsigned* status;
 };
 cudaError_t launch_index_scores(const IndexArgs& a, PFN_cuTensorMapEncodeTiled_v12000 encode,

@@ -335,6 +335,29 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
+// Four heads of a ReLU-weighted sum, two to a packed register:
+// a01 += (w0, w1) * max((x0, x1), 0) and a23 += (w2, w3) * max((x2, x3), 0),
+// the weights w0..w3 read from shared memory at w_addr; each component is
+// rounded as fmaf(w, fmaxf(x, 0), a) rounds it.
+__device__ __forceinline__ void relu_fma4(uint64_t& a01, uint64_t& a23, uint32_t w_addr, uint32_t x0, uint32_t x1,
+                                          uint32_t x2, uint32_t x3) {
+  asm volatile(
+      "{\n\t.reg .b64 w01, w23, x01, x23;\n\t.reg .f32 m0, m1, m2, m3;\n\t"
+      "ld.shared.v2.b64 {w01, w23}, [%2];\n\t"
+      "max.f32 m0, %3, 0f00000000;\n\t"
+      "max.f32 m1, %4, 0f00000000;\n\t"
+      "max.f32 m2, %5, 0f00000000;\n\t"
+      "max.f32 m3, %6, 0f00000000;\n\t"
+      "mov.b64 x01, {m0, m1};\n\t"
+      "mov.b64 x23, {m2, m3};\n\t"
+      "fma.rn.f32x2 %0, w01, x01, %0;\n\t"
+      "fma.rn.f32x2 %1, w23, x23, %1;\n\t}"
+      : "+l"(a01), "+l"(a23)
+      : "r"(w_addr), "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "f"(__uint_as_float(x2)),
+        "f"(__uint_as_float(x3))
+      : "memory");
+}
+
 // ---- shared memory ------------------------------------------------------------
 
 __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {

@@ -811,8 +811,11 @@ cudaError_t launch_topk(const TopkArgs& a, const CompressArgs* ride_along, cudaS
 namespace {
 __global__ void __launch_bounds__(256, 2) zero_kernel(uint32_t* p, const int64_t words, const int zero_blocks,
                                                    const DecodeAppend ap, const CompressArgs key) {
-  pdl_launch_dependents();
+  // dependents start only after this wait: its predecessor has then
+  // completed, so a dependent may read before its own wait whatever this
+  // kernel does not write (the indexer's early key tiles)
   pdl_wait();
+  pdl_launch_dependents();
   const int seq_blocks = static_cast<int>(gridDim.x) - zero_blocks;
   if (static_cast<int>(blockIdx.x) < seq_blocks) {  // one CTA per sequence: its new rows
     __shared__ float red[4], xch[kIdxDim];
