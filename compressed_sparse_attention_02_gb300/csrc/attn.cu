@@ -251,6 +251,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // kFp4: the compressed rows are FP4 entries (a.kv_fp4); a template
 // argument, so that the bf16 kernel carries none of that code.
+// The query's 64 x 512 bf16 rows into eight 128-byte-swizzled 64-channel
+// blocks, on q_full (one thread).
+__device__ __forceinline__ void load_q(const CUtensorMap& tm_q, uint8_t* q_s, int64_t row_q, uint64_t* q_full) {
+  prefetch_tensormap(&tm_q);
+  mbar_arrive_expect_tx(q_full, kQBytes);
+#pragma unroll
+  for (int blk = 0; blk < 8; ++blk)
+    tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
+}
+
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_swa,
@@ -296,7 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_arrive();  // waited on before the first access to a peer
   }
-  pdl_wait();  // before any global access and before TMEM is taken
+  // Without a.early: wait before any global access and before TMEM is
+  // taken.  With it, the barriers are set up and Q (an input no kernel of the
+  // chain writes) starts loading first.
+  if (!a.early) pdl_wait();
   const int quad = warp & 3;         // TMEM lane quadrant == 32 tile rows
   const int hw0 = (warp >> 2) * HW;  // first head of this worker warp
   // the query's row set is cut into `split` slices combined in the cluster,
@@ -308,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row_q = static_cast<int64_t>(b) * a.Q + qi;
   const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + qi;
 
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   if (tid == 0) {
     mbar_init(q_full, 1);
     mbar_init(s_full, 1);
@@ -323,6 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     flags[1] = 0;
     flags[2] = 0;
   }
+  if (a.early) {  // Q by TMA now; TMEM and the predecessors' outputs after the wait
+    __syncthreads();
+    if (warp == kMmaWarp && lane == 0) load_q(tm_q, q_s, row_q, q_full);
+    pdl_wait();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   if (tid < kHeads) {
     m_ref[tid] = -INFINITY;
     l_sum[tid] = 0.f;
@@ -408,11 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     // ---------------- Q by TMA, then the MMAs of every tile ----------------
     if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      mbar_arrive_expect_tx(q_full, kQBytes);
-#pragma unroll
-      for (int blk = 0; blk < 8; ++blk)
-        tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
+      if (!a.early) load_q(tm_q, q_s, row_q, q_full);
       // (waited for even without a tile: the epilogue may reuse the Q buffer)
       bool ok = wait_or_abort(q_full, 0, abort_flag, a.status);
       constexpr uint32_t idesc_s = instr_desc(kTileRows, kHeads, 1, 1, 0, 0);  // bf16, K-major A/B
@@ -936,55 +950,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 // maximum M over the slices' reference maxima and the sink (log2 units), the
 // denominator 2^(sink - M) + sum_s l_s 2^(m_s - M), and the output
 // sum_s O_s 2^(m_s - M) / den (the merge the cluster does on chip).  One CTA
-// per (query, head): thread c loads channels 4c .. 4c+3 of every slice at
-// once (independent loads) while one warp reduces the slices' (max, sum),
-// then sums them; the inverse RoPE rotates its two channel pairs in place.  G is
-// a bound on gsplit (2, 4, 8 or 16), so that a launch with few slices keeps
-// few registers and many CTAs per SM.
+// per query and 8 heads, one warp per head (few CTAs: a launch of one CTA per
+// head spent most of its time dispatching them): lane l loads channels
+// 16l .. 16l+15 of every slice (up to 4 slices at once, before the factors)
+// while its warp reduces the slices' (max, sum), then sums them; the inverse
+// RoPE rotates its channel pairs in place.  G is a bound on gsplit (2, 4, 8
+// or 16), so that a launch with few slices keeps few registers.
+constexpr int kCombineHeads = 8;
 template <int G>
-__global__ void __launch_bounds__(kDim / 4) attn_combine_kernel(const AttnArgs a, const int gsplit) {
+__global__ void __launch_bounds__(32 * kCombineHeads) attn_combine_kernel(const AttnArgs a, const int gsplit) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float fs[G];
   const int64_t row_q = blockIdx.x;
-  const int h = blockIdx.y, tid = threadIdx.x;
-  // the slices' outputs do not depend on the factors: their loads go out first
-  const int c0 = 4 * tid;
-  float4 o[G];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kCombineHeads + warp;  // one warp per head
+  const int c0 = 16 * lane;                          // 16 channels per lane
+  const float* po = a.part_o + (row_q * gsplit * kHeads + h) * kDim + c0;
+  const int64_t slice_ld = static_cast<int64_t>(kHeads) * kDim;
+  // up to 4 slices: their outputs do not depend on the factors, so their
+  // loads go out first
+  constexpr int kPre = G <= 4 ? G : 1;
+  float4 o[kPre][4];
+  if constexpr (G <= 4) {
 #pragma unroll
-  for (int s = 0; s < G; ++s)
-    if (s < gsplit) o[s] = *reinterpret_cast<const float4*>(a.part_o + ((row_q * gsplit + s) * kHeads + h) * kDim + c0);
-  if (tid < 32) {
-    const float* ml = a.part_ml + row_q * gsplit * 2 * kHeads;
-    const float sk = a.sink[h] * kLog2e;
-    const float ms = tid < gsplit ? ml[tid * 2 * kHeads + h] : -INFINITY;
-    const float ls = tid < gsplit ? ml[tid * 2 * kHeads + kHeads + h] : 0.f;
-    float M = fmaxf(sk, ms);
+    for (int s = 0; s < G; ++s)
+      if (s < gsplit)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float den = (M == -INFINITY || ms == -INFINITY) ? 0.f : ls * exp2f(ms - M);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    den += M == -INFINITY ? 0.f : exp2f(sk - M);
-    if (tid < gsplit) fs[tid] = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M) / den;
-    if (tid == 0 && a.lse) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
+        for (int v = 0; v < 4; ++v) o[s][v] = *reinterpret_cast<const float4*>(po + s * slice_ld + 4 * v);
   }
-  __syncthreads();
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // the factors: lane s holds slice s's (max, sum); with the sink logit
+  // they give each slice's weight exp2(m_s - M) / den
+  const float* ml = a.part_ml + row_q * gsplit * 2 * kHeads;
+  const float sk = a.sink[h] * kLog2e;
+  const float ms = lane < gsplit ? ml[lane * 2 * kHeads + h] : -INFINITY;
+  const float ls = lane < gsplit ? ml[lane * 2 * kHeads + kHeads + h] : 0.f;
+  float M = fmaxf(sk, ms);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float den = (M == -INFINITY || ms == -INFINITY) ? 0.f : ls * exp2f(ms - M);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  den += M == -INFINITY ? 0.f : exp2f(sk - M);
+  const float fl = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M) / den;
+  if (lane == 0 && a.lse) a.lse[row_q * kHeads + h] = M == -INFINITY ? -INFINITY : (M + log2f(den)) / kLog2e;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
   for (int s = 0; s < G; ++s) {
     if (s < gsplit) {
-      const float f = fs[s];
-      acc[0] = fmaf(f, o[s].x, acc[0]);
-      acc[1] = fmaf(f, o[s].y, acc[1]);
-      acc[2] = fmaf(f, o[s].z, acc[2]);
-      acc[3] = fmaf(f, o[s].w, acc[3]);
+      const float f = __shfl_sync(0xffffffffu, fl, s);
+      float4 ov[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        ov[v] = G <= 4 ? o[s < kPre ? s : 0][v] : *reinterpret_cast<const float4*>(po + s * slice_ld + 4 * v);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        acc[4 * v + 0] = fmaf(f, ov[v].x, acc[4 * v + 0]);
+        acc[4 * v + 1] = fmaf(f, ov[v].y, acc[4 * v + 1]);
+        acc[4 * v + 2] = fmaf(f, ov[v].z, acc[4 * v + 2]);
+        acc[4 * v + 3] = fmaf(f, ov[v].w, acc[4 * v + 3]);
+      }
     }
   }
-  if (a.inverse_rope && c0 >= kDim - kRope) {  // pairs (c0, c0+1), (c0+2, c0+3): (u, v) -> (u cos + v sin, -u sin + v cos)
+  if (a.inverse_rope && c0 >= kDim - kRope) {  // pairs (c, c+1): (u, v) -> (u cos + v sin, -u sin + v cos)
     const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[row_q]) : a.pos_base + row_q % a.Q;
 #pragma unroll
-    for (int pr = 0; pr < 2; ++pr) {
+    for (int pr = 0; pr < 8; ++pr) {
       float rs, rc;
       rope_angle(c0 + 2 * pr, t, a, &rs, &rc);
       const float u = acc[2 * pr], v = acc[2 * pr + 1];
@@ -992,9 +1024,15 @@ __global__ void __launch_bounds__(kDim / 4) attn_combine_kernel(const AttnArgs a
       acc[2 * pr + 1] = fmaf(v, rc, -u * rs);
     }
   }
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
-  *reinterpret_cast<uint2*>(a.out + (row_q * kHeads + h) * kDim + c0) =
-      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 pr2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&pr2);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.out + (row_q * kHeads + h) * kDim + c0);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // The largest cluster size (a power of two up to kMaxSplit) that the device
@@ -1098,7 +1136,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& args, PFN_cuTensorMapEncodeTiled_
     e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes, stream, tm_q,
                    tm_swa, tm_kv, a, 1, gsplit);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(queries), kHeads), block(kDim / 4);
+    const dim3 grid(static_cast<unsigned>(queries), kHeads / kCombineHeads), block(32 * kCombineHeads);
     static_assert(kMaxGSplit == 16, "the merge kernel is instantiated for bounds up to 16");
     if (gsplit <= 2) return launch_pdl(attn_combine_kernel<2>, grid, block, 0, stream, a, gsplit);
     if (gsplit <= 4) return launch_pdl(attn_combine_kernel<4>, grid, block, 0, stream, a, gsplit);

@@ -272,7 +272,7 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
                     const uint16_t* q, const void* kv, int64_t n_cap, const int32_t* idx, const uint16_t* swa,
                     int32_t swa_mode, int64_t swa_len, const int32_t* swa_pos0, int64_t swa_pos0_base,
                     const float* sink, uint16_t* out, float* lse, cudaStream_t st, bool dense = false,
-                    void* split_ws = nullptr, size_t split_ws_bytes = 0) {
+                    void* split_ws = nullptr, size_t split_ws_bytes = 0, bool early = false) {
   unsigned* status = status_ptr();
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!status || !enc) return CSA_ERR_CUDA;
@@ -314,6 +314,7 @@ csa_status run_attn(const csa_params* p, int32_t B, int32_t Q, const int32_t* q_
   aa.sm_scale = p->sm_scale;
   aa.inverse_rope = p->inverse_rope;
   csa::fill_rope_turns(static_cast<double>(p->rope_theta), aa.rope_turns);
+  aa.early = early ? 1 : 0;
   aa.status = status;
   return cuda_status(csa::launch_sparse_attn(aa, enc, st));
 }
@@ -769,7 +770,7 @@ csa_status layer_decode(const csa_params* p, int32_t B, const int32_t* q_pos, co
   const size_t attn_off = round_up(w.total, 256);
   s = run_attn(p, B, 1, q_pos, 0, q, kv_comp, n_cap, idx_out, swa_ring, 0, p->swa_window, nullptr, 0, sink, out,
                lse, st, false, static_cast<uint8_t*>(workspace) + attn_off,
-               workspace_bytes > attn_off ? workspace_bytes - attn_off : 0);
+               workspace_bytes > attn_off ? workspace_bytes - attn_off : 0, true);
   trace(4, st);
   return s;
 }

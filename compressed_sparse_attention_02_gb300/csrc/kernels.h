@@ -244,6 +244,11 @@ struct AttnArgs {
   int gsplit_cap;
   int inverse_rope;            // 1: rotate the output's RoPE channels back by -t
   uint64_t rope_turns[kRope / 2];  // theta^(-2j/R) / (2 pi) * 2^64 (fill_rope_turns)
+  // 1: the call's first kernel was a launch_zero kernel (which lets its
+  // dependents start only once its own predecessor has completed) and no
+  // kernel since writes q, q_pos or sink: the kernel loads them before
+  // waiting for its predecessor
+  int early;
   unsigned* status;
   // set by launch_sparse_attn: tensor maps of the window buffer and of the
   // bf16 cache exist, so tiles of 128 consecutive present rows load by TMA
