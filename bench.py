@@ -42,13 +42,14 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="decode workload id (1, 2 or 3)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling captures only)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, stage trace and CPU baseline")
-    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index", "compressor", "prefill"],
+    ap.add_argument("--section", choices=["decode", "reindex", "fp4_index", "compressor", "prefill", "hca"],
                     default="decode",
                     help="reindex: only the hierarchical indexer's Reindex layer on --workload (4 Full-layer "
                          "calls make the pools, then --warmup and --steps Reindex calls; for profiling); "
                          "fp4_index: only the FP4 indexer section on --workload; compressor: only the bulk "
                          "compressor section; prefill: only --warmup and --steps calls of the self-contained "
-                         "prefill layer call on the 64K-context chunk, the first --queries queries of it")
+                         "prefill layer call on the 64K-context chunk, the first --queries queries of it; hca: "
+                         "only the HCA section (dense attention at 128K and 1M, the single-stream compressor)")
     ap.add_argument("--queries", type=int, default=4096, help="prefill section: queries of the chunk (a multiple "
                                                               "of 4, for profiling captures of fewer)")
     return ap.parse_args()
@@ -1291,6 +1292,13 @@ def main():
     if args.section == "prefill":
         if rank == 0:
             print(json.dumps(prefill_section(args)), flush=True)
+        return
+    if args.section == "hca":
+        if rank == 0:
+            import torch
+
+            import compressed_sparse_attention_02_gb300 as csa
+            print(json.dumps(hca_profile(csa, torch, torch.device("cuda", 0))), flush=True)
         return
     if args.section == "compressor":
         if rank == 0:

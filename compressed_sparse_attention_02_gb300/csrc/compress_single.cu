@@ -48,6 +48,37 @@ __device__ __forceinline__ void online_add(const float (&logit)[8], const float 
   }
 }
 
+// Folds two rows' logits and values into the running state of 8 channels:
+// one rescale of the state per pair (the larger of the two rows' logits and
+// the running maximum), and each exponent's argument as one fused
+// multiply-add of the logit with log2(e) against the new maximum's product;
+// the multiply-adds run on channel pairs (packed fp32, each component
+// rounded as the scalar operation rounds it).
+__device__ __forceinline__ void online_add2(const float (&l0)[8], const float (&c0)[8], const float (&l1)[8],
+                                            const float (&c1)[8], float (&mx)[8], float (&den)[8], float (&num)[8]) {
+  const float2 k2 = make_float2(kLog2e, kLog2e), nk2 = make_float2(-kLog2e, -kLog2e);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float nm0 = fmaxf(mx[j], fmaxf(l0[j], l1[j])), nm1 = fmaxf(mx[j + 1], fmaxf(l0[j + 1], l1[j + 1]));
+    const float2 nk = __fmul2_rn(make_float2(nm0, nm1), nk2);  // -max * log2(e)
+    const float2 as = __ffma2_rn(make_float2(mx[j], mx[j + 1]), k2, nk);  // -inf while the state is empty
+    const float2 a0 = __ffma2_rn(make_float2(l0[j], l0[j + 1]), k2, nk);
+    const float2 a1 = __ffma2_rn(make_float2(l1[j], l1[j + 1]), k2, nk);
+    const float2 sc = make_float2(ex2_approx(as.x), ex2_approx(as.y));
+    const float2 p0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+    const float2 p1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
+    const float2 t = __ffma2_rn(p0, make_float2(c0[j], c0[j + 1]), __fmul2_rn(p1, make_float2(c1[j], c1[j + 1])));
+    const float2 nu = __ffma2_rn(make_float2(num[j], num[j + 1]), sc, t);
+    const float2 de = __ffma2_rn(make_float2(den[j], den[j + 1]), sc, __fadd2_rn(p0, p1));
+    num[j] = nu.x;
+    num[j + 1] = nu.y;
+    den[j] = de.x;
+    den[j + 1] = de.y;
+    mx[j] = nm0;
+    mx[j + 1] = nm1;
+  }
+}
+
 // The logits Z (+ bias) and values C of 8 channels of one row.
 __device__ __forceinline__ void load_row(const uint16_t* C, const uint16_t* Z, const uint16_t* bias, float (&logit)[8],
                                          float (&c)[8]) {
@@ -119,18 +150,29 @@ __global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single
     for (int u = 0; u < kMine; ++u) bcur[u] = bnext[u];
     load_bias(j + 1, bnext);
     ok = __syncthreads_and(mbar_wait_sleep(&bar[slot], static_cast<uint32_t>(j / kStages) & 1u, a.status)) && ok;
-#pragma unroll
-    for (int u = 0; u < kMine; ++u) {
-      const int rr = g + kRowGroups * u;
-      if (rr >= rows) break;
-      float logit[8], c[8], bv[8];
+    {
+      // this thread's two rows of the stage (rows g and g + 4), or the one
+      // of them that exists when the block has fewer than 8 rows
+      float logit[kMine][8], c[kMine][8];
       using V = Bf16Vec<8>;
-      V::unpack(*reinterpret_cast<const uint4*>(ring_z + (slot * kStageRows + rr) * kDim + d0), logit);
-      V::unpack(*reinterpret_cast<const uint4*>(ring_c + (slot * kStageRows + rr) * kDim + d0), c);
-      V::unpack(bcur[u], bv);  // (zero without a bias)
 #pragma unroll
-      for (int q = 0; q < 8; ++q) logit[q] += bv[q];
-      online_add(logit, c, mx, den, num);
+      for (int u = 0; u < kMine; ++u) {
+        const int rr = g + kRowGroups * u < rows ? g + kRowGroups * u : g;
+        float bv[8];
+        V::unpack(*reinterpret_cast<const uint4*>(ring_z + (slot * kStageRows + rr) * kDim + d0), logit[u]);
+        V::unpack(*reinterpret_cast<const uint4*>(ring_c + (slot * kStageRows + rr) * kDim + d0), c[u]);
+        V::unpack(bcur[u], bv);  // (zero without a bias)
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) {
+          const float2 lb = __fadd2_rn(make_float2(logit[u][q], logit[u][q + 1]), make_float2(bv[q], bv[q + 1]));
+          logit[u][q] = lb.x;
+          logit[u][q + 1] = lb.y;
+        }
+      }
+      if (g + kRowGroups < rows)
+        online_add2(logit[0], c[0], logit[1], c[1], mx, den, num);
+      else if (g < rows)
+        online_add(logit[0], c[0], mx, den, num);
     }
     __syncthreads();  // the slot is read
     if (threadIdx.x == 0 && j + kStages < stages) issue(slot, j + kStages);
