@@ -33,6 +33,9 @@ QSETS = 4
 UNIT = "queries/s"
 
 
+GRAPH_STEPS = 16  # decode steps per captured CUDA graph
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -254,15 +257,56 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     launches = csa.csa_launch_count() - launches0
     torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1)
+    # A serving loop replays captured steps: GRAPH_STEPS consecutive decode
+    # steps (their query sets rotating as above) in one CUDA graph, replayed
+    # for the same number of steps; the faster of the two launch forms counts.
+    graph_ms, graph_why, g_steps = None, None, 0
+    reps = args.steps // GRAPH_STEPS
+    if reps >= 1:
+        try:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                for _ in range(3):
+                    step()
+            cap.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            lc0 = csa.csa_launch_count()
+            with torch.cuda.graph(graph, stream=cap):
+                for _ in range(GRAPH_STEPS):
+                    step()
+            per_step = (csa.csa_launch_count() - lc0) / GRAPH_STEPS
+            with torch.cuda.stream(stream):
+                graph.replay()
+            torch.cuda.synchronize()
+            barrier()
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for _ in range(reps):
+                    graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            graph_ms, g_steps = e0.elapsed_time(e1), reps * GRAPH_STEPS
+            g_launches = int(round(per_step * g_steps))
+            del graph
+        except Exception as exc:  # keep the eager number
+            graph_why = "graph capture failed: %s" % str(exc).splitlines()[0][:120]
     if clocks:
         clocks.mark()
     barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    eager_ms = max_over_ranks(eager_ms, world, dev)
+    if graph_ms is not None:
+        graph_ms = max_over_ranks(graph_ms, world, dev)
+    steps_timed, ms, launch = args.steps, eager_ms, "eager stream launches"
+    if graph_ms is not None and graph_ms / g_steps < eager_ms / args.steps:
+        steps_timed, ms, launch, launches = g_steps, graph_ms, "CUDA graphs of %d steps, replayed" % GRAPH_STEPS, \
+            g_launches
     if clocks:
         clocks.stop()
     result = {
-        "metric": METRIC, "value": job_value(world, B, args.steps, ms), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": job_value(world, B, steps_timed, ms), "unit": UNIT, "n_gpus": world,
+        "steps": steps_timed, "warmup": args.warmup, "ms_per_step": ms / steps_timed, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
         "data": "synthetic (seeded N(0,1) inputs in the pages' shapes; no trained weights)",
         "config": {"workload": w.name, "batch_per_gpu": B, "context_tokens": w.t + 1,
@@ -271,6 +315,9 @@ def run_ours(args, rank, world, local_rank):
                          "%d sets so consecutive steps gather different rows"
                          % (B * w.n_cap * 128 >> 20, B * w.n_cap * 1024 >> 20, QSETS)},
         "gpu_launches": launches,
+        "launch": launch,
+        "eager_ms_per_step": eager_ms / args.steps,
+        "graph_ms_per_step": graph_ms / g_steps if graph_ms is not None else graph_why,
     }
     if clocks:
         result["clocks"] = clocks.summary()

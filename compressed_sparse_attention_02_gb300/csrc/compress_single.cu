@@ -29,7 +29,13 @@ constexpr int kGroupThreads = kDim / 8;  // 64: 8 channels per thread
 constexpr int kRowGroups = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kStageRows = 8;  // rows of C (and of Z) per stage
-constexpr int kStages = 4;     // stages in flight
+#ifndef CSA_HCA_STAGES
+#define CSA_HCA_STAGES 4
+#endif
+#ifndef CSA_HCA_CTAS_PER_SM
+#define CSA_HCA_CTAS_PER_SM 3
+#endif
+constexpr int kStages = CSA_HCA_STAGES;  // stages in flight
 constexpr uint32_t kStageBytes = kStageRows * kDim * 2;
 constexpr size_t kBulkSmem = 2 * kStages * kStageBytes + kStages * sizeof(uint64_t);  // C and Z rings, barriers
 static_assert((kRowGroups - 1) * 3 * kDim * sizeof(float) <= kStages * kStageBytes, "merge states fit the C ring");
@@ -95,7 +101,7 @@ __device__ __forceinline__ void load_row(const uint16_t* C, const uint16_t* Z, c
 
 __device__ __forceinline__ void group0_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kGroupThreads * kRowGroups, 3) compress_single_kernel(const CompressArgs a) {
+__global__ void __launch_bounds__(kGroupThreads * kRowGroups, CSA_HCA_CTAS_PER_SM) compress_single_kernel(const CompressArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* ring_c = reinterpret_cast<uint16_t*>(smem);                   // [kStages][kStageRows][kDim]
   uint16_t* ring_z = ring_c + kStages * kStageRows * kDim;                // [kStages][kStageRows][kDim]
