@@ -768,8 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       pml[tid] = m_ref[tid];
       pml[kHeads + tid] = l_sum[tid];
     }
-    // staged as [64 heads][512] fp32 in the (free) KV buffer, then one bulk copy
-    float* stage = reinterpret_cast<float*>(kv_s);
+    // [64 heads][512] fp32 straight from TMEM to global memory: for a head a
+    // warp's lanes hold 32 consecutive channels, so each store is one
+    // 128-byte line, and nothing waits for the stores before the CTA exits
     if (worker) {
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
@@ -783,15 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 32; ++h) v[h] = 0u;
         }
 #pragma unroll
-        for (int h = 0; h < 32; ++h) stage[(hw0 + h) * kDim + chn] = __uint_as_float(v[h]);
+        for (int h = 0; h < 32; ++h) po[(hw0 + h) * kDim + chn] = __uint_as_float(v[h]);
       }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_store(po, stage, kHeads * kDim * 4);
-      bulk_commit_group();
-      bulk_wait_read_all();
     }
   } else if (split == 1) {
     if (tid < kHeads) factors(tid, m_ref, l_sum, 0, 1, alpha);
