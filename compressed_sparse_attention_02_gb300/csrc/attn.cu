@@ -790,10 +790,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (split == 1) {
     if (tid < kHeads) factors(tid, m_ref, l_sum, 0, 1, alpha);
     __syncthreads();
-    // O^T from TMEM into a [64 heads][512] bf16 staging tile in the (free) Q
-    // buffer (for a head, a warp's lanes hold 32 consecutive channels), then
-    // one bulk copy to the output
-    uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
+    // O^T from TMEM straight to the [64 heads][512] bf16 output (for a head, a
+    // warp's lanes hold 32 consecutive channels: one 64-byte run per store);
+    // nothing waits for the stores before the CTA exits
     if (worker) {
       // this warp's 32 head factors, read before any staging store (which
       // the compiler could not otherwise move them past)
@@ -824,17 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const __nv_bfloat162 ob = __floats2bfloat162_rn(o0, o1);
           const uint32_t u = *reinterpret_cast<const uint32_t*>(&ob);
-          stage[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(u);
-          stage[(hw0 + h + 1) * kDim + chn] = static_cast<uint16_t>(u >> 16);
+          og[(hw0 + h) * kDim + chn] = static_cast<uint16_t>(u);
+          og[(hw0 + h + 1) * kDim + chn] = static_cast<uint16_t>(u >> 16);
         }
       }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_store(og, stage, kHeads * kDim * 2);
-      bulk_commit_group();
-      bulk_wait_read_all();
     }
   } else {
     // Channel slice c (cw channels, whole 128-channel blocks) of the output
