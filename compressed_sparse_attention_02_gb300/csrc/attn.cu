@@ -1073,6 +1073,12 @@ bool encode_rows_map(CUtensorMap* m, PFN_cuTensorMapEncodeTiled_v12000 encode, c
 
 }  // namespace
 
+// Slices of at most this many tiles take the split-KV form (fp32 partials and
+// the merge kernel) rather than a cluster's on-chip merge.
+#ifndef CSA_ATTN_GSPLIT_TILES
+#define CSA_ATTN_GSPLIT_TILES 3
+#endif
+
 cudaError_t launch_sparse_attn(const AttnArgs& args, PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t stream) {
   if (args.B <= 0 || args.Q <= 0) return cudaSuccess;
   AttnArgs a = args;
@@ -1116,7 +1122,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& args, PFN_cuTensorMapEncodeTiled_
     g = g < a.gsplit_cap ? g : a.gsplit_cap;
     const int64_t tiles = (rows_max + kTileRows - 1) / kTileRows;
     g = g < tiles ? g : tiles;
-    if (g >= 2 && (g > cluster_max || (tiles + g - 1) / g <= 3)) gsplit = static_cast<int>(g);
+    if (g >= 2 && (g > cluster_max || (tiles + g - 1) / g <= CSA_ATTN_GSPLIT_TILES)) gsplit = static_cast<int>(g);
   }
   if (gsplit > 1) {
     e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.Q) * gsplit, a.B), dim3(kThreads), kSmemBytes, stream, tm_q,
