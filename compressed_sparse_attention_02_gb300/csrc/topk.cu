@@ -326,11 +326,49 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int b = static_cast<int>(blockIdx.z) - (second ? a0.B : 0), q = blockIdx.y;
   if (q >= a.Q) return;
   const int64_t row = static_cast<int64_t>(b) * a.Q + q;
-  int64_t ventries;
-  const int64_t V = row_extent(a, b, q, &ventries);
   const int t = threadIdx.x;
   const int g = blockIdx.x;  // the rank in the cluster
+  const bool bf16 = a.bf16_scores != 0;
+  const int esz = bf16 ? 2 : 4;
+  const uint8_t* srow = reinterpret_cast<const uint8_t*>(a.scores) + row * a.score_ld * esz;
+  // The barriers, and the loads that do not depend on the row's extent (a
+  // q_pos read): the row's first-digit counts and, when every CTA holds one
+  // chunk (chunk g), that chunk's scores as far as the score row reaches.
+  uint32_t spec_bytes = 0;  // thread 0: bytes of chunk g loaded ahead
+  if (t == 0) {
+    mbar_init(&sm.hist_bar, 1);
+    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&sm.vals_bar[i], 1);
+    mbar_init(&sm.sum_bar, G * kWarps);
+    mbar_init(&sm.res_bar[0], 1);
+    mbar_init(&sm.res_bar[1], 1);
+    mbar_init(&sm.peer_bar, 1);
+    fence_mbar_init();
+    // the bytes other CTAs will store here (a result not sent leaves its phase open)
+    mbar_arrive_expect_tx(&sm.res_bar[0], 16);
+    mbar_arrive_expect_tx(&sm.res_bar[1], 16);
+    mbar_arrive_expect_tx(&sm.peer_bar, 16 * G);
+    mbar_arrive_expect_tx(&sm.hist_bar, kKeyBins * 4);
+    bulk_load(sm.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
+    if (!kMulti) {
+      const int64_t len = min(static_cast<int64_t>(kItems), a.score_ld - static_cast<int64_t>(g) * kItems);
+      if (len > 0) {  // score rows are padded to 16 bytes
+        spec_bytes = static_cast<uint32_t>((len * esz + 15) & ~int64_t(15));
+        mbar_arrive_expect_tx(&sm.vals_bar[0], spec_bytes);
+        bulk_load(vbase, srow + static_cast<int64_t>(g) * kItems * esz, spec_bytes, &sm.vals_bar[0]);
+      }
+    }
+  }
+  // this CTA's own copies have landed (before it leaves early)
+  const auto own_copies_landed = [&] {
+    if (t == 0) {
+      mbar_wait(&sm.hist_bar, 0, a.status);
+      if (spec_bytes) mbar_wait(&sm.vals_bar[0], 0, a.status);
+    }
+  };
+  int64_t ventries;
+  const int64_t V = row_extent(a, b, q, &ventries);
   if (V <= a.k) {  // every visible entry is selected; the cluster's first CTA writes the row
+    own_copies_landed();
     if (g != 0) return;
     for (int j = t; j < a.k; j += kThreads) {
       a.idx_out[row * a.k + j] = j < V ? out_entry(a, row, ventries, j) : -1;
@@ -346,11 +384,8 @@ __global__ void __launch_bounds__(kThreads, 4)
   const int64_t i_lo = c0 * kItems;
   const int64_t i_hi = nmine > 0 ? min(i_lo + static_cast<int64_t>(nmine) * kItems, V) : i_lo;
   const bool resident = !kMulti || cpc == 1;  // the CTA's only chunk stays staged in slot 0 throughout
-  const bool bf16 = a.bf16_scores != 0;
-  const int esz = bf16 ? 2 : 4;
   // the CTA's bitmap words: on chip, or (ranges of more than 8 chunks) the row's global scratch
   uint32_t* bm = cpc * kChunkWords <= kSmemWords ? sm.bm : a.bits + row * a.bits_ld + c0 * kChunkWords;
-  const uint8_t* srow = reinterpret_cast<const uint8_t*>(a.scores) + row * a.score_ld * esz;
   auto chunk_len = [&](int j) { return static_cast<int>(min(V - (c0 + j) * kItems, static_cast<int64_t>(kItems))); };
   const int nslot = 1 << slot_shift;
   auto vals = [&](int slot) { return vbase + slot * kItems; };
@@ -359,22 +394,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     mbar_arrive_expect_tx(&sm.vals_bar[slot], bytes);
     bulk_load(vals(slot), srow + (c0 + j) * kItems * esz, bytes, &sm.vals_bar[slot]);
   };
-  if (t == 0) {
-    mbar_init(&sm.hist_bar, 1);
-    for (int i = 0; i < kMaxSlots; ++i) mbar_init(&sm.vals_bar[i], 1);
-    mbar_init(&sm.sum_bar, G * kWarps);
-    mbar_init(&sm.res_bar[0], 1);
-    mbar_init(&sm.res_bar[1], 1);
-    mbar_init(&sm.peer_bar, 1);
-    fence_mbar_init();
-    // the bytes other CTAs will store here (a result not sent leaves its phase open)
-    mbar_arrive_expect_tx(&sm.res_bar[0], 16);
-    mbar_arrive_expect_tx(&sm.res_bar[1], 16);
-    mbar_arrive_expect_tx(&sm.peer_bar, 16 * G);
-    mbar_arrive_expect_tx(&sm.hist_bar, kKeyBins * 4);
-    bulk_load(sm.hist, a.hist + row * kKeyBins, kKeyBins * 4, &sm.hist_bar);
-    for (int j = 0; j < nslot && j < nmine; ++j) issue(j, j);
-  }
+  if (kMulti && t == 0)
+    for (int j = 0; j < nslot && j < nmine; ++j) issue(j, j);  // (one chunk a CTA: loading since the start)
   for (int i = t; i < 1024; i += kThreads) sm.h3[i] = 0;
   // rank 0's results, before they come: read alike by every CTA should a wait give up
   if (t < 2) sm.res[t] = make_uint4(0u, 0u, 0u, 0u);
@@ -612,10 +633,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       }
       ++s;
     }
-    if (!ok && t == 0) {  // no copy of ours stays in flight past the CTA
-      mbar_wait(&sm.hist_bar, 0, a.status);
-      if (nmine > 0) mbar_wait(&sm.vals_bar[0], 0, a.status);
-    }
+    if (!ok || nmine == 0) own_copies_landed();  // no copy of ours stays in flight past the CTA
     if (G > 1) cluster_wait();
     return;
   }
