@@ -340,6 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp && lane == 0) load_q(tm_q, q_s, row_q, q_full);
     pdl_wait();
   }
+  // This thread's share of the selection, read right after the dependency
+  // wait so that its latency overlaps the set-up (and the q_pos read)
+  constexpr int kIdxPer = (kMaxTopk + kThreads - 1) / kThreads;
+  const int per = (a.k + kThreads - 1) / kThreads;  // <= kIdxPer
+  const int lo = min(a.k, tid * per), hi = min(a.k, lo + per);
+  int32_t pv[kIdxPer];
+  if (!a.dense) {
+    const int32_t* ig = a.idx + row_q * a.k;
+#pragma unroll
+    for (int u = 0; u < kIdxPer; ++u) pv[u] = lo + u < hi ? ig[lo + u] : -1;
+  }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   if (tid < kHeads) {
     m_ref[tid] = -INFINITY;
@@ -368,12 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Compact the selected entries (drop -1, flag out-of-range indices).
   // Dense (HCA): the rows are the visible entries 0 .. V(t)-1, no list.
   if (!a.dense) {
-    const int32_t* ig = a.idx + row_q * a.k;
-    const int per = (a.k + kThreads - 1) / kThreads;
-    const int lo = min(a.k, tid * per), hi = min(a.k, lo + per);
     int cnt = 0;
-    for (int j = lo; j < hi; ++j) {
-      const int32_t v = ig[j];
+#pragma unroll
+    for (int u = 0; u < kIdxPer; ++u) {
+      const int32_t v = pv[u];
+      if (lo + u >= hi) break;
       if (v >= 0 && v < a.n_cap) ++cnt;
       else if (v != -1 && rank == 0) record_error(a.status, kErrIndexRange);
     }
@@ -388,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     int before = x - cnt;
     for (int w = 0; w < warp; ++w) before += wtot[w];
-    for (int j = lo; j < hi; ++j) {
-      const int32_t v = ig[j];
+#pragma unroll
+    for (int u = 0; u < kIdxPer; ++u) {
+      const int32_t v = pv[u];
+      if (lo + u >= hi) break;
       if (v >= 0 && v < a.n_cap) sel_s[before++] = v;
     }
     if (tid == kThreads - 1) flags[0] = before;
