@@ -36,6 +36,15 @@ UNIT = "queries/s"
 GRAPH_STEPS = 16  # decode steps per captured CUDA graph
 
 
+def pick_launch(eager_ms, eager_steps, graph_ms, graph_steps):
+    """The faster of the two timed launch forms of the decode loop, per step:
+    (steps, total ms, description, graph chosen).  graph_ms is None when no
+    graph ran."""
+    if graph_ms is not None and graph_steps > 0 and graph_ms / graph_steps < eager_ms / eager_steps:
+        return graph_steps, graph_ms, "CUDA graphs of %d steps, replayed" % GRAPH_STEPS, True
+    return eager_steps, eager_ms, "eager stream launches", False
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -298,10 +307,9 @@ def run_ours(args, rank, world, local_rank):
     eager_ms = max_over_ranks(eager_ms, world, dev)
     if graph_ms is not None:
         graph_ms = max_over_ranks(graph_ms, world, dev)
-    steps_timed, ms, launch = args.steps, eager_ms, "eager stream launches"
-    if graph_ms is not None and graph_ms / g_steps < eager_ms / args.steps:
-        steps_timed, ms, launch, launches = g_steps, graph_ms, "CUDA graphs of %d steps, replayed" % GRAPH_STEPS, \
-            g_launches
+    steps_timed, ms, launch, graph_chosen = pick_launch(eager_ms, args.steps, graph_ms, g_steps)
+    if graph_chosen:
+        launches = g_launches
     if clocks:
         clocks.stop()
     result = {

@@ -61,3 +61,12 @@ def test_reference_arm_prints_on_rank_zero_only():
                        capture_output=True, text=True, timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_the_faster_launch_form_gives_the_value():
+    """bench.py times the decode loop eagerly and as replayed CUDA graphs and
+    reports the faster per step; without a graph it keeps the eager timing."""
+    import bench
+    assert bench.pick_launch(170.0, 2000, 164.0, 1984)[::3] == (1984, True)  # graphs faster per step
+    assert bench.pick_launch(170.0, 2000, 171.0, 1984)[::3] == (2000, False)  # eager faster per step
+    assert bench.pick_launch(170.0, 2000, None, 0) == (2000, 170.0, "eager stream launches", False)
