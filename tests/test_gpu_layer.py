@@ -376,3 +376,55 @@ def test_layer_prefill_with_keys_chunk_of_4096_at_61440(csa):
     xo["kI"] = kI
     qs = [0, 1, 2047, 4095]
     check_prefill(w, xo, kv, idx.cpu().numpy(), out, lse.cpu().numpy(), 0, qs)
+
+
+def test_two_decode_steps_replayed_as_a_cuda_graph_match_eager_launches(csa):
+    """Two consecutive self-contained decode steps (positions t and t+1)
+    captured in one CUDA graph and replayed give, bit for bit, what the same
+    two calls give launched eagerly: outputs, selections, lse and every cache
+    they write.  (The benchmark replays such graphs; inside a graph the step's
+    kernels keep their programmatic launch edges, across the two steps as
+    well, and each kernel's reads before its dependency wait see the same
+    data as in a stream.)"""
+    n_cap, k = 4096, 512
+    t = 4 * n_cap - 2  # step A completes no block, step B (t + 1) completes the last one
+    w = syn.Workload("decode-graph", 83, "decode", B=8, t=t, topk=k, n_cap=n_cap)
+    x = syn.decode_inputs(w, device=DEV)
+    p = csa.csa_default_params(topk=k)
+    B = w.B
+    keys = decode_keys_src(csa, x)
+    pos_a = x["q_pos"].clone()
+    pos_b = (x["q_pos"] + 1).contiguous()
+    row_a = x["swa"][:, 3].contiguous()
+    row_b = x["swa"][:, 5].contiguous()
+    ws = csa.workspace(csa.CSA_OP_LAYER_DECODE, p, B, 1, n_cap)
+
+    def buffers():
+        return {"kv": x["kv"].clone(), "kI": x["kI"].clone(), "swa": x["swa"].clone(),
+                "idx": torch.empty(B, k, dtype=torch.int32, device=DEV),
+                "out": torch.empty(B, 64, 512, dtype=torch.bfloat16, device=DEV),
+                "lse": torch.empty(B, 64, dtype=torch.float32, device=DEV)}
+
+    def two_steps(o):
+        for pos, row in ((pos_a, row_a), (pos_b, row_b)):
+            csa.csa_layer_decode_with_keys(p, B, pos, row, keys, x["ring_Ca"], x["ring_Za"], x["ring_Cb"],
+                                           x["ring_Zb"], x["Ba"], x["Bb"], x["rms_w"], o["kv"], n_cap, o["kI"],
+                                           x["qI"], x["wI"], x["q"], o["swa"], x["sink"], o["idx"], o["out"],
+                                           o["lse"], ws)
+
+    eager = buffers()
+    two_steps(eager)
+    torch.cuda.synchronize()
+    assert csa.csa_check_status() == 0
+
+    replayed = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        two_steps(replayed)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert csa.csa_check_status() == 0
+    for name in ("idx", "out", "lse", "kv", "kI", "swa"):
+        assert torch.equal(eager[name].view(torch.uint8), replayed[name].view(torch.uint8)), name
