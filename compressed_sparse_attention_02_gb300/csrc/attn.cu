@@ -249,8 +249,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   }
 }
 
-// kFp4: the compressed rows are FP4 entries (a.kv_fp4); a template
-// argument, so that the bf16 kernel carries none of that code.
 // The query's 64 x 512 bf16 rows into eight 128-byte-swizzled 64-channel
 // blocks, on q_full (one thread).
 __device__ __forceinline__ void load_q(const CUtensorMap& tm_q, uint8_t* q_s, int64_t row_q, uint64_t* q_full) {
@@ -261,6 +259,8 @@ __device__ __forceinline__ void load_q(const CUtensorMap& tm_q, uint8_t* q_s, in
     tma_load_2d(q_s + blk * kQBlock, &tm_q, blk * 64, static_cast<int32_t>(row_q * kHeads), q_full);
 }
 
+// kFp4: the compressed rows are FP4 entries (a.kv_fp4); a template
+// argument, so that the bf16 kernel carries none of that code.
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_swa,
@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp's lanes hold 32 consecutive channels: one 64-byte run per store);
     // nothing waits for the stores before the CTA exits
     if (worker) {
-      // this warp's 32 head factors, read before any staging store (which
+      // this warp's 32 head factors, read before any output store (which
       // the compiler could not otherwise move them past)
       float fa[32];
 #pragma unroll
