@@ -323,18 +323,6 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, boo
   return r != 0;
 }
 
-// Two independent fp32 fused multiply-adds in one instruction, a * b + c per
-// component, each rounded as fmaf rounds it.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 ra, ra, rb, rc;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
 // Four heads of a ReLU-weighted sum, two to a packed register:
 // a01 += (w0, w1) * max((x0, x1), 0) and a23 += (w2, w3) * max((x2, x3), 0),
 // the weights w0..w3 read from shared memory at w_addr; each component is
@@ -356,14 +344,6 @@ __device__ __forceinline__ void relu_fma4(uint64_t& a01, uint64_t& a23, uint32_t
       : "r"(w_addr), "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "f"(__uint_as_float(x2)),
         "f"(__uint_as_float(x3))
       : "memory");
-}
-
-// ---- shared memory ------------------------------------------------------------
-
-__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
 }
 
 // ---- proxy fences -----------------------------------------------------------
