@@ -450,11 +450,13 @@ csa_status csa_reindex_topk(const csa_params *p, int32_t B, int32_t Q,
  *
  * workspace: optional.  With csa_workspace_size(CSA_OP_SPARSE_ATTN, p, B, Q,
  *          n_cap) bytes (a token amount when B*Q > SMs/2), each query's rows
- *          are cut into as many slices as the workspace holds and one wave
- *          of CTAs allows (up to 16, at most one per 128 rows), one CTA
+ *          may be cut into as many slices as the workspace holds and one
+ *          wave of CTAs allows (up to 16, at most one per 128 rows), one CTA
  *          each, merged by a second kernel (the same result up to fp32
- *          summation order); NULL or too few bytes: one launch, at most a
- *          thread-block cluster's slices per query, merged on chip.
+ *          summation order): taken when that gives more slices than a
+ *          thread-block cluster holds, or slices of at most 3 tiles of 128
+ *          rows.  Otherwise (and with NULL or too few bytes): one launch, at
+ *          most a thread-block cluster's slices per query, merged on chip.
  *
  * With p->inverse_rope = 1 each head's output then gets the inverse of the
  * RoPE the rows carry, at the query position ([CSA2 详解] §12.1 "Partial RoPE
