@@ -666,11 +666,12 @@ csa_status csa_hca_layer_decode(const csa_params *p, int32_t B,
  * _with_keys) and csa_layer_prefill(_with_keys) call records events[0] on
  * its stream before its first kernel and events[s] after stage s: 1 the
  * first kernel (counters cleared, new rows stored, indexer key computed) and
- * the compressor, 2 indexer scores, 3 top-k, 4 sparse attention.  csa_index_topk, csa_index_topk_pool and csa_reindex_topk record
- * events[1] before their indexer kernel (after clearing their workspace),
- * events[2] after it and events[3] after their top-k launches.  events ==
- * NULL turns tracing off.  The setting is process-wide; set it only while no
- * traced call runs on another thread.
+ * the compressor, 2 indexer scores, 3 top-k, 4 sparse attention.
+ * csa_index_topk, csa_index_topk_static, csa_index_topk_pool and
+ * csa_reindex_topk record events[1] before their indexer kernel (after
+ * clearing their workspace), events[2] after it and events[3] after their
+ * top-k launches.  events == NULL turns tracing off.  The setting is
+ * process-wide; set it only while no traced call runs on another thread.
  */
 csa_status csa_set_trace_events(void *const *events, int32_t n_events);
 
